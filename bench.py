@@ -1,0 +1,345 @@
+"""Benchmark: GPT-2 training steps (forward, backward, AdamW) through the C ABI.
+
+Default workload: GPT-2 124M shape, bf16 activations with fp32 master weights,
+B=32, T=1024, Zipf(1.1) token ids with an EoS id every ~Poisson(700) tokens
+(the pages' batch-32 peak-memory workload; synthetic data, random init).
+
+One JSON line on rank 0:
+  value      training tokens/s of the whole job (inputs resident in HBM),
+             timed with CUDA events over exactly --steps steps after --warmup
+             untimed steps, max over ranks;
+  e2e        the same metric through the public API with the token batches
+             copied from pinned host memory every step and the loss read back;
+  roofline   the matmul kernel (the dominant one): algorithmic FLOPs / its
+             CUDA-event time in an instrumented pass, against the measured
+             sustained bf16 peak;
+  cpu_baseline  the CPU oracle timed on this host (rank 0, N=1 only).
+With --gpus N > 1 (under torchrun) every rank trains its own replica on its
+own GPU and data; there is no exchange (replicas only).
+--impl reference times the CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GPT-2 124M train tokens/sec on 1 GB300 (fwd+bwd+AdamW); MFU; kernel HBM GB/s"
+SPEC_BF16_DENSE_TFLOPS = 2250.0  # NVIDIA's dense bf16 figure for one GB300
+HP = dict(beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+
+
+def lr_at(step: int) -> float:
+    return 3e-4 * min(1.0, step / 5.0)  # linear warmup over 5 steps, then constant
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+def model_flops_per_token(L, C, V, T) -> float:
+    """6 N + 12 L T C, N counted with the real vocabulary."""
+    n = V * C + T * C + L * (12 * C * C + 13 * C) + 2 * C
+    return 6.0 * n + 12.0 * L * T * C
+
+
+def workload_cfg(name: str, B: int | None):
+    from step_gpt_train_gb300 import data
+    w = data.WORKLOADS[name]
+    cfg = {k: w[k] for k in ("n_layer", "n_embd", "n_head", "vocab", "vocab_padded", "max_T", "mode")}
+    cfg["max_B"] = B or w["B"]
+    return w, cfg
+
+
+def workload_label(name: str, w: dict, B: int, T: int) -> str:
+    eos = " + EoS every ~Poisson(700)" if w["eos_every"] else ""
+    model = {"124m-b32": "GPT-2 124M", "124m-b8": "GPT-2 124M", "350m-b16": "GPT-2 350M", "1p5b-b8": "GPT-2 1.5B",
+             "tiny": "tiny GPT-2"}[name]
+    prec = "bf16 activations, fp32 master" if w["mode"] == 1 else "fp32"
+    return f"{model} training step, B={B}, T={T}, {prec}, {w['stream']} ids{eos}, random init"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gemm_traffic_from_profile():
+    """DRAM bytes per matmul launch from the committed ncu summary, if it was taken
+    on the current matmul source; else None."""
+    path = os.path.join(ROOT, "profiles", "gemm_tc_kernel_124m_b32.txt")
+    src = os.path.join(ROOT, "step_gpt_train_gb300", "csrc", "gemm_tc.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = dict(l.split(":", 1) for l in text.splitlines() if ":" in l)
+    if fields.get("source_sha256_16", "").strip() != digest:
+        return None
+    try:
+        return float(fields["traffic_bytes_per_launch_full_step_avg"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_baseline(w_name: str):
+    """The oracle, as it stands, on one bounded sample of the workload."""
+    from oracle import gpt2_ref as R
+    from step_gpt_train_gb300 import data
+    w = data.WORKLOADS[w_name]
+    cfg = R.Config(w["n_layer"], w["n_embd"], w["n_head"], w["vocab"], w["vocab_padded"], w["max_T"])
+    T = 1024
+    tok, tgt = data.workload_batches(w_name, 1, B=1, T=T)
+    params = R.init_params(cfg, 1234)
+    t0 = time.perf_counter()
+    R.train_step(cfg, params, tok[0], tgt[0], None, lr_at(1), HP["beta1"], HP["beta2"], HP["eps"],
+                 HP["weight_decay"], 1)
+    dt = time.perf_counter() - t0
+    return {"value": T / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one oracle train step (forward, backward, AdamW over all parameters), float64 numpy, "
+                      f"GPT-2 {w_name.split('-')[0].upper()} shape, B=1, T={T}, first window of the same "
+                      f"token stream; init excluded; {dt:.1f} s"}
+
+
+def run_reference(args, rank: int):
+    """Reference arm: the CPU oracle timed as it stands, on a bounded sample per step."""
+    if rank != 0:
+        return
+    from oracle import gpt2_ref as R
+    from step_gpt_train_gb300 import data
+    w, _ = workload_cfg(args.config, None)
+    cfg = R.Config(w["n_layer"], w["n_embd"], w["n_head"], w["vocab"], w["vocab_padded"], w["max_T"])
+    B, T = 1, args.ref_T
+    tok, tgt = data.workload_batches(args.config, args.warmup + args.steps, B=B, T=T)
+    params = R.init_params(cfg, 1234)
+    state = None
+    times = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        _, _, params, state = R.train_step(cfg, params, tok[s], tgt[s], state, lr_at(s + 1), HP["beta1"],
+                                           HP["beta2"], HP["eps"], HP["weight_decay"], s + 1)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = B * T * len(times) / total
+    sample = (f"each step one oracle train step (float64 numpy) at B={B}, T={T} of the {args.config} "
+              f"stream; GPT-2 {args.config.split('-')[0].upper()} shape")
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_label(args.config, w, B, T), "sample_per_step": f"B={B}, T={T}"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="124m-b32")
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-T", type=int, default=256)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from step_gpt_train_gb300 import data
+    from step_gpt_train_gb300.gpt2 import GPT2, load_library
+
+    load_library(build=True)
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    w, cfg = workload_cfg(args.config, args.batch)
+    B, T = cfg["max_B"], w["T"]
+    K, W = args.steps, args.warmup
+    model = GPT2(cfg, seed=1234)
+    stream = model.stream
+    tok, tgt = data.workload_batches(args.config, W + K, seed=1234 + rank, B=B, T=T)
+    d_tok = torch.from_numpy(tok).cuda()
+    d_tgt = torch.from_numpy(tgt).cuda()
+
+    def step(s, tk, tg):
+        loss = model.forward(tk, tg)
+        model.backward()
+        model.adamw_step(lr_at(s + 1), t=s + 1, **HP)
+        return loss
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---------------------------------------------------------------- device-resident timing
+    for s in range(W):
+        step(s, d_tok[s], d_tgt[s])
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    launches0 = model.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    losses = []
+    for s in range(W, W + K):
+        losses.append(step(s, d_tok[s], d_tgt[s]))
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = model.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1) / K
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = B * T * world
+    value = tokens_per_step / (ms / 1000.0)
+
+    # ---------------------------------------------------------------- end to end through the API
+    pin_tok = torch.from_numpy(tok).pin_memory()
+    pin_tgt = torch.from_numpy(tgt).pin_memory()
+    buf_tok = torch.empty(B, T, dtype=torch.int32, device="cuda")
+    buf_tgt = torch.empty(B, T, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for k in range(K):
+        s = W + k
+        with torch.cuda.stream(stream):
+            buf_tok.copy_(pin_tok[s], non_blocking=True)
+            buf_tgt.copy_(pin_tgt[s], non_blocking=True)
+        step(W + K + k, buf_tok, buf_tgt)  # the loss comes back to the host inside forward
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / K
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
+           "d2h_bytes_per_step": 8}
+
+    # ---------------------------------------------------------------- instrumented pass: per-kernel times
+    model.reset_stats()
+    model.set_timing(True)
+    for k in range(K):
+        s = W + k
+        step(2 * (W + K) + k, d_tok[s], d_tgt[s])
+    fam_ms = model.family_times_ms()
+    stats = model.family_stats()
+    model.set_timing(False)
+    peaks = measured_peaks()
+    mm_ms = fam_ms["matmul"]
+    mm_flops = stats["matmul"]["work"]
+    mm_launches = stats["matmul"]["launches"]
+    achieved = mm_flops / (mm_ms / 1000.0) / 1e12 if mm_ms > 0 else None
+    peak = peaks.get("bf16_tflops_sustained")
+    peak_src = "measured sustained (MEASURED_PEAKS.json)"
+    if not peak:
+        peak, peak_src = 1700.0, "fallback"
+    traffic = gemm_traffic_from_profile()
+    roofline = {"kernel": "gemm_tc_kernel (every matmul of the step)", "bound": "tensor",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None, "peak_source": peak_src,
+                "traffic": traffic, "launches_per_step": mm_launches / K,
+                "flops_per_step": mm_flops / K}
+    kernel_ms = {f: v / K for f, v in fam_ms.items() if v > 0}
+
+    fpt = model_flops_per_token(cfg["n_layer"], cfg["n_embd"], cfg["vocab"], T)
+    tflops = value * fpt / 1e12
+    mfu = {"model_flops_per_token": fpt, "tflops": tflops / world,
+           "vs_spec_2250": tflops / world / SPEC_BF16_DENSE_TFLOPS,
+           "vs_measured_burst": (tflops / world / peaks["bf16_tflops"]) if peaks.get("bf16_tflops") else None}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_label(args.config, w, B, T),
+                       "parallelism": f"replicas x{world} (no exchange)" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2: each step touches ~15 GB of weights, activations and state",
+                       "roofline_pass": "per-kernel times from a separate instrumented pass of the same steps"},
+            "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "roofline": roofline, "mfu": mfu,
+            "kernel_ms_per_step": kernel_ms, "loss_first_last": [losses[0], losses[-1]]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    model.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * gpt2_ops.h - the kernels of the GPT-2 training step, one entry point each.
+ *
+ * These are the same kernels gpt2_forward/gpt2_backward/gpt2_adamw_step run,
+ * exposed on caller-owned device buffers so that each can be checked alone.
+ * The kernel list is the one of llm.c "State of the Union [May 3, 2024]",
+ * kernel table under "Runtime, DRAM traffic, instructions": encoder forward
+ * and backward, layernorm forward and backward, the bf16 matmuls, attention
+ * forward and backward, GELU forward and backward, residual, the fused
+ * classifier, the bias-gradient reduction and AdamW.
+ *
+ * Conventions:
+ *   - dtype: GPT2_MODE_FP32 (0) for fp32 activations, GPT2_MODE_BF16 (1) for
+ *     bf16 activations. Arithmetic inside a kernel is fp32 in both.
+ *   - Every pointer is a device pointer unless stated. All tensors are
+ *     dense and row-major. Activation buffers need 16-byte alignment.
+ *   - stream is a cudaStream_t (NULL = legacy default stream). Calls only
+ *     enqueue work; they never synchronise, allocate or free.
+ *   - scratch: caller-owned device memory of at least the size the matching
+ *     *_scratch_bytes() call returns (256-byte aligned); its contents on
+ *     entry do not matter. Two calls that share a scratch buffer must not
+ *     overlap on the device.
+ *   - d_status: optional device int; kernels OR an error bit into it
+ *     (1 = token id out of range, 2 = bounded wait timed out, 4 = target id
+ *     out of range) and never trap.
+ *   - Return GPT2_OK or a negative gpt2_status (see gpt2.h) for bad
+ *     arguments or a failed launch.
+ */
+#ifndef GPT2_OPS_H
+#define GPT2_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* x0[b,t,:] = wte[tokens[b,t],:] + wpe[t,:] (section "Single GPU training":
+ * GPT-2's token plus learned position embedding; kernel "encoder_forward").
+ * x0 [B*T, C], wte [>=V, C], wpe [>=T, C] in dtype. An id outside [0,V) sets
+ * bit 1 of *d_status and reads row 0 instead. */
+int gpt2_op_encoder_forward(int dtype, void* x0, const int32_t* tokens, const void* wte,
+                            const void* wpe, int B, int T, int C, int V, int* d_status,
+                            void* stream);
+
+/* Embedding backward ("encoder_backward"): dwte[v,:] += sum of dx0 rows
+ * whose token is v, summed in ascending position order (deterministic);
+ * dwpe[t,:] = sum_b dx0[b,t,:] for t < T (rows t >= T untouched).
+ * dwte [Vp, C] fp32 (accumulated into), dwpe [>=T, C] fp32 (overwritten),
+ * dx0 [B*T, C] dtype, tokens in [0, Vp). */
+size_t gpt2_op_encoder_backward_scratch(int B, int T, int C);
+int gpt2_op_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0,
+                             const int32_t* tokens, int B, int T, int C, int Vp,
+                             void* scratch, size_t scratch_bytes, void* stream);
+
+/* LayerNorm forward ("layernorm_forward"): per row of x [N, C],
+ * y = (x - mean) * rstd * gamma + beta, rstd = 1/sqrt(biased var + 1e-5);
+ * mean and rstd [N] fp32 are saved for the backward. C % 8 == 0, C <= 2048. */
+int gpt2_op_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x,
+                              const void* gamma, const void* beta, int N, int C, void* stream);
+
+/* LayerNorm backward ("layernorm_backward"): with xhat = (x-mean)*rstd and
+ * dxhat = dy*gamma, dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat))
+ * (dtype, overwritten); dgamma = sum_rows dy xhat, dbeta = sum_rows dy (fp32,
+ * overwritten, deterministic two-stage reduction through scratch). */
+size_t gpt2_op_layernorm_backward_scratch(int N, int C);
+int gpt2_op_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, const void* dy,
+                               const void* x, const void* gamma, const float* mean,
+                               const float* rstd, int N, int C, void* scratch,
+                               size_t scratch_bytes, void* stream);
+
+/* Matmul (the bf16 GEMMs of the kernel table, "ampere_bf16" and
+ * "cutlass::Kernel2"): D[M,N] = sum_k A(m,k) B(n,k) (+ bias[n]).
+ * A(m,k) is A[m*K + k] (a_mn_major = 0) or A[k*M + m] (a_mn_major = 1);
+ * B(n,k) is B[n*K + k] (b_mn_major = 0) or B[k*N + n] (b_mn_major = 1).
+ * So the linear forward is (0,0) with B = W [N,K]; the input gradient
+ * dX = dY W is (0,1); the weight gradient dW = dY^T X is (1,1).
+ * A, B and bias (optional, length N, dtype) are in dtype; D is fp32 if
+ * d_fp32 else dtype, overwritten. bf16: tcgen05 tensor cores (TMA-fed,
+ * fp32 accumulate in tensor memory); fp32: fp32 FMA. Needs K % 8 == 0 and
+ * N % 8 == 0 (and M % 8 == 0 when a_mn_major); 16-byte aligned buffers.
+ * Scratch holds split-K partial sums (fp32 D only). */
+size_t gpt2_op_matmul_scratch(int dtype, int M, int N, int K, int d_fp32);
+int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major, const void* B,
+                   int b_mn_major, const void* bias, int M, int N, int K, void* scratch,
+                   size_t scratch_bytes, int* d_status, void* stream);
+
+/* Causal multi-head attention forward ("flash attention", section "Single
+ * GPU training"; kernel "cudnn_generated_fort_native_sdpa"): qkv [B*T, 3C]
+ * holds q | k | v column blocks, head h at columns h*hd..h*hd+hd-1 of each.
+ * o [B*T, C] (dtype) = softmax(q k^T / sqrt(hd), causal) v per head; lse
+ * [B, H, T] fp32 = log-sum-exp of each scaled score row. The T x T score
+ * matrix is never stored. hd == 64 for bf16; hd <= 64 for fp32. */
+int gpt2_op_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T,
+                              int C, int H, void* stream);
+
+/* Attention backward (kernels "compute_dot_do_o", the SDPA backward and
+ * "rearrange_n_convert_dq" of the table): D = rowsum(dO * O) into scratch,
+ * then with P recomputed from lse: dV = P^T dO, dS = P (dO V^T - D),
+ * dQ = dS K / sqrt(hd), dK = dS^T Q / sqrt(hd), written to dqkv [B*T, 3C]
+ * (dtype, overwritten) in the q | k | v layout. Deterministic (no atomics). */
+size_t gpt2_op_attention_backward_scratch(int B, int T, int H);
+int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv,
+                               const void* o, const float* lse, int B, int T, int C, int H,
+                               void* scratch, size_t scratch_bytes, void* stream);
+
+/* GELU, tanh form ("gelu_forward"): g = 0.5 u (1 + tanh(sqrt(2/pi)(u + 0.044715 u^3))).
+ * n % 8 == 0. In place (g == u) is allowed. */
+int gpt2_op_gelu_forward(int dtype, void* g, const void* u, int64_t n, void* stream);
+
+/* GELU backward ("gelu_backward"): du = dg * g'(u). In place (du == dg) allowed. */
+int gpt2_op_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n,
+                          void* stream);
+
+/* Residual forward ("residual_forward"): out = a + b, n % 8 == 0. */
+int gpt2_op_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n,
+                             void* stream);
+
+/* Residual backward: the gradient reaching a residual join from the
+ * branch is added to the stream gradient, dres += dbranch, n % 8 == 0. */
+int gpt2_op_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n,
+                              void* stream);
+
+/* Bias gradient ("matmul_backward_bias"): dbias[c] = sum_rows dy[r, c]
+ * (fp32, overwritten), dy [N, C] dtype; deterministic two-stage reduction. */
+size_t gpt2_op_bias_backward_scratch(int N, int C);
+int gpt2_op_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch,
+                          size_t scratch_bytes, void* stream);
+
+/* Fused classifier ("fused_classifier", section "Single GPU training" and
+ * "Fine print"): per row i of logits [N, Vp] (dtype), over columns j < V only:
+ * lse_i = log sum exp z_ij, losses[i] = lse_i - z_i,targets[i] (fp32), and in
+ * place z_ij <- dloss * (exp(z_ij - lse_i) - [j == target_i]) for j < V,
+ * 0 for V <= j < Vp. Normalised logits are never stored. dloss is the
+ * gradient of the loss w.r.t. each row's loss (1/N for a mean).
+ * A target outside [0,V) sets bit 4 of *d_status and is treated as 0. */
+int gpt2_op_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N,
+                       int V, int Vp, float dloss, int* d_status, void* stream);
+
+/* Mean of losses [N] into *out (device fp32): fixed-order tree, deterministic. */
+int gpt2_op_mean_loss(float* out, const float* losses, int N, void* stream);
+
+/* AdamW ("adamw_kernel"): over n fp32 elements, m = b1 m + (1-b1) g;
+ * v = b2 v + (1-b2) g^2; theta -= lr (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps)
+ * + wd theta); if param_bf16 != NULL also writes bf16(theta) (round to
+ * nearest even) there. n % 4 == 0. */
+int gpt2_op_adamw(float* master, void* param_bf16, const float* grad, float* m, float* v,
+                  int64_t n, float lr, float beta1, float beta2, float eps, float weight_decay,
+                  int t, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_OPS_H */

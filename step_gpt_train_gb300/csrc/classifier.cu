@@ -1,0 +1,178 @@
+// Fused softmax cross-entropy classifier and the mean-loss reduction.
+//
+// One block per row of logits. The row is read from HBM once into registers
+// (raw 16-byte vectors), reduced to (max, sum of exp) over the real vocabulary
+// columns, and the gradient is written back in place over the logits. The
+// normalised probabilities are never stored. Columns V..Vp-1 (padding) get 0.
+#include "common.cuh"
+#include "launch.h"
+
+#include <cfloat>
+
+#define LOG2E 1.4426950408889634f
+
+// exp(x - m) for the two modes: ex2.approx for bf16 activations (its error is
+// far below bf16 resolution), the accurate expf for the fp32 parity mode.
+template <typename T> __device__ __forceinline__ float exp_shift(float x, float m);
+template <> __device__ __forceinline__ float exp_shift<bf16>(float x, float m) { return ex2_approx((x - m) * LOG2E); }
+template <> __device__ __forceinline__ float exp_shift<float>(float x, float m) { return expf(x - m); }
+
+template <typename T> struct RawVec;
+template <> struct RawVec<bf16> { uint4 r; };
+template <> struct RawVec<float> { float4 a, b; };
+
+__device__ __forceinline__ void raw_load(RawVec<bf16>& v, const bf16* p) { v.r = __ldcs(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void raw_load(RawVec<float>& v, const float* p) {
+    v.a = __ldcs(reinterpret_cast<const float4*>(p));
+    v.b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+}
+__device__ __forceinline__ void raw_unpack(const RawVec<bf16>& v, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v.r);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+__device__ __forceinline__ void raw_unpack(const RawVec<float>& v, float (&f)[8]) {
+    f[0] = v.a.x; f[1] = v.a.y; f[2] = v.a.z; f[3] = v.a.w;
+    f[4] = v.b.x; f[5] = v.b.y; f[6] = v.b.z; f[7] = v.b.w;
+}
+
+template <int NT>
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* sh) {
+    const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+    v = is_max ? warp_max(v) : warp_sum(v);
+    __syncthreads();  // sh may still be read from a previous reduction
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    float r = is_max ? -FLT_MAX : 0.f;
+    if (threadIdx.x < 32) {
+        float x = threadIdx.x < NT / 32 ? sh[threadIdx.x] : (is_max ? -FLT_MAX : 0.f);
+        r = is_max ? warp_max(x) : warp_sum(x);
+        if (threadIdx.x == 0) sh[32] = r;
+    }
+    __syncthreads();
+    return sh[32];
+}
+
+// NT threads per row, VPT 8-element vectors per thread (Vp <= 8 * NT * VPT).
+template <typename T, int NT, int VPT>
+__global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, float* __restrict__ losses,
+                                                        const int32_t* __restrict__ targets, int V, int Vp,
+                                                        float dloss, int* status) {
+    __shared__ float sh[33];
+    const int row = blockIdx.x;
+    T* z = logits + (int64_t)row * Vp;
+    const int nv = Vp / 8;
+    RawVec<T> cache[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx < nv) raw_load(cache[i], z + idx * 8);
+    }
+    int tgt = targets[row];
+    if (tgt < 0 || tgt >= V) {
+        if (threadIdx.x == 0) set_status(status, GPT2_FLAG_TARGET_RANGE);
+        tgt = 0;
+    }
+    // max over the real columns
+    float m = -FLT_MAX;
+    float zt = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx < nv) {
+            float f[8];
+            raw_unpack(cache[i], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int col = idx * 8 + j;
+                if (col < V) m = fmaxf(m, f[j]);
+                if (col == tgt) zt = f[j];
+            }
+        }
+    }
+    m = block_reduce<NT>(m, true, sh);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx < nv) {
+            float f[8];
+            raw_unpack(cache[i], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                if (idx * 8 + j < V) s += exp_shift<T>(f[j], m);
+        }
+    }
+    s = block_reduce<NT>(s, false, sh);
+    const float scale = dloss / s;
+    // the thread holding the target column reports the loss: lse - z_t
+    if (((tgt / 8) % NT) == (int)threadIdx.x) losses[row] = m + logf(s) - zt;
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx < nv) {
+            float f[8];
+            raw_unpack(cache[i], f);
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int col = idx * 8 + j;
+                float d = col < V ? exp_shift<T>(f[j], m) * scale : 0.f;
+                if (col == tgt) d -= dloss;
+                f[j] = d;
+            }
+            store8(z + idx * 8, f);
+        }
+    }
+}
+
+template <typename T, int NT>
+static int classifier_dispatch(void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
+                               float dloss, int* status, cudaStream_t s) {
+    const int nv = Vp / 8;
+    const int vpt = (nv + NT - 1) / NT;
+#define CLS_CALL(K)                                                                                                \
+    classifier_kernel<T, NT, K><<<N, NT, 0, s>>>((T*)logits, losses, targets, V, Vp, dloss, status); \
+    return 1;
+    switch (vpt) {
+        case 1: CLS_CALL(1)
+        case 2: CLS_CALL(2)
+        case 3: CLS_CALL(3)
+        case 4: CLS_CALL(4)
+        case 5: CLS_CALL(5)
+        case 6: CLS_CALL(6)
+        case 7: CLS_CALL(7)
+        case 8: CLS_CALL(8)
+        default: return GPT2_ERR_ARG;
+    }
+#undef CLS_CALL
+}
+
+int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
+                      float dloss, int* status, cudaStream_t s) {
+    if (N == 0) return 0;
+    if (dtype == GPT2_MODE_BF16) {
+        if (Vp <= 8 * 256 * 2) return classifier_dispatch<bf16, 256>(logits, losses, targets, N, V, Vp, dloss, status, s);
+        return classifier_dispatch<bf16, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s);
+    }
+    if (Vp <= 8 * 256 * 2) return classifier_dispatch<float, 256>(logits, losses, targets, N, V, Vp, dloss, status, s);
+    return classifier_dispatch<float, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s);
+}
+
+// Mean of N losses: each of 1024 threads sums a fixed strided subset in
+// order, then a fixed shuffle tree; deterministic.
+__global__ void __launch_bounds__(1024) mean_loss_kernel(float* out, const float* __restrict__ losses, int N) {
+    __shared__ float sh[33];
+    float s = 0.f;
+    for (int i = threadIdx.x; i < N; i += 1024) s += losses[i];
+    s = block_reduce<1024>(s, false, sh);
+    if (threadIdx.x == 0) *out = s / (float)N;
+}
+
+int launch_mean_loss(float* out, const float* losses, int N, cudaStream_t s) {
+    mean_loss_kernel<<<1, 1024, 0, s>>>(out, losses, N);
+    return 1;
+}

@@ -1,0 +1,126 @@
+// Shared device helpers for the GPT-2 step kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/gpt2.h"
+#include "../../include/gpt2_ops.h"
+
+typedef __nv_bfloat16 bf16;
+
+// Bits OR-ed into a device status word; never a trap.
+#define GPT2_FLAG_TOKEN_RANGE 1
+#define GPT2_FLAG_TIMEOUT 2
+#define GPT2_FLAG_TARGET_RANGE 4
+
+// Bounded spin: a wait gives up after this many clock cycles (~2 s at 2 GHz).
+#define GPT2_WAIT_LIMIT_CYCLES (4000000000LL)
+
+__device__ __forceinline__ void set_status(int* status, int bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// ---- 8-element vector access: one 16-byte access for bf16, two for fp32 ----
+
+__device__ __forceinline__ void load8(const bf16* p, float (&f)[8]) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 v = __bfloat1622float2(h[i]);
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+    float4 a = reinterpret_cast<const float4*>(p)[0];
+    float4 b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+// Streaming (evict-first) variants for data read exactly once.
+__device__ __forceinline__ void load8_stream(const bf16* p, float (&f)[8]) {
+    uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float2 v = __bfloat1622float2(h[i]);
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+__device__ __forceinline__ void load8_stream(const float* p, float (&f)[8]) {
+    float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void store8(bf16* p, const float (&f)[8]) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_float<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---- warp / block reductions (fixed shuffle order: deterministic) ----
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---- hardware approximate transcendental instructions (PTX, MUFU) ----
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// GELU tanh-form constants: sqrt(2/pi) and the cubic coefficient.
+#define GELU_K 0.7978845608028654f
+#define GELU_A 0.044715f
+
+// GELU's 0.5 (1 + tanh(y)) evaluated as the logistic function of 2y,
+// 1 / (1 + exp(-2y)) (the same quantity, since tanh y = 2 sigmoid(2y) - 1).
+// This form keeps full relative accuracy on the negative tail, where
+// 1 + tanh(y) cancels. bf16 activations use the hardware exp2 and a fast
+// divide; the fp32 parity mode uses expf and an IEEE divide.
+template <typename T> __device__ __forceinline__ float gelu_sigmoid(float y);
+template <> __device__ __forceinline__ float gelu_sigmoid<bf16>(float y) {
+    const float z = fminf(-2.f * 1.4426950408889634f * y, 126.f);  // exp(-2y) = 2^z, capped below overflow
+    return __fdividef(1.f, 1.f + ex2_approx(z));
+}
+template <> __device__ __forceinline__ float gelu_sigmoid<float>(float y) { return 1.f / (1.f + expf(-2.f * y)); }
+
+// ---- host-side helpers ----
+
+static inline int grid_for(int64_t work_items, int threads, int max_blocks) {
+    int64_t b = (work_items + threads - 1) / threads;
+    if (b < 1) b = 1;
+    if (b > max_blocks) b = max_blocks;
+    return (int)b;
+}
+
+// Number of SMs on the current device (cached per process).
+int gpt2_num_sms();

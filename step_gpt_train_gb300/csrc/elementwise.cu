@@ -1,0 +1,554 @@
+// Elementwise and reduction kernels of the GPT-2 step: encoder forward and
+// backward, GELU, residual, bias gradient, AdamW. All loads and stores are
+// 16-byte vectors (8 bf16 or 2 x 4 fp32), so every warp access is a
+// coalesced 512-byte span.
+#include "common.cuh"
+#include "launch.h"
+
+#include <algorithm>
+#include <cmath>
+
+// ===================================================================== encoder
+
+// x0[r,:] = wte[tok[r],:] + wpe[r % T,:]. Thread per 8-element vector.
+template <typename T>
+__global__ void __launch_bounds__(256) encoder_fwd_kernel(T* __restrict__ x0, const int32_t* __restrict__ tokens,
+                                                          const T* __restrict__ wte, const T* __restrict__ wpe,
+                                                          int BT, int Tlen, int C, int V, int* status) {
+    const int cv = C / 8;
+    const int64_t total = (int64_t)BT * cv;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int r = (int)(i / cv);
+    const int c = (int)(i % cv) * 8;
+    int tok = tokens[r];
+    if (tok < 0 || tok >= V) {
+        set_status(status, GPT2_FLAG_TOKEN_RANGE);
+        tok = 0;
+    }
+    float a[8], b[8];
+    load8(wte + (int64_t)tok * C + c, a);
+    load8(wpe + (int64_t)(r % Tlen) * C + c, b);
+#pragma unroll
+    for (int j = 0; j < 8; j++) a[j] += b[j];
+    store8(x0 + (int64_t)r * C + c, a);
+}
+
+int launch_encoder_forward(int dtype, void* x0, const int32_t* tokens, const void* wte, const void* wpe, int B,
+                           int T, int C, int V, int* status, cudaStream_t s) {
+    const int64_t total = (int64_t)B * T * (C / 8);
+    const int blocks = (int)((total + 255) / 256);
+    if (dtype == GPT2_MODE_BF16)
+        encoder_fwd_kernel<bf16><<<blocks, 256, 0, s>>>((bf16*)x0, tokens, (const bf16*)wte, (const bf16*)wpe, B * T,
+                                                        T, C, V, status);
+    else
+        encoder_fwd_kernel<float><<<blocks, 256, 0, s>>>((float*)x0, tokens, (const float*)wte, (const float*)wpe,
+                                                         B * T, T, C, V, status);
+    return 1;
+}
+
+// ---- encoder backward ----
+// dwpe[t,:] = sum over b (in order) of dx0[b*T+t,:]: thread per (t, vector).
+template <typename T>
+__global__ void __launch_bounds__(256) encoder_bwd_wpe_kernel(float* __restrict__ dwpe, const T* __restrict__ dx0,
+                                                              int B, int Tlen, int C) {
+    const int cv = C / 8;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)Tlen * cv) return;
+    const int t = (int)(i / cv);
+    const int c = (int)(i % cv) * 8;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int b = 0; b < B; b++) {
+        float v[8];
+        load8(dx0 + ((int64_t)b * Tlen + t) * C + c, v);
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[j] += v[j];
+    }
+    store8(dwpe + (int64_t)t * C + c, acc);
+}
+
+// dwte: the positions are sorted by token id with a stable two-pass LSD radix
+// sort (8-bit digits, ids < 65536); then each token's rows are summed in
+// ascending position order, split into 32-entry chunks of the sorted list so
+// that a very frequent id is summed by many warps, and the chunk pieces of a
+// long run are combined in chunk order. Every token row of dwte has exactly
+// one writer, so the result is deterministic.
+
+#define ENC_TILE 1024  // sorted elements per block in the radix passes
+#define ENC_CHUNK 32   // sorted entries per warp in the summation
+
+// Pass setup: keys = token ids, values = positions.
+__global__ void enc_init_kernel(uint32_t* keys, int32_t* vals, const int32_t* tokens, int n) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        keys[i] = (uint32_t)tokens[i];
+        vals[i] = i;
+    }
+}
+
+// hist[d * nblk + blk] = count of digit d in tile blk.
+__global__ void __launch_bounds__(ENC_TILE) enc_hist_kernel(int32_t* hist, const uint32_t* keys, int n, int shift) {
+    __shared__ int h[256];
+    if (threadIdx.x < 256) h[threadIdx.x] = 0;
+    __syncthreads();
+    int i = blockIdx.x * ENC_TILE + threadIdx.x;
+    if (i < n) atomicAdd(&h[(keys[i] >> shift) & 255], 1);
+    __syncthreads();
+    if (threadIdx.x < 256) hist[threadIdx.x * gridDim.x + blockIdx.x] = h[threadIdx.x];
+}
+
+// Exclusive scan of hist in (digit, block) order, single block.
+__global__ void __launch_bounds__(1024) enc_scan_kernel(int32_t* hist, int total) {
+    __shared__ int partial[1024];
+    const int per = (total + 1023) / 1024;
+    const int lo = threadIdx.x * per;
+    const int hi = min(total, lo + per);
+    int s = 0;
+    for (int i = lo; i < hi; i++) s += hist[i];
+    partial[threadIdx.x] = s;
+    __syncthreads();
+    // Hillis-Steele inclusive scan over 1024 partial sums.
+    for (int off = 1; off < 1024; off <<= 1) {
+        int v = threadIdx.x >= off ? partial[threadIdx.x - off] : 0;
+        __syncthreads();
+        partial[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = threadIdx.x == 0 ? 0 : partial[threadIdx.x - 1];
+    for (int i = lo; i < hi; i++) {
+        int c = hist[i];
+        hist[i] = run;
+        run += c;
+    }
+}
+
+// Stable scatter of one tile: rank within a warp from __match_any_sync,
+// across warps from a per-warp digit-count table.
+__global__ void __launch_bounds__(ENC_TILE) enc_scatter_kernel(uint32_t* keys_out, int32_t* vals_out,
+                                                               const uint32_t* keys, const int32_t* vals,
+                                                               const int32_t* offsets, int n, int shift) {
+    __shared__ int cnt[ENC_TILE / 32][256];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i = threadIdx.x; i < (ENC_TILE / 32) * 256; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    __syncthreads();
+    const int i = blockIdx.x * ENC_TILE + threadIdx.x;
+    const bool valid = i < n;
+    const uint32_t key = valid ? keys[i] : 0xffffffffu;
+    const int d = valid ? (int)((key >> shift) & 255) : 256;
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const int rank = __popc(peers & ((1u << lane) - 1));
+    if (valid && rank == 0) cnt[warp][d] = __popc(peers);
+    __syncthreads();
+    if (threadIdx.x < 256) {  // exclusive prefix over warps for digit threadIdx.x
+        int run = 0;
+        for (int w = 0; w < ENC_TILE / 32; w++) {
+            int c = cnt[w][threadIdx.x];
+            cnt[w][threadIdx.x] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    if (valid) {
+        const int dst = offsets[d * gridDim.x + blockIdx.x] + cnt[warp][d] + rank;
+        keys_out[dst] = key;
+        vals_out[dst] = vals[i];
+    }
+}
+
+__device__ __forceinline__ bool enc_is_head(const uint32_t* skey, int j) {
+    return j == 0 || skey[j] != skey[j - 1];
+}
+
+// Sum of rows [lo, hi) of the sorted list into acc (lane's vectors).
+template <typename T, int VPL>
+__device__ __forceinline__ void enc_sum_rows(float (&acc)[VPL][8], const T* dx0, const int32_t* spos, int lo, int hi,
+                                             int C, int lane) {
+    const int cv = C / 8;
+    for (int j = lo; j < hi; j++) {
+        const T* row = dx0 + (int64_t)spos[j] * C;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            int idx = lane + 32 * i;
+            if (idx < cv) {
+                float v[8];
+                load8(row + idx * 8, v);
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc[i][k] += v[k];
+            }
+        }
+    }
+}
+
+template <int VPL>
+__device__ __forceinline__ void enc_flush(float (&acc)[VPL][8], float* dst, bool accumulate, int C, int lane) {
+    const int cv = C / 8;
+#pragma unroll
+    for (int i = 0; i < VPL; i++) {
+        int idx = lane + 32 * i;
+        if (idx < cv) {
+            float* p = dst + idx * 8;
+            if (accumulate) {
+                float o[8];
+                load8(p, o);
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc[i][k] += o[k];
+            }
+            store8(p, acc[i]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; k++) acc[i][k] = 0.f;
+    }
+}
+
+// One warp per 32-entry chunk of the sorted list. A run of equal ids that
+// lies wholly inside the chunk is added to dwte here. A run that crosses the
+// chunk's end and starts inside it goes to tail[chunk]; the piece at the
+// chunk's start that continues a run from an earlier chunk goes to head[chunk].
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256) enc_piece_kernel(float* dwte, float* head, float* tail, const T* dx0,
+                                                        const uint32_t* skey, const int32_t* spos, int n, int C) {
+    const int chunk = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    const int lo = chunk * ENC_CHUNK;
+    if (lo >= n) return;
+    const int hi = min(n, lo + ENC_CHUNK);
+    float acc[VPL][8];
+#pragma unroll
+    for (int i = 0; i < VPL; i++)
+#pragma unroll
+        for (int k = 0; k < 8; k++) acc[i][k] = 0.f;
+    int ps = lo;
+    while (ps < hi) {
+        int pe = ps + 1;
+        while (pe < hi && skey[pe] == skey[ps]) pe++;
+        enc_sum_rows<T, VPL>(acc, dx0, spos, ps, pe, C, lane);
+        const bool starts = enc_is_head(skey, ps);
+        const bool ends = (pe == n) || skey[pe] != skey[ps];
+        if (starts && ends)
+            enc_flush<VPL>(acc, dwte + (int64_t)skey[ps] * C, true, C, lane);
+        else if (!starts)
+            enc_flush<VPL>(acc, head + (int64_t)chunk * C, false, C, lane);
+        else
+            enc_flush<VPL>(acc, tail + (int64_t)chunk * C, false, C, lane);
+        ps = pe;
+    }
+}
+
+// One warp per chunk whose last run starts inside it and continues: sums
+// tail[chunk] + head[chunk+1] + ... in chunk order, adds to dwte.
+template <int VPL>
+__global__ void __launch_bounds__(256) enc_combine_kernel(float* dwte, const float* head, const float* tail,
+                                                          const uint32_t* skey, int n, int C) {
+    const int chunk = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    const int lo = chunk * ENC_CHUNK;
+    if (lo >= n) return;
+    const int hi = min(n, lo + ENC_CHUNK);
+    if (hi == n || skey[hi] != skey[hi - 1]) return;  // last run ends in this chunk
+    int start = hi - 1;
+    while (start > lo && skey[start - 1] == skey[hi - 1]) start--;
+    if (!enc_is_head(skey, start)) return;  // run began in an earlier chunk
+    const int cv = C / 8;
+    float acc[VPL][8];
+#pragma unroll
+    for (int i = 0; i < VPL; i++) {
+        int idx = lane + 32 * i;
+        if (idx < cv) load8(tail + (int64_t)chunk * C + idx * 8, acc[i]);
+    }
+    const uint32_t key = skey[hi - 1];
+    for (int c = chunk + 1;; c++) {
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            int idx = lane + 32 * i;
+            if (idx < cv) {
+                float v[8];
+                load8(head + (int64_t)c * C + idx * 8, v);
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc[i][k] += v[k];
+            }
+        }
+        const int chi = min(n, (c + 1) * ENC_CHUNK);
+        if (chi == n || skey[chi] != key || skey[chi - 1] != key) break;
+    }
+    enc_flush<VPL>(acc, dwte + (int64_t)key * C, true, C, lane);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t encoder_backward_scratch(int B, int T, int C) {
+    const size_t n = (size_t)B * T;
+    const size_t nblk = (n + ENC_TILE - 1) / ENC_TILE;
+    const size_t nchunk = (n + ENC_CHUNK - 1) / ENC_CHUNK;
+    return 4 * align256(n * 4) + align256(256 * nblk * 4) + 2 * align256(nchunk * C * 4);
+}
+
+template <typename T, int VPL>
+static void enc_sum_launch(float* dwte, float* head, float* tail, const void* dx0, const uint32_t* skey,
+                           const int32_t* spos, int n, int C, cudaStream_t s) {
+    const int nchunk = (n + ENC_CHUNK - 1) / ENC_CHUNK;
+    const int blocks = (nchunk * 32 + 255) / 256;
+    enc_piece_kernel<T, VPL><<<blocks, 256, 0, s>>>(dwte, head, tail, (const T*)dx0, skey, spos, n, C);
+    enc_combine_kernel<VPL><<<blocks, 256, 0, s>>>(dwte, head, tail, skey, n, C);
+}
+
+template <typename T>
+static void enc_sum_dispatch(float* dwte, float* head, float* tail, const void* dx0, const uint32_t* skey,
+                             const int32_t* spos, int n, int C, cudaStream_t s) {
+    const int vpl = (C / 8 + 31) / 32;
+    switch (vpl) {
+        case 1: enc_sum_launch<T, 1>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        case 2: enc_sum_launch<T, 2>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        case 3: enc_sum_launch<T, 3>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        case 4: enc_sum_launch<T, 4>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        case 5: enc_sum_launch<T, 5>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        case 6: enc_sum_launch<T, 6>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        case 7: enc_sum_launch<T, 7>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+        default: enc_sum_launch<T, 8>(dwte, head, tail, dx0, skey, spos, n, C, s); break;
+    }
+}
+
+int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0, const int32_t* tokens, int B, int T,
+                            int C, void* scratch, cudaStream_t s) {
+    const int n = B * T;
+    const int nblk = (n + ENC_TILE - 1) / ENC_TILE;
+    const int nchunk = (n + ENC_CHUNK - 1) / ENC_CHUNK;
+    char* p = (char*)scratch;
+    uint32_t* ka = (uint32_t*)p; p += align256((size_t)n * 4);
+    int32_t* va = (int32_t*)p; p += align256((size_t)n * 4);
+    uint32_t* kb = (uint32_t*)p; p += align256((size_t)n * 4);
+    int32_t* vb = (int32_t*)p; p += align256((size_t)n * 4);
+    int32_t* hist = (int32_t*)p; p += align256((size_t)256 * nblk * 4);
+    float* head = (float*)p; p += align256((size_t)nchunk * C * 4);
+    float* tail = (float*)p;
+    int launches = 0;
+    {
+        const int blocks = (T * (C / 8) + 255) / 256;
+        if (dtype == GPT2_MODE_BF16)
+            encoder_bwd_wpe_kernel<bf16><<<blocks, 256, 0, s>>>(dwpe, (const bf16*)dx0, B, T, C);
+        else
+            encoder_bwd_wpe_kernel<float><<<blocks, 256, 0, s>>>(dwpe, (const float*)dx0, B, T, C);
+        launches++;
+    }
+    enc_init_kernel<<<(n + 255) / 256, 256, 0, s>>>(ka, va, tokens, n);
+    launches++;
+    for (int pass = 0; pass < 2; pass++) {
+        const int shift = pass * 8;
+        uint32_t* kin = pass == 0 ? ka : kb;
+        int32_t* vin = pass == 0 ? va : vb;
+        uint32_t* kout = pass == 0 ? kb : ka;
+        int32_t* vout = pass == 0 ? vb : va;
+        enc_hist_kernel<<<nblk, ENC_TILE, 0, s>>>(hist, kin, n, shift);
+        enc_scan_kernel<<<1, 1024, 0, s>>>(hist, 256 * nblk);
+        enc_scatter_kernel<<<nblk, ENC_TILE, 0, s>>>(kout, vout, kin, vin, hist, n, shift);
+        launches += 3;
+    }
+    // After two passes the sorted list is back in (ka, va).
+    if (dtype == GPT2_MODE_BF16)
+        enc_sum_dispatch<bf16>(dwte, head, tail, dx0, ka, va, n, C, s);
+    else
+        enc_sum_dispatch<float>(dwte, head, tail, dx0, ka, va, n, C, s);
+    launches += 2;
+    return launches;
+}
+
+// ===================================================================== GELU, residual
+
+// g = u s and g' = s + 2 u s (1 - s) sqrt(2/pi) (1 + 3*0.044715 u^2), with
+// s = 0.5 (1 + tanh(y)), y = sqrt(2/pi) (u + 0.044715 u^3); the derivative uses
+// 1 - tanh(y)^2 = 4 s (1 - s).
+template <typename T>
+__device__ __forceinline__ float gelu_fwd_f(float u) {
+    const float y = GELU_K * (u + GELU_A * u * u * u);
+    return u * gelu_sigmoid<T>(y);
+}
+template <typename T>
+__device__ __forceinline__ float gelu_grad_f(float u) {
+    const float y = GELU_K * (u + GELU_A * u * u * u);
+    const float s = gelu_sigmoid<T>(y);
+    return s + 2.f * u * s * (1.f - s) * GELU_K * (1.f + 3.f * GELU_A * u * u);
+}
+
+#define EW_UNROLL 4
+#define EW_THREADS 256
+
+// op 0: out = gelu(a); op 1: out = b * gelu'(a); op 2: out = a + b.
+template <typename T, int OP>
+__global__ void __launch_bounds__(EW_THREADS) ew_kernel(T* out, const T* a, const T* b, int64_t n8) {
+    // No __restrict__: out may alias a (in-place GELU and residual accumulate).
+    // Each thread loads all its inputs before its first store.
+    const int64_t base = (int64_t)blockIdx.x * (EW_THREADS * EW_UNROLL) + threadIdx.x;
+    float va[EW_UNROLL][8], vb[EW_UNROLL][8];
+#pragma unroll
+    for (int u = 0; u < EW_UNROLL; u++) {
+        const int64_t i = base + (int64_t)u * EW_THREADS;
+        if (i < n8) {
+            load8_stream(a + i * 8, va[u]);
+            if (OP != 0) load8_stream(b + i * 8, vb[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < EW_UNROLL; u++) {
+        const int64_t i = base + (int64_t)u * EW_THREADS;
+        if (i < n8) {
+            float r[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (OP == 0) r[j] = gelu_fwd_f<T>(va[u][j]);
+                else if (OP == 1) r[j] = vb[u][j] * gelu_grad_f<T>(va[u][j]);
+                else r[j] = va[u][j] + vb[u][j];
+            }
+            store8(out + i * 8, r);
+        }
+    }
+}
+
+template <int OP>
+static int ew_launch(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s) {
+    const int64_t n8 = n / 8;
+    const int64_t per_block = EW_THREADS * EW_UNROLL;
+    const int blocks = (int)((n8 + per_block - 1) / per_block);
+    if (blocks == 0) return 0;
+    if (dtype == GPT2_MODE_BF16)
+        ew_kernel<bf16, OP><<<blocks, EW_THREADS, 0, s>>>((bf16*)out, (const bf16*)a, (const bf16*)b, n8);
+    else
+        ew_kernel<float, OP><<<blocks, EW_THREADS, 0, s>>>((float*)out, (const float*)a, (const float*)b, n8);
+    return 1;
+}
+
+int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream_t s) {
+    return ew_launch<0>(dtype, g, u, nullptr, n, s);
+}
+int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s) {
+    return ew_launch<1>(dtype, du, u, dg, n, s);
+}
+int launch_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s) {
+    return ew_launch<2>(dtype, out, a, b, n, s);
+}
+int launch_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n, cudaStream_t s) {
+    return ew_launch<2>(dtype, dres, dres, dbranch, n, s);
+}
+
+// ===================================================================== bias gradient
+
+#define BIAS_ROWS_PER_CHUNK 128
+
+// Stage 1: block (32 column vectors) x (8 row lanes) sums one chunk of rows
+// for 256 columns into partial[chunk][c].
+template <typename T>
+__global__ void __launch_bounds__(256) bias_partial_kernel(float* __restrict__ partial, const T* __restrict__ dy,
+                                                           int N, int C) {
+    __shared__ float sm[8][256 + 8];
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+    const int c = (blockIdx.x * 32 + tx) * 8;
+    const int r0 = blockIdx.y * BIAS_ROWS_PER_CHUNK;
+    const int r1 = min(N, r0 + BIAS_ROWS_PER_CHUNK);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (c < C) {
+        for (int r = r0 + ty; r < r1; r += 8) {
+            float v[8];
+            load8(dy + (int64_t)r * C + c, v);
+#pragma unroll
+            for (int j = 0; j < 8; j++) acc[j] += v[j];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) sm[ty][tx * 8 + j] = acc[j];
+    __syncthreads();
+    const int col = threadIdx.x;  // 0..255 within this block's slab
+    const int gc = blockIdx.x * 256 + col;
+    if (gc < C) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) s += sm[k][col];
+        partial[(int64_t)blockIdx.y * C + gc] = s;
+    }
+}
+
+__global__ void bias_reduce_kernel(float* __restrict__ dbias, const float* __restrict__ partial, int chunks, int C) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float s = 0.f;
+    for (int k = 0; k < chunks; k++) s += partial[(int64_t)k * C + c];
+    dbias[c] = s;
+}
+
+size_t bias_backward_scratch(int N, int C) {
+    const size_t chunks = (N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
+    return chunks * C * 4;
+}
+
+int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s) {
+    const int chunks = (N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
+    dim3 grid((C + 255) / 256, chunks);
+    if (dtype == GPT2_MODE_BF16)
+        bias_partial_kernel<bf16><<<grid, 256, 0, s>>>((float*)scratch, (const bf16*)dy, N, C);
+    else
+        bias_partial_kernel<float><<<grid, 256, 0, s>>>((float*)scratch, (const float*)dy, N, C);
+    bias_reduce_kernel<<<(C + 255) / 256, 256, 0, s>>>(dbias, (const float*)scratch, chunks, C);
+    return 2;
+}
+
+// ===================================================================== AdamW
+
+#define ADAM_UNROLL 2
+
+// Thread per 4 consecutive parameters (float4), ADAM_UNROLL groups per thread.
+__global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ theta, bf16* __restrict__ pbf,
+                                                    const float* __restrict__ grad, float* __restrict__ m,
+                                                    float* __restrict__ v, int64_t n4, float lr, float b1, float b2,
+                                                    float eps, float wd, float inv_bc1, float inv_bc2) {
+    const int64_t base = (int64_t)blockIdx.x * (256 * ADAM_UNROLL) + threadIdx.x;
+    float4 th[ADAM_UNROLL], g[ADAM_UNROLL], mm[ADAM_UNROLL], vv[ADAM_UNROLL];
+#pragma unroll
+    for (int u = 0; u < ADAM_UNROLL; u++) {
+        const int64_t i = base + u * 256;
+        if (i < n4) {
+            th[u] = __ldcs(reinterpret_cast<const float4*>(theta) + i);
+            g[u] = __ldcs(reinterpret_cast<const float4*>(grad) + i);
+            mm[u] = __ldcs(reinterpret_cast<const float4*>(m) + i);
+            vv[u] = __ldcs(reinterpret_cast<const float4*>(v) + i);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < ADAM_UNROLL; u++) {
+        const int64_t i = base + u * 256;
+        if (i >= n4) continue;
+        float* pt = &th[u].x;
+        const float* pg = &g[u].x;
+        float* pm = &mm[u].x;
+        float* pv = &vv[u].x;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float gj = pg[j];
+            pm[j] = b1 * pm[j] + (1.f - b1) * gj;
+            pv[j] = b2 * pv[j] + (1.f - b2) * gj * gj;
+            const float mhat = pm[j] * inv_bc1;
+            const float vhat = pv[j] * inv_bc2;
+            pt[j] = pt[j] - lr * (mhat / (sqrtf(vhat) + eps) + wd * pt[j]);
+        }
+        __stcs(reinterpret_cast<float4*>(theta) + i, th[u]);
+        __stcs(reinterpret_cast<float4*>(m) + i, mm[u]);
+        __stcs(reinterpret_cast<float4*>(v) + i, vv[u]);
+        if (pbf) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(pt[0], pt[1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(pt[2], pt[3]);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&lo);
+            w.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(pbf)[i] = w;
+        }
+    }
+}
+
+int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v, int64_t n, float lr, float b1,
+                 float b2, float eps, float wd, int t, cudaStream_t s) {
+    const int64_t n4 = n / 4;
+    const double bc1 = 1.0 - pow((double)b1, (double)t);
+    const double bc2 = 1.0 - pow((double)b2, (double)t);
+    const int64_t per_block = 256 * ADAM_UNROLL;
+    const int blocks = (int)((n4 + per_block - 1) / per_block);
+    if (blocks == 0) return 0;
+    adamw_kernel<<<blocks, 256, 0, s>>>(master, (bf16*)pbf, grad, m, v, n4, lr, b1, b2, eps, wd,
+                                        (float)(1.0 / bc1), (float)(1.0 / bc2));
+    return 1;
+}

@@ -1,0 +1,551 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// D[M,N] = sum_k A(m,k) B(n,k) (+ bias[n]), bf16 operands, fp32 accumulation
+// in tensor memory (TMEM). These are the matmuls of the GPT-2 step: the
+// linear forwards (A = activations, K-major; B = weight [N,K], K-major), the
+// input gradients dX = dY W (B = W read MN-major) and the weight gradients
+// dW = dY^T X (both operands MN-major, fp32 output, long K = B*T, split-K).
+//
+// Structure: a persistent kernel, one CTA per SM, 6 warps.
+//   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
+//               into a ring of shared-memory stages, completion on mbarriers.
+//   warp 1      allocates TMEM (two BN-column fp32 accumulators) and one
+//               thread issues tcgen05.mma (M=128, N=BN, K=16) from shared-
+//               memory descriptors; tcgen05.commit frees each stage and
+//               signals a finished accumulator.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31 = tile rows), + bias, convert, store.
+// Two accumulators let the epilogue of one tile overlap the MMAs of the next.
+// Every mbarrier wait is bounded: on timeout the kernel sets a status bit,
+// stops, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include "common.cuh"
+#include "launch.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;               // 64 bf16 = 128 bytes = one swizzle row
+constexpr int NUM_THREADS = 192;     // 6 warps
+constexpr int EPI_WARP0 = 2;
+
+template <int BN> struct TileCfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+struct GemmArgs {
+    void* D;             // output (bf16 or fp32), or null when writing split partials
+    const void* bias;    // bf16 [N] or null
+    float* partial;      // split-K partial sums [splits][M][N] (when splits > 1)
+    int* status;
+    int M, N, K;
+    int d_fp32;
+    int splits;
+    int kb_per_split;
+    int n_tiles;         // ceil(N / BN)
+    int units;           // m_tiles * n_tiles * splits
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity. Returns false (after
+// flagging) on timeout or when another role has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    if (mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; it++) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
+                set_status(status, GPT2_FLAG_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+// Bounded wait used while shutting down (ignores the abort flag).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* status) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (clock64() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
+            set_status(status, GPT2_FLAG_TIMEOUT);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem), kind::f16 (bf16 operands), fp32 accumulate.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of the accumulator for this thread's lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
+// start address >> 4 in bits 0-13, leading-dimension byte offset >> 4 in
+// 16-29, stride-dimension byte offset >> 4 in 32-45, descriptor version 1 in
+// 46-47, layout type 2 (128-byte swizzle) in 61-63.
+// K-major operand (rows of 64 k-values = 128 B, 8-row groups of 1024 B):
+//   SBO = 1024 (next 8 rows), LBO unused.
+// MN-major operand (rows of 64 m- or n-values at one k, 8-k-row groups of
+//   1024 B, 64-wide MN chunks one after another): LBO = chunk stride,
+//   SBO = 1024 (next 8 k-rows).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
+// bf16 (bits 7-9 and 10-12 = 1), A/B major-ness (bits 15, 16: 1 = MN-major),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    using Cfg = TileCfg<BN>;
+    constexpr int S = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned operand ring (the 128-byte swizzle pattern repeats every 1024 B).
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t a_stage0 = base;
+    const uint32_t b_stage0 = base + S * Cfg::A_BYTES;
+    uint8_t* bar_area = gbase + S * Cfg::STAGE_BYTES;
+    const uint32_t bars = base + S * Cfg::STAGE_BYTES;
+    // barrier layout: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (2 * S + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * S + 5) + 4);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr((const void*)tmem_slot)),
+                     "r"(Cfg::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_kb = (g.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[S];
+            for (int s = 0; s < S; s++) issued_phase[s] = -1;
+            bool ok = true;
+            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
+                const int split = u % g.splits;
+                const int tile = u / g.splits;
+                const int m0 = (tile / g.n_tiles) * BM, n0 = (tile % g.n_tiles) * BN;
+                const int kb0 = split * g.kb_per_split;
+                const int kb1 = min(num_kb, kb0 + g.kb_per_split);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                    const uint32_t sa = a_stage0 + stage * Cfg::A_BYTES;
+                    const uint32_t sb = b_stage0 + stage * Cfg::B_BYTES;
+                    if (!A_MN) {
+                        tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m0);
+                    } else {
+                        tma_load_2d(sa, &tmA, full_bar(stage), m0, kb * BK);
+                        tma_load_2d(sa + 64 * 128, &tmA, full_bar(stage), m0 + 64, kb * BK);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, n0);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN / 64; c++)
+                            tma_load_2d(sb + c * 64 * 128, &tmB, full_bar(stage), n0 + 64 * c, kb * BK);
+                    }
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // make sure no copy into this CTA's shared memory is still in flight
+            for (int s = 0; s < S; s++)
+                if (issued_phase[s] >= 0) mbar_drain(full_bar(s), (uint32_t)issued_phase[s], g.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
+            constexpr uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-wide k step
+            constexpr uint32_t b_kstep = B_MN ? 16 * 128 : 32;
+            constexpr uint32_t a_lbo = A_MN ? 64 * 128 : 16;
+            constexpr uint32_t b_lbo = B_MN ? 64 * 128 : 16;
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
+                const int split = u % g.splits;
+                const int kb0 = split * g.kb_per_split;
+                const int kb1 = min(num_kb, kb0 + g.kb_per_split);
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = a_stage0 + stage * Cfg::A_BYTES;
+                    const uint32_t sb = b_stage0 + stage * Cfg::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; k++) {
+                        const uint64_t ad = sw128_desc(sa + k * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = sw128_desc(sb + k * b_kstep, b_lbo, 1024);
+                        tc_mma(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));  // stage reusable once these MMAs finish
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));  // accumulator complete
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // all MMAs issued by this thread must finish before TMEM is freed
+            tc_commit(drain_bar);
+            mbar_drain(drain_bar, 0, g.status);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2..5)
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        const int row_in_tile = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
+            const int split = u % g.splits;
+            const int tile = u / g.splits;
+            const int m0 = (tile / g.n_tiles) * BM, n0 = (tile % g.n_tiles) * BN;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, g.status)) break;
+            tc_fence_after();
+            const int m = m0 + row_in_tile;
+            const bool row_ok = m < g.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c++) {
+                const int n = n0 + c * 32;
+                if (n >= g.N) break;  // uniform across the warp
+                float v[32];
+                tc_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
+                if (!row_ok) continue;
+                if (g.splits > 1) {
+                    float* dst = g.partial + ((size_t)split * g.M + m) * g.N + n;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        if (n + q * 8 < g.N) {
+                            float f[8];
+#pragma unroll
+                            for (int j = 0; j < 8; j++) f[j] = v[q * 8 + j];
+                            store8(dst + q * 8, f);
+                        }
+                    }
+                } else {
+                    if (g.bias) {
+                        const bf16* bp = reinterpret_cast<const bf16*>(g.bias) + n;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (n + q * 8 < g.N) {
+                                float bb[8];
+                                load8(bp + q * 8, bb);
+#pragma unroll
+                                for (int j = 0; j < 8; j++) v[q * 8 + j] += bb[j];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        if (n + q * 8 < g.N) {
+                            float f[8];
+#pragma unroll
+                            for (int j = 0; j < 8; j++) f[j] = v[q * 8 + j];
+                            if (g.d_fp32)
+                                store8(reinterpret_cast<float*>(g.D) + (size_t)m * g.N + n + q * 8, f);
+                            else
+                                store8(reinterpret_cast<bf16*>(g.D) + (size_t)m * g.N + n + q * 8, f);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(Cfg::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// D = sum over splits of partial (+ bias), fp32 or bf16 out. Fixed order.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(void* D, int d_fp32, const float* __restrict__ partial,
+                                                            const bf16* __restrict__ bias, int splits, int64_t MN,
+                                                            int N) {
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (i >= MN) return;
+    float acc[8];
+    load8(partial + i, acc);
+    for (int s = 1; s < splits; s++) {
+        float v[8];
+        load8(partial + (int64_t)s * MN + i, v);
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[j] += v[j];
+    }
+    if (bias) {
+        float b[8];
+        load8(bias + (i % N), b);
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[j] += b[j];
+    }
+    if (d_fp32)
+        store8(reinterpret_cast<float*>(D) + i, acc);
+    else
+        store8(reinterpret_cast<bf16*>(D) + i, acc);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix, box
+// [box_outer, 64] (64 inner elements = 128 bytes), 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int bn, splits, kb_per_split, n_tiles, m_tiles, units, grid;
+};
+
+Plan make_plan(int M, int N, int K, int d_fp32) {
+    Plan p;
+    p.bn = N <= 128 ? 128 : 256;
+    p.m_tiles = (M + BM - 1) / BM;
+    p.n_tiles = (N + p.bn - 1) / p.bn;
+    const int num_kb = (K + BK - 1) / BK;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int sms = gpt2_num_sms();
+    p.splits = 1;
+    if (d_fp32 && tiles < sms) {
+        // weight gradients: few output tiles and a long K; split K so that
+        // about two units land on every SM, each with >= 4 k-blocks.
+        int want = (2 * sms + tiles - 1) / tiles;
+        int cap = num_kb / 4 > 0 ? num_kb / 4 : 1;
+        p.splits = want < cap ? want : cap;
+        if (p.splits < 1) p.splits = 1;
+    }
+    p.kb_per_split = (num_kb + p.splits - 1) / p.splits;
+    p.splits = (num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
+    p.units = tiles * p.splits;
+    p.grid = p.units < sms ? p.units : sms;
+    return p;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args, int grid, cudaStream_t s) {
+    using Cfg = TileCfg<BN>;
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES);
+        configured = true;
+    }
+    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, args);
+}
+
+template <int BN>
+void launch_tc_layout(int a_mn, int b_mn, const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
+                      int grid, cudaStream_t s) {
+    if (!a_mn && !b_mn) launch_tc<BN, false, false>(ma, mb, args, grid, s);
+    else if (!a_mn && b_mn) launch_tc<BN, false, true>(ma, mb, args, grid, s);
+    else if (a_mn && !b_mn) launch_tc<BN, true, false>(ma, mb, args, grid, s);
+    else launch_tc<BN, true, true>(ma, mb, args, grid, s);
+}
+
+}  // namespace
+
+size_t matmul_tc_scratch(int M, int N, int K, int d_fp32) {
+    Plan p = make_plan(M, N, K, d_fp32);
+    return p.splits > 1 ? (size_t)p.splits * M * N * 4 : 0;
+}
+
+int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
+                     int N, int K, void* scratch, int* status, cudaStream_t s) {
+    Plan p = make_plan(M, N, K, d_fp32);
+    CUtensorMap ma, mb;
+    bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
+    ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
+                     : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
+    if (!ok) return GPT2_ERR_CUDA;
+    GemmArgs g;
+    g.D = D;
+    g.bias = p.splits > 1 ? nullptr : bias;
+    g.partial = (float*)scratch;
+    g.status = status;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.d_fp32 = d_fp32;
+    g.splits = p.splits;
+    g.kb_per_split = p.kb_per_split;
+    g.n_tiles = p.n_tiles;
+    g.units = p.units;
+    if (p.bn == 128) launch_tc_layout<128>(a_mn, b_mn, ma, mb, g, p.grid, s);
+    else launch_tc_layout<256>(a_mn, b_mn, ma, mb, g, p.grid, s);
+    if (p.splits > 1) {
+        const int64_t MN = (int64_t)M * N;
+        const int blocks = (int)((MN / 8 + 255) / 256);
+        splitk_reduce_kernel<<<blocks, 256, 0, s>>>(D, d_fp32, (const float*)scratch, (const bf16*)bias, p.splits,
+                                                    MN, N);
+        return 2;
+    }
+    return 1;
+}

@@ -1,0 +1,48 @@
+// Host-side launchers of the step's kernels. Each enqueues its kernels on
+// stream s and returns the number of kernel launches it made (>= 0), or a
+// negative gpt2_status for an unsupported shape. Arguments are already
+// validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+int launch_encoder_forward(int dtype, void* x0, const int32_t* tokens, const void* wte, const void* wpe, int B,
+                           int T, int C, int V, int* status, cudaStream_t s);
+size_t encoder_backward_scratch(int B, int T, int C);
+int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0, const int32_t* tokens, int B, int T,
+                            int C, void* scratch, cudaStream_t s);
+
+int launch_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                             const void* beta, int N, int C, cudaStream_t s);
+size_t layernorm_backward_scratch(int N, int C);
+int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                              const void* gamma, const float* mean, const float* rstd, int N, int C, void* scratch,
+                              cudaStream_t s);
+
+int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream_t s);
+int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s);
+int launch_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s);
+int launch_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n, cudaStream_t s);
+
+size_t bias_backward_scratch(int N, int C);
+int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s);
+
+int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
+                      float dloss, int* status, cudaStream_t s);
+int launch_mean_loss(float* out, const float* losses, int N, cudaStream_t s);
+
+int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v, int64_t n, float lr, float b1,
+                 float b2, float eps, float wd, int t, cudaStream_t s);
+
+int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
+                             cudaStream_t s);
+size_t attention_backward_scratch(int B, int T, int H);
+int launch_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* o,
+                              const float* lse, int B, int T, int C, int H, void* scratch, cudaStream_t s);
+
+// Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
+size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32);
+int launch_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias,
+                  int M, int N, int K, void* scratch, int* status, cudaStream_t s);

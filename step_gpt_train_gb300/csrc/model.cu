@@ -1,0 +1,745 @@
+// GPT-2 training step: workspace plan, init, and the forward / backward /
+// AdamW launch sequences behind the C ABI of gpt2.h.
+//
+// The sequence follows the kernel table of llm.c "State of the Union
+// [May 3, 2024]" ("Runtime, DRAM traffic, instructions"): per step one
+// encoder forward, 2L+1 layernorm forwards, 4 matmuls per layer plus the LM
+// head, L attention forwards, 2L residuals, L GELUs, the fused classifier;
+// then the mirrored backward and one AdamW over every parameter.
+#include "common.cuh"
+#include "launch.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+int gpt2_num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    }
+    return n;
+}
+
+namespace {
+
+constexpr size_t WS_ALIGN = 1024;
+constexpr int64_t PARAM_ALIGN = 64;  // elements; keeps every tensor 128-byte aligned in bf16
+
+enum InitKind { INIT_NORMAL = 0, INIT_ZERO = 1, INIT_ONE = 2 };
+
+struct TensorSpec {
+    std::string name;
+    int64_t rows, cols;
+    int64_t offset;  // element offset in the flat parameter buffers
+    int init;
+    double std;
+};
+
+struct LayerBufs {
+    void *x, *ln1, *qkv, *atty, *x1, *ln2, *fch, *fchg;
+    float *mean1, *rstd1, *lse, *mean2, *rstd2;
+};
+
+}  // namespace
+
+struct gpt2 {
+    gpt2_config cfg;
+    int L, C, H, V, Vp, maxT, maxB, mode, dtype;
+    size_t act;  // bytes per activation element
+    cudaStream_t stream;
+    uint8_t* ws;
+    size_t ws_bytes;
+    std::vector<TensorSpec> tensors;
+    int64_t np;  // flat parameter count (with alignment gaps)
+    float *master, *grads, *adam_m, *adam_v;
+    void* params;  // compute copy: bf16 (bf16 mode) or the master itself
+    int* status;
+    float* loss_dev;
+    int32_t* tokens;
+    std::vector<LayerBufs> layers;
+    void *xL, *lnf, *logits, *fwd_tmp;
+    float *meanf, *rstdf, *losses;
+    void *dres, *dtmp, *dtmp2, *dbig, *dqkv;
+    void* scratch;
+    size_t scratch_bytes;
+    int B, T;
+    int state;  // 0: none, 1: forward with targets done, 2: backward done
+    int64_t launches;
+    int64_t fam_calls[GPT2_K_COUNT], fam_launches[GPT2_K_COUNT];
+    double fam_work[GPT2_K_COUNT], fam_ms[GPT2_K_COUNT];
+    bool timing;
+    struct Pending { int fam; cudaEvent_t a, b; };
+    std::vector<Pending> pending;
+    std::vector<cudaEvent_t> pool;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool config_ok(const gpt2_config* c) {
+    if (!c) return false;
+    if (c->n_layer < 1 || c->n_embd < 8 || c->n_head < 1 || c->vocab < 1 || c->max_T < 1 || c->max_B < 1) return false;
+    if (c->n_embd % 8 || c->n_embd % c->n_head || c->n_embd > 2048) return false;
+    if (c->vocab_padded < c->vocab || c->vocab_padded % 8 || c->vocab_padded > 65536) return false;
+    const int hd = c->n_embd / c->n_head;
+    if (c->mode == GPT2_MODE_BF16) return hd == 64;
+    if (c->mode == GPT2_MODE_FP32) return hd == 8 || hd == 16 || hd == 32 || hd == 64;
+    return false;
+}
+
+std::vector<TensorSpec> make_specs(const gpt2_config* c, int64_t* np_out) {
+    const int64_t C = c->n_embd, L = c->n_layer;
+    const double std_w = 0.02, std_res = 0.02 / std::sqrt(2.0 * (double)L);
+    std::vector<TensorSpec> t;
+    auto add = [&](const std::string& n, int64_t r, int64_t cc, int init, double sd) {
+        t.push_back({n, r, cc, 0, init, sd});
+    };
+    add("wte", c->vocab_padded, C, INIT_NORMAL, std_w);
+    add("wpe", c->max_T, C, INIT_NORMAL, std_w);
+    for (int l = 0; l < L; l++) {
+        const std::string p = "h" + std::to_string(l) + ".";
+        add(p + "ln1.g", C, 1, INIT_ONE, 0);
+        add(p + "ln1.b", C, 1, INIT_ZERO, 0);
+        add(p + "qkv.w", 3 * C, C, INIT_NORMAL, std_w);
+        add(p + "qkv.b", 3 * C, 1, INIT_ZERO, 0);
+        add(p + "proj.w", C, C, INIT_NORMAL, std_res);
+        add(p + "proj.b", C, 1, INIT_ZERO, 0);
+        add(p + "ln2.g", C, 1, INIT_ONE, 0);
+        add(p + "ln2.b", C, 1, INIT_ZERO, 0);
+        add(p + "fc.w", 4 * C, C, INIT_NORMAL, std_w);
+        add(p + "fc.b", 4 * C, 1, INIT_ZERO, 0);
+        add(p + "fcproj.w", C, 4 * C, INIT_NORMAL, std_res);
+        add(p + "fcproj.b", C, 1, INIT_ZERO, 0);
+    }
+    add("lnf.g", C, 1, INIT_ONE, 0);
+    add("lnf.b", C, 1, INIT_ZERO, 0);
+    int64_t off = 0;
+    for (auto& s : t) {
+        s.offset = off;
+        off += (s.rows * s.cols + PARAM_ALIGN - 1) / PARAM_ALIGN * PARAM_ALIGN;
+    }
+    *np_out = off;
+    return t;
+}
+
+enum { T_WTE = 0, T_WPE = 1 };
+inline int tidx(int l, int k) { return 2 + 12 * l + k; }  // k: 0 ln1.g 1 ln1.b 2 qkv.w 3 qkv.b 4 proj.w 5 proj.b
+                                                          //    6 ln2.g 7 ln2.b 8 fc.w 9 fc.b 10 fcproj.w 11 fcproj.b
+inline int tlnf(int L, int k) { return 2 + 12 * L + k; }
+
+// Carve the workspace. With m == nullptr only the total size is computed.
+size_t plan(const gpt2_config* c, gpt2* m) {
+    int64_t np = 0;
+    make_specs(c, &np);
+    const size_t act = c->mode == GPT2_MODE_BF16 ? 2 : 4;
+    const size_t BT = (size_t)c->max_B * c->max_T;
+    const size_t C = c->n_embd, L = c->n_layer, Vp = c->vocab_padded, H = c->n_head;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        off = align_up(off, WS_ALIGN);
+        size_t r = off;
+        off += bytes;
+        return r;
+    };
+    const size_t o_status = take(256);
+    const size_t o_tokens = take(BT * 4);
+    const size_t o_master = take((size_t)np * 4);
+    const size_t o_params = c->mode == GPT2_MODE_BF16 ? take((size_t)np * 2) : o_master;
+    const size_t o_grads = take((size_t)np * 4);
+    const size_t o_m = take((size_t)np * 4);
+    const size_t o_v = take((size_t)np * 4);
+    std::vector<size_t> lo(13 * L);
+    for (size_t l = 0; l < L; l++) {
+        size_t* p = &lo[13 * l];
+        p[0] = take(BT * C * act);      // x (layer input)
+        p[1] = take(BT * C * act);      // ln1
+        p[2] = take(BT * 3 * C * act);  // qkv
+        p[3] = take(BT * C * act);      // atty
+        p[4] = take(BT * C * act);      // x1
+        p[5] = take(BT * C * act);      // ln2
+        p[6] = take(BT * 4 * C * act);  // fch
+        p[7] = take(BT * 4 * C * act);  // fchg
+        p[8] = take(BT * 4);            // mean1
+        p[9] = take(BT * 4);            // rstd1
+        p[10] = take(BT * H * 4);       // lse
+        p[11] = take(BT * 4);           // mean2
+        p[12] = take(BT * 4);           // rstd2
+    }
+    const size_t o_xL = take(BT * C * act);
+    const size_t o_lnf = take(BT * C * act);
+    const size_t o_meanf = take(BT * 4);
+    const size_t o_rstdf = take(BT * 4);
+    const size_t o_logits = take(BT * Vp * act);
+    const size_t o_losses = take(BT * 4);
+    const size_t o_fwd_tmp = take(BT * C * act);
+    const size_t o_dres = take(BT * C * act);
+    const size_t o_dtmp = take(BT * C * act);
+    const size_t o_dtmp2 = take(BT * C * act);
+    const size_t o_dbig = take(BT * 4 * C * act);
+    const size_t o_dqkv = take(BT * 3 * C * act);
+    // scratch: the largest need of any scratch-using op of the backward
+    const int dt = c->mode;
+    const int iBT = (int)BT, iC = (int)C, iVp = (int)Vp;
+    size_t sc = 256;
+    auto need = [&](size_t b) { sc = b > sc ? b : sc; };
+    const int outs[4] = {3 * iC, iC, 4 * iC, iC};
+    const int ins[4] = {iC, iC, iC, 4 * iC};
+    for (int k = 0; k < 4; k++) {
+        need(matmul_scratch(dt, outs[k], ins[k], iBT, 1));       // dW
+        need(matmul_scratch(dt, iBT, ins[k], outs[k], 0));       // dX
+        need(bias_backward_scratch(iBT, outs[k]));
+    }
+    need(matmul_scratch(dt, iVp, iC, iBT, 1));
+    need(matmul_scratch(dt, iBT, iC, iVp, 0));
+    need(layernorm_backward_scratch(iBT, iC));
+    need(attention_backward_scratch(c->max_B, c->max_T, (int)H));
+    need(encoder_backward_scratch(c->max_B, c->max_T, iC));
+    const size_t o_scratch = take(sc);
+    const size_t total = align_up(off, WS_ALIGN);
+    if (m) {
+        uint8_t* w = m->ws;
+        m->np = np;
+        m->status = (int*)(w + o_status);
+        m->loss_dev = (float*)(w + o_status + 64);
+        m->tokens = (int32_t*)(w + o_tokens);
+        m->master = (float*)(w + o_master);
+        m->params = w + o_params;
+        m->grads = (float*)(w + o_grads);
+        m->adam_m = (float*)(w + o_m);
+        m->adam_v = (float*)(w + o_v);
+        m->layers.resize(L);
+        for (size_t l = 0; l < L; l++) {
+            size_t* p = &lo[13 * l];
+            LayerBufs& b = m->layers[l];
+            b.x = w + p[0]; b.ln1 = w + p[1]; b.qkv = w + p[2]; b.atty = w + p[3]; b.x1 = w + p[4];
+            b.ln2 = w + p[5]; b.fch = w + p[6]; b.fchg = w + p[7];
+            b.mean1 = (float*)(w + p[8]); b.rstd1 = (float*)(w + p[9]); b.lse = (float*)(w + p[10]);
+            b.mean2 = (float*)(w + p[11]); b.rstd2 = (float*)(w + p[12]);
+        }
+        m->xL = w + o_xL;
+        m->lnf = w + o_lnf;
+        m->meanf = (float*)(w + o_meanf);
+        m->rstdf = (float*)(w + o_rstdf);
+        m->logits = w + o_logits;
+        m->losses = (float*)(w + o_losses);
+        m->fwd_tmp = w + o_fwd_tmp;
+        m->dres = w + o_dres;
+        m->dtmp = w + o_dtmp;
+        m->dtmp2 = w + o_dtmp2;
+        m->dbig = w + o_dbig;
+        m->dqkv = w + o_dqkv;
+        m->scratch = w + o_scratch;
+        m->scratch_bytes = sc;
+    }
+    return total;
+}
+
+// ---- counter-based init (splitmix64 + Box-Muller, both published) ----
+
+inline uint64_t splitmix64_next(uint64_t& s) {
+    s += 0x9E3779B97F4A7C15ULL;
+    uint64_t z = s;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+// Element i of tensor k: counter k*2^40 + i; state seed ^ (counter * golden);
+// two splitmix64 outputs give u1 in (0,1], u2 in [0,1); z = sqrt(-2 ln u1) cos(2 pi u2).
+inline float init_draw(uint64_t seed, uint64_t k, uint64_t i, double sd) {
+    uint64_t s = seed ^ (((k << 40) + i) * 0x9E3779B97F4A7C15ULL);
+    const uint64_t r1 = splitmix64_next(s);
+    const uint64_t r2 = splitmix64_next(s);
+    const double u1 = ((double)(r1 >> 11) + 1.0) * 0x1p-53;
+    const double u2 = (double)(r2 >> 11) * 0x1p-53;
+    const double z = std::sqrt(-2.0 * std::log(u1)) * std::cos(2.0 * 3.141592653589793 * u2);
+    return (float)(sd * z);
+}
+
+void init_host(const gpt2_config* c, uint64_t seed, const std::vector<TensorSpec>& specs, float* out) {
+    unsigned nth = std::thread::hardware_concurrency();
+    if (nth == 0) nth = 4;
+    if (nth > 32) nth = 32;
+    std::vector<std::thread> th;
+    for (unsigned w = 0; w < nth; w++) {
+        th.emplace_back([&, w] {
+            for (size_t k = 0; k < specs.size(); k++) {
+                const TensorSpec& s = specs[k];
+                const int64_t n = s.rows * s.cols;
+                const int64_t per = (n + nth - 1) / nth;
+                const int64_t lo = (int64_t)w * per, hi = std::min<int64_t>(n, lo + per);
+                for (int64_t i = lo; i < hi; i++) {
+                    float v;
+                    if (s.init == INIT_ZERO) v = 0.f;
+                    else if (s.init == INIT_ONE) v = 1.f;
+                    else v = init_draw(seed, (uint64_t)k, (uint64_t)i, s.std);
+                    if (k == T_WTE && i / s.cols >= c->vocab) v = 0.f;  // padded vocab rows
+                    out[s.offset + i] = v;
+                }
+            }
+        });
+    }
+    for (auto& t : th) t.join();
+}
+
+__global__ void f32_to_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ in, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = __float2bfloat16_rn(in[i]);
+}
+__global__ void bf16_to_f32_kernel(float* __restrict__ out, const bf16* __restrict__ in, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = __bfloat162float(in[i]);
+}
+
+// ---- op accounting ----
+
+struct Op {
+    gpt2* m;
+    int fam;
+    cudaEvent_t a = nullptr;
+    Op(gpt2* mm, int f) : m(mm), fam(f) {
+        if (m->timing) {
+            if (m->pool.empty()) {
+                cudaEvent_t e;
+                cudaEventCreate(&e);
+                m->pool.push_back(e);
+            }
+            a = m->pool.back();
+            m->pool.pop_back();
+            cudaEventRecord(a, m->stream);
+        }
+    }
+    // Record the op's launches and work; returns GPT2_OK or an error.
+    int done(int launches, double work) {
+        if (launches < 0) return launches;
+        m->launches += launches;
+        m->fam_calls[fam] += 1;
+        m->fam_launches[fam] += launches;
+        m->fam_work[fam] += work;
+        if (a) {
+            cudaEvent_t b;
+            if (m->pool.empty()) cudaEventCreate(&b);
+            else { b = m->pool.back(); m->pool.pop_back(); }
+            cudaEventRecord(b, m->stream);
+            m->pending.push_back({fam, a, b});
+            a = nullptr;
+        }
+        return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    }
+};
+
+#define TRY(x)                     \
+    do {                           \
+        int _r = (x);              \
+        if (_r != GPT2_OK) return _r; \
+    } while (0)
+
+inline void* P(gpt2* m, int i) { return (uint8_t*)m->params + (size_t)m->tensors[i].offset * m->act; }
+inline float* G(gpt2* m, int i) { return m->grads + m->tensors[i].offset; }
+
+int op_matmul(gpt2* m, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
+              int N, int K) {
+    Op op(m, GPT2_K_MATMUL);
+    return op.done(launch_matmul(m->dtype, D, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, m->scratch, m->status,
+                                 m->stream),
+                   2.0 * M * N * K);
+}
+
+// y = x W^T + b for x [BT, in], W [out, in].
+int linear_fwd(gpt2* m, void* y, const void* x, int wi, int bi, int BT, int in, int out) {
+    return op_matmul(m, y, 0, x, 0, P(m, wi), 0, bi >= 0 ? P(m, bi) : nullptr, BT, out, in);
+}
+
+// dx = dy W, dW = dy^T x, db = column sums of dy.
+int linear_bwd(gpt2* m, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in, int out) {
+    TRY(op_matmul(m, dx, 0, dy, 0, P(m, wi), 1, nullptr, BT, in, out));
+    TRY(op_matmul(m, G(m, wi), 1, dy, 1, x, 1, nullptr, out, in, BT));
+    if (bi >= 0) {
+        Op op(m, GPT2_K_BIAS_BWD);
+        TRY(op.done(launch_bias_backward(m->dtype, G(m, bi), dy, BT, out, m->scratch, m->stream),
+                    (double)BT * out * m->act + out * 4.0));
+    }
+    return GPT2_OK;
+}
+
+int ln_fwd(gpt2* m, void* y, float* mean, float* rstd, const void* x, int gi, int BT) {
+    Op op(m, GPT2_K_LAYERNORM_FWD);
+    return op.done(launch_layernorm_forward(m->dtype, y, mean, rstd, x, P(m, gi), P(m, gi + 1), BT, m->C, m->stream),
+                   (double)BT * (2.0 * m->C * m->act + 8));
+}
+
+int ln_bwd(gpt2* m, void* dx, const void* dy, const void* x, int gi, const float* mean, const float* rstd, int BT) {
+    Op op(m, GPT2_K_LAYERNORM_BWD);
+    return op.done(launch_layernorm_backward(m->dtype, dx, G(m, gi), G(m, gi + 1), dy, x, P(m, gi), mean, rstd, BT,
+                                             m->C, m->scratch, m->stream),
+                   (double)BT * (3.0 * m->C * m->act + 8));
+}
+
+int residual_fwd(gpt2* m, void* out, const void* a, const void* b, int64_t n) {
+    Op op(m, GPT2_K_RESIDUAL_FWD);
+    return op.done(launch_residual_forward(m->dtype, out, a, b, n, m->stream), 3.0 * n * m->act);
+}
+
+int residual_bwd(gpt2* m, void* dres, const void* dbranch, int64_t n) {
+    Op op(m, GPT2_K_RESIDUAL_BWD);
+    return op.done(launch_residual_backward(m->dtype, dres, dbranch, n, m->stream), 3.0 * n * m->act);
+}
+
+double attn_fwd_flops(int B, int T, int C) { return 2.0 * 2.0 * B * C * (double)T * (T + 1) / 2.0; }
+
+int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
+    const int BT = B * T, C = m->C, L = m->L;
+    {
+        Op op(m, GPT2_K_ENCODER_FWD);
+        TRY(op.done(launch_encoder_forward(m->dtype, m->layers[0].x, m->tokens, P(m, T_WTE), P(m, T_WPE), B, T, C,
+                                           m->V, m->status, m->stream),
+                    (double)BT * (3.0 * C * m->act + 4)));
+    }
+    for (int l = 0; l < L; l++) {
+        LayerBufs& b = m->layers[l];
+        void* xnext = l + 1 < L ? m->layers[l + 1].x : m->xL;
+        TRY(ln_fwd(m, b.ln1, b.mean1, b.rstd1, b.x, tidx(l, 0), BT));
+        TRY(linear_fwd(m, b.qkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
+        {
+            Op op(m, GPT2_K_ATTENTION_FWD);
+            TRY(op.done(launch_attention_forward(m->dtype, b.atty, b.lse, b.qkv, B, T, C, m->H, m->stream),
+                        attn_fwd_flops(B, T, C)));
+        }
+        TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
+        TRY(residual_fwd(m, b.x1, b.x, m->fwd_tmp, (int64_t)BT * C));
+        TRY(ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, tidx(l, 6), BT));
+        TRY(linear_fwd(m, b.fch, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
+        {
+            Op op(m, GPT2_K_GELU_FWD);
+            TRY(op.done(launch_gelu_forward(m->dtype, b.fchg, b.fch, (int64_t)BT * 4 * C, m->stream),
+                        2.0 * BT * 4 * C * m->act));
+        }
+        TRY(linear_fwd(m, m->fwd_tmp, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
+        TRY(residual_fwd(m, xnext, b.x1, m->fwd_tmp, (int64_t)BT * C));
+    }
+    TRY(ln_fwd(m, m->lnf, m->meanf, m->rstdf, m->xL, tlnf(L, 0), BT));
+    TRY(op_matmul(m, m->logits, 0, m->lnf, 0, P(m, T_WTE), 0, nullptr, BT, m->Vp, C));
+    if (targets) {
+        {
+            Op op(m, GPT2_K_CLASSIFIER);
+            TRY(op.done(launch_classifier(m->dtype, m->logits, m->losses, targets, BT, m->V, m->Vp, 1.0f / BT,
+                                          m->status, m->stream),
+                        (double)BT * (2.0 * m->Vp * m->act + 8)));
+        }
+        Op op(m, GPT2_K_LOSS_MEAN);
+        TRY(op.done(launch_mean_loss(m->loss_dev, m->losses, BT, m->stream), BT * 4.0));
+    }
+    return GPT2_OK;
+}
+
+int backward_impl(gpt2* m) {
+    const int B = m->B, T = m->T, BT = B * T, C = m->C, L = m->L;
+    // LM head (tied with wte): dlnf = dlogits wte; dwte = dlogits^T lnf (overwrites dwte)
+    TRY(op_matmul(m, m->dtmp, 0, m->logits, 0, P(m, T_WTE), 1, nullptr, BT, C, m->Vp));
+    TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT));
+    TRY(ln_bwd(m, m->dres, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, BT));
+    for (int l = L - 1; l >= 0; l--) {
+        LayerBufs& b = m->layers[l];
+        // MLP branch
+        TRY(linear_bwd(m, m->dbig, m->dres, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
+        {
+            Op op(m, GPT2_K_GELU_BWD);
+            TRY(op.done(launch_gelu_backward(m->dtype, m->dbig, b.fch, m->dbig, (int64_t)BT * 4 * C, m->stream),
+                        3.0 * BT * 4 * C * m->act));
+        }
+        TRY(linear_bwd(m, m->dtmp, m->dbig, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
+        TRY(ln_bwd(m, m->dtmp2, m->dtmp, b.x1, tidx(l, 6), b.mean2, b.rstd2, BT));
+        TRY(residual_bwd(m, m->dres, m->dtmp2, (int64_t)BT * C));
+        // attention branch
+        TRY(linear_bwd(m, m->dtmp, m->dres, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
+        {
+            Op op(m, GPT2_K_ATTENTION_BWD);
+            TRY(op.done(launch_attention_backward(m->dtype, m->dqkv, m->dtmp, b.qkv, b.atty, b.lse, B, T, C, m->H,
+                                                  m->scratch, m->stream),
+                        2.5 * attn_fwd_flops(B, T, C)));
+        }
+        TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
+        TRY(ln_bwd(m, m->dtmp2, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, BT));
+        TRY(residual_bwd(m, m->dres, m->dtmp2, (int64_t)BT * C));
+    }
+    if (T < m->maxT &&
+        cudaMemsetAsync(G(m, T_WPE) + (size_t)T * C, 0, (size_t)(m->maxT - T) * C * 4, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;  // positions >= T get a zero gradient
+    Op op(m, GPT2_K_ENCODER_BWD);
+    return op.done(launch_encoder_backward(m->dtype, G(m, T_WTE), G(m, T_WPE), m->dres, m->tokens, B, T, C,
+                                           m->scratch, m->stream),
+                   (double)BT * (C * m->act + 4) * 2 + (double)BT * C * 8);
+}
+
+int cuda_ok(cudaError_t e) { return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA; }
+
+int refresh_compute_copy(gpt2* m, int64_t off, int64_t n) {
+    if (m->mode != GPT2_MODE_BF16 || n == 0) return GPT2_OK;
+    f32_to_bf16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, m->stream>>>((bf16*)m->params + off, m->master + off, n);
+    m->launches++;
+    return cuda_ok(cudaGetLastError());
+}
+
+int read_status(gpt2* m) {
+    int st = 0;
+    if (cudaMemcpyAsync(&st, m->status, sizeof(int), cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    if (cudaStreamSynchronize(m->stream) != cudaSuccess) return GPT2_ERR_CUDA;
+    if (st & GPT2_FLAG_TIMEOUT) return GPT2_ERR_TIMEOUT;
+    if (st & (GPT2_FLAG_TOKEN_RANGE | GPT2_FLAG_TARGET_RANGE)) return GPT2_ERR_TOKEN_RANGE;
+    return GPT2_OK;
+}
+
+}  // namespace
+
+// =============================================================== C ABI
+
+extern "C" {
+
+int gpt2_workspace_bytes(const gpt2_config* cfg, size_t* bytes_out) {
+    if (!config_ok(cfg) || !bytes_out) return GPT2_ERR_ARG;
+    *bytes_out = plan(cfg, nullptr);
+    return GPT2_OK;
+}
+
+int gpt2_init(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, void* d_workspace, size_t workspace_bytes,
+              void* cuda_stream) {
+    if (!out || !config_ok(cfg) || !d_workspace) return GPT2_ERR_ARG;
+    *out = nullptr;
+    if (((uintptr_t)d_workspace) % WS_ALIGN) return GPT2_ERR_WORKSPACE;
+    const size_t need = plan(cfg, nullptr);
+    if (workspace_bytes < need) return GPT2_ERR_WORKSPACE;
+    gpt2* m = new gpt2();
+    m->cfg = *cfg;
+    m->L = cfg->n_layer; m->C = cfg->n_embd; m->H = cfg->n_head; m->V = cfg->vocab; m->Vp = cfg->vocab_padded;
+    m->maxT = cfg->max_T; m->maxB = cfg->max_B; m->mode = cfg->mode; m->dtype = cfg->mode;
+    m->act = cfg->mode == GPT2_MODE_BF16 ? 2 : 4;
+    m->stream = (cudaStream_t)cuda_stream;
+    m->ws = (uint8_t*)d_workspace;
+    m->ws_bytes = workspace_bytes;
+    int64_t np = 0;
+    m->tensors = make_specs(cfg, &np);
+    plan(cfg, m);
+    m->B = m->T = 0;
+    m->state = 0;
+    m->launches = 0;
+    for (int f = 0; f < GPT2_K_COUNT; f++) {
+        m->fam_calls[f] = m->fam_launches[f] = 0;
+        m->fam_work[f] = m->fam_ms[f] = 0;
+    }
+    m->timing = false;
+    std::vector<float> host((size_t)m->np, 0.f);
+    init_host(cfg, seed, m->tensors, host.data());
+    int r = GPT2_OK;
+    if (cudaMemsetAsync(m->status, 0, 256, m->stream) != cudaSuccess ||
+        cudaMemcpyAsync(m->master, host.data(), (size_t)m->np * 4, cudaMemcpyHostToDevice, m->stream) != cudaSuccess ||
+        cudaMemsetAsync(m->grads, 0, (size_t)m->np * 4, m->stream) != cudaSuccess ||
+        cudaMemsetAsync(m->adam_m, 0, (size_t)m->np * 4, m->stream) != cudaSuccess ||
+        cudaMemsetAsync(m->adam_v, 0, (size_t)m->np * 4, m->stream) != cudaSuccess)
+        r = GPT2_ERR_CUDA;
+    if (r == GPT2_OK) r = refresh_compute_copy(m, 0, m->np);
+    if (r == GPT2_OK) r = cuda_ok(cudaStreamSynchronize(m->stream));
+    if (r != GPT2_OK) {
+        delete m;
+        return r;
+    }
+    *out = m;
+    return GPT2_OK;
+}
+
+int gpt2_forward(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T, float* loss_out) {
+    if (!m || !d_tokens || B < 1 || T < 1 || B > m->maxB || T > m->maxT) return GPT2_ERR_ARG;
+    if (d_targets && !loss_out) return GPT2_ERR_ARG;
+    m->state = 0;
+    m->B = B;
+    m->T = T;
+    if (cudaMemsetAsync(m->status, 0, sizeof(int), m->stream) != cudaSuccess ||
+        cudaMemcpyAsync(m->tokens, d_tokens, (size_t)B * T * 4, cudaMemcpyDeviceToDevice, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    TRY(forward_impl(m, d_targets, B, T));
+    if (!d_targets) return GPT2_OK;
+    float loss = 0.f;
+    if (cudaMemcpyAsync(&loss, m->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    TRY(read_status(m));  // synchronises the stream
+    *loss_out = loss;
+    if (!std::isfinite(loss)) return GPT2_ERR_NONFINITE;
+    m->state = 1;
+    return GPT2_OK;
+}
+
+int gpt2_backward(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    if (m->state != 1) return GPT2_ERR_STATE;
+    TRY(backward_impl(m));
+    m->state = 2;
+    return GPT2_OK;
+}
+
+int gpt2_adamw_step(gpt2_t* m, float lr, float beta1, float beta2, float eps, float weight_decay, int t) {
+    if (!m) return GPT2_ERR_ARG;
+    if (t < 1 || !(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) || !(eps >= 0.f) ||
+        !std::isfinite(lr) || !std::isfinite(weight_decay))
+        return GPT2_ERR_ARG;
+    if (m->state != 2) return GPT2_ERR_STATE;
+    Op op(m, GPT2_K_ADAMW);
+    TRY(op.done(launch_adamw(m->master, m->mode == GPT2_MODE_BF16 ? m->params : nullptr, m->grads, m->adam_m,
+                             m->adam_v, m->np, lr, beta1, beta2, eps, weight_decay, t, m->stream),
+                (double)m->np * (m->mode == GPT2_MODE_BF16 ? 30.0 : 28.0)));
+    m->state = 3;
+    return GPT2_OK;
+}
+
+int gpt2_destroy(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    cudaStreamSynchronize(m->stream);
+    for (auto& p : m->pending) {
+        cudaEventDestroy(p.a);
+        cudaEventDestroy(p.b);
+    }
+    for (auto e : m->pool) cudaEventDestroy(e);
+    delete m;
+    return GPT2_OK;
+}
+
+const char* gpt2_strerror(int s) {
+    switch (s) {
+        case GPT2_OK: return "ok";
+        case GPT2_ERR_ARG: return "invalid argument";
+        case GPT2_ERR_STATE: return "call out of order";
+        case GPT2_ERR_TOKEN_RANGE: return "token or target id out of range";
+        case GPT2_ERR_NONFINITE: return "loss is not finite";
+        case GPT2_ERR_TIMEOUT: return "device wait timed out";
+        case GPT2_ERR_CUDA: return "CUDA runtime error";
+        case GPT2_ERR_WORKSPACE: return "workspace too small or misaligned";
+        default: return "unknown status";
+    }
+}
+
+int gpt2_num_tensors(const gpt2_t* m) { return m ? (int)m->tensors.size() : GPT2_ERR_ARG; }
+
+int gpt2_tensor_info(const gpt2_t* m, int i, const char** name, int64_t shape[2]) {
+    if (!m || i < 0 || i >= (int)m->tensors.size()) return GPT2_ERR_ARG;
+    if (name) *name = m->tensors[i].name.c_str();
+    if (shape) {
+        shape[0] = m->tensors[i].rows;
+        shape[1] = m->tensors[i].cols;
+    }
+    return GPT2_OK;
+}
+
+int gpt2_copy_tensor(gpt2_t* m, int i, int kind, float* host_dst) {
+    if (!m || !host_dst || i < 0 || i >= (int)m->tensors.size()) return GPT2_ERR_ARG;
+    const TensorSpec& s = m->tensors[i];
+    const int64_t n = s.rows * s.cols;
+    const float* src = nullptr;
+    switch (kind) {
+        case GPT2_TENSOR_MASTER: src = m->master; break;
+        case GPT2_TENSOR_GRAD: src = m->grads; break;
+        case GPT2_TENSOR_ADAM_M: src = m->adam_m; break;
+        case GPT2_TENSOR_ADAM_V: src = m->adam_v; break;
+        case GPT2_TENSOR_PARAM:
+            if (m->mode != GPT2_MODE_BF16) {
+                src = m->master;
+                break;
+            } else {
+                std::vector<uint16_t> tmp((size_t)n);
+                if (cudaMemcpyAsync(tmp.data(), (bf16*)m->params + s.offset, (size_t)n * 2, cudaMemcpyDeviceToHost,
+                                    m->stream) != cudaSuccess ||
+                    cudaStreamSynchronize(m->stream) != cudaSuccess)
+                    return GPT2_ERR_CUDA;
+                for (int64_t k = 0; k < n; k++) {
+                    const uint32_t bits = (uint32_t)tmp[(size_t)k] << 16;
+                    std::memcpy(&host_dst[k], &bits, 4);
+                }
+                return GPT2_OK;
+            }
+        default: return GPT2_ERR_ARG;
+    }
+    if (cudaMemcpyAsync(host_dst, src + s.offset, (size_t)n * 4, cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    return cuda_ok(cudaStreamSynchronize(m->stream));
+}
+
+int gpt2_load_tensor(gpt2_t* m, int i, const float* host_src) {
+    if (!m || !host_src || i < 0 || i >= (int)m->tensors.size()) return GPT2_ERR_ARG;
+    const TensorSpec& s = m->tensors[i];
+    const int64_t n = s.rows * s.cols;
+    if (cudaMemcpyAsync(m->master + s.offset, host_src, (size_t)n * 4, cudaMemcpyHostToDevice, m->stream) !=
+        cudaSuccess)
+        return GPT2_ERR_CUDA;
+    TRY(refresh_compute_copy(m, s.offset, n));
+    return cuda_ok(cudaStreamSynchronize(m->stream));
+}
+
+int gpt2_copy_losses(gpt2_t* m, float* host_dst) {
+    if (!m || !host_dst) return GPT2_ERR_ARG;
+    if (m->state < 1) return GPT2_ERR_STATE;
+    if (cudaMemcpyAsync(host_dst, m->losses, (size_t)m->B * m->T * 4, cudaMemcpyDeviceToHost, m->stream) !=
+        cudaSuccess)
+        return GPT2_ERR_CUDA;
+    return cuda_ok(cudaStreamSynchronize(m->stream));
+}
+
+int64_t gpt2_num_params(const gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    int64_t n = 0;
+    for (auto& s : m->tensors) n += s.rows * s.cols;
+    return n;
+}
+
+int64_t gpt2_launch_count(const gpt2_t* m) { return m ? m->launches : GPT2_ERR_ARG; }
+
+int gpt2_family_stats(const gpt2_t* m, int family, int64_t* calls, int64_t* launches, double* work) {
+    if (!m || family < 0 || family >= GPT2_K_COUNT) return GPT2_ERR_ARG;
+    if (calls) *calls = m->fam_calls[family];
+    if (launches) *launches = m->fam_launches[family];
+    if (work) *work = m->fam_work[family];
+    return GPT2_OK;
+}
+
+int gpt2_set_timing(gpt2_t* m, int enable) {
+    if (!m) return GPT2_ERR_ARG;
+    m->timing = enable != 0;
+    return GPT2_OK;
+}
+
+int gpt2_family_time(gpt2_t* m, int family, double* ms) {
+    if (!m || family < 0 || family >= GPT2_K_COUNT || !ms) return GPT2_ERR_ARG;
+    if (cudaStreamSynchronize(m->stream) != cudaSuccess) return GPT2_ERR_CUDA;
+    for (auto& p : m->pending) {
+        float t = 0.f;
+        cudaEventElapsedTime(&t, p.a, p.b);
+        m->fam_ms[p.fam] += t;
+        m->pool.push_back(p.a);
+        m->pool.push_back(p.b);
+    }
+    m->pending.clear();
+    *ms = m->fam_ms[family];
+    return GPT2_OK;
+}
+
+int gpt2_reset_stats(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    if (cudaStreamSynchronize(m->stream) != cudaSuccess) return GPT2_ERR_CUDA;
+    for (auto& p : m->pending) {
+        m->pool.push_back(p.a);
+        m->pool.push_back(p.b);
+    }
+    m->pending.clear();
+    m->launches = 0;
+    for (int f = 0; f < GPT2_K_COUNT; f++) {
+        m->fam_calls[f] = m->fam_launches[f] = 0;
+        m->fam_work[f] = m->fam_ms[f] = 0;
+    }
+    return GPT2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+// C entry points of gpt2_ops.h: argument checks, then the kernel launchers.
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+inline bool dt_ok(int dtype) { return dtype == GPT2_MODE_FP32 || dtype == GPT2_MODE_BF16; }
+inline bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline int finish(int launches) {
+    if (launches < 0) return launches;
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+inline cudaStream_t st(void* s) { return (cudaStream_t)s; }
+
+}  // namespace
+
+extern "C" {
+
+int gpt2_op_encoder_forward(int dtype, void* x0, const int32_t* tokens, const void* wte, const void* wpe, int B,
+                            int T, int C, int V, int* d_status, void* stream) {
+    if (!dt_ok(dtype) || !x0 || !tokens || !wte || !wpe || B < 0 || T < 0 || C <= 0 || C % 8 || V < 1)
+        return GPT2_ERR_ARG;
+    if (!al16(x0) || !al16(wte) || !al16(wpe)) return GPT2_ERR_ARG;
+    if ((int64_t)B * T == 0) return GPT2_OK;
+    return finish(launch_encoder_forward(dtype, x0, tokens, wte, wpe, B, T, C, V, d_status, st(stream)));
+}
+
+size_t gpt2_op_encoder_backward_scratch(int B, int T, int C) {
+    if (B < 0 || T < 0 || C < 0) return 0;
+    return encoder_backward_scratch(B, T, C);
+}
+
+int gpt2_op_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0, const int32_t* tokens, int B,
+                             int T, int C, int Vp, void* scratch, size_t scratch_bytes, void* stream) {
+    if (!dt_ok(dtype) || !dwte || !dwpe || !dx0 || !tokens || B < 0 || T < 0 || C <= 0 || C % 8 || Vp < 1 ||
+        Vp > 65536)
+        return GPT2_ERR_ARG;
+    if ((int64_t)B * T == 0) return GPT2_OK;
+    if (!scratch || scratch_bytes < encoder_backward_scratch(B, T, C)) return GPT2_ERR_WORKSPACE;
+    if (!al16(dwte) || !al16(dwpe) || !al16(dx0)) return GPT2_ERR_ARG;
+    return finish(launch_encoder_backward(dtype, dwte, dwpe, dx0, tokens, B, T, C, scratch, st(stream)));
+}
+
+int gpt2_op_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                              const void* beta, int N, int C, void* stream) {
+    if (!dt_ok(dtype) || !y || !mean || !rstd || !x || !gamma || !beta || N < 0 || C <= 0 || C % 8 || C > 2048)
+        return GPT2_ERR_ARG;
+    if (!al16(y) || !al16(x) || !al16(gamma) || !al16(beta)) return GPT2_ERR_ARG;
+    return finish(launch_layernorm_forward(dtype, y, mean, rstd, x, gamma, beta, N, C, st(stream)));
+}
+
+size_t gpt2_op_layernorm_backward_scratch(int N, int C) {
+    if (N < 0 || C < 0) return 0;
+    return layernorm_backward_scratch(N, C);
+}
+
+int gpt2_op_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                               const void* gamma, const float* mean, const float* rstd, int N, int C, void* scratch,
+                               size_t scratch_bytes, void* stream) {
+    if (!dt_ok(dtype) || !dx || !dgamma || !dbeta || !dy || !x || !gamma || !mean || !rstd || N < 0 || C <= 0 ||
+        C % 8 || C > 2048)
+        return GPT2_ERR_ARG;
+    if (!scratch || scratch_bytes < layernorm_backward_scratch(N, C)) return GPT2_ERR_WORKSPACE;
+    if (!al16(dx) || !al16(dy) || !al16(x) || !al16(gamma)) return GPT2_ERR_ARG;
+    return finish(launch_layernorm_backward(dtype, dx, dgamma, dbeta, dy, x, gamma, mean, rstd, N, C, scratch,
+                                            st(stream)));
+}
+
+size_t gpt2_op_matmul_scratch(int dtype, int M, int N, int K, int d_fp32) {
+    if (!dt_ok(dtype) || M < 0 || N < 0 || K < 0) return 0;
+    return matmul_scratch(dtype, M, N, K, d_fp32);
+}
+
+int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major, const void* B, int b_mn_major,
+                   const void* bias, int M, int N, int K, void* scratch, size_t scratch_bytes, int* d_status,
+                   void* stream) {
+    if (!dt_ok(dtype) || !D || !A || !B || M < 0 || N < 0 || K < 1) return GPT2_ERR_ARG;
+    if (dtype == GPT2_MODE_BF16) {
+        if (K % 8 || N % 8 || (a_mn_major && M % 8)) return GPT2_ERR_ARG;
+        if (!al16(D) || !al16(A) || !al16(B) || (bias && !al16(bias))) return GPT2_ERR_ARG;
+    }
+    if ((int64_t)M * N == 0) return GPT2_OK;
+    const size_t need = matmul_scratch(dtype, M, N, K, d_fp32);
+    if (need && (!scratch || scratch_bytes < need)) return GPT2_ERR_WORKSPACE;
+    return finish(launch_matmul(dtype, D, d_fp32, A, a_mn_major, B, b_mn_major, bias, M, N, K, scratch, d_status,
+                                st(stream)));
+}
+
+int gpt2_op_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
+                              void* stream) {
+    if (!dt_ok(dtype) || !o || !lse || !qkv || B < 0 || T < 0 || C <= 0 || H <= 0 || C % H || C % 8)
+        return GPT2_ERR_ARG;
+    if (!al16(o) || !al16(qkv)) return GPT2_ERR_ARG;
+    return finish(launch_attention_forward(dtype, o, lse, qkv, B, T, C, H, st(stream)));
+}
+
+size_t gpt2_op_attention_backward_scratch(int B, int T, int H) {
+    if (B < 0 || T < 0 || H < 0) return 0;
+    return attention_backward_scratch(B, T, H);
+}
+
+int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* o,
+                               const float* lse, int B, int T, int C, int H, void* scratch, size_t scratch_bytes,
+                               void* stream) {
+    if (!dt_ok(dtype) || !dqkv || !dout || !qkv || !o || !lse || B < 0 || T < 0 || C <= 0 || H <= 0 || C % H ||
+        C % 8)
+        return GPT2_ERR_ARG;
+    if (!scratch || scratch_bytes < attention_backward_scratch(B, T, H)) return GPT2_ERR_WORKSPACE;
+    if (!al16(dqkv) || !al16(dout) || !al16(qkv) || !al16(o)) return GPT2_ERR_ARG;
+    return finish(launch_attention_backward(dtype, dqkv, dout, qkv, o, lse, B, T, C, H, scratch, st(stream)));
+}
+
+int gpt2_op_gelu_forward(int dtype, void* g, const void* u, int64_t n, void* stream) {
+    if (!dt_ok(dtype) || !g || !u || n < 0 || n % 8 || !al16(g) || !al16(u)) return GPT2_ERR_ARG;
+    return finish(launch_gelu_forward(dtype, g, u, n, st(stream)));
+}
+
+int gpt2_op_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, void* stream) {
+    if (!dt_ok(dtype) || !du || !u || !dg || n < 0 || n % 8 || !al16(du) || !al16(u) || !al16(dg))
+        return GPT2_ERR_ARG;
+    return finish(launch_gelu_backward(dtype, du, u, dg, n, st(stream)));
+}
+
+int gpt2_op_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n, void* stream) {
+    if (!dt_ok(dtype) || !out || !a || !b || n < 0 || n % 8 || !al16(out) || !al16(a) || !al16(b))
+        return GPT2_ERR_ARG;
+    return finish(launch_residual_forward(dtype, out, a, b, n, st(stream)));
+}
+
+int gpt2_op_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n, void* stream) {
+    if (!dt_ok(dtype) || !dres || !dbranch || n < 0 || n % 8 || !al16(dres) || !al16(dbranch)) return GPT2_ERR_ARG;
+    return finish(launch_residual_backward(dtype, dres, dbranch, n, st(stream)));
+}
+
+size_t gpt2_op_bias_backward_scratch(int N, int C) {
+    if (N < 0 || C < 0) return 0;
+    return bias_backward_scratch(N, C);
+}
+
+int gpt2_op_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, size_t scratch_bytes,
+                          void* stream) {
+    if (!dt_ok(dtype) || !dbias || !dy || N < 0 || C <= 0 || C % 8 || !al16(dy)) return GPT2_ERR_ARG;
+    if (N == 0) return cudaMemsetAsync(dbias, 0, (size_t)C * 4, st(stream)) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    if (!scratch || scratch_bytes < bias_backward_scratch(N, C)) return GPT2_ERR_WORKSPACE;
+    return finish(launch_bias_backward(dtype, dbias, dy, N, C, scratch, st(stream)));
+}
+
+int gpt2_op_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
+                       float dloss, int* d_status, void* stream) {
+    if (!dt_ok(dtype) || !logits || !losses || !targets || N < 0 || V < 1 || Vp < V || Vp % 8 || !al16(logits))
+        return GPT2_ERR_ARG;
+    return finish(launch_classifier(dtype, logits, losses, targets, N, V, Vp, dloss, d_status, st(stream)));
+}
+
+int gpt2_op_mean_loss(float* out, const float* losses, int N, void* stream) {
+    if (!out || !losses || N < 1) return GPT2_ERR_ARG;
+    return finish(launch_mean_loss(out, losses, N, st(stream)));
+}
+
+int gpt2_op_adamw(float* master, void* param_bf16, const float* grad, float* m, float* v, int64_t n, float lr,
+                  float beta1, float beta2, float eps, float weight_decay, int t, void* stream) {
+    if (!master || !grad || !m || !v || n < 0 || n % 4 || t < 1) return GPT2_ERR_ARG;
+    if (!al16(master) || !al16(grad) || !al16(m) || !al16(v) || (param_bf16 && ((uintptr_t)param_bf16 & 7u)))
+        return GPT2_ERR_ARG;
+    return finish(launch_adamw(master, param_bf16, grad, m, v, n, lr, beta1, beta2, eps, weight_decay, t,
+                               st(stream)));
+}
+
+}  // extern "C"

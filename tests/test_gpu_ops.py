@@ -1,0 +1,350 @@
+"""Per-kernel parity: each CUDA kernel (through the C ABI) against the oracle.
+
+Inputs are seeded and, in bf16 mode, exactly representable in bf16, so both
+sides start from the same values; the oracle computes in float64.
+Tolerances: bf16 outputs carry one round-to-nearest-even (relative 2^-9),
+checked at 2^-8 relative plus a small floor near zero; fp32 outputs at
+1e-5 relative (fp32 accumulation against float64).
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import gpt2_ref as R
+from step_gpt_train_gb300 import data
+from tests._gpu_util import (BF16_REL, assert_close, dev, dev_f32, host, inputs, rel_l2)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    from step_gpt_train_gb300 import gpt2 as g
+    g.load_library(build=True)
+    torch.cuda.set_device(0)
+    return torch
+
+
+def _gemm_ref(A, a_mn, B, b_mn, M, N, K, bias):
+    a = A.reshape(K, M).T if a_mn else A.reshape(M, K)
+    b = B.reshape(K, N).T if b_mn else B.reshape(N, K)
+    d = a.astype(np.float64) @ b.astype(np.float64).T
+    if bias is not None:
+        d = d + bias
+    return d
+
+
+GEMM_CASES = [
+    # M, N, K, a_mn, b_mn, d_fp32, bias
+    (300, 392, 200, 0, 0, 0, True),    # linear forward, ragged M, N (two 256 tiles), K
+    (300, 120, 200, 0, 0, 0, True),    # 128-wide tiles
+    (300, 200, 392, 0, 1, 0, False),   # input gradient dX = dY W
+    (392, 200, 304, 1, 1, 1, False),   # weight gradient dW = dY^T X, fp32 out
+    (128, 256, 4096, 1, 1, 1, False),  # weight gradient with split-K
+    (136, 264, 72, 1, 0, 0, False),    # A M-major, B K-major
+    (520, 1032, 1000, 0, 0, 1, True),  # fp32 out with bias through split-K reduce
+]
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("case", GEMM_CASES)
+def test_matmul(torch_cuda, mode, case):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_matmul
+    M, N, K, a_mn, b_mn, d_fp32, use_bias = case
+    A = inputs(1, (M * K,), 1.0, mode)
+    B = inputs(2, (N * K,), 1.0, mode)
+    bias = inputs(3, (N,), 1.0, mode) if use_bias else None
+    dA, dB = dev(A, mode), dev(B, mode)
+    dbias = dev(bias, mode) if use_bias else None
+    out_dtype = torch.float32 if (d_fp32 or mode == 0) else torch.bfloat16
+    D = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
+    gpt2_op_matmul(D, dA, a_mn, dB, b_mn, M, N, K, bias=dbias)
+    torch.cuda.synchronize()
+    ref = _gemm_ref(A, a_mn, B, b_mn, M, N, K, bias)
+    got = host(D)
+    assert np.all(np.isfinite(got))
+    if out_dtype == torch.bfloat16:
+        assert_close(got, ref, BF16_REL, atol_frac=1e-3, what="bf16 matmul")
+    else:
+        assert_close(got, ref, 1e-5, atol_frac=1e-5, what="fp32 matmul")
+
+
+def test_matmul_full_size_sampled(torch_cuda):
+    """Bench-size GEMMs (GPT-2 124M at B*T = 32768); outputs sampled and computed one by one."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_matmul
+    rng = np.random.default_rng(5)
+    # LM head forward: [32768, 768] x [50304, 768]^T -> bf16 [32768, 50304]
+    M, N, K = 32768, 50304, 768
+    A = dev(inputs(101, (M, K), 1.0))
+    B = dev(inputs(102, (N, K), 0.02))
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    gpt2_op_matmul(D, A, 0, B, 0, M, N, K)
+    torch.cuda.synchronize()
+    ms, ns = rng.integers(0, M, 3000), rng.integers(0, N, 3000)
+    ns[:200] = N - 1 - rng.integers(0, 128, 200)  # the ragged last column tile
+    a, b = host(A[ms]), host(B[ns])
+    ref = np.einsum("ik,ik->i", a, b)
+    got = host(D[ms, ns])
+    assert_close(got, ref, BF16_REL, atol_frac=1e-3, what="LM head sampled")
+    # MLP projection weight gradient: dW = dY^T X, K = 32768, fp32 out (split-K)
+    M, N, K = 768, 3072, 32768
+    dY = dev(inputs(103, (K, M), 1.0))
+    X = dev(inputs(104, (K, N), 1.0))
+    W = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    gpt2_op_matmul(W, dY, 1, X, 1, M, N, K)
+    torch.cuda.synchronize()
+    ms, ns = rng.integers(0, M, 400), rng.integers(0, N, 400)
+    ref = np.einsum("ki,ki->i", host(dY[:, ms]), host(X[:, ns]))
+    assert_close(host(W[ms, ns]), ref, 1e-5, atol_frac=1e-5, what="dW sampled")
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("C", [64, 768, 1600])
+def test_layernorm(torch_cuda, mode, C):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_layernorm_backward, gpt2_op_layernorm_forward
+    N = 333
+    x = inputs(10, (N, C), 2.0, mode) + (inputs(11, (N, 1), 1.0, mode) if mode == 0 else 0)
+    x = data.round_to_bf16(x) if mode == 1 else x
+    g = inputs(12, (C,), 1.0, mode)
+    b = inputs(13, (C,), 1.0, mode)
+    dy = inputs(14, (N, C), 1.0, mode)
+    dx_, dg_, db_ = dev(x, mode), dev(g, mode), dev(b, mode)
+    y = torch.empty_like(dx_)
+    mean = torch.empty(N, device="cuda")
+    rstd = torch.empty(N, device="cuda")
+    gpt2_op_layernorm_forward(y, mean, rstd, dx_, dg_, db_)
+    dx = torch.empty_like(dx_)
+    dgam = torch.full((C,), float("nan"), device="cuda")
+    dbet = torch.full((C,), float("nan"), device="cuda")
+    gpt2_op_layernorm_backward(dx, dgam, dbet, dev(dy, mode), dx_, dg_, mean, rstd)
+    torch.cuda.synchronize()
+    ry, rmean, rrstd = R.layernorm_forward(x.astype(np.float64), g.astype(np.float64), b.astype(np.float64))
+    rdx, rdg, rdb = R.layernorm_backward(dy.astype(np.float64), x.astype(np.float64), g.astype(np.float64),
+                                         rmean, rrstd)
+    tol = BF16_REL if mode == 1 else 1e-5
+    assert_close(host(mean), rmean, 1e-6, atol=1e-6, what="mean")
+    assert_close(host(rstd), rrstd, 1e-5, what="rstd")
+    assert_close(host(y), ry, tol, atol_frac=1e-3 if mode == 1 else 1e-6, what="y")
+    assert_close(host(dx), rdx, 2 * tol, atol_frac=2e-3 if mode == 1 else 1e-6, what="dx")
+    assert_close(host(dgam), rdg, 1e-4, atol_frac=1e-5, what="dgamma")
+    assert_close(host(dbet), rdb, 1e-4, atol_frac=1e-5, what="dbeta")
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+def test_gelu(torch_cuda, mode):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_gelu_backward, gpt2_op_gelu_forward
+    u = np.concatenate([np.linspace(-12, 12, 4000, dtype=np.float32), inputs(20, (4000,), 3.0, 0)])
+    u = data.round_to_bf16(u) if mode == 1 else u
+    dg = inputs(21, u.shape, 1.0, mode)
+    du_, ddg = dev(u, mode), dev(dg, mode)
+    g = torch.empty_like(du_)
+    gpt2_op_gelu_forward(g, du_)
+    dd = torch.empty_like(du_)
+    gpt2_op_gelu_backward(dd, du_, ddg)
+    torch.cuda.synchronize()
+    tol = BF16_REL if mode == 1 else 1e-5
+    rg = R.gelu_forward(u.astype(np.float64))
+    rdu = R.gelu_backward(u.astype(np.float64), dg.astype(np.float64))
+    assert_close(host(g), rg, tol, atol=1e-30, what="gelu")
+    assert_close(host(dd), rdu, tol, atol=1e-6, what="gelu backward")
+    # in place, as the step uses it
+    gpt2_op_gelu_backward(ddg, du_, ddg)
+    torch.cuda.synchronize()
+    assert_close(host(ddg), rdu, tol, atol=1e-6, what="gelu backward in place")
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+def test_residual(torch_cuda, mode):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_residual_backward, gpt2_op_residual_forward
+    a = inputs(30, (1000, 24), 1.0, mode)
+    b = inputs(31, (1000, 24), 1.0, mode)
+    da, db = dev(a, mode), dev(b, mode)
+    out = torch.empty_like(da)
+    gpt2_op_residual_forward(out, da, db)
+    gpt2_op_residual_backward(da, db)  # da += db
+    torch.cuda.synchronize()
+    ref = a.astype(np.float64) + b.astype(np.float64)
+    ref = data.round_to_bf16(ref.astype(np.float32)) if mode == 1 else ref
+    assert_close(host(out), ref, 1e-7 if mode == 1 else 1e-7, what="residual")
+    assert_close(host(da), ref, 1e-7, what="residual backward")
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("C", [200, 3072])
+def test_bias_backward(torch_cuda, mode, C):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_bias_backward
+    dy = inputs(40, (1000, C), 1.0, mode)
+    out = torch.full((C,), float("nan"), device="cuda")
+    gpt2_op_bias_backward(out, dev(dy, mode))
+    torch.cuda.synchronize()
+    assert_close(host(out), dy.astype(np.float64).sum(0), 1e-5, atol=1e-4, what="bias grad")
+
+
+ATT_CASES = [(1, 2, 64, 3), (1, 2, 200, 2), (1, 1, 1024, 2), (0, 2, 64, 4), (0, 3, 37, 4)]
+
+
+@pytest.mark.parametrize("case", ATT_CASES)
+def test_attention(torch_cuda, case):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_attention_backward, gpt2_op_attention_forward
+    mode, B, T, H = case
+    hd = 64 if mode == 1 else 16
+    C = H * hd
+    qkv = inputs(50, (B, T, 3 * C), 1.0, mode)
+    dout = inputs(51, (B, T, C), 1.0, mode)
+    dq = dev(qkv, mode)
+    o = torch.empty(B, T, C, dtype=dq.dtype, device="cuda")
+    lse = torch.empty(B, H, T, device="cuda")
+    gpt2_op_attention_forward(o, lse, dq, B, T, H)
+    dqkv = torch.full_like(dq, float("nan"))
+    gpt2_op_attention_backward(dqkv, dev(dout, mode), dq, o, lse, B, T, H)
+    torch.cuda.synchronize()
+    ro, rlse = R.attention_forward(qkv.astype(np.float64), H)
+    rd = R.attention_backward(dout.astype(np.float64), qkv.astype(np.float64), rlse, H)
+    assert_close(host(lse), rlse, 1e-5, atol=1e-4, what="lse")
+    if mode == 1:
+        assert rel_l2(host(o), ro) < 1e-2
+        assert_close(host(o), ro, 2e-2, atol_frac=3e-2, what="o")
+        for k, part in enumerate("qkv"):
+            sl = slice(k * C, (k + 1) * C)
+            assert rel_l2(host(dqkv)[..., sl], rd[..., sl]) < 2e-2, part
+    else:
+        assert_close(host(o), ro, 1e-4, atol_frac=1e-5, what="o")
+        assert_close(host(dqkv), rd, 1e-4, atol_frac=1e-5, what="dqkv")
+    # deterministic: the backward run again gives identical bits
+    again = torch.full_like(dq, float("nan"))
+    gpt2_op_attention_backward(again, dev(dout, mode), dq, o, lse, B, T, H)
+    torch.cuda.synchronize()
+    assert torch.equal(again, dqkv)
+
+
+CLS_CASES = [(1, 77, 1000, 1024), (0, 77, 1000, 1024), (1, 64, 50257, 50304), (0, 16, 50257, 50304)]
+
+
+@pytest.mark.parametrize("case", CLS_CASES)
+def test_classifier(torch_cuda, case):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_classifier, gpt2_op_mean_loss
+    mode, N, V, Vp = case
+    z = inputs(60, (N, Vp), 2.0, mode)
+    z[:, V:] = 7.0  # padded columns must be ignored
+    tgt = data.token_stream("uniform", N, 61, vocab=V)
+    tgt[0] = V - 1
+    dz = dev(z, mode)
+    losses = torch.empty(N, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpt2_op_classifier(dz, losses, dev(tgt), V, 1.0 / N, status=status)
+    mean = torch.empty(1, device="cuda")
+    gpt2_op_mean_loss(mean, losses)
+    torch.cuda.synchronize()
+    rl, rd = R.classifier(z.astype(np.float64), tgt, V)
+    assert int(status.item()) == 0
+    assert_close(host(losses), rl, 1e-5, atol=2e-5, what="losses")
+    assert abs(float(mean.item()) - rl.mean()) < 1e-5
+    got = host(dz)
+    assert np.all(got[:, V:] == 0.0)
+    tol = BF16_REL if mode == 1 else 1e-5
+    assert_close(got, rd, tol, atol=1e-7 / N, what="dlogits")
+    # a target outside [0, V) is reported, not trapped
+    bad = tgt.copy()
+    bad[3] = V + 5
+    status.zero_()
+    gpt2_op_classifier(dev(z, mode), losses, dev(bad), V, 1.0 / N, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 4
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+def test_encoder_forward(torch_cuda, mode):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_encoder_forward
+    V, C, B, T = (256, 64, 3, 100) if mode == 1 else (50257, 64, 3, 100)
+    wte = inputs(70, (V, C), 0.5, mode)
+    wpe = inputs(71, (T, C), 0.5, mode)
+    wte[:, 0] = np.arange(V)  # integer ids, exact in bf16 up to 256
+    wpe[:, 0] = 0
+    wpe[:, 1] = np.arange(T) if mode == 0 else np.arange(T) % 128
+    wte[:, 1] = 0
+    tok = data.token_stream("uniform" if mode == 1 else "zipf", B * T, 72, vocab=V).reshape(B, T)
+    x0 = torch.empty(B * T, C, dtype=torch.bfloat16 if mode == 1 else torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpt2_op_encoder_forward(x0, dev(tok), dev(wte, mode), dev(wpe, mode), V, status=status)
+    torch.cuda.synchronize()
+    got = host(x0).reshape(B, T, C)
+    assert np.array_equal(got[..., 0].astype(np.int64), tok)  # bit-exact indexing
+    assert np.array_equal(got[..., 1], np.broadcast_to(wpe[:T, 1], (B, T)))
+    ref = R.encoder_forward(wte.astype(np.float64), wpe.astype(np.float64), tok)
+    if mode == 1:
+        ref = data.round_to_bf16(ref.astype(np.float32))
+    assert_close(got, ref, 1e-7, what="x0")
+    assert int(status.item()) == 0
+    tok[1, 5] = V
+    gpt2_op_encoder_forward(x0, dev(tok), dev(wte, mode), dev(wpe, mode), V, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1
+
+
+ENC_BWD_CASES = [(1, "zipf", 4, 300, 768), (0, "zipf", 2, 64, 64), (1, "same", 2, 1024, 128),
+                 (1, "zipf", 32, 1024, 768)]
+
+
+@pytest.mark.parametrize("case", ENC_BWD_CASES)
+def test_encoder_backward(torch_cuda, case):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_encoder_backward
+    mode, kind, B, T, C = case
+    Vp = 50304
+    if kind == "same":
+        tok = np.full((B, T), 7, dtype=np.int32)
+        tok[0, :5] = [3, 7, 7, 9, 7]
+    else:
+        tok = data.token_stream("zipf", B * T, 80).reshape(B, T)
+    dx0 = inputs(81, (B * T, C), 1.0, mode)
+    base = data.normal(82, (Vp, C), 1.0)  # dwte already holds the LM-head part
+    dwte = dev_f32(base)
+    dwpe = torch.full((T, C), float("nan"), device="cuda")
+    dtok = dev(tok)
+    gpt2_op_encoder_backward(dwte, dwpe, dev(dx0, mode), dtok)
+    torch.cuda.synchronize()
+    rwte, rwpe = R.encoder_backward(dx0.astype(np.float64).reshape(B, T, C), tok, Vp, T)
+    assert_close(host(dwpe), rwpe, 1e-5, atol=1e-5, what="dwpe")
+    assert_close(host(dwte), rwte + base, 1e-5, atol=2e-5 * math.sqrt(B * T), what="dwte")
+    # deterministic
+    dwte2 = dev_f32(base)
+    gpt2_op_encoder_backward(dwte2, dwpe, dev(dx0, mode), dtok)
+    torch.cuda.synchronize()
+    assert torch.equal(dwte, dwte2)
+
+
+def test_adamw(torch_cuda):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_adamw
+    n = 40004
+    theta = data.normal(90, (n,), 1.0)
+    m = torch.zeros(n, device="cuda")
+    v = torch.zeros(n, device="cuda")
+    th = dev_f32(theta)
+    pbf = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    rt, rm, rv = theta.astype(np.float64), np.zeros(n), np.zeros(n)
+    hp = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    for t in range(1, 4):
+        g = data.normal(91 + t, (n,), 1.0)
+        g[:10] = 0.0
+        gpt2_op_adamw(th, pbf, dev_f32(g), m, v, t=t, **hp)
+        rt, rm, rv = R.adamw_update(rt, g.astype(np.float64), rm, rv, hp["lr"], hp["beta1"], hp["beta2"],
+                                    hp["eps"], hp["weight_decay"], t)
+    torch.cuda.synchronize()
+    assert_close(host(th), rt, 1e-6, atol=1e-7, what="theta")
+    assert_close(host(m), rm, 1e-5, atol=1e-7, what="m")
+    assert_close(host(v), rv, 1e-5, atol=1e-8, what="v")
+    # the bf16 copy is the round-to-nearest-even of the fp32 master, bit for bit
+    master = th.cpu().numpy()
+    assert np.array_equal(host(pbf), data.round_to_bf16(master).astype(np.float64))

@@ -1,0 +1,291 @@
+"""Whole training step through the C ABI against the CPU oracle.
+
+Acceptance (fp32 mode): loss abs err <= 1e-4, every parameter-gradient tensor
+relative L2 err <= 1e-4. bf16 mode: loss abs err <= 2e-2, per-tensor gradient
+relative L2 err <= 3e-2, updated master weights relative L2 err <= 1e-3 (over
+the whole parameter vector). Token and target indexing is bit-exact, padded
+vocabulary rows stay exactly zero.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import gpt2_ref as R
+from step_gpt_train_gb300 import data
+from tests._gpu_util import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+HP = dict(beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    from step_gpt_train_gb300 import gpt2 as g
+    g.load_library(build=True)
+    torch.cuda.set_device(0)
+    return torch
+
+
+def make_model(cfg, seed=1234):
+    from step_gpt_train_gb300.gpt2 import GPT2
+    return GPT2(cfg, seed)
+
+
+def rcfg(cfg):
+    return R.Config(cfg["n_layer"], cfg["n_embd"], cfg["n_head"], cfg["vocab"], cfg["vocab_padded"], cfg["max_T"])
+
+
+def lr_at(step, warmup):
+    return 3e-4 * min(1.0, step / warmup) if warmup else 3e-4
+
+
+def run_steps(torch, model, tokens, targets, steps, warmup):
+    from step_gpt_train_gb300.gpt2 import TENSOR_GRAD, TENSOR_MASTER
+    losses, grads, masters = [], [], []
+    for s in range(steps):
+        loss = model.forward(torch.from_numpy(tokens[s]).cuda(), torch.from_numpy(targets[s]).cuda())
+        model.backward()
+        grads.append(model.tensors(TENSOR_GRAD))
+        model.adamw_step(lr_at(s + 1, warmup), t=s + 1, **HP)
+        masters.append(model.tensors(TENSOR_MASTER))
+        losses.append(loss)
+    return losses, grads, masters
+
+
+def oracle_steps(cfg, params, tokens, targets, steps, warmup, dtype):
+    c = rcfg(cfg)
+    state = None
+    out = []
+    for s in range(steps):
+        loss, grads, params, state = R.train_step(c, params, tokens[s], targets[s], state, lr_at(s + 1, warmup),
+                                                  HP["beta1"], HP["beta2"], HP["eps"], HP["weight_decay"], s + 1,
+                                                  dtype=dtype)
+        out.append((loss, grads, params))
+    return out
+
+
+def flat(d):
+    return np.concatenate([np.asarray(d[k], dtype=np.float64).reshape(-1) for k in sorted(d)])
+
+
+def check_step(cfg, got_loss, got_grads, got_master, ref, loss_tol, grad_tol, master_tol):
+    ref_loss, ref_grads, ref_params = ref
+    assert abs(got_loss - ref_loss) <= loss_tol, (got_loss, ref_loss)
+    worst = {}
+    for name, g in ref_grads.items():
+        if np.linalg.norm(g) == 0:
+            assert np.all(got_grads[name] == 0), name
+            continue
+        worst[name] = rel_l2(got_grads[name], g)
+    bad = {k: v for k, v in worst.items() if v > grad_tol}
+    assert not bad, sorted(bad.items(), key=lambda kv: -kv[1])[:8]
+    V = cfg["vocab"]
+    assert np.all(got_grads["wte"][V:] == 0) and np.all(got_master["wte"][V:] == 0)
+    err = rel_l2(flat(got_master), flat(ref_params))
+    assert err <= master_tol, err
+    return max(worst.values())
+
+
+TINY = dict(n_layer=2, n_embd=64, n_head=4, vocab=512, vocab_padded=512, max_T=64, max_B=4, mode=0)
+SMALL_BF16 = dict(n_layer=2, n_embd=128, n_head=2, vocab=1000, vocab_padded=1024, max_T=128, max_B=3, mode=1)
+
+
+def test_init_matches_oracle(torch_cuda):
+    """The library's counter-based init equals the oracle's (libm log may differ by 1 ulp in rare draws)."""
+    from step_gpt_train_gb300.gpt2 import TENSOR_MASTER
+    for cfg in (TINY, dict(SMALL_BF16)):
+        model = make_model(cfg)
+        got = model.tensors(TENSOR_MASTER)
+        ref = R.init_params(rcfg(cfg), 1234)
+        assert model.names == [n for n, _, _ in R.param_specs(rcfg(cfg))]
+        for name in ref:
+            a, b = got[name], ref[name]
+            diff = a.view(np.int32).astype(np.int64) - b.view(np.int32).astype(np.int64)
+            assert np.abs(diff).max() <= 1, name
+            assert np.count_nonzero(diff) <= max(2, a.size // 100000), name
+        model.close()
+
+
+def test_fp32_tiny_parity_three_steps(torch_cuda):
+    """The small exact-parity workload (L2 C64 H4 V512 T64 B4, fp32, uniform ids), 3 AdamW steps."""
+    torch = torch_cuda
+    tok, tgt = data.batches("uniform", 4, 64, 3, 1234, vocab=512)
+    model = make_model(TINY)
+    losses, grads, masters = run_steps(torch, model, tok, tgt, 3, warmup=0)
+    ref = oracle_steps(TINY, R.init_params(rcfg(TINY), 1234), tok, tgt, 3, 0, np.float64)
+    for s in range(3):
+        check_step(TINY, losses[s], grads[s], masters[s], ref[s], 1e-4, 1e-4, 1e-4)
+    assert abs(losses[0] - math.log(512)) < 0.05
+    model.close()
+
+
+def test_bf16_small_parity_two_steps(torch_cuda):
+    """bf16, head size 64, a ragged sequence length (T=100 over 64-row tiles)."""
+    torch = torch_cuda
+    cfg = SMALL_BF16
+    tok, tgt = data.batches("zipf", 3, 100, 2, 7, vocab=1000)
+    model = make_model(cfg)
+    losses, grads, masters = run_steps(torch, model, tok, tgt, 2, warmup=5)
+    ref = oracle_steps(cfg, R.init_params(rcfg(cfg), 1234), tok, tgt, 2, 5, np.float64)
+    for s in range(2):
+        check_step(cfg, losses[s], grads[s], masters[s], ref[s], 2e-2, 3e-2, 1e-3)
+    model.close()
+
+
+def test_deterministic(torch_cuda):
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import TENSOR_GRAD
+    tok, tgt = data.batches("zipf", 3, 128, 1, 3, vocab=1000)
+    outs = []
+    for _ in range(2):
+        m = make_model(SMALL_BF16)
+        loss = m.forward(torch.from_numpy(tok[0]).cuda(), torch.from_numpy(tgt[0]).cuda())
+        m.backward()
+        outs.append((loss, m.tensors(TENSOR_GRAD)))
+        m.close()
+    assert outs[0][0] == outs[1][0]
+    for k in outs[0][1]:
+        assert np.array_equal(outs[0][1][k], outs[1][1][k]), k
+
+
+def test_launch_inventory_matches_page_table(torch_cuda):
+    """Per-step op counts for L = 12 equal the kernel table's counts (llm.c "State of the Union")."""
+    torch = torch_cuda
+    facts = json.load(open(os.path.join(GOLDEN, "gpt2_facts.json")))["kernel_launches_per_step_124m"]
+    cfg = dict(n_layer=12, n_embd=768, n_head=12, vocab=50257, vocab_padded=50304, max_T=64, max_B=1, mode=1)
+    model = make_model(cfg)
+    tok, tgt = data.batches("zipf", 1, 64, 1, 5)
+    model.reset_stats()
+    model.forward(torch.from_numpy(tok[0]).cuda(), torch.from_numpy(tgt[0]).cuda())
+    model.backward()
+    model.adamw_step(1e-4, t=1, **HP)
+    st = model.family_stats()
+    for fam in ("matmul", "attention_forward", "attention_backward", "gelu_forward", "gelu_backward",
+                "layernorm_forward", "layernorm_backward", "residual_forward", "bias_backward", "classifier",
+                "adamw", "encoder_forward", "encoder_backward"):
+        assert st[fam]["calls"] == facts[fam], (fam, st[fam]["calls"], facts[fam])
+    assert st["residual_backward"]["calls"] == 24
+    assert model.launch_count() == sum(v["launches"] for v in st.values())
+    model.close()
+
+
+def test_124m_b8_parity(torch_cuda):
+    """GPT-2 124M, bf16, B=8, T=1024, Zipf(1.1) ids: one full step against the fp32 oracle."""
+    torch = torch_cuda
+    w = data.WORKLOADS["124m-b8"]
+    cfg = {k: w[k] for k in ("n_layer", "n_embd", "n_head", "vocab", "vocab_padded", "max_T", "mode")}
+    cfg["max_B"] = 8
+    tok, tgt = data.workload_batches("124m-b8", 1)
+    model = make_model(cfg)
+    losses, grads, masters = run_steps(torch, model, tok, tgt, 1, warmup=5)
+    model.close()
+    params = R.init_params(rcfg(cfg), 1234)
+    ref = oracle_steps(cfg, params, tok, tgt, 1, 5, np.float32)
+    worst = check_step(cfg, losses[0], grads[0], masters[0], ref[0], 2e-2, 3e-2, 1e-3)
+    print(f"124M B8: loss {losses[0]:.5f} vs {ref[0][0]:.5f}; worst grad rel L2 {worst:.3e}")
+
+
+def test_124m_b32_bench_config_sampled(torch_cuda):
+    """The benchmarked workload (124M, B=32, T=1024, Zipf + EoS): per-position losses of
+    sampled sequences against the oracle's forward on those sequences alone."""
+    torch = torch_cuda
+    w = data.WORKLOADS["124m-b32"]
+    cfg = {k: w[k] for k in ("n_layer", "n_embd", "n_head", "vocab", "vocab_padded", "max_T", "mode")}
+    cfg["max_B"] = 32
+    tok, tgt = data.workload_batches("124m-b32", 2)
+    assert (tok == data.GPT2_EOS).any()
+    model = make_model(cfg)
+    loss0 = model.forward(torch.from_numpy(tok[0]).cuda(), torch.from_numpy(tgt[0]).cuda())
+    per_pos = model.losses(32, 1024)
+    model.backward()
+    model.adamw_step(lr_at(1, 5), t=1, **HP)
+    loss1 = model.forward(torch.from_numpy(tok[1]).cuda(), torch.from_numpy(tgt[1]).cuda())
+    model.close()
+    assert abs(float(per_pos.astype(np.float64).mean()) - loss0) < 1e-4
+    assert abs(loss0 - (math.log(50257) + 2e-4 * 768)) < 0.1
+    assert math.isfinite(loss1)
+    params = R.init_params(rcfg(cfg), 1234)
+    c = rcfg(cfg)
+    for b in (0, 17):
+        ref = R.position_losses(c, params, tok[0, b:b + 1], tgt[0, b:b + 1], dtype=np.float32)[0]
+        err = np.abs(per_pos[b] - ref)
+        assert err.max() < 5e-2 and err.mean() < 1e-2, (b, err.max(), err.mean())
+
+
+@pytest.mark.parametrize("name", ["350m-b16", "1p5b-b8"])
+def test_large_models_b1_parity(torch_cuda, name):
+    """350M and 1.5B shapes at B=1, T=1024: one full step against the fp32 oracle."""
+    torch = torch_cuda
+    w = data.WORKLOADS[name]
+    cfg = {k: w[k] for k in ("n_layer", "n_embd", "n_head", "vocab", "vocab_padded", "max_T", "mode")}
+    cfg["max_B"] = 1
+    tok, tgt = data.workload_batches(name, 1, B=1)
+    model = make_model(cfg)
+    losses, grads, masters = run_steps(torch, model, tok, tgt, 1, warmup=5)
+    model.close()
+    ref = oracle_steps(cfg, R.init_params(rcfg(cfg), 1234), tok, tgt, 1, 5, np.float32)
+    worst = check_step(cfg, losses[0], grads[0], masters[0], ref[0], 2e-2, 3e-2, 1e-3)
+    print(f"{name} B1: loss {losses[0]:.5f} vs {ref[0][0]:.5f}; worst grad rel L2 {worst:.3e}")
+
+
+def test_errors_are_reported_not_trapped(torch_cuda):
+    torch = torch_cuda
+    from step_gpt_train_gb300 import gpt2 as g
+    cfg = dict(SMALL_BF16)
+    model = make_model(cfg)
+    tok, tgt = data.batches("zipf", 3, 100, 1, 9, vocab=1000)
+    dt, dg = torch.from_numpy(tok[0]).cuda(), torch.from_numpy(tgt[0]).cuda()
+    with pytest.raises(g.GPT2Error) as e:
+        model.backward()
+    assert e.value.status == -2
+    bad = tok[0].copy()
+    bad[1, 3] = 1000
+    with pytest.raises(g.GPT2Error) as e:
+        model.forward(torch.from_numpy(bad).cuda(), dg)
+    assert e.value.status == -3
+    badt = tgt[0].copy()
+    badt[2, 7] = -1
+    with pytest.raises(g.GPT2Error) as e:
+        model.forward(dt, torch.from_numpy(badt).cuda())
+    assert e.value.status == -3
+    with pytest.raises(g.GPT2Error) as e:
+        model.backward()  # the failed forward does not enable a backward
+    assert e.value.status == -2
+    big = torch.zeros(4, 100, dtype=torch.int32, device="cuda")
+    with pytest.raises(g.GPT2Error) as e:
+        model.forward(big, big)
+    assert e.value.status == -1
+    # the context is still usable: a normal step runs
+    loss = model.forward(dt, dg)
+    assert math.isfinite(loss)
+    with pytest.raises(g.GPT2Error) as e:
+        model.adamw_step(1e-4, t=1, **HP)  # no backward yet
+    assert e.value.status == -2
+    model.backward()
+    with pytest.raises(g.GPT2Error) as e:
+        model.adamw_step(1e-4, t=0, **HP)
+    assert e.value.status == -1
+    model.adamw_step(1e-4, t=1, **HP)
+    with pytest.raises(g.GPT2Error) as e:
+        model.adamw_step(1e-4, t=2, **HP)  # one update per backward
+    assert e.value.status == -2
+    model.close()
+    bad_cfg = g.make_config(2, 128, 4, 1000, 1024, 128, 3, 1)  # head size 32 in bf16 mode
+    with pytest.raises(g.GPT2Error):
+        g.gpt2_workspace_bytes(bad_cfg)
+    good = g.make_config(2, 128, 2, 1000, 1024, 128, 3, 1)
+    need = g.gpt2_workspace_bytes(good)
+    ws = torch.empty(need + 2048, dtype=torch.uint8, device="cuda")
+    base = (ws.data_ptr() + 1023) // 1024 * 1024
+    with pytest.raises(g.GPT2Error) as e:
+        g.gpt2_init(good, 1, base, need - 1, torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == -7
+    with pytest.raises(g.GPT2Error) as e:
+        g.gpt2_init(good, 1, base + 256, need, torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == -7
