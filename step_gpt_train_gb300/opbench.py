@@ -1,0 +1,232 @@
+"""Per-kernel micro-benchmark of the GPT-2 step's ops at a model's shapes.
+
+Each op runs through its C entry point (gpt2_ops.h) on device buffers,
+timed with CUDA events on the launching stream after warm-up, and is
+reported against its roofline: algorithmic FLOPs against the measured bf16
+peak for the matmuls and attention, algorithmic bytes against the measured
+HBM bandwidth for the rest. Also the small, self-contained program for ncu
+captures of one kernel.
+
+  python -m step_gpt_train_gb300.opbench [--ops a,b] [--iters N] [--B 32 --T 1024 --C 768 --H 12]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--ops", default="all")
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--B", type=int, default=32)
+    ap.add_argument("--T", type=int, default=1024)
+    ap.add_argument("--C", type=int, default=768)
+    ap.add_argument("--H", type=int, default=12)
+    ap.add_argument("--V", type=int, default=50257)
+    ap.add_argument("--Vp", type=int, default=50304)
+    args = ap.parse_args(argv)
+
+    import torch
+    from step_gpt_train_gb300 import gpt2 as g
+
+    g.load_library(build=True)
+    torch.cuda.set_device(0)
+    hbm, tc, src = peaks()
+    B, T, C, H, V, Vp = args.B, args.T, args.C, args.H, args.V, args.Vp
+    N = B * T
+    bf = torch.bfloat16
+    dev = "cuda"
+
+    def rnd(*shape, dtype=bf, std=1.0):
+        return (torch.randn(*shape, device=dev) * std).to(dtype)
+
+    ops = {}
+
+    def gemm_op(M, Nn, K, a_mn, b_mn, fp32_out, bias):
+        def setup():
+            A = rnd(M * K)
+            Bm = rnd(Nn * K, std=0.02)
+            D = torch.empty(M, Nn, device=dev, dtype=torch.float32 if fp32_out else bf)
+            b = rnd(Nn) if bias else None
+            sc = torch.empty(max(256, g.load_library().gpt2_op_matmul_scratch(1, M, Nn, K, int(fp32_out))),
+                             dtype=torch.uint8, device=dev)
+            lib = g.load_library()
+
+            def run():
+                g.check(lib.gpt2_op_matmul(1, D.data_ptr(), int(fp32_out), A.data_ptr(), a_mn, Bm.data_ptr(),
+                                           b_mn, b.data_ptr() if b is not None else None, M, Nn, K,
+                                           sc.data_ptr(), sc.numel(), None, torch.cuda.current_stream().cuda_stream))
+            return run
+        return setup, 2.0 * M * Nn * K, "flop"
+
+    shapes = {"qkv": (3 * C, C), "proj": (C, C), "fc": (4 * C, C), "fcproj": (C, 4 * C), "lmhead": (Vp, C)}
+    for name, (out, inp) in shapes.items():
+        ops[f"gemm_{name}_fwd"] = gemm_op(N, out, inp, 0, 0, False, name != "lmhead")
+        ops[f"gemm_{name}_dx"] = gemm_op(N, inp, out, 0, 1, False, False)
+        ops[f"gemm_{name}_dw"] = gemm_op(out, inp, N, 1, 1, True, False)
+
+    def attn_fwd():
+        qkv = rnd(N, 3 * C)
+        o = torch.empty(N, C, device=dev, dtype=bf)
+        lse = torch.empty(B * H * T, device=dev)
+        return lambda: g.gpt2_op_attention_forward(o, lse, qkv, B, T, H)
+
+    def attn_bwd():
+        qkv = rnd(N, 3 * C)
+        o = torch.empty(N, C, device=dev, dtype=bf)
+        lse = torch.empty(B * H * T, device=dev)
+        g.gpt2_op_attention_forward(o, lse, qkv, B, T, H)
+        do = rnd(N, C)
+        dq = torch.empty_like(qkv)
+        sc = torch.empty(B * H * T * 4, dtype=torch.uint8, device=dev)
+        lib = g.load_library()
+        return lambda: g.check(lib.gpt2_op_attention_backward(1, dq.data_ptr(), do.data_ptr(), qkv.data_ptr(),
+                                                              o.data_ptr(), lse.data_ptr(), B, T, C, H,
+                                                              sc.data_ptr(), sc.numel(),
+                                                              torch.cuda.current_stream().cuda_stream))
+
+    att_flops = 4.0 * B * C * T * (T + 1) / 2
+    ops["attention_fwd"] = (attn_fwd, att_flops, "flop")
+    ops["attention_bwd"] = (attn_bwd, 2.5 * att_flops, "flop")
+
+    def ln_fwd():
+        x, gm, bt = rnd(N, C), rnd(C), rnd(C)
+        y = torch.empty_like(x)
+        mean, rstd = torch.empty(N, device=dev), torch.empty(N, device=dev)
+        return lambda: g.gpt2_op_layernorm_forward(y, mean, rstd, x, gm, bt)
+
+    def ln_bwd():
+        x, gm, bt, dy = rnd(N, C), rnd(C), rnd(C), rnd(N, C)
+        y = torch.empty_like(x)
+        mean, rstd = torch.empty(N, device=dev), torch.empty(N, device=dev)
+        g.gpt2_op_layernorm_forward(y, mean, rstd, x, gm, bt)
+        dx = torch.empty_like(x)
+        dgm, dbt = torch.empty(C, device=dev), torch.empty(C, device=dev)
+        lib = g.load_library()
+        sc = torch.empty(lib.gpt2_op_layernorm_backward_scratch(N, C), dtype=torch.uint8, device=dev)
+        return lambda: g.check(lib.gpt2_op_layernorm_backward(1, dx.data_ptr(), dgm.data_ptr(), dbt.data_ptr(),
+                                                              dy.data_ptr(), x.data_ptr(), gm.data_ptr(),
+                                                              mean.data_ptr(), rstd.data_ptr(), N, C,
+                                                              sc.data_ptr(), sc.numel(),
+                                                              torch.cuda.current_stream().cuda_stream))
+
+    ops["layernorm_fwd"] = (ln_fwd, N * (2.0 * C * 2 + 8), "byte")
+    ops["layernorm_bwd"] = (ln_bwd, N * (3.0 * C * 2 + 8), "byte")
+
+    def gelu_fwd():
+        u = rnd(N * 4 * C)
+        out = torch.empty_like(u)
+        return lambda: g.gpt2_op_gelu_forward(out, u)
+
+    def gelu_bwd():
+        u, dgr = rnd(N * 4 * C), rnd(N * 4 * C)
+        return lambda: g.gpt2_op_gelu_backward(dgr, u, dgr)
+
+    ops["gelu_fwd"] = (gelu_fwd, N * 4.0 * C * 4, "byte")
+    ops["gelu_bwd"] = (gelu_bwd, N * 4.0 * C * 6, "byte")
+
+    def residual():
+        a, b_ = rnd(N * C), rnd(N * C)
+        out = torch.empty_like(a)
+        return lambda: g.gpt2_op_residual_forward(out, a, b_)
+
+    ops["residual_fwd"] = (residual, N * C * 6.0, "byte")
+
+    def bias_bwd(cols):
+        def setup():
+            dy = rnd(N, cols)
+            db = torch.empty(cols, device=dev)
+            lib = g.load_library()
+            sc = torch.empty(lib.gpt2_op_bias_backward_scratch(N, cols), dtype=torch.uint8, device=dev)
+            return lambda: g.check(lib.gpt2_op_bias_backward(1, db.data_ptr(), dy.data_ptr(), N, cols,
+                                                             sc.data_ptr(), sc.numel(),
+                                                             torch.cuda.current_stream().cuda_stream))
+        return setup
+
+    ops["bias_bwd_fc"] = (bias_bwd(4 * C), N * 4.0 * C * 2, "byte")
+    ops["bias_bwd_proj"] = (bias_bwd(C), N * C * 2.0, "byte")
+
+    def classifier():
+        z = rnd(N, Vp, std=2.0)
+        z0 = z.clone()
+        losses = torch.empty(N, device=dev)
+        tgt = torch.randint(0, V, (N,), device=dev, dtype=torch.int32)
+
+        def run():
+            g.gpt2_op_classifier(z, losses, tgt, V, 1.0 / N)
+        return run
+
+    ops["classifier"] = (classifier, N * (2.0 * Vp * 2 + 8), "byte")
+
+    def adamw():
+        n = 124_475_904
+        th, gr, m, v = (torch.randn(n, device=dev) for _ in range(4))
+        v.abs_()
+        pb = torch.empty(n, dtype=bf, device=dev)
+        return lambda: g.gpt2_op_adamw(th, pb, gr, m, v, 1e-9, 0.9, 0.95, 1e-8, 0.0, 1)
+
+    ops["adamw"] = (adamw, 124_475_904 * 30.0, "byte")
+
+    def enc_fwd():
+        tok = torch.randint(0, V, (B, T), device=dev, dtype=torch.int32)
+        wte, wpe = rnd(Vp, C), rnd(T, C)
+        x0 = torch.empty(N, C, device=dev, dtype=bf)
+        return lambda: g.gpt2_op_encoder_forward(x0, tok, wte, wpe, V)
+
+    def enc_bwd():
+        from step_gpt_train_gb300 import data
+        tok = torch.from_numpy(data.token_stream("zipf", N, 3).reshape(B, T)).cuda()
+        dx0 = rnd(N, C)
+        dwte, dwpe = torch.zeros(Vp, C, device=dev), torch.zeros(T, C, device=dev)
+        lib = g.load_library()
+        sc = torch.empty(lib.gpt2_op_encoder_backward_scratch(B, T, C), dtype=torch.uint8, device=dev)
+        return lambda: g.check(lib.gpt2_op_encoder_backward(1, dwte.data_ptr(), dwpe.data_ptr(), dx0.data_ptr(),
+                                                            tok.data_ptr(), B, T, C, Vp, sc.data_ptr(), sc.numel(),
+                                                            torch.cuda.current_stream().cuda_stream))
+
+    ops["encoder_fwd"] = (enc_fwd, N * (3.0 * C * 2 + 4), "byte")
+    ops["encoder_bwd"] = (enc_bwd, N * (C * 2 * 2.0 + 8) + T * C * 4.0, "byte")
+
+    names = list(ops) if args.ops == "all" else args.ops.split(",")
+    for name in names:
+        setup, work, kind = ops[name]
+        run = setup()
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.iters):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / args.iters
+        if kind == "flop":
+            achieved = work / (us * 1e-6) / 1e12
+            rec = {"op": name, "us": us, "tflops": achieved, "frac_of_bf16_peak": achieved / tc}
+        else:
+            achieved = work / (us * 1e-6) / 1e9
+            rec = {"op": name, "us": us, "gbs": achieved, "frac_of_hbm": achieved / hbm}
+        rec["peaks"] = src
+        print(json.dumps(rec), flush=True)
+        del run
+        torch.cuda.empty_cache()
+
+
+if __name__ == "__main__":
+    main()

@@ -151,7 +151,9 @@ def test_gelu(torch_cuda, mode):
     tol = BF16_REL if mode == 1 else 1e-5
     rg = R.gelu_forward(u.astype(np.float64))
     rdu = R.gelu_backward(u.astype(np.float64), dg.astype(np.float64))
-    assert_close(host(g), rg, tol, atol=1e-30, what="gelu")
+    # The float64 oracle evaluates the tanh form, whose 1 + tanh(y) cancels on the
+    # negative tail: its absolute error there is about |u| * 1e-16, hence the floor.
+    assert_close(host(g), rg, tol, atol=2e-15, what="gelu")
     assert_close(host(dd), rdu, tol, atol=1e-6, what="gelu backward")
     # in place, as the step uses it
     gpt2_op_gelu_backward(ddg, du_, ddg)
