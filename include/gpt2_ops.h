@@ -128,6 +128,29 @@ size_t gpt2_op_bias_backward_scratch(int N, int C);
 int gpt2_op_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch,
                           size_t scratch_bytes, void* stream);
 
+/* Bias gradient without caller scratch. The paper has no counterpart to
+ * this entry point: it serves callers that cannot allocate or lend device
+ * memory (for example a program whose device memory is wholly owned by
+ * another runtime's allocator or a fixed pool, or code that must not call
+ * cudaMalloc because it can synchronise the device). It computes exactly
+ * what gpt2_op_bias_backward computes, dbias[c] = sum_rows dy[r, c] (fp32,
+ * overwritten), but its partial sums go to a fixed 4 MiB array inside the
+ * library instead of caller scratch. It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   - Limit: ceil(N/128) * C <= 1,048,576 (e.g. N = 32768 rows with
+ *     C <= 4096). Larger sizes return GPT2_ERR_WORKSPACE and launch nothing.
+ *   - The array is held by every GPU that loads the library until the
+ *     process exits. The first call on each device looks up its device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array. Calls that overlap on the GPU (on
+ *     different streams, or from several threads) race and give wrong
+ *     results; order them on one stream. Nothing in the array needs to
+ *     start at zero: each call writes every partial it reads.
+ * Arguments as gpt2_op_bias_backward, without the scratch. */
+int gpt2_op_bias_backward_noalloc(int dtype, float* dbias, const void* dy, int N, int C,
+                                  void* stream);
+
 /* Fused classifier ("fused_classifier", section "Single GPU training" and
  * "Fine print"): per row i of logits [N, Vp] (dtype), over columns j < V only:
  * lse_i = log sum exp z_ij, losses[i] = lse_i - z_i,targets[i] (fp32), and in

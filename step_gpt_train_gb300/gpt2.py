@@ -91,6 +91,7 @@ _SIGNATURES = {
     "gpt2_op_residual_backward": (c_int, [c_int, c_void_p, c_void_p, c_int64, c_void_p]),
     "gpt2_op_bias_backward_scratch": (c_size_t, [c_int, c_int]),
     "gpt2_op_bias_backward": (c_int, [c_int, c_void_p, c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "gpt2_op_bias_backward_noalloc": (c_int, [c_int, c_void_p, c_void_p, c_int, c_int, c_void_p]),
     "gpt2_op_classifier": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p,
                                    c_void_p]),
     "gpt2_op_mean_loss": (c_int, [c_void_p, c_void_p, c_int, c_void_p]),
@@ -378,6 +379,13 @@ def gpt2_op_bias_backward(dbias, dy, stream=None):
     check(lib.gpt2_op_bias_backward(_dtype_of(dy), _p(dbias), _p(dy), N, C, _p(sc), sc.numel(), _s(stream)),
           "gpt2_op_bias_backward")
     return sc
+
+
+def gpt2_op_bias_backward_noalloc(dbias, dy, stream=None):
+    """Bias gradient with the library's fixed internal scratch (no caller scratch)."""
+    N, C = dy.shape
+    check(load_library().gpt2_op_bias_backward_noalloc(_dtype_of(dy), _p(dbias), _p(dy), N, C, _s(stream)),
+          "gpt2_op_bias_backward_noalloc")
 
 
 def gpt2_op_classifier(logits, losses, targets, V, dloss, status=None, stream=None):
