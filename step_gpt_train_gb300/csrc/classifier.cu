@@ -77,20 +77,23 @@ __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, 
         if (threadIdx.x == 0) set_status(status, GPT2_FLAG_TARGET_RANGE);
         tgt = 0;
     }
-    // max over the real columns
+    // Only the vector that straddles V (and vectors past it) need a column
+    // test; every other vector is handled without per-element checks.
+    const int full_nv = V / 8;  // vectors wholly inside the real vocabulary
     float m = -FLT_MAX;
-    float zt = 0.f;
 #pragma unroll
     for (int i = 0; i < VPT; i++) {
         const int idx = threadIdx.x + i * NT;
         if (idx < nv) {
             float f[8];
             raw_unpack(cache[i], f);
+            if (idx < full_nv) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int col = idx * 8 + j;
-                if (col < V) m = fmaxf(m, f[j]);
-                if (col == tgt) zt = f[j];
+                for (int j = 0; j < 8; j++) m = fmaxf(m, f[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (idx * 8 + j < V) m = fmaxf(m, f[j]);
             }
         }
     }
@@ -102,27 +105,46 @@ __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, 
         if (idx < nv) {
             float f[8];
             raw_unpack(cache[i], f);
+            if (idx < full_nv) {
 #pragma unroll
-            for (int j = 0; j < 8; j++)
-                if (idx * 8 + j < V) s += exp_shift<T>(f[j], m);
+                for (int j = 0; j < 8; j++) s += exp_shift<T>(f[j], m);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (idx * 8 + j < V) s += exp_shift<T>(f[j], m);
+            }
         }
     }
     s = block_reduce<NT>(s, false, sh);
     const float scale = dloss / s;
-    // the thread holding the target column reports the loss: lse - z_t
-    if (((tgt / 8) % NT) == (int)threadIdx.x) losses[row] = m + logf(s) - zt;
+    const int tvec = tgt / 8;
 #pragma unroll
     for (int i = 0; i < VPT; i++) {
         const int idx = threadIdx.x + i * NT;
         if (idx < nv) {
             float f[8];
             raw_unpack(cache[i], f);
+            if (idx == tvec) {
+                // the thread holding the target column reports the loss: lse - z_t
+                const int jt = tgt % 8;
+                float zt = f[0];
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int col = idx * 8 + j;
-                float d = col < V ? exp_shift<T>(f[j], m) * scale : 0.f;
-                if (col == tgt) d -= dloss;
-                f[j] = d;
+                for (int j = 1; j < 8; j++)
+                    if (j == jt) zt = f[j];
+                losses[row] = m + logf(s) - zt;
+            }
+            if (idx < full_nv) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) f[j] = exp_shift<T>(f[j], m) * scale;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++) f[j] = idx * 8 + j < V ? exp_shift<T>(f[j], m) * scale : 0.f;
+            }
+            if (idx == tvec) {
+                const int jt = tgt % 8;
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (j == jt) f[j] -= dloss;
             }
             store8(z + idx * 8, f);
         }

@@ -444,9 +444,10 @@ __global__ void __launch_bounds__(256) bias_partial_kernel(float* __restrict__ p
     const int r1 = min(N, r0 + BIAS_ROWS_PER_CHUNK);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (c < C) {
+#pragma unroll 4
         for (int r = r0 + ty; r < r1; r += 8) {
             float v[8];
-            load8(dy + (int64_t)r * C + c, v);
+            load8_stream(dy + (int64_t)r * C + c, v);
 #pragma unroll
             for (int j = 0; j < 8; j++) acc[j] += v[j];
         }
@@ -464,12 +465,34 @@ __global__ void __launch_bounds__(256) bias_partial_kernel(float* __restrict__ p
     }
 }
 
-__global__ void bias_reduce_kernel(float* __restrict__ dbias, const float* __restrict__ partial, int chunks, int C) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
+// Deterministic column sums of an fp32 [R, ncols] matrix (row stride ncols):
+// out[c] = sum over r of in[r][c], r in ascending order within each of 32
+// row lanes, then the 32 lane sums in lane order. Block = 32 columns x 32 row
+// lanes; a warp reads 32 consecutive floats of one row (coalesced). Columns
+// c >= split go to out2[c - split] (two outputs that share one pass).
+__global__ void __launch_bounds__(1024) colsum_kernel(float* __restrict__ out, float* __restrict__ out2,
+                                                      int split, const float* __restrict__ in, int R, int ncols) {
+    __shared__ float sm[32][33];
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+    const int c = blockIdx.x * 32 + tx;
     float s = 0.f;
-    for (int k = 0; k < chunks; k++) s += partial[(int64_t)k * C + c];
-    dbias[c] = s;
+    if (c < ncols) {
+#pragma unroll 4
+        for (int r = ty; r < R; r += 32) s += in[(int64_t)r * ncols + c];
+    }
+    sm[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && c < ncols) {
+        float t = 0.f;
+        for (int k = 0; k < 32; k++) t += sm[k][tx];
+        if (c < split) out[c] = t;
+        else out2[c - split] = t;
+    }
+}
+
+int launch_colsum(float* out, float* out2, int split, const float* in, int R, int ncols, cudaStream_t s) {
+    colsum_kernel<<<(ncols + 31) / 32, 1024, 0, s>>>(out, out2, split, in, R, ncols);
+    return 1;
 }
 
 size_t bias_backward_scratch(int N, int C) {
@@ -484,7 +507,7 @@ int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, 
         bias_partial_kernel<bf16><<<grid, 256, 0, s>>>((float*)scratch, (const bf16*)dy, N, C);
     else
         bias_partial_kernel<float><<<grid, 256, 0, s>>>((float*)scratch, (const float*)dy, N, C);
-    bias_reduce_kernel<<<(C + 255) / 256, 256, 0, s>>>(dbias, (const float*)scratch, chunks, C);
+    launch_colsum(dbias, nullptr, C, (const float*)scratch, chunks, C, s);
     return 2;
 }
 

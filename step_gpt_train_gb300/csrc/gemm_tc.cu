@@ -6,15 +6,22 @@
 // input gradients dX = dY W (B = W read MN-major) and the weight gradients
 // dW = dY^T X (both operands MN-major, fp32 output, long K = B*T, split-K).
 //
-// Structure: a persistent kernel, one CTA per SM, 6 warps.
+// Structure: a persistent kernel, one CTA per SM, 10 warps.
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
 //               into a ring of shared-memory stages, completion on mbarriers.
 //   warp 1      allocates TMEM (two BN-column fp32 accumulators) and one
 //               thread issues tcgen05.mma (M=128, N=BN, K=16) from shared-
 //               memory descriptors; tcgen05.commit frees each stage and
 //               signals a finished accumulator.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32*(w%4)..+31 = tile rows), + bias, convert, store.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31 = tile rows; two warps per lane quarter,
+//               each owning half of the tile's columns), + bias (each warp
+//               stages its own slice in shared memory once per tile, so only
+//               warp-level syncs are needed), convert, then each 32-row chunk
+//               goes through a 2 KB swizzled shared-memory buffer to a TMA
+//               bulk-tensor store (coalesced, asynchronous; TMA clips rows and
+//               columns outside the matrix). The next chunk's TMEM load is in
+//               flight while the current one is stored.
 // Two accumulators let the epilogue of one tile overlap the MMAs of the next.
 // Every mbarrier wait is bounded: on timeout the kernel sets a status bit,
 // stops, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
@@ -29,8 +36,9 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;               // 64 bf16 = 128 bytes = one swizzle row
-constexpr int NUM_THREADS = 192;     // 6 warps
+constexpr int NUM_THREADS = 320;     // 10 warps
 constexpr int EPI_WARP0 = 2;
+constexpr int EPI_WARPS = 8;
 
 template <int BN> struct TileCfg {
     static constexpr int STAGES = BN == 256 ? 4 : 6;
@@ -38,7 +46,11 @@ template <int BN> struct TileCfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int OUT_STAGE_BYTES = 2048;                        // per epilogue warp: 32 rows x 64 B
+    static constexpr int OUT_BYTES = EPI_WARPS * OUT_STAGE_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int BIAS_BYTES = EPI_WARPS * (BN / 2) * 4;         // per warp: its half of the tile (fp32)
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 /*align*/ + BAR_BYTES + BIAS_BYTES;
 };
 
 struct GemmArgs {
@@ -130,9 +142,9 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
-// 32 consecutive fp32 columns of the accumulator for this thread's lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// Issue a load of 32 consecutive fp32 accumulator columns of this thread's
+// TMEM lane; the registers are valid only after tc_ld_wait on them.
+__device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -142,9 +154,78 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Wait for this thread's outstanding TMEM loads. The registers are listed as
+// read-write operands so that no use of them is scheduled before the wait.
+__device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// TMA store of a [1, 32, box_x] box from shared memory (3-D map: columns,
+// rows, split), tracked by this thread's bulk-async group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Write 16 bytes (chunk q of 4) of this lane's 64-byte row into a buffer laid
+// out with the 64-byte swizzle: 16-byte chunk q of row r sits at chunk
+// position q ^ ((r >> 1) & 3), so the 32 lanes of a warp spread over all banks.
+__device__ __forceinline__ void stage16(uint8_t* buf, int row, int q, uint4 v) {
+    *reinterpret_cast<uint4*>(buf + row * 64 + ((q ^ ((row >> 1) & 3)) << 4)) = v;
+}
+
+// One 32-column chunk of this warp's 32 rows: + bias, convert, stage, TMA store.
+// fp32 output goes out as two 16-column halves. ncols_valid = columns of the
+// chunk inside the matrix (> 0).
+__device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
+                                          uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD, int x,
+                                          int y, int z, int ncols_valid, int lane) {
+    float f[32];
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    for (int j = 0; j < 32; j++) f[j] = __uint_as_float(r[j]) + (bias_s ? bias_s[j] : 0.f);
+    if (!fp32_out) {
+        if (lane == 0) bulk_wait_read_all();  // the buffer's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint4 v;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[q * 8 + 2 * i], f[q * 8 + 2 * i + 1]);
+            stage16(stage, lane, q, v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tma_store_3d(mapD, stage_addr, x, y, z);
+    } else {
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            if (hh * 16 >= ncols_valid) break;  // uniform across the warp
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                stage16(stage, lane, q,
+                        make_uint4(__float_as_uint(f[hh * 16 + q * 4]), __float_as_uint(f[hh * 16 + q * 4 + 1]),
+                                   __float_as_uint(f[hh * 16 + q * 4 + 2]), __float_as_uint(f[hh * 16 + q * 4 + 3])));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tma_store_3d(mapD, stage_addr, x + hh * 16, y, z);
+        }
+    }
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
@@ -177,7 +258,8 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool 
 
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, GemmArgs g) {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -187,8 +269,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t a_stage0 = base;
     const uint32_t b_stage0 = base + S * Cfg::A_BYTES;
-    uint8_t* bar_area = gbase + S * Cfg::STAGE_BYTES;
-    const uint32_t bars = base + S * Cfg::STAGE_BYTES;
+    uint8_t* out_stage = gbase + S * Cfg::STAGE_BYTES;  // [EPI_WARPS][2 KB], 1024-aligned
+    uint8_t* bar_area = out_stage + Cfg::OUT_BYTES;
+    const uint32_t bars = base + S * Cfg::STAGE_BYTES + Cfg::OUT_BYTES;
     // barrier layout: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
@@ -207,7 +290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -326,63 +409,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_drain(drain_bar, 0, g.status);
         }
     } else {
-        // ---------------------------------------------------- epilogue (warps 2..5)
-        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        // ---------------------------------------------------- epilogue (warps 2..9)
+        const int ew = warp - EPI_WARP0;         // 0..7
+        const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
+        const int half = ew >> 2;                // which half of the tile's columns
+        constexpr int CHUNKS = BN / 64;          // 32-column chunks per warp
         const int row_in_tile = quad * 32 + lane;
+        // this warp's bias slice [BN/2 columns] and output staging buffer
+        float* bias_s = reinterpret_cast<float*>(bar_area + Cfg::BAR_BYTES) + ew * (BN / 2);
+        uint8_t* stage = out_stage + ew * Cfg::OUT_STAGE_BYTES;
+        const uint32_t stage_addr = smem_addr(stage);
+        const bool use_bias = g.bias != nullptr && g.splits == 1;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
             const int split = u % g.splits;
             const int tile = u / g.splits;
             const int m0 = (tile / g.n_tiles) * BM, n0 = (tile % g.n_tiles) * BN;
+            const int cfirst = half * CHUNKS;
+            if (use_bias) {
+                // the bias of this warp's half of the tile; the buffer's only
+                // reader is this same warp, done with the previous tile
+                const bf16* bp = reinterpret_cast<const bf16*>(g.bias);
+                const int nb = n0 + cfirst * 32;
+                __syncwarp();
+                for (int i = lane; i < BN / 2; i += 32) bias_s[i] = nb + i < g.N ? __bfloat162float(bp[nb + i]) : 0.f;
+                __syncwarp();
+            }
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, g.status)) break;
             tc_fence_after();
-            const int m = m0 + row_in_tile;
-            const bool row_ok = m < g.M;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; c++) {
-                const int n = n0 + c * 32;
-                if (n >= g.N) break;  // uniform across the warp
-                float v[32];
-                tc_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
-                if (!row_ok) continue;
-                if (g.splits > 1) {
-                    float* dst = g.partial + ((size_t)split * g.M + m) * g.N + n;
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+            const int y = m0 + quad * 32;
+            int nchunks = 0;  // chunks of this warp with a valid row and column (uniform across the warp)
+            if (y < g.M) {
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        if (n + q * 8 < g.N) {
-                            float f[8];
-#pragma unroll
-                            for (int j = 0; j < 8; j++) f[j] = v[q * 8 + j];
-                            store8(dst + q * 8, f);
-                        }
-                    }
-                } else {
-                    if (g.bias) {
-                        const bf16* bp = reinterpret_cast<const bf16*>(g.bias) + n;
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            if (n + q * 8 < g.N) {
-                                float bb[8];
-                                load8(bp + q * 8, bb);
-#pragma unroll
-                                for (int j = 0; j < 8; j++) v[q * 8 + j] += bb[j];
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        if (n + q * 8 < g.N) {
-                            float f[8];
-#pragma unroll
-                            for (int j = 0; j < 8; j++) f[j] = v[q * 8 + j];
-                            if (g.d_fp32)
-                                store8(reinterpret_cast<float*>(g.D) + (size_t)m * g.N + n + q * 8, f);
-                            else
-                                store8(reinterpret_cast<bf16*>(g.D) + (size_t)m * g.N + n + q * 8, f);
-                        }
-                    }
-                }
+                for (int c = 0; c < CHUNKS; c++)
+                    if (n0 + (cfirst + c) * 32 < g.N) nchunks = c + 1;
+            }
+            const bool fp32_out = g.splits > 1 || g.d_fp32 != 0;
+            const int z = g.splits > 1 ? split : 0;
+            auto xcol = [&](int c) { return n0 + (cfirst + c) * 32; };
+            auto bias_at = [&](int c) -> const float* { return use_bias ? bias_s + c * 32 : nullptr; };
+            uint32_t ra[32], rb[32];
+            if (nchunks > 0) {
+                tc_ld32_issue(tbase + (uint32_t)(cfirst * 32), ra);
+                tc_ld_wait(ra);
+            }
+            for (int c = 0; c < nchunks; c += 2) {
+                // ra holds chunk c; chunk c+1 is loaded into rb while ra is stored
+                const bool more = c + 1 < nchunks;
+                if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
+                epi_chunk(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, xcol(c), y, z, g.N - xcol(c), lane);
+                __syncwarp();  // reconverge before the warp-collective TMEM ops
+                if (!more) break;
+                tc_ld_wait(rb);
+                const bool more2 = c + 2 < nchunks;
+                if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
+                epi_chunk(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, xcol(c + 1), y, z,
+                          g.N - xcol(c + 1), lane);
+                __syncwarp();
+                if (more2) tc_ld_wait(ra);
             }
             tc_fence_before();
             __syncwarp();
@@ -392,12 +478,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_all();  // this warp's stores are complete
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
+        __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(Cfg::TMEM_COLS)
                      : "memory");
     }
@@ -461,6 +550,22 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over an output [Z][M][N] (bf16 or fp32): box of 32 rows by
+// 64 bytes of columns, 64-byte swizzle; stores outside [0,N) x [0,M) are clipped.
+bool make_out_map(CUtensorMap* map, const void* ptr, bool fp32, uint64_t N, uint64_t M, uint64_t Z) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const uint64_t es = fp32 ? 4 : 2;
+    cuuint64_t dims[3] = {N, M, Z};
+    cuuint64_t strides[2] = {N * es, M * N * es};
+    cuuint32_t box[3] = {(cuuint32_t)(64 / es), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct Plan {
     int bn, splits, kb_per_split, n_tiles, m_tiles, units, grid;
 };
@@ -490,7 +595,8 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
 }
 
 template <int BN, bool A_MN, bool B_MN>
-void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args, int grid, cudaStream_t s) {
+void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& args, int grid,
+               cudaStream_t s) {
     using Cfg = TileCfg<BN>;
     static bool configured = false;
     if (!configured) {
@@ -498,16 +604,16 @@ void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& arg
                              Cfg::SMEM_BYTES);
         configured = true;
     }
-    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, args);
+    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, args);
 }
 
 template <int BN>
-void launch_tc_layout(int a_mn, int b_mn, const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
-                      int grid, cudaStream_t s) {
-    if (!a_mn && !b_mn) launch_tc<BN, false, false>(ma, mb, args, grid, s);
-    else if (!a_mn && b_mn) launch_tc<BN, false, true>(ma, mb, args, grid, s);
-    else if (a_mn && !b_mn) launch_tc<BN, true, false>(ma, mb, args, grid, s);
-    else launch_tc<BN, true, true>(ma, mb, args, grid, s);
+void launch_tc_layout(int a_mn, int b_mn, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                      const GemmArgs& args, int grid, cudaStream_t s) {
+    if (!a_mn && !b_mn) launch_tc<BN, false, false>(ma, mb, md, args, grid, s);
+    else if (!a_mn && b_mn) launch_tc<BN, false, true>(ma, mb, md, args, grid, s);
+    else if (a_mn && !b_mn) launch_tc<BN, true, false>(ma, mb, md, args, grid, s);
+    else launch_tc<BN, true, true>(ma, mb, md, args, grid, s);
 }
 
 }  // namespace
@@ -524,6 +630,9 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
     bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
     ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
                      : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
+    CUtensorMap md;
+    if (p.splits > 1) ok = ok && make_out_map(&md, scratch, true, (uint64_t)N, (uint64_t)M, (uint64_t)p.splits);
+    else ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
     if (!ok) return GPT2_ERR_CUDA;
     GemmArgs g;
     g.D = D;
@@ -538,8 +647,8 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
     g.kb_per_split = p.kb_per_split;
     g.n_tiles = p.n_tiles;
     g.units = p.units;
-    if (p.bn == 128) launch_tc_layout<128>(a_mn, b_mn, ma, mb, g, p.grid, s);
-    else launch_tc_layout<256>(a_mn, b_mn, ma, mb, g, p.grid, s);
+    if (p.bn == 128) launch_tc_layout<128>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
+    else launch_tc_layout<256>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
     if (p.splits > 1) {
         const int64_t MN = (int64_t)M * N;
         const int blocks = (int)((MN / 8 + 255) / 256);

@@ -26,6 +26,9 @@ int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int
 int launch_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s);
 int launch_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n, cudaStream_t s);
 
+// out[c] (c < split) / out2[c - split] (c >= split) = column sums of in [R, ncols], deterministic.
+int launch_colsum(float* out, float* out2, int split, const float* in, int R, int ncols, cudaStream_t s);
+
 size_t bias_backward_scratch(int N, int C);
 int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s);
 

@@ -5,8 +5,8 @@
 
 #define LN_EPS 1e-5f
 #define LN_FWD_WARPS 8
-#define LN_BWD_WARPS 4
-#define LN_BWD_MAX_BLOCKS 512
+#define LN_BWD_WARPS 8
+#define LN_BWD_MAX_BLOCKS 608  // four resident blocks on each of 152 SMs
 
 // y = (x - mean) * rstd * gamma + beta, biased variance, eps 1e-5.
 // VPL = 8-element vectors per lane (C <= 256 * VPL).
@@ -64,12 +64,14 @@ __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict
 }
 
 // dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat)), dxhat = dy gamma.
-// Each warp also accumulates dy*xhat and dy for its lane's columns in its own
-// shared-memory rows (no two threads touch the same word); column idx*8+j is
-// kept at word j*(C/8)+idx so a warp's accesses hit 32 distinct banks. The
-// block then sums its warps in order into partial[block][0..2C).
+// Warp per row, rows strided over a fixed grid; the next row's x and dy are
+// loaded (raw) before the current row is computed. Each warp accumulates
+// dy*xhat and dy for its lane's columns in its own shared-memory rows (no two
+// threads touch the same word; column idx*8+j at word j*(C/8)+idx, so a
+// warp's accesses hit 32 distinct banks). The block then sums its warps in
+// order into partial[block][0..2C); a column reduce finishes dgamma, dbeta.
 template <typename T, int VPL>
-__global__ void __launch_bounds__(LN_BWD_WARPS * 32) ln_bwd_kernel(T* __restrict__ dx, float* __restrict__ partial,
+__global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1) ln_bwd_kernel(T* __restrict__ dx, float* __restrict__ partial,
                                                                    const T* __restrict__ dy, const T* __restrict__ x,
                                                                    const T* __restrict__ gamma,
                                                                    const float* __restrict__ mean,
@@ -84,7 +86,32 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32) ln_bwd_kernel(T* __restrict
         acc_b[c] = 0.f;
     }
     __syncwarp();
-    for (int row = blockIdx.x * LN_BWD_WARPS + w; row < N; row += gridDim.x * LN_BWD_WARPS) {
+    const int stride = gridDim.x * LN_BWD_WARPS;
+    int row = blockIdx.x * LN_BWD_WARPS + w;
+    Raw8<T> rx[VPL], rd[VPL];
+    if (row < N) {
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                raw_load(rx[i], x + (int64_t)row * C + idx * 8);
+                raw_load(rd[i], dy + (int64_t)row * C + idx * 8);
+            }
+        }
+    }
+    while (row < N) {
+        const int next = row + stride;
+        Raw8<T> nx[VPL], nd[VPL];
+        if (next < N) {
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int idx = lane + 32 * i;
+                if (idx < cv) {
+                    raw_load(nx[i], x + (int64_t)next * C + idx * 8);
+                    raw_load(nd[i], dy + (int64_t)next * C + idx * 8);
+                }
+            }
+        }
         const float mu = mean[row], rs = rstd[row];
         float xh[VPL][8], dh[VPL][8];
         float s1 = 0.f, s2 = 0.f;
@@ -93,8 +120,8 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32) ln_bwd_kernel(T* __restrict
             const int idx = lane + 32 * i;
             if (idx < cv) {
                 float g[8];
-                load8(x + (int64_t)row * C + idx * 8, xh[i]);
-                load8(dy + (int64_t)row * C + idx * 8, dh[i]);
+                raw_unpack(rx[i], xh[i]);
+                raw_unpack(rd[i], dh[i]);
                 load8(gamma + idx * 8, g);
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
@@ -120,6 +147,12 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32) ln_bwd_kernel(T* __restrict
                 store8(dx + (int64_t)row * C + idx * 8, o);
             }
         }
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            rx[i] = nx[i];
+            rd[i] = nd[i];
+        }
+        row = next;
     }
     __syncthreads();
     for (int a = threadIdx.x; a < C; a += blockDim.x) {
@@ -133,19 +166,6 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32) ln_bwd_kernel(T* __restrict
         partial[(size_t)blockIdx.x * 2 * C + c] = sg;
         partial[(size_t)blockIdx.x * 2 * C + C + c] = sb;
     }
-}
-
-__global__ void ln_bwd_reduce_kernel(float* __restrict__ dgamma, float* __restrict__ dbeta,
-                                     const float* __restrict__ partial, int nblk, int C) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
-    float sg = 0.f, sb = 0.f;
-    for (int k = 0; k < nblk; k++) {
-        sg += partial[(size_t)k * 2 * C + c];
-        sb += partial[(size_t)k * 2 * C + C + c];
-    }
-    dgamma[c] = sg;
-    dbeta[c] = sb;
 }
 
 static int ln_vpl(int C) { return (C / 8 + 31) / 32; }
@@ -213,6 +233,6 @@ int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, 
         ln_bwd_launch<float, V>(blocks, smem, dx, partial, dy, x, gamma, mean, rstd, N, C, s);
     LN_DISPATCH(ln_vpl(C), LN_BWD_CALL)
 #undef LN_BWD_CALL
-    ln_bwd_reduce_kernel<<<(C + 255) / 256, 256, 0, s>>>(dgamma, dbeta, partial, blocks, C);
+    launch_colsum(dgamma, dbeta, C, partial, blocks, 2 * C, s);
     return 2;
 }
