@@ -1,10 +1,10 @@
-// Causal multi-head attention, forward and backward, flash-style: the T x T
-// score matrix exists only tile by tile in registers.
+// Causal multi-head attention backward (and the fp32 forward), flash-style:
+// the T x T score matrix exists only tile by tile in registers. The bf16
+// forward is the tcgen05 kernel of attention_tc.cu.
 //
-// bf16 path (head size 64): 64-query x 64-key tiles, four warps of 16 rows,
-// bf16 tensor-core MMAs (m16n8k16, fp32 accumulate) for QK^T and PV, softmax
-// in fp32 registers with a running max and sum (exp2 of log2-scaled scores),
-// K/V tiles double-buffered in XOR-swizzled shared memory by cp.async.
+// bf16 backward (head size 64): 64 x 64 tiles, four warps of 16 rows, bf16
+// tensor-core MMAs (m16n8k16, fp32 accumulate), K/V/Q/dO tiles in
+// XOR-swizzled shared memory by cp.async.
 // The backward recomputes P from the saved log-sum-exp and runs two kernels,
 // one per key block (dK, dV) and one per query block (dQ), so that every
 // output element has a single writer: no atomics, deterministic.
@@ -150,112 +150,6 @@ __device__ __forceinline__ void store_rows_bf16(bf16* g, const float (&acc)[8][4
             *reinterpret_cast<uint32_t*>(g + (int64_t)r0 * ld + c) = pack_bf16(acc[nt][0] * scale, acc[nt][1] * scale);
         if (r1 < T)
             *reinterpret_cast<uint32_t*>(g + (int64_t)r1 * ld + c) = pack_bf16(acc[nt][2] * scale, acc[nt][3] * scale);
-    }
-}
-
-// ============================================================ bf16 forward
-
-__global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(bf16* __restrict__ o, float* __restrict__ lse,
-                                                            const bf16* __restrict__ qkv, int T, int C, int H,
-                                                            float scale_log2) {
-    __shared__ __align__(1024) bf16 sQ[64 * 64];
-    __shared__ __align__(1024) bf16 sK[2][64 * 64];
-    __shared__ __align__(1024) bf16 sV[2][64 * 64];
-    const int qb = gridDim.x - 1 - blockIdx.x;  // longest rows first
-    const int b = blockIdx.y / H, h = blockIdx.y % H;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int ld = 3 * C;
-    const bf16* base = qkv + (int64_t)b * T * ld + h * 64;
-    const uint32_t tq = smem_u32(sQ);
-    const uint32_t tk[2] = {smem_u32(sK[0]), smem_u32(sK[1])};
-    const uint32_t tv[2] = {smem_u32(sV[0]), smem_u32(sV[1])};
-
-    load_tile64(tq, base, qb * 64, T, ld, tid);
-    load_tile64(tk[0], base + C, 0, T, ld, tid);
-    load_tile64(tv[0], base + 2 * C, 0, T, ld, tid);
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-
-    uint32_t qf[4][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; kk++) frag_a(qf[kk], tq, w * 16, kk * 16, lane);
-
-    float acc[8][4];
-    zero_acc(acc);
-    float mrow[2] = {-FLT_MAX, -FLT_MAX}, lrow[2] = {0.f, 0.f};
-    const int gq = lane >> 2, tq4 = lane & 3;
-    const int row0 = qb * 64 + w * 16 + gq;  // this thread's rows: row0, row0 + 8
-    const int nkb = qb + 1;
-    for (int kb = 0; kb < nkb; kb++) {
-        const int buf = kb & 1;
-        if (kb + 1 < nkb) {
-            load_tile64(tk[buf ^ 1], base + C, (kb + 1) * 64, T, ld, tid);
-            load_tile64(tv[buf ^ 1], base + 2 * C, (kb + 1) * 64, T, ld, tid);
-        }
-        cp_async_commit();
-        float s[8][4];
-        zero_acc(s);
-        mma_rows_x_tileT(s, qf, tk[buf], lane);
-        float mx[2] = {-FLT_MAX, -FLT_MAX};
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) {
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int key = kb * 64 + nt * 8 + 2 * tq4 + (e & 1);
-                const int row = row0 + (e >> 1) * 8;
-                float x = s[nt][e] * scale_log2;
-                if (key > row || key >= T) x = -FLT_MAX;
-                s[nt][e] = x;
-                mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            const float mnew = fmaxf(mrow[r], mx[r]);
-            const float alpha = ex2_approx(mrow[r] - mnew);
-            mrow[r] = mnew;
-            lrow[r] *= alpha;
-#pragma unroll
-            for (int nt = 0; nt < 8; nt++) {
-                acc[nt][2 * r] *= alpha;
-                acc[nt][2 * r + 1] *= alpha;
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) {
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const float x = s[nt][e];
-                const float p = x == -FLT_MAX ? 0.f : ex2_approx(x - mrow[e >> 1]);
-                s[nt][e] = p;
-                lrow[e >> 1] += p;
-            }
-        }
-        mma_p_x_tile(acc, s, tv[buf], lane);
-        cp_async_wait<0>();
-        __syncthreads();
-    }
-#pragma unroll
-    for (int r = 0; r < 2; r++) {
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-    const float inv0 = 1.f / lrow[0], inv1 = 1.f / lrow[1];
-#pragma unroll
-    for (int nt = 0; nt < 8; nt++) {
-        acc[nt][0] *= inv0;
-        acc[nt][1] *= inv0;
-        acc[nt][2] *= inv1;
-        acc[nt][3] *= inv1;
-    }
-    store_rows_bf16(o + (int64_t)b * T * C, acc, 1.f, qb * 64 + w * 16, T, C, h * 64, lane);
-    if (tq4 == 0) {
-        float* l = lse + ((int64_t)b * H + h) * T;
-        if (row0 < T) l[row0] = (mrow[0] + log2f(lrow[0])) * ATT_LN2;
-        if (row0 + 8 < T) l[row0 + 8] = (mrow[1] + log2f(lrow[1])) * ATT_LN2;
     }
 }
 
@@ -599,15 +493,12 @@ __global__ void attn_bwd_dkdv_f32_kernel(float* __restrict__ dqkv, const float* 
 // ============================================================ launchers
 
 int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
-                             cudaStream_t s) {
+                             int* status, cudaStream_t s) {
     const int hd = C / H;
     if (B * T == 0) return 0;
     if (dtype == GPT2_MODE_BF16) {
         if (hd != 64) return GPT2_ERR_ARG;
-        dim3 grid((T + 63) / 64, B * H);
-        attn_fwd_bf16_kernel<<<grid, 128, 0, s>>>((bf16*)o, lse, (const bf16*)qkv, T, C, H,
-                                                  ATT_LOG2E / sqrtf((float)hd));
-        return 1;
+        return launch_attention_forward_tc((bf16*)o, lse, (const bf16*)qkv, B, T, C, H, status, s);
     }
     const int64_t n = (int64_t)B * H * T;
     const int blocks = (int)((n + 127) / 128);

@@ -4,6 +4,7 @@
 // validated by the caller.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -40,7 +41,9 @@ int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v
                  float b2, float eps, float wd, int t, cudaStream_t s);
 
 int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
-                             cudaStream_t s);
+                             int* status, cudaStream_t s);
+int launch_attention_forward_tc(__nv_bfloat16* o, float* lse, const __nv_bfloat16* qkv, int B, int T, int C, int H,
+                                int* status, cudaStream_t s);
 size_t attention_backward_scratch(int B, int T, int H);
 int launch_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* o,
                               const float* lse, int B, int T, int C, int H, void* scratch, cudaStream_t s);

@@ -409,7 +409,7 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
         TRY(linear_fwd(m, b.qkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
         {
             Op op(m, GPT2_K_ATTENTION_FWD);
-            TRY(op.done(launch_attention_forward(m->dtype, b.atty, b.lse, b.qkv, B, T, C, m->H, m->stream),
+            TRY(op.done(launch_attention_forward(m->dtype, b.atty, b.lse, b.qkv, B, T, C, m->H, m->status, m->stream),
                         attn_fwd_flops(B, T, C)));
         }
         TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));

@@ -91,7 +91,7 @@ int gpt2_op_attention_forward(int dtype, void* o, float* lse, const void* qkv, i
     if (!dt_ok(dtype) || !o || !lse || !qkv || B < 0 || T < 0 || C <= 0 || H <= 0 || C % H || C % 8)
         return GPT2_ERR_ARG;
     if (!al16(o) || !al16(qkv)) return GPT2_ERR_ARG;
-    return finish(launch_attention_forward(dtype, o, lse, qkv, B, T, C, H, st(stream)));
+    return finish(launch_attention_forward(dtype, o, lse, qkv, B, T, C, H, nullptr, st(stream)));
 }
 
 size_t gpt2_op_attention_backward_scratch(int B, int T, int H) {
