@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int i = lane; i < BN / 2; i += 32) bias_s[i] = nb + i < g.N ? __bfloat162float(bp[nb + i]) : 0.f;
                 __syncwarp();
             }
-            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, g.status)) break;
+            if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag, g.status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
             const int y = m0 + quad * 32;

@@ -42,11 +42,15 @@ int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v
 
 int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
                              int* status, cudaStream_t s);
+int launch_attention_backward_tc(__nv_bfloat16* dqkv, const __nv_bfloat16* dout, const __nv_bfloat16* qkv,
+                                 const float* lse, const float* D, int B, int T, int C, int H, int* status,
+                                 cudaStream_t s);
 int launch_attention_forward_tc(__nv_bfloat16* o, float* lse, const __nv_bfloat16* qkv, int B, int T, int C, int H,
                                 int* status, cudaStream_t s);
 size_t attention_backward_scratch(int B, int T, int H);
 int launch_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* o,
-                              const float* lse, int B, int T, int C, int H, void* scratch, cudaStream_t s);
+                              const float* lse, int B, int T, int C, int H, void* scratch, int* status,
+                              cudaStream_t s);
 
 // Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
 size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32);

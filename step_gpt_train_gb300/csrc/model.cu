@@ -462,7 +462,7 @@ int backward_impl(gpt2* m) {
         {
             Op op(m, GPT2_K_ATTENTION_BWD);
             TRY(op.done(launch_attention_backward(m->dtype, m->dqkv, m->dtmp, b.qkv, b.atty, b.lse, B, T, C, m->H,
-                                                  m->scratch, m->stream),
+                                                  m->scratch, m->status, m->stream),
                         2.5 * attn_fwd_flops(B, T, C)));
         }
         TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));

@@ -107,7 +107,7 @@ int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const vo
         return GPT2_ERR_ARG;
     if (!scratch || scratch_bytes < attention_backward_scratch(B, T, H)) return GPT2_ERR_WORKSPACE;
     if (!al16(dqkv) || !al16(dout) || !al16(qkv) || !al16(o)) return GPT2_ERR_ARG;
-    return finish(launch_attention_backward(dtype, dqkv, dout, qkv, o, lse, B, T, C, H, scratch, st(stream)));
+    return finish(launch_attention_backward(dtype, dqkv, dout, qkv, o, lse, B, T, C, H, scratch, nullptr, st(stream)));
 }
 
 int gpt2_op_gelu_forward(int dtype, void* g, const void* u, int64_t n, void* stream) {

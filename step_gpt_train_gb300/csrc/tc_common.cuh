@@ -48,6 +48,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         }
     }
 }
+// Bounded wait by every lane of a warp, with one outcome for the whole warp:
+// if any lane gave up, all give up, so no lane goes on alone into a warp-wide
+// operation (a shuffle, __syncwarp or a .sync.aligned TMEM access).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
 // Bounded wait used while shutting down (ignores the abort flag).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* status) {
     const long long t0 = clock64();
