@@ -338,7 +338,9 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
 namespace {
 
 constexpr int BW_THREADS = 320;
-constexpr int BW_EW = 8;  // elementwise warps
+constexpr int BW_EW = 8;     // elementwise warps
+constexpr int DKDV_ST = 3;   // Q/dO (and lse/D) stages of the dK/dV kernel
+constexpr int DQ_ST = 4;     // K/V stages of the dQ kernel
 
 struct BwdArgs {
     bf16* dqkv;          // [B*T, 3C]
@@ -385,28 +387,30 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // K | V | Q0 dO0 | Q1 dO1 | P^T (2 chunks) | dS^T (2 chunks) | lse/D slots | barriers
+    // K | V | DKDV_ST x (Q, dO) | P^T (2 chunks) | dS^T (2 chunks) | lse/D slots | barriers
+    constexpr int NS = DKDV_ST;
     const uint32_t sK = base, sV = base + AT_TILE;
     auto sQ = [&](int st) { return base + (2 + 2 * st) * AT_TILE; };
     auto sO = [&](int st) { return base + (3 + 2 * st) * AT_TILE; };
-    const uint32_t sP = base + 6 * AT_TILE, sS = base + 8 * AT_TILE;
-    uint8_t* gP = gbase + 6 * AT_TILE;
-    uint8_t* gS = gbase + 8 * AT_TILE;
-    float* ldslot = reinterpret_cast<float*>(gbase + 10 * AT_TILE);  // [2][256]: lse2[128], D[128]
-    const uint32_t bars = base + 10 * AT_TILE + 2048;
-    uint8_t* bar_area = gbase + 10 * AT_TILE + 2048;
+    const uint32_t sP = base + (2 + 2 * NS) * AT_TILE, sS = base + (4 + 2 * NS) * AT_TILE;
+    uint8_t* gP = gbase + (2 + 2 * NS) * AT_TILE;
+    uint8_t* gS = gbase + (4 + 2 * NS) * AT_TILE;
+    float* ldslot = reinterpret_cast<float*>(gbase + (6 + 2 * NS) * AT_TILE);  // [NS][256]: lse2[128], D[128]
+    const uint32_t bars = base + (6 + 2 * NS) * AT_TILE + NS * 1024;
+    uint8_t* bar_area = gbase + (6 + 2 * NS) * AT_TILE + NS * 1024;
     const uint32_t kv_full = bars;
     auto qd_full = [&](int i) { return bars + 8u * (1 + i); };
-    auto qd_empty = [&](int i) { return bars + 8u * (3 + i); };
-    auto ld_full = [&](int i) { return bars + 8u * (5 + i); };
-    auto ld_empty = [&](int i) { return bars + 8u * (7 + i); };
-    const uint32_t s_full = bars + 8u * 9, s_free = bars + 8u * 10;
-    const uint32_t dp_full = bars + 8u * 11, dp_free = bars + 8u * 12;
-    const uint32_t p_full = bars + 8u * 13, p_free = bars + 8u * 14;
-    const uint32_t ds_full = bars + 8u * 15, ds_free = bars + 8u * 16;
-    const uint32_t o_done = bars + 8u * 17, drain = bars + 8u * 18;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * 19);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * 19 + 4);
+    auto qd_empty = [&](int i) { return bars + 8u * (1 + NS + i); };
+    auto ld_full = [&](int i) { return bars + 8u * (1 + 2 * NS + i); };
+    auto ld_empty = [&](int i) { return bars + 8u * (1 + 3 * NS + i); };
+    const uint32_t bx = bars + 8u * (1 + 4 * NS);
+    const uint32_t s_full = bx, s_free = bx + 8u;
+    const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
+    const uint32_t p_full = bx + 32u, p_free = bx + 40u;
+    const uint32_t ds_full = bx + 48u, ds_free = bx + 56u;
+    const uint32_t o_done = bx + 64u, drain = bx + 72u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (1 + 4 * NS) + 80);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (1 + 4 * NS) + 84);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int kt = blockIdx.x;  // key tile; the first tiles have the most query blocks
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < NS; i++) {
             mbar_init(qd_full(i), 1);
             mbar_init(qd_empty(i), 1);
             mbar_init(ld_full(i), 1);
@@ -444,7 +448,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        int qd_issued[2] = {-1, -1};
+        int qd_issued[NS];
+        for (int i = 0; i < NS; i++) qd_issued[i] = -1;
         if (lane == 0) {
             mbar_expect_tx(kv_full, 2 * AT_TILE);
             tma_load_3d(sK, &tm_qkv, kv_full, a.C + h * AT_HD, kt * AT_N, b);
@@ -453,8 +458,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const float* lrow = a.lse + ((int64_t)b * a.H + h) * a.T;
         const float* drow = a.D + ((int64_t)b * a.H + h) * a.T;
         for (int n = 0; n < nblk; n++) {
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
+            const int st = n % NS;
+            const uint32_t ph = (n / NS) & 1;
             const int q0 = (kt + n) * AT_M;
             int ok = 1;
             if (lane == 0) {
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
         if (lane == 0) {
             mbar_drain(kv_full, 0, a.status);
-            for (int st = 0; st < 2; st++)
+            for (int st = 0; st < NS; st++)
                 if (qd_issued[st] >= 0) mbar_drain(qd_full(st), (uint32_t)qd_issued[st], a.status);
         }
     } else if (warp == 1) {
@@ -489,9 +494,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);  // K-major x K-major
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);  // K-major x MN-major
             bool ok = mbar_wait(kv_full, 0, abort_flag, a.status);
-            auto issue_sdp = [&](int n) -> bool {  // S^T(n) and dP^T(n)
-                const int st = n & 1;
-                if (!mbar_wait(qd_full(st), (n >> 1) & 1, abort_flag, a.status)) return false;
+            auto issue_sdp = [&](int n) -> bool {  // S^T(n)
+                const int st = n % NS;
+                if (!mbar_wait(qd_full(st), (n / NS) & 1, abort_flag, a.status)) return false;
                 if (!mbar_wait(s_free, (n & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 return true;
             };
             auto issue_dp = [&](int n) -> bool {
-                const int st = n & 1;
+                const int st = n % NS;
                 if (!mbar_wait(dp_free, (n & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
@@ -514,7 +519,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             };
             if (ok) ok = issue_sdp(0) && issue_dp(0);
             for (int n = 0; ok && n < nblk; n++) {
-                const int st = n & 1;
+                const int st = n % NS;
                 if (n + 1 < nblk && !(ok = issue_sdp(n + 1))) break;
                 // dV += P^T dO
                 if (!(ok = mbar_wait(p_full, n & 1, abort_flag, a.status))) break;
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         bool ok = true;
         for (int n = 0; n < nblk; n++) {
-            const int st = n & 1;
+            const int st = n % NS;
             const int q0 = (kt + n) * AT_M + half * 64;  // first query of this thread's columns
             const bool diag = n == 0;
             uint32_t sv[2][32];
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            if (!(ok = warp_wait(ld_full(st), (n >> 1) & 1, abort_flag, a.status))) break;
+            if (!(ok = warp_wait(ld_full(st), (n / NS) & 1, abort_flag, a.status))) break;
             const float* slot = ldslot + st * 256 + half * 64;
             float p[64];
             uint32_t pk[32];
@@ -638,23 +643,25 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // Q | dO | K0 V0 | K1 V1 | dS (2 chunks) | barriers
+    // Q | dO | DQ_ST x (K, V) | dS (2 chunks) | barriers
+    constexpr int NS = DQ_ST;
     const uint32_t sQ = base, sO = base + AT_TILE;
     auto sK = [&](int st) { return base + (2 + 2 * st) * AT_TILE; };
     auto sV = [&](int st) { return base + (3 + 2 * st) * AT_TILE; };
-    const uint32_t sS = base + 6 * AT_TILE;
-    uint8_t* gS = gbase + 6 * AT_TILE;
-    const uint32_t bars = base + 8 * AT_TILE;
-    uint8_t* bar_area = gbase + 8 * AT_TILE;
+    const uint32_t sS = base + (2 + 2 * NS) * AT_TILE;
+    uint8_t* gS = gbase + (2 + 2 * NS) * AT_TILE;
+    const uint32_t bars = base + (4 + 2 * NS) * AT_TILE;
+    uint8_t* bar_area = gbase + (4 + 2 * NS) * AT_TILE;
     const uint32_t qo_full = bars;
     auto kv_full = [&](int i) { return bars + 8u * (1 + i); };
-    auto kv_empty = [&](int i) { return bars + 8u * (3 + i); };
-    const uint32_t s_full = bars + 8u * 5, s_free = bars + 8u * 6;
-    const uint32_t dp_full = bars + 8u * 7, dp_free = bars + 8u * 8;
-    const uint32_t ds_full = bars + 8u * 9, ds_free = bars + 8u * 10;
-    const uint32_t o_done = bars + 8u * 11, drain = bars + 8u * 12;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * 13);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * 13 + 4);
+    auto kv_empty = [&](int i) { return bars + 8u * (1 + NS + i); };
+    const uint32_t bx = bars + 8u * (1 + 2 * NS);
+    const uint32_t s_full = bx, s_free = bx + 8u;
+    const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
+    const uint32_t ds_full = bx + 32u, ds_free = bx + 40u;
+    const uint32_t o_done = bx + 48u, drain = bx + 56u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (1 + 2 * NS) + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (1 + 2 * NS) + 68);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int qt = gridDim.x - 1 - blockIdx.x;  // longest rows first
@@ -663,7 +670,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(qo_full, 1);
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < NS; i++) {
             mbar_init(kv_full(i), 1);
             mbar_init(kv_empty(i), 1);
         }
@@ -687,13 +694,14 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            int kv_issued[2] = {-1, -1};
+            int kv_issued[NS];
+            for (int i = 0; i < NS; i++) kv_issued[i] = -1;
             mbar_expect_tx(qo_full, 2 * AT_TILE);
             tma_load_3d(sQ, &tm_qkv, qo_full, h * AT_HD, qt * AT_M, b);
             tma_load_3d(sO, &tm_do, qo_full, h * AT_HD, qt * AT_M, b);
             for (int j = 0; j < nkb; j++) {
-                const int st = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
+                const int st = j % NS;
+                const uint32_t ph = (j / NS) & 1;
                 if (!mbar_wait(kv_empty(st), ph ^ 1u, abort_flag, a.status)) break;
                 mbar_expect_tx(kv_full(st), 2 * AT_TILE);
                 tma_load_3d(sK(st), &tm_qkv, kv_full(st), a.C + h * AT_HD, j * AT_N, b);
@@ -701,7 +709,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 kv_issued[st] = (int)ph;
             }
             mbar_drain(qo_full, 0, a.status);
-            for (int st = 0; st < 2; st++)
+            for (int st = 0; st < NS; st++)
                 if (kv_issued[st] >= 0) mbar_drain(kv_full(st), (uint32_t)kv_issued[st], a.status);
         }
     } else if (warp == 1) {
@@ -710,8 +718,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);
             bool ok = mbar_wait(qo_full, 0, abort_flag, a.status);
             auto issue_s = [&](int j) -> bool {
-                const int st = j & 1;
-                if (!mbar_wait(kv_full(st), (j >> 1) & 1, abort_flag, a.status)) return false;
+                const int st = j % NS;
+                if (!mbar_wait(kv_full(st), (j / NS) & 1, abort_flag, a.status)) return false;
                 if (!mbar_wait(s_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
@@ -722,7 +730,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 return true;
             };
             auto issue_dp = [&](int j) -> bool {
-                const int st = j & 1;
+                const int st = j % NS;
                 if (!mbar_wait(dp_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
@@ -734,7 +742,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             };
             if (ok) ok = issue_s(0) && issue_dp(0);
             for (int j = 0; ok && j < nkb; j++) {
-                const int st = j & 1;
+                const int st = j % NS;
                 if (j + 1 < nkb && !(ok = issue_s(j + 1) && issue_dp(j + 1))) break;
                 // dQ += dS K
                 if (!(ok = mbar_wait(ds_full, j & 1, abort_flag, a.status))) break;
@@ -831,8 +839,9 @@ bool make_do_map(CUtensorMap* map, const void* dout, int B, int T, int C) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int DKDV_SMEM = 10 * AT_TILE + 2048 + 256 + 1024;
-constexpr int DQ_SMEM = 8 * AT_TILE + 256 + 1024;
+constexpr int DKDV_SMEM = (6 + 2 * DKDV_ST) * AT_TILE + DKDV_ST * 1024 + 256 + 1024;
+constexpr int DQ_SMEM = (4 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
+static_assert(DKDV_SMEM <= 232448 && DQ_SMEM <= 232448, "shared memory per CTA");
 
 }  // namespace
 
