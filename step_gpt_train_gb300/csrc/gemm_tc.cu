@@ -4,7 +4,7 @@
 // in tensor memory (TMEM). These are the matmuls of the GPT-2 step: the
 // linear forwards (A = activations, K-major; B = weight [N,K], K-major), the
 // input gradients dX = dY W (B = W read MN-major) and the weight gradients
-// dW = dY^T X (both operands MN-major, fp32 output, long K = B*T, split-K).
+// dW = dY^T X (both operands MN-major, fp32 output, long K = B*T).
 //
 // Structure: a persistent kernel, one CTA per SM, 10 warps.
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
@@ -23,6 +23,12 @@
 //               columns outside the matrix). The next chunk's TMEM load is in
 //               flight while the current one is stored.
 // Two accumulators let the epilogue of one tile overlap the MMAs of the next.
+// Work is a round robin of units over the CTAs. A unit is a whole 128 x BN
+// tile or, for weight gradients with few tiles and a long K, one of S equal
+// k-ranges of a tile (split-K). Units are numbered tile-major, so the CTAs
+// that run at the same time read the same k-blocks of A and B in lockstep and
+// share them through L2. A split unit stores an fp32 partial tile; a reduce
+// kernel adds the S partials of each tile in split order (deterministic).
 // Every mbarrier wait is bounded: on timeout the kernel sets a status bit,
 // stops, waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
@@ -42,11 +48,11 @@ constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;
 
 template <int BN> struct TileCfg {
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // power of two >= two accumulators
     static constexpr int OUT_STAGE_BYTES = 2048;                        // per epilogue warp: 32 rows x 64 B
     static constexpr int OUT_BYTES = EPI_WARPS * OUT_STAGE_BYTES;
     static constexpr int BAR_BYTES = 256;
@@ -55,17 +61,33 @@ template <int BN> struct TileCfg {
 };
 
 struct GemmArgs {
-    void* D;             // output (bf16 or fp32), or null when writing split partials
     const void* bias;    // bf16 [N] or null
-    float* partial;      // split-K partial sums [splits][M][N] (when splits > 1)
     int* status;
     int M, N, K;
     int d_fp32;
-    int splits;
-    int kb_per_split;
+    int splits;          // k-ranges per tile (1: whole tiles, direct output)
+    int kbs;             // k-blocks per split
     int n_tiles;         // ceil(N / BN)
     int units;           // m_tiles * n_tiles * splits
+    int num_kb;          // ceil(K / 64)
 };
+
+// One unit of a CTA's work: k-blocks [kb0, kb1) of a tile; z = partial slot.
+struct Work {
+    int tile, kb0, kb1, z;
+};
+
+// The idx-th unit of this CTA, or false when there is none.
+__device__ __forceinline__ bool get_work(const GemmArgs& g, int idx, Work& w) {
+    const int u = blockIdx.x + idx * gridDim.x;
+    if (u >= g.units) return false;
+    const int sp = u % g.splits;
+    w.tile = u / g.splits;
+    w.kb0 = sp * g.kbs;
+    w.kb1 = min(g.num_kb, w.kb0 + g.kbs);
+    w.z = u;
+    return true;
+}
 
 // One 32-column chunk of this warp's 32 rows: + bias, convert, stage, TMA store.
 // fp32 output goes out as two 16-column halves. ncols_valid = columns of the
@@ -113,7 +135,7 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, GemmArgs g) {
+                   const __grid_constant__ CUtensorMap tmD, const GemmArgs g) {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -163,7 +185,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_kb = (g.K + BK - 1) / BK;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -173,13 +194,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int issued_phase[S];
             for (int s = 0; s < S; s++) issued_phase[s] = -1;
             bool ok = true;
-            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
-                const int split = u % g.splits;
-                const int tile = u / g.splits;
-                const int m0 = (tile / g.n_tiles) * BM, n0 = (tile % g.n_tiles) * BN;
-                const int kb0 = split * g.kb_per_split;
-                const int kb1 = min(num_kb, kb0 + g.kb_per_split);
-                for (int kb = kb0; kb < kb1; kb++) {
+            Work w;
+            for (int idx = 0; ok && get_work(g, idx, w); idx++) {
+                const int m0 = (w.tile / g.n_tiles) * BM, n0 = (w.tile % g.n_tiles) * BN;
+                for (int kb = w.kb0; kb < w.kb1; kb++) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
                         ok = false;
                         break;
@@ -224,10 +242,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < g.units && ok; u += gridDim.x) {
-                const int split = u % g.splits;
-                const int kb0 = split * g.kb_per_split;
-                const int kb1 = min(num_kb, kb0 + g.kb_per_split);
+            Work w;
+            for (int idx = 0; ok && get_work(g, idx, w); idx++) {
+                const int kb0 = w.kb0, kb1 = w.kb1;
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -276,10 +293,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool use_bias = g.bias != nullptr && g.splits == 1;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < g.units; u += gridDim.x) {
-            const int split = u % g.splits;
-            const int tile = u / g.splits;
-            const int m0 = (tile / g.n_tiles) * BM, n0 = (tile % g.n_tiles) * BN;
+        Work w;
+        for (int idx = 0; get_work(g, idx, w); idx++) {
+            const int m0 = (w.tile / g.n_tiles) * BM, n0 = (w.tile % g.n_tiles) * BN;
             const int cfirst = half * CHUNKS;
             if (use_bias) {
                 // the bias of this warp's half of the tile; the buffer's only
@@ -300,9 +316,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int c = 0; c < CHUNKS; c++)
                     if (n0 + (cfirst + c) * 32 < g.N) nchunks = c + 1;
             }
-            const bool fp32_out = g.splits > 1 || g.d_fp32 != 0;
-            const int z = g.splits > 1 ? split : 0;
-            auto xcol = [&](int c) { return n0 + (cfirst + c) * 32; };
+            const bool split = g.splits > 1;
+            const bool fp32_out = split || g.d_fp32 != 0;
+            // split partials are stored tile-local: [unit][128 rows][BN columns]
+            const int z = split ? w.z : 0;
+            const int ys = split ? quad * 32 : y;
+            auto xcol = [&](int c) { return (split ? 0 : n0) + (cfirst + c) * 32; };
+            auto ncols = [&](int c) { return g.N - (n0 + (cfirst + c) * 32); };
             auto bias_at = [&](int c) -> const float* { return use_bias ? bias_s + c * 32 : nullptr; };
             uint32_t ra[32], rb[32];
             if (nchunks > 0) {
@@ -313,14 +333,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // ra holds chunk c; chunk c+1 is loaded into rb while ra is stored
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
-                epi_chunk(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, xcol(c), y, z, g.N - xcol(c), lane);
+                epi_chunk(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, xcol(c), ys, z, ncols(c), lane);
                 __syncwarp();  // reconverge before the warp-collective TMEM ops
                 if (!more) break;
                 tc_ld_wait(rb);
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
-                epi_chunk(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, xcol(c + 1), y, z,
-                          g.N - xcol(c + 1), lane);
+                epi_chunk(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, xcol(c + 1), ys, z, ncols(c + 1),
+                          lane);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
             }
@@ -346,30 +366,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// D = sum over splits of partial (+ bias), fp32 or bf16 out. Fixed order.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(void* D, int d_fp32, const float* __restrict__ partial,
-                                                            const bf16* __restrict__ bias, int splits, int64_t MN,
-                                                            int N) {
+// Split-K reduce: D[m][n] (fp32) = bias[n] (if any) + the partial tiles of
+// the tile of (m, n), added in split order. 8 consecutive columns per thread
+// (N and BN are multiples of 8).
+__global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ D, const float* __restrict__ partial,
+                                                           const bf16* __restrict__ bias, int M, int N, int BN,
+                                                           int n_tiles, int splits) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-    if (i >= MN) return;
-    float acc[8];
-    load8(partial + i, acc);
-    for (int s = 1; s < splits; s++) {
+    if (i >= (int64_t)M * N) return;
+    const int m = (int)(i / N), n = (int)(i % N);
+    const int64_t tile = (int64_t)(m / BM) * n_tiles + n / BN;
+    const int64_t tile_elems = (int64_t)BM * BN;
+    const float* p = partial + tile * splits * tile_elems + (int64_t)(m % BM) * BN + n % BN;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (bias) load8(bias + n, acc);
+    for (int sp = 0; sp < splits; sp++) {
         float v[8];
-        load8(partial + (int64_t)s * MN + i, v);
+        load8(p + sp * tile_elems, v);
 #pragma unroll
         for (int j = 0; j < 8; j++) acc[j] += v[j];
     }
-    if (bias) {
-        float b[8];
-        load8(bias + (i % N), b);
-#pragma unroll
-        for (int j = 0; j < 8; j++) acc[j] += b[j];
-    }
-    if (d_fp32)
-        store8(reinterpret_cast<float*>(D) + i, acc);
-    else
-        store8(reinterpret_cast<bf16*>(D) + i, acc);
+    store8(D + i, acc);
 }
 
 // ---------------------------------------------------------------- host side
@@ -407,29 +424,51 @@ bool make_out_map(CUtensorMap* map, const void* ptr, bool fp32, uint64_t N, uint
 }
 
 struct Plan {
-    int bn, splits, kb_per_split, n_tiles, m_tiles, units, grid;
+    int bn, n_tiles, m_tiles, tiles, num_kb, splits, kbs, units, grid;
 };
+
+// HBM bytes moved in the time one SM takes for one 128 x 256 x 64 k-block of
+// MMAs (about 0.32 us at 13 TFLOP/s per SM and 6.8 TB/s): the exchange rate
+// between partial-sum traffic and MMA time in the split-K cost model.
+constexpr double KB_HBM_BYTES = 2.0e6;
 
 Plan make_plan(int M, int N, int K, int d_fp32) {
     Plan p;
-    p.bn = N <= 128 ? 128 : 256;
-    p.m_tiles = (M + BM - 1) / BM;
-    p.n_tiles = (N + p.bn - 1) / p.bn;
-    const int num_kb = (K + BK - 1) / BK;
-    const int tiles = p.m_tiles * p.n_tiles;
     const int sms = gpt2_num_sms();
+    p.m_tiles = (M + BM - 1) / BM;
+    p.num_kb = (K + BK - 1) / BK;
+    // tile width: 256, or 192 where that cuts (tile waves x width) by more
+    // than 10% (e.g. N = 768: 1024 tiles in 7 waves instead of 768 in 6);
+    // 128 only for narrow matrices
+    const long long t256 = (long long)p.m_tiles * ((N + 255) / 256);
+    const long long t192 = (long long)p.m_tiles * ((N + 191) / 192);
+    const long long c256 = (t256 + sms - 1) / sms * 256, c192 = (t192 + sms - 1) / sms * 192;
+    p.bn = N <= 128 ? 128 : (c192 * 10 < c256 * 9 ? 192 : 256);
     p.splits = 1;
-    if (d_fp32 && tiles < sms) {
-        // weight gradients: few output tiles and a long K; split K so that
-        // about two units land on every SM, each with >= 4 k-blocks.
-        int want = (2 * sms + tiles - 1) / tiles;
-        int cap = num_kb / 4 > 0 ? num_kb / 4 : 1;
-        p.splits = want < cap ? want : cap;
-        if (p.splits < 1) p.splits = 1;
+    if (d_fp32) {
+        // Weight gradients: cost(S) = waves x k-blocks per unit (the busiest
+        // SM's MMA time, in 128x256 k-block units) + the fp32 partials written
+        // and read back. S = 1 keeps the chosen width; S > 1 uses 256.
+        auto waves = [&](long long units) { return (double)((units + sms - 1) / sms); };
+        const long long t1 = (long long)p.m_tiles * ((N + p.bn - 1) / p.bn);
+        double best = waves(t1) * p.num_kb * (p.bn / 256.0);
+        const int bn_split = N <= 128 ? 128 : 256;
+        const long long ts = (long long)p.m_tiles * ((N + bn_split - 1) / bn_split);
+        for (int sp = 2; sp <= 64 && sp * 4 <= p.num_kb; sp++) {
+            const int kbs = (p.num_kb + sp - 1) / sp;
+            const double cost = waves(ts * sp) * kbs * (bn_split / 256.0) + (double)sp * M * N * 8 / KB_HBM_BYTES;
+            if (cost < best) {
+                best = cost;
+                p.splits = sp;
+            }
+        }
+        if (p.splits > 1) p.bn = bn_split;
     }
-    p.kb_per_split = (num_kb + p.splits - 1) / p.splits;
-    p.splits = (num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty split
-    p.units = tiles * p.splits;
+    p.n_tiles = (N + p.bn - 1) / p.bn;
+    p.tiles = p.m_tiles * p.n_tiles;
+    p.kbs = (p.num_kb + p.splits - 1) / p.splits;
+    p.splits = (p.num_kb + p.kbs - 1) / p.kbs;  // no empty split
+    p.units = p.tiles * p.splits;
     p.grid = p.units < sms ? p.units : sms;
     return p;
 }
@@ -460,7 +499,7 @@ void launch_tc_layout(int a_mn, int b_mn, const CUtensorMap& ma, const CUtensorM
 
 size_t matmul_tc_scratch(int M, int N, int K, int d_fp32) {
     Plan p = make_plan(M, N, K, d_fp32);
-    return p.splits > 1 ? (size_t)p.splits * M * N * 4 : 0;
+    return p.splits > 1 ? (size_t)p.units * BM * p.bn * 4 : 0;
 }
 
 int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
@@ -471,29 +510,29 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
     ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
                      : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
     CUtensorMap md;
-    if (p.splits > 1) ok = ok && make_out_map(&md, scratch, true, (uint64_t)N, (uint64_t)M, (uint64_t)p.splits);
+    if (p.splits > 1) ok = ok && make_out_map(&md, scratch, true, (uint64_t)p.bn, BM, (uint64_t)p.units);
     else ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
     if (!ok) return GPT2_ERR_CUDA;
     GemmArgs g;
-    g.D = D;
     g.bias = p.splits > 1 ? nullptr : bias;
-    g.partial = (float*)scratch;
     g.status = status;
     g.M = M;
     g.N = N;
     g.K = K;
     g.d_fp32 = d_fp32;
     g.splits = p.splits;
-    g.kb_per_split = p.kb_per_split;
+    g.kbs = p.kbs;
     g.n_tiles = p.n_tiles;
     g.units = p.units;
+    g.num_kb = p.num_kb;
     if (p.bn == 128) launch_tc_layout<128>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
+    else if (p.bn == 192) launch_tc_layout<192>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
     else launch_tc_layout<256>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
     if (p.splits > 1) {
         const int64_t MN = (int64_t)M * N;
         const int blocks = (int)((MN / 8 + 255) / 256);
-        splitk_reduce_kernel<<<blocks, 256, 0, s>>>(D, d_fp32, (const float*)scratch, (const bf16*)bias, p.splits,
-                                                    MN, N);
+        split_reduce_kernel<<<blocks, 256, 0, s>>>((float*)D, (const float*)scratch, (const bf16*)bias, M, N, p.bn,
+                                                   p.n_tiles, p.splits);
         return 2;
     }
     return 1;

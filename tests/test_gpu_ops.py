@@ -36,6 +36,14 @@ def _gemm_ref(A, a_mn, B, b_mn, M, N, K, bias):
     return d
 
 
+def tc_accum_atol(K, ref):
+    """Error bound of a tensor-core fp32 accumulation over K: the accumulator is
+    rounded once per 16-deep MMA step, at most one unit in the last place of the
+    running sum each time; the running sum is bounded by 4 max|result| for
+    these random inputs."""
+    return (K / 16) * 2.0 ** -23 * 4 * float(np.abs(ref).max())
+
+
 GEMM_CASES = [
     # M, N, K, a_mn, b_mn, d_fp32, bias
     (300, 392, 200, 0, 0, 0, True),    # linear forward, ragged M, N (two 256 tiles), K
@@ -44,7 +52,10 @@ GEMM_CASES = [
     (392, 200, 304, 1, 1, 1, False),   # weight gradient dW = dY^T X, fp32 out
     (128, 256, 4096, 1, 1, 1, False),  # weight gradient with split-K
     (136, 264, 72, 1, 0, 0, False),    # A M-major, B K-major
-    (520, 1032, 1000, 0, 0, 1, True),  # fp32 out with bias through split-K reduce
+    (520, 1032, 1000, 0, 0, 1, True),  # fp32 out with bias through the stream-K reduce
+    (300, 768, 256, 0, 0, 0, True),    # 192-wide tiles
+    (300, 776, 320, 0, 1, 0, False),   # 192-wide tiles, ragged last column tile
+    (392, 776, 2000, 1, 1, 1, False),  # stream-K weight gradient, ragged M and N
 ]
 
 
@@ -68,6 +79,8 @@ def test_matmul(torch_cuda, mode, case):
     assert np.all(np.isfinite(got))
     if out_dtype == torch.bfloat16:
         assert_close(got, ref, BF16_REL, atol_frac=1e-3, what="bf16 matmul")
+    elif mode == 1:
+        assert_close(got, ref, 1e-5, atol=tc_accum_atol(K, ref), what="fp32 tensor-core matmul")
     else:
         assert_close(got, ref, 1e-5, atol_frac=1e-5, what="fp32 matmul")
 
@@ -99,7 +112,7 @@ def test_matmul_full_size_sampled(torch_cuda):
     torch.cuda.synchronize()
     ms, ns = rng.integers(0, M, 400), rng.integers(0, N, 400)
     ref = np.einsum("ki,ki->i", host(dY[:, ms]), host(X[:, ns]))
-    assert_close(host(W[ms, ns]), ref, 1e-5, atol_frac=1e-5, what="dW sampled")
+    assert_close(host(W[ms, ns]), ref, 1e-5, atol=tc_accum_atol(K, ref), what="dW sampled")
 
 
 @pytest.mark.parametrize("mode", [1, 0])
