@@ -70,6 +70,31 @@ int gpt2_op_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta,
                                const float* rstd, int N, int C, void* scratch,
                                size_t scratch_bytes, void* stream);
 
+/* Residual join followed by LayerNorm, one pass: xsum = x + r (rounded to
+ * dtype, stored), then y, mean, rstd = LayerNorm of xsum exactly as
+ * gpt2_op_layernorm_forward computes it. In the GPT-2 block every residual
+ * sum ("residual_forward") is read next by a LayerNorm ("layernorm_forward";
+ * llm.c "State of the Union", section "Runtime, DRAM traffic,
+ * instructions"). xsum must not overlap x, r or y. Limits as for
+ * gpt2_op_layernorm_forward. */
+int gpt2_op_residual_layernorm_forward(int dtype, void* y, float* mean, float* rstd, void* xsum,
+                                       const void* x, const void* r, const void* gamma,
+                                       const void* beta, int N, int C, void* stream);
+
+/* LayerNorm backward into the residual-stream gradient: with dx as in
+ * gpt2_op_layernorm_backward, dres = dx (accumulate = 0) or dres += dx
+ * (accumulate = 1, the residual join of the backward pass; dres is read and
+ * written in place). dgamma, dbeta as in gpt2_op_layernorm_backward; if
+ * dres_colsum is not null it receives the column sums of the resulting dres
+ * (as stored, in dtype), fp32 [C], overwritten: the bias gradient
+ * ("matmul_backward_bias") of the projection whose output joined the
+ * residual stream at this point. Scratch: gpt2_op_layernorm_backward_scratch. */
+int gpt2_op_layernorm_backward_residual(int dtype, void* dres, int accumulate, float* dgamma,
+                                        float* dbeta, float* dres_colsum, const void* dy,
+                                        const void* x, const void* gamma, const float* mean,
+                                        const float* rstd, int N, int C, void* scratch,
+                                        size_t scratch_bytes, void* stream);
+
 /* Matmul (the bf16 GEMMs of the kernel table, "ampere_bf16" and
  * "cutlass::Kernel2"): D[M,N] = sum_k A(m,k) B(n,k) (+ bias[n]).
  * A(m,k) is A[m*K + k] (a_mn_major = 0) or A[k*M + m] (a_mn_major = 1);

@@ -470,8 +470,15 @@ __global__ void __launch_bounds__(256) bias_partial_kernel(float* __restrict__ p
 // row lanes, then the 32 lane sums in lane order. Block = 32 columns x 32 row
 // lanes; a warp reads 32 consecutive floats of one row (coalesced). Columns
 // c >= split go to out2[c - split] (two outputs that share one pass).
-__global__ void __launch_bounds__(1024) colsum_kernel(float* __restrict__ out, float* __restrict__ out2,
-                                                      int split, const float* __restrict__ in, int R, int ncols) {
+// out_q[c] = column sums of in [R, ncols] for column q * seg + c: the ncols
+// columns are up to three consecutive segments of seg columns, each going to
+// its own output. Fixed order (deterministic).
+struct ColsumOut {
+    float* p[3];
+};
+
+__global__ void __launch_bounds__(1024) colsum_kernel(ColsumOut outs, int seg, const float* __restrict__ in, int R,
+                                                      int ncols) {
     __shared__ float sm[32][33];
     const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
     const int c = blockIdx.x * 32 + tx;
@@ -485,14 +492,20 @@ __global__ void __launch_bounds__(1024) colsum_kernel(float* __restrict__ out, f
     if (ty == 0 && c < ncols) {
         float t = 0.f;
         for (int k = 0; k < 32; k++) t += sm[k][tx];
-        if (c < split) out[c] = t;
-        else out2[c - split] = t;
+        const int q = c / seg;
+        if (q < 3 && outs.p[q]) outs.p[q][c - q * seg] = t;
     }
 }
 
-int launch_colsum(float* out, float* out2, int split, const float* in, int R, int ncols, cudaStream_t s) {
-    colsum_kernel<<<(ncols + 31) / 32, 1024, 0, s>>>(out, out2, split, in, R, ncols);
+int launch_colsum3(float* out0, float* out1, float* out2, int seg, const float* in, int R, int ncols,
+                   cudaStream_t s) {
+    ColsumOut o = {{out0, out1, out2}};
+    colsum_kernel<<<(ncols + 31) / 32, 1024, 0, s>>>(o, seg, in, R, ncols);
     return 1;
+}
+
+int launch_colsum(float* out, float* out2, int split, const float* in, int R, int ncols, cudaStream_t s) {
+    return launch_colsum3(out, out2, nullptr, split, in, R, ncols, s);
 }
 
 size_t bias_backward_scratch(int N, int C) {

@@ -22,6 +22,18 @@ int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, 
                               const void* gamma, const float* mean, const float* rstd, int N, int C, void* scratch,
                               cudaStream_t s);
 
+// The residual join followed by LayerNorm: xsum = x + r (rounded to dtype),
+// y = LayerNorm(xsum).
+int launch_residual_layernorm_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x,
+                                      const void* r, const void* gamma, const void* beta, int N, int C,
+                                      cudaStream_t s);
+// LayerNorm backward into the residual gradient: dres = dx (accumulate == 0)
+// or dres += dx; dres_colsum (optional) = column sums of the resulting dres.
+int launch_layernorm_backward_residual(int dtype, void* dres, int accumulate, float* dgamma, float* dbeta,
+                                       float* dres_colsum, const void* dy, const void* x, const void* gamma,
+                                       const float* mean, const float* rstd, int N, int C, void* scratch,
+                                       cudaStream_t s);
+
 int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream_t s);
 int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s);
 int launch_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s);
@@ -29,6 +41,9 @@ int launch_residual_backward(int dtype, void* dres, const void* dbranch, int64_t
 
 // out[c] (c < split) / out2[c - split] (c >= split) = column sums of in [R, ncols], deterministic.
 int launch_colsum(float* out, float* out2, int split, const float* in, int R, int ncols, cudaStream_t s);
+// out_q[c] = column sums of column q * seg + c of in [R, ncols], q < 3 (null outputs skipped).
+int launch_colsum3(float* out0, float* out1, float* out2, int seg, const float* in, int R, int ncols,
+                   cudaStream_t s);
 
 size_t bias_backward_scratch(int N, int C);
 int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s);

@@ -9,10 +9,14 @@
 #define LN_BWD_MAX_BLOCKS 608  // four resident blocks on each of 152 SMs
 
 // y = (x - mean) * rstd * gamma + beta, biased variance, eps 1e-5.
+// With r != null the row normalised is the residual sum x + r, rounded to T
+// and stored to xsum first (the residual join followed by the next block's
+// LayerNorm, in one pass over the row).
 // VPL = 8-element vectors per lane (C <= 256 * VPL).
 template <typename T, int VPL>
 __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict__ y, float* __restrict__ mean,
-                                                                   float* __restrict__ rstd, const T* __restrict__ x,
+                                                                   float* __restrict__ rstd, T* __restrict__ xsum,
+                                                                   const T* __restrict__ x, const T* __restrict__ r,
                                                                    const T* __restrict__ gamma,
                                                                    const T* __restrict__ beta, int N, int C) {
     const int row = blockIdx.x * LN_FWD_WARPS + threadIdx.x / 32;
@@ -27,6 +31,13 @@ __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict
         const int idx = lane + 32 * i;
         if (idx < cv) {
             load8_stream(xr + idx * 8, v[i]);
+            if (r) {
+                float u[8];
+                load8_stream(r + (int64_t)row * C + idx * 8, u);
+#pragma unroll
+                for (int j = 0; j < 8; j++) v[i][j] = to_float(from_float<T>(v[i][j] + u[j]));
+                store8(xsum + (int64_t)row * C + idx * 8, v[i]);
+            }
 #pragma unroll
             for (int j = 0; j < 8; j++) s += v[i][j];
         }
@@ -66,25 +77,27 @@ __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict
 // dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat)), dxhat = dy gamma.
 // Warp per row, rows strided over a fixed grid; the next row's x and dy are
 // loaded (raw) before the current row is computed. Each warp accumulates
-// dy*xhat and dy for its lane's columns in its own shared-memory rows (no two
-// threads touch the same word; column idx*8+j at word j*(C/8)+idx, so a
-// warp's accesses hit 32 distinct banks). The block then sums its warps in
-// order into partial[block][0..2C); a column reduce finishes dgamma, dbeta.
+// dy*xhat and dy (and, with np == 3, the values it writes) for its lane's
+// columns in its own shared-memory rows (no two threads touch the same word;
+// column idx*8+j at word j*(C/8)+idx, so a warp's accesses hit 32 distinct
+// banks). The block then sums its warps in order into
+// partial[block][0..np*C); a column reduce finishes dgamma, dbeta (and the
+// column sums of the output, which are the bias gradient of the linear layer
+// that reads this gradient next).
+// Output: with res == null, out = dx; otherwise res += dx in place (the
+// residual join of the backward pass), and out = res.
 template <typename T, int VPL>
-__global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1) ln_bwd_kernel(T* __restrict__ dx, float* __restrict__ partial,
-                                                                   const T* __restrict__ dy, const T* __restrict__ x,
-                                                                   const T* __restrict__ gamma,
-                                                                   const float* __restrict__ mean,
-                                                                   const float* __restrict__ rstd, int N, int C) {
-    extern __shared__ float sh[];  // [LN_BWD_WARPS][2][C]
+__global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1)
+    ln_bwd_kernel(T* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
+                  const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+                  const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C) {
+    extern __shared__ float sh[];  // [LN_BWD_WARPS][np][C]
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cv = C / 8;
-    float* acc_g = sh + (size_t)w * 2 * C;
+    float* acc_g = sh + (size_t)w * np * C;
     float* acc_b = acc_g + C;
-    for (int c = lane; c < C; c += 32) {
-        acc_g[c] = 0.f;
-        acc_b[c] = 0.f;
-    }
+    float* acc_o = acc_b + C;  // used when np == 3
+    for (int c = lane; c < np * C; c += 32) acc_g[c] = 0.f;
     __syncwarp();
     const int stride = gridDim.x * LN_BWD_WARPS;
     int row = blockIdx.x * LN_BWD_WARPS + w;
@@ -144,7 +157,17 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1) ln_bwd_ke
                 float o[8];
 #pragma unroll
                 for (int j = 0; j < 8; j++) o[j] = rs * (dh[i][j] - m1 - xh[i][j] * m2);
-                store8(dx + (int64_t)row * C + idx * 8, o);
+                if (accumulate) {  // the residual gradient this row's result is added to
+                    float rv[8];
+                    load8(out + (int64_t)row * C + idx * 8, rv);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) o[j] += rv[j];
+                }
+                store8(out + (int64_t)row * C + idx * 8, o);
+                if (np == 3) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) acc_o[j * cv + idx] += to_float(from_float<T>(o[j]));
+                }
             }
         }
 #pragma unroll
@@ -155,17 +178,163 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1) ln_bwd_ke
         row = next;
     }
     __syncthreads();
-    for (int a = threadIdx.x; a < C; a += blockDim.x) {
-        float sg = 0.f, sb = 0.f;
+    for (int a = threadIdx.x; a < np * C; a += blockDim.x) {
+        float sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < LN_BWD_WARPS; k++) {
-            sg += sh[(size_t)k * 2 * C + a];
-            sb += sh[(size_t)k * 2 * C + C + a];
-        }
-        const int c = (a % cv) * 8 + a / cv;
-        partial[(size_t)blockIdx.x * 2 * C + c] = sg;
-        partial[(size_t)blockIdx.x * 2 * C + C + c] = sb;
+        for (int k = 0; k < LN_BWD_WARPS; k++) sum += sh[(size_t)k * np * C + a];
+        const int q = a / C, e = a % C;  // which array; element within it
+        const int c = (e % cv) * 8 + e / cv;
+        partial[(size_t)blockIdx.x * np * C + (size_t)q * C + c] = sum;
     }
+}
+
+// The same backward for C <= 1024 (VPL <= 4), arranged for memory-level
+// parallelism: each warp keeps a ring of LN_STAGES row slots in shared memory
+// that cp.async fills (x, dy, the residual gradient when accumulating, mean,
+// rstd), LN_STAGES - 1 rows ahead of the row it computes. A lane copies and
+// reads only its own 16-byte pieces of a row (plus lane 0's mean and rstd,
+// read after a warp barrier). The per-column sums are register accumulators
+// of the lane that owns the column; at the end the warps' sums go through
+// shared memory and are added in warp order into partial[block].
+#define LN_STAGES 3
+#define LN_STAGED_MAX_ROW_BYTES 2048  // rows of up to 1024 bf16 or 512 fp32 values
+template <typename T, int VPL>
+__global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
+    ln_bwd_staged_kernel(T* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
+                         const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+                         const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C) {
+    extern __shared__ __align__(16) uint8_t sm_raw[];
+    constexpr int PIECES = (int)sizeof(T) / 2;  // 16-byte copies per 8-element vector
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int cv = C / 8;
+    const size_t row_bytes = (size_t)C * sizeof(T);
+    const size_t slot_bytes = 3 * row_bytes + 16;  // x | dy | residual gradient | mean, rstd
+    uint8_t* ring = sm_raw + (size_t)w * LN_STAGES * slot_bytes;
+    const int stride = gridDim.x * LN_BWD_WARPS;
+    const int row0 = blockIdx.x * LN_BWD_WARPS + w;
+
+    auto issue = [&](int row, int slot) {
+        if (row < N) {
+            uint8_t* sb = ring + (size_t)slot * slot_bytes;
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int idx = lane + 32 * i;
+                if (idx < cv) {
+#pragma unroll
+                    for (int p = 0; p < PIECES; p++) {
+                        const size_t off = (size_t)idx * 8 * sizeof(T) + p * 16;
+                        const size_t goff = ((size_t)row * C + idx * 8) * sizeof(T) + p * 16;
+                        cp_async16(sb + off, (const uint8_t*)x + goff);
+                        cp_async16(sb + row_bytes + off, (const uint8_t*)dy + goff);
+                        if (accumulate) cp_async16(sb + 2 * row_bytes + off, (const uint8_t*)out + goff);
+                    }
+                }
+            }
+            if (lane == 0) {
+                cp_async4(sb + 3 * row_bytes, mean + row);
+                cp_async4(sb + 3 * row_bytes + 4, rstd + row);
+            }
+        }
+        cp_async_commit();  // one group per row slot, empty past the end
+    };
+
+    float ag[VPL][8], ab[VPL][8], ao[VPL][8];
+#pragma unroll
+    for (int i = 0; i < VPL; i++)
+#pragma unroll
+        for (int j = 0; j < 8; j++) ag[i][j] = ab[i][j] = ao[i][j] = 0.f;
+
+#pragma unroll
+    for (int k = 0; k < LN_STAGES - 1; k++) issue(row0 + k * stride, k);
+    int slot = 0;
+    for (int row = row0; row < N; row += stride) {
+        // refill the slot read in the previous iteration (all lanes are done with it)
+        __syncwarp();
+        issue(row + (LN_STAGES - 1) * stride, (slot + LN_STAGES - 1) % LN_STAGES);
+        cp_async_wait<LN_STAGES - 1>();  // this row's group has landed
+        __syncwarp();                     // ... for every lane (mean and rstd come from lane 0)
+        const uint8_t* sb = ring + (size_t)slot * slot_bytes;
+        const T* sx = reinterpret_cast<const T*>(sb);
+        const T* sdy = reinterpret_cast<const T*>(sb + row_bytes);
+        const T* sres = reinterpret_cast<const T*>(sb + 2 * row_bytes);
+        const float mu = reinterpret_cast<const float*>(sb + 3 * row_bytes)[0];
+        const float rs = reinterpret_cast<const float*>(sb + 3 * row_bytes)[1];
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                float xv[8], dv[8], g[8];
+                load8(sx + idx * 8, xv);
+                load8(sdy + idx * 8, dv);
+                load8(gamma + idx * 8, g);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float xh = (xv[j] - mu) * rs;
+                    ag[i][j] += dv[j] * xh;
+                    ab[i][j] += dv[j];
+                    const float dh = dv[j] * g[j];
+                    s1 += dh;
+                    s2 += dh * xh;
+                }
+            }
+        }
+        const float m1 = warp_sum(s1) / (float)C;
+        const float m2 = warp_sum(s2) / (float)C;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                float xv[8], dv[8], g[8], o[8];
+                load8(sx + idx * 8, xv);
+                load8(sdy + idx * 8, dv);
+                load8(gamma + idx * 8, g);
+#pragma unroll
+                for (int j = 0; j < 8; j++) o[j] = rs * (dv[j] * g[j] - m1 - (xv[j] - mu) * rs * m2);
+                if (accumulate) {
+                    float rv[8];
+                    load8(sres + idx * 8, rv);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) o[j] += rv[j];
+                }
+                store8(out + (int64_t)row * C + idx * 8, o);
+                if (np == 3) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) ao[i][j] += to_float(from_float<T>(o[j]));
+                }
+            }
+        }
+        slot = (slot + 1) % LN_STAGES;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    // the warps' column sums, [warp][np][C] over the ring's memory, then summed in warp order
+    float* red = reinterpret_cast<float*>(sm_raw);
+#pragma unroll
+    for (int i = 0; i < VPL; i++) {
+        const int idx = lane + 32 * i;
+        if (idx < cv) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                float* r = red + (size_t)w * np * C + idx * 8 + j;
+                r[0] = ag[i][j];
+                r[C] = ab[i][j];
+                if (np == 3) r[2 * C] = ao[i][j];
+            }
+        }
+    }
+    __syncthreads();
+    for (int a = threadIdx.x; a < np * C; a += blockDim.x) {
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < LN_BWD_WARPS; k++) sum += red[(size_t)k * np * C + a];
+        partial[(size_t)blockIdx.x * np * C + a] = sum;
+    }
+}
+
+static size_t ln_staged_smem(int dtype, int C) {
+    const size_t es = dtype == GPT2_MODE_BF16 ? 2 : 4;
+    return (size_t)LN_BWD_WARPS * LN_STAGES * (3 * C * es + 16);
 }
 
 static int ln_vpl(int C) { return (C / 8 + 31) / 32; }
@@ -182,22 +351,34 @@ static int ln_vpl(int C) { return (C / 8 + 31) / 32; }
         default: CALL(8); break; \
     }
 
-int launch_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
-                             const void* beta, int N, int C, cudaStream_t s) {
+static int ln_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x, const void* r,
+                      const void* gamma, const void* beta, int N, int C, cudaStream_t s) {
     const int blocks = (N + LN_FWD_WARPS - 1) / LN_FWD_WARPS;
     if (blocks == 0) return 0;
-#define LN_FWD_CALL(V)                                                                                       \
-    if (dtype == GPT2_MODE_BF16)                                                                             \
-        ln_fwd_kernel<bf16, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((bf16*)y, mean, rstd, (const bf16*)x,    \
-                                                                    (const bf16*)gamma, (const bf16*)beta, N, \
-                                                                    C);                                      \
-    else                                                                                                     \
-        ln_fwd_kernel<float, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((float*)y, mean, rstd, (const float*)x, \
-                                                                     (const float*)gamma, (const float*)beta, \
-                                                                     N, C);
+#define LN_FWD_CALL(V)                                                                                            \
+    if (dtype == GPT2_MODE_BF16)                                                                                  \
+        ln_fwd_kernel<bf16, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((bf16*)y, mean, rstd, (bf16*)xsum,            \
+                                                                    (const bf16*)x, (const bf16*)r,               \
+                                                                    (const bf16*)gamma, (const bf16*)beta, N, C); \
+    else                                                                                                          \
+        ln_fwd_kernel<float, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((float*)y, mean, rstd, (float*)xsum,         \
+                                                                     (const float*)x, (const float*)r,            \
+                                                                     (const float*)gamma, (const float*)beta, N,  \
+                                                                     C);
     LN_DISPATCH(ln_vpl(C), LN_FWD_CALL)
 #undef LN_FWD_CALL
     return 1;
+}
+
+int launch_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                             const void* beta, int N, int C, cudaStream_t s) {
+    return ln_forward(dtype, y, mean, rstd, nullptr, x, nullptr, gamma, beta, N, C, s);
+}
+
+int launch_residual_layernorm_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x,
+                                      const void* r, const void* gamma, const void* beta, int N, int C,
+                                      cudaStream_t s) {
+    return ln_forward(dtype, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s);
 }
 
 static int ln_bwd_blocks(int N) {
@@ -205,34 +386,97 @@ static int ln_bwd_blocks(int N) {
     return b < LN_BWD_MAX_BLOCKS ? (b < 1 ? 1 : b) : LN_BWD_MAX_BLOCKS;
 }
 
-size_t layernorm_backward_scratch(int N, int C) { return (size_t)ln_bwd_blocks(N) * 2 * C * 4; }
+// The staged kernel: two resident blocks per SM, every row of a block's
+// stride handled in one pass of the grid.
+static int ln_bwd_staged_blocks(int N) {
+    const int cap = 2 * gpt2_num_sms();
+    int b = (N + LN_BWD_WARPS - 1) / LN_BWD_WARPS;
+    return b < cap ? (b < 1 ? 1 : b) : cap;
+}
+
+size_t layernorm_backward_scratch(int N, int C) {
+    const int b = ln_bwd_blocks(N) > ln_bwd_staged_blocks(N) ? ln_bwd_blocks(N) : ln_bwd_staged_blocks(N);
+    return (size_t)b * 3 * C * 4;
+}
 
 template <typename T, int VPL>
-static void ln_bwd_launch(int blocks, size_t smem, void* dx, float* partial, const void* dy, const void* x,
-                          const void* gamma, const float* mean, const float* rstd, int N, int C, cudaStream_t s) {
+static void ln_bwd_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np, const void* dy,
+                          const void* x, const void* gamma, const float* mean, const float* rstd, int N, int C,
+                          cudaStream_t s) {
     static bool configured = false;  // per instantiation: allow > 48 KB dynamic smem once
     if (!configured) {
         cudaFuncSetAttribute(ln_bwd_kernel<T, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LN_BWD_WARPS * 2 * 2048 * 4);
+                             LN_BWD_WARPS * 3 * 2048 * 4);
         configured = true;
     }
-    ln_bwd_kernel<T, VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((T*)dx, partial, (const T*)dy, (const T*)x,
-                                                                  (const T*)gamma, mean, rstd, N, C);
+    ln_bwd_kernel<T, VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((T*)out, accumulate, partial, np, (const T*)dy,
+                                                                  (const T*)x, (const T*)gamma, mean, rstd, N, C);
+}
+
+template <typename T, int VPL>
+static void ln_bwd_staged_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np,
+                                 const void* dy, const void* x, const void* gamma, const float* mean,
+                                 const float* rstd, int N, int C, cudaStream_t s) {
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(ln_bwd_staged_kernel<T, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16));
+        configured = true;
+    }
+    ln_bwd_staged_kernel<T, VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>(
+        (T*)out, accumulate, partial, np, (const T*)dy, (const T*)x, (const T*)gamma, mean, rstd, N, C);
+}
+
+static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, float* dbeta, float* dout_colsum,
+                       const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, int N,
+                       int C, void* scratch, cudaStream_t s) {
+    const int np = dout_colsum ? 3 : 2;
+    float* partial_s = (float*)scratch;
+    if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
+        // 111 KB of ring per block at C = 768 bf16, two blocks per SM
+        const int blocks = ln_bwd_staged_blocks(N);
+        const size_t smem = ln_staged_smem(dtype, C);
+#define LN_BWD_STAGED_CALL(V)                                                                                   \
+    if (dtype == GPT2_MODE_BF16)                                                                                \
+        ln_bwd_staged_launch<bf16, V>(blocks, smem, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd, N, \
+                                      C, s);                                                                    \
+    else                                                                                                        \
+        ln_bwd_staged_launch<float, V>(blocks, smem, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd,  \
+                                       N, C, s);
+        switch (ln_vpl(C)) {
+            case 1: LN_BWD_STAGED_CALL(1); break;
+            case 2: LN_BWD_STAGED_CALL(2); break;
+            case 3: LN_BWD_STAGED_CALL(3); break;
+            default: LN_BWD_STAGED_CALL(4); break;
+        }
+#undef LN_BWD_STAGED_CALL
+        launch_colsum3(dgamma, dbeta, dout_colsum, C, partial_s, blocks, np * C, s);
+        return 2;
+    }
+    const int blocks = ln_bwd_blocks(N);
+    const size_t smem = (size_t)LN_BWD_WARPS * np * C * 4;
+    float* partial = (float*)scratch;
+#define LN_BWD_CALL(V)                                                                                           \
+    if (dtype == GPT2_MODE_BF16)                                                                                 \
+        ln_bwd_launch<bf16, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);  \
+    else                                                                                                         \
+        ln_bwd_launch<float, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);
+    LN_DISPATCH(ln_vpl(C), LN_BWD_CALL)
+#undef LN_BWD_CALL
+    launch_colsum3(dgamma, dbeta, dout_colsum, C, partial, blocks, np * C, s);
+    return 2;
 }
 
 int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                               const void* gamma, const float* mean, const float* rstd, int N, int C, void* scratch,
                               cudaStream_t s) {
-    const int blocks = ln_bwd_blocks(N);
-    const size_t smem = (size_t)LN_BWD_WARPS * 2 * C * 4;
-    float* partial = (float*)scratch;
-#define LN_BWD_CALL(V)                                                                                     \
-    if (dtype == GPT2_MODE_BF16)                                                                           \
-        ln_bwd_launch<bf16, V>(blocks, smem, dx, partial, dy, x, gamma, mean, rstd, N, C, s);             \
-    else                                                                                                   \
-        ln_bwd_launch<float, V>(blocks, smem, dx, partial, dy, x, gamma, mean, rstd, N, C, s);
-    LN_DISPATCH(ln_vpl(C), LN_BWD_CALL)
-#undef LN_BWD_CALL
-    launch_colsum(dgamma, dbeta, C, partial, blocks, 2 * C, s);
-    return 2;
+    return ln_backward(dtype, dx, false, dgamma, dbeta, nullptr, dy, x, gamma, mean, rstd, N, C, scratch, s);
+}
+
+int launch_layernorm_backward_residual(int dtype, void* dres, int accumulate, float* dgamma, float* dbeta,
+                                       float* dres_colsum, const void* dy, const void* x, const void* gamma,
+                                       const float* mean, const float* rstd, int N, int C, void* scratch,
+                                       cudaStream_t s) {
+    return ln_backward(dtype, dres, accumulate != 0, dgamma, dbeta, dres_colsum, dy, x, gamma, mean, rstd, N, C,
+                       scratch, s);
 }

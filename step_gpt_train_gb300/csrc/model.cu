@@ -65,7 +65,7 @@ struct gpt2 {
     std::vector<LayerBufs> layers;
     void *xL, *lnf, *logits, *fwd_tmp;
     float *meanf, *rstdf, *losses;
-    void *dres, *dtmp, *dtmp2, *dbig, *dqkv;
+    void *dres, *dtmp, *dbig, *dqkv;
     void* scratch;
     size_t scratch_bytes;
     int B, T;
@@ -181,7 +181,6 @@ size_t plan(const gpt2_config* c, gpt2* m) {
     const size_t o_fwd_tmp = take(BT * C * act);
     const size_t o_dres = take(BT * C * act);
     const size_t o_dtmp = take(BT * C * act);
-    const size_t o_dtmp2 = take(BT * C * act);
     const size_t o_dbig = take(BT * 4 * C * act);
     const size_t o_dqkv = take(BT * 3 * C * act);
     // scratch: the largest need of any scratch-using op of the backward
@@ -232,7 +231,6 @@ size_t plan(const gpt2_config* c, gpt2* m) {
         m->fwd_tmp = w + o_fwd_tmp;
         m->dres = w + o_dres;
         m->dtmp = w + o_dtmp;
-        m->dtmp2 = w + o_dtmp2;
         m->dbig = w + o_dbig;
         m->dqkv = w + o_dqkv;
         m->scratch = w + o_scratch;
@@ -375,21 +373,24 @@ int ln_fwd(gpt2* m, void* y, float* mean, float* rstd, const void* x, int gi, in
                    (double)BT * (2.0 * m->C * m->act + 8));
 }
 
-int ln_bwd(gpt2* m, void* dx, const void* dy, const void* x, int gi, const float* mean, const float* rstd, int BT) {
+// Residual join then LayerNorm: xsum = x + r; y = LN(xsum) with the norm at gi.
+int res_ln_fwd(gpt2* m, void* y, float* mean, float* rstd, void* xsum, const void* x, const void* r, int gi, int BT) {
+    Op op(m, GPT2_K_LAYERNORM_FWD);
+    return op.done(launch_residual_layernorm_forward(m->dtype, y, mean, rstd, xsum, x, r, P(m, gi), P(m, gi + 1), BT,
+                                                     m->C, m->stream),
+                   (double)BT * (4.0 * m->C * m->act + 8));
+}
+
+// LayerNorm backward into the residual gradient: dres (+)= dx; the column sums
+// of the new dres go to the bias gradient bi (when bi >= 0): the bias of the
+// linear layer whose output joins the residual stream at this point.
+int ln_bwd_res(gpt2* m, int accumulate, const void* dy, const void* x, int gi, const float* mean, const float* rstd,
+               int bi, int BT) {
     Op op(m, GPT2_K_LAYERNORM_BWD);
-    return op.done(launch_layernorm_backward(m->dtype, dx, G(m, gi), G(m, gi + 1), dy, x, P(m, gi), mean, rstd, BT,
-                                             m->C, m->scratch, m->stream),
-                   (double)BT * (3.0 * m->C * m->act + 8));
-}
-
-int residual_fwd(gpt2* m, void* out, const void* a, const void* b, int64_t n) {
-    Op op(m, GPT2_K_RESIDUAL_FWD);
-    return op.done(launch_residual_forward(m->dtype, out, a, b, n, m->stream), 3.0 * n * m->act);
-}
-
-int residual_bwd(gpt2* m, void* dres, const void* dbranch, int64_t n) {
-    Op op(m, GPT2_K_RESIDUAL_BWD);
-    return op.done(launch_residual_backward(m->dtype, dres, dbranch, n, m->stream), 3.0 * n * m->act);
+    return op.done(launch_layernorm_backward_residual(m->dtype, m->dres, accumulate, G(m, gi), G(m, gi + 1),
+                                                      bi >= 0 ? G(m, bi) : nullptr, dy, x, P(m, gi), mean, rstd, BT,
+                                                      m->C, m->scratch, m->stream),
+                   (double)BT * ((3.0 + accumulate) * m->C * m->act + 8));
 }
 
 double attn_fwd_flops(int B, int T, int C) { return 2.0 * 2.0 * B * C * (double)T * (T + 1) / 2.0; }
@@ -402,10 +403,10 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
                                            m->V, m->status, m->stream),
                     (double)BT * (3.0 * C * m->act + 4)));
     }
+    // each residual join is fused with the LayerNorm that reads its result
+    TRY(ln_fwd(m, m->layers[0].ln1, m->layers[0].mean1, m->layers[0].rstd1, m->layers[0].x, tidx(0, 0), BT));
     for (int l = 0; l < L; l++) {
         LayerBufs& b = m->layers[l];
-        void* xnext = l + 1 < L ? m->layers[l + 1].x : m->xL;
-        TRY(ln_fwd(m, b.ln1, b.mean1, b.rstd1, b.x, tidx(l, 0), BT));
         TRY(linear_fwd(m, b.qkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
         {
             Op op(m, GPT2_K_ATTENTION_FWD);
@@ -413,8 +414,7 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
                         attn_fwd_flops(B, T, C)));
         }
         TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
-        TRY(residual_fwd(m, b.x1, b.x, m->fwd_tmp, (int64_t)BT * C));
-        TRY(ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, tidx(l, 6), BT));
+        TRY(res_ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, b.x, m->fwd_tmp, tidx(l, 6), BT));
         TRY(linear_fwd(m, b.fch, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
         {
             Op op(m, GPT2_K_GELU_FWD);
@@ -422,9 +422,13 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
                         2.0 * BT * 4 * C * m->act));
         }
         TRY(linear_fwd(m, m->fwd_tmp, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
-        TRY(residual_fwd(m, xnext, b.x1, m->fwd_tmp, (int64_t)BT * C));
+        if (l + 1 < L) {
+            LayerBufs& n = m->layers[l + 1];
+            TRY(res_ln_fwd(m, n.ln1, n.mean1, n.rstd1, n.x, b.x1, m->fwd_tmp, tidx(l + 1, 0), BT));
+        } else {
+            TRY(res_ln_fwd(m, m->lnf, m->meanf, m->rstdf, m->xL, b.x1, m->fwd_tmp, tlnf(L, 0), BT));
+        }
     }
-    TRY(ln_fwd(m, m->lnf, m->meanf, m->rstdf, m->xL, tlnf(L, 0), BT));
     TRY(op_matmul(m, m->logits, 0, m->lnf, 0, P(m, T_WTE), 0, nullptr, BT, m->Vp, C));
     if (targets) {
         {
@@ -444,21 +448,22 @@ int backward_impl(gpt2* m) {
     // LM head (tied with wte): dlnf = dlogits wte; dwte = dlogits^T lnf (overwrites dwte)
     TRY(op_matmul(m, m->dtmp, 0, m->logits, 0, P(m, T_WTE), 1, nullptr, BT, C, m->Vp));
     TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT));
-    TRY(ln_bwd(m, m->dres, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, BT));
+    // the LayerNorm backwards write the residual gradient dres and, on the
+    // way, the bias gradient of the projection whose output joins there
+    TRY(ln_bwd_res(m, 0, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, tidx(L - 1, 11), BT));
     for (int l = L - 1; l >= 0; l--) {
         LayerBufs& b = m->layers[l];
         // MLP branch
-        TRY(linear_bwd(m, m->dbig, m->dres, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
+        TRY(linear_bwd(m, m->dbig, m->dres, b.fchg, tidx(l, 10), -1, BT, 4 * C, C));
         {
             Op op(m, GPT2_K_GELU_BWD);
             TRY(op.done(launch_gelu_backward(m->dtype, m->dbig, b.fch, m->dbig, (int64_t)BT * 4 * C, m->stream),
                         3.0 * BT * 4 * C * m->act));
         }
         TRY(linear_bwd(m, m->dtmp, m->dbig, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
-        TRY(ln_bwd(m, m->dtmp2, m->dtmp, b.x1, tidx(l, 6), b.mean2, b.rstd2, BT));
-        TRY(residual_bwd(m, m->dres, m->dtmp2, (int64_t)BT * C));
+        TRY(ln_bwd_res(m, 1, m->dtmp, b.x1, tidx(l, 6), b.mean2, b.rstd2, tidx(l, 5), BT));
         // attention branch
-        TRY(linear_bwd(m, m->dtmp, m->dres, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
+        TRY(linear_bwd(m, m->dtmp, m->dres, b.atty, tidx(l, 4), -1, BT, C, C));
         {
             Op op(m, GPT2_K_ATTENTION_BWD);
             TRY(op.done(launch_attention_backward(m->dtype, m->dqkv, m->dtmp, b.qkv, b.atty, b.lse, B, T, C, m->H,
@@ -466,8 +471,7 @@ int backward_impl(gpt2* m) {
                         2.5 * attn_fwd_flops(B, T, C)));
         }
         TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
-        TRY(ln_bwd(m, m->dtmp2, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, BT));
-        TRY(residual_bwd(m, m->dres, m->dtmp2, (int64_t)BT * C));
+        TRY(ln_bwd_res(m, 1, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, l > 0 ? tidx(l - 1, 11) : -1, BT));
     }
     if (T < m->maxT &&
         cudaMemsetAsync(G(m, T_WPE) + (size_t)T * C, 0, (size_t)(m->maxT - T) * C * 4, m->stream) != cudaSuccess)

@@ -66,6 +66,29 @@ int gpt2_op_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta,
                                             st(stream)));
 }
 
+int gpt2_op_residual_layernorm_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x,
+                                       const void* r, const void* gamma, const void* beta, int N, int C,
+                                       void* stream) {
+    if (!dt_ok(dtype) || !y || !mean || !rstd || !xsum || !x || !r || !gamma || !beta || N < 0 || C <= 0 ||
+        C % 8 || C > 2048)
+        return GPT2_ERR_ARG;
+    if (!al16(y) || !al16(xsum) || !al16(x) || !al16(r) || !al16(gamma) || !al16(beta)) return GPT2_ERR_ARG;
+    return finish(launch_residual_layernorm_forward(dtype, y, mean, rstd, xsum, x, r, gamma, beta, N, C, st(stream)));
+}
+
+int gpt2_op_layernorm_backward_residual(int dtype, void* dres, int accumulate, float* dgamma, float* dbeta,
+                                        float* dres_colsum, const void* dy, const void* x, const void* gamma,
+                                        const float* mean, const float* rstd, int N, int C, void* scratch,
+                                        size_t scratch_bytes, void* stream) {
+    if (!dt_ok(dtype) || !dres || !dgamma || !dbeta || !dy || !x || !gamma || !mean || !rstd || N < 0 || C <= 0 ||
+        C % 8 || C > 2048 || (accumulate != 0 && accumulate != 1))
+        return GPT2_ERR_ARG;
+    if (!scratch || scratch_bytes < layernorm_backward_scratch(N, C)) return GPT2_ERR_WORKSPACE;
+    if (!al16(dres) || !al16(dy) || !al16(x) || !al16(gamma)) return GPT2_ERR_ARG;
+    return finish(launch_layernorm_backward_residual(dtype, dres, accumulate, dgamma, dbeta, dres_colsum, dy, x, gamma,
+                                                     mean, rstd, N, C, scratch, st(stream)));
+}
+
 size_t gpt2_op_matmul_scratch(int dtype, int M, int N, int K, int d_fp32) {
     if (!dt_ok(dtype) || M < 0 || N < 0 || K < 0) return 0;
     return matmul_scratch(dtype, M, N, K, d_fp32);

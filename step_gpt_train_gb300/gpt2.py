@@ -77,6 +77,11 @@ _SIGNATURES = {
     "gpt2_op_layernorm_backward_scratch": (c_size_t, [c_int, c_int]),
     "gpt2_op_layernorm_backward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                            c_void_p, c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "gpt2_op_residual_layernorm_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                   c_void_p, c_void_p, c_int, c_int, c_void_p]),
+    "gpt2_op_layernorm_backward_residual": (c_int, [c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                    c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p,
+                                                    c_size_t, c_void_p]),
     "gpt2_op_matmul_scratch": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "gpt2_op_matmul": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
                                c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -323,6 +328,25 @@ def gpt2_op_layernorm_backward(dx, dgamma, dbeta, dy, x, gamma, mean, rstd, stre
     check(lib.gpt2_op_layernorm_backward(_dtype_of(x), _p(dx), _p(dgamma), _p(dbeta), _p(dy), _p(x), _p(gamma),
                                          _p(mean), _p(rstd), N, C, _p(sc), sc.numel(), _s(stream)),
           "gpt2_op_layernorm_backward")
+    return sc
+
+
+def gpt2_op_residual_layernorm_forward(y, mean, rstd, xsum, x, r, gamma, beta, stream=None):
+    N, C = x.shape
+    check(load_library().gpt2_op_residual_layernorm_forward(_dtype_of(x), _p(y), _p(mean), _p(rstd), _p(xsum), _p(x),
+                                                            _p(r), _p(gamma), _p(beta), N, C, _s(stream)),
+          "gpt2_op_residual_layernorm_forward")
+
+
+def gpt2_op_layernorm_backward_residual(dres, accumulate, dgamma, dbeta, dres_colsum, dy, x, gamma, mean, rstd,
+                                        stream=None):
+    N, C = x.shape
+    lib = load_library()
+    sc = _scratch(lib.gpt2_op_layernorm_backward_scratch(N, C))
+    check(lib.gpt2_op_layernorm_backward_residual(_dtype_of(x), _p(dres), int(accumulate), _p(dgamma), _p(dbeta),
+                                                  _p(dres_colsum), _p(dy), _p(x), _p(gamma), _p(mean), _p(rstd), N,
+                                                  C, _p(sc), sc.numel(), _s(stream)),
+          "gpt2_op_layernorm_backward_residual")
     return sc
 
 

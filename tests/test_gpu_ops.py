@@ -13,7 +13,7 @@ import pytest
 
 from oracle import gpt2_ref as R
 from step_gpt_train_gb300 import data
-from tests._gpu_util import (BF16_REL, assert_close, dev, dev_f32, host, inputs, rel_l2)
+from tests._gpu_util import (BF16_REL, assert_close, dev, dev_f32, host, inputs, rel_l2, torch_dtype)
 
 pytestmark = pytest.mark.gpu
 
@@ -146,6 +146,57 @@ def test_layernorm(torch_cuda, mode, C):
     assert_close(host(dx), rdx, 2 * tol, atol_frac=2e-3 if mode == 1 else 1e-6, what="dx")
     assert_close(host(dgam), rdg, 1e-4, atol_frac=1e-5, what="dgamma")
     assert_close(host(dbet), rdb, 1e-4, atol_frac=1e-5, what="dbeta")
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("C", [64, 768])
+@pytest.mark.parametrize("accumulate", [0, 1])
+def test_residual_layernorm(torch_cuda, mode, C, accumulate):
+    """Residual join + LayerNorm forward, and LayerNorm backward into the residual
+    gradient with the column sums of the result (the projection bias gradient)."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import (gpt2_op_layernorm_backward_residual,
+                                           gpt2_op_residual_layernorm_forward)
+    N = 4133  # several grid strides of the backward and a ragged tail
+    x = inputs(30, (N, C), 2.0, mode)
+    r = inputs(31, (N, C), 1.0, mode)
+    g = inputs(32, (C,), 1.0, mode)
+    b = inputs(33, (C,), 1.0, mode)
+    dy = inputs(34, (N, C), 1.0, mode)
+    dres0 = inputs(35, (N, C), 1.0, mode)
+    g_, b_ = dev(g, mode), dev(b, mode)
+    xsum = torch.empty(N, C, dtype=torch_dtype(mode), device="cuda")
+    y = torch.empty_like(xsum)
+    mean = torch.empty(N, device="cuda")
+    rstd = torch.empty(N, device="cuda")
+    gpt2_op_residual_layernorm_forward(y, mean, rstd, xsum, dev(x, mode), dev(r, mode), g_, b_)
+    dres = dev(dres0, mode)
+    dgam = torch.full((C,), float("nan"), device="cuda")
+    dbet = torch.full((C,), float("nan"), device="cuda")
+    dbias = torch.full((C,), float("nan"), device="cuda")
+    gpt2_op_layernorm_backward_residual(dres, accumulate, dgam, dbet, dbias, dev(dy, mode), xsum, g_, mean, rstd)
+    torch.cuda.synchronize()
+    # the sum of two bf16 (or fp32) values, rounded once to the storage type
+    s64 = x.astype(np.float64) + r.astype(np.float64)
+    s_ref = data.round_to_bf16(s64.astype(np.float32)) if mode == 1 else s64.astype(np.float32)
+    assert np.array_equal(host(xsum), s_ref.astype(np.float64)), "residual sum"
+    sx = s_ref.astype(np.float64)
+    ry, rmean, rrstd = R.layernorm_forward(sx, g.astype(np.float64), b.astype(np.float64))
+    rdx, rdg, rdb = R.layernorm_backward(dy.astype(np.float64), sx, g.astype(np.float64), rmean, rrstd)
+    tol = BF16_REL if mode == 1 else 1e-5
+    assert_close(host(y), ry, tol, atol_frac=1e-3 if mode == 1 else 1e-6, what="y")
+    rres = rdx + (dres0.astype(np.float64) if accumulate else 0.0)
+    assert_close(host(dres), rres, 2 * tol, atol_frac=2e-3 if mode == 1 else 1e-6, what="dres")
+    assert_close(host(dgam), rdg, 1e-4, atol_frac=1e-5, what="dgamma")
+    assert_close(host(dbet), rdb, 1e-4, atol_frac=1e-5, what="dbeta")
+    # column sums of what was stored (fp32 accumulation of N terms) ...
+    assert_close(host(dbias), host(dres).sum(axis=0), 1e-5, atol=N * 2.0 ** -23 * float(np.abs(host(dres)).max()),
+                 what="dres column sums")
+    # ... and of the exact result: at most the sum over rows of the per-element
+    # bounds checked above
+    rms = float(np.sqrt(np.mean(rres * rres)))
+    col_bound = (2 * tol * np.abs(rres) + (2e-3 if mode == 1 else 1e-6) * rms).sum(axis=0)
+    assert np.all(np.abs(host(dbias) - rres.sum(axis=0)) <= col_bound * 1.001), "dres column sums vs oracle"
 
 
 @pytest.mark.parametrize("mode", [1, 0])
