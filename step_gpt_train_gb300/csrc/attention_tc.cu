@@ -315,7 +315,8 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
 
 // =============================================================================
 // Attention backward on tcgen05 (bf16, head size 64), two deterministic
-// kernels: one per 128-key tile (dK, dV) and one per 128-query tile (dQ).
+// kernels: dK, dV with a 128-key tile as the work item, and dQ with a
+// 128-query tile.
 // Every output element has one writer; no atomics.
 //
 // dK/dV kernel, for each 128-query block i at or after the key tile:
@@ -326,28 +327,41 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
 // dQ kernel, for each 128-key block j at or before the query tile:
 //   S = Q K_j^T, dP = dO V_j^T, P, dS as above (rows = queries),
 //   dQ += dS K_j;  dK and dQ are scaled by 1/sqrt(hd) at the end.
-// P^T and dS^T (dS) are written to shared memory as bf16 in the MMA's K-major
-// 128-byte swizzled layout; the accumulators stay in TMEM until the end.
+// P^T and dS^T (dS) go back into tensor memory as bf16 pairs (tcgen05.st),
+// and the dV, dK and dQ products read them from there as their A operand, so
+// the only shared-memory operands are the Q, dO, K and V tiles the TMA loads.
 //
-// Warps: 0 TMA producer (lane 0) and, in the dK/dV kernel, all lanes stage
-// each block's log-sum-exp and D into shared memory; 1 MMA issuer; 2..9
-// elementwise (warp w serves TMEM lanes 32*(w%4).. and half of the 128
-// columns). One CTA per SM (512 TMEM columns).
+// Both are persistent (one CTA per SM walking a list of (tile, batch-head)
+// items, longest first), so the operand rings and the MMA / elementwise
+// hand-offs carry on across items; an item's accumulators go from TMEM to
+// global memory while the next item's first products are computed.
+// Warps: 0 TMA producer (lane 0); 1 MMA issuer; 2..17
+// elementwise (warp w serves TMEM lanes 32*(w%4).. and one quarter, 32, of
+// the 128 columns: four warps per scheduler, so that the exp / multiply
+// chains of one warp hide the latencies of the others). One CTA per SM (512
+// TMEM columns).
 // =============================================================================
 
 namespace {
 
-constexpr int BW_THREADS = 320;
-constexpr int BW_EW = 8;     // elementwise warps
-constexpr int DKDV_ST = 3;   // Q/dO (and lse/D) stages of the dK/dV kernel
-constexpr int DQ_ST = 4;     // K/V stages of the dQ kernel
+constexpr int BW_EW = 16;                   // elementwise warps
+constexpr int BW_THREADS = 64 + 32 * BW_EW;  // + producer and MMA warps
+constexpr int EW_COLS = 32;                 // columns of a 128-wide tile per elementwise thread
+constexpr int DKDV_ST = 5;   // Q/dO stages of the dK/dV kernel
+constexpr int DQ_ST = 5;     // K/V stages of the dQ kernel
+// TMEM columns. dK/dV kernel: S^T, dP^T (fp32), dV, dK (fp32), P^T, dS^T
+// (bf16 pairs: 128 queries in 64 columns).
+constexpr uint32_t KV_S = 0, KV_DP = 128, KV_DV = 256, KV_DK = 320, KV_P = 384, KV_DS = 448;
+// dQ kernel: S, dP (fp32), dQ (fp32), dS (bf16 pairs).
+constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256, Q_DS = 320;
 
 struct BwdArgs {
     bf16* dqkv;          // [B*T, 3C]
     const float* lse;    // [B, H, T]
     const float* D;      // [B, H, T]
     int* status;
-    int T, C, H;
+    int B, T, C, H;
+    int nqt;             // 128-row tiles per sequence
     float scale_log2;    // log2(e) / sqrt(hd)
     float scale;         // 1 / sqrt(hd)
 };
@@ -363,23 +377,62 @@ __device__ __forceinline__ void store32_bf16(bf16* dst, const uint32_t (&v)[32],
     }
 }
 
-// Write this thread's 64 bf16 values (row r, columns half*64 .. +63) into a
-// [128][128] K-major operand buffer (two 64-column chunks of 16 KB, 128-byte
-// swizzle: 16-byte unit u of row r at position u ^ (r & 7)).
-__device__ __forceinline__ void write_row64(uint8_t* buf, int r, int half, const uint32_t (&pk)[32]) {
-    uint8_t* row = buf + half * AT_TILE + r * 128;
-#pragma unroll
-    for (int u = 0; u < 8; u++)
-        *reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-}
-
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// -------------------------------------------------------------------------- schedule
+// Both kernels are persistent: CTA c takes the work items c, c + G, c + 2G, ...
+// (G = grid size) of a list ordered longest first, and its producer, MMA and
+// elementwise roles walk the same sequence of (item, block) steps, so the
+// operand rings run on across item boundaries instead of starting cold.
+struct Item {
+    int tile, bh, nblk;  // dK/dV: key tile, blocks tile..nqt-1; dQ: query tile, blocks 0..tile
+};
+
+template <bool DQ> __device__ __forceinline__ bool get_item(const BwdArgs& a, int i, Item& it) {
+    const int BH = a.B * a.H;
+    const int idx = blockIdx.x + i * gridDim.x;
+    if (idx >= a.nqt * BH) return false;
+    it.bh = idx % BH;
+    if (DQ) {
+        it.tile = a.nqt - 1 - idx / BH;
+        it.nblk = it.tile + 1;
+    } else {
+        it.tile = idx / BH;
+        it.nblk = a.nqt - it.tile;
+    }
+    return true;
+}
+
+// Position in a CTA's step sequence: item i, block n of it, step counter g.
+struct Cur {
+    int i, n, g;
+    bool valid;
+    Item it;
+};
+template <bool DQ> __device__ __forceinline__ Cur cur_first(const BwdArgs& a) {
+    Cur c;
+    c.i = 0;
+    c.n = 0;
+    c.g = 0;
+    c.valid = get_item<DQ>(a, 0, c.it);
+    return c;
+}
+template <bool DQ> __device__ __forceinline__ Cur cur_next(const BwdArgs& a, Cur c) {
+    c.g++;
+    if (++c.n >= c.it.nblk) {
+        c.i++;
+        c.n = 0;
+        c.valid = get_item<DQ>(a, c.i, c.it);
+    }
+    return c;
+}
+
 // -------------------------------------------------------------------------- dK, dV
+// Shared memory: K | V | DKDV_ST x (Q, dO) | per elementwise warp 64 floats
+// (its columns' lse and D) | barriers.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                             BwdArgs a) {
@@ -387,44 +440,35 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // K | V | DKDV_ST x (Q, dO) | P^T (2 chunks) | dS^T (2 chunks) | lse/D slots | barriers
     constexpr int NS = DKDV_ST;
     const uint32_t sK = base, sV = base + AT_TILE;
     auto sQ = [&](int st) { return base + (2 + 2 * st) * AT_TILE; };
     auto sO = [&](int st) { return base + (3 + 2 * st) * AT_TILE; };
-    const uint32_t sP = base + (2 + 2 * NS) * AT_TILE, sS = base + (4 + 2 * NS) * AT_TILE;
-    uint8_t* gP = gbase + (2 + 2 * NS) * AT_TILE;
-    uint8_t* gS = gbase + (4 + 2 * NS) * AT_TILE;
-    float* ldslot = reinterpret_cast<float*>(gbase + (6 + 2 * NS) * AT_TILE);  // [NS][256]: lse2[128], D[128]
-    const uint32_t bars = base + (6 + 2 * NS) * AT_TILE + NS * 1024;
-    uint8_t* bar_area = gbase + (6 + 2 * NS) * AT_TILE + NS * 1024;
-    const uint32_t kv_full = bars;
-    auto qd_full = [&](int i) { return bars + 8u * (1 + i); };
-    auto qd_empty = [&](int i) { return bars + 8u * (1 + NS + i); };
-    auto ld_full = [&](int i) { return bars + 8u * (1 + 2 * NS + i); };
-    auto ld_empty = [&](int i) { return bars + 8u * (1 + 3 * NS + i); };
-    const uint32_t bx = bars + 8u * (1 + 4 * NS);
+    float* ldslots = reinterpret_cast<float*>(gbase + (2 + 2 * NS) * AT_TILE);  // [BW_EW][64]
+    const uint32_t bars = base + (2 + 2 * NS) * AT_TILE + BW_EW * 256;
+    uint8_t* bar_area = gbase + (2 + 2 * NS) * AT_TILE + BW_EW * 256;
+    const uint32_t k_full = bars, k_empty = bars + 8u, v_full = bars + 16u, v_empty = bars + 24u;
+    auto qd_full = [&](int i) { return bars + 8u * (4 + i); };
+    auto qd_empty = [&](int i) { return bars + 8u * (4 + NS + i); };
+    const uint32_t bx = bars + 8u * (4 + 2 * NS);
     const uint32_t s_full = bx, s_free = bx + 8u;
     const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
     const uint32_t p_full = bx + 32u, p_free = bx + 40u;
     const uint32_t ds_full = bx + 48u, ds_free = bx + 56u;
-    const uint32_t o_done = bx + 64u, drain = bx + 72u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (1 + 4 * NS) + 80);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (1 + 4 * NS) + 84);
+    const uint32_t acc_full = bx + 64u, acc_empty = bx + 72u, drain = bx + 80u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (4 + 2 * NS) + 88);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (4 + 2 * NS) + 92);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int kt = blockIdx.x;  // key tile; the first tiles have the most query blocks
-    const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
-    const int nqt = (a.T + AT_M - 1) / AT_M;
-    const int nblk = nqt - kt;  // query blocks kt .. nqt-1
 
     if (threadIdx.x == 0) {
-        mbar_init(kv_full, 1);
+        mbar_init(k_full, 1);
+        mbar_init(k_empty, 1);
+        mbar_init(v_full, 1);
+        mbar_init(v_empty, 1);
         for (int i = 0; i < NS; i++) {
             mbar_init(qd_full(i), 1);
             mbar_init(qd_empty(i), 1);
-            mbar_init(ld_full(i), 1);
-            mbar_init(ld_empty(i), BW_EW);
         }
         mbar_init(s_full, 1);
         mbar_init(s_free, BW_EW);
@@ -434,7 +478,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(p_free, 1);
         mbar_init(ds_full, BW_EW);
         mbar_init(ds_free, 1);
-        mbar_init(o_done, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, BW_EW);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -444,47 +489,45 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;  // S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384)
+    const uint32_t tmem = *tmem_slot;  // columns KV_*
 
     if (warp == 0) {
-        // ------------------------------------------------------ producer
-        int qd_issued[NS];
-        for (int i = 0; i < NS; i++) qd_issued[i] = -1;
         if (lane == 0) {
-            mbar_expect_tx(kv_full, 2 * AT_TILE);
-            tma_load_3d(sK, &tm_qkv, kv_full, a.C + h * AT_HD, kt * AT_N, b);
-            tma_load_3d(sV, &tm_qkv, kv_full, 2 * a.C + h * AT_HD, kt * AT_N, b);
-        }
-        const float* lrow = a.lse + ((int64_t)b * a.H + h) * a.T;
-        const float* drow = a.D + ((int64_t)b * a.H + h) * a.T;
-        for (int n = 0; n < nblk; n++) {
-            const int st = n % NS;
-            const uint32_t ph = (n / NS) & 1;
-            const int q0 = (kt + n) * AT_M;
-            int ok = 1;
-            if (lane == 0) {
-                ok = mbar_wait(qd_empty(st), ph ^ 1u, abort_flag, a.status);
-                if (ok) {
+            // -------------------------------------------------- TMA producer
+            int qd_issued[NS];
+            for (int i = 0; i < NS; i++) qd_issued[i] = -1;
+            int k_items = 0, v_items = 0, g = 0;  // K and V loads issued (for the final drain)
+            bool ok = true;
+            for (int i = 0; ok; i++) {
+                Item it;
+                if (!get_item<false>(a, i, it)) break;
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                auto load_qd = [&](int n) -> bool {
+                    const int st = g % NS;
+                    const uint32_t ph = (g / NS) & 1;
+                    if (!mbar_wait(qd_empty(st), ph ^ 1u, abort_flag, a.status)) return false;
                     mbar_expect_tx(qd_full(st), 2 * AT_TILE);
-                    tma_load_3d(sQ(st), &tm_qkv, qd_full(st), h * AT_HD, q0, b);
-                    tma_load_3d(sO(st), &tm_do, qd_full(st), h * AT_HD, q0, b);
+                    tma_load_3d(sQ(st), &tm_qkv, qd_full(st), h * AT_HD, (it.tile + n) * AT_M, b);
+                    tma_load_3d(sO(st), &tm_do, qd_full(st), h * AT_HD, (it.tile + n) * AT_M, b);
                     qd_issued[st] = (int)ph;
-                }
+                    g++;
+                    return true;
+                };
+                // the item's first Q/dO block, then its K and V (once the previous
+                // item's last S^T and dP^T have read theirs), then the other blocks
+                if (!(ok = load_qd(0))) break;
+                if (!(ok = mbar_wait(k_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(k_full, AT_TILE);
+                tma_load_3d(sK, &tm_qkv, k_full, a.C + h * AT_HD, it.tile * AT_N, b);
+                k_items = i + 1;
+                if (!(ok = mbar_wait(v_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(v_full, AT_TILE);
+                tma_load_3d(sV, &tm_qkv, v_full, 2 * a.C + h * AT_HD, it.tile * AT_N, b);
+                v_items = i + 1;
+                for (int n = 1; ok && n < it.nblk; n++) ok = load_qd(n);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok || !warp_wait(ld_empty(st), ph ^ 1u, abort_flag, a.status)) break;
-            float* slot = ldslot + st * 256;
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int c = lane * 4 + e, q = q0 + c;
-                slot[c] = q < a.T ? lrow[q] * 1.4426950408889634f : 0.f;
-                slot[128 + c] = q < a.T ? drow[q] : 0.f;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ld_full(st));
-        }
-        if (lane == 0) {
-            mbar_drain(kv_full, 0, a.status);
+            if (k_items > 0) mbar_drain(k_full, (uint32_t)((k_items - 1) & 1), a.status);
+            if (v_items > 0) mbar_drain(v_full, (uint32_t)((v_items - 1) & 1), a.status);
             for (int st = 0; st < NS; st++)
                 if (qd_issued[st] >= 0) mbar_drain(qd_full(st), (uint32_t)qd_issued[st], a.status);
         }
@@ -493,136 +536,175 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             // -------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);  // K-major x K-major
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);  // K-major x MN-major
-            bool ok = mbar_wait(kv_full, 0, abort_flag, a.status);
-            auto issue_sdp = [&](int n) -> bool {  // S^T(n)
-                const int st = n % NS;
-                if (!mbar_wait(qd_full(st), (n / NS) & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(s_free, (n & 1) ^ 1u, abort_flag, a.status)) return false;
+            auto issue_s = [&](const Cur& x) -> bool {  // S^T = K Q^T
+                const int st = x.g % NS;
+                if (x.n == 0 && !mbar_wait(k_full, x.i & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(qd_full(st), (x.g / NS) & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(s_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; k++)
-                    tc_mma(tmem, sw128_desc(sK + k * 32, 16, 1024), sw128_desc(sQ(st) + k * 32, 16, 1024), idesc_s,
-                           k > 0 ? 1u : 0u);
+                    tc_mma(tmem + KV_S, sw128_desc(sK + k * 32, 16, 1024), sw128_desc(sQ(st) + k * 32, 16, 1024),
+                           idesc_s, k > 0 ? 1u : 0u);
                 tc_commit(s_full);
+                if (x.n == x.it.nblk - 1) tc_commit(k_empty);  // the item's last read of K
                 return true;
             };
-            auto issue_dp = [&](int n) -> bool {
-                const int st = n % NS;
-                if (!mbar_wait(dp_free, (n & 1) ^ 1u, abort_flag, a.status)) return false;
+            auto issue_dp = [&](const Cur& x) -> bool {  // dP^T = V dO^T
+                const int st = x.g % NS;
+                if (x.n == 0 && !mbar_wait(v_full, x.i & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(dp_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; k++)
-                    tc_mma(tmem + 128u, sw128_desc(sV + k * 32, 16, 1024), sw128_desc(sO(st) + k * 32, 16, 1024),
+                    tc_mma(tmem + KV_DP, sw128_desc(sV + k * 32, 16, 1024), sw128_desc(sO(st) + k * 32, 16, 1024),
                            idesc_s, k > 0 ? 1u : 0u);
                 tc_commit(dp_full);
+                if (x.n == x.it.nblk - 1) tc_commit(v_empty);  // the item's last read of V
                 return true;
             };
-            if (ok) ok = issue_sdp(0) && issue_dp(0);
-            for (int n = 0; ok && n < nblk; n++) {
-                const int st = n % NS;
-                if (n + 1 < nblk && !(ok = issue_sdp(n + 1))) break;
-                // dV += P^T dO
-                if (!(ok = mbar_wait(p_full, n & 1, abort_flag, a.status))) break;
+            Cur c = cur_first<false>(a);
+            bool ok = !c.valid || (issue_s(c) && issue_dp(c));
+            while (ok && c.valid) {
+                const Cur nx = cur_next<false>(a, c);
+                const int st = c.g % NS;
+                if (nx.valid && !(ok = issue_s(nx))) break;
+                // dV += P^T dO (the first block of an item starts the accumulator
+                // once the elementwise warps have stored the previous item's)
+                if (!(ok = mbar_wait(p_full, c.g & 1, abort_flag, a.status))) break;
+                if (c.n == 0 && c.i > 0 && !(ok = mbar_wait(acc_empty, (c.i - 1) & 1, abort_flag, a.status))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
-                    tc_mma(tmem + 256u, sw128_desc(sP + (kk >> 2) * AT_TILE + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(sO(st) + kk * 2048, 8192, 1024), idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + KV_DV, tmem + KV_P + kk * 8, sw128_desc(sO(st) + kk * 2048, 8192, 1024), idesc_o,
+                              (c.n > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(p_free);
-                if (n + 1 < nblk && !(ok = issue_dp(n + 1))) break;
+                if (nx.valid && !(ok = issue_dp(nx))) break;
                 // dK += dS^T Q
-                if (!(ok = mbar_wait(ds_full, n & 1, abort_flag, a.status))) break;
+                if (!(ok = mbar_wait(ds_full, c.g & 1, abort_flag, a.status))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
-                    tc_mma(tmem + 320u, sw128_desc(sS + (kk >> 2) * AT_TILE + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(sQ(st) + kk * 2048, 8192, 1024), idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + KV_DK, tmem + KV_DS + kk * 8, sw128_desc(sQ(st) + kk * 2048, 8192, 1024), idesc_o,
+                              (c.n > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(ds_free);
                 tc_commit(qd_empty(st));
+                if (c.n == c.it.nblk - 1) tc_commit(acc_full);  // the item's dV and dK are complete
+                c = nx;
             }
-            if (ok) tc_commit(o_done);
             tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
     } else {
-        // ------------------------------------------------------ elementwise (warps 2..9)
+        // ------------------------------------------------------ elementwise (warps 2..17)
         const int ew = warp - 2;
-        const int quad = warp & 3, half = ew >> 2;
-        const int r = quad * 32 + lane;      // key row = TMEM lane
-        const int key = kt * AT_N + r;
+        const int quad = warp & 3, part = ew >> 2;
+        const int r = quad * 32 + lane;  // key row within the tile = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        float* slot = ldslots + ew * 64;  // [0,32): -lse * log2(e), [32,64): D of this warp's 32 queries
+        // -lse (log2 units) and D of query column part*32 + lane of a step's block; 0 past T
+        auto load_ld = [&](const Cur& x, float& l2, float& d) {
+            const int q = (x.it.tile + x.n) * AT_M + part * EW_COLS + lane;
+            const int64_t o = (int64_t)x.it.bh * a.T + q;
+            l2 = q < a.T ? -a.lse[o] * 1.4426950408889634f : 0.f;
+            d = q < a.T ? a.D[o] : 0.f;
+        };
+        const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
+        Cur c = cur_first<false>(a);
+        float l2_nx = 0.f, d_nx = 0.f;
+        if (c.valid) load_ld(c, l2_nx, d_nx);
         bool ok = true;
-        for (int n = 0; n < nblk; n++) {
-            const int st = n % NS;
-            const int q0 = (kt + n) * AT_M + half * 64;  // first query of this thread's columns
-            const bool diag = n == 0;
-            uint32_t sv[2][32];
-            if (!(ok = warp_wait(s_full, n & 1, abort_flag, a.status))) break;
+        while (c.valid) {
+            const Cur nx = cur_next<false>(a, c);
+            const int g = c.g;
+            const int key = c.it.tile * AT_N + r;
+            const int q0 = (c.it.tile + c.n) * AT_M + part * EW_COLS;  // first query of this thread's columns
+            const bool diag = c.n == 0;
+            __syncwarp();  // every lane is done with the previous step's slot
+            slot[lane] = l2_nx;
+            slot[32 + lane] = d_nx;
+            __syncwarp();
+            if (nx.valid) load_ld(nx, l2_nx, d_nx);  // the next step's, in flight meanwhile
+            uint32_t sv[32];
+            if (!(ok = warp_wait(s_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
-            tc_ld32_issue(trow + (uint32_t)(half * 64), sv[0]);
-            tc_ld32_issue(trow + (uint32_t)(half * 64 + 32), sv[1]);
-            tc_ld_wait(sv[0]);
-            tc_ld_wait(sv[1]);
+            tc_ld32_issue(trow + KV_S + (uint32_t)(part * EW_COLS), sv);
+            tc_ld_wait(sv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            if (!(ok = warp_wait(ld_full(st), (n / NS) & 1, abort_flag, a.status))) break;
-            const float* slot = ldslot + st * 256 + half * 64;
-            float p[64];
-            uint32_t pk[32];
+            // P^T = exp2(S^T scale - lse); the mask is needed only on the
+            // diagonal block (query < key) and past the sequence end
+            float p[EW_COLS];
+            uint32_t pk[EW_COLS / 2];
+            const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(slot);
+            if (diag || q0 + EW_COLS > a.T) {
+                const int lo = diag ? key - q0 : 0, hi = a.T - q0;  // valid columns [lo, hi)
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                float pp[2];
-#pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const int cc = c + e, q = q0 + cc;
-                    const float x = __uint_as_float(sv[cc >> 5][cc & 31]) * a.scale_log2 - slot[cc];
-                    pp[e] = ((diag && q < key) || q >= a.T) ? 0.f : ex2_approx(x);
-                    p[cc] = pp[e];
+                for (int cc = 0; cc < EW_COLS; cc += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(sv[cc], sv[cc + 1]), scale2, nl2[cc / 2]), x0, x1);
+                    p[cc] = (cc >= lo && cc < hi) ? ex2_approx(x0) : 0.f;
+                    p[cc + 1] = (cc + 1 >= lo && cc + 1 < hi) ? ex2_approx(x1) : 0.f;
+                    pk[cc / 2] = pack2(p[cc], p[cc + 1]);
                 }
-                pk[c / 2] = pack2(pp[0], pp[1]);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < EW_COLS; cc += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(sv[cc], sv[cc + 1]), scale2, nl2[cc / 2]), x0, x1);
+                    p[cc] = ex2_approx(x0);
+                    p[cc + 1] = ex2_approx(x1);
+                    pk[cc / 2] = pack2(p[cc], p[cc + 1]);
+                }
             }
-            if (!(ok = warp_wait(p_free, (n & 1) ^ 1u, abort_flag, a.status))) break;
-            write_row64(gP, r, half, pk);
-            fence_proxy_async_smem();
+            if (!(ok = warp_wait(p_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
+            tc_st16(trow + KV_P + (uint32_t)(part * EW_COLS / 2), pk);
+            tc_st_wait();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
             // dS^T = P^T (dP^T - D)
-            if (!(ok = warp_wait(dp_full, n & 1, abort_flag, a.status))) break;
+            if (!(ok = warp_wait(dp_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
-            tc_ld32_issue(trow + 128u + (uint32_t)(half * 64), sv[0]);
-            tc_ld32_issue(trow + 128u + (uint32_t)(half * 64 + 32), sv[1]);
-            tc_ld_wait(sv[0]);
-            tc_ld_wait(sv[1]);
+            tc_ld32_issue(trow + KV_DP + (uint32_t)(part * EW_COLS), sv);
+            tc_ld_wait(sv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dp_free);
+            const uint64_t* d2 = reinterpret_cast<const uint64_t*>(slot + 32);
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                const float d0 = p[c] * (__uint_as_float(sv[c >> 5][c & 31]) - slot[128 + c]);
-                const float d1 = p[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - slot[128 + c + 1]);
-                pk[c / 2] = pack2(d0, d1);
+            for (int cc = 0; cc < EW_COLS; cc += 2) {
+                float d0, d1;
+                f2_unpack(f2_mul(f2_pack(p[cc], p[cc + 1]), f2_sub(f2_pack(sv[cc], sv[cc + 1]), d2[cc / 2])), d0, d1);
+                pk[cc / 2] = pack2(d0, d1);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ld_empty(st));  // lse and D of this block are no longer read
-            if (!(ok = warp_wait(ds_free, (n & 1) ^ 1u, abort_flag, a.status))) break;
-            write_row64(gS, r, half, pk);
-            fence_proxy_async_smem();
+            if (!(ok = warp_wait(ds_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
+            tc_st16(trow + KV_DS + (uint32_t)(part * EW_COLS / 2), pk);
+            tc_st_wait();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
-        }
-        if (ok && warp_wait(o_done, 0, abort_flag, a.status)) {
-            tc_fence_after();
-            uint32_t dv[32], dk[32];
-            tc_ld32_issue(trow + 256u + (uint32_t)(half * 32), dv);
-            tc_ld32_issue(trow + 320u + (uint32_t)(half * 32), dk);
-            tc_ld_wait(dv);
-            tc_ld_wait(dk);
-            if (key < a.T) {
-                bf16* out = a.dqkv + ((int64_t)b * a.T + key) * 3 * a.C + h * AT_HD + half * 32;
-                store32_bf16(out + a.C, dk, a.scale);
-                store32_bf16(out + 2 * a.C, dv, 1.f);
+            if (c.n == c.it.nblk - 1) {
+                // the item's accumulators: parts 0, 1 store dV columns part*32..,
+                // parts 2, 3 dK columns (part-2)*32..; then hand TMEM back
+                if (!(ok = warp_wait(acc_full, c.i & 1, abort_flag, a.status))) break;
+                tc_fence_after();
+                const bool is_dk = part >= 2;
+                const int c0 = (part & 1) * 32;
+                uint32_t acc[32];
+                tc_ld32_issue(trow + (is_dk ? KV_DK : KV_DV) + (uint32_t)c0, acc);
+                tc_ld_wait(acc);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                if (key < a.T) {
+                    const int b = c.it.bh / a.H, h = c.it.bh % a.H;
+                    bf16* out = a.dqkv + ((int64_t)b * a.T + key) * 3 * a.C + (is_dk ? a.C : 2 * a.C) + h * AT_HD + c0;
+                    store32_bf16(out, acc, is_dk ? a.scale : 1.f);
+                }
             }
+            c = nx;
         }
     }
 
@@ -636,6 +718,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 }
 
 // -------------------------------------------------------------------------- dQ
+// Shared memory: Q | dO | DQ_ST x (K, V) | barriers.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                           BwdArgs a) {
@@ -643,33 +726,30 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // Q | dO | DQ_ST x (K, V) | dS (2 chunks) | barriers
     constexpr int NS = DQ_ST;
     const uint32_t sQ = base, sO = base + AT_TILE;
     auto sK = [&](int st) { return base + (2 + 2 * st) * AT_TILE; };
     auto sV = [&](int st) { return base + (3 + 2 * st) * AT_TILE; };
-    const uint32_t sS = base + (2 + 2 * NS) * AT_TILE;
-    uint8_t* gS = gbase + (2 + 2 * NS) * AT_TILE;
-    const uint32_t bars = base + (4 + 2 * NS) * AT_TILE;
-    uint8_t* bar_area = gbase + (4 + 2 * NS) * AT_TILE;
-    const uint32_t qo_full = bars;
-    auto kv_full = [&](int i) { return bars + 8u * (1 + i); };
-    auto kv_empty = [&](int i) { return bars + 8u * (1 + NS + i); };
-    const uint32_t bx = bars + 8u * (1 + 2 * NS);
+    const uint32_t bars = base + (2 + 2 * NS) * AT_TILE;
+    uint8_t* bar_area = gbase + (2 + 2 * NS) * AT_TILE;
+    const uint32_t q_full = bars, q_empty = bars + 8u, o_full = bars + 16u, o_empty = bars + 24u;
+    auto kv_full = [&](int i) { return bars + 8u * (4 + i); };
+    auto kv_empty = [&](int i) { return bars + 8u * (4 + NS + i); };
+    const uint32_t bx = bars + 8u * (4 + 2 * NS);
     const uint32_t s_full = bx, s_free = bx + 8u;
     const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
     const uint32_t ds_full = bx + 32u, ds_free = bx + 40u;
-    const uint32_t o_done = bx + 48u, drain = bx + 56u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (1 + 2 * NS) + 64);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (1 + 2 * NS) + 68);
+    const uint32_t acc_full = bx + 48u, acc_empty = bx + 56u, drain = bx + 64u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (4 + 2 * NS) + 72);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (4 + 2 * NS) + 76);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest rows first
-    const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
-    const int nkb = qt + 1;
 
     if (threadIdx.x == 0) {
-        mbar_init(qo_full, 1);
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(o_full, 1);
+        mbar_init(o_empty, 1);
         for (int i = 0; i < NS; i++) {
             mbar_init(kv_full(i), 1);
             mbar_init(kv_empty(i), 1);
@@ -680,7 +760,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(dp_free, BW_EW);
         mbar_init(ds_full, BW_EW);
         mbar_init(ds_free, 1);
-        mbar_init(o_done, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, BW_EW);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -690,130 +771,197 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;  // S [0,128) dP [128,256) dQ [256,320)
+    const uint32_t tmem = *tmem_slot;  // columns Q_*
 
     if (warp == 0) {
         if (lane == 0) {
+            // -------------------------------------------------- TMA producer
             int kv_issued[NS];
             for (int i = 0; i < NS; i++) kv_issued[i] = -1;
-            mbar_expect_tx(qo_full, 2 * AT_TILE);
-            tma_load_3d(sQ, &tm_qkv, qo_full, h * AT_HD, qt * AT_M, b);
-            tma_load_3d(sO, &tm_do, qo_full, h * AT_HD, qt * AT_M, b);
-            for (int j = 0; j < nkb; j++) {
-                const int st = j % NS;
-                const uint32_t ph = (j / NS) & 1;
-                if (!mbar_wait(kv_empty(st), ph ^ 1u, abort_flag, a.status)) break;
-                mbar_expect_tx(kv_full(st), 2 * AT_TILE);
-                tma_load_3d(sK(st), &tm_qkv, kv_full(st), a.C + h * AT_HD, j * AT_N, b);
-                tma_load_3d(sV(st), &tm_qkv, kv_full(st), 2 * a.C + h * AT_HD, j * AT_N, b);
-                kv_issued[st] = (int)ph;
+            int q_items = 0, o_items = 0, g = 0;  // Q and dO loads issued (for the final drain)
+            bool ok = true;
+            for (int i = 0; ok; i++) {
+                Item it;
+                if (!get_item<true>(a, i, it)) break;
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                auto load_kv = [&](int j) -> bool {
+                    const int st = g % NS;
+                    const uint32_t ph = (g / NS) & 1;
+                    if (!mbar_wait(kv_empty(st), ph ^ 1u, abort_flag, a.status)) return false;
+                    mbar_expect_tx(kv_full(st), 2 * AT_TILE);
+                    tma_load_3d(sK(st), &tm_qkv, kv_full(st), a.C + h * AT_HD, j * AT_N, b);
+                    tma_load_3d(sV(st), &tm_qkv, kv_full(st), 2 * a.C + h * AT_HD, j * AT_N, b);
+                    kv_issued[st] = (int)ph;
+                    g++;
+                    return true;
+                };
+                // the item's first K/V block, then its Q and dO (once the previous
+                // item's last S and dP have read theirs), then the other blocks
+                if (!(ok = load_kv(0))) break;
+                if (!(ok = mbar_wait(q_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(q_full, AT_TILE);
+                tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HD, it.tile * AT_M, b);
+                q_items = i + 1;
+                if (!(ok = mbar_wait(o_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(o_full, AT_TILE);
+                tma_load_3d(sO, &tm_do, o_full, h * AT_HD, it.tile * AT_M, b);
+                o_items = i + 1;
+                for (int j = 1; ok && j < it.nblk; j++) ok = load_kv(j);
             }
-            mbar_drain(qo_full, 0, a.status);
+            if (q_items > 0) mbar_drain(q_full, (uint32_t)((q_items - 1) & 1), a.status);
+            if (o_items > 0) mbar_drain(o_full, (uint32_t)((o_items - 1) & 1), a.status);
             for (int st = 0; st < NS; st++)
                 if (kv_issued[st] >= 0) mbar_drain(kv_full(st), (uint32_t)kv_issued[st], a.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
+            // -------------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);
-            bool ok = mbar_wait(qo_full, 0, abort_flag, a.status);
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % NS;
-                if (!mbar_wait(kv_full(st), (j / NS) & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(s_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
+            auto issue_s = [&](const Cur& x) -> bool {  // S = Q K^T
+                const int st = x.g % NS;
+                if (x.n == 0 && !mbar_wait(q_full, x.i & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(kv_full(st), (x.g / NS) & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(s_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; k++)
-                    tc_mma(tmem, sw128_desc(sQ + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024), idesc_s,
-                           k > 0 ? 1u : 0u);
+                    tc_mma(tmem + Q_S, sw128_desc(sQ + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024),
+                           idesc_s, k > 0 ? 1u : 0u);
                 tc_commit(s_full);
+                if (x.n == x.it.nblk - 1) tc_commit(q_empty);  // the item's last read of Q
                 return true;
             };
-            auto issue_dp = [&](int j) -> bool {
-                const int st = j % NS;
-                if (!mbar_wait(dp_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
+            auto issue_dp = [&](const Cur& x) -> bool {  // dP = dO V^T
+                const int st = x.g % NS;
+                if (x.n == 0 && !mbar_wait(o_full, x.i & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(dp_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 4; k++)
-                    tc_mma(tmem + 128u, sw128_desc(sO + k * 32, 16, 1024), sw128_desc(sV(st) + k * 32, 16, 1024),
+                    tc_mma(tmem + Q_DP, sw128_desc(sO + k * 32, 16, 1024), sw128_desc(sV(st) + k * 32, 16, 1024),
                            idesc_s, k > 0 ? 1u : 0u);
                 tc_commit(dp_full);
+                if (x.n == x.it.nblk - 1) tc_commit(o_empty);  // the item's last read of dO
                 return true;
             };
-            if (ok) ok = issue_s(0) && issue_dp(0);
-            for (int j = 0; ok && j < nkb; j++) {
-                const int st = j % NS;
-                if (j + 1 < nkb && !(ok = issue_s(j + 1) && issue_dp(j + 1))) break;
+            Cur c = cur_first<true>(a);
+            bool ok = !c.valid || (issue_s(c) && issue_dp(c));
+            while (ok && c.valid) {
+                const Cur nx = cur_next<true>(a, c);
+                const int st = c.g % NS;
+                if (nx.valid && !(ok = issue_s(nx) && issue_dp(nx))) break;
                 // dQ += dS K
-                if (!(ok = mbar_wait(ds_full, j & 1, abort_flag, a.status))) break;
+                if (!(ok = mbar_wait(ds_full, c.g & 1, abort_flag, a.status))) break;
+                if (c.n == 0 && c.i > 0 && !(ok = mbar_wait(acc_empty, (c.i - 1) & 1, abort_flag, a.status))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
-                    tc_mma(tmem + 256u, sw128_desc(sS + (kk >> 2) * AT_TILE + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(sK(st) + kk * 2048, 8192, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + Q_DQ, tmem + Q_DS + kk * 8, sw128_desc(sK(st) + kk * 2048, 8192, 1024), idesc_o,
+                              (c.n > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(ds_free);
                 tc_commit(kv_empty(st));
+                if (c.n == c.it.nblk - 1) tc_commit(acc_full);
+                c = nx;
             }
-            if (ok) tc_commit(o_done);
             tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
     } else {
         const int ew = warp - 2;
-        const int quad = warp & 3, half = ew >> 2;
-        const int r = quad * 32 + lane;  // query row = TMEM lane
-        const int q = qt * AT_M + r;
+        const int quad = warp & 3, part = ew >> 2;
+        const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-        const int qc = q < a.T ? q : 0;
-        const float lse2 = a.lse[((int64_t)b * a.H + h) * a.T + qc] * 1.4426950408889634f;
-        const float Dq = a.D[((int64_t)b * a.H + h) * a.T + qc];
+        // this row's lse (log2 units) and D for an item; the next item's are loaded ahead
+        auto load_row = [&](const Item& it, float& l2, float& d) {
+            const int q = it.tile * AT_M + r;
+            const int64_t o = (int64_t)it.bh * a.T + (q < a.T ? q : 0);
+            l2 = a.lse[o] * 1.4426950408889634f;
+            d = a.D[o];
+        };
+        Cur c = cur_first<true>(a);
+        float l2_nx = 0.f, d_nx = 0.f, lse2 = 0.f, Dq = 0.f;
+        if (c.valid) load_row(c.it, l2_nx, d_nx);
         bool ok = true;
-        for (int j = 0; j < nkb; j++) {
-            const int k0 = j * AT_N + half * 64;  // first key of this thread's columns
-            const bool diag = j == qt;
-            uint32_t sv[2][32];
-            if (!(ok = warp_wait(s_full, j & 1, abort_flag, a.status))) break;
+        while (c.valid) {
+            const Cur nx = cur_next<true>(a, c);
+            const int g = c.g;
+            const int q = c.it.tile * AT_M + r;
+            if (c.n == 0) {
+                lse2 = l2_nx;
+                Dq = d_nx;
+                Item it2;
+                if (get_item<true>(a, c.i + 1, it2)) load_row(it2, l2_nx, d_nx);
+            }
+            const int k0 = c.n * AT_N + part * EW_COLS;  // first key of this thread's columns
+            const bool diag = c.n == c.it.tile;
+            uint32_t sv[32];
+            if (!(ok = warp_wait(s_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
-            tc_ld32_issue(trow + (uint32_t)(half * 64), sv[0]);
-            tc_ld32_issue(trow + (uint32_t)(half * 64 + 32), sv[1]);
-            tc_ld_wait(sv[0]);
-            tc_ld_wait(sv[1]);
+            tc_ld32_issue(trow + Q_S + (uint32_t)(part * EW_COLS), sv);
+            tc_ld_wait(sv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            float p[64];
+            // P = exp2(S scale - lse); masked only on the diagonal block (key >
+            // query) and past the sequence end
+            float p[EW_COLS];
+            const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2), nl2 = f2_pack(-lse2, -lse2);
+            if (diag || k0 + EW_COLS > a.T) {
+                const int hi = min(diag ? q - k0 + 1 : EW_COLS, a.T - k0);  // valid columns [0, hi)
 #pragma unroll
-            for (int c = 0; c < 64; c++) {
-                const int kk = k0 + c;
-                const float x = __uint_as_float(sv[c >> 5][c & 31]) * a.scale_log2 - lse2;
-                p[c] = ((diag && kk > q) || kk >= a.T) ? 0.f : ex2_approx(x);
+                for (int cc = 0; cc < EW_COLS; cc += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(sv[cc], sv[cc + 1]), scale2, nl2), x0, x1);
+                    p[cc] = cc < hi ? ex2_approx(x0) : 0.f;
+                    p[cc + 1] = cc + 1 < hi ? ex2_approx(x1) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < EW_COLS; cc += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(sv[cc], sv[cc + 1]), scale2, nl2), x0, x1);
+                    p[cc] = ex2_approx(x0);
+                    p[cc + 1] = ex2_approx(x1);
+                }
             }
-            if (!(ok = warp_wait(dp_full, j & 1, abort_flag, a.status))) break;
+            if (!(ok = warp_wait(dp_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
-            tc_ld32_issue(trow + 128u + (uint32_t)(half * 64), sv[0]);
-            tc_ld32_issue(trow + 128u + (uint32_t)(half * 64 + 32), sv[1]);
-            tc_ld_wait(sv[0]);
-            tc_ld_wait(sv[1]);
+            tc_ld32_issue(trow + Q_DP + (uint32_t)(part * EW_COLS), sv);
+            tc_ld_wait(sv);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dp_free);
-            uint32_t pk[32];
+            uint32_t pk[EW_COLS / 2];
+            const uint64_t dq2 = f2_pack(Dq, Dq);
 #pragma unroll
-            for (int c = 0; c < 64; c += 2)
-                pk[c / 2] = pack2(p[c] * (__uint_as_float(sv[c >> 5][c & 31]) - Dq),
-                                  p[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - Dq));
-            if (!(ok = warp_wait(ds_free, (j & 1) ^ 1u, abort_flag, a.status))) break;
-            write_row64(gS, r, half, pk);
-            fence_proxy_async_smem();
+            for (int cc = 0; cc < EW_COLS; cc += 2) {
+                float d0, d1;
+                f2_unpack(f2_mul(f2_pack(p[cc], p[cc + 1]), f2_sub(f2_pack(sv[cc], sv[cc + 1]), dq2)), d0, d1);
+                pk[cc / 2] = pack2(d0, d1);
+            }
+            if (!(ok = warp_wait(ds_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
+            tc_st16(trow + Q_DS + (uint32_t)(part * EW_COLS / 2), pk);
+            tc_st_wait();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
-        }
-        if (ok && warp_wait(o_done, 0, abort_flag, a.status)) {
-            tc_fence_after();
-            uint32_t dq[32];
-            tc_ld32_issue(trow + 256u + (uint32_t)(half * 32), dq);
-            tc_ld_wait(dq);
-            if (q < a.T) store32_bf16(a.dqkv + ((int64_t)b * a.T + q) * 3 * a.C + h * AT_HD + half * 32, dq, a.scale);
+            if (c.n == c.it.nblk - 1) {
+                // parts 0, 1 store dQ columns part*32 ..; every warp hands TMEM back
+                if (!(ok = warp_wait(acc_full, c.i & 1, abort_flag, a.status))) break;
+                tc_fence_after();
+                uint32_t dq[32];  // parts 2, 3 read the same columns and do not store them
+                tc_ld32_issue(trow + Q_DQ + (uint32_t)((part & 1) * 32), dq);
+                tc_ld_wait(dq);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                if (part < 2 && q < a.T) {
+                    const int b = c.it.bh / a.H, h = c.it.bh % a.H;
+                    store32_bf16(a.dqkv + ((int64_t)b * a.T + q) * 3 * a.C + h * AT_HD + part * 32, dq, a.scale);
+                }
+            }
+            c = cur_next<true>(a, c);
         }
     }
 
@@ -839,8 +987,8 @@ bool make_do_map(CUtensorMap* map, const void* dout, int B, int T, int C) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int DKDV_SMEM = (6 + 2 * DKDV_ST) * AT_TILE + DKDV_ST * 1024 + 256 + 1024;
-constexpr int DQ_SMEM = (4 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
+constexpr int DKDV_SMEM = (2 + 2 * DKDV_ST) * AT_TILE + BW_EW * 256 + 256 + 1024;
+constexpr int DQ_SMEM = (2 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
 static_assert(DKDV_SMEM <= 232448 && DQ_SMEM <= 232448, "shared memory per CTA");
 
 }  // namespace
@@ -862,12 +1010,15 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     a.lse = lse;
     a.D = D;
     a.status = status;
+    a.B = B;
     a.T = T;
     a.C = C;
     a.H = H;
+    a.nqt = (T + AT_M - 1) / AT_M;
     a.scale = 1.0f / sqrtf((float)(C / H));
     a.scale_log2 = 1.4426950408889634f * a.scale;
-    dim3 grid((T + AT_M - 1) / AT_M, B * H);
+    const int items = a.nqt * B * H;
+    const int grid = items < gpt2_num_sms() ? items : gpt2_num_sms();  // persistent: one CTA per SM
     attn_bwd_dkdv_tc_kernel<<<grid, BW_THREADS, DKDV_SMEM, s>>>(mq, mo, a);
     attn_bwd_dq_tc_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, mo, a);
     return 2;

@@ -1,8 +1,12 @@
 """Summarise Nsight Compute output for the step's kernels.
 
-  python -m step_gpt_train_gb300.ncu_summary launches <launches.csv>
-      per kernel: launches, total device time, share of the captured time
-      (input: `ncu --metrics gpu__time_duration.sum --csv --log-file ...`)
+  python -m step_gpt_train_gb300.ncu_summary launches <launches.csv> [marker-regex n]
+      per kernel: launches, total device time, share of the captured time,
+      and DRAM bytes per launch when the capture has them
+      (input: `ncu --metrics gpu__time_duration.sum[,dram__bytes_read.sum,
+      dram__bytes_write.sum] --csv --log-file ...`); with a marker, only the
+      launches from the n-th launch (1-based) of a kernel matching the marker
+      up to the next one: one training step when the marker is its first kernel
   python -m step_gpt_train_gb300.ncu_summary raw <report.ncu-rep> [kernel-regex]
       the headline counters of each captured launch (needs the ncu CLI)
 """
@@ -41,22 +45,53 @@ def short_name(name: str) -> str:
     return name.strip()
 
 
-def launches(path: str) -> str:
+def _ns(value: str, unit: str) -> float:
+    v = float(value.replace(",", ""))
+    return v * {"ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6, "nsecond": 1}.get(unit, 1)
+
+
+def _bytes(value: str, unit: str) -> float:
+    v = float(value.replace(",", ""))
+    return v * {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}.get(unit, 1)
+
+
+def launches(path: str, marker: str | None = None, nth: int = 1) -> str:
     text = "".join(l for l in open(path) if not l.startswith("=="))
-    rows = [r for r in csv.DictReader(io.StringIO(text)) if r.get("Metric Name") == "gpu__time_duration.sum"]
+    per_launch = collections.OrderedDict()  # launch id -> {name, ns, read, write}
+    for r in csv.DictReader(io.StringIO(text)):
+        lid = r.get("ID")
+        d = per_launch.setdefault(lid, {"name": short_name(r["Kernel Name"])})
+        m, unit, val = r.get("Metric Name"), r.get("Metric Unit"), r.get("Metric Value")
+        if m == "gpu__time_duration.sum":
+            d["ns"] = _ns(val, unit)
+        elif m == "dram__bytes_read.sum":
+            d["read"] = _bytes(val, unit)
+        elif m == "dram__bytes_write.sum":
+            d["write"] = _bytes(val, unit)
+    rows = [d for d in per_launch.values() if "ns" in d]
+    window = ""
+    if marker:
+        starts = [i for i, d in enumerate(rows) if re.search(marker, d["name"])]
+        if len(starts) < nth:
+            raise SystemExit(f"marker {marker!r} occurs {len(starts)} times, fewer than {nth}")
+        lo = starts[nth - 1]
+        hi = starts[nth] if len(starts) > nth else len(rows)
+        rows = rows[lo:hi]
+        window = f"; window: launch {nth} of {marker!r} to the next ({len(rows)} launches)"
+    has_dram = all("read" in d and "write" in d for d in rows) and rows
     per = collections.OrderedDict()
-    for r in rows:
-        k = short_name(r["Kernel Name"])
-        unit = r["Metric Unit"]
-        v = float(r["Metric Value"].replace(",", ""))
-        ns = v * {"ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6, "nsecond": 1}.get(unit, 1)
-        c, t = per.get(k, (0, 0.0))
-        per[k] = (c + 1, t + ns)
-    total = sum(t for _, t in per.values())
-    out = [f"captured launches: {len(rows)}; total device time {total / 1e6:.3f} ms (serialised, cold cache)",
-           "", f"{'kernel':70s} {'launches':>8s} {'total ms':>10s} {'share':>7s}"]
-    for k, (c, t) in sorted(per.items(), key=lambda kv: -kv[1][1]):
-        out.append(f"{k[:70]:70s} {c:8d} {t / 1e6:10.3f} {100 * t / total:6.2f}%")
+    for d in rows:
+        c, t, by = per.get(d["name"], (0, 0.0, 0.0))
+        per[d["name"]] = (c + 1, t + d["ns"], by + (d["read"] + d["write"] if has_dram else 0.0))
+    total = sum(t for _, t, _ in per.values())
+    out = [f"captured launches: {len(rows)}; total device time {total / 1e6:.3f} ms (serialised, cold cache){window}",
+           "", f"{'kernel':64s} {'launches':>8s} {'total ms':>10s} {'share':>7s}" +
+           (f" {'DRAM MB/launch':>15s}" if has_dram else "")]
+    for k, (c, t, by) in sorted(per.items(), key=lambda kv: -kv[1][1]):
+        line = f"{k[:64]:64s} {c:8d} {t / 1e6:10.3f} {100 * t / total:6.2f}%"
+        if has_dram:
+            line += f" {by / c / 1e6:15.1f}"
+        out.append(line)
     return "\n".join(out)
 
 
@@ -80,6 +115,7 @@ def raw(path: str, pattern: str = ".*") -> str:
 
 if __name__ == "__main__":
     if sys.argv[1] == "launches":
-        print(launches(sys.argv[2]))
+        print(launches(sys.argv[2], sys.argv[3] if len(sys.argv) > 3 else None,
+                       int(sys.argv[4]) if len(sys.argv) > 4 else 1))
     else:
         print(raw(sys.argv[2], sys.argv[3] if len(sys.argv) > 3 else ".*"))
