@@ -353,21 +353,6 @@ int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0
 
 // ===================================================================== GELU, residual
 
-// g = u s and g' = s + 2 u s (1 - s) sqrt(2/pi) (1 + 3*0.044715 u^2), with
-// s = 0.5 (1 + tanh(y)), y = sqrt(2/pi) (u + 0.044715 u^3); the derivative uses
-// 1 - tanh(y)^2 = 4 s (1 - s).
-template <typename T>
-__device__ __forceinline__ float gelu_fwd_f(float u) {
-    const float y = GELU_K * (u + GELU_A * u * u * u);
-    return u * gelu_sigmoid<T>(y);
-}
-template <typename T>
-__device__ __forceinline__ float gelu_grad_f(float u) {
-    const float y = GELU_K * (u + GELU_A * u * u * u);
-    const float s = gelu_sigmoid<T>(y);
-    return s + 2.f * u * s * (1.f - s) * GELU_K * (1.f + 3.f * GELU_A * u * u);
-}
-
 #define EW_UNROLL 4
 #define EW_THREADS 256
 

@@ -60,8 +60,14 @@ template <int BN> struct TileCfg {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 /*align*/ + BAR_BYTES + BIAS_BYTES;
 };
 
+// Epilogue operations fused into the bf16-output GEMM.
+constexpr int EPI_NONE = 0;
+constexpr int EPI_GELU = 1;      // D = x (bf16), D2 = gelu(D): the MLP's first linear and its GELU
+constexpr int EPI_GELU_BWD = 2;  // D = bf16(x) * gelu'(aux): the input gradient of that GELU
+
 struct GemmArgs {
     const void* bias;    // bf16 [N] or null
+    const bf16* aux;     // EPI_GELU_BWD: the GELU input u [M][N]
     int* status;
     int M, N, K;
     int d_fp32;
@@ -89,29 +95,63 @@ __device__ __forceinline__ bool get_work(const GemmArgs& g, int idx, Work& w) {
     return true;
 }
 
-// One 32-column chunk of this warp's 32 rows: + bias, convert, stage, TMA store.
-// fp32 output goes out as two 16-column halves. ncols_valid = columns of the
-// chunk inside the matrix (> 0).
+// Stage 32 bf16 values of this lane's row (64 bytes) once the buffer's
+// previous TMA store has read it, then store the 32 x 32 box at (x, y, z).
+__device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* stage, uint32_t stage_addr,
+                                                 const CUtensorMap* map, int x, int y, int z, int lane) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        uint4 v;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[q * 8 + 2 * i], f[q * 8 + 2 * i + 1]);
+        stage16(stage, lane, q, v);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_3d(map, stage_addr, x, y, z);
+}
+
+// One 32-column chunk of this warp's 32 rows: + bias, the epilogue op,
+// convert, stage, TMA store. fp32 output goes out as two 16-column halves.
+// ncols_valid = columns of the chunk inside the matrix (> 0). aux holds this
+// lane's 32 GELU inputs (EPI_GELU_BWD).
+template <int EPI>
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
-                                          uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD, int x,
-                                          int y, int z, int ncols_valid, int lane) {
+                                          uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD,
+                                          const CUtensorMap* mapD2, const uint4 (&aux)[4], int x, int y, int z,
+                                          int ncols_valid, int lane) {
     float f[32];
 #pragma unroll
     for (int j = 0; j < 32; j++) f[j] = __uint_as_float(r[j]) + (bias_s ? bias_s[j] : 0.f);
-    if (!fp32_out) {
-        if (lane == 0) bulk_wait_read_all();  // the buffer's previous store has read it
-        __syncwarp();
+    if (EPI != EPI_NONE) {
+        // the linear output as stored in bf16 (what a separate GELU pass would read)
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            uint4 v;
-            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+        for (int j = 0; j < 32; j++) f[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
+        if (EPI == EPI_GELU_BWD) {
 #pragma unroll
-            for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[q * 8 + 2 * i], f[q * 8 + 2 * i + 1]);
-            stage16(stage, lane, q, v);
+            for (int q = 0; q < 4; q++) {
+                float u[8];
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&aux[q]);
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    u[2 * i] = __low2float(h[i]);
+                    u[2 * i + 1] = __high2float(h[i]);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; e++) f[q * 8 + e] *= gelu_grad_f<bf16>(u[e]);
+            }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tma_store_3d(mapD, stage_addr, x, y, z);
+        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
+        if (EPI == EPI_GELU) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) f[j] = gelu_fwd_f<bf16>(f[j]);
+            stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane);
+        }
+    } else if (!fp32_out) {
+        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
     } else {
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
@@ -132,10 +172,11 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
 
 // ---------------------------------------------------------------- kernel
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                   const GemmArgs g) {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -306,6 +347,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int i = lane; i < BN / 2; i += 32) bias_s[i] = nb + i < g.N ? __bfloat162float(bp[nb + i]) : 0.f;
                 __syncwarp();
             }
+            // EPI_GELU_BWD: this lane's GELU inputs, a ring of two chunks; the
+            // first two load while the tile's MMAs run, and each slot is
+            // refilled with the chunk after next once its chunk is done
+            uint4 aux[2][4];
+            auto load_aux = [&](int c, uint4 (&dst)[4]) {
+                const int row = m0 + row_in_tile;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int col = n0 + (cfirst + c) * 32 + q * 8;
+                    dst[q] = (row < g.M && col < g.N) ? *reinterpret_cast<const uint4*>(g.aux + (int64_t)row * g.N + col)
+                                                      : make_uint4(0, 0, 0, 0);
+                }
+            };
+            if (EPI == EPI_GELU_BWD) {
+                load_aux(0, aux[0]);
+                if (CHUNKS > 1) load_aux(1, aux[1]);
+            }
             if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag, g.status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
@@ -333,14 +391,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // ra holds chunk c; chunk c+1 is loaded into rb while ra is stored
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
-                epi_chunk(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, xcol(c), ys, z, ncols(c), lane);
+                epi_chunk<EPI>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z, ncols(c),
+                               lane);
+                if (EPI == EPI_GELU_BWD && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();  // reconverge before the warp-collective TMEM ops
                 if (!more) break;
                 tc_ld_wait(rb);
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
-                epi_chunk(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, xcol(c + 1), ys, z, ncols(c + 1),
-                          lane);
+                epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1), ys, z,
+                               ncols(c + 1), lane);
+                if (EPI == EPI_GELU_BWD && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
             }
@@ -473,26 +534,41 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
     return p;
 }
 
-template <int BN, bool A_MN, bool B_MN>
-void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const GemmArgs& args, int grid,
-               cudaStream_t s) {
+template <int BN, bool A_MN, bool B_MN, int EPI>
+void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
+               const GemmArgs& args, int grid, cudaStream_t s) {
     using Cfg = TileCfg<BN>;
     static bool configured = false;
     if (!configured) {
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES);
         configured = true;
     }
-    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, args);
+    gemm_tc_kernel<BN, A_MN, B_MN, EPI><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
 }
 
+// The operand layouts, and the fused epilogues only where the step uses them:
+// GELU after a linear forward (A, B K-major), its gradient after an input
+// gradient (B MN-major).
 template <int BN>
-void launch_tc_layout(int a_mn, int b_mn, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
-                      const GemmArgs& args, int grid, cudaStream_t s) {
-    if (!a_mn && !b_mn) launch_tc<BN, false, false>(ma, mb, md, args, grid, s);
-    else if (!a_mn && b_mn) launch_tc<BN, false, true>(ma, mb, md, args, grid, s);
-    else if (a_mn && !b_mn) launch_tc<BN, true, false>(ma, mb, md, args, grid, s);
-    else launch_tc<BN, true, true>(ma, mb, md, args, grid, s);
+bool launch_tc_layout(int epi, int a_mn, int b_mn, const CUtensorMap& ma, const CUtensorMap& mb,
+                      const CUtensorMap& md, const CUtensorMap& md2, const GemmArgs& args, int grid, cudaStream_t s) {
+    if (epi == EPI_GELU) {
+        if (a_mn || b_mn) return false;
+        launch_tc<BN, false, false, EPI_GELU>(ma, mb, md, md2, args, grid, s);
+    } else if (epi == EPI_GELU_BWD) {
+        if (a_mn || !b_mn) return false;
+        launch_tc<BN, false, true, EPI_GELU_BWD>(ma, mb, md, md2, args, grid, s);
+    } else if (!a_mn && !b_mn) {
+        launch_tc<BN, false, false, EPI_NONE>(ma, mb, md, md2, args, grid, s);
+    } else if (!a_mn && b_mn) {
+        launch_tc<BN, false, true, EPI_NONE>(ma, mb, md, md2, args, grid, s);
+    } else if (a_mn && !b_mn) {
+        launch_tc<BN, true, false, EPI_NONE>(ma, mb, md, md2, args, grid, s);
+    } else {
+        launch_tc<BN, true, true, EPI_NONE>(ma, mb, md, md2, args, grid, s);
+    }
+    return true;
 }
 
 }  // namespace
@@ -502,19 +578,25 @@ size_t matmul_tc_scratch(int M, int N, int K, int d_fp32) {
     return p.splits > 1 ? (size_t)p.units * BM * p.bn * 4 : 0;
 }
 
-int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
-                     int N, int K, void* scratch, int* status, cudaStream_t s) {
-    Plan p = make_plan(M, N, K, d_fp32);
+namespace {
+
+// D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
+int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
+              int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s) {
+    Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
     CUtensorMap ma, mb;
     bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
     ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
                      : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
-    CUtensorMap md;
+    CUtensorMap md, md2;
     if (p.splits > 1) ok = ok && make_out_map(&md, scratch, true, (uint64_t)p.bn, BM, (uint64_t)p.units);
     else ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
+    if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
+    else md2 = md;
     if (!ok) return GPT2_ERR_CUDA;
     GemmArgs g;
     g.bias = p.splits > 1 ? nullptr : bias;
+    g.aux = aux;
     g.status = status;
     g.M = M;
     g.N = N;
@@ -525,9 +607,11 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
     g.n_tiles = p.n_tiles;
     g.units = p.units;
     g.num_kb = p.num_kb;
-    if (p.bn == 128) launch_tc_layout<128>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
-    else if (p.bn == 192) launch_tc_layout<192>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
-    else launch_tc_layout<256>(a_mn, b_mn, ma, mb, md, g, p.grid, s);
+    bool launched;
+    if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
+    else if (p.bn == 192) launched = launch_tc_layout<192>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
+    else launched = launch_tc_layout<256>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
+    if (!launched) return GPT2_ERR_ARG;
     if (p.splits > 1) {
         const int64_t MN = (int64_t)M * N;
         const int blocks = (int)((MN / 8 + 255) / 256);
@@ -536,4 +620,24 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
         return 2;
     }
     return 1;
+}
+
+}  // namespace
+
+int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
+                     int N, int K, void* scratch, int* status, cudaStream_t s) {
+    return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s);
+}
+
+int launch_matmul_gelu(void* pre, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
+                       int* status, cudaStream_t s) {
+    if (M == 0 || N == 0) return 0;
+    return matmul_tc(EPI_GELU, pre, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s);
+}
+
+int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* u, int M, int N, int K,
+                                int* status, cudaStream_t s) {
+    if (M == 0 || N == 0) return 0;
+    return matmul_tc(EPI_GELU_BWD, du, nullptr, (const bf16*)u, 0, dY, 0, W, 1, nullptr, M, N, K, nullptr, status,
+                     s);
 }

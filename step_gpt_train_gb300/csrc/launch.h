@@ -67,6 +67,14 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
                               const float* lse, int B, int T, int C, int H, void* scratch, int* status,
                               cudaStream_t s);
 
+// bf16 linear forward with the GELU fused into its epilogue: pre = A W^T +
+// bias (A [M,K], W [N,K], both K-major), out = gelu(pre); see gpt2_op_matmul_gelu.
+int launch_matmul_gelu(void* pre, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
+                       int* status, cudaStream_t s);
+// bf16 input gradient through a GELU: du = (dY W) * gelu'(u), dY [M,K], W [K,N].
+int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* u, int M, int N, int K,
+                                int* status, cudaStream_t s);
+
 // Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
 size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32);
 int launch_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias,

@@ -415,8 +415,14 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
         }
         TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
         TRY(res_ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, b.x, m->fwd_tmp, tidx(l, 6), BT));
-        TRY(linear_fwd(m, b.fch, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
-        {
+        if (m->dtype == GPT2_MODE_BF16) {
+            // the GELU runs in the epilogue of its linear (both outputs kept)
+            Op op(m, GPT2_K_MATMUL);
+            TRY(op.done(launch_matmul_gelu(b.fch, b.fchg, b.ln2, P(m, tidx(l, 8)), P(m, tidx(l, 9)), BT, 4 * C, C,
+                                           m->status, m->stream),
+                        2.0 * BT * 4 * C * C));
+        } else {
+            TRY(linear_fwd(m, b.fch, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
             Op op(m, GPT2_K_GELU_FWD);
             TRY(op.done(launch_gelu_forward(m->dtype, b.fchg, b.fch, (int64_t)BT * 4 * C, m->stream),
                         2.0 * BT * 4 * C * m->act));
@@ -454,8 +460,16 @@ int backward_impl(gpt2* m) {
     for (int l = L - 1; l >= 0; l--) {
         LayerBufs& b = m->layers[l];
         // MLP branch
-        TRY(linear_bwd(m, m->dbig, m->dres, b.fchg, tidx(l, 10), -1, BT, 4 * C, C));
-        {
+        if (m->dtype == GPT2_MODE_BF16) {
+            // dW of the MLP projection, then its input gradient with the GELU's
+            // derivative applied in the GEMM epilogue
+            TRY(op_matmul(m, G(m, tidx(l, 10)), 1, m->dres, 1, b.fchg, 1, nullptr, C, 4 * C, BT));
+            Op op(m, GPT2_K_MATMUL);
+            TRY(op.done(launch_matmul_gelu_backward(m->dbig, m->dres, P(m, tidx(l, 10)), b.fch, BT, 4 * C, C,
+                                                    m->status, m->stream),
+                        2.0 * BT * 4 * C * C));
+        } else {
+            TRY(linear_bwd(m, m->dbig, m->dres, b.fchg, tidx(l, 10), -1, BT, 4 * C, C));
             Op op(m, GPT2_K_GELU_BWD);
             TRY(op.done(launch_gelu_backward(m->dtype, m->dbig, b.fch, m->dbig, (int64_t)BT * 4 * C, m->stream),
                         3.0 * BT * 4 * C * m->act));

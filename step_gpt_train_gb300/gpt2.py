@@ -85,6 +85,10 @@ _SIGNATURES = {
     "gpt2_op_matmul_scratch": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "gpt2_op_matmul": (c_int, [c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
                                c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "gpt2_op_matmul_gelu": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                    c_void_p, c_void_p]),
+    "gpt2_op_matmul_gelu_backward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                             c_void_p, c_void_p]),
     "gpt2_op_attention_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                           c_void_p]),
     "gpt2_op_attention_backward_scratch": (c_size_t, [c_int, c_int, c_int]),
@@ -359,6 +363,22 @@ def gpt2_op_matmul(D, A, a_mn, B, b_mn, M, N, K, bias=None, status=None, stream=
     check(lib.gpt2_op_matmul(dt, _p(D), d_fp32, _p(A), int(a_mn), _p(B), int(b_mn), _p(bias), M, N, K, _p(sc),
                              sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul")
     return sc
+
+
+def gpt2_op_matmul_gelu(pre, out, A, W, bias=None, status=None, stream=None):
+    """pre = A W^T + bias, out = gelu(pre); A [M, K], W [N, K]."""
+    M, K = A.shape
+    N = W.shape[0]
+    check(load_library().gpt2_op_matmul_gelu(_dtype_of(A), _p(pre), _p(out), _p(A), _p(W), _p(bias), M, N, K,
+                                             _p(status), _s(stream)), "gpt2_op_matmul_gelu")
+
+
+def gpt2_op_matmul_gelu_backward(du, dY, W, u, status=None, stream=None):
+    """du = (dY W) * gelu'(u); dY [M, K], W [K, N], u [M, N]."""
+    M, K = dY.shape
+    N = W.shape[1]
+    check(load_library().gpt2_op_matmul_gelu_backward(_dtype_of(dY), _p(du), _p(dY), _p(W), _p(u), M, N, K,
+                                                      _p(status), _s(stream)), "gpt2_op_matmul_gelu_backward")
 
 
 def gpt2_op_attention_forward(o, lse, qkv, B, T, H, stream=None):

@@ -80,6 +80,23 @@ def main(argv=None):
         ops[f"gemm_{name}_dx"] = gemm_op(N, inp, out, 0, 1, False, False)
         ops[f"gemm_{name}_dw"] = gemm_op(out, inp, N, 1, 1, True, False)
 
+    def gemm_gelu_op():  # the MLP's first linear with its GELU in the epilogue
+        def setup():
+            A, W, b = rnd(N, C), rnd(4 * C, C, std=0.02), rnd(4 * C)
+            pre, out = torch.empty(N, 4 * C, device=dev, dtype=bf), torch.empty(N, 4 * C, device=dev, dtype=bf)
+            return lambda: g.gpt2_op_matmul_gelu(pre, out, A, W, b, stream=torch.cuda.current_stream().cuda_stream)
+        return setup, 2.0 * N * 4 * C * C, "flop"
+
+    def gemm_gelu_bwd_op():  # the MLP projection's input gradient through the GELU
+        def setup():
+            dY, W, u = rnd(N, C), rnd(C, 4 * C, std=0.02), rnd(N, 4 * C)
+            du = torch.empty(N, 4 * C, device=dev, dtype=bf)
+            return lambda: g.gpt2_op_matmul_gelu_backward(du, dY, W, u, stream=torch.cuda.current_stream().cuda_stream)
+        return setup, 2.0 * N * 4 * C * C, "flop"
+
+    ops["gemm_fc_fwd_gelu"] = gemm_gelu_op()
+    ops["gemm_fcproj_dx_gelu"] = gemm_gelu_bwd_op()
+
     def attn_fwd():
         qkv = rnd(N, 3 * C)
         o = torch.empty(N, C, device=dev, dtype=bf)

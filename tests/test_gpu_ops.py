@@ -226,6 +226,54 @@ def test_gelu(torch_cuda, mode):
 
 
 @pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("shape", [(300, 776, 256), (1000, 3072, 768)])
+def test_matmul_gelu(torch_cuda, mode, shape):
+    """Linear + GELU with the GELU in the GEMM epilogue, and the input gradient
+    through the GELU: against the oracle, and bit for bit against the separate
+    matmul and GELU kernels."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import (gpt2_op_gelu_backward, gpt2_op_gelu_forward, gpt2_op_matmul,
+                                           gpt2_op_matmul_gelu, gpt2_op_matmul_gelu_backward)
+    M, N, K = shape  # 300 rows: a ragged 128-row tile; N = 776: a ragged column tile
+    A = inputs(60, (M, K), 1.0, mode)
+    W = inputs(61, (N, K), K ** -0.5, mode)
+    b = inputs(62, (N,), 0.5, mode)
+    dA, dW, db = dev(A, mode), dev(W, mode), dev(b, mode)
+    pre = torch.empty(M, N, dtype=torch_dtype(mode), device="cuda")
+    out = torch.empty_like(pre)
+    gpt2_op_matmul_gelu(pre, out, dA, dW, db)
+    # the separate kernels
+    pre2, out2 = torch.empty_like(pre), torch.empty_like(pre)
+    gpt2_op_matmul(pre2, dA, 0, dW, 0, M, N, K, bias=db)
+    gpt2_op_gelu_forward(out2, pre2)
+    # backward: du = (dY W) gelu'(u), W [N2 = K of the next linear, N]
+    K2 = 512
+    dY = inputs(63, (M, K2), 1.0, mode)
+    W2 = inputs(64, (K2, N), K2 ** -0.5, mode)
+    ddY, dW2 = dev(dY, mode), dev(W2, mode)
+    du = torch.empty_like(pre)
+    gpt2_op_matmul_gelu_backward(du, ddY, dW2, pre)
+    dg2, du2 = torch.empty_like(pre), torch.empty_like(pre)
+    gpt2_op_matmul(dg2, ddY, 0, dW2, 1, M, N, K2)
+    gpt2_op_gelu_backward(du2, pre, dg2)
+    torch.cuda.synchronize()
+    assert torch.equal(pre, pre2) and torch.equal(out, out2), "fused forward differs from matmul + gelu"
+    assert torch.equal(du, du2), "fused backward differs from matmul + gelu backward"
+    tol = BF16_REL if mode == 1 else 1e-5
+    rpre = R.linear_forward(A.astype(np.float64), W.astype(np.float64), b.astype(np.float64))
+    # as for the plain matmul: fp32 accumulation over K, relative to the output's rms
+    assert_close(host(pre), rpre, tol, atol_frac=1e-3 if mode == 1 else 1e-5, what="pre-activation")
+    # the GELU of the stored pre-activation
+    assert_close(host(out), R.gelu_forward(host(pre)), tol, atol=2e-15, what="gelu(pre)")
+    rdg = dY.astype(np.float64) @ W2.astype(np.float64)
+    rdu = R.gelu_backward(host(pre), rdg)
+    # gelu'(u) sums O(1) terms that cancel near its zero (u ~ -0.75): a few fp32
+    # ulps of 1, times |dY W|, in absolute terms
+    floor = 8 * 2.0 ** -23 * float(np.abs(rdg).max())
+    assert_close(host(du), rdu, 2 * tol, atol_frac=2e-3 if mode == 1 else 1e-6, atol=floor, what="du")
+
+
+@pytest.mark.parametrize("mode", [1, 0])
 def test_residual(torch_cuda, mode):
     torch = torch_cuda
     from step_gpt_train_gb300.gpt2 import gpt2_op_residual_backward, gpt2_op_residual_forward

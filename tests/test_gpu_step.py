@@ -166,10 +166,13 @@ def test_launch_inventory_matches_page_table(torch_cuda):
     model.backward()
     model.adamw_step(1e-4, t=1, **HP)
     st = model.family_stats()
-    for fam in ("matmul", "attention_forward", "attention_backward", "gelu_forward", "gelu_backward",
-                "layernorm_forward", "layernorm_backward", "classifier", "adamw", "encoder_forward",
-                "encoder_backward"):
+    for fam in ("matmul", "attention_forward", "attention_backward", "layernorm_forward", "layernorm_backward",
+                "classifier", "adamw", "encoder_forward", "encoder_backward"):
         assert st[fam]["calls"] == facts[fam], (fam, st[fam]["calls"], facts[fam])
+    # the GELU and its backward run in the epilogues of the matmuls around them
+    # (the MLP's first linear, and the input gradient of its projection)
+    assert st["gelu_forward"]["calls"] == facts["gelu_forward"] - 12 == 0
+    assert st["gelu_backward"]["calls"] == facts["gelu_backward"] - 12 == 0
     # Fusions: every residual join runs inside the LayerNorm forward that reads
     # its sum (24 of the 25), and the LayerNorm backwards, which add into the
     # residual gradient as in the table, also emit the bias gradients of the
