@@ -113,23 +113,26 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
 
 /* Linear forward with the GELU after it fused into the GEMM epilogue (the
  * MLP's first linear, "matmul_forward", followed by "gelu_forward" in the
- * kernel table): pre[M,N] = A W^T + bias (A [M,K], W [N,K] row-major, bias
- * [N] optional), out = gelu(pre) with the tanh-approximation GELU of
- * gpt2_op_gelu_forward applied to pre as stored. Both outputs in dtype,
- * overwritten. bf16: one tensor-core GEMM whose epilogue writes both; fp32:
- * the fp32 GEMM then the GELU kernel. Same shape and alignment rules as
+ * kernel table): u = A W^T + bias (A [M,K], W [N,K] row-major, bias [N]
+ * optional), rounded to dtype; out = gelu(u) with the tanh-approximation
+ * GELU of gpt2_op_gelu_forward, and dgelu = gelu'(u), the factor the
+ * backward needs (the backward of the step uses nothing else of u). Both
+ * outputs [M,N] in dtype, overwritten, not overlapping. bf16: one
+ * tensor-core GEMM whose epilogue writes both; fp32: the fp32 GEMM (into
+ * dgelu) then one elementwise pass. Same shape and alignment rules as
  * gpt2_op_matmul. */
-int gpt2_op_matmul_gelu(int dtype, void* pre, void* out, const void* A, const void* W,
+int gpt2_op_matmul_gelu(int dtype, void* dgelu, void* out, const void* A, const void* W,
                         const void* bias, int M, int N, int K, int* d_status, void* stream);
 
-/* Input gradient of that linear's GELU input, fused ("gelu_backward" of the
+/* The input gradient of that GELU's input, fused ("gelu_backward" of the
  * kernel table folded into the preceding "matmul_backward"): du[M,N] =
- * (dY W)[m,n] * gelu'(u[m,n]) with dY [M,K], W [K,N] row-major (the weight
- * of the linear that read gelu(u)), u [M,N] the GELU input; the product
- * dY W is rounded to dtype before the multiply, as a separate GELU pass
- * would read it. du overwritten, in dtype; du must not overlap u. */
-int gpt2_op_matmul_gelu_backward(int dtype, void* du, const void* dY, const void* W, const void* u,
-                                 int M, int N, int K, int* d_status, void* stream);
+ * (dY W)[m,n] * dgelu[m,n] with dY [M,K], W [K,N] row-major (the weight of
+ * the linear that read gelu(u)) and dgelu from gpt2_op_matmul_gelu; the
+ * product dY W is rounded to dtype before the multiply. du overwritten, in
+ * dtype; it may not overlap dgelu. */
+int gpt2_op_matmul_gelu_backward(int dtype, void* du, const void* dY, const void* W,
+                                 const void* dgelu, int M, int N, int K, int* d_status,
+                                 void* stream);
 
 /* Causal multi-head attention forward ("flash attention", section "Single
  * GPU training"; kernel "cudnn_generated_fort_native_sdpa"): qkv [B*T, 3C]

@@ -166,6 +166,14 @@ __device__ __forceinline__ float gelu_grad_f(float u) {
     const float s = gelu_sigmoid<T>(y);
     return s + 2.f * u * s * (1.f - s) * GELU_K * (1.f + 3.f * GELU_A * u * u);
 }
+// Both at once (one sigmoid): g = gelu(u), d = gelu'(u).
+template <typename T>
+__device__ __forceinline__ void gelu_both_f(float u, float& g, float& d) {
+    const float y = GELU_K * (u + GELU_A * u * u * u);
+    const float s = gelu_sigmoid<T>(y);
+    g = u * s;
+    d = s + 2.f * u * s * (1.f - s) * GELU_K * (1.f + 3.f * GELU_A * u * u);
+}
 
 // ---- host-side helpers ----
 

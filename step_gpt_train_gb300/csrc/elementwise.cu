@@ -356,9 +356,10 @@ int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0
 #define EW_UNROLL 4
 #define EW_THREADS 256
 
-// op 0: out = gelu(a); op 1: out = b * gelu'(a); op 2: out = a + b.
+// op 0: out = gelu(a); op 1: out = b * gelu'(a); op 2: out = a + b; op 3:
+// out = a * b; op 4: out = gelu(a) and b = gelu'(a) (b may alias a).
 template <typename T, int OP>
-__global__ void __launch_bounds__(EW_THREADS) ew_kernel(T* out, const T* a, const T* b, int64_t n8) {
+__global__ void __launch_bounds__(EW_THREADS) ew_kernel(T* out, const T* a, T* b, int64_t n8) {
     // No __restrict__: out may alias a (in-place GELU and residual accumulate).
     // Each thread loads all its inputs before its first store.
     const int64_t base = (int64_t)blockIdx.x * (EW_THREADS * EW_UNROLL) + threadIdx.x;
@@ -368,35 +369,38 @@ __global__ void __launch_bounds__(EW_THREADS) ew_kernel(T* out, const T* a, cons
         const int64_t i = base + (int64_t)u * EW_THREADS;
         if (i < n8) {
             load8_stream(a + i * 8, va[u]);
-            if (OP != 0) load8_stream(b + i * 8, vb[u]);
+            if (OP != 0 && OP != 4) load8_stream(b + i * 8, vb[u]);
         }
     }
 #pragma unroll
     for (int u = 0; u < EW_UNROLL; u++) {
         const int64_t i = base + (int64_t)u * EW_THREADS;
         if (i < n8) {
-            float r[8];
+            float r[8], r2[8];
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 if (OP == 0) r[j] = gelu_fwd_f<T>(va[u][j]);
                 else if (OP == 1) r[j] = vb[u][j] * gelu_grad_f<T>(va[u][j]);
-                else r[j] = va[u][j] + vb[u][j];
+                else if (OP == 2) r[j] = va[u][j] + vb[u][j];
+                else if (OP == 3) r[j] = va[u][j] * vb[u][j];
+                else gelu_both_f<T>(va[u][j], r[j], r2[j]);
             }
             store8(out + i * 8, r);
+            if (OP == 4) store8(b + i * 8, r2);
         }
     }
 }
 
 template <int OP>
-static int ew_launch(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s) {
+static int ew_launch(int dtype, void* out, const void* a, void* b, int64_t n, cudaStream_t s) {
     const int64_t n8 = n / 8;
     const int64_t per_block = EW_THREADS * EW_UNROLL;
     const int blocks = (int)((n8 + per_block - 1) / per_block);
     if (blocks == 0) return 0;
     if (dtype == GPT2_MODE_BF16)
-        ew_kernel<bf16, OP><<<blocks, EW_THREADS, 0, s>>>((bf16*)out, (const bf16*)a, (const bf16*)b, n8);
+        ew_kernel<bf16, OP><<<blocks, EW_THREADS, 0, s>>>((bf16*)out, (const bf16*)a, (bf16*)b, n8);
     else
-        ew_kernel<float, OP><<<blocks, EW_THREADS, 0, s>>>((float*)out, (const float*)a, (const float*)b, n8);
+        ew_kernel<float, OP><<<blocks, EW_THREADS, 0, s>>>((float*)out, (const float*)a, (float*)b, n8);
     return 1;
 }
 
@@ -404,13 +408,19 @@ int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream
     return ew_launch<0>(dtype, g, u, nullptr, n, s);
 }
 int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s) {
-    return ew_launch<1>(dtype, du, u, dg, n, s);
+    return ew_launch<1>(dtype, du, u, const_cast<void*>(dg), n, s);
 }
 int launch_residual_forward(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s) {
-    return ew_launch<2>(dtype, out, a, b, n, s);
+    return ew_launch<2>(dtype, out, a, const_cast<void*>(b), n, s);
 }
 int launch_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n, cudaStream_t s) {
-    return ew_launch<2>(dtype, dres, dres, dbranch, n, s);
+    return ew_launch<2>(dtype, dres, dres, const_cast<void*>(dbranch), n, s);
+}
+int launch_mul(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s) {
+    return ew_launch<3>(dtype, out, a, const_cast<void*>(b), n, s);
+}
+int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n, cudaStream_t s) {
+    return ew_launch<4>(dtype, out, u, dgelu, n, s);
 }
 
 // ===================================================================== bias gradient

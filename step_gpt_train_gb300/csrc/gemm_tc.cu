@@ -62,12 +62,12 @@ template <int BN> struct TileCfg {
 
 // Epilogue operations fused into the bf16-output GEMM.
 constexpr int EPI_NONE = 0;
-constexpr int EPI_GELU = 1;      // D = x (bf16), D2 = gelu(D): the MLP's first linear and its GELU
-constexpr int EPI_GELU_BWD = 2;  // D = bf16(x) * gelu'(aux): the input gradient of that GELU
+constexpr int EPI_GELU = 1;  // u = bf16(x); D = gelu'(u), D2 = gelu(u): the MLP's first linear and its GELU
+constexpr int EPI_MUL = 2;   // D = bf16(x) * aux: the input gradient through that GELU, aux = gelu'(u)
 
 struct GemmArgs {
     const void* bias;    // bf16 [N] or null
-    const bf16* aux;     // EPI_GELU_BWD: the GELU input u [M][N]
+    const bf16* aux;     // EPI_MUL: the factor [M][N]
     int* status;
     int M, N, K;
     int d_fp32;
@@ -117,7 +117,7 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
 // One 32-column chunk of this warp's 32 rows: + bias, the epilogue op,
 // convert, stage, TMA store. fp32 output goes out as two 16-column halves.
 // ncols_valid = columns of the chunk inside the matrix (> 0). aux holds this
-// lane's 32 GELU inputs (EPI_GELU_BWD).
+// lane's 32 factors (EPI_MUL).
 template <int EPI>
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
                                           uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD,
@@ -127,28 +127,26 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
 #pragma unroll
     for (int j = 0; j < 32; j++) f[j] = __uint_as_float(r[j]) + (bias_s ? bias_s[j] : 0.f);
     if (EPI != EPI_NONE) {
-        // the linear output as stored in bf16 (what a separate GELU pass would read)
+        // the linear output rounded to bf16, as a separate pass would read it
 #pragma unroll
         for (int j = 0; j < 32; j++) f[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
-        if (EPI == EPI_GELU_BWD) {
+        if (EPI == EPI_MUL) {
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                float u[8];
                 const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&aux[q]);
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
-                    u[2 * i] = __low2float(h[i]);
-                    u[2 * i + 1] = __high2float(h[i]);
+                    f[q * 8 + 2 * i] *= __low2float(h[i]);
+                    f[q * 8 + 2 * i + 1] *= __high2float(h[i]);
                 }
-#pragma unroll
-                for (int e = 0; e < 8; e++) f[q * 8 + e] *= gelu_grad_f<bf16>(u[e]);
             }
-        }
-        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
-        if (EPI == EPI_GELU) {
+            stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
+        } else {
+            float gd[32];
 #pragma unroll
-            for (int j = 0; j < 32; j++) f[j] = gelu_fwd_f<bf16>(f[j]);
-            stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane);
+            for (int j = 0; j < 32; j++) gelu_both_f<bf16>(f[j], f[j], gd[j]);
+            stage_store_bf16(gd, stage, stage_addr, mapD, x, y, z, lane);  // gelu'(u), kept for the backward
+            stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane);   // gelu(u)
         }
     } else if (!fp32_out) {
         stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
@@ -347,7 +345,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int i = lane; i < BN / 2; i += 32) bias_s[i] = nb + i < g.N ? __bfloat162float(bp[nb + i]) : 0.f;
                 __syncwarp();
             }
-            // EPI_GELU_BWD: this lane's GELU inputs, a ring of two chunks; the
+            // EPI_MUL: this lane's factors, a ring of two chunks; the
             // first two load while the tile's MMAs run, and each slot is
             // refilled with the chunk after next once its chunk is done
             uint4 aux[2][4];
@@ -360,7 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                       : make_uint4(0, 0, 0, 0);
                 }
             };
-            if (EPI == EPI_GELU_BWD) {
+            if (EPI == EPI_MUL) {
                 load_aux(0, aux[0]);
                 if (CHUNKS > 1) load_aux(1, aux[1]);
             }
@@ -393,7 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
                 epi_chunk<EPI>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z, ncols(c),
                                lane);
-                if (EPI == EPI_GELU_BWD && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
+                if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();  // reconverge before the warp-collective TMEM ops
                 if (!more) break;
                 tc_ld_wait(rb);
@@ -401,7 +399,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
                 epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1), ys, z,
                                ncols(c + 1), lane);
-                if (EPI == EPI_GELU_BWD && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
+                if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
             }
@@ -556,9 +554,9 @@ bool launch_tc_layout(int epi, int a_mn, int b_mn, const CUtensorMap& ma, const 
     if (epi == EPI_GELU) {
         if (a_mn || b_mn) return false;
         launch_tc<BN, false, false, EPI_GELU>(ma, mb, md, md2, args, grid, s);
-    } else if (epi == EPI_GELU_BWD) {
+    } else if (epi == EPI_MUL) {
         if (a_mn || !b_mn) return false;
-        launch_tc<BN, false, true, EPI_GELU_BWD>(ma, mb, md, md2, args, grid, s);
+        launch_tc<BN, false, true, EPI_MUL>(ma, mb, md, md2, args, grid, s);
     } else if (!a_mn && !b_mn) {
         launch_tc<BN, false, false, EPI_NONE>(ma, mb, md, md2, args, grid, s);
     } else if (!a_mn && b_mn) {
@@ -629,15 +627,15 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
     return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s);
 }
 
-int launch_matmul_gelu(void* pre, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
+int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
                        int* status, cudaStream_t s) {
     if (M == 0 || N == 0) return 0;
-    return matmul_tc(EPI_GELU, pre, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s);
+    return matmul_tc(EPI_GELU, dgelu, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s);
 }
 
-int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* u, int M, int N, int K,
+int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* dgelu, int M, int N, int K,
                                 int* status, cudaStream_t s) {
     if (M == 0 || N == 0) return 0;
-    return matmul_tc(EPI_GELU_BWD, du, nullptr, (const bf16*)u, 0, dY, 0, W, 1, nullptr, M, N, K, nullptr, status,
+    return matmul_tc(EPI_MUL, du, nullptr, (const bf16*)dgelu, 0, dY, 0, W, 1, nullptr, M, N, K, nullptr, status,
                      s);
 }

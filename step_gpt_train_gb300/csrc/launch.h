@@ -67,13 +67,18 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
                               const float* lse, int B, int T, int C, int H, void* scratch, int* status,
                               cudaStream_t s);
 
-// bf16 linear forward with the GELU fused into its epilogue: pre = A W^T +
-// bias (A [M,K], W [N,K], both K-major), out = gelu(pre); see gpt2_op_matmul_gelu.
-int launch_matmul_gelu(void* pre, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
+// bf16 linear forward with the GELU fused into its epilogue: u = A W^T + bias
+// (A [M,K], W [N,K], both K-major) rounded to bf16, out = gelu(u), dgelu =
+// gelu'(u) (kept for the backward); see gpt2_op_matmul_gelu.
+int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
                        int* status, cudaStream_t s);
-// bf16 input gradient through a GELU: du = (dY W) * gelu'(u), dY [M,K], W [K,N].
-int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* u, int M, int N, int K,
+// bf16 input gradient through that GELU: du = bf16(dY W) * dgelu, dY [M,K], W [K,N].
+int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* dgelu, int M, int N, int K,
                                 int* status, cudaStream_t s);
+// out = gelu(u) and dgelu = gelu'(u) (dgelu may be u itself); n % 8 == 0.
+int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n, cudaStream_t s);
+// out = a * b elementwise; n % 8 == 0.
+int launch_mul(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s);
 
 // Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
 size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32);

@@ -416,7 +416,8 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
         TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
         TRY(res_ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, b.x, m->fwd_tmp, tidx(l, 6), BT));
         if (m->dtype == GPT2_MODE_BF16) {
-            // the GELU runs in the epilogue of its linear (both outputs kept)
+            // the GELU runs in the epilogue of its linear, which keeps gelu'
+            // (in fch) for the backward instead of the GELU input
             Op op(m, GPT2_K_MATMUL);
             TRY(op.done(launch_matmul_gelu(b.fch, b.fchg, b.ln2, P(m, tidx(l, 8)), P(m, tidx(l, 9)), BT, 4 * C, C,
                                            m->status, m->stream),
@@ -461,8 +462,8 @@ int backward_impl(gpt2* m) {
         LayerBufs& b = m->layers[l];
         // MLP branch
         if (m->dtype == GPT2_MODE_BF16) {
-            // dW of the MLP projection, then its input gradient with the GELU's
-            // derivative applied in the GEMM epilogue
+            // dW of the MLP projection, then its input gradient times the
+            // GELU's derivative (kept in fch by the forward), in the GEMM epilogue
             TRY(op_matmul(m, G(m, tidx(l, 10)), 1, m->dres, 1, b.fchg, 1, nullptr, C, 4 * C, BT));
             Op op(m, GPT2_K_MATMUL);
             TRY(op.done(launch_matmul_gelu_backward(m->dbig, m->dres, P(m, tidx(l, 10)), b.fch, BT, 4 * C, C,

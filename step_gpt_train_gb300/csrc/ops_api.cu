@@ -109,36 +109,36 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
                                 st(stream)));
 }
 
-int gpt2_op_matmul_gelu(int dtype, void* pre, void* out, const void* A, const void* W, const void* bias, int M, int N,
-                        int K, int* d_status, void* stream) {
-    if (!dt_ok(dtype) || !pre || !out || !A || !W || M < 0 || N < 0 || K < 1 || pre == out) return GPT2_ERR_ARG;
+int gpt2_op_matmul_gelu(int dtype, void* dgelu, void* out, const void* A, const void* W, const void* bias, int M,
+                        int N, int K, int* d_status, void* stream) {
+    if (!dt_ok(dtype) || !dgelu || !out || !A || !W || M < 0 || N < 0 || K < 1 || dgelu == out) return GPT2_ERR_ARG;
     if (dtype != GPT2_MODE_BF16 && ((int64_t)M * N) % 8) return GPT2_ERR_ARG;  // the GELU pass works on 8-vectors
     if (dtype == GPT2_MODE_BF16) {
         if (K % 8 || N % 8) return GPT2_ERR_ARG;
-        if (!al16(pre) || !al16(out) || !al16(A) || !al16(W) || (bias && !al16(bias))) return GPT2_ERR_ARG;
+        if (!al16(dgelu) || !al16(out) || !al16(A) || !al16(W) || (bias && !al16(bias))) return GPT2_ERR_ARG;
     }
     if ((int64_t)M * N == 0) return GPT2_OK;
     if (dtype == GPT2_MODE_BF16)
-        return finish(launch_matmul_gelu(pre, out, A, W, bias, M, N, K, d_status, st(stream)));
-    const int r = launch_matmul(dtype, pre, 0, A, 0, W, 0, bias, M, N, K, nullptr, d_status, st(stream));
+        return finish(launch_matmul_gelu(dgelu, out, A, W, bias, M, N, K, d_status, st(stream)));
+    const int r = launch_matmul(dtype, dgelu, 0, A, 0, W, 0, bias, M, N, K, nullptr, d_status, st(stream));
     if (r < 0) return r;
-    return finish(launch_gelu_forward(dtype, out, pre, (int64_t)M * N, st(stream)));
+    return finish(launch_gelu_both(dtype, out, dgelu, dgelu, (int64_t)M * N, st(stream)));
 }
 
-int gpt2_op_matmul_gelu_backward(int dtype, void* du, const void* dY, const void* W, const void* u, int M, int N, int K,
-                                 int* d_status, void* stream) {
-    if (!dt_ok(dtype) || !du || !dY || !W || !u || M < 0 || N < 0 || K < 1 || du == u) return GPT2_ERR_ARG;
-    if (dtype != GPT2_MODE_BF16 && ((int64_t)M * N) % 8) return GPT2_ERR_ARG;  // the GELU pass works on 8-vectors
+int gpt2_op_matmul_gelu_backward(int dtype, void* du, const void* dY, const void* W, const void* dgelu, int M, int N,
+                                 int K, int* d_status, void* stream) {
+    if (!dt_ok(dtype) || !du || !dY || !W || !dgelu || M < 0 || N < 0 || K < 1 || du == dgelu) return GPT2_ERR_ARG;
+    if (dtype != GPT2_MODE_BF16 && ((int64_t)M * N) % 8) return GPT2_ERR_ARG;  // the multiply works on 8-vectors
     if (dtype == GPT2_MODE_BF16) {
         if (K % 8 || N % 8) return GPT2_ERR_ARG;
-        if (!al16(du) || !al16(dY) || !al16(W) || !al16(u)) return GPT2_ERR_ARG;
+        if (!al16(du) || !al16(dY) || !al16(W) || !al16(dgelu)) return GPT2_ERR_ARG;
     }
     if ((int64_t)M * N == 0) return GPT2_OK;
     if (dtype == GPT2_MODE_BF16)
-        return finish(launch_matmul_gelu_backward(du, dY, W, u, M, N, K, d_status, st(stream)));
+        return finish(launch_matmul_gelu_backward(du, dY, W, dgelu, M, N, K, d_status, st(stream)));
     const int r = launch_matmul(dtype, du, 0, dY, 0, W, 1, nullptr, M, N, K, nullptr, d_status, st(stream));
     if (r < 0) return r;
-    return finish(launch_gelu_backward(dtype, du, u, du, (int64_t)M * N, st(stream)));
+    return finish(launch_mul(dtype, du, du, dgelu, (int64_t)M * N, st(stream)));
 }
 
 int gpt2_op_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,

@@ -365,19 +365,19 @@ def gpt2_op_matmul(D, A, a_mn, B, b_mn, M, N, K, bias=None, status=None, stream=
     return sc
 
 
-def gpt2_op_matmul_gelu(pre, out, A, W, bias=None, status=None, stream=None):
-    """pre = A W^T + bias, out = gelu(pre); A [M, K], W [N, K]."""
+def gpt2_op_matmul_gelu(dgelu, out, A, W, bias=None, status=None, stream=None):
+    """u = A W^T + bias; out = gelu(u), dgelu = gelu'(u); A [M, K], W [N, K]."""
     M, K = A.shape
     N = W.shape[0]
-    check(load_library().gpt2_op_matmul_gelu(_dtype_of(A), _p(pre), _p(out), _p(A), _p(W), _p(bias), M, N, K,
+    check(load_library().gpt2_op_matmul_gelu(_dtype_of(A), _p(dgelu), _p(out), _p(A), _p(W), _p(bias), M, N, K,
                                              _p(status), _s(stream)), "gpt2_op_matmul_gelu")
 
 
-def gpt2_op_matmul_gelu_backward(du, dY, W, u, status=None, stream=None):
-    """du = (dY W) * gelu'(u); dY [M, K], W [K, N], u [M, N]."""
+def gpt2_op_matmul_gelu_backward(du, dY, W, dgelu, status=None, stream=None):
+    """du = (dY W) * dgelu; dY [M, K], W [K, N], dgelu [M, N]."""
     M, K = dY.shape
     N = W.shape[1]
-    check(load_library().gpt2_op_matmul_gelu_backward(_dtype_of(dY), _p(du), _p(dY), _p(W), _p(u), M, N, K,
+    check(load_library().gpt2_op_matmul_gelu_backward(_dtype_of(dY), _p(du), _p(dY), _p(W), _p(dgelu), M, N, K,
                                                       _p(status), _s(stream)), "gpt2_op_matmul_gelu_backward")
 
 

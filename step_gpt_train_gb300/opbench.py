@@ -84,14 +84,14 @@ def main(argv=None):
         def setup():
             A, W, b = rnd(N, C), rnd(4 * C, C, std=0.02), rnd(4 * C)
             pre, out = torch.empty(N, 4 * C, device=dev, dtype=bf), torch.empty(N, 4 * C, device=dev, dtype=bf)
-            return lambda: g.gpt2_op_matmul_gelu(pre, out, A, W, b, stream=torch.cuda.current_stream().cuda_stream)
+            return lambda: g.gpt2_op_matmul_gelu(pre, out, A, W, b, stream=torch.cuda.current_stream())
         return setup, 2.0 * N * 4 * C * C, "flop"
 
     def gemm_gelu_bwd_op():  # the MLP projection's input gradient through the GELU
         def setup():
             dY, W, u = rnd(N, C), rnd(C, 4 * C, std=0.02), rnd(N, 4 * C)
             du = torch.empty(N, 4 * C, device=dev, dtype=bf)
-            return lambda: g.gpt2_op_matmul_gelu_backward(du, dY, W, u, stream=torch.cuda.current_stream().cuda_stream)
+            return lambda: g.gpt2_op_matmul_gelu_backward(du, dY, W, u, stream=torch.cuda.current_stream())
         return setup, 2.0 * N * 4 * C * C, "flop"
 
     ops["gemm_fc_fwd_gelu"] = gemm_gelu_op()
