@@ -35,8 +35,8 @@ constexpr int AT_HD = 64;                  // head size
 constexpr int AT_TILE = AT_M * AT_HD * 2;  // 16 KB: 128 rows of 64 bf16
 constexpr int AT_THREADS = 192;
 // shared memory: Q | K stage 0 | K stage 1 | V | P (two 64-key chunks) | barriers
-constexpr int AT_SMEM = 6 * AT_TILE + 256 + 1024;  // Q | K0 | K1 | V | P (2 chunks) | barriers
-constexpr uint32_t AT_TMEM_COLS = 256;     // S [0,128), O [128,192)
+constexpr int AT_SMEM = 4 * AT_TILE + 256 + 1024;  // Q | K0 | K1 | V | barriers
+constexpr uint32_t AT_TMEM_COLS = 256;     // S [0,128), O [128,192), P [192,256) (bf16 pairs)
 constexpr float AT_LN2 = 0.6931471805599453f;
 constexpr float AT_RESCALE = 8.f;          // log2 of the largest P before the reference max moves
 
@@ -57,10 +57,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     const uint32_t sQ = base;
     auto sK = [&](int st) { return base + (1 + st) * AT_TILE; };
     const uint32_t sV = base + 3 * AT_TILE;
-    const uint32_t sP = base + 4 * AT_TILE;
-    uint8_t* gP = gbase + 4 * AT_TILE;
-    const uint32_t bars = base + 6 * AT_TILE;
-    uint8_t* bar_area = gbase + 6 * AT_TILE;
+    const uint32_t bars = base + 4 * AT_TILE;
+    uint8_t* bar_area = gbase + 4 * AT_TILE;
     // barriers: q_full, k_full[2], k_empty[2], v_full, v_empty, s_full, s_free, p_full, p_free, o_done, drain
     const uint32_t q_full = bars;
     auto k_full = [&](int i) { return bars + 8u * (1 + i); };
@@ -154,8 +152,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < AT_N / 16; kk++)
-                    tc_mma(tmem + 128u, sw128_desc(sP + (kk >> 2) * AT_TILE + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(sV + kk * 2048, 8192, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV + kk * 2048, 8192, 1024), idesc_o,
+                              (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(p_free);
                 tc_commit(v_empty);
             }
@@ -182,18 +180,27 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);  // the MMA may now write S(j+1)
-            // scaled scores, masked on the diagonal block
+            // The row maximum of the raw scores (the scale is positive), with
+            // the keys after the query masked to -FLT_MAX on the diagonal block;
+            // eight independent maxima keep the dependency chains short.
             const bool diag = j == qt;
-            float mx = -FLT_MAX;
+            if (diag) {
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        if (j * AT_N + c * 32 + i > q) v[c][i] = __float_as_uint(-FLT_MAX);
+            }
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) m8[e] = -FLT_MAX;
 #pragma unroll
             for (int c = 0; c < 4; c++)
 #pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    float x = __uint_as_float(v[c][i]) * a.scale_log2;
-                    if (diag && j * AT_N + c * 32 + i > q) x = -FLT_MAX;
-                    v[c][i] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
-                }
+                for (int i = 0; i < 32; i++) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(v[c][i]));
+#pragma unroll
+            for (int e = 0; e < 4; e++) m8[e] = fmaxf(m8[e], m8[e + 4]);
+            const float mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])) * a.scale_log2;
             // move the reference max only when it grew by more than AT_RESCALE
             float factor = 1.f;
             const bool move = mx > m + AT_RESCALE;
@@ -202,19 +209,30 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                 m = mx;
                 l *= factor;
             }
-            // P as packed bf16 pairs: pk[c*16 + i/2] holds keys c*32+i, c*32+i+1
+            // P = exp2(s scale - m) as packed bf16 pairs (pk[c*16 + i/2] holds keys
+            // c*32+i, c*32+i+1), the row sum in four paired accumulators
             uint32_t pk[64];
+            const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-m, -m);
+            uint64_t l2[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int c = 0; c < 4; c++)
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float x0 = __uint_as_float(v[c][i]), x1 = __uint_as_float(v[c][i + 1]);
-                    const float p0 = x0 == -FLT_MAX ? 0.f : ex2_approx(x0 - m);
-                    const float p1 = x1 == -FLT_MAX ? 0.f : ex2_approx(x1 - m);
-                    l += p0 + p1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(v[c][i], v[c][i + 1]), scale2, nm2), x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    l2[(i >> 1) & 3] = f2_add(l2[(i >> 1) & 3], f2_pack(p0, p1));
                     __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
                     pk[c * 16 + i / 2] = *reinterpret_cast<uint32_t*>(&hh);
                 }
+            {
+                float s0, s1, s2, s3, s4, s5, s6, s7;
+                f2_unpack(l2[0], s0, s1);
+                f2_unpack(l2[1], s2, s3);
+                f2_unpack(l2[2], s4, s5);
+                f2_unpack(l2[3], s6, s7);
+                l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+            }
             // PV(j-1) has finished with the P buffer and with O
             if (!(ok = warp_wait(p_free, (j & 1) ^ 1u, abort_flag, a.status))) break;
             if (j > 0 && __any_sync(0xffffffffu, move)) {
@@ -231,14 +249,16 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                 tc_st_wait();
                 tc_fence_before();
             }
-            uint8_t* prow = gP + r * 128;
-#pragma unroll
-            for (int u = 0; u < 16; u++) {  // 16-byte units: keys 8u .. 8u+7
-                const uint4 w = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                const int kc = u >> 3, uu = u & 7;  // 64-key chunk, unit within the 128-byte row
-                *reinterpret_cast<uint4*>(prow + kc * AT_TILE + ((uu ^ (r & 7)) << 4)) = w;
+            // P to TMEM, the A operand of PV
+            {
+                uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+                uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+                tc_fence_after();
+                tc_st32(trow + 192u, p0);
+                tc_st32(trow + 224u, p1);
+                tc_st_wait();
+                tc_fence_before();
             }
-            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
