@@ -6,6 +6,7 @@
 // normalised probabilities are never stored. Columns V..Vp-1 (padding) get 0.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 #include <cfloat>
 
@@ -151,6 +152,125 @@ __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, 
     }
 }
 
+// The bf16 classifier as a persistent kernel: a CTA walks rows row0, row0 + G,
+// ... (G = grid size), each copied whole into shared memory by the bulk-copy
+// engine, reduced there and written back in place. With NBUF = 2 the next
+// row is copied into the other buffer while this one is processed; with
+// NBUF = 1 two CTAs share an SM and overlap each other's copies.
+template <int NT, int NBUF>
+__global__ void __launch_bounds__(NT, 2 / NBUF) classifier_stream_kernel(bf16* __restrict__ logits, float* __restrict__ losses,
+                                                                  const int32_t* __restrict__ targets, int N, int V,
+                                                                  int Vp, float dloss, int* status) {
+    extern __shared__ __align__(128) uint8_t cls_smem[];  // NBUF rows of Vp bf16
+    __shared__ float sh[33];
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int abort_flag;
+    const uint32_t row_bytes = (uint32_t)Vp * 2;
+    const bf16* bufs[2] = {reinterpret_cast<const bf16*>(cls_smem),
+                           reinterpret_cast<const bf16*>(cls_smem) + (NBUF == 2 ? Vp : 0)};
+    const uint32_t bar[2] = {tc::smem_addr(&bars[0]), tc::smem_addr(&bars[1])};
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar[0], 1);
+        tc::mbar_init(bar[1], 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    int issued[2] = {-1, -1};  // thread 0: phase parity of the last copy into each buffer
+    auto issue = [&](int row, int slot, int k) {
+        tc::mbar_expect_tx(bar[slot], row_bytes);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(logits + (int64_t)row * Vp);
+        const uint32_t dst = tc::smem_addr(bufs[slot]);
+        for (uint32_t off = 0; off < row_bytes; off += 32768u)
+            tc::bulk_load_1d(dst + off, src + off, row_bytes - off < 32768u ? row_bytes - off : 32768u, bar[slot]);
+        issued[slot] = (k >> 1) & 1;
+    };
+    const int nv = Vp / 8;
+    const int full_nv = V / 8;  // vectors wholly inside the real vocabulary
+    if (threadIdx.x == 0 && (int)blockIdx.x < N) issue(blockIdx.x, 0, 0);
+    int k = 0;
+    for (int row = blockIdx.x; row < N; row += gridDim.x, k++) {
+        const int slot = NBUF == 2 ? (k & 1) : 0;
+        const int next = row + gridDim.x;
+        // the other buffer was released by the barrier that ended the previous row
+        if (NBUF == 2 && threadIdx.x == 0 && next < N) issue(next, slot ^ 1, k + 1);
+        const bool ok = tc::mbar_wait(bar[slot], NBUF == 2 ? (k >> 1) & 1 : k & 1, &abort_flag, status);
+        if (__syncthreads_or(!ok)) break;  // one outcome for the whole block
+        const bf16* z = bufs[slot];
+        int tgt = targets[row];
+        if (tgt < 0 || tgt >= V) {
+            if (threadIdx.x == 0) set_status(status, GPT2_FLAG_TARGET_RANGE);
+            tgt = 0;
+        }
+        float m = -FLT_MAX;
+        for (int idx = threadIdx.x; idx < nv; idx += NT) {
+            float f[8];
+            load8(z + idx * 8, f);
+            if (idx < full_nv) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) m = fmaxf(m, f[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (idx * 8 + j < V) m = fmaxf(m, f[j]);
+            }
+        }
+        m = block_reduce<NT>(m, true, sh);
+        float s = 0.f;
+        for (int idx = threadIdx.x; idx < nv; idx += NT) {
+            float f[8];
+            load8(z + idx * 8, f);
+            if (idx < full_nv) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) s += exp_shift<bf16>(f[j], m);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (idx * 8 + j < V) s += exp_shift<bf16>(f[j], m);
+            }
+        }
+        s = block_reduce<NT>(s, false, sh);
+        const float scale = dloss / s;
+        const int tvec = tgt / 8;
+        bf16* zg = logits + (int64_t)row * Vp;
+        for (int idx = threadIdx.x; idx < nv; idx += NT) {
+            float f[8];
+            load8(z + idx * 8, f);
+            if (idx == tvec) {
+                const int jt = tgt % 8;
+                float zt = f[0];
+#pragma unroll
+                for (int j = 1; j < 8; j++)
+                    if (j == jt) zt = f[j];
+                losses[row] = m + logf(s) - zt;
+            }
+            if (idx < full_nv) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) f[j] = exp_shift<bf16>(f[j], m) * scale;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++) f[j] = idx * 8 + j < V ? exp_shift<bf16>(f[j], m) * scale : 0.f;
+            }
+            if (idx == tvec) {
+                const int jt = tgt % 8;
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (j == jt) f[j] -= dloss;
+            }
+            store8(zg + idx * 8, f);
+        }
+        __syncthreads();  // every thread is done with this buffer before it is refilled
+        if (NBUF == 1 && threadIdx.x == 0 && next < N) issue(next, 0, 2 * (k + 1));
+    }
+    // copies still in flight after an early exit
+    if (threadIdx.x == 0)
+        for (int b = 0; b < 2; b++)
+            if (issued[b] >= 0) tc::mbar_drain(bar[b], (uint32_t)issued[b], status);
+}
+
+#define CLS_STREAM_MAX_SMEM (220 * 1024)  // two rows per SM
+
 template <typename T, int NT>
 static int classifier_dispatch(void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
                                float dloss, int* status, cudaStream_t s) {
@@ -177,6 +297,21 @@ int launch_classifier(int dtype, void* logits, float* losses, const int32_t* tar
                       float dloss, int* status, cudaStream_t s) {
     if (N == 0) return 0;
     if (dtype == GPT2_MODE_BF16) {
+        const size_t smem = (size_t)Vp * 2 * 2;  // two rows per SM either way
+        if (Vp > 8 * 256 * 2 && smem <= CLS_STREAM_MAX_SMEM) {
+            // two CTAs of 512 threads per SM, one row buffer each (measured
+            // faster than one CTA with two buffers: the CTAs' phases interleave)
+            static bool configured = false;
+            if (!configured) {
+                cudaFuncSetAttribute(classifier_stream_kernel<512, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CLS_STREAM_MAX_SMEM / 2);
+                configured = true;
+            }
+            const int grid = N < 2 * gpt2_num_sms() ? N : 2 * gpt2_num_sms();
+            classifier_stream_kernel<512, 1><<<grid, 512, smem / 2, s>>>((bf16*)logits, losses, targets, N, V, Vp, dloss,
+                                                                         status);
+            return 1;
+        }
         if (Vp <= 8 * 256 * 2) return classifier_dispatch<bf16, 256>(logits, losses, targets, N, V, Vp, dloss, status, s);
         return classifier_dispatch<bf16, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s);
     }
