@@ -2,6 +2,7 @@
 // registers (16-byte vector loads), statistics by warp shuffles.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 #define LN_EPS 1e-5f
 #define LN_FWD_WARPS 8
@@ -332,6 +333,153 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     }
 }
 
+// bf16 pair (element 0 in the low half) to an fp32 pair.
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return tc::f2_pack(w << 16, w & 0xffff0000u); }
+
+// The bf16 staged backward with paired fp32 arithmetic (f32x2): the same ring
+// and the same per-element formulas as ln_bwd_staged_kernel, two columns per
+// instruction; gamma is held in shared memory as fp32 for the block. Column
+// pairs (2p, 2p+1) of a lane's 8-vector sit in one 64-bit accumulator.
+template <int VPL>
+__global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
+    ln_bwd_bf16_kernel(bf16* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
+                       const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ gamma,
+                       const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C) {
+    using namespace tc;
+    extern __shared__ __align__(16) uint8_t sm_raw[];
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int cv = C / 8;
+    const size_t g_bytes = ((size_t)C * 4 + 15) & ~(size_t)15;
+    float* sg = reinterpret_cast<float*>(sm_raw);  // gamma, fp32
+    const size_t row_bytes = (size_t)C * 2;
+    const size_t slot_bytes = 3 * row_bytes + 16;  // x | dy | residual gradient | mean, rstd
+    uint8_t* ring = sm_raw + g_bytes + (size_t)w * LN_STAGES * slot_bytes;
+    const int stride = gridDim.x * LN_BWD_WARPS;
+    const int row0 = blockIdx.x * LN_BWD_WARPS + w;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) sg[c] = __bfloat162float(gamma[c]);
+
+    auto issue = [&](int row, int slot) {
+        if (row < N) {
+            uint8_t* sb = ring + (size_t)slot * slot_bytes;
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int idx = lane + 32 * i;
+                if (idx < cv) {
+                    const size_t off = (size_t)idx * 16, goff = ((size_t)row * C + idx * 8) * 2;
+                    cp_async16(sb + off, (const uint8_t*)x + goff);
+                    cp_async16(sb + row_bytes + off, (const uint8_t*)dy + goff);
+                    if (accumulate) cp_async16(sb + 2 * row_bytes + off, (const uint8_t*)out + goff);
+                }
+            }
+            if (lane == 0) {
+                cp_async4(sb + 3 * row_bytes, mean + row);
+                cp_async4(sb + 3 * row_bytes + 4, rstd + row);
+            }
+        }
+        cp_async_commit();
+    };
+
+    uint64_t ag[VPL][4], ab[VPL][4], ao[VPL][4];
+#pragma unroll
+    for (int i = 0; i < VPL; i++)
+#pragma unroll
+        for (int p = 0; p < 4; p++) ag[i][p] = ab[i][p] = ao[i][p] = 0;
+    __syncthreads();  // gamma staged
+
+#pragma unroll
+    for (int k = 0; k < LN_STAGES - 1; k++) issue(row0 + k * stride, k);
+    int slot = 0;
+    for (int row = row0; row < N; row += stride) {
+        __syncwarp();
+        issue(row + (LN_STAGES - 1) * stride, (slot + LN_STAGES - 1) % LN_STAGES);
+        cp_async_wait<LN_STAGES - 1>();
+        __syncwarp();
+        const uint8_t* sb = ring + (size_t)slot * slot_bytes;
+        const float mu = reinterpret_cast<const float*>(sb + 3 * row_bytes)[0];
+        const float rs = reinterpret_cast<const float*>(sb + 3 * row_bytes)[1];
+        const uint64_t rs2 = f2_pack(rs, rs), nmr2 = f2_pack(-mu * rs, -mu * rs);
+        uint64_t s1 = 0, s2 = 0;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                const uint4 xr = *reinterpret_cast<const uint4*>(sb + idx * 16);
+                const uint4 dr = *reinterpret_cast<const uint4*>(sb + row_bytes + idx * 16);
+                const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w}, dw[4] = {dr.x, dr.y, dr.z, dr.w};
+                const uint64_t* g2 = reinterpret_cast<const uint64_t*>(sg + idx * 8);
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    const uint64_t x2 = bf2_to_f2(xw[p]), d2 = bf2_to_f2(dw[p]);
+                    const uint64_t xh = f2_fma(x2, rs2, nmr2);
+                    ag[i][p] = f2_fma(d2, xh, ag[i][p]);
+                    ab[i][p] = f2_add(ab[i][p], d2);
+                    const uint64_t dh = f2_mul(d2, g2[p]);
+                    s1 = f2_add(s1, dh);
+                    s2 = f2_fma(dh, xh, s2);
+                }
+            }
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(s1, a0, a1);
+        f2_unpack(s2, b0, b1);
+        const float m1 = warp_sum(a0 + a1) / (float)C;
+        const float m2 = warp_sum(b0 + b1) / (float)C;
+        const uint64_t m1_2 = f2_pack(m1, m1), m2_2 = f2_pack(m2, m2);
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                const uint4 xr = *reinterpret_cast<const uint4*>(sb + idx * 16);
+                const uint4 dr = *reinterpret_cast<const uint4*>(sb + row_bytes + idx * 16);
+                uint4 rr = make_uint4(0, 0, 0, 0);
+                if (accumulate) rr = *reinterpret_cast<const uint4*>(sb + 2 * row_bytes + idx * 16);
+                const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w}, dw[4] = {dr.x, dr.y, dr.z, dr.w};
+                const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+                const uint64_t* g2 = reinterpret_cast<const uint64_t*>(sg + idx * 8);
+                uint32_t ow[4];
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    const uint64_t xh = f2_fma(bf2_to_f2(xw[p]), rs2, nmr2);
+                    const uint64_t dh = f2_mul(bf2_to_f2(dw[p]), g2[p]);
+                    // rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat))
+                    uint64_t o = f2_mul(rs2, f2_sub(dh, f2_fma(xh, m2_2, m1_2)));
+                    if (accumulate) o = f2_add(o, bf2_to_f2(rw[p]));
+                    float o0, o1;
+                    f2_unpack(o, o0, o1);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+                    ow[p] = *reinterpret_cast<uint32_t*>(&h);
+                    if (np == 3) ao[i][p] = f2_add(ao[i][p], bf2_to_f2(ow[p]));
+                }
+                *reinterpret_cast<uint4*>(out + (int64_t)row * C + idx * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+        }
+        slot = (slot + 1) % LN_STAGES;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(sm_raw + g_bytes);  // [warp][np][C] over the rings
+#pragma unroll
+    for (int i = 0; i < VPL; i++) {
+        const int idx = lane + 32 * i;
+        if (idx < cv) {
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                float* r = red + (size_t)w * np * C + idx * 8 + 2 * p;
+                f2_unpack(ag[i][p], r[0], r[1]);
+                f2_unpack(ab[i][p], r[C], r[C + 1]);
+                if (np == 3) f2_unpack(ao[i][p], r[2 * C], r[2 * C + 1]);
+            }
+        }
+    }
+    __syncthreads();
+    for (int a = threadIdx.x; a < np * C; a += blockDim.x) {
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < LN_BWD_WARPS; k++) sum += red[(size_t)k * np * C + a];
+        partial[(size_t)blockIdx.x * np * C + a] = sum;
+    }
+}
+
 static size_t ln_staged_smem(int dtype, int C) {
     const size_t es = dtype == GPT2_MODE_BF16 ? 2 : 4;
     return (size_t)LN_BWD_WARPS * LN_STAGES * (3 * C * es + 16);
@@ -427,6 +575,21 @@ static void ln_bwd_staged_launch(int blocks, size_t smem, void* out, bool accumu
         (T*)out, accumulate, partial, np, (const T*)dy, (const T*)x, (const T*)gamma, mean, rstd, N, C);
 }
 
+template <int VPL>
+static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np,
+                               const void* dy, const void* x, const void* gamma, const float* mean,
+                               const float* rstd, int N, int C, cudaStream_t s) {
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(ln_bwd_bf16_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16) + 1024 * 4);
+        configured = true;
+    }
+    ln_bwd_bf16_kernel<VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((bf16*)out, accumulate, partial, np,
+                                                                     (const bf16*)dy, (const bf16*)x,
+                                                                     (const bf16*)gamma, mean, rstd, N, C);
+}
+
 static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, float* dbeta, float* dout_colsum,
                        const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, int N,
                        int C, void* scratch, cudaStream_t s) {
@@ -438,8 +601,8 @@ static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, flo
         const size_t smem = ln_staged_smem(dtype, C);
 #define LN_BWD_STAGED_CALL(V)                                                                                   \
     if (dtype == GPT2_MODE_BF16)                                                                                \
-        ln_bwd_staged_launch<bf16, V>(blocks, smem, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd, N, \
-                                      C, s);                                                                    \
+        ln_bwd_bf16_launch<V>(blocks, smem + (((size_t)C * 4 + 15) & ~(size_t)15), out, accumulate, partial_s,  \
+                              np, dy, x, gamma, mean, rstd, N, C, s);                                           \
     else                                                                                                        \
         ln_bwd_staged_launch<float, V>(blocks, smem, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd,  \
                                        N, C, s);

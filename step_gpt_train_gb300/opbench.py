@@ -142,8 +142,24 @@ def main(argv=None):
                                                               sc.data_ptr(), sc.numel(),
                                                               torch.cuda.current_stream().cuda_stream))
 
+    def ln_fwd_res():  # the step's form: residual join then LayerNorm
+        x, r, gm, bt = rnd(N, C), rnd(N, C), rnd(C), rnd(C)
+        y, xs = torch.empty_like(x), torch.empty_like(x)
+        mean, rstd = torch.empty(N, device=dev), torch.empty(N, device=dev)
+        return lambda: g.gpt2_op_residual_layernorm_forward(y, mean, rstd, xs, x, r, gm, bt)
+
+    def ln_bwd_res():  # the step's form: into the residual gradient, with the bias column sums
+        x, gm, bt, dy, dres = rnd(N, C), rnd(C), rnd(C), rnd(N, C), rnd(N, C)
+        y = torch.empty_like(x)
+        mean, rstd = torch.empty(N, device=dev), torch.empty(N, device=dev)
+        g.gpt2_op_layernorm_forward(y, mean, rstd, x, gm, bt)
+        dgm, dbt, dbias = (torch.empty(C, device=dev) for _ in range(3))
+        return lambda: g.gpt2_op_layernorm_backward_residual(dres, 1, dgm, dbt, dbias, dy, x, gm, mean, rstd)
+
     ops["layernorm_fwd"] = (ln_fwd, N * (2.0 * C * 2 + 8), "byte")
     ops["layernorm_bwd"] = (ln_bwd, N * (3.0 * C * 2 + 8), "byte")
+    ops["layernorm_fwd_res"] = (ln_fwd_res, N * (4.0 * C * 2 + 8), "byte")
+    ops["layernorm_bwd_res"] = (ln_bwd_res, N * (4.0 * C * 2 + 8), "byte")
 
     def gelu_fwd():
         u = rnd(N * 4 * C)
