@@ -14,26 +14,34 @@
 
 // ============================================================ backward: D = rowsum(dO * O)
 
+// One 8-element vector of dO and of O per thread; the hd/8 threads of a
+// (row, head) pair are adjacent lanes and add their partial dot products by a
+// shuffle tree (hd/8 is 1, 2, 4 or 8). All loads of a warp are contiguous.
 template <typename T>
 __global__ void attn_bwd_dot_kernel(float* __restrict__ D, const T* __restrict__ dout, const T* __restrict__ o,
                                     int B, int Tlen, int C, int H) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (b, t, h)
-    if (i >= (int64_t)B * Tlen * H) return;
-    const int h = (int)(i % H);
-    const int64_t bt = i / H;
-    const int hd = C / H;
-    const T* a = dout + bt * C + h * hd;
-    const T* c = o + bt * C + h * hd;
+    const int hd = C / H, parts = hd / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // ((b, t, h), part)
+    const int64_t pair = i / parts;
+    const int part = (int)(i % parts);
+    const bool valid = pair < (int64_t)B * Tlen * H;
     float s = 0.f;
-    for (int d = 0; d < hd; d += 8) {
+    if (valid) {
+        const int h = (int)(pair % H);
+        const int64_t bt = pair / H;
         float x[8], y[8];
-        load8(a + d, x);
-        load8(c + d, y);
+        load8(dout + bt * C + h * hd + part * 8, x);
+        load8(o + bt * C + h * hd + part * 8, y);
 #pragma unroll
         for (int j = 0; j < 8; j++) s += x[j] * y[j];
     }
-    const int b = (int)(bt / Tlen), t = (int)(bt % Tlen);
-    D[((int64_t)b * H + h) * Tlen + t] = s;
+    for (int off = parts / 2; off > 0; off /= 2) s += __shfl_xor_sync(0xffffffffu, s, off, parts);
+    if (valid && part == 0) {
+        const int h = (int)(pair % H);
+        const int64_t bt = pair / H;
+        const int b = (int)(bt / Tlen), t = (int)(bt % Tlen);
+        D[((int64_t)b * H + h) * Tlen + t] = s;
+    }
 }
 
 // ============================================================ fp32 path
@@ -195,10 +203,11 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
                               const float* lse, int B, int T, int C, int H, void* scratch, int* status,
                               cudaStream_t s) {
     const int hd = C / H;
+    if (hd != 8 && hd != 16 && hd != 32 && hd != 64) return GPT2_ERR_ARG;  // the head sizes built
     if (B * T == 0) return 0;
     float* D = (float*)scratch;
     const int64_t nrows = (int64_t)B * T * H;
-    const int dblocks = (int)((nrows + 255) / 256);
+    const int dblocks = (int)((nrows * (hd / 8) + 255) / 256);  // hd/8 threads per (row, head)
     const float scale = 1.0f / sqrtf((float)hd);
     if (dtype == GPT2_MODE_BF16) {
         if (hd != 64) return GPT2_ERR_ARG;

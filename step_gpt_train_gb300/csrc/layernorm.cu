@@ -8,6 +8,8 @@
 #define LN_FWD_WARPS 8
 #define LN_BWD_WARPS 8
 #define LN_BWD_MAX_BLOCKS 608  // four resident blocks on each of 152 SMs
+#define LN_STAGES 3                    // row slots per warp in the staged kernels
+#define LN_STAGED_MAX_ROW_BYTES 2048  // rows of up to 1024 bf16 or 512 fp32 values
 
 // y = (x - mean) * rstd * gamma + beta, biased variance, eps 1e-5.
 // With r != null the row normalised is the residual sum x + r, rounded to T
@@ -73,6 +75,107 @@ __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict
         mean[row] = mu;
         rstd[row] = rs;
     }
+}
+
+// The same forward arranged like the staged backward: a persistent grid,
+// warps striding over rows, each with a ring of LN_STAGES row slots in shared
+// memory (x, and r when given) that cp.async fills LN_STAGES - 1 rows ahead,
+// so that loads stay in flight while rows are normalised. A lane copies and
+// reads only its own 16-byte pieces. Same arithmetic as ln_fwd_kernel.
+#define LN_FWD_STAGED_WARPS 8
+template <typename T, int VPL>
+__global__ void __launch_bounds__(LN_FWD_STAGED_WARPS * 32)
+    ln_fwd_staged_kernel(T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, T* __restrict__ xsum,
+                         const T* __restrict__ x, const T* __restrict__ r, const T* __restrict__ gamma,
+                         const T* __restrict__ beta, int N, int C) {
+    extern __shared__ __align__(16) uint8_t sm_raw[];
+    constexpr int PIECES = (int)sizeof(T) / 2;  // 16-byte copies per 8-element vector
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int cv = C / 8;
+    const size_t row_bytes = (size_t)C * sizeof(T);
+    const size_t slot_bytes = 2 * row_bytes;  // x | r
+    uint8_t* ring = sm_raw + (size_t)w * LN_STAGES * slot_bytes;
+    const int stride = gridDim.x * LN_FWD_STAGED_WARPS;
+    const int row0 = blockIdx.x * LN_FWD_STAGED_WARPS + w;
+    auto issue = [&](int row, int slot) {
+        if (row < N) {
+            uint8_t* sb = ring + (size_t)slot * slot_bytes;
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int idx = lane + 32 * i;
+                if (idx < cv) {
+#pragma unroll
+                    for (int p = 0; p < PIECES; p++) {
+                        const size_t off = (size_t)idx * 8 * sizeof(T) + p * 16;
+                        const size_t goff = ((size_t)row * C + idx * 8) * sizeof(T) + p * 16;
+                        cp_async16(sb + off, (const uint8_t*)x + goff);
+                        if (r) cp_async16(sb + row_bytes + off, (const uint8_t*)r + goff);
+                    }
+                }
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < LN_STAGES - 1; k++) issue(row0 + k * stride, k);
+    int slot = 0;
+    for (int row = row0; row < N; row += stride) {
+        __syncwarp();
+        issue(row + (LN_STAGES - 1) * stride, (slot + LN_STAGES - 1) % LN_STAGES);
+        cp_async_wait<LN_STAGES - 1>();  // this lane's pieces of the row have landed
+        const uint8_t* sb = ring + (size_t)slot * slot_bytes;
+        const T* sx = reinterpret_cast<const T*>(sb);
+        const T* sr = reinterpret_cast<const T*>(sb + row_bytes);
+        float v[VPL][8];
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                load8(sx + idx * 8, v[i]);
+                if (r) {
+                    float u[8];
+                    load8(sr + idx * 8, u);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) v[i][j] = to_float(from_float<T>(v[i][j] + u[j]));
+                    store8(xsum + (int64_t)row * C + idx * 8, v[i]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; j++) sum += v[i][j];
+            }
+        }
+        const float mu = warp_sum(sum) / (float)C;
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            if (lane + 32 * i < cv) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float d = v[i][j] - mu;
+                    ss += d * d;
+                }
+            }
+        }
+        const float rs = 1.0f / sqrtf(warp_sum(ss) / (float)C + LN_EPS);
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                float g[8], b[8], o[8];
+                load8(gamma + idx * 8, g);
+                load8(beta + idx * 8, b);
+#pragma unroll
+                for (int j = 0; j < 8; j++) o[j] = (v[i][j] - mu) * rs * g[j] + b[j];
+                store8(y + (int64_t)row * C + idx * 8, o);
+            }
+        }
+        if (lane == 0) {
+            mean[row] = mu;
+            rstd[row] = rs;
+        }
+        slot = (slot + 1) % LN_STAGES;
+    }
+    cp_async_wait<0>();
 }
 
 // dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat)), dxhat = dy gamma.
@@ -197,8 +300,7 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1)
 // read after a warp barrier). The per-column sums are register accumulators
 // of the lane that owns the column; at the end the warps' sums go through
 // shared memory and are added in warp order into partial[block].
-#define LN_STAGES 3
-#define LN_STAGED_MAX_ROW_BYTES 2048  // rows of up to 1024 bf16 or 512 fp32 values
+
 template <typename T, int VPL>
 __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     ln_bwd_staged_kernel(T* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
@@ -499,10 +601,45 @@ static int ln_vpl(int C) { return (C / 8 + 31) / 32; }
         default: CALL(8); break; \
     }
 
+template <typename T, int VPL>
+static void ln_fwd_staged_launch(int blocks, size_t smem, void* y, float* mean, float* rstd, void* xsum,
+                                 const void* x, const void* r, const void* gamma, const void* beta, int N, int C,
+                                 cudaStream_t s) {
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(ln_fwd_staged_kernel<T, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LN_FWD_STAGED_WARPS * LN_STAGES * 2 * LN_STAGED_MAX_ROW_BYTES);
+        configured = true;
+    }
+    ln_fwd_staged_kernel<T, VPL><<<blocks, LN_FWD_STAGED_WARPS * 32, smem, s>>>(
+        (T*)y, mean, rstd, (T*)xsum, (const T*)x, (const T*)r, (const T*)gamma, (const T*)beta, N, C);
+}
+
 static int ln_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x, const void* r,
                       const void* gamma, const void* beta, int N, int C, cudaStream_t s) {
     const int blocks = (N + LN_FWD_WARPS - 1) / LN_FWD_WARPS;
     if (blocks == 0) return 0;
+    const size_t es = dtype == GPT2_MODE_BF16 ? 2 : 4;
+    if ((size_t)C * es <= LN_STAGED_MAX_ROW_BYTES) {
+        // three blocks of 8 warps per SM (74 KB of ring each at C = 768 bf16)
+        const size_t smem = (size_t)LN_FWD_STAGED_WARPS * LN_STAGES * 2 * C * es;
+        int sblocks = 3 * gpt2_num_sms();
+        const int need = (N + LN_FWD_STAGED_WARPS - 1) / LN_FWD_STAGED_WARPS;
+        if (sblocks > need) sblocks = need;
+#define LN_FWD_STAGED_CALL(V)                                                                                     \
+    if (dtype == GPT2_MODE_BF16)                                                                                  \
+        ln_fwd_staged_launch<bf16, V>(sblocks, smem, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s);           \
+    else                                                                                                          \
+        ln_fwd_staged_launch<float, V>(sblocks, smem, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s);
+        switch (ln_vpl(C)) {
+            case 1: LN_FWD_STAGED_CALL(1); break;
+            case 2: LN_FWD_STAGED_CALL(2); break;
+            case 3: LN_FWD_STAGED_CALL(3); break;
+            default: LN_FWD_STAGED_CALL(4); break;
+        }
+#undef LN_FWD_STAGED_CALL
+        return 1;
+    }
 #define LN_FWD_CALL(V)                                                                                            \
     if (dtype == GPT2_MODE_BF16)                                                                                  \
         ln_fwd_kernel<bf16, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((bf16*)y, mean, rstd, (bf16*)xsum,            \
