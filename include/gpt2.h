@@ -108,7 +108,8 @@ int gpt2_forward(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, i
                  float* loss_out);
 
 /* Backward pass of the last forward (which must have had targets).
- * Overwrites every parameter gradient (no accumulation). */
+ * Overwrites every parameter gradient, or adds to them after
+ * gpt2_set_grad_accumulation(m, 1). */
 int gpt2_backward(gpt2_t* m);
 
 /* One AdamW step on every parameter tensor from the last backward's
@@ -118,6 +119,47 @@ int gpt2_backward(gpt2_t* m);
  * Weight decay applies to every tensor. */
 int gpt2_adamw_step(gpt2_t* m, float lr, float beta1, float beta2, float eps,
                     float weight_decay, int t);
+
+/* ---- the training loop around the step (gradient accumulation, clipping,
+ * decay mask, learning-rate schedule) ---- */
+
+/* accumulate = 1: every following gpt2_backward adds its gradients to the ones
+ * held (each micro-batch contributes the gradient of its own mean loss);
+ * accumulate = 0 (the default): each backward overwrites them. Start an
+ * accumulation with gpt2_zero_grad(). Host-only; takes effect at the next
+ * backward. */
+int gpt2_set_grad_accumulation(gpt2_t* m, int accumulate);
+
+/* Set every parameter gradient to 0 (enqueued on the model's stream). */
+int gpt2_zero_grad(gpt2_t* m);
+
+/* ||g||_2 over all parameter gradients (fp32, deterministic two-stage sum),
+ * kept on the device; if norm_out is not NULL it is also written there after
+ * one stream synchronisation. */
+int gpt2_grad_norm(gpt2_t* m, float* norm_out);
+
+/* AdamW with the usual training-loop options. lr ... t as for
+ * gpt2_adamw_step. grad_scale > 0 multiplies every gradient first (e.g. 1/n
+ * after accumulating n micro-batches). max_grad_norm > 0 clips by the global
+ * norm: g *= min(1, max_grad_norm / (||g grad_scale|| + 1e-6)), the norm
+ * computed on the device (no host synchronisation); 0 disables clipping.
+ * decay_mask = 1 applies weight_decay only to the 2-D tensors (wte, wpe and
+ * the weight matrices) and not to biases and LayerNorm parameters; 0 applies
+ * it to every tensor. With grad_scale 1, max_grad_norm 0 and decay_mask 0 this
+ * is gpt2_adamw_step. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int t;
+    float grad_scale;
+    float max_grad_norm;
+    int decay_mask;
+} gpt2_adamw_config;
+int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* cfg);
+
+/* Learning rate of step t (1-based): linear warmup to lr_max over `warmup`
+ * steps, then a half-cosine from lr_max down to lr_min at step `total`, and
+ * lr_min after it. Host-only. */
+float gpt2_lr_cosine(int t, int warmup, int total, float lr_max, float lr_min);
 
 /* Free the handle (not the workspace, which the caller owns). */
 int gpt2_destroy(gpt2_t* m);

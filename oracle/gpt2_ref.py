@@ -334,6 +334,50 @@ def adamw_update(theta, g, m, v, lr, beta1, beta2, eps, weight_decay, t):
 
 
 # --------------------------------------------------------------------------
+# The training loop around the step (the "next" rows: gradient accumulation,
+# global-norm clipping, a weight-decay mask, a cosine learning-rate schedule)
+# --------------------------------------------------------------------------
+
+def global_grad_norm(grads: dict):
+    """||g||_2 over every parameter gradient, in float64."""
+    return math.sqrt(sum(float(np.sum(np.asarray(g, dtype=np.float64) ** 2)) for g in grads.values()))
+
+
+def clip_factor(norm, max_norm, grad_scale=1.0):
+    """The global-norm clip applied to g * grad_scale: min(1, max_norm / (||g|| grad_scale + 1e-6));
+    1 when max_norm is 0 (no clipping)."""
+    if max_norm <= 0:
+        return 1.0
+    return min(1.0, max_norm / (norm * grad_scale + 1e-6))
+
+
+def decays(name: str, arr) -> bool:
+    """Weight decay applies to the 2-D tensors (wte, wpe, weight matrices), not
+    to biases and LayerNorm parameters (the decay-mask reading)."""
+    return np.ndim(arr) == 2
+
+
+def adamw_update_ex(theta, g, m, v, lr, beta1, beta2, eps, weight_decay, t, grad_scale=1.0, clip=1.0):
+    """AdamW on the gradient g * grad_scale * clip (the moments, bias correction and
+    decoupled decay as in adamw_update)."""
+    return adamw_update(theta, np.asarray(g) * (grad_scale * clip), m, v, lr, beta1, beta2, eps, weight_decay, t)
+
+
+def lr_cosine(t, warmup, total, lr_max, lr_min):
+    """Step t (1-based): linear warmup over `warmup` steps to lr_max, then
+    lr_min + (lr_max - lr_min) (1 + cos(pi (t - warmup) / (total - warmup))) / 2
+    up to step `total`, lr_min after it."""
+    if t < 1:
+        return 0.0
+    if warmup > 0 and t <= warmup:
+        return lr_max * t / warmup
+    if t >= total:
+        return lr_min
+    frac = (t - warmup) / (total - warmup)
+    return lr_min + 0.5 * (lr_max - lr_min) * (1.0 + math.cos(math.pi * frac))
+
+
+# --------------------------------------------------------------------------
 # The whole step
 # --------------------------------------------------------------------------
 

@@ -51,7 +51,7 @@ int launch_encoder_forward(int dtype, void* x0, const int32_t* tokens, const voi
 // dwpe[t,:] = sum over b (in order) of dx0[b*T+t,:]: thread per (t, vector).
 template <typename T>
 __global__ void __launch_bounds__(256) encoder_bwd_wpe_kernel(float* __restrict__ dwpe, const T* __restrict__ dx0,
-                                                              int B, int Tlen, int C) {
+                                                              int B, int Tlen, int C, int accumulate) {
     const int cv = C / 8;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)Tlen * cv) return;
@@ -63,6 +63,12 @@ __global__ void __launch_bounds__(256) encoder_bwd_wpe_kernel(float* __restrict_
         load8(dx0 + ((int64_t)b * Tlen + t) * C + c, v);
 #pragma unroll
         for (int j = 0; j < 8; j++) acc[j] += v[j];
+    }
+    if (accumulate) {
+        float d[8];
+        load8(dwpe + (int64_t)t * C + c, d);
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[j] = d[j] + acc[j];
     }
     store8(dwpe + (int64_t)t * C + c, acc);
 }
@@ -308,7 +314,7 @@ static void enc_sum_dispatch(float* dwte, float* head, float* tail, const void* 
 }
 
 int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0, const int32_t* tokens, int B, int T,
-                            int C, void* scratch, cudaStream_t s) {
+                            int C, void* scratch, cudaStream_t s, int accumulate) {
     const int n = B * T;
     const int nblk = (n + ENC_TILE - 1) / ENC_TILE;
     const int nchunk = (n + ENC_CHUNK - 1) / ENC_CHUNK;
@@ -324,9 +330,9 @@ int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0
     {
         const int blocks = (T * (C / 8) + 255) / 256;
         if (dtype == GPT2_MODE_BF16)
-            encoder_bwd_wpe_kernel<bf16><<<blocks, 256, 0, s>>>(dwpe, (const bf16*)dx0, B, T, C);
+            encoder_bwd_wpe_kernel<bf16><<<blocks, 256, 0, s>>>(dwpe, (const bf16*)dx0, B, T, C, accumulate);
         else
-            encoder_bwd_wpe_kernel<float><<<blocks, 256, 0, s>>>(dwpe, (const float*)dx0, B, T, C);
+            encoder_bwd_wpe_kernel<float><<<blocks, 256, 0, s>>>(dwpe, (const float*)dx0, B, T, C, accumulate);
         launches++;
     }
     enc_init_kernel<<<(n + 255) / 256, 256, 0, s>>>(ka, va, tokens, n);
@@ -473,7 +479,7 @@ struct ColsumOut {
 };
 
 __global__ void __launch_bounds__(1024) colsum_kernel(ColsumOut outs, int seg, const float* __restrict__ in, int R,
-                                                      int ncols) {
+                                                      int ncols, int accumulate) {
     __shared__ float sm[32][33];
     const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
     const int c = blockIdx.x * 32 + tx;
@@ -488,14 +494,17 @@ __global__ void __launch_bounds__(1024) colsum_kernel(ColsumOut outs, int seg, c
         float t = 0.f;
         for (int k = 0; k < 32; k++) t += sm[k][tx];
         const int q = c / seg;
-        if (q < 3 && outs.p[q]) outs.p[q][c - q * seg] = t;
+        if (q < 3 && outs.p[q]) {
+            float* o = outs.p[q] + (c - q * seg);
+            *o = accumulate ? *o + t : t;
+        }
     }
 }
 
 int launch_colsum3(float* out0, float* out1, float* out2, int seg, const float* in, int R, int ncols,
-                   cudaStream_t s) {
+                   cudaStream_t s, int accumulate) {
     ColsumOut o = {{out0, out1, out2}};
-    colsum_kernel<<<(ncols + 31) / 32, 1024, 0, s>>>(o, seg, in, R, ncols);
+    colsum_kernel<<<(ncols + 31) / 32, 1024, 0, s>>>(o, seg, in, R, ncols, accumulate);
     return 1;
 }
 
@@ -508,14 +517,15 @@ size_t bias_backward_scratch(int N, int C) {
     return chunks * C * 4;
 }
 
-int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s) {
+int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s,
+                         int accumulate) {
     const int chunks = (N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
     dim3 grid((C + 255) / 256, chunks);
     if (dtype == GPT2_MODE_BF16)
         bias_partial_kernel<bf16><<<grid, 256, 0, s>>>((float*)scratch, (const bf16*)dy, N, C);
     else
         bias_partial_kernel<float><<<grid, 256, 0, s>>>((float*)scratch, (const float*)dy, N, C);
-    launch_colsum(dbias, nullptr, C, (const float*)scratch, chunks, C, s);
+    launch_colsum3(dbias, nullptr, nullptr, C, (const float*)scratch, chunks, C, s, accumulate);
     return 2;
 }
 
@@ -524,11 +534,19 @@ int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, 
 #define ADAM_UNROLL 2
 
 // Thread per 4 consecutive parameters (float4), ADAM_UNROLL groups per thread.
+// The gradient enters as g * grad_scale * clip, clip = min(1, max_norm /
+// (||g|| grad_scale + 1e-6)) when gnorm (the device-held ||g||) is given and
+// max_norm > 0; weight decay applies to the 64-element chunks whose bit is set
+// in decay_bits (every chunk when decay_bits is null).
 __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ theta, bf16* __restrict__ pbf,
                                                     const float* __restrict__ grad, float* __restrict__ m,
                                                     float* __restrict__ v, int64_t n4, float lr, float b1, float b2,
-                                                    float eps, float wd, float inv_bc1, float inv_bc2) {
+                                                    float eps, float wd, float inv_bc1, float inv_bc2,
+                                                    float grad_scale, const float* __restrict__ gnorm, float max_norm,
+                                                    const uint32_t* __restrict__ decay_bits) {
     const int64_t base = (int64_t)blockIdx.x * (256 * ADAM_UNROLL) + threadIdx.x;
+    float gs = grad_scale;
+    if (gnorm && max_norm > 0.f) gs *= fminf(1.f, max_norm / (*gnorm * grad_scale + 1e-6f));
     float4 th[ADAM_UNROLL], g[ADAM_UNROLL], mm[ADAM_UNROLL], vv[ADAM_UNROLL];
 #pragma unroll
     for (int u = 0; u < ADAM_UNROLL; u++) {
@@ -548,14 +566,16 @@ __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ theta, b
         const float* pg = &g[u].x;
         float* pm = &mm[u].x;
         float* pv = &vv[u].x;
+        // float4 i holds elements 4i..4i+3, in 64-element chunk i / 16
+        const float wdu = decay_bits && !((decay_bits[i >> 9] >> ((i >> 4) & 31)) & 1u) ? 0.f : wd;
 #pragma unroll
         for (int j = 0; j < 4; j++) {
-            const float gj = pg[j];
+            const float gj = pg[j] * gs;
             pm[j] = b1 * pm[j] + (1.f - b1) * gj;
             pv[j] = b2 * pv[j] + (1.f - b2) * gj * gj;
             const float mhat = pm[j] * inv_bc1;
             const float vhat = pv[j] * inv_bc2;
-            pt[j] = pt[j] - lr * (mhat / (sqrtf(vhat) + eps) + wd * pt[j]);
+            pt[j] = pt[j] - lr * (mhat / (sqrtf(vhat) + eps) + wdu * pt[j]);
         }
         __stcs(reinterpret_cast<float4*>(theta) + i, th[u]);
         __stcs(reinterpret_cast<float4*>(m) + i, mm[u]);
@@ -572,7 +592,8 @@ __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ theta, b
 }
 
 int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v, int64_t n, float lr, float b1,
-                 float b2, float eps, float wd, int t, cudaStream_t s) {
+                 float b2, float eps, float wd, int t, cudaStream_t s, float grad_scale, const float* gnorm,
+                 float max_norm, const uint32_t* decay_bits) {
     const int64_t n4 = n / 4;
     const double bc1 = 1.0 - pow((double)b1, (double)t);
     const double bc2 = 1.0 - pow((double)b2, (double)t);
@@ -580,6 +601,57 @@ int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v
     const int blocks = (int)((n4 + per_block - 1) / per_block);
     if (blocks == 0) return 0;
     adamw_kernel<<<blocks, 256, 0, s>>>(master, (bf16*)pbf, grad, m, v, n4, lr, b1, b2, eps, wd,
-                                        (float)(1.0 / bc1), (float)(1.0 / bc2));
+                                        (float)(1.0 / bc1), (float)(1.0 / bc2), grad_scale, gnorm, max_norm,
+                                        decay_bits);
     return 1;
+}
+
+// ===================================================================== gradient norm
+
+// ||g||_2 over n fp32 values (n % 4 == 0), deterministic: block b sums its
+// fixed contiguous range of float4s (thread t takes every 256th from t, then a
+// fixed shuffle tree), one block adds the GN_BLOCKS partial sums in order.
+#define GN_BLOCKS 1024
+
+__global__ void __launch_bounds__(256) grad_sumsq_kernel(float* __restrict__ partial, const float* __restrict__ g,
+                                                         int64_t n4) {
+    __shared__ float sh[8];
+    const int64_t per = (n4 + GN_BLOCKS - 1) / GN_BLOCKS;
+    const int64_t lo = (int64_t)blockIdx.x * per;
+    const int64_t hi = lo + per < n4 ? lo + per : n4;
+    float acc = 0.f;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += 256) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(g) + i);
+        acc += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    acc = warp_sum(acc);
+    if (threadIdx.x % 32 == 0) sh[threadIdx.x / 32] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; w++) t += sh[w];
+        partial[blockIdx.x] = t;
+    }
+}
+
+__global__ void __launch_bounds__(1024) grad_norm_final_kernel(float* __restrict__ out,
+                                                               const float* __restrict__ partial) {
+    __shared__ float sh[32];
+    float v = partial[threadIdx.x];  // GN_BLOCKS == blockDim.x
+    v = warp_sum(v);
+    if (threadIdx.x % 32 == 0) sh[threadIdx.x / 32] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 32; w++) t += sh[w];
+        *out = sqrtf(t);
+    }
+}
+
+size_t grad_norm_scratch() { return GN_BLOCKS * 4; }
+
+int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s) {
+    grad_sumsq_kernel<<<GN_BLOCKS, 256, 0, s>>>(partial, g, n / 4);
+    grad_norm_final_kernel<<<1, GN_BLOCKS, 0, s>>>(norm_out, partial);
+    return 2;
 }

@@ -3,16 +3,17 @@
 #include "common.cuh"
 #include "launch.h"
 
-size_t matmul_tc_scratch(int M, int N, int K, int d_fp32);
+size_t matmul_tc_scratch(int M, int N, int K, int d_fp32, int accumulate);
 int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
-                     int N, int K, void* scratch, int* status, cudaStream_t s);
+                     int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate);
 
 // 64 x 64 output tile, 16-deep k slices through shared memory, 256 threads,
-// 4 x 4 outputs per thread. A(m,k) = A[m*K+k] or A[k*M+m]; B likewise.
+// 4 x 4 outputs per thread. A(m,k) = A[m*K+k] or A[k*M+m]; B likewise. With
+// accumulate the result is added to D.
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(256) gemm_f32_kernel(float* __restrict__ D, const float* __restrict__ A,
                                                        const float* __restrict__ B, const float* __restrict__ bias,
-                                                       int M, int N, int K) {
+                                                       int M, int N, int K, int accumulate) {
     __shared__ float As[16][64 + 4];
     __shared__ float Bs[16][64 + 4];
     const int tid = threadIdx.x;
@@ -64,29 +65,32 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(float* __restrict__ D, co
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             const int n = n0 + tx * 4 + j;
-            if (n < N) D[(int64_t)m * N + n] = acc[i][j] + (bias ? bias[n] : 0.f);
+            if (n < N) {
+                const float v = acc[i][j] + (bias ? bias[n] : 0.f);
+                D[(int64_t)m * N + n] = accumulate ? D[(int64_t)m * N + n] + v : v;
+            }
         }
     }
 }
 
-size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32) {
-    if (dtype == GPT2_MODE_BF16) return matmul_tc_scratch(M, N, K, d_fp32);
+size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32, int accumulate) {
+    if (dtype == GPT2_MODE_BF16) return matmul_tc_scratch(M, N, K, d_fp32, accumulate);
     return 0;
 }
 
 int launch_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias,
-                  int M, int N, int K, void* scratch, int* status, cudaStream_t s) {
+                  int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate) {
     if (M == 0 || N == 0) return 0;
     if (dtype == GPT2_MODE_BF16)
-        return launch_matmul_tc(D, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s);
+        return launch_matmul_tc(D, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s, accumulate);
     dim3 grid((N + 63) / 64, (M + 63) / 64);
     float* d = (float*)D;
     const float* a = (const float*)A;
     const float* b = (const float*)B;
     const float* bb = (const float*)bias;
-    if (!a_mn && !b_mn) gemm_f32_kernel<false, false><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K);
-    else if (!a_mn && b_mn) gemm_f32_kernel<false, true><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K);
-    else if (a_mn && !b_mn) gemm_f32_kernel<true, false><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K);
-    else gemm_f32_kernel<true, true><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K);
+    if (!a_mn && !b_mn) gemm_f32_kernel<false, false><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K, accumulate);
+    else if (!a_mn && b_mn) gemm_f32_kernel<false, true><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K, accumulate);
+    else if (a_mn && !b_mn) gemm_f32_kernel<true, false><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K, accumulate);
+    else gemm_f32_kernel<true, true><<<grid, 256, 0, s>>>(d, a, b, bb, M, N, K, accumulate);
     return 1;
 }

@@ -71,7 +71,8 @@ struct GemmArgs {
     int* status;
     int M, N, K;
     int d_fp32;
-    int splits;          // k-ranges per tile (1: whole tiles, direct output)
+    int splits;          // k-ranges per tile
+    int partials;        // 1: store fp32 partial tiles for the reduce kernel (split-K or accumulation)
     int kbs;             // k-blocks per split
     int n_tiles;         // ceil(N / BN)
     int units;           // m_tiles * n_tiles * splits
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float* bias_s = reinterpret_cast<float*>(bar_area + Cfg::BAR_BYTES) + ew * (BN / 2);
         uint8_t* stage = out_stage + ew * Cfg::OUT_STAGE_BYTES;
         const uint32_t stage_addr = smem_addr(stage);
-        const bool use_bias = g.bias != nullptr && g.splits == 1;
+        const bool use_bias = g.bias != nullptr && !g.partials;
         int acc = 0;
         uint32_t acc_phase = 0;
         Work w;
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int c = 0; c < CHUNKS; c++)
                     if (n0 + (cfirst + c) * 32 < g.N) nchunks = c + 1;
             }
-            const bool split = g.splits > 1;
+            const bool split = g.partials != 0;
             const bool fp32_out = split || g.d_fp32 != 0;
             // split partials are stored tile-local: [unit][128 rows][BN columns]
             const int z = split ? w.z : 0;
@@ -426,11 +427,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Split-K reduce: D[m][n] (fp32) = bias[n] (if any) + the partial tiles of
-// the tile of (m, n), added in split order. 8 consecutive columns per thread
-// (N and BN are multiples of 8).
+// the tile of (m, n), added in split order; with accumulate, added to D's
+// current value. 8 consecutive columns per thread (N and BN are multiples of 8).
 __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ D, const float* __restrict__ partial,
                                                            const bf16* __restrict__ bias, int M, int N, int BN,
-                                                           int n_tiles, int splits) {
+                                                           int n_tiles, int splits, int accumulate) {
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= (int64_t)M * N) return;
     const int m = (int)(i / N), n = (int)(i % N);
@@ -439,6 +440,12 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ D
     const float* p = partial + tile * splits * tile_elems + (int64_t)(m % BM) * BN + n % BN;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (bias) load8(bias + n, acc);
+    if (accumulate) {
+        float d[8];
+        load8(D + i, d);
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[j] += d[j];
+    }
     for (int sp = 0; sp < splits; sp++) {
         float v[8];
         load8(p + sp * tile_elems, v);
@@ -571,29 +578,32 @@ bool launch_tc_layout(int epi, int a_mn, int b_mn, const CUtensorMap& ma, const 
 
 }  // namespace
 
-size_t matmul_tc_scratch(int M, int N, int K, int d_fp32) {
+size_t matmul_tc_scratch(int M, int N, int K, int d_fp32, int accumulate) {
     Plan p = make_plan(M, N, K, d_fp32);
-    return p.splits > 1 ? (size_t)p.units * BM * p.bn * 4 : 0;
+    return p.splits > 1 || (d_fp32 && accumulate) ? (size_t)p.units * BM * p.bn * 4 : 0;
 }
 
 namespace {
 
 // D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
 int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
-              int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s) {
+              int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s,
+              int accumulate = 0) {
     Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
+    // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
+    const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     CUtensorMap ma, mb;
     bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
     ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
                      : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
     CUtensorMap md, md2;
-    if (p.splits > 1) ok = ok && make_out_map(&md, scratch, true, (uint64_t)p.bn, BM, (uint64_t)p.units);
+    if (partials) ok = ok && make_out_map(&md, scratch, true, (uint64_t)p.bn, BM, (uint64_t)p.units);
     else ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
     if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
     else md2 = md;
     if (!ok) return GPT2_ERR_CUDA;
     GemmArgs g;
-    g.bias = p.splits > 1 ? nullptr : bias;
+    g.bias = partials ? nullptr : bias;
     g.aux = aux;
     g.status = status;
     g.M = M;
@@ -601,6 +611,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     g.K = K;
     g.d_fp32 = d_fp32;
     g.splits = p.splits;
+    g.partials = partials ? 1 : 0;
     g.kbs = p.kbs;
     g.n_tiles = p.n_tiles;
     g.units = p.units;
@@ -610,11 +621,11 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     else if (p.bn == 192) launched = launch_tc_layout<192>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else launched = launch_tc_layout<256>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     if (!launched) return GPT2_ERR_ARG;
-    if (p.splits > 1) {
+    if (partials) {
         const int64_t MN = (int64_t)M * N;
         const int blocks = (int)((MN / 8 + 255) / 256);
         split_reduce_kernel<<<blocks, 256, 0, s>>>((float*)D, (const float*)scratch, (const bf16*)bias, M, N, p.bn,
-                                                   p.n_tiles, p.splits);
+                                                   p.n_tiles, p.splits, accumulate && d_fp32 ? 1 : 0);
         return 2;
     }
     return 1;
@@ -623,8 +634,9 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
 }  // namespace
 
 int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
-                     int N, int K, void* scratch, int* status, cudaStream_t s) {
-    return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s);
+                     int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate) {
+    return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s,
+                     accumulate);
 }
 
 int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,

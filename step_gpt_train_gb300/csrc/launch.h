@@ -12,8 +12,10 @@
 int launch_encoder_forward(int dtype, void* x0, const int32_t* tokens, const void* wte, const void* wpe, int B,
                            int T, int C, int V, int* status, cudaStream_t s);
 size_t encoder_backward_scratch(int B, int T, int C);
+// dwte rows of the ids += the embedding gradient (dwte holds the LM head's
+// part); dwpe[t] = (or +=, with accumulate) the column sums over the batch.
 int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0, const int32_t* tokens, int B, int T,
-                            int C, void* scratch, cudaStream_t s);
+                            int C, void* scratch, cudaStream_t s, int accumulate = 0);
 
 int launch_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
                              const void* beta, int N, int C, cudaStream_t s);
@@ -29,10 +31,11 @@ int launch_residual_layernorm_forward(int dtype, void* y, float* mean, float* rs
                                       cudaStream_t s);
 // LayerNorm backward into the residual gradient: dres = dx (accumulate == 0)
 // or dres += dx; dres_colsum (optional) = column sums of the resulting dres.
+// grad_accumulate: dgamma, dbeta and dres_colsum are added to instead of overwritten.
 int launch_layernorm_backward_residual(int dtype, void* dres, int accumulate, float* dgamma, float* dbeta,
                                        float* dres_colsum, const void* dy, const void* x, const void* gamma,
                                        const float* mean, const float* rstd, int N, int C, void* scratch,
-                                       cudaStream_t s);
+                                       cudaStream_t s, int grad_accumulate = 0);
 
 int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream_t s);
 int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s);
@@ -43,17 +46,25 @@ int launch_residual_backward(int dtype, void* dres, const void* dbranch, int64_t
 int launch_colsum(float* out, float* out2, int split, const float* in, int R, int ncols, cudaStream_t s);
 // out_q[c] = column sums of column q * seg + c of in [R, ncols], q < 3 (null outputs skipped).
 int launch_colsum3(float* out0, float* out1, float* out2, int seg, const float* in, int R, int ncols,
-                   cudaStream_t s);
+                   cudaStream_t s, int accumulate = 0);
 
 size_t bias_backward_scratch(int N, int C);
-int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s);
+int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s,
+                         int accumulate = 0);
 
 int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
                       float dloss, int* status, cudaStream_t s);
 int launch_mean_loss(float* out, const float* losses, int N, cudaStream_t s);
 
+// grad_scale multiplies the gradient; with gnorm (device ||g||) and max_norm > 0
+// the gradient is also clipped to max_norm; decay_bits (one bit per 64-element
+// chunk, null = all) selects where weight decay applies.
 int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v, int64_t n, float lr, float b1,
-                 float b2, float eps, float wd, int t, cudaStream_t s);
+                 float b2, float eps, float wd, int t, cudaStream_t s, float grad_scale = 1.f,
+                 const float* gnorm = nullptr, float max_norm = 0.f, const uint32_t* decay_bits = nullptr);
+// *norm_out = ||g||_2 over n fp32 values (n % 4 == 0), deterministic; partial: grad_norm_scratch() bytes.
+size_t grad_norm_scratch();
+int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s);
 
 int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
                              int* status, cudaStream_t s);
@@ -81,6 +92,8 @@ int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n
 int launch_mul(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s);
 
 // Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
-size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32);
+// accumulate (fp32 D only): D += the product instead of D = it; the scratch
+// size then covers the partial tiles that route through the reduce kernel.
+size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32, int accumulate = 0);
 int launch_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias,
-                  int M, int N, int K, void* scratch, int* status, cudaStream_t s);
+                  int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate = 0);

@@ -729,7 +729,7 @@ static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumula
 
 static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, float* dbeta, float* dout_colsum,
                        const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, int N,
-                       int C, void* scratch, cudaStream_t s) {
+                       int C, void* scratch, cudaStream_t s, int grad_accumulate = 0) {
     const int np = dout_colsum ? 3 : 2;
     float* partial_s = (float*)scratch;
     if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
@@ -750,7 +750,7 @@ static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, flo
             default: LN_BWD_STAGED_CALL(4); break;
         }
 #undef LN_BWD_STAGED_CALL
-        launch_colsum3(dgamma, dbeta, dout_colsum, C, partial_s, blocks, np * C, s);
+        launch_colsum3(dgamma, dbeta, dout_colsum, C, partial_s, blocks, np * C, s, grad_accumulate);
         return 2;
     }
     const int blocks = ln_bwd_blocks(N);
@@ -763,7 +763,7 @@ static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, flo
         ln_bwd_launch<float, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);
     LN_DISPATCH(ln_vpl(C), LN_BWD_CALL)
 #undef LN_BWD_CALL
-    launch_colsum3(dgamma, dbeta, dout_colsum, C, partial, blocks, np * C, s);
+    launch_colsum3(dgamma, dbeta, dout_colsum, C, partial, blocks, np * C, s, grad_accumulate);
     return 2;
 }
 
@@ -776,7 +776,7 @@ int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, 
 int launch_layernorm_backward_residual(int dtype, void* dres, int accumulate, float* dgamma, float* dbeta,
                                        float* dres_colsum, const void* dy, const void* x, const void* gamma,
                                        const float* mean, const float* rstd, int N, int C, void* scratch,
-                                       cudaStream_t s) {
+                                       cudaStream_t s, int grad_accumulate) {
     return ln_backward(dtype, dres, accumulate != 0, dgamma, dbeta, dres_colsum, dy, x, gamma, mean, rstd, N, C,
-                       scratch, s);
+                       scratch, s, grad_accumulate);
 }

@@ -70,6 +70,10 @@ struct gpt2 {
     size_t scratch_bytes;
     int B, T;
     int state;  // 0: none, 1: forward with targets done, 2: backward done
+    int grad_accum;          // backward adds into the gradients instead of overwriting them
+    float* gnorm;            // device: ||g||_2 of the last gpt2_grad_norm / clipped AdamW step
+    float* gnorm_partial;    // device: its per-block partial sums
+    uint32_t* decay_bits;    // device: one bit per 64-element chunk, set for the 2-D tensors
     int64_t launches;
     int64_t fam_calls[GPT2_K_COUNT], fam_launches[GPT2_K_COUNT];
     double fam_work[GPT2_K_COUNT], fam_ms[GPT2_K_COUNT];
@@ -155,6 +159,8 @@ size_t plan(const gpt2_config* c, gpt2* m) {
     const size_t o_grads = take((size_t)np * 4);
     const size_t o_m = take((size_t)np * 4);
     const size_t o_v = take((size_t)np * 4);
+    const size_t o_gnp = take(grad_norm_scratch());
+    const size_t o_decay = take((((size_t)np / 64 + 1) + 31) / 32 * 4);
     std::vector<size_t> lo(13 * L);
     for (size_t l = 0; l < L; l++) {
         size_t* p = &lo[13 * l];
@@ -191,11 +197,11 @@ size_t plan(const gpt2_config* c, gpt2* m) {
     const int outs[4] = {3 * iC, iC, 4 * iC, iC};
     const int ins[4] = {iC, iC, iC, 4 * iC};
     for (int k = 0; k < 4; k++) {
-        need(matmul_scratch(dt, outs[k], ins[k], iBT, 1));       // dW
+        need(matmul_scratch(dt, outs[k], ins[k], iBT, 1, 1));    // dW (also when accumulating)
         need(matmul_scratch(dt, iBT, ins[k], outs[k], 0));       // dX
         need(bias_backward_scratch(iBT, outs[k]));
     }
-    need(matmul_scratch(dt, iVp, iC, iBT, 1));
+    need(matmul_scratch(dt, iVp, iC, iBT, 1, 1));
     need(matmul_scratch(dt, iBT, iC, iVp, 0));
     need(layernorm_backward_scratch(iBT, iC));
     need(attention_backward_scratch(c->max_B, c->max_T, (int)H));
@@ -213,6 +219,9 @@ size_t plan(const gpt2_config* c, gpt2* m) {
         m->grads = (float*)(w + o_grads);
         m->adam_m = (float*)(w + o_m);
         m->adam_v = (float*)(w + o_v);
+        m->gnorm = (float*)(w + o_status + 128);
+        m->gnorm_partial = (float*)(w + o_gnp);
+        m->decay_bits = (uint32_t*)(w + o_decay);
         m->layers.resize(L);
         for (size_t l = 0; l < L; l++) {
             size_t* p = &lo[13 * l];
@@ -343,10 +352,10 @@ inline void* P(gpt2* m, int i) { return (uint8_t*)m->params + (size_t)m->tensors
 inline float* G(gpt2* m, int i) { return m->grads + m->tensors[i].offset; }
 
 int op_matmul(gpt2* m, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
-              int N, int K) {
+              int N, int K, int accumulate = 0) {
     Op op(m, GPT2_K_MATMUL);
     return op.done(launch_matmul(m->dtype, D, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, m->scratch, m->status,
-                                 m->stream),
+                                 m->stream, accumulate),
                    2.0 * M * N * K);
 }
 
@@ -358,10 +367,10 @@ int linear_fwd(gpt2* m, void* y, const void* x, int wi, int bi, int BT, int in, 
 // dx = dy W, dW = dy^T x, db = column sums of dy.
 int linear_bwd(gpt2* m, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in, int out) {
     TRY(op_matmul(m, dx, 0, dy, 0, P(m, wi), 1, nullptr, BT, in, out));
-    TRY(op_matmul(m, G(m, wi), 1, dy, 1, x, 1, nullptr, out, in, BT));
+    TRY(op_matmul(m, G(m, wi), 1, dy, 1, x, 1, nullptr, out, in, BT, m->grad_accum));
     if (bi >= 0) {
         Op op(m, GPT2_K_BIAS_BWD);
-        TRY(op.done(launch_bias_backward(m->dtype, G(m, bi), dy, BT, out, m->scratch, m->stream),
+        TRY(op.done(launch_bias_backward(m->dtype, G(m, bi), dy, BT, out, m->scratch, m->stream, m->grad_accum),
                     (double)BT * out * m->act + out * 4.0));
     }
     return GPT2_OK;
@@ -389,7 +398,7 @@ int ln_bwd_res(gpt2* m, int accumulate, const void* dy, const void* x, int gi, c
     Op op(m, GPT2_K_LAYERNORM_BWD);
     return op.done(launch_layernorm_backward_residual(m->dtype, m->dres, accumulate, G(m, gi), G(m, gi + 1),
                                                       bi >= 0 ? G(m, bi) : nullptr, dy, x, P(m, gi), mean, rstd, BT,
-                                                      m->C, m->scratch, m->stream),
+                                                      m->C, m->scratch, m->stream, m->grad_accum),
                    (double)BT * ((3.0 + accumulate) * m->C * m->act + 8));
 }
 
@@ -454,7 +463,7 @@ int backward_impl(gpt2* m) {
     const int B = m->B, T = m->T, BT = B * T, C = m->C, L = m->L;
     // LM head (tied with wte): dlnf = dlogits wte; dwte = dlogits^T lnf (overwrites dwte)
     TRY(op_matmul(m, m->dtmp, 0, m->logits, 0, P(m, T_WTE), 1, nullptr, BT, C, m->Vp));
-    TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT));
+    TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT, m->grad_accum));
     // the LayerNorm backwards write the residual gradient dres and, on the
     // way, the bias gradient of the projection whose output joins there
     TRY(ln_bwd_res(m, 0, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, tidx(L - 1, 11), BT));
@@ -464,7 +473,7 @@ int backward_impl(gpt2* m) {
         if (m->dtype == GPT2_MODE_BF16) {
             // dW of the MLP projection, then its input gradient times the
             // GELU's derivative (kept in fch by the forward), in the GEMM epilogue
-            TRY(op_matmul(m, G(m, tidx(l, 10)), 1, m->dres, 1, b.fchg, 1, nullptr, C, 4 * C, BT));
+            TRY(op_matmul(m, G(m, tidx(l, 10)), 1, m->dres, 1, b.fchg, 1, nullptr, C, 4 * C, BT, m->grad_accum));
             Op op(m, GPT2_K_MATMUL);
             TRY(op.done(launch_matmul_gelu_backward(m->dbig, m->dres, P(m, tidx(l, 10)), b.fch, BT, 4 * C, C,
                                                     m->status, m->stream),
@@ -488,12 +497,12 @@ int backward_impl(gpt2* m) {
         TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
         TRY(ln_bwd_res(m, 1, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, l > 0 ? tidx(l - 1, 11) : -1, BT));
     }
-    if (T < m->maxT &&
+    if (T < m->maxT && !m->grad_accum &&
         cudaMemsetAsync(G(m, T_WPE) + (size_t)T * C, 0, (size_t)(m->maxT - T) * C * 4, m->stream) != cudaSuccess)
-        return GPT2_ERR_CUDA;  // positions >= T get a zero gradient
+        return GPT2_ERR_CUDA;  // positions >= T get a zero gradient (kept as they are when accumulating)
     Op op(m, GPT2_K_ENCODER_BWD);
     return op.done(launch_encoder_backward(m->dtype, G(m, T_WTE), G(m, T_WPE), m->dres, m->tokens, B, T, C,
-                                           m->scratch, m->stream),
+                                           m->scratch, m->stream, m->grad_accum),
                    (double)BT * (C * m->act + 4) * 2 + (double)BT * C * 8);
 }
 
@@ -554,6 +563,15 @@ int gpt2_init(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, void* d_works
         m->fam_work[f] = m->fam_ms[f] = 0;
     }
     m->timing = false;
+    m->grad_accum = 0;
+    // weight decay on the 2-D tensors (wte, wpe, the weight matrices), not on
+    // biases and LayerNorm parameters; every tensor starts on a 64-element boundary
+    std::vector<uint32_t> bits(((size_t)m->np / 64 + 1 + 31) / 32, 0u);
+    for (const auto& t : m->tensors) {
+        if (t.cols <= 1) continue;
+        const int64_t c0 = t.offset / 64, c1 = (t.offset + t.rows * t.cols + 63) / 64;
+        for (int64_t c = c0; c < c1; c++) bits[(size_t)c / 32] |= 1u << (c % 32);
+    }
     std::vector<float> host((size_t)m->np, 0.f);
     init_host(cfg, seed, m->tensors, host.data());
     int r = GPT2_OK;
@@ -561,7 +579,8 @@ int gpt2_init(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, void* d_works
         cudaMemcpyAsync(m->master, host.data(), (size_t)m->np * 4, cudaMemcpyHostToDevice, m->stream) != cudaSuccess ||
         cudaMemsetAsync(m->grads, 0, (size_t)m->np * 4, m->stream) != cudaSuccess ||
         cudaMemsetAsync(m->adam_m, 0, (size_t)m->np * 4, m->stream) != cudaSuccess ||
-        cudaMemsetAsync(m->adam_v, 0, (size_t)m->np * 4, m->stream) != cudaSuccess)
+        cudaMemsetAsync(m->adam_v, 0, (size_t)m->np * 4, m->stream) != cudaSuccess ||
+        cudaMemcpyAsync(m->decay_bits, bits.data(), bits.size() * 4, cudaMemcpyHostToDevice, m->stream) != cudaSuccess)
         r = GPT2_ERR_CUDA;
     if (r == GPT2_OK) r = refresh_compute_copy(m, 0, m->np);
     if (r == GPT2_OK) r = cuda_ok(cudaStreamSynchronize(m->stream));
@@ -614,6 +633,61 @@ int gpt2_adamw_step(gpt2_t* m, float lr, float beta1, float beta2, float eps, fl
                 (double)m->np * (m->mode == GPT2_MODE_BF16 ? 30.0 : 28.0)));
     m->state = 3;
     return GPT2_OK;
+}
+
+int gpt2_set_grad_accumulation(gpt2_t* m, int accumulate) {
+    if (!m || (accumulate != 0 && accumulate != 1)) return GPT2_ERR_ARG;
+    m->grad_accum = accumulate;
+    return GPT2_OK;
+}
+
+int gpt2_zero_grad(gpt2_t* m) {
+    if (!m) return GPT2_ERR_ARG;
+    return cuda_ok(cudaMemsetAsync(m->grads, 0, (size_t)m->np * 4, m->stream));
+}
+
+int gpt2_grad_norm(gpt2_t* m, float* norm_out) {
+    if (!m) return GPT2_ERR_ARG;
+    if (launch_grad_norm(m->gnorm, m->gnorm_partial, m->grads, m->np, m->stream) < 0) return GPT2_ERR_CUDA;
+    m->launches += 2;
+    if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
+    if (!norm_out) return GPT2_OK;
+    float v = 0.f;
+    if (cudaMemcpyAsync(&v, m->gnorm, sizeof(float), cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    TRY(cuda_ok(cudaStreamSynchronize(m->stream)));
+    *norm_out = v;
+    return GPT2_OK;
+}
+
+int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* c) {
+    if (!m || !c) return GPT2_ERR_ARG;
+    if (c->t < 1 || !(c->beta1 >= 0.f && c->beta1 < 1.f) || !(c->beta2 >= 0.f && c->beta2 < 1.f) || !(c->eps >= 0.f) ||
+        !std::isfinite(c->lr) || !std::isfinite(c->weight_decay) || !(c->grad_scale > 0.f) ||
+        !std::isfinite(c->grad_scale) || !(c->max_grad_norm >= 0.f) || (c->decay_mask != 0 && c->decay_mask != 1))
+        return GPT2_ERR_ARG;
+    if (m->state != 2) return GPT2_ERR_STATE;
+    if (c->max_grad_norm > 0.f) {
+        // the norm stays on the device: the clip factor is formed inside AdamW
+        if (launch_grad_norm(m->gnorm, m->gnorm_partial, m->grads, m->np, m->stream) < 0) return GPT2_ERR_CUDA;
+        m->launches += 2;
+    }
+    Op op(m, GPT2_K_ADAMW);
+    TRY(op.done(launch_adamw(m->master, m->mode == GPT2_MODE_BF16 ? m->params : nullptr, m->grads, m->adam_m,
+                             m->adam_v, m->np, c->lr, c->beta1, c->beta2, c->eps, c->weight_decay, c->t, m->stream,
+                             c->grad_scale, c->max_grad_norm > 0.f ? m->gnorm : nullptr, c->max_grad_norm,
+                             c->decay_mask ? m->decay_bits : nullptr),
+                (double)m->np * (m->mode == GPT2_MODE_BF16 ? 30.0 : 28.0)));
+    m->state = 3;
+    return GPT2_OK;
+}
+
+float gpt2_lr_cosine(int t, int warmup, int total, float lr_max, float lr_min) {
+    if (t < 1) return 0.f;
+    if (warmup > 0 && t <= warmup) return lr_max * (float)t / (float)warmup;
+    if (t >= total) return lr_min;
+    const double frac = (double)(t - warmup) / (double)(total - warmup);  // in (0, 1)
+    return (float)(lr_min + 0.5 * (lr_max - lr_min) * (1.0 + std::cos(3.14159265358979323846 * frac)));
 }
 
 int gpt2_destroy(gpt2_t* m) {

@@ -44,6 +44,12 @@ class gpt2_config(ctypes.Structure):
                 ("vocab_padded", c_int32), ("max_T", c_int32), ("max_B", c_int32), ("mode", c_int32)]
 
 
+class gpt2_adamw_config(ctypes.Structure):
+    _fields_ = [("lr", c_float), ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
+                ("weight_decay", c_float), ("t", c_int32), ("grad_scale", c_float), ("max_grad_norm", c_float),
+                ("decay_mask", c_int32)]
+
+
 _lib = None
 
 # name -> (restype, argtypes)
@@ -54,6 +60,11 @@ _SIGNATURES = {
     "gpt2_backward": (c_int, [c_void_p]),
     "gpt2_adamw_step": (c_int, [c_void_p, c_float, c_float, c_float, c_float, c_float, c_int]),
     "gpt2_destroy": (c_int, [c_void_p]),
+    "gpt2_set_grad_accumulation": (c_int, [c_void_p, c_int]),
+    "gpt2_zero_grad": (c_int, [c_void_p]),
+    "gpt2_grad_norm": (c_int, [c_void_p, POINTER(c_float)]),
+    "gpt2_adamw_step_ex": (c_int, [c_void_p, POINTER(gpt2_adamw_config)]),
+    "gpt2_lr_cosine": (c_float, [c_int, c_int, c_int, c_float, c_float]),
     "gpt2_strerror": (c_char_p, [c_int]),
     "gpt2_num_tensors": (c_int, [c_void_p]),
     "gpt2_tensor_info": (c_int, [c_void_p, c_int, POINTER(c_char_p), POINTER(c_int64)]),
@@ -228,8 +239,27 @@ class GPT2:
     def backward(self):
         gpt2_backward(self.h)
 
-    def adamw_step(self, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1):
-        gpt2_adamw_step(self.h, lr, beta1, beta2, eps, weight_decay, t)
+    def adamw_step(self, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1, grad_scale=None,
+                   max_grad_norm=None, decay_mask=None):
+        """gpt2_adamw_step, or gpt2_adamw_step_ex when any of grad_scale,
+        max_grad_norm or decay_mask is given."""
+        if grad_scale is None and max_grad_norm is None and decay_mask is None:
+            gpt2_adamw_step(self.h, lr, beta1, beta2, eps, weight_decay, t)
+            return
+        c = gpt2_adamw_config(lr, beta1, beta2, eps, weight_decay, t, 1.0 if grad_scale is None else grad_scale,
+                              0.0 if max_grad_norm is None else max_grad_norm, int(bool(decay_mask)))
+        check(self.lib.gpt2_adamw_step_ex(self.h, ctypes.byref(c)), "gpt2_adamw_step_ex")
+
+    def set_grad_accumulation(self, on: bool) -> None:
+        check(self.lib.gpt2_set_grad_accumulation(self.h, int(bool(on))), "gpt2_set_grad_accumulation")
+
+    def zero_grad(self) -> None:
+        check(self.lib.gpt2_zero_grad(self.h), "gpt2_zero_grad")
+
+    def grad_norm(self) -> float:
+        v = c_float()
+        check(self.lib.gpt2_grad_norm(self.h, ctypes.byref(v)), "gpt2_grad_norm")
+        return v.value
 
     def tensor(self, i: int, kind: int = TENSOR_MASTER) -> np.ndarray:
         out = np.empty(self.shapes[i], dtype=np.float32)
@@ -363,6 +393,10 @@ def gpt2_op_matmul(D, A, a_mn, B, b_mn, M, N, K, bias=None, status=None, stream=
     check(lib.gpt2_op_matmul(dt, _p(D), d_fp32, _p(A), int(a_mn), _p(B), int(b_mn), _p(bias), M, N, K, _p(sc),
                              sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul")
     return sc
+
+
+def gpt2_lr_cosine(t: int, warmup: int, total: int, lr_max: float, lr_min: float) -> float:
+    return float(load_library().gpt2_lr_cosine(int(t), int(warmup), int(total), float(lr_max), float(lr_min)))
 
 
 def gpt2_op_matmul_gelu(dgelu, out, A, W, bias=None, status=None, stream=None):
