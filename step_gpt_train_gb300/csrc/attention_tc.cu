@@ -124,41 +124,48 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
             if (v_issued >= 0) mbar_drain(v_full, (uint32_t)v_issued, a.status);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // -------------------------------------------------- MMA issuer
+        {
+            // -------------------------------------------------- MMA issuer: the
+            // whole warp runs the schedule (warp-uniform operands), one elected
+            // lane issues the MMAs and commits
+            const bool leader = elect_one();
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);
-            bool ok = mbar_wait(q_full, 0, abort_flag, a.status);
+            bool ok = warp_wait(q_full, 0, abort_flag, a.status);
             // S(j) = Q K(j)^T; the K stage is free once these MMAs finish
             auto issue_s = [&](int j) -> bool {
                 const int st = j & 1;
-                if (!mbar_wait(k_full(st), (j >> 1) & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(s_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
+                if (!warp_wait(k_full(st), (j >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(s_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int k = 0; k < AT_HD / 16; k++)
-                    tc_mma(tmem, sw128_desc(sQ + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024), idesc_s,
-                           k > 0 ? 1u : 0u);
-                tc_commit(s_full);
-                tc_commit(k_empty(st));
+                    for (int k = 0; k < AT_HD / 16; k++)
+                        tc_mma(tmem, sw128_desc(sQ + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024), idesc_s,
+                               k > 0 ? 1u : 0u);
+                }
+                if (leader) tc_commit(s_full);
+                if (leader) tc_commit(k_empty(st));
                 return true;
             };
             if (ok) ok = issue_s(0);
             for (int j = 0; ok && j < nkb; j++) {
                 if (j + 1 < nkb && !(ok = issue_s(j + 1))) break;
                 // O += P(j) V(j)
-                if (!(ok = mbar_wait(p_full, j & 1, abort_flag, a.status))) break;
-                if (!(ok = mbar_wait(v_full, j & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(p_full, j & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(v_full, j & 1, abort_flag, a.status))) break;
                 tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < AT_N / 16; kk++)
-                    tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV + kk * 2048, 8192, 1024), idesc_o,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(p_free);
-                tc_commit(v_empty);
+                    for (int kk = 0; kk < AT_N / 16; kk++)
+                        tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV + kk * 2048, 8192, 1024), idesc_o,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (leader) tc_commit(p_free);
+                if (leader) tc_commit(v_empty);
             }
-            if (ok) tc_commit(o_done);
-            tc_commit(drain);
+            if (leader && ok) tc_commit(o_done);
+            if (leader) tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
     } else {
@@ -367,8 +374,8 @@ namespace {
 constexpr int BW_EW = 16;                   // elementwise warps
 constexpr int BW_THREADS = 64 + 32 * BW_EW;  // + producer and MMA warps
 constexpr int EW_COLS = 32;                 // columns of a 128-wide tile per elementwise thread
-constexpr int DKDV_ST = 5;   // Q/dO stages of the dK/dV kernel
-constexpr int DQ_ST = 5;     // K/V stages of the dQ kernel
+constexpr int DKDV_ST = 4;   // Q/dO stages of the dK/dV kernel
+constexpr int DQ_ST = 4;     // K/V stages of the dQ kernel
 // TMEM columns. dK/dV kernel: S^T, dP^T (fp32), dV, dK (fp32), P^T, dS^T
 // (bf16 pairs: 128 queries in 64 columns).
 constexpr uint32_t KV_S = 0, KV_DP = 128, KV_DV = 256, KV_DK = 320, KV_P = 384, KV_DS = 448;
@@ -451,8 +458,8 @@ template <bool DQ> __device__ __forceinline__ Cur cur_next(const BwdArgs& a, Cur
 }
 
 // -------------------------------------------------------------------------- dK, dV
-// Shared memory: K | V | DKDV_ST x (Q, dO) | per elementwise warp 64 floats
-// (its columns' lse and D) | barriers.
+// Shared memory: 2 x (K, V) (an item's tile and the next one's) | DKDV_ST x
+// (Q, dO) | per elementwise warp 64 floats (its columns' lse and D) | barriers.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                             BwdArgs a) {
@@ -461,31 +468,38 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     constexpr int NS = DKDV_ST;
-    const uint32_t sK = base, sV = base + AT_TILE;
-    auto sQ = [&](int st) { return base + (2 + 2 * st) * AT_TILE; };
-    auto sO = [&](int st) { return base + (3 + 2 * st) * AT_TILE; };
-    float* ldslots = reinterpret_cast<float*>(gbase + (2 + 2 * NS) * AT_TILE);  // [BW_EW][64]
-    const uint32_t bars = base + (2 + 2 * NS) * AT_TILE + BW_EW * 256;
-    uint8_t* bar_area = gbase + (2 + 2 * NS) * AT_TILE + BW_EW * 256;
-    const uint32_t k_full = bars, k_empty = bars + 8u, v_full = bars + 16u, v_empty = bars + 24u;
-    auto qd_full = [&](int i) { return bars + 8u * (4 + i); };
-    auto qd_empty = [&](int i) { return bars + 8u * (4 + NS + i); };
-    const uint32_t bx = bars + 8u * (4 + 2 * NS);
+    // item i uses K/V buffer i & 1 (its (i >> 1)-th use)
+    auto sK = [&](int b) { return base + (2 * b) * AT_TILE; };
+    auto sV = [&](int b) { return base + (2 * b + 1) * AT_TILE; };
+    auto sQ = [&](int st) { return base + (4 + 2 * st) * AT_TILE; };
+    auto sO = [&](int st) { return base + (5 + 2 * st) * AT_TILE; };
+    float* ldslots = reinterpret_cast<float*>(gbase + (4 + 2 * NS) * AT_TILE);  // [BW_EW][64]
+    const uint32_t bars = base + (4 + 2 * NS) * AT_TILE + BW_EW * 256;
+    uint8_t* bar_area = gbase + (4 + 2 * NS) * AT_TILE + BW_EW * 256;
+    auto k_full = [&](int b) { return bars + 8u * b; };
+    auto k_empty = [&](int b) { return bars + 8u * (2 + b); };
+    auto v_full = [&](int b) { return bars + 8u * (4 + b); };
+    auto v_empty = [&](int b) { return bars + 8u * (6 + b); };
+    auto qd_full = [&](int i) { return bars + 8u * (8 + i); };
+    auto qd_empty = [&](int i) { return bars + 8u * (8 + NS + i); };
+    const uint32_t bx = bars + 8u * (8 + 2 * NS);
     const uint32_t s_full = bx, s_free = bx + 8u;
     const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
-    const uint32_t p_full = bx + 32u, p_free = bx + 40u;
+    const uint32_t p_full = bx + 32u;
     const uint32_t ds_full = bx + 48u, ds_free = bx + 56u;
     const uint32_t acc_full = bx + 64u, acc_empty = bx + 72u, drain = bx + 80u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (4 + 2 * NS) + 88);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (4 + 2 * NS) + 92);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 88);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 92);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(k_full, 1);
-        mbar_init(k_empty, 1);
-        mbar_init(v_full, 1);
-        mbar_init(v_empty, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(k_full(b), 1);
+            mbar_init(k_empty(b), 1);
+            mbar_init(v_full(b), 1);
+            mbar_init(v_empty(b), 1);
+        }
         for (int i = 0; i < NS; i++) {
             mbar_init(qd_full(i), 1);
             mbar_init(qd_empty(i), 1);
@@ -495,7 +509,6 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(dp_full, 1);
         mbar_init(dp_free, BW_EW);
         mbar_init(p_full, BW_EW);
-        mbar_init(p_free, 1);
         mbar_init(ds_full, BW_EW);
         mbar_init(ds_free, 1);
         mbar_init(acc_full, 1);
@@ -514,9 +527,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------- TMA producer
-            int qd_issued[NS];
+            int qd_issued[NS], kv_issued[2] = {-1, -1};  // parity of each buffer's last load (final drain)
             for (int i = 0; i < NS; i++) qd_issued[i] = -1;
-            int k_items = 0, v_items = 0, g = 0;  // K and V loads issued (for the final drain)
+            int g = 0;
             bool ok = true;
             for (int i = 0; ok; i++) {
                 Item it;
@@ -533,54 +546,64 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     g++;
                     return true;
                 };
-                // the item's first Q/dO block, then its K and V (once the previous
-                // item's last S^T and dP^T have read theirs), then the other blocks
+                // the item's first Q/dO block, then its K and V (into the buffer
+                // that the item before last has finished with), then the other blocks
+                const int kb = i & 1;
+                const uint32_t kph = (uint32_t)(i >> 1) & 1u;
                 if (!(ok = load_qd(0))) break;
-                if (!(ok = mbar_wait(k_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(k_full, AT_TILE);
-                tma_load_3d(sK, &tm_qkv, k_full, a.C + h * AT_HD, it.tile * AT_N, b);
-                k_items = i + 1;
-                if (!(ok = mbar_wait(v_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(v_full, AT_TILE);
-                tma_load_3d(sV, &tm_qkv, v_full, 2 * a.C + h * AT_HD, it.tile * AT_N, b);
-                v_items = i + 1;
+                if (!(ok = mbar_wait(k_empty(kb), kph ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(k_full(kb), AT_TILE);
+                tma_load_3d(sK(kb), &tm_qkv, k_full(kb), a.C + h * AT_HD, it.tile * AT_N, b);
+                if (!(ok = mbar_wait(v_empty(kb), kph ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(v_full(kb), AT_TILE);
+                tma_load_3d(sV(kb), &tm_qkv, v_full(kb), 2 * a.C + h * AT_HD, it.tile * AT_N, b);
+                kv_issued[kb] = (int)kph;
                 for (int n = 1; ok && n < it.nblk; n++) ok = load_qd(n);
             }
-            if (k_items > 0) mbar_drain(k_full, (uint32_t)((k_items - 1) & 1), a.status);
-            if (v_items > 0) mbar_drain(v_full, (uint32_t)((v_items - 1) & 1), a.status);
+            for (int kb = 0; kb < 2; kb++)
+                if (kv_issued[kb] >= 0) {
+                    mbar_drain(k_full(kb), (uint32_t)kv_issued[kb], a.status);
+                    mbar_drain(v_full(kb), (uint32_t)kv_issued[kb], a.status);
+                }
             for (int st = 0; st < NS; st++)
                 if (qd_issued[st] >= 0) mbar_drain(qd_full(st), (uint32_t)qd_issued[st], a.status);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // -------------------------------------------------- MMA issuer
+        {
+            // -------------------------------------------------- MMA issuer: the
+            // whole warp runs the schedule (warp-uniform operands), one elected
+            // lane issues the MMAs and commits
+            const bool leader = elect_one();
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);  // K-major x K-major
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);  // K-major x MN-major
             auto issue_s = [&](const Cur& x) -> bool {  // S^T = K Q^T
-                const int st = x.g % NS;
-                if (x.n == 0 && !mbar_wait(k_full, x.i & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(qd_full(st), (x.g / NS) & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(s_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
+                const int st = x.g % NS, kb = x.i & 1;
+                if (x.n == 0 && !warp_wait(k_full(kb), (x.i >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(qd_full(st), (x.g / NS) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(s_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
+                // one 16-wide k step = 32 bytes = 2 units of the descriptors' address field
+                const uint64_t da = sw128_desc(sK(kb), 16, 1024), db = sw128_desc(sQ(st), 16, 1024);
+                if (leader) {
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-                    tc_mma(tmem + KV_S, sw128_desc(sK + k * 32, 16, 1024), sw128_desc(sQ(st) + k * 32, 16, 1024),
-                           idesc_s, k > 0 ? 1u : 0u);
-                tc_commit(s_full);
-                if (x.n == x.it.nblk - 1) tc_commit(k_empty);  // the item's last read of K
+                    for (int k = 0; k < 4; k++) tc_mma(tmem + KV_S, da + 2 * k, db + 2 * k, idesc_s, k > 0 ? 1u : 0u);
+                }
+                if (leader) tc_commit(s_full);
+                if (leader && x.n == x.it.nblk - 1) tc_commit(k_empty(kb));  // the item's last read of K
                 return true;
             };
             auto issue_dp = [&](const Cur& x) -> bool {  // dP^T = V dO^T
-                const int st = x.g % NS;
-                if (x.n == 0 && !mbar_wait(v_full, x.i & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(dp_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
+                const int st = x.g % NS, kb = x.i & 1;
+                if (x.n == 0 && !warp_wait(v_full(kb), (x.i >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(dp_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
+                const uint64_t da = sw128_desc(sV(kb), 16, 1024), db = sw128_desc(sO(st), 16, 1024);
+                if (leader) {
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-                    tc_mma(tmem + KV_DP, sw128_desc(sV + k * 32, 16, 1024), sw128_desc(sO(st) + k * 32, 16, 1024),
-                           idesc_s, k > 0 ? 1u : 0u);
-                tc_commit(dp_full);
-                if (x.n == x.it.nblk - 1) tc_commit(v_empty);  // the item's last read of V
+                    for (int k = 0; k < 4; k++) tc_mma(tmem + KV_DP, da + 2 * k, db + 2 * k, idesc_s, k > 0 ? 1u : 0u);
+                }
+                if (leader) tc_commit(dp_full);
+                if (leader && x.n == x.it.nblk - 1) tc_commit(v_empty(kb));  // the item's last read of V
                 return true;
             };
             Cur c = cur_first<false>(a);
@@ -591,28 +614,33 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 if (nx.valid && !(ok = issue_s(nx))) break;
                 // dV += P^T dO (the first block of an item starts the accumulator
                 // once the elementwise warps have stored the previous item's)
-                if (!(ok = mbar_wait(p_full, c.g & 1, abort_flag, a.status))) break;
-                if (c.n == 0 && c.i > 0 && !(ok = mbar_wait(acc_empty, (c.i - 1) & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(p_full, c.g & 1, abort_flag, a.status))) break;
+                if (c.n == 0 && c.i > 0 && !(ok = warp_wait(acc_empty, (c.i - 1) & 1, abort_flag, a.status))) break;
                 tc_fence_after();
+                // MN-major B: one 16-row k step = 2048 bytes = 128 units of the address field
+                const uint64_t dbo = sw128_desc(sO(st), 8192, 1024);
+                const uint32_t acc0 = c.n > 0 ? 1u : 0u;
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++)
-                    tc_mma_ts(tmem + KV_DV, tmem + KV_P + kk * 8, sw128_desc(sO(st) + kk * 2048, 8192, 1024), idesc_o,
-                              (c.n > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(p_free);
+                    for (int kk = 0; kk < 8; kk++)
+                        tc_mma_ts(tmem + KV_DV, tmem + KV_P + kk * 8, dbo + 128 * kk, idesc_o, kk > 0 ? 1u : acc0);
+                }
                 if (nx.valid && !(ok = issue_dp(nx))) break;
                 // dK += dS^T Q
-                if (!(ok = mbar_wait(ds_full, c.g & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(ds_full, c.g & 1, abort_flag, a.status))) break;
                 tc_fence_after();
+                const uint64_t dbq = sw128_desc(sQ(st), 8192, 1024);
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++)
-                    tc_mma_ts(tmem + KV_DK, tmem + KV_DS + kk * 8, sw128_desc(sQ(st) + kk * 2048, 8192, 1024), idesc_o,
-                              (c.n > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(ds_free);
-                tc_commit(qd_empty(st));
-                if (c.n == c.it.nblk - 1) tc_commit(acc_full);  // the item's dV and dK are complete
+                    for (int kk = 0; kk < 8; kk++)
+                        tc_mma_ts(tmem + KV_DK, tmem + KV_DS + kk * 8, dbq + 128 * kk, idesc_o, kk > 0 ? 1u : acc0);
+                }
+                if (leader) tc_commit(ds_free);
+                if (leader) tc_commit(qd_empty(st));
+                if (leader && c.n == c.it.nblk - 1) tc_commit(acc_full);  // the item's dV and dK are complete
                 c = nx;
             }
-            tc_commit(drain);
+            if (leader) tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
     } else {
@@ -622,17 +650,45 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const int r = quad * 32 + lane;  // key row within the tile = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         float* slot = ldslots + ew * 64;  // [0,32): -lse * log2(e), [32,64): D of this warp's 32 queries
-        // -lse (log2 units) and D of query column part*32 + lane of a step's block; 0 past T
-        auto load_ld = [&](const Cur& x, float& l2, float& d) {
+        // lse and D of query column part*32 + lane of a step's block, loaded a
+        // step ahead and used as they are (no arithmetic waits on the loads
+        // until the step they belong to); `in` says whether the query is < T
+        auto load_ld = [&](const Cur& x, float& l, float& d, bool& in) {
             const int q = (x.it.tile + x.n) * AT_M + part * EW_COLS + lane;
-            const int64_t o = (int64_t)x.it.bh * a.T + q;
-            l2 = q < a.T ? -a.lse[o] * 1.4426950408889634f : 0.f;
-            d = q < a.T ? a.D[o] : 0.f;
+            in = q < a.T;
+            const int64_t o = (int64_t)x.it.bh * a.T + (in ? q : 0);
+            l = a.lse[o];
+            d = a.D[o];
         };
         const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
+        // An item's dV and dK leave TMEM during the next item's first step,
+        // once its exponentials are done, so the last dK product of the item
+        // runs while they are computed: parts 0, 1 store dV columns part*32..,
+        // parts 2, 3 dK columns (part-2)*32..; then TMEM is handed back.
+        int pend_i = -1, pend_key = 0, pend_bh = 0;
+        auto flush = [&]() -> bool {
+            if (!warp_wait(acc_full, pend_i & 1, abort_flag, a.status)) return false;
+            tc_fence_after();
+            const bool is_dk = part >= 2;
+            const int c0 = (part & 1) * 32;
+            uint32_t acc[32];
+            tc_ld32_issue(trow + (is_dk ? KV_DK : KV_DV) + (uint32_t)c0, acc);
+            tc_ld_wait(acc);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+            if (pend_key < a.T) {
+                const int b = pend_bh / a.H, h = pend_bh % a.H;
+                bf16* out = a.dqkv + ((int64_t)b * a.T + pend_key) * 3 * a.C + (is_dk ? a.C : 2 * a.C) + h * AT_HD + c0;
+                store32_bf16(out, acc, is_dk ? a.scale : 1.f);
+            }
+            pend_i = -1;
+            return true;
+        };
         Cur c = cur_first<false>(a);
-        float l2_nx = 0.f, d_nx = 0.f;
-        if (c.valid) load_ld(c, l2_nx, d_nx);
+        float l_nx = 0.f, d_nx = 0.f;
+        bool in_nx = false;
+        if (c.valid) load_ld(c, l_nx, d_nx, in_nx);
         bool ok = true;
         while (c.valid) {
             const Cur nx = cur_next<false>(a, c);
@@ -641,10 +697,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             const int q0 = (c.it.tile + c.n) * AT_M + part * EW_COLS;  // first query of this thread's columns
             const bool diag = c.n == 0;
             __syncwarp();  // every lane is done with the previous step's slot
-            slot[lane] = l2_nx;
-            slot[32 + lane] = d_nx;
+            slot[lane] = in_nx ? -l_nx * 1.4426950408889634f : 0.f;  // 0 past the sequence end
+            slot[32 + lane] = in_nx ? d_nx : 0.f;
             __syncwarp();
-            if (nx.valid) load_ld(nx, l2_nx, d_nx);  // the next step's, in flight meanwhile
+            if (nx.valid) load_ld(nx, l_nx, d_nx, in_nx);  // the next step's, in flight meanwhile
             uint32_t sv[32];
             if (!(ok = warp_wait(s_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
@@ -678,12 +734,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     pk[cc / 2] = pack2(p[cc], p[cc + 1]);
                 }
             }
-            if (!(ok = warp_wait(p_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
+            // the previous step's P^T and dS^T have been read: its dK product,
+            // issued after its dV product, is complete (one wait covers both stores)
+            if (!(ok = warp_wait(ds_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
             tc_st16(trow + KV_P + (uint32_t)(part * EW_COLS / 2), pk);
             tc_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
+            if (pend_i >= 0 && !(ok = flush())) break;
             // dS^T = P^T (dP^T - D)
             if (!(ok = warp_wait(dp_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
@@ -699,33 +758,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 f2_unpack(f2_mul(f2_pack(p[cc], p[cc + 1]), f2_sub(f2_pack(sv[cc], sv[cc + 1]), d2[cc / 2])), d0, d1);
                 pk[cc / 2] = pack2(d0, d1);
             }
-            if (!(ok = warp_wait(ds_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
             tc_st16(trow + KV_DS + (uint32_t)(part * EW_COLS / 2), pk);
             tc_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
             if (c.n == c.it.nblk - 1) {
-                // the item's accumulators: parts 0, 1 store dV columns part*32..,
-                // parts 2, 3 dK columns (part-2)*32..; then hand TMEM back
-                if (!(ok = warp_wait(acc_full, c.i & 1, abort_flag, a.status))) break;
-                tc_fence_after();
-                const bool is_dk = part >= 2;
-                const int c0 = (part & 1) * 32;
-                uint32_t acc[32];
-                tc_ld32_issue(trow + (is_dk ? KV_DK : KV_DV) + (uint32_t)c0, acc);
-                tc_ld_wait(acc);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
-                if (key < a.T) {
-                    const int b = c.it.bh / a.H, h = c.it.bh % a.H;
-                    bf16* out = a.dqkv + ((int64_t)b * a.T + key) * 3 * a.C + (is_dk ? a.C : 2 * a.C) + h * AT_HD + c0;
-                    store32_bf16(out, acc, is_dk ? a.scale : 1.f);
-                }
+                pend_i = c.i;
+                pend_key = key;
+                pend_bh = c.it.bh;
             }
             c = nx;
         }
+        if (ok && pend_i >= 0) flush();
     }
 
     tc_fence_before();
@@ -738,7 +783,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 }
 
 // -------------------------------------------------------------------------- dQ
-// Shared memory: Q | dO | DQ_ST x (K, V) | barriers.
+// Shared memory: 2 x (Q, dO) (an item's tile and the next one's) | DQ_ST x
+// (K, V) | barriers.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                           BwdArgs a) {
@@ -747,29 +793,36 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     constexpr int NS = DQ_ST;
-    const uint32_t sQ = base, sO = base + AT_TILE;
-    auto sK = [&](int st) { return base + (2 + 2 * st) * AT_TILE; };
-    auto sV = [&](int st) { return base + (3 + 2 * st) * AT_TILE; };
-    const uint32_t bars = base + (2 + 2 * NS) * AT_TILE;
-    uint8_t* bar_area = gbase + (2 + 2 * NS) * AT_TILE;
-    const uint32_t q_full = bars, q_empty = bars + 8u, o_full = bars + 16u, o_empty = bars + 24u;
-    auto kv_full = [&](int i) { return bars + 8u * (4 + i); };
-    auto kv_empty = [&](int i) { return bars + 8u * (4 + NS + i); };
-    const uint32_t bx = bars + 8u * (4 + 2 * NS);
+    // item i uses Q/dO buffer i & 1 (its (i >> 1)-th use)
+    auto sQ = [&](int b) { return base + (2 * b) * AT_TILE; };
+    auto sO = [&](int b) { return base + (2 * b + 1) * AT_TILE; };
+    auto sK = [&](int st) { return base + (4 + 2 * st) * AT_TILE; };
+    auto sV = [&](int st) { return base + (5 + 2 * st) * AT_TILE; };
+    const uint32_t bars = base + (4 + 2 * NS) * AT_TILE;
+    uint8_t* bar_area = gbase + (4 + 2 * NS) * AT_TILE;
+    auto q_full = [&](int b) { return bars + 8u * b; };
+    auto q_empty = [&](int b) { return bars + 8u * (2 + b); };
+    auto o_full = [&](int b) { return bars + 8u * (4 + b); };
+    auto o_empty = [&](int b) { return bars + 8u * (6 + b); };
+    auto kv_full = [&](int i) { return bars + 8u * (8 + i); };
+    auto kv_empty = [&](int i) { return bars + 8u * (8 + NS + i); };
+    const uint32_t bx = bars + 8u * (8 + 2 * NS);
     const uint32_t s_full = bx, s_free = bx + 8u;
     const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
     const uint32_t ds_full = bx + 32u, ds_free = bx + 40u;
     const uint32_t acc_full = bx + 48u, acc_empty = bx + 56u, drain = bx + 64u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (4 + 2 * NS) + 72);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (4 + 2 * NS) + 76);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 72);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 76);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        mbar_init(o_full, 1);
-        mbar_init(o_empty, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(q_full(b), 1);
+            mbar_init(q_empty(b), 1);
+            mbar_init(o_full(b), 1);
+            mbar_init(o_empty(b), 1);
+        }
         for (int i = 0; i < NS; i++) {
             mbar_init(kv_full(i), 1);
             mbar_init(kv_empty(i), 1);
@@ -796,9 +849,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------- TMA producer
-            int kv_issued[NS];
+            int kv_issued[NS], qo_issued[2] = {-1, -1};  // parity of each buffer's last load (final drain)
             for (int i = 0; i < NS; i++) kv_issued[i] = -1;
-            int q_items = 0, o_items = 0, g = 0;  // Q and dO loads issued (for the final drain)
+            int g = 0;
             bool ok = true;
             for (int i = 0; ok; i++) {
                 Item it;
@@ -815,54 +868,64 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     g++;
                     return true;
                 };
-                // the item's first K/V block, then its Q and dO (once the previous
-                // item's last S and dP have read theirs), then the other blocks
+                // the item's first K/V block, then its Q and dO (into the buffer
+                // that the item before last has finished with), then the other blocks
+                const int qb = i & 1;
+                const uint32_t qph = (uint32_t)(i >> 1) & 1u;
                 if (!(ok = load_kv(0))) break;
-                if (!(ok = mbar_wait(q_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(q_full, AT_TILE);
-                tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HD, it.tile * AT_M, b);
-                q_items = i + 1;
-                if (!(ok = mbar_wait(o_empty, (i & 1) ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(o_full, AT_TILE);
-                tma_load_3d(sO, &tm_do, o_full, h * AT_HD, it.tile * AT_M, b);
-                o_items = i + 1;
+                if (!(ok = mbar_wait(q_empty(qb), qph ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(q_full(qb), AT_TILE);
+                tma_load_3d(sQ(qb), &tm_qkv, q_full(qb), h * AT_HD, it.tile * AT_M, b);
+                if (!(ok = mbar_wait(o_empty(qb), qph ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(o_full(qb), AT_TILE);
+                tma_load_3d(sO(qb), &tm_do, o_full(qb), h * AT_HD, it.tile * AT_M, b);
+                qo_issued[qb] = (int)qph;
                 for (int j = 1; ok && j < it.nblk; j++) ok = load_kv(j);
             }
-            if (q_items > 0) mbar_drain(q_full, (uint32_t)((q_items - 1) & 1), a.status);
-            if (o_items > 0) mbar_drain(o_full, (uint32_t)((o_items - 1) & 1), a.status);
+            for (int qb = 0; qb < 2; qb++)
+                if (qo_issued[qb] >= 0) {
+                    mbar_drain(q_full(qb), (uint32_t)qo_issued[qb], a.status);
+                    mbar_drain(o_full(qb), (uint32_t)qo_issued[qb], a.status);
+                }
             for (int st = 0; st < NS; st++)
                 if (kv_issued[st] >= 0) mbar_drain(kv_full(st), (uint32_t)kv_issued[st], a.status);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // -------------------------------------------------- MMA issuer
+        {
+            // -------------------------------------------------- MMA issuer: the
+            // whole warp runs the schedule (warp-uniform operands), one elected
+            // lane issues the MMAs and commits
+            const bool leader = elect_one();
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);
             auto issue_s = [&](const Cur& x) -> bool {  // S = Q K^T
-                const int st = x.g % NS;
-                if (x.n == 0 && !mbar_wait(q_full, x.i & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(kv_full(st), (x.g / NS) & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(s_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
+                const int st = x.g % NS, qb = x.i & 1;
+                if (x.n == 0 && !warp_wait(q_full(qb), (x.i >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(kv_full(st), (x.g / NS) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(s_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
+                // one 16-wide k step = 32 bytes = 2 units of the descriptors' address field
+                const uint64_t da = sw128_desc(sQ(qb), 16, 1024), db = sw128_desc(sK(st), 16, 1024);
+                if (leader) {
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-                    tc_mma(tmem + Q_S, sw128_desc(sQ + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024),
-                           idesc_s, k > 0 ? 1u : 0u);
-                tc_commit(s_full);
-                if (x.n == x.it.nblk - 1) tc_commit(q_empty);  // the item's last read of Q
+                    for (int k = 0; k < 4; k++) tc_mma(tmem + Q_S, da + 2 * k, db + 2 * k, idesc_s, k > 0 ? 1u : 0u);
+                }
+                if (leader) tc_commit(s_full);
+                if (leader && x.n == x.it.nblk - 1) tc_commit(q_empty(qb));  // the item's last read of Q
                 return true;
             };
             auto issue_dp = [&](const Cur& x) -> bool {  // dP = dO V^T
-                const int st = x.g % NS;
-                if (x.n == 0 && !mbar_wait(o_full, x.i & 1, abort_flag, a.status)) return false;
-                if (!mbar_wait(dp_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
+                const int st = x.g % NS, qb = x.i & 1;
+                if (x.n == 0 && !warp_wait(o_full(qb), (x.i >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(dp_free, (x.g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
+                const uint64_t da = sw128_desc(sO(qb), 16, 1024), db = sw128_desc(sV(st), 16, 1024);
+                if (leader) {
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-                    tc_mma(tmem + Q_DP, sw128_desc(sO + k * 32, 16, 1024), sw128_desc(sV(st) + k * 32, 16, 1024),
-                           idesc_s, k > 0 ? 1u : 0u);
-                tc_commit(dp_full);
-                if (x.n == x.it.nblk - 1) tc_commit(o_empty);  // the item's last read of dO
+                    for (int k = 0; k < 4; k++) tc_mma(tmem + Q_DP, da + 2 * k, db + 2 * k, idesc_s, k > 0 ? 1u : 0u);
+                }
+                if (leader) tc_commit(dp_full);
+                if (leader && x.n == x.it.nblk - 1) tc_commit(o_empty(qb));  // the item's last read of dO
                 return true;
             };
             Cur c = cur_first<true>(a);
@@ -872,19 +935,23 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 const int st = c.g % NS;
                 if (nx.valid && !(ok = issue_s(nx) && issue_dp(nx))) break;
                 // dQ += dS K
-                if (!(ok = mbar_wait(ds_full, c.g & 1, abort_flag, a.status))) break;
-                if (c.n == 0 && c.i > 0 && !(ok = mbar_wait(acc_empty, (c.i - 1) & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(ds_full, c.g & 1, abort_flag, a.status))) break;
+                if (c.n == 0 && c.i > 0 && !(ok = warp_wait(acc_empty, (c.i - 1) & 1, abort_flag, a.status))) break;
                 tc_fence_after();
+                // MN-major B: one 16-row k step = 2048 bytes = 128 units of the address field
+                const uint64_t dbk = sw128_desc(sK(st), 8192, 1024);
+                const uint32_t acc0 = c.n > 0 ? 1u : 0u;
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++)
-                    tc_mma_ts(tmem + Q_DQ, tmem + Q_DS + kk * 8, sw128_desc(sK(st) + kk * 2048, 8192, 1024), idesc_o,
-                              (c.n > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(ds_free);
-                tc_commit(kv_empty(st));
-                if (c.n == c.it.nblk - 1) tc_commit(acc_full);
+                    for (int kk = 0; kk < 8; kk++)
+                        tc_mma_ts(tmem + Q_DQ, tmem + Q_DS + kk * 8, dbk + 128 * kk, idesc_o, kk > 0 ? 1u : acc0);
+                }
+                if (leader) tc_commit(ds_free);
+                if (leader) tc_commit(kv_empty(st));
+                if (leader && c.n == c.it.nblk - 1) tc_commit(acc_full);
                 c = nx;
             }
-            tc_commit(drain);
+            if (leader) tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
     } else {
@@ -892,26 +959,47 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const int quad = warp & 3, part = ew >> 2;
         const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-        // this row's lse (log2 units) and D for an item; the next item's are loaded ahead
-        auto load_row = [&](const Item& it, float& l2, float& d) {
+        // this row's lse and D for an item; the next item's are loaded ahead and
+        // used as they are (converted to log2 units when their item starts)
+        auto load_row = [&](const Item& it, float& l, float& d) {
             const int q = it.tile * AT_M + r;
             const int64_t o = (int64_t)it.bh * a.T + (q < a.T ? q : 0);
-            l2 = a.lse[o] * 1.4426950408889634f;
+            l = a.lse[o];
             d = a.D[o];
         };
+        // An item's dQ leaves TMEM during the next item's first step, once its
+        // exponentials are done, so the item's last dQ product runs meanwhile:
+        // parts 0, 1 store dQ columns part*32..; every warp hands TMEM back.
+        int pend_i = -1, pend_q = 0, pend_bh = 0;
+        auto flush = [&]() -> bool {
+            if (!warp_wait(acc_full, pend_i & 1, abort_flag, a.status)) return false;
+            tc_fence_after();
+            uint32_t dq[32];  // parts 2, 3 read the same columns and do not store them
+            tc_ld32_issue(trow + Q_DQ + (uint32_t)((part & 1) * 32), dq);
+            tc_ld_wait(dq);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+            if (part < 2 && pend_q < a.T) {
+                const int b = pend_bh / a.H, h = pend_bh % a.H;
+                store32_bf16(a.dqkv + ((int64_t)b * a.T + pend_q) * 3 * a.C + h * AT_HD + part * 32, dq, a.scale);
+            }
+            pend_i = -1;
+            return true;
+        };
         Cur c = cur_first<true>(a);
-        float l2_nx = 0.f, d_nx = 0.f, lse2 = 0.f, Dq = 0.f;
-        if (c.valid) load_row(c.it, l2_nx, d_nx);
+        float l_nx = 0.f, d_nx = 0.f, lse2 = 0.f, Dq = 0.f;
+        if (c.valid) load_row(c.it, l_nx, d_nx);
         bool ok = true;
         while (c.valid) {
             const Cur nx = cur_next<true>(a, c);
             const int g = c.g;
             const int q = c.it.tile * AT_M + r;
             if (c.n == 0) {
-                lse2 = l2_nx;
+                lse2 = l_nx * 1.4426950408889634f;
                 Dq = d_nx;
                 Item it2;
-                if (get_item<true>(a, c.i + 1, it2)) load_row(it2, l2_nx, d_nx);
+                if (get_item<true>(a, c.i + 1, it2)) load_row(it2, l_nx, d_nx);
             }
             const int k0 = c.n * AT_N + part * EW_COLS;  // first key of this thread's columns
             const bool diag = c.n == c.it.tile;
@@ -945,6 +1033,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     p[cc + 1] = ex2_approx(x1);
                 }
             }
+            if (pend_i >= 0 && !(ok = flush())) break;
             if (!(ok = warp_wait(dp_full, g & 1, abort_flag, a.status))) break;
             tc_fence_after();
             tc_ld32_issue(trow + Q_DP + (uint32_t)(part * EW_COLS), sv);
@@ -967,22 +1056,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
             if (c.n == c.it.nblk - 1) {
-                // parts 0, 1 store dQ columns part*32 ..; every warp hands TMEM back
-                if (!(ok = warp_wait(acc_full, c.i & 1, abort_flag, a.status))) break;
-                tc_fence_after();
-                uint32_t dq[32];  // parts 2, 3 read the same columns and do not store them
-                tc_ld32_issue(trow + Q_DQ + (uint32_t)((part & 1) * 32), dq);
-                tc_ld_wait(dq);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
-                if (part < 2 && q < a.T) {
-                    const int b = c.it.bh / a.H, h = c.it.bh % a.H;
-                    store32_bf16(a.dqkv + ((int64_t)b * a.T + q) * 3 * a.C + h * AT_HD + part * 32, dq, a.scale);
-                }
+                pend_i = c.i;
+                pend_q = q;
+                pend_bh = c.it.bh;
             }
             c = cur_next<true>(a, c);
         }
+        if (ok && pend_i >= 0) flush();
     }
 
     tc_fence_before();
@@ -1007,8 +1087,8 @@ bool make_do_map(CUtensorMap* map, const void* dout, int B, int T, int C) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int DKDV_SMEM = (2 + 2 * DKDV_ST) * AT_TILE + BW_EW * 256 + 256 + 1024;
-constexpr int DQ_SMEM = (2 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
+constexpr int DKDV_SMEM = (4 + 2 * DKDV_ST) * AT_TILE + BW_EW * 256 + 256 + 1024;
+constexpr int DQ_SMEM = (4 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
 static_assert(DKDV_SMEM <= 232448 && DQ_SMEM <= 232448, "shared memory per CTA");
 
 }  // namespace

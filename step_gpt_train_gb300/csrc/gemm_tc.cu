@@ -270,8 +270,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (issued_phase[s] >= 0) mbar_drain(full_bar(s), (uint32_t)issued_phase[s], g.status);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        {
+            // ------------------------------------------------ MMA issuer: the
+            // whole warp runs the schedule (warp-uniform operands), one elected
+            // lane issues the MMAs and commits
+            const bool leader = elect_one();
             constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
             constexpr uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-wide k step
             constexpr uint32_t b_kstep = B_MN ? 16 * 128 : 32;
@@ -285,11 +288,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             Work w;
             for (int idx = 0; ok && get_work(g, idx, w); idx++) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
-                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, g.status)) {
+                    if (!warp_wait(full_bar(stage), phase, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
@@ -300,23 +303,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < BK / 16; k++) {
                         const uint64_t ad = sw128_desc(sa + k * a_kstep, a_lbo, 1024);
                         const uint64_t bd = sw128_desc(sb + k * b_kstep, b_lbo, 1024);
-                        tc_mma(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if (leader) tc_mma(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(stage));  // stage reusable once these MMAs finish
+                    if (leader) tc_commit(empty_bar(stage));  // stage reusable once these MMAs finish
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(tfull_bar(acc));  // accumulator complete
+                if (leader) tc_commit(tfull_bar(acc));  // accumulator complete
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             // all MMAs issued by this thread must finish before TMEM is freed
-            tc_commit(drain_bar);
+            if (leader) tc_commit(drain_bar);
             mbar_drain(drain_bar, 0, g.status);
         }
     } else {

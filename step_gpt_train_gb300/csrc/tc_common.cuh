@@ -48,6 +48,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         }
     }
 }
+// One lane of a fully active warp (the lowest), for work that a single
+// thread issues on the warp's behalf.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+    return pred != 0;
+}
 // Bounded wait by every lane of a warp, with one outcome for the whole warp:
 // if any lane gave up, all give up, so no lane goes on alone into a warp-wide
 // operation (a shuffle, __syncwarp or a .sync.aligned TMEM access).
