@@ -34,8 +34,8 @@ constexpr int AT_N = 128;                  // keys per block
 constexpr int AT_HD = 64;                  // head size
 constexpr int AT_TILE = AT_M * AT_HD * 2;  // 16 KB: 128 rows of 64 bf16
 constexpr int AT_THREADS = 192;
-// shared memory: Q | K stage 0 | K stage 1 | V | P (two 64-key chunks) | barriers
-constexpr int AT_SMEM = 4 * AT_TILE + 256 + 1024;  // Q | K0 | K1 | V | barriers
+// shared memory: Q | K stage 0 | K stage 1 | V stage 0 | V stage 1 | barriers
+constexpr int AT_SMEM = 5 * AT_TILE + 256 + 1024;
 constexpr uint32_t AT_TMEM_COLS = 256;     // S [0,128), O [128,192), P [192,256) (bf16 pairs)
 constexpr float AT_LN2 = 0.6931471805599453f;
 constexpr float AT_RESCALE = 8.f;          // log2 of the largest P before the reference max moves
@@ -56,19 +56,21 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t sQ = base;
     auto sK = [&](int st) { return base + (1 + st) * AT_TILE; };
-    const uint32_t sV = base + 3 * AT_TILE;
-    const uint32_t bars = base + 4 * AT_TILE;
-    uint8_t* bar_area = gbase + 4 * AT_TILE;
-    // barriers: q_full, k_full[2], k_empty[2], v_full, v_empty, s_full, s_free, p_full, p_free, o_done, drain
+    auto sV = [&](int st) { return base + (3 + st) * AT_TILE; };
+    const uint32_t bars = base + 5 * AT_TILE;
+    uint8_t* bar_area = gbase + 5 * AT_TILE;
+    // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free, p_full, p_free,
+    // o_done, drain
     const uint32_t q_full = bars;
     auto k_full = [&](int i) { return bars + 8u * (1 + i); };
     auto k_empty = [&](int i) { return bars + 8u * (3 + i); };
-    const uint32_t v_full = bars + 8u * 5, v_empty = bars + 8u * 6;
-    const uint32_t s_full = bars + 8u * 7, s_free = bars + 8u * 8;
-    const uint32_t p_full = bars + 8u * 9, p_free = bars + 8u * 10;
-    const uint32_t o_done = bars + 8u * 11, drain = bars + 8u * 12;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * 13);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * 13 + 4);
+    auto v_full = [&](int i) { return bars + 8u * (5 + i); };
+    auto v_empty = [&](int i) { return bars + 8u * (7 + i); };
+    const uint32_t s_full = bars + 8u * 9, s_free = bars + 8u * 10;
+    const uint32_t p_full = bars + 8u * 11, p_free = bars + 8u * 12;
+    const uint32_t o_done = bars + 8u * 13, drain = bars + 8u * 14;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * 15);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * 15 + 4);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int qt = gridDim.x - 1 - blockIdx.x;  // longest rows first
@@ -80,9 +82,9 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
         for (int i = 0; i < 2; i++) {
             mbar_init(k_full(i), 1);
             mbar_init(k_empty(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
         }
-        mbar_init(v_full, 1);
-        mbar_init(v_empty, 1);
         mbar_init(s_full, 1);
         mbar_init(s_free, 4);
         mbar_init(p_full, 4);
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------- TMA producer
-            int k_issued[2] = {-1, -1}, v_issued = -1;
+            int k_issued[2] = {-1, -1}, v_issued[2] = {-1, -1};  // parity of each stage's last load
             mbar_expect_tx(q_full, AT_TILE);
             tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HD, qt * AT_M, b);
             for (int j = 0; j < nkb; j++) {
@@ -112,16 +114,17 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                 mbar_expect_tx(k_full(st), AT_TILE);
                 tma_load_3d(sK(st), &tm_qkv, k_full(st), a.C + h * AT_HD, j * AT_N, b);
                 k_issued[st] = (int)ph;
-                // V(j) once PV(j-1) has read the buffer
-                if (!mbar_wait(v_empty, (j & 1) ^ 1u, abort_flag, a.status)) break;
-                mbar_expect_tx(v_full, AT_TILE);
-                tma_load_3d(sV, &tm_qkv, v_full, 2 * a.C + h * AT_HD, j * AT_N, b);
-                v_issued = j & 1;
+                // V(j) once PV(j-2) has read the stage
+                if (!mbar_wait(v_empty(st), ph ^ 1u, abort_flag, a.status)) break;
+                mbar_expect_tx(v_full(st), AT_TILE);
+                tma_load_3d(sV(st), &tm_qkv, v_full(st), 2 * a.C + h * AT_HD, j * AT_N, b);
+                v_issued[st] = (int)ph;
             }
             mbar_drain(q_full, 0, a.status);
-            for (int st = 0; st < 2; st++)
+            for (int st = 0; st < 2; st++) {
                 if (k_issued[st] >= 0) mbar_drain(k_full(st), (uint32_t)k_issued[st], a.status);
-            if (v_issued >= 0) mbar_drain(v_full, (uint32_t)v_issued, a.status);
+                if (v_issued[st] >= 0) mbar_drain(v_full(st), (uint32_t)v_issued[st], a.status);
+            }
         }
     } else if (warp == 1) {
         {
@@ -153,16 +156,16 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                 if (j + 1 < nkb && !(ok = issue_s(j + 1))) break;
                 // O += P(j) V(j)
                 if (!(ok = warp_wait(p_full, j & 1, abort_flag, a.status))) break;
-                if (!(ok = warp_wait(v_full, j & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(v_full(j & 1), (j >> 1) & 1, abort_flag, a.status))) break;
                 tc_fence_after();
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < AT_N / 16; kk++)
-                        tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV + kk * 2048, 8192, 1024), idesc_o,
+                        tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV(j & 1) + kk * 2048, 8192, 1024), idesc_o,
                                   (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (leader) tc_commit(p_free);
-                if (leader) tc_commit(v_empty);
+                if (leader) tc_commit(v_empty(j & 1));
             }
             if (leader && ok) tc_commit(o_done);
             if (leader) tc_commit(drain);
@@ -362,19 +365,23 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
 // items, longest first), so the operand rings and the MMA / elementwise
 // hand-offs carry on across items; an item's accumulators go from TMEM to
 // global memory while the next item's first products are computed.
-// Warps: 0 TMA producer (lane 0); 1 MMA issuer; 2..17
-// elementwise (warp w serves TMEM lanes 32*(w%4).. and one quarter, 32, of
-// the 128 columns: four warps per scheduler, so that the exp / multiply
-// chains of one warp hide the latencies of the others). One CTA per SM (512
-// TMEM columns).
+// Warps: 0 TMA producer (lane 0; an item's K/V (dQ kernel: Q/dO) tiles are
+// loaded while the item before it runs); 1 MMA issuer (the whole warp, one
+// elected lane issuing); 2..17 elementwise (warp w serves TMEM lanes 32*(w%4)..
+// and one quarter, 32, of the 128 columns: four warps per scheduler, so that
+// the exp / multiply chains of one warp hide the latencies of the others);
+// 18 sends an item's accumulators, which the elementwise warps stage in shared
+// memory as bf16, to global memory with TMA stores. One CTA per SM (512 TMEM
+// columns).
 // =============================================================================
 
 namespace {
 
-constexpr int BW_EW = 16;                   // elementwise warps
-constexpr int BW_THREADS = 64 + 32 * BW_EW;  // + producer and MMA warps
+constexpr int BW_EW = 16;                        // elementwise warps
+constexpr int BW_STORE_WARP = 2 + BW_EW;          // issues the TMA stores of the accumulators
+constexpr int BW_THREADS = 32 * (BW_STORE_WARP + 1);  // + producer, MMA and store warps
 constexpr int EW_COLS = 32;                 // columns of a 128-wide tile per elementwise thread
-constexpr int DKDV_ST = 4;   // Q/dO stages of the dK/dV kernel
+constexpr int DKDV_ST = 3;   // Q/dO stages of the dK/dV kernel
 constexpr int DQ_ST = 4;     // K/V stages of the dQ kernel
 // TMEM columns. dK/dV kernel: S^T, dP^T (fp32), dV, dK (fp32), P^T, dS^T
 // (bf16 pairs: 128 queries in 64 columns).
@@ -393,20 +400,27 @@ struct BwdArgs {
     float scale;         // 1 / sqrt(hd)
 };
 
-// Store 32 fp32 values (times s) as bf16 to global (64 bytes).
-__device__ __forceinline__ void store32_bf16(bf16* dst, const uint32_t (&v)[32], float s) {
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) f[e] = __uint_as_float(v[u * 8 + e]) * s;
-        store8(dst + u * 8, f);
-    }
-}
-
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// A warp's 32 x 32 block of an accumulator (lane = row, 32 fp32 columns, as a
+// 32x32b TMEM load leaves it), times s, as bf16 into row `row`, 16-byte units
+// 4 * half .. 4 * half + 3, of a 128-row x 128-byte tile laid out with the
+// 128-byte swizzle (unit u of row r at u ^ (r & 7)): the layout a tensor map
+// with SWIZZLE_128B stores from.
+__device__ __forceinline__ void stage_block_sw128(uint8_t* tile, int row, int half, const uint32_t (&v)[32],
+                                                  float s) {
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        uint4 w;
+        w.x = pack2(__uint_as_float(v[8 * u + 0]) * s, __uint_as_float(v[8 * u + 1]) * s);
+        w.y = pack2(__uint_as_float(v[8 * u + 2]) * s, __uint_as_float(v[8 * u + 3]) * s);
+        w.z = pack2(__uint_as_float(v[8 * u + 4]) * s, __uint_as_float(v[8 * u + 5]) * s);
+        w.w = pack2(__uint_as_float(v[8 * u + 6]) * s, __uint_as_float(v[8 * u + 7]) * s);
+        *reinterpret_cast<uint4*>(tile + row * 128 + (((half * 4 + u) ^ (row & 7)) << 4)) = w;
+    }
 }
 
 // -------------------------------------------------------------------------- schedule
@@ -459,10 +473,11 @@ template <bool DQ> __device__ __forceinline__ Cur cur_next(const BwdArgs& a, Cur
 
 // -------------------------------------------------------------------------- dK, dV
 // Shared memory: 2 x (K, V) (an item's tile and the next one's) | DKDV_ST x
-// (Q, dO) | per elementwise warp 64 floats (its columns' lse and D) | barriers.
+// (Q, dO) | dV, dK staging tiles for the TMA stores | per elementwise warp 64
+// floats (its columns' lse and D) | barriers.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                            BwdArgs a) {
+                            const __grid_constant__ CUtensorMap tm_dqkv, BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -473,9 +488,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     auto sV = [&](int b) { return base + (2 * b + 1) * AT_TILE; };
     auto sQ = [&](int st) { return base + (4 + 2 * st) * AT_TILE; };
     auto sO = [&](int st) { return base + (5 + 2 * st) * AT_TILE; };
-    float* ldslots = reinterpret_cast<float*>(gbase + (4 + 2 * NS) * AT_TILE);  // [BW_EW][64]
-    const uint32_t bars = base + (4 + 2 * NS) * AT_TILE + BW_EW * 256;
-    uint8_t* bar_area = gbase + (4 + 2 * NS) * AT_TILE + BW_EW * 256;
+    uint8_t* stg = gbase + (4 + 2 * NS) * AT_TILE;  // dV tile, then the dK tile
+    const uint32_t stg_addr = base + (4 + 2 * NS) * AT_TILE;
+    float* ldslots = reinterpret_cast<float*>(gbase + (6 + 2 * NS) * AT_TILE);  // [BW_EW][64]
+    const uint32_t bars = base + (6 + 2 * NS) * AT_TILE + BW_EW * 256;
+    uint8_t* bar_area = gbase + (6 + 2 * NS) * AT_TILE + BW_EW * 256;
     auto k_full = [&](int b) { return bars + 8u * b; };
     auto k_empty = [&](int b) { return bars + 8u * (2 + b); };
     auto v_full = [&](int b) { return bars + 8u * (4 + b); };
@@ -488,8 +505,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t p_full = bx + 32u;
     const uint32_t ds_full = bx + 48u, ds_free = bx + 56u;
     const uint32_t acc_full = bx + 64u, acc_empty = bx + 72u, drain = bx + 80u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 88);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 92);
+    const uint32_t stg_free = bx + 88u, stg_full = bx + 96u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 104);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 108);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -514,6 +532,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, BW_EW);
         mbar_init(drain, 1);
+        mbar_init(stg_free, 1);
+        mbar_init(stg_full, BW_EW);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -530,7 +550,23 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             int qd_issued[NS], kv_issued[2] = {-1, -1};  // parity of each buffer's last load (final drain)
             for (int i = 0; i < NS; i++) qd_issued[i] = -1;
             int g = 0;
-            bool ok = true;
+            // K and V of item i into buffer i & 1, once the item before last has
+            // finished with it
+            auto load_kv = [&](int i, const Item& it) -> bool {
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                const int kb = i & 1;
+                const uint32_t kph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(k_empty(kb), kph ^ 1u, abort_flag, a.status)) return false;
+                mbar_expect_tx(k_full(kb), AT_TILE);
+                tma_load_3d(sK(kb), &tm_qkv, k_full(kb), a.C + h * AT_HD, it.tile * AT_N, b);
+                if (!mbar_wait(v_empty(kb), kph ^ 1u, abort_flag, a.status)) return false;
+                mbar_expect_tx(v_full(kb), AT_TILE);
+                tma_load_3d(sV(kb), &tm_qkv, v_full(kb), 2 * a.C + h * AT_HD, it.tile * AT_N, b);
+                kv_issued[kb] = (int)kph;
+                return true;
+            };
+            Item it0;
+            bool ok = !get_item<false>(a, 0, it0) || load_kv(0, it0);
             for (int i = 0; ok; i++) {
                 Item it;
                 if (!get_item<false>(a, i, it)) break;
@@ -546,18 +582,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     g++;
                     return true;
                 };
-                // the item's first Q/dO block, then its K and V (into the buffer
-                // that the item before last has finished with), then the other blocks
-                const int kb = i & 1;
-                const uint32_t kph = (uint32_t)(i >> 1) & 1u;
+                // the item's first Q/dO block, then the next item's K and V (a
+                // whole item ahead of their first use), then the other blocks
                 if (!(ok = load_qd(0))) break;
-                if (!(ok = mbar_wait(k_empty(kb), kph ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(k_full(kb), AT_TILE);
-                tma_load_3d(sK(kb), &tm_qkv, k_full(kb), a.C + h * AT_HD, it.tile * AT_N, b);
-                if (!(ok = mbar_wait(v_empty(kb), kph ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(v_full(kb), AT_TILE);
-                tma_load_3d(sV(kb), &tm_qkv, v_full(kb), 2 * a.C + h * AT_HD, it.tile * AT_N, b);
-                kv_issued[kb] = (int)kph;
+                Item nit;
+                if (get_item<false>(a, i + 1, nit) && !(ok = load_kv(i + 1, nit))) break;
                 for (int n = 1; ok && n < it.nblk; n++) ok = load_qd(n);
             }
             for (int kb = 0; kb < 2; kb++)
@@ -643,6 +672,22 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             if (leader) tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
+    } else if (warp == BW_STORE_WARP) {
+        // ------------------------------------------------------ accumulator stores
+        // item f's dV and dK tiles, once the elementwise warps have staged them
+        Item it;
+        for (int f = 0; get_item<false>(a, f, it); f++) {
+            if (!warp_wait(stg_full, f & 1, abort_flag, a.status)) break;
+            if (lane == 0) {
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                tma_store_3d(&tm_dqkv, stg_addr, 2 * a.C + h * AT_HD, it.tile * AT_N, b);        // dV
+                tma_store_3d(&tm_dqkv, stg_addr + AT_TILE, a.C + h * AT_HD, it.tile * AT_N, b);  // dK
+                bulk_wait_read_all();  // the tiles may be written again
+                mbar_arrive(stg_free);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) bulk_wait_all();  // the stores are complete before the CTA ends
     } else {
         // ------------------------------------------------------ elementwise (warps 2..17)
         const int ew = warp - 2;
@@ -663,25 +708,28 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
         // An item's dV and dK leave TMEM during the next item's first step,
         // once its exponentials are done, so the last dK product of the item
-        // runs while they are computed: parts 0, 1 store dV columns part*32..,
-        // parts 2, 3 dK columns (part-2)*32..; then TMEM is handed back.
-        int pend_i = -1, pend_key = 0, pend_bh = 0;
+        // runs while they are computed. Parts 0, 1 hold dV columns part*32..,
+        // parts 2, 3 dK columns (part-2)*32..; each warp hands TMEM back and
+        // writes its block into the staging tiles (once the store warp has sent
+        // the previous item's out), and the store warp sends both tiles out.
+        int pend_i = -1, nflush = 0;
         auto flush = [&]() -> bool {
             if (!warp_wait(acc_full, pend_i & 1, abort_flag, a.status)) return false;
             tc_fence_after();
             const bool is_dk = part >= 2;
-            const int c0 = (part & 1) * 32;
+            const int half = part & 1;
             uint32_t acc[32];
-            tc_ld32_issue(trow + (is_dk ? KV_DK : KV_DV) + (uint32_t)c0, acc);
+            tc_ld32_issue(trow + (is_dk ? KV_DK : KV_DV) + (uint32_t)(half * 32), acc);
             tc_ld_wait(acc);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
-            if (pend_key < a.T) {
-                const int b = pend_bh / a.H, h = pend_bh % a.H;
-                bf16* out = a.dqkv + ((int64_t)b * a.T + pend_key) * 3 * a.C + (is_dk ? a.C : 2 * a.C) + h * AT_HD + c0;
-                store32_bf16(out, acc, is_dk ? a.scale : 1.f);
-            }
+            if (!warp_wait(stg_free, (nflush & 1) ^ 1u, abort_flag, a.status)) return false;
+            stage_block_sw128(stg + (is_dk ? AT_TILE : 0), r, half, acc, is_dk ? a.scale : 1.f);
+            fence_proxy_async_smem();  // the writes, visible to the TMA
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stg_full);
+            nflush++;
             pend_i = -1;
             return true;
         };
@@ -763,11 +811,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
-            if (c.n == c.it.nblk - 1) {
-                pend_i = c.i;
-                pend_key = key;
-                pend_bh = c.it.bh;
-            }
+            if (c.n == c.it.nblk - 1) pend_i = c.i;
             c = nx;
         }
         if (ok && pend_i >= 0) flush();
@@ -784,10 +828,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
 // -------------------------------------------------------------------------- dQ
 // Shared memory: 2 x (Q, dO) (an item's tile and the next one's) | DQ_ST x
-// (K, V) | barriers.
+// (K, V) | dQ staging tile for the TMA store | barriers.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                          BwdArgs a) {
+                          const __grid_constant__ CUtensorMap tm_dqkv, BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -798,8 +842,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     auto sO = [&](int b) { return base + (2 * b + 1) * AT_TILE; };
     auto sK = [&](int st) { return base + (4 + 2 * st) * AT_TILE; };
     auto sV = [&](int st) { return base + (5 + 2 * st) * AT_TILE; };
-    const uint32_t bars = base + (4 + 2 * NS) * AT_TILE;
-    uint8_t* bar_area = gbase + (4 + 2 * NS) * AT_TILE;
+    uint8_t* stg = gbase + (4 + 2 * NS) * AT_TILE;
+    const uint32_t stg_addr = base + (4 + 2 * NS) * AT_TILE;
+    const uint32_t bars = base + (5 + 2 * NS) * AT_TILE;
+    uint8_t* bar_area = gbase + (5 + 2 * NS) * AT_TILE;
     auto q_full = [&](int b) { return bars + 8u * b; };
     auto q_empty = [&](int b) { return bars + 8u * (2 + b); };
     auto o_full = [&](int b) { return bars + 8u * (4 + b); };
@@ -811,8 +857,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t dp_full = bx + 16u, dp_free = bx + 24u;
     const uint32_t ds_full = bx + 32u, ds_free = bx + 40u;
     const uint32_t acc_full = bx + 48u, acc_empty = bx + 56u, drain = bx + 64u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 72);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 76);
+    const uint32_t stg_free = bx + 72u, stg_full = bx + 80u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 88);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 92);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -836,6 +883,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, BW_EW);
         mbar_init(drain, 1);
+        mbar_init(stg_free, 1);
+        mbar_init(stg_full, BW_EW);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -852,7 +901,23 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             int kv_issued[NS], qo_issued[2] = {-1, -1};  // parity of each buffer's last load (final drain)
             for (int i = 0; i < NS; i++) kv_issued[i] = -1;
             int g = 0;
-            bool ok = true;
+            // Q and dO of item i into buffer i & 1, once the item before last has
+            // finished with it
+            auto load_qo = [&](int i, const Item& it) -> bool {
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                const int qb = i & 1;
+                const uint32_t qph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(q_empty(qb), qph ^ 1u, abort_flag, a.status)) return false;
+                mbar_expect_tx(q_full(qb), AT_TILE);
+                tma_load_3d(sQ(qb), &tm_qkv, q_full(qb), h * AT_HD, it.tile * AT_M, b);
+                if (!mbar_wait(o_empty(qb), qph ^ 1u, abort_flag, a.status)) return false;
+                mbar_expect_tx(o_full(qb), AT_TILE);
+                tma_load_3d(sO(qb), &tm_do, o_full(qb), h * AT_HD, it.tile * AT_M, b);
+                qo_issued[qb] = (int)qph;
+                return true;
+            };
+            Item it0;
+            bool ok = !get_item<true>(a, 0, it0) || load_qo(0, it0);
             for (int i = 0; ok; i++) {
                 Item it;
                 if (!get_item<true>(a, i, it)) break;
@@ -868,18 +933,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     g++;
                     return true;
                 };
-                // the item's first K/V block, then its Q and dO (into the buffer
-                // that the item before last has finished with), then the other blocks
-                const int qb = i & 1;
-                const uint32_t qph = (uint32_t)(i >> 1) & 1u;
+                // the item's first K/V block, then the next item's Q and dO (a
+                // whole item ahead of their first use), then the other blocks
                 if (!(ok = load_kv(0))) break;
-                if (!(ok = mbar_wait(q_empty(qb), qph ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(q_full(qb), AT_TILE);
-                tma_load_3d(sQ(qb), &tm_qkv, q_full(qb), h * AT_HD, it.tile * AT_M, b);
-                if (!(ok = mbar_wait(o_empty(qb), qph ^ 1u, abort_flag, a.status))) break;
-                mbar_expect_tx(o_full(qb), AT_TILE);
-                tma_load_3d(sO(qb), &tm_do, o_full(qb), h * AT_HD, it.tile * AT_M, b);
-                qo_issued[qb] = (int)qph;
+                Item nit;
+                if (get_item<true>(a, i + 1, nit) && !(ok = load_qo(i + 1, nit))) break;
                 for (int j = 1; ok && j < it.nblk; j++) ok = load_kv(j);
             }
             for (int qb = 0; qb < 2; qb++)
@@ -954,6 +1012,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             if (leader) tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
+    } else if (warp == BW_STORE_WARP) {
+        // ------------------------------------------------------ accumulator stores
+        // item f's dQ tile, once the elementwise warps have staged it
+        Item it;
+        for (int f = 0; get_item<true>(a, f, it); f++) {
+            if (!warp_wait(stg_full, f & 1, abort_flag, a.status)) break;
+            if (lane == 0) {
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                tma_store_3d(&tm_dqkv, stg_addr, h * AT_HD, it.tile * AT_M, b);
+                bulk_wait_read_all();  // the tile may be written again
+                mbar_arrive(stg_free);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) bulk_wait_all();  // the stores are complete before the CTA ends
     } else {
         const int ew = warp - 2;
         const int quad = warp & 3, part = ew >> 2;
@@ -969,21 +1042,27 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         };
         // An item's dQ leaves TMEM during the next item's first step, once its
         // exponentials are done, so the item's last dQ product runs meanwhile:
-        // parts 0, 1 store dQ columns part*32..; every warp hands TMEM back.
-        int pend_i = -1, pend_q = 0, pend_bh = 0;
+        // Parts 0, 1 hold dQ columns part*32..: they write their blocks into the
+        // staging tile (once the store warp has sent the previous item's out),
+        // every warp hands TMEM back, and the store warp sends the tile out.
+        int pend_i = -1, nflush = 0;
         auto flush = [&]() -> bool {
             if (!warp_wait(acc_full, pend_i & 1, abort_flag, a.status)) return false;
             tc_fence_after();
-            uint32_t dq[32];  // parts 2, 3 read the same columns and do not store them
+            uint32_t dq[32];  // parts p and p + 2 read the same columns; p + 2 does not stage them
             tc_ld32_issue(trow + Q_DQ + (uint32_t)((part & 1) * 32), dq);
             tc_ld_wait(dq);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
-            if (part < 2 && pend_q < a.T) {
-                const int b = pend_bh / a.H, h = pend_bh % a.H;
-                store32_bf16(a.dqkv + ((int64_t)b * a.T + pend_q) * 3 * a.C + h * AT_HD + part * 32, dq, a.scale);
+            if (!warp_wait(stg_free, (nflush & 1) ^ 1u, abort_flag, a.status)) return false;
+            if (part < 2) {
+                stage_block_sw128(stg, r, part, dq, a.scale);
+                fence_proxy_async_smem();  // the writes, visible to the TMA
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stg_full);
+            nflush++;
             pend_i = -1;
             return true;
         };
@@ -1055,11 +1134,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(ds_full);
-            if (c.n == c.it.nblk - 1) {
-                pend_i = c.i;
-                pend_q = q;
-                pend_bh = c.it.bh;
-            }
+            if (c.n == c.it.nblk - 1) pend_i = c.i;
             c = cur_next<true>(a, c);
         }
         if (ok && pend_i >= 0) flush();
@@ -1087,8 +1162,8 @@ bool make_do_map(CUtensorMap* map, const void* dout, int B, int T, int C) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int DKDV_SMEM = (4 + 2 * DKDV_ST) * AT_TILE + BW_EW * 256 + 256 + 1024;
-constexpr int DQ_SMEM = (4 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
+constexpr int DKDV_SMEM = (6 + 2 * DKDV_ST) * AT_TILE + BW_EW * 256 + 256 + 1024;
+constexpr int DQ_SMEM = (5 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
 static_assert(DKDV_SMEM <= 232448 && DQ_SMEM <= 232448, "shared memory per CTA");
 
 }  // namespace
@@ -1097,8 +1172,9 @@ static_assert(DKDV_SMEM <= 232448 && DQ_SMEM <= 232448, "shared memory per CTA")
 // computes it and routes here).
 int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, const float* lse, const float* D,
                                  int B, int T, int C, int H, int* status, cudaStream_t s) {
-    CUtensorMap mq, mo;
-    if (!make_qkv_map(&mq, qkv, B, T, C) || !make_do_map(&mo, dout, B, T, C)) return GPT2_ERR_CUDA;
+    CUtensorMap mq, mo, md;  // md: the same view of dqkv, for the TMA stores of dQ, dK, dV
+    if (!make_qkv_map(&mq, qkv, B, T, C) || !make_do_map(&mo, dout, B, T, C) || !make_qkv_map(&md, dqkv, B, T, C))
+        return GPT2_ERR_CUDA;
     static bool configured = false;
     if (!configured) {
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DKDV_SMEM);
@@ -1119,7 +1195,7 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     a.scale_log2 = 1.4426950408889634f * a.scale;
     const int items = a.nqt * B * H;
     const int grid = items < gpt2_num_sms() ? items : gpt2_num_sms();  // persistent: one CTA per SM
-    attn_bwd_dkdv_tc_kernel<<<grid, BW_THREADS, DKDV_SMEM, s>>>(mq, mo, a);
-    attn_bwd_dq_tc_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, mo, a);
+    attn_bwd_dkdv_tc_kernel<<<grid, BW_THREADS, DKDV_SMEM, s>>>(mq, mo, md, a);
+    attn_bwd_dq_tc_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, mo, md, a);
     return 2;
 }
