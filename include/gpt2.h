@@ -156,6 +156,31 @@ typedef struct {
 } gpt2_adamw_config;
 int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* cfg);
 
+/* ZeRO-1 style sharded update (llm.c "State of the Union", "Multi-GPU
+ * training": optimizer state split over data-parallel ranks). AdamW as in
+ * gpt2_adamw_step_ex, applied only to the elements [begin, begin + count) of
+ * the flat parameter layout (master, moments, compute copy and gradient of
+ * that range; gpt2_flat_params elements: the tensors in canonical order, each
+ * starting on a 64-element boundary, the gaps zero and left zero by AdamW);
+ * a rank that owns a shard calls it for its range, and calls over ranges that
+ * tile [0, n) give, element for element, the values of one
+ * gpt2_adamw_step_ex (the update is elementwise). begin is a multiple of
+ * 2048, count a positive multiple of 4, begin + count <= n. Clipping needs the norm of
+ * every shard's gradient: max_grad_norm must be 0 here, and a caller that
+ * clips combines the shards' gpt2_grad_sumsq_range values into the clip
+ * factor and passes it in grad_scale. Allowed after gpt2_backward and after
+ * another shard call of the same step; GPT2_ERR_ARG / GPT2_ERR_STATE
+ * otherwise. */
+int gpt2_adamw_step_shard(gpt2_t* m, const gpt2_adamw_config* cfg, int64_t begin, int64_t count);
+
+/* Length n of the flat parameter layout (with the alignment gaps). */
+int64_t gpt2_flat_params(const gpt2_t* m);
+
+/* Sum of squares of the gradient elements [begin, begin + count) (fp32,
+ * deterministic order), written to *out (host); synchronises the stream.
+ * begin and count multiples of 4, count >= 4, begin + count <= n. */
+int gpt2_grad_sumsq_range(gpt2_t* m, int64_t begin, int64_t count, float* out);
+
 /* Learning rate of step t (1-based): linear warmup to lr_max over `warmup`
  * steps, then a half-cosine from lr_max down to lr_min at step `total`, and
  * lr_min after it. Host-only. */

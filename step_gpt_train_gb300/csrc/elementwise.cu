@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(256) grad_sumsq_kernel(float* __restrict__ par
 }
 
 __global__ void __launch_bounds__(1024) grad_norm_final_kernel(float* __restrict__ out,
-                                                               const float* __restrict__ partial) {
+                                                               const float* __restrict__ partial, int root) {
     __shared__ float sh[32];
     float v = partial[threadIdx.x];  // GN_BLOCKS == blockDim.x
     v = warp_sum(v);
@@ -644,14 +644,14 @@ __global__ void __launch_bounds__(1024) grad_norm_final_kernel(float* __restrict
     if (threadIdx.x == 0) {
         float t = 0.f;
         for (int w = 0; w < 32; w++) t += sh[w];
-        *out = sqrtf(t);
+        *out = root ? sqrtf(t) : t;
     }
 }
 
 size_t grad_norm_scratch() { return GN_BLOCKS * 4; }
 
-int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s) {
+int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s, int root) {
     grad_sumsq_kernel<<<GN_BLOCKS, 256, 0, s>>>(partial, g, n / 4);
-    grad_norm_final_kernel<<<1, GN_BLOCKS, 0, s>>>(norm_out, partial);
+    grad_norm_final_kernel<<<1, GN_BLOCKS, 0, s>>>(norm_out, partial, root);
     return 2;
 }

@@ -64,7 +64,7 @@ int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v
                  const float* gnorm = nullptr, float max_norm = 0.f, const uint32_t* decay_bits = nullptr);
 // *norm_out = ||g||_2 over n fp32 values (n % 4 == 0), deterministic; partial: grad_norm_scratch() bytes.
 size_t grad_norm_scratch();
-int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s);
+int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s, int root = 1);
 
 int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
                              int* status, cudaStream_t s);

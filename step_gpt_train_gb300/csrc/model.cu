@@ -682,6 +682,43 @@ int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* c) {
     return GPT2_OK;
 }
 
+int64_t gpt2_flat_params(const gpt2_t* m) { return m ? m->np : GPT2_ERR_ARG; }
+
+int gpt2_grad_sumsq_range(gpt2_t* m, int64_t begin, int64_t count, float* out) {
+    if (!m || !out || begin < 0 || count < 4 || count % 4 != 0 || begin % 4 != 0 || begin + count > m->np)
+        return GPT2_ERR_ARG;
+    if (launch_grad_norm(m->gnorm, m->gnorm_partial, m->grads + begin, count, m->stream, 0) < 0) return GPT2_ERR_CUDA;
+    m->launches += 2;
+    if (cudaGetLastError() != cudaSuccess) return GPT2_ERR_CUDA;
+    float v = 0.f;
+    if (cudaMemcpyAsync(&v, m->gnorm, sizeof(float), cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    TRY(cuda_ok(cudaStreamSynchronize(m->stream)));
+    *out = v;
+    return GPT2_OK;
+}
+
+int gpt2_adamw_step_shard(gpt2_t* m, const gpt2_adamw_config* c, int64_t begin, int64_t count) {
+    if (!m || !c) return GPT2_ERR_ARG;
+    if (c->t < 1 || !(c->beta1 >= 0.f && c->beta1 < 1.f) || !(c->beta2 >= 0.f && c->beta2 < 1.f) || !(c->eps >= 0.f) ||
+        !std::isfinite(c->lr) || !std::isfinite(c->weight_decay) || !(c->grad_scale > 0.f) ||
+        !std::isfinite(c->grad_scale) || c->max_grad_norm != 0.f || (c->decay_mask != 0 && c->decay_mask != 1))
+        return GPT2_ERR_ARG;
+    // a shard starts on a 2048-element boundary (one 32-bit word of the
+    // decay mask, one bit per 64 elements) and holds whole float4s
+    if (begin < 0 || count < 4 || begin % 2048 != 0 || count % 4 != 0 || begin + count > m->np) return GPT2_ERR_ARG;
+    if (m->state != 2 && m->state != 4) return GPT2_ERR_STATE;
+    Op op(m, GPT2_K_ADAMW);
+    TRY(op.done(launch_adamw(m->master + begin,
+                             m->mode == GPT2_MODE_BF16 ? (void*)((bf16*)m->params + begin) : nullptr,
+                             m->grads + begin, m->adam_m + begin, m->adam_v + begin, count, c->lr, c->beta1,
+                             c->beta2, c->eps, c->weight_decay, c->t, m->stream, c->grad_scale, nullptr, 0.f,
+                             c->decay_mask ? m->decay_bits + begin / 2048 : nullptr),
+                (double)count * (m->mode == GPT2_MODE_BF16 ? 30.0 : 28.0)));
+    m->state = 4;
+    return GPT2_OK;
+}
+
 float gpt2_lr_cosine(int t, int warmup, int total, float lr_max, float lr_min) {
     if (t < 1) return 0.f;
     if (warmup > 0 && t <= warmup) return lr_max * (float)t / (float)warmup;

@@ -64,6 +64,9 @@ _SIGNATURES = {
     "gpt2_zero_grad": (c_int, [c_void_p]),
     "gpt2_grad_norm": (c_int, [c_void_p, POINTER(c_float)]),
     "gpt2_adamw_step_ex": (c_int, [c_void_p, POINTER(gpt2_adamw_config)]),
+    "gpt2_adamw_step_shard": (c_int, [c_void_p, POINTER(gpt2_adamw_config), ctypes.c_int64, ctypes.c_int64]),
+    "gpt2_grad_sumsq_range": (c_int, [c_void_p, ctypes.c_int64, ctypes.c_int64, POINTER(ctypes.c_float)]),
+    "gpt2_flat_params": (c_int64, [c_void_p]),
     "gpt2_lr_cosine": (c_float, [c_int, c_int, c_int, c_float, c_float]),
     "gpt2_strerror": (c_char_p, [c_int]),
     "gpt2_num_tensors": (c_int, [c_void_p]),
@@ -250,6 +253,19 @@ class GPT2:
                               0.0 if max_grad_norm is None else max_grad_norm, int(bool(decay_mask)))
         check(self.lib.gpt2_adamw_step_ex(self.h, ctypes.byref(c)), "gpt2_adamw_step_ex")
 
+    def adamw_step_shard(self, begin, count, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1,
+                         grad_scale=1.0, decay_mask=False):
+        """gpt2_adamw_step_shard: AdamW on the flat parameter elements [begin, begin + count)."""
+        c = gpt2_adamw_config(lr, beta1, beta2, eps, weight_decay, t, grad_scale, 0.0, int(bool(decay_mask)))
+        check(self.lib.gpt2_adamw_step_shard(self.h, ctypes.byref(c), int(begin), int(count)), "gpt2_adamw_step_shard")
+
+    def grad_sumsq_range(self, begin, count) -> float:
+        """gpt2_grad_sumsq_range: sum of squares of the gradient elements [begin, begin + count)."""
+        out = ctypes.c_float(0.0)
+        check(self.lib.gpt2_grad_sumsq_range(self.h, int(begin), int(count), ctypes.byref(out)),
+              "gpt2_grad_sumsq_range")
+        return out.value
+
     def set_grad_accumulation(self, on: bool) -> None:
         check(self.lib.gpt2_set_grad_accumulation(self.h, int(bool(on))), "gpt2_set_grad_accumulation")
 
@@ -280,6 +296,10 @@ class GPT2:
 
     def num_params(self) -> int:
         return int(self.lib.gpt2_num_params(self.h))
+
+    def flat_params(self) -> int:
+        """Length of the flat parameter layout (tensors on 64-element boundaries)."""
+        return int(self.lib.gpt2_flat_params(self.h))
 
     def launch_count(self) -> int:
         return int(self.lib.gpt2_launch_count(self.h))

@@ -80,3 +80,59 @@ def test_grad_norm_and_clipped_masked_scaled_adamw(torch_cuda):
                                 HP["beta1"], HP["beta2"], HP["eps"], wd, 1, scale, clip)[0]
         assert rel_l2(got[k], ref) <= 1e-6, k
     model.close()
+
+
+@pytest.mark.parametrize("cfg", [TINY, SMALL_BF16])
+def test_sharded_adamw_equals_full_step(torch_cuda, cfg):
+    """ZeRO-1 style update: AdamW over shards that tile the flat parameter layout
+    gives the full step's masters, moments and compute copy bit for bit (the
+    update is elementwise), and the shards' gradient sums of squares add up to
+    the squared global norm."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import TENSOR_ADAM_M, TENSOR_ADAM_V, TENSOR_GRAD, TENSOR_MASTER, TENSOR_PARAM
+    B, T = (4, 64) if cfg is TINY else (3, 100)
+    tok, tgt = data.batches("uniform", B, T, 2, 31, vocab=cfg["vocab"])
+    models = [make_model(cfg), make_model(cfg)]
+    for m in models:
+        m.forward(torch.from_numpy(tok[0]).cuda(), torch.from_numpy(tgt[0]).cuda())
+        m.backward()
+    full, sharded = models
+    n = sharded.flat_params()
+    cut1, cut2 = 2048 * (n // (3 * 2048)), 2048 * (2 * n // (3 * 2048))
+    bounds = [(0, cut1), (cut1, cut2 - cut1), (cut2, n - cut2)]
+    assert all(c > 0 for _, c in bounds)
+    sumsq = sum(sharded.grad_sumsq_range(b, c) for b, c in bounds)
+    assert sumsq == pytest.approx(R.global_grad_norm(sharded.tensors(TENSOR_GRAD)) ** 2, rel=1e-5)
+    for t in (1, 2):
+        lr = 1e-3 * t
+        full.adamw_step(lr, t=t, grad_scale=0.5, decay_mask=True, **HP)
+        for b, c in reversed(bounds):  # any order: the shards are disjoint
+            sharded.adamw_step_shard(b, c, lr, t=t, grad_scale=0.5, decay_mask=True, **HP)
+        if t == 1:
+            for m in models:
+                m.forward(torch.from_numpy(tok[1]).cuda(), torch.from_numpy(tgt[1]).cuda())
+                m.backward()
+    kinds = (TENSOR_MASTER, TENSOR_ADAM_M, TENSOR_ADAM_V) + ((TENSOR_PARAM,) if cfg["mode"] == 1 else ())
+    for kind in kinds:
+        a, b = full.tensors(kind), sharded.tensors(kind)
+        for k in a:
+            assert np.array_equal(a[k], b[k]), (kind, k)
+    for m in models:
+        m.close()
+
+
+def test_shard_arguments_checked(torch_cuda):
+    from step_gpt_train_gb300.gpt2 import GPT2Error
+    torch = torch_cuda
+    tok, tgt = data.batches("uniform", 4, 64, 1, 5, vocab=512)
+    model = make_model(TINY)
+    with pytest.raises(GPT2Error):  # before any backward
+        model.adamw_step_shard(0, 2048, 1e-3)
+    model.forward(torch.from_numpy(tok[0]).cuda(), torch.from_numpy(tgt[0]).cuda())
+    model.backward()
+    n = model.flat_params()
+    for begin, count in ((1024, 2048), (0, 6), (0, n + 4), (-2048, 2048)):
+        with pytest.raises(GPT2Error):
+            model.adamw_step_shard(begin, count, 1e-3)
+    model.adamw_step_shard(0, n, 1e-3)
+    model.close()
