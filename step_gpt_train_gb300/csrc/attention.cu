@@ -14,33 +14,44 @@
 
 // ============================================================ backward: D = rowsum(dO * O)
 
-// One 8-element vector of dO and of O per thread; the hd/8 threads of a
-// (row, head) pair are adjacent lanes and add their partial dot products by a
-// shuffle tree (hd/8 is 1, 2, 4 or 8). All loads of a warp are contiguous.
-template <typename T>
+// One 8-element vector of dO and of O per thread; the PARTS = hd/8 threads
+// of a (row, head) pair are adjacent lanes and add their partial dot products
+// by a shuffle tree (PARTS is 1, 2, 4 or 8). All loads of a warp are
+// contiguous. Indices are 32-bit (the launcher checks B*T*H*PARTS < 2^31):
+// with 64-bit divisions the kernel was bound by integer arithmetic.
+template <typename T, int PARTS>
 __global__ void attn_bwd_dot_kernel(float* __restrict__ D, const T* __restrict__ dout, const T* __restrict__ o,
                                     int B, int Tlen, int C, int H) {
-    const int hd = C / H, parts = hd / 8;
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // ((b, t, h), part)
-    const int64_t pair = i / parts;
-    const int part = (int)(i % parts);
-    const bool valid = pair < (int64_t)B * Tlen * H;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;  // ((b, t, h), part)
+    const int pair = i / PARTS, part = i % PARTS;
+    const bool valid = pair < B * Tlen * H;
+    const int bt = valid ? pair / H : 0, h = pair - bt * H;
     float s = 0.f;
     if (valid) {
-        const int h = (int)(pair % H);
-        const int64_t bt = pair / H;
         float x[8], y[8];
-        load8(dout + bt * C + h * hd + part * 8, x);
-        load8(o + bt * C + h * hd + part * 8, y);
+        const int64_t off = (int64_t)bt * C + h * (8 * PARTS) + part * 8;
+        load8(dout + off, x);
+        load8(o + off, y);
 #pragma unroll
         for (int j = 0; j < 8; j++) s += x[j] * y[j];
     }
-    for (int off = parts / 2; off > 0; off /= 2) s += __shfl_xor_sync(0xffffffffu, s, off, parts);
+#pragma unroll
+    for (int off = PARTS / 2; off > 0; off /= 2) s += __shfl_xor_sync(0xffffffffu, s, off, PARTS);
     if (valid && part == 0) {
-        const int h = (int)(pair % H);
-        const int64_t bt = pair / H;
-        const int b = (int)(bt / Tlen), t = (int)(bt % Tlen);
-        D[((int64_t)b * H + h) * Tlen + t] = s;
+        const int b = bt / Tlen, t = bt - b * Tlen;
+        D[(b * H + h) * Tlen + t] = s;
+    }
+}
+
+template <typename T>
+void launch_dot(float* D, const T* dout, const T* o, int B, int T_, int C, int H, cudaStream_t s) {
+    const int parts = C / H / 8;
+    const int blocks = (int)(((int64_t)B * T_ * H * parts + 255) / 256);
+    switch (parts) {
+        case 1: attn_bwd_dot_kernel<T, 1><<<blocks, 256, 0, s>>>(D, dout, o, B, T_, C, H); break;
+        case 2: attn_bwd_dot_kernel<T, 2><<<blocks, 256, 0, s>>>(D, dout, o, B, T_, C, H); break;
+        case 4: attn_bwd_dot_kernel<T, 4><<<blocks, 256, 0, s>>>(D, dout, o, B, T_, C, H); break;
+        default: attn_bwd_dot_kernel<T, 8><<<blocks, 256, 0, s>>>(D, dout, o, B, T_, C, H); break;
     }
 }
 
@@ -205,18 +216,17 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
     const int hd = C / H;
     if (hd != 8 && hd != 16 && hd != 32 && hd != 64) return GPT2_ERR_ARG;  // the head sizes built
     if (B * T == 0) return 0;
+    if ((int64_t)B * T * H * (hd / 8) + 255 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // 32-bit indices below
     float* D = (float*)scratch;
-    const int64_t nrows = (int64_t)B * T * H;
-    const int dblocks = (int)((nrows * (hd / 8) + 255) / 256);  // hd/8 threads per (row, head)
     const float scale = 1.0f / sqrtf((float)hd);
     if (dtype == GPT2_MODE_BF16) {
         if (hd != 64) return GPT2_ERR_ARG;
-        attn_bwd_dot_kernel<bf16><<<dblocks, 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)o, B, T, C, H);
+        launch_dot(D, (const bf16*)dout, (const bf16*)o, B, T, C, H, s);
         const int r = launch_attention_backward_tc((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, lse, D, B, T, C,
                                                    H, status, s);
         return r < 0 ? r : 1 + r;
     }
-    attn_bwd_dot_kernel<float><<<dblocks, 256, 0, s>>>(D, (const float*)dout, (const float*)o, B, T, C, H);
+    launch_dot(D, (const float*)dout, (const float*)o, B, T, C, H, s);
     const int64_t n = (int64_t)B * H * T;
     const int blocks = (int)((n + 127) / 128);
 #define ATT_BWD_F32(HDV)                                                                                          \

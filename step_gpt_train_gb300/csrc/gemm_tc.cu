@@ -435,9 +435,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ D, const float* __restrict__ partial,
                                                            const bf16* __restrict__ bias, int M, int N, int BN,
                                                            int n_tiles, int splits, int accumulate) {
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-    if (i >= (int64_t)M * N) return;
-    const int m = (int)(i / N), n = (int)(i % N);
+    // 32-bit element index (the launcher keeps M * N < 2^31)
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (i >= M * N) return;
+    const int m = i / N, n = i - m * N;
     const int64_t tile = (int64_t)(m / BM) * n_tiles + n / BN;
     const int64_t tile_elems = (int64_t)BM * BN;
     const float* p = partial + tile * splits * tile_elems + (int64_t)(m % BM) * BN + n % BN;
@@ -595,6 +596,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
+    if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
     CUtensorMap ma, mb;
     bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
     ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
