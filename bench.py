@@ -200,6 +200,8 @@ def main():
     ap.add_argument("--config", default="124m-b32")
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="separate gpt2_forward / gpt2_backward / gpt2_adamw_step calls instead of gpt2_step")
     ap.add_argument("--ref-T", type=int, default=256)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -232,6 +234,8 @@ def main():
     d_tgt = torch.from_numpy(tgt).cuda()
 
     def step(s, tk, tg):
+        if not args.eager:  # one captured graph per step (gpt2_step)
+            return model.step(tk, tg, lr_at(s + 1), t=s + 1, **HP)
         loss = model.forward(tk, tg)
         model.backward()
         model.adamw_step(lr_at(s + 1), t=s + 1, **HP)
@@ -329,6 +333,8 @@ def main():
             "config": {"workload": workload_label(args.config, w, B, T),
                        "parallelism": f"replicas x{world} (no exchange)" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2: each step touches ~15 GB of weights, activations and state",
+                       "api": "gpt2_forward, gpt2_backward, gpt2_adamw_step" if args.eager
+                       else "gpt2_step (the step replayed as one CUDA graph)",
                        "roofline_pass": "per-kernel times from a separate instrumented pass of the same steps"},
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "roofline": roofline, "mfu": mfu,
             "kernel_ms_per_step": kernel_ms, "loss_first_last": [losses[0], losses[-1]]}

@@ -156,6 +156,20 @@ typedef struct {
 } gpt2_adamw_config;
 int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* cfg);
 
+/* One whole training step, replayed as a CUDA graph: tokens and targets
+ * (device, int32 [B,T]) are copied into the library's own buffers, then the
+ * forward to the mean loss, the backward, the global-norm clip when
+ * cfg->max_grad_norm > 0 and AdamW run as one captured graph; the loss comes
+ * back in *loss_out (the stream is synchronised once). The values of cfg
+ * (lr, t, ...) are read by the device each step, so one graph serves every
+ * step; it is captured again when B, T, gradient accumulation, the decay mask
+ * or max_grad_norm change. The first step with new such settings, and every
+ * step while per-op timing is on, run eagerly. The results equal
+ * gpt2_forward, gpt2_backward and gpt2_adamw_step_ex bit for bit. Errors as
+ * for those calls; on success the state is that after gpt2_adamw_step_ex. */
+int gpt2_step(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T,
+              const gpt2_adamw_config* cfg, float* loss_out);
+
 /* ZeRO-1 style sharded update (llm.c "State of the Union", "Multi-GPU
  * training": optimizer state split over data-parallel ranks). AdamW as in
  * gpt2_adamw_step_ex, applied only to the elements [begin, begin + count) of

@@ -543,7 +543,20 @@ __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ theta, b
                                                     float* __restrict__ v, int64_t n4, float lr, float b1, float b2,
                                                     float eps, float wd, float inv_bc1, float inv_bc2,
                                                     float grad_scale, const float* __restrict__ gnorm, float max_norm,
-                                                    const uint32_t* __restrict__ decay_bits) {
+                                                    const uint32_t* __restrict__ decay_bits,
+                                                    const float* __restrict__ hp) {
+    if (hp) {
+        // the step's values from device memory (a captured step graph reads
+        // the values written before each launch)
+        lr = hp[0];
+        b1 = hp[1];
+        b2 = hp[2];
+        eps = hp[3];
+        wd = hp[4];
+        inv_bc1 = hp[5];
+        inv_bc2 = hp[6];
+        grad_scale = hp[7];
+    }
     const int64_t base = (int64_t)blockIdx.x * (256 * ADAM_UNROLL) + threadIdx.x;
     float gs = grad_scale;
     if (gnorm && max_norm > 0.f) gs *= fminf(1.f, max_norm / (*gnorm * grad_scale + 1e-6f));
@@ -591,9 +604,11 @@ __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ theta, b
     }
 }
 
+// hp, when given: a device block {lr, beta1, beta2, eps, weight_decay,
+// 1/(1-beta1^t), 1/(1-beta2^t), grad_scale} read in place of those arguments.
 int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v, int64_t n, float lr, float b1,
                  float b2, float eps, float wd, int t, cudaStream_t s, float grad_scale, const float* gnorm,
-                 float max_norm, const uint32_t* decay_bits) {
+                 float max_norm, const uint32_t* decay_bits, const float* hp) {
     const int64_t n4 = n / 4;
     const double bc1 = 1.0 - pow((double)b1, (double)t);
     const double bc2 = 1.0 - pow((double)b2, (double)t);
@@ -602,7 +617,7 @@ int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v
     if (blocks == 0) return 0;
     adamw_kernel<<<blocks, 256, 0, s>>>(master, (bf16*)pbf, grad, m, v, n4, lr, b1, b2, eps, wd,
                                         (float)(1.0 / bc1), (float)(1.0 / bc2), grad_scale, gnorm, max_norm,
-                                        decay_bits);
+                                        decay_bits, hp);
     return 1;
 }
 

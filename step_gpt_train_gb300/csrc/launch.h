@@ -61,7 +61,8 @@ int launch_mean_loss(float* out, const float* losses, int N, cudaStream_t s);
 // chunk, null = all) selects where weight decay applies.
 int launch_adamw(float* master, void* pbf, const float* grad, float* m, float* v, int64_t n, float lr, float b1,
                  float b2, float eps, float wd, int t, cudaStream_t s, float grad_scale = 1.f,
-                 const float* gnorm = nullptr, float max_norm = 0.f, const uint32_t* decay_bits = nullptr);
+                 const float* gnorm = nullptr, float max_norm = 0.f, const uint32_t* decay_bits = nullptr,
+                 const float* hp = nullptr);
 // *norm_out = ||g||_2 over n fp32 values (n % 4 == 0), deterministic; partial: grad_norm_scratch() bytes.
 size_t grad_norm_scratch();
 int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n, cudaStream_t s, int root = 1);

@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -62,6 +63,8 @@ struct gpt2 {
     int* status;
     float* loss_dev;
     int32_t* tokens;
+    int32_t* targets;  // gpt2_step's copy of the step's targets (a fixed address for its graph)
+    float* hp_dev;     // gpt2_step: the AdamW values of the step, read by the captured AdamW
     std::vector<LayerBufs> layers;
     void *xL, *lnf, *logits, *fwd_tmp;
     float *meanf, *rstdf, *losses;
@@ -81,6 +84,20 @@ struct gpt2 {
     struct Pending { int fam; cudaEvent_t a, b; };
     std::vector<Pending> pending;
     std::vector<cudaEvent_t> pool;
+    // gpt2_step: the captured step and what it was captured for
+    struct StepKey {
+        int B, T, grad_accum, clip, decay_mask;
+        float max_grad_norm;
+        bool operator==(const StepKey& o) const {
+            return B == o.B && T == o.T && grad_accum == o.grad_accum && clip == o.clip &&
+                   decay_mask == o.decay_mask && max_grad_norm == o.max_grad_norm;
+        }
+    };
+    StepKey step_key{};
+    bool step_warm = false;                // one eager step ran with step_key
+    cudaGraphExec_t step_exec = nullptr;   // the captured step for step_key
+    cudaStream_t capture_stream = nullptr;  // the graph is captured here (the caller's may be the legacy stream)
+    int64_t step_launches = 0;             // kernel launches in one replay
 };
 
 namespace {
@@ -154,6 +171,7 @@ size_t plan(const gpt2_config* c, gpt2* m) {
     };
     const size_t o_status = take(256);
     const size_t o_tokens = take(BT * 4);
+    const size_t o_targets = take(BT * 4);
     const size_t o_master = take((size_t)np * 4);
     const size_t o_params = c->mode == GPT2_MODE_BF16 ? take((size_t)np * 2) : o_master;
     const size_t o_grads = take((size_t)np * 4);
@@ -214,6 +232,8 @@ size_t plan(const gpt2_config* c, gpt2* m) {
         m->status = (int*)(w + o_status);
         m->loss_dev = (float*)(w + o_status + 64);
         m->tokens = (int32_t*)(w + o_tokens);
+        m->targets = (int32_t*)(w + o_targets);
+        m->hp_dev = (float*)(w + o_status + 192);
         m->master = (float*)(w + o_master);
         m->params = w + o_params;
         m->grads = (float*)(w + o_grads);
@@ -684,6 +704,112 @@ int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* c) {
 
 int64_t gpt2_flat_params(const gpt2_t* m) { return m ? m->np : GPT2_ERR_ARG; }
 
+namespace {
+
+// Everything of one training step after its inputs are in place: forward to
+// the mean loss, backward, the device-side clip norm when asked, and AdamW
+// with its values read from hp_dev.
+int step_body(gpt2* m, int B, int T, const gpt2_adamw_config* c) {
+    TRY(forward_impl(m, m->targets, B, T));
+    TRY(backward_impl(m));
+    if (c->max_grad_norm > 0.f) {
+        if (launch_grad_norm(m->gnorm, m->gnorm_partial, m->grads, m->np, m->stream) < 0) return GPT2_ERR_CUDA;
+        m->launches += 2;
+    }
+    Op op(m, GPT2_K_ADAMW);
+    return op.done(launch_adamw(m->master, m->mode == GPT2_MODE_BF16 ? m->params : nullptr, m->grads, m->adam_m,
+                                m->adam_v, m->np, c->lr, c->beta1, c->beta2, c->eps, c->weight_decay, c->t,
+                                m->stream, c->grad_scale, c->max_grad_norm > 0.f ? m->gnorm : nullptr,
+                                c->max_grad_norm, c->decay_mask ? m->decay_bits : nullptr, m->hp_dev),
+                   (double)m->np * (m->mode == GPT2_MODE_BF16 ? 30.0 : 28.0));
+}
+
+}  // namespace
+
+int gpt2_step(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T, const gpt2_adamw_config* c,
+              float* loss_out) {
+    if (!m || !d_tokens || !d_targets || !loss_out || !c || B < 1 || T < 1 || B > m->maxB || T > m->maxT)
+        return GPT2_ERR_ARG;
+    if (c->t < 1 || !(c->beta1 >= 0.f && c->beta1 < 1.f) || !(c->beta2 >= 0.f && c->beta2 < 1.f) || !(c->eps >= 0.f) ||
+        !std::isfinite(c->lr) || !std::isfinite(c->weight_decay) || !(c->grad_scale > 0.f) ||
+        !std::isfinite(c->grad_scale) || !(c->max_grad_norm >= 0.f) || (c->decay_mask != 0 && c->decay_mask != 1))
+        return GPT2_ERR_ARG;
+    m->state = 0;
+    m->B = B;
+    m->T = T;
+    // the step's AdamW values, computed as launch_adamw computes its arguments
+    const float hp[8] = {c->lr, c->beta1, c->beta2, c->eps, c->weight_decay,
+                         (float)(1.0 / (1.0 - std::pow((double)c->beta1, (double)c->t))),
+                         (float)(1.0 / (1.0 - std::pow((double)c->beta2, (double)c->t))), c->grad_scale};
+    const size_t bt = (size_t)B * T * 4;
+    if (cudaMemcpyAsync(m->hp_dev, hp, sizeof(hp), cudaMemcpyHostToDevice, m->stream) != cudaSuccess ||
+        cudaMemsetAsync(m->status, 0, sizeof(int), m->stream) != cudaSuccess ||
+        cudaMemcpyAsync(m->tokens, d_tokens, bt, cudaMemcpyDeviceToDevice, m->stream) != cudaSuccess ||
+        cudaMemcpyAsync(m->targets, d_targets, bt, cudaMemcpyDeviceToDevice, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    const gpt2::StepKey key{B, T, m->grad_accum, c->max_grad_norm > 0.f ? 1 : 0, c->decay_mask, c->max_grad_norm};
+    if (!(key == m->step_key)) {
+        if (m->step_exec) cudaGraphExecDestroy(m->step_exec);
+        m->step_exec = nullptr;
+        m->step_warm = false;
+        m->step_key = key;
+    }
+    if (m->timing || !m->step_warm) {
+        // eagerly: with per-op timing on, and the first time for these sizes
+        // and options, so that every lazy setup of the kernels runs outside a capture
+        TRY(step_body(m, B, T, c));
+        m->step_warm = !m->timing;
+    } else {
+        if (!m->step_exec) {
+            // capturing enqueues nothing: the per-family counters are put back after it
+            const int64_t before = m->launches;
+            int64_t calls[GPT2_K_COUNT], launches[GPT2_K_COUNT];
+            double work[GPT2_K_COUNT];
+            std::copy(m->fam_calls, m->fam_calls + GPT2_K_COUNT, calls);
+            std::copy(m->fam_launches, m->fam_launches + GPT2_K_COUNT, launches);
+            std::copy(m->fam_work, m->fam_work + GPT2_K_COUNT, work);
+            cudaGraph_t graph = nullptr;
+            // capture on a stream of the library's own (the legacy default
+            // stream cannot be captured); the work is launched below on the
+            // caller's stream, so capturing enqueues nothing anywhere
+            if (!m->capture_stream && cudaStreamCreateWithFlags(&m->capture_stream, cudaStreamNonBlocking) != cudaSuccess)
+                return GPT2_ERR_CUDA;
+            const cudaStream_t user_stream = m->stream;
+            if (cudaStreamBeginCapture(m->capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+                return GPT2_ERR_CUDA;
+            m->stream = m->capture_stream;
+            const int r = step_body(m, B, T, c);
+            m->stream = user_stream;
+            const cudaError_t e = cudaStreamEndCapture(m->capture_stream, &graph);
+            if (r != GPT2_OK || e != cudaSuccess) {
+                if (graph) cudaGraphDestroy(graph);
+                return r != GPT2_OK ? r : GPT2_ERR_CUDA;
+            }
+            const cudaError_t ie = cudaGraphInstantiate(&m->step_exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (ie != cudaSuccess) {
+                m->step_exec = nullptr;
+                return GPT2_ERR_CUDA;
+            }
+            m->step_launches = m->launches - before;
+            m->launches = before;
+            std::copy(calls, calls + GPT2_K_COUNT, m->fam_calls);
+            std::copy(launches, launches + GPT2_K_COUNT, m->fam_launches);
+            std::copy(work, work + GPT2_K_COUNT, m->fam_work);
+        }
+        if (cudaGraphLaunch(m->step_exec, m->stream) != cudaSuccess) return GPT2_ERR_CUDA;
+        m->launches += m->step_launches;
+    }
+    float loss = 0.f;
+    if (cudaMemcpyAsync(&loss, m->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    TRY(read_status(m));  // synchronises the stream
+    *loss_out = loss;
+    if (!std::isfinite(loss)) return GPT2_ERR_NONFINITE;
+    m->state = 3;
+    return GPT2_OK;
+}
+
 int gpt2_grad_sumsq_range(gpt2_t* m, int64_t begin, int64_t count, float* out) {
     if (!m || !out || begin < 0 || count < 4 || count % 4 != 0 || begin % 4 != 0 || begin + count > m->np)
         return GPT2_ERR_ARG;
@@ -730,6 +856,8 @@ float gpt2_lr_cosine(int t, int warmup, int total, float lr_max, float lr_min) {
 int gpt2_destroy(gpt2_t* m) {
     if (!m) return GPT2_ERR_ARG;
     cudaStreamSynchronize(m->stream);
+    if (m->step_exec) cudaGraphExecDestroy(m->step_exec);
+    if (m->capture_stream) cudaStreamDestroy(m->capture_stream);
     for (auto& p : m->pending) {
         cudaEventDestroy(p.a);
         cudaEventDestroy(p.b);

@@ -67,6 +67,7 @@ _SIGNATURES = {
     "gpt2_adamw_step_shard": (c_int, [c_void_p, POINTER(gpt2_adamw_config), ctypes.c_int64, ctypes.c_int64]),
     "gpt2_grad_sumsq_range": (c_int, [c_void_p, ctypes.c_int64, ctypes.c_int64, POINTER(ctypes.c_float)]),
     "gpt2_flat_params": (c_int64, [c_void_p]),
+    "gpt2_step": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, POINTER(gpt2_adamw_config), POINTER(c_float)]),
     "gpt2_lr_cosine": (c_float, [c_int, c_int, c_int, c_float, c_float]),
     "gpt2_strerror": (c_char_p, [c_int]),
     "gpt2_num_tensors": (c_int, [c_void_p]),
@@ -252,6 +253,18 @@ class GPT2:
         c = gpt2_adamw_config(lr, beta1, beta2, eps, weight_decay, t, 1.0 if grad_scale is None else grad_scale,
                               0.0 if max_grad_norm is None else max_grad_norm, int(bool(decay_mask)))
         check(self.lib.gpt2_adamw_step_ex(self.h, ctypes.byref(c)), "gpt2_adamw_step_ex")
+
+    def step(self, tokens, targets, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1, grad_scale=1.0,
+             max_grad_norm=0.0, decay_mask=False) -> float:
+        """gpt2_step: forward, backward and AdamW as one captured CUDA graph; returns the mean loss.
+        tokens/targets: int32 CUDA tensors [B, T] (contiguous)."""
+        B, T = tokens.shape
+        c = gpt2_adamw_config(lr, beta1, beta2, eps, weight_decay, t, grad_scale, max_grad_norm,
+                              int(bool(decay_mask)))
+        loss = c_float(0.0)
+        check(self.lib.gpt2_step(self.h, tokens.data_ptr(), targets.data_ptr(), B, T, ctypes.byref(c),
+                                 ctypes.byref(loss)), "gpt2_step")
+        return loss.value
 
     def adamw_step_shard(self, begin, count, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1,
                          grad_scale=1.0, decay_mask=False):

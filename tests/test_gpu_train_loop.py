@@ -136,3 +136,32 @@ def test_shard_arguments_checked(torch_cuda):
             model.adamw_step_shard(begin, count, 1e-3)
     model.adamw_step_shard(0, n, 1e-3)
     model.close()
+
+
+@pytest.mark.parametrize("cfg", [TINY, SMALL_BF16])
+def test_step_graph_equals_separate_calls(torch_cuda, cfg):
+    """gpt2_step (forward, backward, clip and AdamW replayed as one captured CUDA
+    graph) gives the losses, masters and moments of the separate calls bit for
+    bit, with the learning rate changing every step and a change of options
+    (which captures a second graph) on the way."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import TENSOR_ADAM_M, TENSOR_ADAM_V, TENSOR_MASTER
+    B, T = (4, 64) if cfg is TINY else (3, 100)
+    tok, tgt = data.batches("uniform", B, T, 6, 41, vocab=cfg["vocab"])
+    sep, graph = make_model(cfg), make_model(cfg)
+    for s in range(6):
+        # steps 0-2: no clip, no mask (eager, capture, replay); 3-5: clip and mask (a new graph)
+        opts = dict(grad_scale=0.5, max_grad_norm=0.05 if s >= 3 else 0.0, decay_mask=s >= 3, **HP)
+        lr = 1e-3 * (1 + s)
+        tt, gg = torch.from_numpy(tok[s]).cuda(), torch.from_numpy(tgt[s]).cuda()
+        la = sep.forward(tt, gg)
+        sep.backward()
+        sep.adamw_step(lr, t=s + 1, **opts)
+        lb = graph.step(tt, gg, lr, t=s + 1, **opts)
+        assert la == lb, (s, la, lb)
+    for kind in (TENSOR_MASTER, TENSOR_ADAM_M, TENSOR_ADAM_V):
+        a, b = sep.tensors(kind), graph.tensors(kind)
+        for k in a:
+            assert np.array_equal(a[k], b[k]), (kind, k)
+    sep.close()
+    graph.close()
