@@ -1,0 +1,71 @@
+"""Pins for the FP8 oracle (e4m3 format, per-tensor quantization, FP8 product),
+against the format's published constants, a library conversion and closed
+forms; no GPU."""
+import numpy as np
+import pytest
+
+from oracle import fp8_ref as F
+
+
+def test_e4m3_format_constants():
+    # OCP 8-bit floating point, E4M3: largest finite 448 = 1.75 * 2^8, smallest
+    # normal 2^-6, smallest subnormal 2^-9, one NaN pattern per sign, no infinity
+    v = F.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x07] == 7 * 2.0 ** -9 and v[0x01] == 2.0 ** -9
+    assert v[0x38] == 1.0 and v[0x40] == 2.0 and v[0x30] == 0.5
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and int(np.isnan(v).sum()) == 2
+    assert v[0x00] == 0.0 and v[0x80] == 0.0 and np.signbit(v[0x80])
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)  # codes 0x00..0x7E increase with value
+
+
+def test_e4m3_round_trip_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    v = F.e4m3_decode(codes)
+    fin = ~np.isnan(v)
+    assert np.array_equal(F.e4m3_encode(v[fin]), codes[fin])
+
+
+def test_e4m3_encode_matches_library_conversion():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.uniform(-448, 448, 50000), rng.normal(0, 1e-2, 50000),
+                        rng.normal(0, 1e-3, 20000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(F.e4m3_encode(x), ref)
+
+
+def test_e4m3_ties_saturation_nan():
+    enc = lambda a: int(F.e4m3_encode(np.float32(a)))
+    assert enc(1.0625) == 0x38 and enc(1.1875) == 0x3A  # midpoints go to the even code
+    assert enc(0.5 * 2.0 ** -9) == 0x00 and enc(1.5 * 2.0 ** -9) == 0x02  # subnormal ties
+    assert enc(448.0) == 0x7E and enc(449.0) == 0x7E and enc(1e30) == 0x7E and enc(-1e30) == 0xFE
+    assert enc(np.nan) == 0x7F
+    assert enc(-1e-30) == 0x80  # the sign survives a rounding to zero
+
+
+def test_quantize_per_tensor_scaling():
+    rng = np.random.default_rng(3)
+    x = (rng.normal(0, 0.02, (64, 96)) * np.where(rng.random((64, 96)) < 0.01, 50.0, 1.0)).astype(np.float32)
+    codes, scale_inv = F.quantize_e4m3(x)
+    i = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert codes[i] in (0x7E, 0xFE)  # the largest magnitude maps to +-448
+    assert scale_inv == np.float32(np.max(np.abs(x))) / np.float32(448.0)
+    back = F.e4m3_decode(codes) * float(scale_inv)
+    normal = np.abs(x) * (448.0 / np.max(np.abs(x))) >= 2.0 ** -6
+    # within half a unit in the last place: 2^-4 relative for normals
+    assert np.all(np.abs(back - x)[normal] <= 2.0 ** -4 * np.abs(x)[normal] * (1 + 1e-6))
+    zeros, s0 = F.quantize_e4m3(np.zeros(8, np.float32))
+    assert np.all(zeros == 0) and s0 == 1.0
+
+
+def test_matmul_fp8_closed_form():
+    # A = [[1, 2], [0.5, -1]], B = [[0.25, 4], [1, 1]] as e4m3 codes, scales 2 and 1/4
+    a = F.e4m3_encode(np.array([[1.0, 2.0], [0.5, -1.0]]))
+    b = F.e4m3_encode(np.array([[0.25, 4.0], [1.0, 1.0]]))
+    d = F.matmul_fp8(a, 2.0, b, 0.25, bias=np.array([1.0, -1.0]))
+    # (A B^T) = [[8.25, 3], [-3.875, -0.5]]; times 0.5; plus the bias
+    assert np.array_equal(d, np.array([[5.125, 0.5], [-0.9375, -1.25]]))
