@@ -76,7 +76,9 @@ struct GemmArgs {
     int kbs;             // k-blocks per split
     int n_tiles;         // ceil(N / BN)
     int units;           // m_tiles * n_tiles * splits
-    int num_kb;          // ceil(K / 64)
+    int num_kb;          // ceil(K / k-block width): 64 bf16 or 128 e4m3 values (128 bytes either way)
+    const float* a_scale;  // e4m3 operands: device scalars by which the codes of A and of B are
+    const float* b_scale;  // multiplied back (the product scales the accumulator)
 };
 
 // One unit of a CTA's work: k-blocks [kb0, kb1) of a tile; z = partial slot.
@@ -119,14 +121,15 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
 // convert, stage, TMA store. fp32 output goes out as two 16-column halves.
 // ncols_valid = columns of the chunk inside the matrix (> 0). aux holds this
 // lane's 32 factors (EPI_MUL).
-template <int EPI>
+template <int EPI, bool F8 = false>
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
                                           uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD,
                                           const CUtensorMap* mapD2, const uint4 (&aux)[4], int x, int y, int z,
-                                          int ncols_valid, int lane) {
+                                          int ncols_valid, int lane, float alpha = 1.f) {
     float f[32];
 #pragma unroll
-    for (int j = 0; j < 32; j++) f[j] = __uint_as_float(r[j]) + (bias_s ? bias_s[j] : 0.f);
+    for (int j = 0; j < 32; j++)
+        f[j] = (F8 ? __uint_as_float(r[j]) * alpha : __uint_as_float(r[j])) + (bias_s ? bias_s[j] : 0.f);
     if (EPI != EPI_NONE) {
         // the linear output rounded to bf16, as a separate pass would read it
 #pragma unroll
@@ -171,11 +174,15 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
 
 // ---------------------------------------------------------------- kernel
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+// F8: e4m3 operands (K-major only): a k-block is 128 values, four K = 32 MMAs
+// of kind::f8f6f4, and the epilogue scales the accumulator by a_scale * b_scale.
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const GemmArgs g) {
+    static_assert(!F8 || (!A_MN && !B_MN && EPI == EPI_NONE), "e4m3 operands: K-major, plain epilogue");
+    constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -246,13 +253,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sa = a_stage0 + stage * Cfg::A_BYTES;
                     const uint32_t sb = b_stage0 + stage * Cfg::B_BYTES;
                     if (!A_MN) {
-                        tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m0);
+                        tma_load_2d(sa, &tmA, full_bar(stage), kb * KE, m0);
                     } else {
                         tma_load_2d(sa, &tmA, full_bar(stage), m0, kb * BK);
                         tma_load_2d(sa + 64 * 128, &tmA, full_bar(stage), m0 + 64, kb * BK);
                     }
                     if (!B_MN) {
-                        tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, n0);
+                        tma_load_2d(sb, &tmB, full_bar(stage), kb * KE, n0);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BN / 64; c++)
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // whole warp runs the schedule (warp-uniform operands), one elected
             // lane issues the MMAs and commits
             const bool leader = elect_one();
-            constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
+            constexpr uint32_t idesc = F8 ? make_idesc_f8(BM, BN) : make_idesc(BM, BN, A_MN, B_MN);
             constexpr uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-wide k step
             constexpr uint32_t b_kstep = B_MN ? 16 * 128 : 32;
             constexpr uint32_t a_lbo = A_MN ? 64 * 128 : 16;
@@ -303,7 +310,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < BK / 16; k++) {
                         const uint64_t ad = sw128_desc(sa + k * a_kstep, a_lbo, 1024);
                         const uint64_t bd = sw128_desc(sb + k * b_kstep, b_lbo, 1024);
-                        if (leader) tc_mma(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if (leader) {
+                            if (F8) tc_mma_f8(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                            else tc_mma(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     if (leader) tc_commit(empty_bar(stage));  // stage reusable once these MMAs finish
                     if (++stage == S) {
@@ -334,6 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* stage = out_stage + ew * Cfg::OUT_STAGE_BYTES;
         const uint32_t stage_addr = smem_addr(stage);
         const bool use_bias = g.bias != nullptr && !g.partials;
+        const float alpha = F8 ? *g.a_scale * *g.b_scale : 1.f;
         int acc = 0;
         uint32_t acc_phase = 0;
         Work w;
@@ -393,16 +404,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // ra holds chunk c; chunk c+1 is loaded into rb while ra is stored
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
-                epi_chunk<EPI>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z, ncols(c),
-                               lane);
+                epi_chunk<EPI, F8>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
+                                   ncols(c), lane, alpha);
                 if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();  // reconverge before the warp-collective TMEM ops
                 if (!more) break;
                 tc_ld_wait(rb);
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
-                epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1), ys, z,
-                               ncols(c + 1), lane);
+                epi_chunk<EPI, F8>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1),
+                                   ys, z, ncols(c + 1), lane, alpha);
                 if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
@@ -477,6 +488,21 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major [outer, inner] matrix of bytes (e4m3 codes), box
+// [box_outer, 128] (128 bytes), 128-byte swizzle, out-of-bounds bytes read as zero.
+bool make_map_u8(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 3-D tensor map over an output [Z][M][N] (bf16 or fp32): box of 32 rows by
 // 64 bytes of columns, 64-byte swizzle; stores outside [0,N) x [0,M) are clipped.
 bool make_out_map(CUtensorMap* map, const void* ptr, bool fp32, uint64_t N, uint64_t M, uint64_t Z) {
@@ -543,17 +569,17 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
     return p;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                const GemmArgs& args, int grid, cudaStream_t s) {
     using Cfg = TileCfg<BN>;
     static bool configured = false;
     if (!configured) {
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES);
         configured = true;
     }
-    gemm_tc_kernel<BN, A_MN, B_MN, EPI><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
+    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
 }
 
 // The operand layouts, and the fused epilogues only where the step uses them:
@@ -608,6 +634,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     else md2 = md;
     if (!ok) return GPT2_ERR_CUDA;
     GemmArgs g;
+    g.a_scale = g.b_scale = nullptr;
     g.bias = partials ? nullptr : bias;
     g.aux = aux;
     g.status = status;
@@ -637,6 +664,42 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
 }
 
 }  // namespace
+
+int launch_matmul_fp8(bf16* D, const uint8_t* A, const float* a_scale, const uint8_t* B, const float* b_scale,
+                      const bf16* bias, int M, int N, int K, int* status, cudaStream_t s) {
+    if (!D || !A || !B || !a_scale || !b_scale || M < 1 || N < 1 || K < 1) return GPT2_ERR_ARG;
+    if (K % 16 != 0 || N % 8 != 0) return GPT2_ERR_ARG;  // 16-byte row strides of A, B and D
+    Plan p = make_plan(M, N, K, 0);  // tile width and grid as for bf16; one k-range per tile
+    p.num_kb = (K + 127) / 128;
+    p.kbs = p.num_kb;
+    p.splits = 1;
+    p.units = p.tiles;
+    p.grid = p.units < gpt2_num_sms() ? p.units : gpt2_num_sms();
+    CUtensorMap ma, mb, md;
+    bool ok = make_map_u8(&ma, A, (uint64_t)K, (uint64_t)M, BM) && make_map_u8(&mb, B, (uint64_t)K, (uint64_t)N, p.bn) &&
+              make_out_map(&md, D, false, (uint64_t)N, (uint64_t)M, 1);
+    if (!ok) return GPT2_ERR_CUDA;
+    GemmArgs g;
+    g.bias = bias;
+    g.aux = nullptr;
+    g.status = status;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.d_fp32 = 0;
+    g.splits = 1;
+    g.partials = 0;
+    g.kbs = p.kbs;
+    g.n_tiles = p.n_tiles;
+    g.units = p.units;
+    g.num_kb = p.num_kb;
+    g.a_scale = a_scale;
+    g.b_scale = b_scale;
+    if (p.bn == 128) launch_tc<128, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
+    else if (p.bn == 192) launch_tc<192, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
+    else launch_tc<256, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
+    return 1;
+}
 
 int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
                      int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate) {

@@ -102,6 +102,10 @@ _SIGNATURES = {
                                c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
     "gpt2_op_matmul_gelu": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                     c_void_p, c_void_p]),
+    "gpt2_op_quantize_fp8_scratch": (c_size_t, []),
+    "gpt2_op_quantize_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_size_t, c_void_p]),
+    "gpt2_op_matmul_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                   c_void_p, c_void_p]),
     "gpt2_op_matmul_gelu_backward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                              c_void_p, c_void_p]),
     "gpt2_op_attention_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
@@ -430,6 +434,22 @@ def gpt2_op_matmul(D, A, a_mn, B, b_mn, M, N, K, bias=None, status=None, stream=
 
 def gpt2_lr_cosine(t: int, warmup: int, total: int, lr_max: float, lr_min: float) -> float:
     return float(load_library().gpt2_lr_cosine(int(t), int(warmup), int(total), float(lr_max), float(lr_min)))
+
+
+def gpt2_op_quantize_fp8(q, scales, x, stream=None):
+    """q (uint8 [n]) = e4m3 codes of x (bf16) scaled per tensor; scales (float32 [2]) = 448/amax, amax/448."""
+    lib = load_library()
+    sc = _scratch(lib.gpt2_op_quantize_fp8_scratch())
+    check(lib.gpt2_op_quantize_fp8(_p(q), _p(scales), _p(x), x.numel(), _p(sc), sc.numel(), _s(stream)),
+          "gpt2_op_quantize_fp8")
+
+
+def gpt2_op_matmul_fp8(D, A, a_scales, B, b_scales, bias=None, status=None, stream=None):
+    """D (bf16 [M,N]) = (A B^T) a_scales[1] b_scales[1] (+ bias); A [M,K], B [N,K] e4m3 codes (uint8)."""
+    M, K = A.shape
+    N = B.shape[0]
+    check(load_library().gpt2_op_matmul_fp8(_p(D), _p(A), _p(a_scales), _p(B), _p(b_scales), _p(bias), M, N, K,
+                                            _p(status), _s(stream)), "gpt2_op_matmul_fp8")
 
 
 def gpt2_op_matmul_gelu(dgelu, out, A, W, bias=None, status=None, stream=None):

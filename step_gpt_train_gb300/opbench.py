@@ -94,6 +94,30 @@ def main(argv=None):
             return lambda: g.gpt2_op_matmul_gelu_backward(du, dY, W, u, stream=torch.cuda.current_stream())
         return setup, 2.0 * N * 4 * C * C, "flop"
 
+    def gemm_fp8_op(Nn, K):  # e4m3 linear forward (codes quantized once; the GEMM is timed)
+        def setup():
+            A, W, b = rnd(N, K), rnd(Nn, K, std=0.02), rnd(Nn)
+            qa = torch.empty(N, K, device=dev, dtype=torch.uint8)
+            qw = torch.empty(Nn, K, device=dev, dtype=torch.uint8)
+            sa = torch.empty(2, device=dev, dtype=torch.float32)
+            sw = torch.empty(2, device=dev, dtype=torch.float32)
+            g.gpt2_op_quantize_fp8(qa, sa, A)
+            g.gpt2_op_quantize_fp8(qw, sw, W)
+            D = torch.empty(N, Nn, device=dev, dtype=bf)
+            return lambda: g.gpt2_op_matmul_fp8(D, qa, sa, qw, sw, bias=b, stream=torch.cuda.current_stream())
+        return setup, 2.0 * N * Nn * K, "flop8"
+
+    def quantize_op():  # per-tensor e4m3 quantization of the MLP's hidden activations
+        def setup():
+            x = rnd(N, 4 * C)
+            q = torch.empty(N, 4 * C, device=dev, dtype=torch.uint8)
+            sc = torch.empty(2, device=dev, dtype=torch.float32)
+            return lambda: g.gpt2_op_quantize_fp8(q, sc, x, stream=torch.cuda.current_stream())
+        return setup, N * 4.0 * C * (2 * 2 + 1), "byte"  # amax pass reads x, quantize reads x, writes q
+
+    ops["gemm_fc_fwd_fp8"] = gemm_fp8_op(4 * C, C)
+    ops["gemm_fcproj_fwd_fp8"] = gemm_fp8_op(C, 4 * C)
+    ops["quantize_fp8"] = quantize_op()
     ops["gemm_fc_fwd_gelu"] = gemm_gelu_op()
     ops["gemm_fcproj_dx_gelu"] = gemm_gelu_bwd_op()
 
@@ -252,6 +276,9 @@ def main(argv=None):
         if kind == "flop":
             achieved = work / (us * 1e-6) / 1e12
             rec = {"op": name, "us": us, "tflops": achieved, "frac_of_bf16_peak": achieved / tc}
+        elif kind == "flop8":  # e4m3 dense peak: twice the bf16 one (the nominal ratio)
+            achieved = work / (us * 1e-6) / 1e12
+            rec = {"op": name, "us": us, "tflops": achieved, "frac_of_fp8_peak": achieved / (2 * tc)}
         else:
             achieved = work / (us * 1e-6) / 1e9
             rec = {"op": name, "us": us, "gbs": achieved, "frac_of_hbm": achieved / hbm}

@@ -464,3 +464,74 @@ def test_adamw(torch_cuda):
     # the bf16 copy is the round-to-nearest-even of the fp32 master, bit for bit
     master = th.cpu().numpy()
     assert np.array_equal(host(pbf), data.round_to_bf16(master).astype(np.float64))
+
+
+# ------------------------------------------------------------------ FP8 linear
+
+@pytest.mark.parametrize("n, std", [(8 * 1000 + 5, 1.0), (1 << 20, 0.02), (37, 3.0)])
+def test_quantize_fp8_bit_exact(torch_cuda, n, std):
+    """Per-tensor e4m3 codes and scales equal the oracle's bit for bit (the
+    scale and the scaled value are fp32 on both sides), ragged tails included."""
+    torch = torch_cuda
+    from oracle import fp8_ref as F
+    from step_gpt_train_gb300.gpt2 import gpt2_op_quantize_fp8
+    x = inputs(61, (n,), std)
+    x[::97] *= 40.0  # a heavy tail: most values land in subnormal and low-exponent codes
+    x = inputs_from_f32(x)
+    q = torch.full((n,), 0xAA, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(2, dtype=torch.float32, device="cuda")
+    gpt2_op_quantize_fp8(q, scales, dev(x))
+    torch.cuda.synchronize()
+    ref_q, ref_si = F.quantize_e4m3(x)
+    s = scales.cpu().numpy()
+    assert s[1] == ref_si and s[0] == np.float32(448.0) / np.float32(np.max(np.abs(x)))
+    got = q.cpu().numpy()
+    bad = np.nonzero(got != ref_q)[0]
+    assert bad.size == 0, (bad[:5], got[bad[:5]], ref_q[bad[:5]], x[bad[:5]])
+
+
+def inputs_from_f32(x):
+    from step_gpt_train_gb300 import data
+    return data.round_to_bf16(np.asarray(x, dtype=np.float32))
+
+
+FP8_CASES = [
+    # M, N, K, bias
+    (300, 200, 272, True),      # ragged M and N, K not a multiple of the 128-value k-block
+    (256, 256, 128, False),
+    (1024, 3072, 768, True),    # GPT-2 124M MLP up-projection shape (1024 rows)
+    (512, 768, 3072, True),     # MLP down-projection shape
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES)
+def test_matmul_fp8(torch_cuda, case):
+    """The FP8 product against the oracle on the same codes and scales: exact
+    products, fp32 accumulation (the tensor-core bound) and one bf16 rounding;
+    and, as a sanity bound, within a few percent of the unquantized product."""
+    torch = torch_cuda
+    from oracle import fp8_ref as F
+    from step_gpt_train_gb300.gpt2 import gpt2_op_matmul_fp8, gpt2_op_quantize_fp8
+    M, N, K, use_bias = case
+    A = inputs(71, (M, K), 1.0)
+    W = inputs(72, (N, K), 0.02)
+    bias = inputs(73, (N,), 0.1) if use_bias else None
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    qw = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sa = torch.zeros(2, dtype=torch.float32, device="cuda")
+    sw = torch.zeros(2, dtype=torch.float32, device="cuda")
+    gpt2_op_quantize_fp8(qa, sa, dev(A))
+    gpt2_op_quantize_fp8(qw, sw, dev(W))
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gpt2_op_matmul_fp8(D, qa, sa, qw, sw, bias=dev(bias) if use_bias else None)
+    torch.cuda.synchronize()
+    got = host(D)
+    assert np.all(np.isfinite(got))
+    ca, cw = qa.cpu().numpy(), qw.cpu().numpy()
+    si_a, si_w = sa.cpu().numpy()[1], sw.cpu().numpy()[1]
+    ref = F.matmul_fp8(ca, si_a, cw, si_w, bias)
+    # fp32 accumulation over K (one rounding per 32-deep step at most) plus the bf16 output rounding
+    atol = (K / 32) * 2.0 ** -23 * 4 * float(np.abs(ref).max()) * 2
+    assert_close(got, ref, BF16_REL, atol=atol, atol_frac=1e-3, what="fp8 matmul")
+    exact = A.astype(np.float64) @ W.astype(np.float64).T + (bias if use_bias else 0.0)
+    assert rel_l2(got, exact) < 0.08
