@@ -320,10 +320,6 @@ __global__ void f32_to_bf16_kernel(bf16* __restrict__ out, const float* __restri
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) out[i] = __float2bfloat16_rn(in[i]);
 }
-__global__ void bf16_to_f32_kernel(float* __restrict__ out, const bf16* __restrict__ in, int64_t n) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) out[i] = __bfloat162float(in[i]);
-}
 
 // ---- op accounting ----
 
