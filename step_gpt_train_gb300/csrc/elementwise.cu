@@ -170,7 +170,31 @@ template <typename T, int VPL>
 __device__ __forceinline__ void enc_sum_rows(float (&acc)[VPL][8], const T* dx0, const int32_t* spos, int lo, int hi,
                                              int C, int lane) {
     const int cv = C / 8;
-    for (int j = lo; j < hi; j++) {
+    // U rows in flight at a time, added in row order (the sums are those of
+    // one row at a time)
+    constexpr int U = VPL <= 3 ? 4 : 2;
+    int j = lo;
+    for (; j + U <= hi; j += U) {
+        float v[U][VPL][8];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const T* row = dx0 + (int64_t)spos[j + u] * C;
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int idx = lane + 32 * i;
+                if (idx < cv) load8(row + idx * 8, v[u][i]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++)
+#pragma unroll
+            for (int i = 0; i < VPL; i++)
+                if (lane + 32 * i < cv) {
+#pragma unroll
+                    for (int k = 0; k < 8; k++) acc[i][k] += v[u][i][k];
+                }
+    }
+    for (; j < hi; j++) {
         const T* row = dx0 + (int64_t)spos[j] * C;
 #pragma unroll
         for (int i = 0; i < VPL; i++) {
@@ -240,32 +264,64 @@ __global__ void __launch_bounds__(256) enc_piece_kernel(float* dwte, float* head
     }
 }
 
-// One warp per chunk whose last run starts inside it and continues: sums
-// tail[chunk] + head[chunk+1] + ... in chunk order, adds to dwte.
+// One block of ENC_COMBINE_WARPS warps per chunk whose last run starts inside
+// it and continues into later chunks (the other blocks return at once): the
+// run's total is tail[chunk] + head[chunk+1] + ... + head[last chunk of the
+// run]. Warp w sums the heads of the chunks chunk+1+w, chunk+1+w+W, ... in
+// increasing order, two loads in flight; the block then adds tail[chunk] and
+// the warps' partial sums in warp order and adds the total to dwte. The
+// order of the additions is fixed, so the result is deterministic.
+#define ENC_COMBINE_WARPS 4
 template <int VPL>
-__global__ void __launch_bounds__(256) enc_combine_kernel(float* dwte, const float* head, const float* tail,
-                                                          const uint32_t* skey, int n, int C) {
-    const int chunk = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
-    const int lane = threadIdx.x % 32;
+__global__ void __launch_bounds__(32 * ENC_COMBINE_WARPS) enc_combine_kernel(float* dwte, const float* head,
+                                                                              const float* tail,
+                                                                              const uint32_t* skey, int n, int C) {
+    __shared__ float part[ENC_COMBINE_WARPS - 1][2048];  // warps 1.. leave their sums here (C <= 2048)
+    const int chunk = blockIdx.x;
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int lo = chunk * ENC_CHUNK;
-    if (lo >= n) return;
     const int hi = min(n, lo + ENC_CHUNK);
     if (hi == n || skey[hi] != skey[hi - 1]) return;  // last run ends in this chunk
     int start = hi - 1;
     while (start > lo && skey[start - 1] == skey[hi - 1]) start--;
     if (!enc_is_head(skey, start)) return;  // run began in an earlier chunk
+    const uint32_t key = skey[hi - 1];
+    // the last chunk of the run: the first later chunk that does not run on into the next
+    int last = chunk + 1;
+    for (;; last++) {
+        const int chi = min(n, (last + 1) * ENC_CHUNK);
+        if (chi == n || skey[chi] != key || skey[chi - 1] != key) break;
+    }
     const int cv = C / 8;
     float acc[VPL][8];
 #pragma unroll
-    for (int i = 0; i < VPL; i++) {
-        int idx = lane + 32 * i;
-        if (idx < cv) load8(tail + (int64_t)chunk * C + idx * 8, acc[i]);
-    }
-    const uint32_t key = skey[hi - 1];
-    for (int c = chunk + 1;; c++) {
+    for (int i = 0; i < VPL; i++)
+#pragma unroll
+        for (int k = 0; k < 8; k++) acc[i][k] = 0.f;
+    int c = chunk + 1 + w;
+    for (; c + ENC_COMBINE_WARPS <= last; c += 2 * ENC_COMBINE_WARPS) {
+        float v0[VPL][8], v1[VPL][8];
 #pragma unroll
         for (int i = 0; i < VPL; i++) {
-            int idx = lane + 32 * i;
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                load8(head + (int64_t)c * C + idx * 8, v0[i]);
+                load8(head + (int64_t)(c + ENC_COMBINE_WARPS) * C + idx * 8, v1[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; i++)
+            if (lane + 32 * i < cv) {
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc[i][k] += v0[i][k];
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc[i][k] += v1[i][k];
+            }
+    }
+    if (c <= last) {
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
             if (idx < cv) {
                 float v[8];
                 load8(head + (int64_t)c * C + idx * 8, v);
@@ -273,10 +329,33 @@ __global__ void __launch_bounds__(256) enc_combine_kernel(float* dwte, const flo
                 for (int k = 0; k < 8; k++) acc[i][k] += v[k];
             }
         }
-        const int chi = min(n, (c + 1) * ENC_CHUNK);
-        if (chi == n || skey[chi] != key || skey[chi - 1] != key) break;
     }
-    enc_flush<VPL>(acc, dwte + (int64_t)key * C, true, C, lane);
+    if (w > 0) {
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv)
+#pragma unroll
+                for (int k = 0; k < 8; k++) part[w - 1][idx * 8 + k] = acc[i][k];
+        }
+    }
+    __syncthreads();
+    if (w == 0) {
+        float tot[VPL][8];
+#pragma unroll
+        for (int i = 0; i < VPL; i++) {
+            const int idx = lane + 32 * i;
+            if (idx < cv) {
+                load8(tail + (int64_t)chunk * C + idx * 8, tot[i]);
+#pragma unroll
+                for (int k = 0; k < 8; k++) tot[i][k] += acc[i][k];
+                for (int ww = 1; ww < ENC_COMBINE_WARPS; ww++)
+#pragma unroll
+                    for (int k = 0; k < 8; k++) tot[i][k] += part[ww - 1][idx * 8 + k];
+            }
+        }
+        enc_flush<VPL>(tot, dwte + (int64_t)key * C, true, C, lane);
+    }
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -294,7 +373,7 @@ static void enc_sum_launch(float* dwte, float* head, float* tail, const void* dx
     const int nchunk = (n + ENC_CHUNK - 1) / ENC_CHUNK;
     const int blocks = (nchunk * 32 + 255) / 256;
     enc_piece_kernel<T, VPL><<<blocks, 256, 0, s>>>(dwte, head, tail, (const T*)dx0, skey, spos, n, C);
-    enc_combine_kernel<VPL><<<blocks, 256, 0, s>>>(dwte, head, tail, skey, n, C);
+    enc_combine_kernel<VPL><<<nchunk, 32 * ENC_COMBINE_WARPS, 0, s>>>(dwte, head, tail, skey, n, C);
 }
 
 template <typename T>
