@@ -247,16 +247,33 @@ __global__ void __launch_bounds__(256) enc_piece_kernel(float* dwte, float* head
     for (int i = 0; i < VPL; i++)
 #pragma unroll
         for (int k = 0; k < 8; k++) acc[i][k] = 0.f;
+    const int cv = C / 8;
     int ps = lo;
     while (ps < hi) {
         int pe = ps + 1;
         while (pe < hi && skey[pe] == skey[ps]) pe++;
-        enc_sum_rows<T, VPL>(acc, dx0, spos, ps, pe, C, lane);
         const bool starts = enc_is_head(skey, ps);
         const bool ends = (pe == n) || skey[pe] != skey[ps];
-        if (starts && ends)
-            enc_flush<VPL>(acc, dwte + (int64_t)skey[ps] * C, true, C, lane);
-        else if (!starts)
+        if (starts && ends) {
+            // the dwte row is loaded first, so its latency overlaps the row sums
+            float* dst = dwte + (int64_t)skey[ps] * C;
+            float pre[VPL][8];
+#pragma unroll
+            for (int i = 0; i < VPL; i++)
+                if (lane + 32 * i < cv) load8(dst + (lane + 32 * i) * 8, pre[i]);
+            enc_sum_rows<T, VPL>(acc, dx0, spos, ps, pe, C, lane);
+#pragma unroll
+            for (int i = 0; i < VPL; i++)
+                if (lane + 32 * i < cv) {
+#pragma unroll
+                    for (int k = 0; k < 8; k++) acc[i][k] += pre[i][k];
+                }
+            enc_flush<VPL>(acc, dst, false, C, lane);
+            ps = pe;
+            continue;
+        }
+        enc_sum_rows<T, VPL>(acc, dx0, spos, ps, pe, C, lane);
+        if (!starts)
             enc_flush<VPL>(acc, head + (int64_t)chunk * C, false, C, lane);
         else
             enc_flush<VPL>(acc, tail + (int64_t)chunk * C, false, C, lane);
@@ -286,11 +303,19 @@ __global__ void __launch_bounds__(32 * ENC_COMBINE_WARPS) enc_combine_kernel(flo
     while (start > lo && skey[start - 1] == skey[hi - 1]) start--;
     if (!enc_is_head(skey, start)) return;  // run began in an earlier chunk
     const uint32_t key = skey[hi - 1];
-    // the last chunk of the run: the first later chunk that does not run on into the next
+    // the last chunk of the run: the first later chunk that does not run on
+    // into the next; each lane tests one chunk, 32 chunks per step
     int last = chunk + 1;
-    for (;; last++) {
-        const int chi = min(n, (last + 1) * ENC_CHUNK);
-        if (chi == n || skey[chi] != key || skey[chi - 1] != key) break;
+    for (;;) {
+        const int cc = last + lane;
+        const int chi = min(n, (cc + 1) * ENC_CHUNK);
+        const bool stop = chi == n || skey[chi] != key || skey[chi - 1] != key;
+        const unsigned m = __ballot_sync(0xffffffffu, stop);
+        if (m) {
+            last += __ffs(m) - 1;
+            break;
+        }
+        last += 32;
     }
     const int cv = C / 8;
     float acc[VPL][8];
