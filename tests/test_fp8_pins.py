@@ -69,3 +69,81 @@ def test_matmul_fp8_closed_form():
     d = F.matmul_fp8(a, 2.0, b, 0.25, bias=np.array([1.0, -1.0]))
     # (A B^T) = [[8.25, 3], [-3.875, -0.5]]; times 0.5; plus the bias
     assert np.array_equal(d, np.array([[5.125, 0.5], [-0.9375, -1.25]]))
+
+
+# ---------------------------------------------------------------- e5m2
+
+def test_e5m2_is_the_top_byte_of_binary16():
+    # e5m2 has binary16's sign and exponent fields and the top two bits of its
+    # mantissa, so code c is the half-precision number with bit pattern c << 8
+    codes = np.arange(256, dtype=np.uint16)
+    half = (codes << 8).astype(np.uint16).view(np.float16).astype(np.float64)
+    v = F.e5m2_decode(codes.astype(np.uint8))
+    assert np.array_equal(np.isnan(v), np.isnan(half))
+    fin = ~np.isnan(half)
+    assert np.array_equal(v[fin], half[fin])
+
+
+def test_e5m2_format_constants():
+    # OCP 8-bit floating point, E5M2: largest finite 57344 = 1.75 * 2^15,
+    # smallest normal 2^-14, smallest subnormal 2^-16, infinities and three
+    # NaN patterns per sign
+    v = F.e5m2_decode(np.arange(256, dtype=np.uint8))
+    assert v[0x7B] == 57344.0 and v[0xFB] == -57344.0
+    assert v[0x7C] == np.inf and v[0xFC] == -np.inf
+    assert v[0x04] == 2.0 ** -14 and v[0x03] == 3 * 2.0 ** -16 and v[0x01] == 2.0 ** -16
+    assert v[0x3C] == 1.0 and v[0x40] == 2.0 and v[0x38] == 0.5
+    assert int(np.isnan(v).sum()) == 6 and np.all(np.isnan(v[[0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]]))
+    assert np.all(np.diff(v[:0x7C]) > 0)
+
+
+def test_e5m2_round_trip_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    v = F.e5m2_decode(codes)
+    fin = np.isfinite(v)
+    assert np.array_equal(F.e5m2_encode(v[fin]), codes[fin])
+
+
+def test_e5m2_encode_matches_library_conversion():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e5m2"):
+        pytest.skip("no float8_e5m2 in this torch")
+    rng = np.random.default_rng(11)
+    # inside the finite range (the library conversion does not saturate beyond it)
+    x = np.concatenate([rng.uniform(-57000, 57000, 50000), rng.normal(0, 1.0, 50000),
+                        rng.normal(0, 1e-4, 20000), rng.normal(0, 1e-6, 20000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(F.e5m2_encode(x), ref)
+
+
+def test_e5m2_ties_saturation_nan():
+    enc = lambda a: int(F.e5m2_encode(np.float32(a)))
+    assert enc(1.125) == 0x3C and enc(1.375) == 0x3E  # midpoints go to the even code
+    assert enc(0.5 * 2.0 ** -16) == 0x00 and enc(1.5 * 2.0 ** -16) == 0x02  # subnormal ties
+    assert enc(57344.0) == 0x7B and enc(61439.0) == 0x7B and enc(1e30) == 0x7B
+    assert enc(np.inf) == 0x7B and enc(-np.inf) == 0xFB  # saturation, not infinity
+    assert enc(np.nan) == 0x7F and enc(-1e-30) == 0x80
+
+
+def test_quantize_e5m2_per_tensor_scaling():
+    rng = np.random.default_rng(5)
+    x = (rng.normal(0, 1e-3, (48, 80)) * np.where(rng.random((48, 80)) < 0.02, 1e3, 1.0)).astype(np.float32)
+    codes, scale_inv = F.quantize_e5m2(x)
+    i = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert codes[i] in (0x7B, 0xFB)  # the largest magnitude maps to +-57344
+    assert scale_inv == np.float32(np.max(np.abs(x))) / np.float32(57344.0)
+    back = F.e5m2_decode(codes) * float(scale_inv)
+    normal = np.abs(x) * (57344.0 / np.max(np.abs(x))) >= 2.0 ** -14
+    # within half a unit in the last place: 2^-3 relative for normals
+    assert np.all(np.abs(back - x)[normal] <= 2.0 ** -3 * np.abs(x)[normal] * (1 + 1e-6))
+
+
+def test_matmul_fp8_mixed_formats_closed_form():
+    # A = [[1, -3], [0.25, 6]] in e5m2 with scale 4; B = [[0.5, 2], [1.75, -1]] in e4m3 with scale 1/8
+    a = F.e5m2_encode(np.array([[1.0, -3.0], [0.25, 6.0]]))
+    b = F.e4m3_encode(np.array([[0.5, 2.0], [1.75, -1.0]]))
+    d = F.matmul_fp8(a, 4.0, b, 0.125, a_fmt="e5m2", b_fmt="e4m3")
+    # (A B^T) = [[-5.5, 4.75], [12.125, -5.5625]]; times 0.5
+    assert np.array_equal(d, np.array([[-2.75, 2.375], [6.0625, -2.78125]]))
+    # the same codes read in the other format give other values: the format is not ignored
+    assert not np.array_equal(F.matmul_fp8(a, 4.0, b, 0.125, a_fmt="e4m3", b_fmt="e4m3"), d)
