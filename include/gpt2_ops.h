@@ -113,27 +113,36 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
 
 /* FP8 linear layer (the modded-nanogpt project page, "NanoGPT (124M) in 90
  * seconds", "How it works": FP8 for the MLP, the QKV projections and the
- * head), with per-tensor scaling to e4m3 (1 sign, 4 exponent bits with bias 7,
- * 3 mantissa bits, largest finite value 448).
+ * head), with per-tensor scaling to one of two 8-bit floating-point formats
+ * (OCP 8-bit floating point):
+ *   GPT2_FP8_E4M3  1 sign, 4 exponent bits (bias 7), 3 mantissa bits, largest
+ *                  finite value fmax = 448 (weights and activations);
+ *   GPT2_FP8_E5M2  1 sign, 5 exponent bits (bias 15), 2 mantissa bits,
+ *                  largest finite value fmax = 57344 (gradients).
  *
- * gpt2_op_quantize_fp8: q[i] = e4m3(x[i] * scales[0]) for n bf16 values x,
- * with scales[0] = 448 / amax and scales[1] = amax / 448 written on the
- * device (both 1 when amax = max |x| is 0); the product is rounded to fp32,
- * then to the nearest e4m3 value (ties to even), saturating at +-448; a NaN
- * stays NaN and does not enter amax. q: n bytes (8-byte aligned), x 16-byte
- * aligned, scales: 2 floats; scratch: gpt2_op_quantize_fp8_scratch() bytes.
+ * gpt2_op_quantize_fp8: q[i] = fp8(x[i] * scales[0]) for n bf16 values x in
+ * the given format, with scales[0] = fmax / amax and scales[1] = amax / fmax
+ * written on the device (both 1 when amax = max |x| is 0); the product is
+ * rounded to fp32, then to the nearest value of the format (ties to even),
+ * saturating at +-fmax; a NaN stays NaN and does not enter amax. q: n bytes
+ * (8-byte aligned), x 16-byte aligned, scales: 2 floats; scratch:
+ * gpt2_op_quantize_fp8_scratch() bytes. An unknown format is GPT2_ERR_ARG.
  *
  * gpt2_op_matmul_fp8: D[M,N] (bf16, overwritten) = (A B^T)[m,n] *
  * a_scales[1] * b_scales[1] (+ bias[n], bf16, optional), A [M,K] and B [N,K]
- * e4m3 codes row-major (B is the [out, in] weight), the scale arrays as
+ * FP8 codes row-major (B is the [out, in] weight), each in its own format
+ * (an e5m2 gradient times an e4m3 weight, for instance), the scale arrays as
  * written by gpt2_op_quantize_fp8 (read on the device). tcgen05 tensor cores
  * (kind::f8f6f4, TMA-fed, fp32 accumulation in tensor memory). Needs K % 16
- * == 0 and N % 8 == 0, 16-byte aligned A, B, D and bias. */
+ * == 0 and N % 8 == 0, 16-byte aligned A, B, D and bias; an unknown format is
+ * GPT2_ERR_ARG. */
+#define GPT2_FP8_E4M3 0
+#define GPT2_FP8_E5M2 1
 size_t gpt2_op_quantize_fp8_scratch(void);
-int gpt2_op_quantize_fp8(void* q, float* scales, const void* x, int64_t n, void* scratch, size_t scratch_bytes,
-                         void* stream);
-int gpt2_op_matmul_fp8(void* D, const void* A, const float* a_scales, const void* B, const float* b_scales,
-                       const void* bias, int M, int N, int K, int* d_status, void* stream);
+int gpt2_op_quantize_fp8(void* q, float* scales, const void* x, int64_t n, int format, void* scratch,
+                         size_t scratch_bytes, void* stream);
+int gpt2_op_matmul_fp8(void* D, const void* A, int a_format, const float* a_scales, const void* B, int b_format,
+                       const float* b_scales, const void* bias, int M, int N, int K, int* d_status, void* stream);
 
 /* Linear forward with the GELU after it fused into the GEMM epilogue (the
  * MLP's first linear, "matmul_forward", followed by "gelu_forward" in the

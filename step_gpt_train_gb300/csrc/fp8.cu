@@ -1,14 +1,17 @@
-// Per-tensor e4m3 quantization for the FP8 linear layer (the modded-nanogpt
+// Per-tensor FP8 quantization for the FP8 linear layer (the modded-nanogpt
 // project page, "NanoGPT (124M) in 90 seconds", "How it works": FP8 for the
-// MLP, the QKV projections and the head). Three launches:
+// MLP, the QKV projections and the head), to e4m3 (largest finite value 448,
+// for weights and activations) or e5m2 (largest finite value 57344, the wider
+// range for gradients), both as in the OCP 8-bit floating point format.
+// Three launches:
 //   amax_partial_kernel  each of FP8_BLOCKS blocks takes the largest |x| of a
 //                        fixed contiguous range (a maximum does not depend on
 //                        the order, so the result is exact);
-//   amax_scale_kernel    one block: amax, scale = 448 / amax, 1 / scale as
-//                        amax / 448 (both 1 when amax is 0);
-//   quantize_e4m3_kernel q = e4m3(x * scale), the product rounded to fp32 and
+//   amax_scale_kernel    one block: amax, scale = fmax / amax, 1 / scale as
+//                        amax / fmax (both 1 when amax is 0);
+//   quantize_fp8_kernel  q = fp8(x * scale), the product rounded to fp32 and
 //                        converted with round-to-nearest-even and saturation
-//                        at +-448 (cvt.rn.satfinite), 8 values per thread.
+//                        at +-fmax (cvt.rn.satfinite), 8 values per thread.
 // NaN inputs do not enter amax (fmaxf ignores them) and quantize to NaN.
 #include "common.cuh"
 #include "launch.h"
@@ -46,7 +49,7 @@ __global__ void __launch_bounds__(256) amax_partial_kernel(float* __restrict__ p
 }
 
 __global__ void __launch_bounds__(FP8_BLOCKS) amax_scale_kernel(float* __restrict__ scales,
-                                                                const float* __restrict__ partial) {
+                                                                const float* __restrict__ partial, float fmax) {
     __shared__ float sh[32];
     float m = partial[threadIdx.x];
 #pragma unroll
@@ -56,20 +59,25 @@ __global__ void __launch_bounds__(FP8_BLOCKS) amax_scale_kernel(float* __restric
     if (threadIdx.x == 0) {
         float t = 0.f;
         for (int w = 0; w < FP8_BLOCKS / 32; w++) t = fmaxf(t, sh[w]);
-        scales[0] = t > 0.f ? 448.f / t : 1.f;
-        scales[1] = t > 0.f ? t / 448.f : 1.f;
+        scales[0] = t > 0.f ? fmax / t : 1.f;
+        scales[1] = t > 0.f ? t / fmax : 1.f;
     }
 }
 
-// Two fp32 values to two e4m3 codes, lo in the low byte.
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+// Two fp32 values to two codes of format FMT (0: e4m3, 1: e5m2), lo in the low byte.
+template <int FMT>
+__device__ __forceinline__ uint16_t fp8x2(float lo, float hi) {
     uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    if constexpr (FMT == 0)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-__global__ void __launch_bounds__(256) quantize_e4m3_kernel(uint8_t* __restrict__ q, const bf16* __restrict__ x,
-                                                            int64_t n, const float* __restrict__ scales) {
+template <int FMT>
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(uint8_t* __restrict__ q, const bf16* __restrict__ x,
+                                                           int64_t n, const float* __restrict__ scales) {
     const float s = scales[0];
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= n) return;
@@ -77,11 +85,11 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(uint8_t* __restrict_
         float v[8];
         load8(x + i, v);
         uint2 w;
-        w.x = (uint32_t)e4m3x2(v[0] * s, v[1] * s) | ((uint32_t)e4m3x2(v[2] * s, v[3] * s) << 16);
-        w.y = (uint32_t)e4m3x2(v[4] * s, v[5] * s) | ((uint32_t)e4m3x2(v[6] * s, v[7] * s) << 16);
+        w.x = (uint32_t)fp8x2<FMT>(v[0] * s, v[1] * s) | ((uint32_t)fp8x2<FMT>(v[2] * s, v[3] * s) << 16);
+        w.y = (uint32_t)fp8x2<FMT>(v[4] * s, v[5] * s) | ((uint32_t)fp8x2<FMT>(v[6] * s, v[7] * s) << 16);
         *reinterpret_cast<uint2*>(q + i) = w;
     } else {
-        for (int64_t k = i; k < n; k++) q[k] = (uint8_t)(e4m3x2(__bfloat162float(x[k]) * s, 0.f) & 0xFF);
+        for (int64_t k = i; k < n; k++) q[k] = (uint8_t)(fp8x2<FMT>(__bfloat162float(x[k]) * s, 0.f) & 0xFF);
     }
 }
 
@@ -89,11 +97,15 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(uint8_t* __restrict_
 
 size_t fp8_quantize_scratch() { return FP8_BLOCKS * 4; }
 
-int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, float* partial, cudaStream_t s) {
+int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, int fmt, float* partial,
+                        cudaStream_t s) {
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return GPT2_ERR_ARG;
     if (n <= 0) return 0;
     amax_partial_kernel<<<FP8_BLOCKS, 256, 0, s>>>(partial, x, n);
-    amax_scale_kernel<<<1, FP8_BLOCKS, 0, s>>>(scales, partial);
+    amax_scale_kernel<<<1, FP8_BLOCKS, 0, s>>>(scales, partial, fmt == FP8_E4M3 ? 448.f : 57344.f);
     const int64_t threads = (n + 7) / 8;
-    quantize_e4m3_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(q, x, n, scales);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    if (fmt == FP8_E4M3) quantize_fp8_kernel<FP8_E4M3><<<blocks, 256, 0, s>>>(q, x, n, scales);
+    else quantize_fp8_kernel<FP8_E5M2><<<blocks, 256, 0, s>>>(q, x, n, scales);
     return 3;
 }

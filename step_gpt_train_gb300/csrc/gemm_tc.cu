@@ -77,8 +77,9 @@ struct GemmArgs {
     int n_tiles;         // ceil(N / BN)
     int units;           // m_tiles * n_tiles * splits
     int num_kb;          // ceil(K / k-block width): 64 bf16 or 128 e4m3 values (128 bytes either way)
-    const float* a_scale;  // e4m3 operands: device scalars by which the codes of A and of B are
+    const float* a_scale;  // FP8 operands: device scalars by which the codes of A and of B are
     const float* b_scale;  // multiplied back (the product scales the accumulator)
+    int a_fmt, b_fmt;      // FP8 operands: their formats (0 e4m3, 1 e5m2)
 };
 
 // One unit of a CTA's work: k-blocks [kb0, kb1) of a tile; z = partial slot.
@@ -174,14 +175,15 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
 
 // ---------------------------------------------------------------- kernel
 
-// F8: e4m3 operands (K-major only): a k-block is 128 values, four K = 32 MMAs
-// of kind::f8f6f4, and the epilogue scales the accumulator by a_scale * b_scale.
+// F8: FP8 operands, e4m3 or e5m2 each (K-major only): a k-block is 128 values,
+// four K = 32 MMAs of kind::f8f6f4, and the epilogue scales the accumulator by
+// a_scale * b_scale.
 template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const GemmArgs g) {
-    static_assert(!F8 || (!A_MN && !B_MN && EPI == EPI_NONE), "e4m3 operands: K-major, plain epilogue");
+    static_assert(!F8 || (!A_MN && !B_MN && EPI == EPI_NONE), "FP8 operands: K-major, plain epilogue");
     constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // whole warp runs the schedule (warp-uniform operands), one elected
             // lane issues the MMAs and commits
             const bool leader = elect_one();
-            constexpr uint32_t idesc = F8 ? make_idesc_f8(BM, BN) : make_idesc(BM, BN, A_MN, B_MN);
+            const uint32_t idesc = F8 ? make_idesc_f8(BM, BN, g.a_fmt, g.b_fmt) : make_idesc(BM, BN, A_MN, B_MN);
             constexpr uint32_t a_kstep = A_MN ? 16 * 128 : 32;  // bytes per 16-wide k step
             constexpr uint32_t b_kstep = B_MN ? 16 * 128 : 32;
             constexpr uint32_t a_lbo = A_MN ? 64 * 128 : 16;
@@ -635,6 +637,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     if (!ok) return GPT2_ERR_CUDA;
     GemmArgs g;
     g.a_scale = g.b_scale = nullptr;
+    g.a_fmt = g.b_fmt = 0;
     g.bias = partials ? nullptr : bias;
     g.aux = aux;
     g.status = status;
@@ -665,9 +668,10 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
 
 }  // namespace
 
-int launch_matmul_fp8(bf16* D, const uint8_t* A, const float* a_scale, const uint8_t* B, const float* b_scale,
-                      const bf16* bias, int M, int N, int K, int* status, cudaStream_t s) {
+int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale, const uint8_t* B, int b_fmt,
+                      const float* b_scale, const bf16* bias, int M, int N, int K, int* status, cudaStream_t s) {
     if (!D || !A || !B || !a_scale || !b_scale || M < 1 || N < 1 || K < 1) return GPT2_ERR_ARG;
+    if ((a_fmt != FP8_E4M3 && a_fmt != FP8_E5M2) || (b_fmt != FP8_E4M3 && b_fmt != FP8_E5M2)) return GPT2_ERR_ARG;
     if (K % 16 != 0 || N % 8 != 0) return GPT2_ERR_ARG;  // 16-byte row strides of A, B and D
     Plan p = make_plan(M, N, K, 0);  // tile width and grid as for bf16; one k-range per tile
     p.num_kb = (K + 127) / 128;
@@ -695,6 +699,8 @@ int launch_matmul_fp8(bf16* D, const uint8_t* A, const float* a_scale, const uin
     g.num_kb = p.num_kb;
     g.a_scale = a_scale;
     g.b_scale = b_scale;
+    g.a_fmt = a_fmt;
+    g.b_fmt = b_fmt;
     if (p.bn == 128) launch_tc<128, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
     else if (p.bn == 192) launch_tc<192, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
     else launch_tc<256, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);

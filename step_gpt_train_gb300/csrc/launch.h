@@ -92,15 +92,17 @@ int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n
 // out = a * b elementwise; n % 8 == 0.
 int launch_mul(int dtype, void* out, const void* a, const void* b, int64_t n, cudaStream_t s);
 
+// FP8 formats (OCP 8-bit floating point): e4m3 (largest finite 448), e5m2 (57344).
+enum { FP8_E4M3 = 0, FP8_E5M2 = 1 };
 // D (bf16 [M,N]) = (A B^T) * (*a_scale) * (*b_scale) (+ bias) on the tensor cores, A [M,K] and B
-// [N,K] e4m3 codes (K-major), fp32 accumulation; K % 16 == 0, N % 8 == 0.
-int launch_matmul_fp8(bf16* D, const uint8_t* A, const float* a_scale, const uint8_t* B, const float* b_scale,
-                      const bf16* bias, int M, int N, int K, int* status, cudaStream_t s);
-// Per-tensor e4m3 quantization of n bf16 values: scales[0] = 448 / amax and
-// scales[1] = amax / 448 (1 and 1 when amax is 0), q = e4m3(x * scales[0]),
-// round to nearest even, saturated; partial: fp8_quantize_scratch() bytes.
+// [N,K] FP8 codes (K-major) in formats a_fmt and b_fmt, fp32 accumulation; K % 16 == 0, N % 8 == 0.
+int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale, const uint8_t* B, int b_fmt,
+                      const float* b_scale, const bf16* bias, int M, int N, int K, int* status, cudaStream_t s);
+// Per-tensor FP8 quantization of n bf16 values to format fmt (largest finite value fmax):
+// scales[0] = fmax / amax and scales[1] = amax / fmax (1 and 1 when amax is 0),
+// q = fp8(x * scales[0]), round to nearest even, saturated; partial: fp8_quantize_scratch() bytes.
 size_t fp8_quantize_scratch();
-int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, float* partial, cudaStream_t s);
+int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, int fmt, float* partial, cudaStream_t s);
 
 // Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
 // accumulate (fp32 D only): D += the product instead of D = it; the scratch

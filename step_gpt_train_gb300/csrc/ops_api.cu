@@ -111,23 +111,27 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
 
 size_t gpt2_op_quantize_fp8_scratch(void) { return fp8_quantize_scratch(); }
 
-int gpt2_op_quantize_fp8(void* q, float* scales, const void* x, int64_t n, void* scratch, size_t scratch_bytes,
-                         void* stream) {
-    if (!q || !scales || !x || n < 0) return GPT2_ERR_ARG;
+static bool fp8_format_ok(int f) { return f == GPT2_FP8_E4M3 || f == GPT2_FP8_E5M2; }
+static_assert(GPT2_FP8_E4M3 == FP8_E4M3 && GPT2_FP8_E5M2 == FP8_E5M2, "FP8 format codes");
+
+int gpt2_op_quantize_fp8(void* q, float* scales, const void* x, int64_t n, int format, void* scratch,
+                         size_t scratch_bytes, void* stream) {
+    if (!q || !scales || !x || n < 0 || !fp8_format_ok(format)) return GPT2_ERR_ARG;
     if (((uintptr_t)q % 8) || !al16(x)) return GPT2_ERR_ARG;
     if (n == 0) return GPT2_OK;
     if (!scratch || scratch_bytes < fp8_quantize_scratch()) return GPT2_ERR_WORKSPACE;
-    return finish(launch_quantize_fp8((uint8_t*)q, scales, (const bf16*)x, n, (float*)scratch, st(stream)));
+    return finish(launch_quantize_fp8((uint8_t*)q, scales, (const bf16*)x, n, format, (float*)scratch, st(stream)));
 }
 
-int gpt2_op_matmul_fp8(void* D, const void* A, const float* a_scales, const void* B, const float* b_scales,
-                       const void* bias, int M, int N, int K, int* d_status, void* stream) {
+int gpt2_op_matmul_fp8(void* D, const void* A, int a_format, const float* a_scales, const void* B, int b_format,
+                       const float* b_scales, const void* bias, int M, int N, int K, int* d_status, void* stream) {
     if (!D || !A || !B || !a_scales || !b_scales || M < 0 || N < 0 || K < 1) return GPT2_ERR_ARG;
+    if (!fp8_format_ok(a_format) || !fp8_format_ok(b_format)) return GPT2_ERR_ARG;
     if (K % 16 || N % 8) return GPT2_ERR_ARG;
     if (!al16(D) || !al16(A) || !al16(B) || (bias && !al16(bias))) return GPT2_ERR_ARG;
     if ((int64_t)M * N == 0) return GPT2_OK;
-    return finish(launch_matmul_fp8((bf16*)D, (const uint8_t*)A, a_scales + 1, (const uint8_t*)B, b_scales + 1,
-                                    (const bf16*)bias, M, N, K, d_status, st(stream)));
+    return finish(launch_matmul_fp8((bf16*)D, (const uint8_t*)A, a_format, a_scales + 1, (const uint8_t*)B, b_format,
+                                    b_scales + 1, (const bf16*)bias, M, N, K, d_status, st(stream)));
 }
 
 int gpt2_op_matmul_gelu(int dtype, void* dgelu, void* out, const void* A, const void* W, const void* bias, int M,

@@ -106,7 +106,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
-// D(tmem) (+)= A(smem) * B(smem), kind::f8f6f4 (here e4m3 operands), fp32
+// D(tmem) (+)= A(smem) * B(smem), kind::f8f6f4 (e4m3 or e5m2 operands), fp32
 // accumulate; one instruction is K = 32 (32 bytes of each row).
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -266,15 +266,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// Instruction descriptor, kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), the
+// formats of A and B in bits 7-9 and 10-12 (0 = e4m3, 1 = e5m2), both K-major,
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, int a_fmt, int b_fmt) {
+    return (1u << 4) | ((uint32_t)(a_fmt & 7) << 7) | ((uint32_t)(b_fmt & 7) << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
 // bf16 (bits 7-9 and 10-12 = 1), A/B major-ness (bits 15, 16: 1 = MN-major),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0 in
-// bits 7-9 and 10-12), fp32 accumulator, both K-major.
-__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

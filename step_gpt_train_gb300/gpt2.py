@@ -25,6 +25,7 @@ STATUS_NAMES = {
 }
 
 TENSOR_PARAM, TENSOR_MASTER, TENSOR_GRAD, TENSOR_ADAM_M, TENSOR_ADAM_V = range(5)
+FP8_E4M3, FP8_E5M2 = 0, 1  # the FP8 formats of gpt2_op_quantize_fp8 / gpt2_op_matmul_fp8
 
 FAMILIES = ["encoder_forward", "layernorm_forward", "matmul", "attention_forward", "residual_forward",
             "gelu_forward", "classifier", "loss_mean", "layernorm_backward", "gelu_backward",
@@ -103,9 +104,9 @@ _SIGNATURES = {
     "gpt2_op_matmul_gelu": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                     c_void_p, c_void_p]),
     "gpt2_op_quantize_fp8_scratch": (c_size_t, []),
-    "gpt2_op_quantize_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_size_t, c_void_p]),
-    "gpt2_op_matmul_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
-                                   c_void_p, c_void_p]),
+    "gpt2_op_quantize_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_void_p, c_size_t, c_void_p]),
+    "gpt2_op_matmul_fp8": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                   c_int, c_int, c_void_p, c_void_p]),
     "gpt2_op_matmul_gelu_backward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                              c_void_p, c_void_p]),
     "gpt2_op_attention_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
@@ -436,20 +437,24 @@ def gpt2_lr_cosine(t: int, warmup: int, total: int, lr_max: float, lr_min: float
     return float(load_library().gpt2_lr_cosine(int(t), int(warmup), int(total), float(lr_max), float(lr_min)))
 
 
-def gpt2_op_quantize_fp8(q, scales, x, stream=None):
-    """q (uint8 [n]) = e4m3 codes of x (bf16) scaled per tensor; scales (float32 [2]) = 448/amax, amax/448."""
+def gpt2_op_quantize_fp8(q, scales, x, fmt=FP8_E4M3, stream=None):
+    """q (uint8 [n]) = FP8 codes (format fmt) of x (bf16) scaled per tensor;
+    scales (float32 [2]) = fmax/amax, amax/fmax (fmax 448 for e4m3, 57344 for e5m2)."""
     lib = load_library()
     sc = _scratch(lib.gpt2_op_quantize_fp8_scratch())
-    check(lib.gpt2_op_quantize_fp8(_p(q), _p(scales), _p(x), x.numel(), _p(sc), sc.numel(), _s(stream)),
+    check(lib.gpt2_op_quantize_fp8(_p(q), _p(scales), _p(x), x.numel(), int(fmt), _p(sc), sc.numel(), _s(stream)),
           "gpt2_op_quantize_fp8")
 
 
-def gpt2_op_matmul_fp8(D, A, a_scales, B, b_scales, bias=None, status=None, stream=None):
-    """D (bf16 [M,N]) = (A B^T) a_scales[1] b_scales[1] (+ bias); A [M,K], B [N,K] e4m3 codes (uint8)."""
+def gpt2_op_matmul_fp8(D, A, a_scales, B, b_scales, bias=None, a_fmt=FP8_E4M3, b_fmt=FP8_E4M3, status=None,
+                       stream=None):
+    """D (bf16 [M,N]) = (A B^T) a_scales[1] b_scales[1] (+ bias); A [M,K], B [N,K] FP8 codes (uint8) in
+    formats a_fmt and b_fmt."""
     M, K = A.shape
     N = B.shape[0]
-    check(load_library().gpt2_op_matmul_fp8(_p(D), _p(A), _p(a_scales), _p(B), _p(b_scales), _p(bias), M, N, K,
-                                            _p(status), _s(stream)), "gpt2_op_matmul_fp8")
+    check(load_library().gpt2_op_matmul_fp8(_p(D), _p(A), int(a_fmt), _p(a_scales), _p(B), int(b_fmt),
+                                            _p(b_scales), _p(bias), M, N, K, _p(status), _s(stream)),
+          "gpt2_op_matmul_fp8")
 
 
 def gpt2_op_matmul_gelu(dgelu, out, A, W, bias=None, status=None, stream=None):

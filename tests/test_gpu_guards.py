@@ -63,7 +63,7 @@ def test_guards_matmul(torch_cuda):
 
 def test_guards_fp8(torch_cuda):
     torch = torch_cuda
-    from step_gpt_train_gb300.gpt2 import gpt2_op_matmul_fp8, gpt2_op_quantize_fp8
+    from step_gpt_train_gb300.gpt2 import FP8_E5M2, gpt2_op_matmul_fp8, gpt2_op_quantize_fp8
     M, N, K = 300, 200, 272
     qa, qw = Guarded(torch, (M, K), torch.uint8), Guarded(torch, (N, K), torch.uint8)
     sa, sw = Guarded(torch, (2,), torch.float32), Guarded(torch, (2,), torch.float32)
@@ -73,8 +73,13 @@ def test_guards_fp8(torch_cuda):
     gpt2_op_matmul_fp8(D.t, qa.t, sa.t, qw.t, sw.t, bias=dev(inputs(8, (N,))))
     q_odd = Guarded(torch, (8 * 1001 + 3,), torch.uint8)  # the scalar tail of the quantizer
     gpt2_op_quantize_fp8(q_odd.t, sa.t, dev(inputs(9, (8 * 1001 + 3,))))
+    # e5m2: the other quantizer instantiation, and an e5m2 x e4m3 product
+    qg, sg = Guarded(torch, (M, K), torch.uint8), Guarded(torch, (2,), torch.float32)
+    gpt2_op_quantize_fp8(qg.t, sg.t, dev(inputs(22, (M, K))), FP8_E5M2)
+    D2 = Guarded(torch, (M, N), torch.bfloat16)
+    gpt2_op_matmul_fp8(D2.t, qg.t, sg.t, qw.t, sw.t, a_fmt=FP8_E5M2)
     torch.cuda.synchronize()
-    assert all(x.intact() for x in (qa, qw, sa, sw, D, q_odd))
+    assert all(x.intact() for x in (qa, qw, sa, sw, D, q_odd, qg, sg, D2))
 
 
 def test_guards_layernorm(torch_cuda):

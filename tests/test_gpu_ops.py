@@ -468,23 +468,28 @@ def test_adamw(torch_cuda):
 
 # ------------------------------------------------------------------ FP8 linear
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("n, std", [(8 * 1000 + 5, 1.0), (1 << 20, 0.02), (37, 3.0)])
-def test_quantize_fp8_bit_exact(torch_cuda, n, std):
-    """Per-tensor e4m3 codes and scales equal the oracle's bit for bit (the
-    scale and the scaled value are fp32 on both sides), ragged tails included."""
+def test_quantize_fp8_bit_exact(torch_cuda, n, std, fmt):
+    """Per-tensor FP8 codes and scales equal the oracle's bit for bit (the
+    scale and the scaled value are fp32 on both sides), ragged tails included,
+    in both formats."""
     torch = torch_cuda
     from oracle import fp8_ref as F
-    from step_gpt_train_gb300.gpt2 import gpt2_op_quantize_fp8
+    from step_gpt_train_gb300.gpt2 import FP8_E4M3, FP8_E5M2, gpt2_op_quantize_fp8
     x = inputs(61, (n,), std)
     x[::97] *= 40.0  # a heavy tail: most values land in subnormal and low-exponent codes
+    if fmt == "e5m2":
+        x[::1013] *= 1e4  # a wider range still: e5m2 spans 2^-16 .. 57344
     x = inputs_from_f32(x)
     q = torch.full((n,), 0xAA, dtype=torch.uint8, device="cuda")
     scales = torch.zeros(2, dtype=torch.float32, device="cuda")
-    gpt2_op_quantize_fp8(q, scales, dev(x))
+    gpt2_op_quantize_fp8(q, scales, dev(x), FP8_E4M3 if fmt == "e4m3" else FP8_E5M2)
     torch.cuda.synchronize()
-    ref_q, ref_si = F.quantize_e4m3(x)
+    ref_q, ref_si = F.quantize(x, fmt)
+    fmax = np.float32(F.FORMATS[fmt][3])
     s = scales.cpu().numpy()
-    assert s[1] == ref_si and s[0] == np.float32(448.0) / np.float32(np.max(np.abs(x)))
+    assert s[1] == ref_si and s[0] == fmax / np.float32(np.max(np.abs(x)))
     got = q.cpu().numpy()
     bad = np.nonzero(got != ref_q)[0]
     assert bad.size == 0, (bad[:5], got[bad[:5]], ref_q[bad[:5]], x[bad[:5]])
@@ -496,11 +501,15 @@ def inputs_from_f32(x):
 
 
 FP8_CASES = [
-    # M, N, K, bias
-    (300, 200, 272, True),      # ragged M and N, K not a multiple of the 128-value k-block
-    (256, 256, 128, False),
-    (1024, 3072, 768, True),    # GPT-2 124M MLP up-projection shape (1024 rows)
-    (512, 768, 3072, True),     # MLP down-projection shape
+    # M, N, K, bias, A format, B format
+    (300, 200, 272, True, "e4m3", "e4m3"),      # ragged M and N, K not a multiple of the 128-value k-block
+    (256, 256, 128, False, "e4m3", "e4m3"),
+    (1024, 3072, 768, True, "e4m3", "e4m3"),    # GPT-2 124M MLP up-projection shape (1024 rows)
+    (512, 768, 3072, True, "e4m3", "e4m3"),     # MLP down-projection shape
+    (300, 200, 272, False, "e5m2", "e4m3"),     # an e5m2 gradient times an e4m3 weight, ragged
+    (1024, 3072, 768, False, "e5m2", "e4m3"),   # input gradient of the MLP down-projection: dY [rows, C], W^T [4C, C]
+    (256, 392, 400, True, "e4m3", "e5m2"),
+    (512, 768, 1024, False, "e5m2", "e5m2"),
 ]
 
 
@@ -508,30 +517,58 @@ FP8_CASES = [
 def test_matmul_fp8(torch_cuda, case):
     """The FP8 product against the oracle on the same codes and scales: exact
     products, fp32 accumulation (the tensor-core bound) and one bf16 rounding;
-    and, as a sanity bound, within a few percent of the unquantized product."""
+    and, as a sanity bound, close to the unquantized product (a few percent
+    for e4m3's 3 mantissa bits, more for e5m2's 2)."""
     torch = torch_cuda
     from oracle import fp8_ref as F
-    from step_gpt_train_gb300.gpt2 import gpt2_op_matmul_fp8, gpt2_op_quantize_fp8
-    M, N, K, use_bias = case
+    from step_gpt_train_gb300.gpt2 import FP8_E4M3, FP8_E5M2, gpt2_op_matmul_fp8, gpt2_op_quantize_fp8
+    M, N, K, use_bias, fa, fb = case
+    code = {"e4m3": FP8_E4M3, "e5m2": FP8_E5M2}
     A = inputs(71, (M, K), 1.0)
+    if fa == "e5m2":
+        A[:, ::31] *= 300.0  # gradient-like: a few columns far larger than the rest
     W = inputs(72, (N, K), 0.02)
     bias = inputs(73, (N,), 0.1) if use_bias else None
     qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
     qw = torch.empty((N, K), dtype=torch.uint8, device="cuda")
     sa = torch.zeros(2, dtype=torch.float32, device="cuda")
     sw = torch.zeros(2, dtype=torch.float32, device="cuda")
-    gpt2_op_quantize_fp8(qa, sa, dev(A))
-    gpt2_op_quantize_fp8(qw, sw, dev(W))
+    gpt2_op_quantize_fp8(qa, sa, dev(A), code[fa])
+    gpt2_op_quantize_fp8(qw, sw, dev(W), code[fb])
     D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    gpt2_op_matmul_fp8(D, qa, sa, qw, sw, bias=dev(bias) if use_bias else None)
+    gpt2_op_matmul_fp8(D, qa, sa, qw, sw, bias=dev(bias) if use_bias else None, a_fmt=code[fa], b_fmt=code[fb])
     torch.cuda.synchronize()
     got = host(D)
     assert np.all(np.isfinite(got))
     ca, cw = qa.cpu().numpy(), qw.cpu().numpy()
     si_a, si_w = sa.cpu().numpy()[1], sw.cpu().numpy()[1]
-    ref = F.matmul_fp8(ca, si_a, cw, si_w, bias)
+    ref = F.matmul_fp8(ca, si_a, cw, si_w, bias, a_fmt=fa, b_fmt=fb)
     # fp32 accumulation over K (one rounding per 32-deep step at most) plus the bf16 output rounding
     atol = (K / 32) * 2.0 ** -23 * 4 * float(np.abs(ref).max()) * 2
     assert_close(got, ref, BF16_REL, atol=atol, atol_frac=1e-3, what="fp8 matmul")
     exact = A.astype(np.float64) @ W.astype(np.float64).T + (bias if use_bias else 0.0)
-    assert rel_l2(got, exact) < 0.08
+    assert rel_l2(got, exact) < (0.08 if fa == fb == "e4m3" else 0.15)
+    if fa != fb:
+        # the formats are honoured: the same codes read as the other pair of formats give another
+        # product (where it is finite: e4m3's top codes are infinities and NaNs in e5m2)
+        with np.errstate(invalid="ignore", over="ignore"):
+            other = F.matmul_fp8(ca, si_a, cw, si_w, bias, a_fmt=fb, b_fmt=fa)
+        fin = np.isfinite(other)
+        assert fin.mean() > 0.5 and rel_l2(got[fin], other[fin]) > 0.1
+
+
+def test_fp8_format_checked(torch_cuda):
+    """An unknown FP8 format is an argument error, reported before any launch."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import GPT2Error, gpt2_op_matmul_fp8, gpt2_op_quantize_fp8
+    q = torch.empty(64, dtype=torch.uint8, device="cuda")
+    sc = torch.ones(2, dtype=torch.float32, device="cuda")
+    x = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(GPT2Error):
+        gpt2_op_quantize_fp8(q, sc, x, 2)
+    D = torch.empty((16, 16), dtype=torch.bfloat16, device="cuda")
+    A = torch.zeros((16, 32), dtype=torch.uint8, device="cuda")
+    with pytest.raises(GPT2Error):
+        gpt2_op_matmul_fp8(D, A, sc, A, sc, a_fmt=7)
+    with pytest.raises(GPT2Error):
+        gpt2_op_matmul_fp8(D, A, sc, A, sc, b_fmt=-1)
