@@ -75,49 +75,108 @@ def workload_label(name: str, w: dict, B: int, T: int) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clock and throttle samples while the timed region runs."""
+    """nvidia-smi clock and throttle samples, kept only where they fall inside
+    the timed region. Each sample carries the time nvidia-smi took it (its
+    timestamp field, local time); mark_start() / mark_stop() record the
+    region's bounds on the host clock, and a sample counts when its timestamp
+    lies between them (its arrival time when the timestamp does not parse).
+    wait_first() returns once the first sample has arrived, so that the
+    sampler's start-up does not eat into a short region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 100
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, cmd: list[str] | None = None):
+        import threading
         self.proc = None
-        self.gpu = gpu_index
+        self.lines: list[tuple[float, str]] = []  # (arrival time, line)
+        self.t_start = self.t_stop = None  # (monotonic, wall clock) pairs
+        self._first = threading.Event()
+        if cmd is None:
+            cmd = ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", str(self.INTERVAL_MS)]
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line))
+            self._first.set()
+
+    def wait_first(self, timeout: float = 2.0) -> bool:
+        return self.proc is not None and self._first.wait(timeout)
+
+    @staticmethod
+    def _now():
+        import datetime
+        return time.monotonic(), datetime.datetime.now()
+
+    def mark_start(self):
+        self.t_start = self._now()
+
+    def mark_stop(self):
+        self.t_stop = self._now()
+
+    @staticmethod
+    def _stamp(field: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(field.strip(), "%Y/%m/%d %H:%M:%S.%f")
+        except ValueError:
+            return None
 
     def stop(self):
         if not self.proc:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            self.proc.wait()
+        self._reader.join(timeout=5)
+        inside, after = [], []
+        for arrival, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            ts = self._stamp(parts[0])
+            k = 1 if ts is not None else 0  # bound index: wall clock, else arrival time
+            t = ts if ts is not None else arrival
+            lo = self.t_start[k] if self.t_start else None
+            hi = self.t_stop[k] if self.t_stop else None
+            if (lo is None or t >= lo) and (hi is None or t <= hi):
+                inside.append(parts)
+            elif hi is not None and t > hi:
+                after.append(parts)
+        note = None
+        if not inside and after:  # a region shorter than the interval: the first sample after it
+            inside, note = after[:1], "no sample inside the timed region; the first one after it"
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+        for parts in inside:
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if note:
+            out["note"] = note
+        return out
 
 
 def gemm_traffic_from_profile():
@@ -194,7 +253,7 @@ def run_reference(args, rank: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="124m-b32")
@@ -252,14 +311,18 @@ def main():
     barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
+    sampler.wait_first()
+    barrier()
     launches0 = model.launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
     ev0.record(stream)
     losses = []
     for s in range(W, W + K):
         losses.append(step(s, d_tok[s], d_tgt[s]))
     ev1.record(stream)
     torch.cuda.synchronize()
+    sampler.mark_stop()
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
