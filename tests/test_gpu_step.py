@@ -229,6 +229,35 @@ def test_124m_b32_bench_config_sampled(torch_cuda):
         assert err.max() < 5e-2 and err.mean() < 1e-2, (b, err.max(), err.mean())
 
 
+def test_124m_b32_graph_step_equals_separate_calls(torch_cuda):
+    """The benchmarked launch configuration: gpt2_step at 124M, B=32, T=1024
+    (Zipf ids with EoS), three steps as bench.py runs them (the first eager,
+    the second captured into the step graph, the third replayed), against
+    gpt2_forward / gpt2_backward / gpt2_adamw_step bit for bit: every loss and
+    every master weight. With the sampled oracle parity of the separate calls
+    above, this carries parity over to the graph the bench times."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import TENSOR_MASTER
+    w = data.WORKLOADS["124m-b32"]
+    cfg = {k: w[k] for k in ("n_layer", "n_embd", "n_head", "vocab", "vocab_padded", "max_T", "mode")}
+    cfg["max_B"] = 32
+    tok, tgt = data.workload_batches("124m-b32", 3)
+    sep, graph = make_model(cfg), make_model(cfg)
+    for s in range(3):
+        lr = lr_at(s + 1, 5)
+        tt, gg = torch.from_numpy(tok[s]).cuda(), torch.from_numpy(tgt[s]).cuda()
+        la = sep.forward(tt, gg)
+        sep.backward()
+        sep.adamw_step(lr, t=s + 1, **HP)
+        lb = graph.step(tt, gg, lr, t=s + 1, **HP)
+        assert la == lb, (s, la, lb)
+    a, b = sep.tensors(TENSOR_MASTER), graph.tensors(TENSOR_MASTER)
+    sep.close()
+    graph.close()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
 @pytest.mark.parametrize("name", ["350m-b16", "1p5b-b8"])
 def test_large_models_b1_parity(torch_cuda, name):
     """350M and 1.5B shapes at B=1, T=1024: one full step against the fp32 oracle."""
