@@ -156,7 +156,10 @@ typedef struct {
 } gpt2_adamw_config;
 int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* cfg);
 
-/* One whole training step, replayed as a CUDA graph: tokens and targets
+/* One whole training step (the step above: llm.c "State of the Union",
+ * "Single GPU training"), replayed as a CUDA graph (the modded-nanogpt
+ * project page, "How it works", lists CUDA-graph capture among its systems
+ * techniques): tokens and targets
  * (device, int32 [B,T]) are copied into the library's own buffers, then the
  * forward to the mean loss, the backward, the global-norm clip when
  * cfg->max_grad_norm > 0 and AdamW run as one captured graph; the loss comes
