@@ -95,7 +95,10 @@ int gpt2_workspace_bytes(const gpt2_config* cfg, size_t* bytes_out);
 int gpt2_init(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, void* d_workspace,
               size_t workspace_bytes, void* cuda_stream);
 
-/* Forward pass on tokens [B, T] (device int32, row-major). With targets
+/* Forward pass on tokens [B, T] (device int32, row-major): the forward rows
+ * of llm.c's kernel table ("State of the Union", "Runtime, DRAM traffic,
+ * instructions": encoder_forward, layernorm_forward, the matmuls, attention,
+ * gelu_forward, residual_forward, fused_classifier). With targets
  * (device int32 [B, T]) it also runs the fused classifier: per-position
  * loss at the label index, dlogits written in place over the logits, and
  * writes the mean loss over the B*T positions to *loss_out (host float) after
@@ -107,13 +110,17 @@ int gpt2_init(gpt2_t** out, const gpt2_config* cfg, uint64_t seed, void* d_works
 int gpt2_forward(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T,
                  float* loss_out);
 
-/* Backward pass of the last forward (which must have had targets).
+/* Backward pass of the last forward (which must have had targets): the
+ * backward rows of the same kernel table (matmul and bias backward,
+ * gelu_backward, layernorm_backward, attention backward,
+ * encoder_backward).
  * Overwrites every parameter gradient, or adds to them after
  * gpt2_set_grad_accumulation(m, 1). */
 int gpt2_backward(gpt2_t* m);
 
 /* One AdamW step on every parameter tensor from the last backward's
- * gradients: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+ * gradients (the kernel table's adamw row; "Single GPU training": the
+ * parameter master copy kept in fp32): m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
  * theta -= lr (m/(1-b1^t) / (sqrt(v/(1-b2^t)) + eps) + weight_decay theta),
  * then the bf16 copy is refreshed (bf16 mode). t >= 1 is the 1-based step.
  * Weight decay applies to every tensor. */
