@@ -179,18 +179,56 @@ class ClockSampler:
         return out
 
 
+GEMM_SOURCES = ("gemm_tc.cu", "tc_common.cuh", "common.cuh")  # the matmul kernel and the headers it includes
+
+
+def strip_code(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to one
+    space; string and character literals are kept as written."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif text[i] in "\"'":
+            q, j = text[i], i + 1
+            while j < n and text[j] != q:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def gemm_code_digest() -> str:
+    """sha256 (first 16 hex digits) of the matmul kernel's code: its source and
+    the headers it includes, comments and whitespace aside, so that a change
+    of a comment does not invalidate a measurement of the same code."""
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "step_gpt_train_gb300", "csrc", name)) as f:
+            h.update(strip_code(f.read()).encode())
+        h.update(b"\0")
+    return h.hexdigest()[:16]
+
+
 def gemm_traffic_from_profile():
     """DRAM bytes per matmul launch from the committed ncu summary, if it was taken
-    on the current matmul source; else None."""
+    on the current matmul code; else None."""
     path = os.path.join(ROOT, "profiles", "gemm_tc_kernel_124m_b32.txt")
-    src = os.path.join(ROOT, "step_gpt_train_gb300", "csrc", "gemm_tc.cu")
     try:
         text = open(path).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = gemm_code_digest()
     except OSError:
         return None
     fields = dict(l.split(":", 1) for l in text.splitlines() if ":" in l)
-    if fields.get("source_sha256_16", "").strip() != digest:
+    if fields.get("code_sha256_16", "").strip() != digest:
         return None
     try:
         return float(fields["traffic_bytes_per_launch_full_step_avg"].strip())

@@ -9,10 +9,12 @@
 // Structure: a persistent kernel, one CTA per SM, 10 warps.
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
 //               into a ring of shared-memory stages, completion on mbarriers.
-//   warp 1      allocates TMEM (two BN-column fp32 accumulators) and one
-//               thread issues tcgen05.mma (M=128, N=BN, K=16) from shared-
-//               memory descriptors; tcgen05.commit frees each stage and
-//               signals a finished accumulator.
+//   warp 1      allocates TMEM (two BN-column fp32 accumulators) and runs
+//               the MMA schedule warp-uniformly: one elected lane issues
+//               tcgen05.mma (M=128, N=BN, K=16; kind::f8f6f4 with K=32 for
+//               FP8 operands) from shared-memory descriptors, and
+//               tcgen05.commit frees each stage and signals a finished
+//               accumulator.
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4)..+31 = tile rows; two warps per lane quarter,
 //               each owning half of the tile's columns), + bias (each warp

@@ -96,3 +96,26 @@ def test_without_timestamps_arrival_time_decides():
     time.sleep(0.2)
     out = s.stop()
     assert out is not None and 5 <= out["samples"] <= 30
+
+
+def test_strip_code_drops_comments_only():
+    src = ('int a = 1; // a comment\n/* a block\n comment */ const char* s = "x // y /* z */";\n'
+           "char q = '\\''; asm(\"mov.b32 %0, %1;\" : \"=r\"(a));\n")
+    out = bench.strip_code(src)
+    assert "comment" not in out
+    assert '"x // y /* z */"' in out and "'\\''" in out and '"mov.b32 %0, %1;"' in out
+    # a changed comment or re-indented code leaves the digest input unchanged; a changed token does not
+    assert bench.strip_code(src.replace("a comment", "another note").replace("int a", "int   a")) == out
+    assert bench.strip_code(src.replace("int a = 1", "int a = 2")) != out
+
+
+def test_gemm_traffic_is_read_only_for_the_captured_code():
+    # the committed summary carries the digest of the code it measured; the
+    # bench reports its traffic only while the digest matches the sources
+    text = open(os.path.join(ROOT, "profiles", "gemm_tc_kernel_124m_b32.txt")).read()
+    fields = dict(l.split(":", 1) for l in text.splitlines() if ":" in l)
+    got = bench.gemm_traffic_from_profile()
+    if fields["code_sha256_16"].strip() == bench.gemm_code_digest():
+        assert got == float(fields["traffic_bytes_per_launch_full_step_avg"])
+    else:
+        assert got is None
