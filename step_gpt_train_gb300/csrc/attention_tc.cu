@@ -8,17 +8,18 @@
 //                         hand the S buffer back, and form
 //                         P = exp2(S log2(e)/sqrt(hd) - m) with a per-row
 //                         reference m, accumulating the row sum l;
-//                         P goes to shared memory as bf16 in the MMA's
-//                         K-major 128-byte swizzled layout;
-//   O += P V_j            tcgen05.mma M=128 N=64 K=128, into a TMEM accumulator.
+//                         P goes back to TMEM as bf16 pairs (tcgen05.st);
+//   O += P V_j            tcgen05.mma M=128 N=64 K=128 with P read from TMEM
+//                         as the A operand, into a TMEM accumulator.
 // The reference m moves only when a row's maximum grows by more than 8 (log2
 // units), so P <= 256; when it moves, the row's O (in TMEM) and l are scaled
 // by exp2(m_old - m_new) before the next PV MMA. Finally O / l and the
 // log-sum-exp m + log l are written.
 //
-// Warps: 0 TMA producer (Q once; K per block into a two-stage ring, V into
-// one buffer), 1 TMEM allocation and MMA issue (one thread; it issues S for
-// block j+1 before PV for block j), 2..5 softmax. Every wait is bounded.
+// Warps: 0 TMA producer (Q once; K and V per block, each into a two-stage
+// ring, so that K(j+1) never waits for PV(j-1)), 1 TMEM allocation and the
+// MMA schedule (run by the whole warp, one elected lane issuing; S for block
+// j+1 is issued before PV for block j), 2..5 softmax. Every wait is bounded.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"

@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(256) encoder_bwd_wpe_kernel(float* __restrict_
 // sort (8-bit digits, ids < 65536); then each token's rows are summed in
 // ascending position order, split into 32-entry chunks of the sorted list so
 // that a very frequent id is summed by many warps, and the chunk pieces of a
-// long run are combined in chunk order. Every token row of dwte has exactly
-// one writer, so the result is deterministic.
+// long run are combined in a fixed order (enc_combine_kernel). Every token
+// row of dwte has exactly one writer, so the result is deterministic.
 
 #define ENC_TILE 1024  // sorted elements per block in the radix passes
 #define ENC_CHUNK 32   // sorted entries per warp in the summation
