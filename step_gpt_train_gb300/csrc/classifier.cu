@@ -1,9 +1,16 @@
 // Fused softmax cross-entropy classifier and the mean-loss reduction.
 //
-// One block per row of logits. The row is read from HBM once into registers
-// (raw 16-byte vectors), reduced to (max, sum of exp) over the real vocabulary
-// columns, and the gradient is written back in place over the logits. The
-// normalised probabilities are never stored. Columns V..Vp-1 (padding) get 0.
+// Each row of logits is read from HBM once, reduced to (max, sum of exp)
+// over the real vocabulary columns, and the gradient is written back in place
+// over the logits. The normalised probabilities are never stored. Columns
+// V..Vp-1 (padding) get 0. Two forms:
+//   classifier_stream_kernel  bf16 rows wider than 4096 (the GPT-2 step): a
+//                             persistent kernel, two CTAs per SM, each row
+//                             copied whole into shared memory by one bulk
+//                             copy and processed from there;
+//   classifier_kernel         fp32 rows and narrow bf16 rows: one block per
+//                             row, the row held in registers (raw 16-byte
+//                             vectors).
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
