@@ -5,7 +5,10 @@
 // [May 3, 2024]" ("Runtime, DRAM traffic, instructions"): per step one
 // encoder forward, 2L+1 layernorm forwards, 4 matmuls per layer plus the LM
 // head, L attention forwards, 2L residuals, L GELUs, the fused classifier;
-// then the mirrored backward and one AdamW over every parameter.
+// then the mirrored backward and one AdamW over every parameter. Around it:
+// gradient accumulation, the global gradient norm and clipping, the decay
+// mask, gpt2_step (the whole step captured once and replayed as a CUDA
+// graph) and the sharded (ZeRO-1 style) AdamW over ranges of the flat layout.
 #include "common.cuh"
 #include "launch.h"
 
