@@ -236,6 +236,22 @@ def gemm_traffic_from_profile():
         return None
 
 
+def oracle_threads() -> int:
+    """Threads the oracle's numpy BLAS runs on: threadpoolctl's report where it
+    is installed, else the cores this process may run on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(w_name: str):
     """The oracle, as it stands, on one bounded sample of the workload."""
     from oracle import gpt2_ref as R
@@ -249,7 +265,7 @@ def cpu_baseline(w_name: str):
     R.train_step(cfg, params, tok[0], tgt[0], None, lr_at(1), HP["beta1"], HP["beta2"], HP["eps"],
                  HP["weight_decay"], 1)
     dt = time.perf_counter() - t0
-    return {"value": T / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": T / dt, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
             "sample": f"one oracle train step (forward, backward, AdamW over all parameters), float64 numpy, "
                       f"GPT-2 {w_name.split('-')[0].upper()} shape, B=1, T={T}, first window of the same "
                       f"token stream; init excluded; {dt:.1f} s"}
@@ -282,7 +298,7 @@ def run_reference(args, rank: int):
             "warmup": args.warmup, "ms_per_step": 1000 * total / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": workload_label(args.config, w, B, T), "sample_per_step": f"B={B}, T={T}"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

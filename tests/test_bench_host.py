@@ -119,3 +119,40 @@ def test_gemm_traffic_is_read_only_for_the_captured_code():
         assert got == float(fields["traffic_bytes_per_launch_full_step_avg"])
     else:
         assert got is None
+
+
+def run_bench(args, env_extra=None):
+    import json
+    import subprocess
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                       timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    # the oracle arm needs no GPU: the tiny workload keeps it to seconds
+    (line,) = run_bench(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "3", "--ref-T", "64"])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["vs_baseline"] is None and "workload" in line["config"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert abs(line["ms_per_step"] - 64 * 1000.0 / line["value"]) < 1e-6 * line["ms_per_step"]
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    assert run_bench(["--impl", "reference", "--config", "tiny", "--steps", "1", "--ref-T", "8", "--gpus", "2"],
+                     {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_warmup_floor_is_three():
+    (line,) = run_bench(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0", "--ref-T", "8"])
+    assert line["warmup"] == 3
