@@ -199,7 +199,9 @@ int gpt2_op_residual_forward(int dtype, void* out, const void* a, const void* b,
                              void* stream);
 
 /* Residual backward: the gradient reaching a residual join from the
- * branch is added to the stream gradient, dres += dbranch, n % 8 == 0. */
+ * branch is added to the stream gradient, dres += dbranch, n % 8 == 0.
+ * llm.c's kernel table has no row of its own for it (the step folds it into
+ * the LayerNorm backward, gpt2_op_layernorm_backward_residual). */
 int gpt2_op_residual_backward(int dtype, void* dres, const void* dbranch, int64_t n,
                               void* stream);
 
@@ -209,8 +211,10 @@ size_t gpt2_op_bias_backward_scratch(int N, int C);
 int gpt2_op_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch,
                           size_t scratch_bytes, void* stream);
 
-/* Bias gradient without caller scratch. The paper has no counterpart to
- * this entry point: it serves callers that cannot allocate or lend device
+/* Bias gradient without caller scratch: the reduction of
+ * "matmul_backward_bias" in llm.c's kernel table ("State of the Union",
+ * "Runtime, DRAM traffic, instructions"), whose code has no entry point of
+ * this form. It serves callers that cannot allocate or lend device
  * memory (for example a program whose device memory is wholly owned by
  * another runtime's allocator or a fixed pool, or code that must not call
  * cudaMalloc because it can synchronise the device). It computes exactly
@@ -242,7 +246,9 @@ int gpt2_op_bias_backward_noalloc(int dtype, float* dbias, const void* dy, int N
 int gpt2_op_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N,
                        int V, int Vp, float dloss, int* d_status, void* stream);
 
-/* Mean of losses [N] into *out (device fp32): fixed-order tree, deterministic. */
+/* Mean of losses [N] into *out (device fp32): fixed-order tree, deterministic.
+ * The mean loss of the forward with targets (llm.c "State of the Union",
+ * "Single GPU training"). */
 int gpt2_op_mean_loss(float* out, const float* losses, int N, void* stream);
 
 /* AdamW ("adamw_kernel"): over n fp32 elements, m = b1 m + (1-b1) g;
