@@ -94,17 +94,20 @@ def main(argv=None):
             return lambda: g.gpt2_op_matmul_gelu_backward(du, dY, W, u, stream=torch.cuda.current_stream())
         return setup, 2.0 * N * 4 * C * C, "flop"
 
-    def gemm_fp8_op(Nn, K):  # e4m3 linear forward (codes quantized once; the GEMM is timed)
+    def gemm_fp8_op(Nn, K, a_fmt=g.FP8_E4M3, use_bias=True):
+        # FP8 linear layer (codes quantized once; the GEMM is timed): A [N, K] in a_fmt
+        # (e4m3 activations, or an e5m2 gradient for an input gradient), W [Nn, K] e4m3
         def setup():
             A, W, b = rnd(N, K), rnd(Nn, K, std=0.02), rnd(Nn)
             qa = torch.empty(N, K, device=dev, dtype=torch.uint8)
             qw = torch.empty(Nn, K, device=dev, dtype=torch.uint8)
             sa = torch.empty(2, device=dev, dtype=torch.float32)
             sw = torch.empty(2, device=dev, dtype=torch.float32)
-            g.gpt2_op_quantize_fp8(qa, sa, A)
+            g.gpt2_op_quantize_fp8(qa, sa, A, a_fmt)
             g.gpt2_op_quantize_fp8(qw, sw, W)
             D = torch.empty(N, Nn, device=dev, dtype=bf)
-            return lambda: g.gpt2_op_matmul_fp8(D, qa, sa, qw, sw, bias=b, stream=torch.cuda.current_stream())
+            return lambda: g.gpt2_op_matmul_fp8(D, qa, sa, qw, sw, bias=b if use_bias else None, a_fmt=a_fmt,
+                                                stream=torch.cuda.current_stream())
         return setup, 2.0 * N * Nn * K, "flop8"
 
     def quantize_op():  # per-tensor e4m3 quantization of the MLP's hidden activations
@@ -117,6 +120,8 @@ def main(argv=None):
 
     ops["gemm_fc_fwd_fp8"] = gemm_fp8_op(4 * C, C)
     ops["gemm_fcproj_fwd_fp8"] = gemm_fp8_op(C, 4 * C)
+    # input gradient of the MLP down-projection: dY [N, C] (e5m2) times W^T stored [4C, C] (e4m3)
+    ops["gemm_fcproj_dx_fp8_e5m2"] = gemm_fp8_op(4 * C, C, a_fmt=g.FP8_E5M2, use_bias=False)
     ops["quantize_fp8"] = quantize_op()
     ops["gemm_fc_fwd_gelu"] = gemm_gelu_op()
     ops["gemm_fcproj_dx_gelu"] = gemm_gelu_bwd_op()
