@@ -54,3 +54,15 @@ def test_library_needs_no_driver_library():
     out = subprocess.run(["readelf", "-d", path], capture_output=True, text=True).stdout
     needed = [l for l in out.splitlines() if "(NEEDED)" in l]
     assert needed and not any("libcuda" in l or "libcudart" in l for l in needed), needed
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback: without the built library every entry point of the binding raises
+    import pytest
+    from step_gpt_train_gb300 import gpt2 as g
+    monkeypatch.setattr(g, "_lib", None)
+    monkeypatch.setattr(g._build, "LIB", str(tmp_path / "absent" / "libgpt2.so"))
+    with pytest.raises(ImportError):
+        g.load_library()
+    with pytest.raises(ImportError):
+        g.gpt2_lr_cosine(1, 1, 10, 1e-3, 0.0)
