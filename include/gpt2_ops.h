@@ -105,6 +105,7 @@ int gpt2_op_layernorm_backward_residual(int dtype, void* dres, int accumulate, f
  * d_fp32 else dtype, overwritten. bf16: tcgen05 tensor cores (TMA-fed,
  * fp32 accumulate in tensor memory); fp32: fp32 FMA. Needs K % 8 == 0 and
  * N % 8 == 0 (and M % 8 == 0 when a_mn_major); 16-byte aligned buffers.
+ * K >= 1 (K = 0 is GPT2_ERR_ARG); M = 0 or N = 0 launches nothing.
  * Scratch holds split-K partial sums (fp32 D only). */
 size_t gpt2_op_matmul_scratch(int dtype, int M, int N, int K, int d_fp32);
 int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major, const void* B,

@@ -35,7 +35,11 @@ int gpt2_op_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx
     if (!dt_ok(dtype) || !dwte || !dwpe || !dx0 || !tokens || B < 0 || T < 0 || C <= 0 || C % 8 || Vp < 1 ||
         Vp > 65536)
         return GPT2_ERR_ARG;
-    if ((int64_t)B * T == 0) return GPT2_OK;
+    if ((int64_t)B * T == 0) {
+        // no rows: dwte gains nothing; dwpe[0, T) is the empty sum (zero) when only B is 0
+        if (T > 0 && cudaMemsetAsync(dwpe, 0, (size_t)T * C * 4, st(stream)) != cudaSuccess) return GPT2_ERR_CUDA;
+        return GPT2_OK;
+    }
     if (!scratch || scratch_bytes < encoder_backward_scratch(B, T, C)) return GPT2_ERR_WORKSPACE;
     if (!al16(dwte) || !al16(dwpe) || !al16(dx0)) return GPT2_ERR_ARG;
     return finish(launch_encoder_backward(dtype, dwte, dwpe, dx0, tokens, B, T, C, scratch, st(stream)));
