@@ -1,9 +1,13 @@
-"""Zero sizes: every op of gpt2_ops.h called with an empty input.
+"""Degenerate sizes: every op of gpt2_ops.h called with an empty input, and
+attention over a single position.
 
 Collected last on purpose (like the other test_zz file), so that a run that
 stops at the first failure has already run every other test.
 """
+import numpy as np
 import pytest
+
+from tests._gpu_util import assert_close, dev, host, inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -77,3 +81,34 @@ def test_empty_inputs(torch_cuda):
     assert bool((dbias == 0).all()) and bool((dgamma == 0).all()) and bool((dbeta == 0).all())
     assert bool((dwpe[:8 * C] == 0).all()) and bool((dwpe[8 * C:] == 7.0).all())  # rows t >= T untouched
     assert bool((dwte == 7.0).all())  # accumulated into: an empty batch adds nothing
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+def test_attention_single_position(torch_cuda, mode):
+    """T = 1: the one query sees only its own key, so P = 1 and, in closed
+    form, o = v, lse = q.k / sqrt(hd), dV = dO, and dS = P (dP - D) = 0 because
+    D = dO.o = dO.v = dP, so dQ = dK = 0 up to the rounding of dP and D."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_attention_backward, gpt2_op_attention_forward
+    B, T, H = 3, 1, 2
+    hd = 64 if mode == 1 else 16
+    C = H * hd
+    qkv = inputs(52, (B, T, 3 * C), 1.0, mode)
+    dout = inputs(53, (B, T, C), 1.0, mode)
+    dq = dev(qkv, mode)
+    o = torch.full((B, T, C), float("nan"), dtype=dq.dtype, device="cuda")
+    lse = torch.full((B, H, T), float("nan"), device="cuda")
+    gpt2_op_attention_forward(o, lse, dq, B, T, H)
+    dqkv = torch.full_like(dq, float("nan"))
+    gpt2_op_attention_backward(dqkv, dev(dout, mode), dq, o, lse, B, T, H)
+    torch.cuda.synchronize()
+    q, k, v = (qkv[..., i * C:(i + 1) * C].astype(np.float64) for i in range(3))
+    tol = 2.0 ** -8 if mode == 1 else 1e-6
+    assert_close(host(o), v, tol, atol=1e-30, what="o = v")
+    qk = (q.reshape(B, H, hd) * k.reshape(B, H, hd)).sum(-1) / np.sqrt(hd)
+    assert_close(host(lse).reshape(B, H), qk, 1e-5, atol=1e-4, what="lse = q.k/sqrt(hd)")
+    g = host(dqkv)
+    assert_close(g[..., 2 * C:], dout.astype(np.float64), tol, atol=1e-30, what="dV = dO")
+    assert np.all(np.isfinite(g))
+    small = 1e-3 if mode == 1 else 1e-4
+    assert np.abs(g[..., :2 * C]).max() < small, np.abs(g[..., :2 * C]).max()  # dQ, dK
