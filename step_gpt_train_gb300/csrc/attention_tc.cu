@@ -326,11 +326,12 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
                                 cudaStream_t s) {
     CUtensorMap map;
     if (!make_qkv_map(&map, qkv, B, T, C)) return GPT2_ERR_CUDA;
-    static bool configured = false;
-    if (!configured) {
+    // once per process; a function-local static is initialised thread-safely
+    static const bool configured = [] {
         cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
-        configured = true;
-    }
+        return true;
+    }();
+    (void)configured;
     FwdArgs a;
     a.o = o;
     a.lse = lse;
@@ -1176,12 +1177,13 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     CUtensorMap mq, mo, md;  // md: the same view of dqkv, for the TMA stores of dQ, dK, dV
     if (!make_qkv_map(&mq, qkv, B, T, C) || !make_do_map(&mo, dout, B, T, C) || !make_qkv_map(&md, dqkv, B, T, C))
         return GPT2_ERR_CUDA;
-    static bool configured = false;
-    if (!configured) {
+    // once per process; a function-local static is initialised thread-safely
+    static const bool configured = [] {
         cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DKDV_SMEM);
         cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
-        configured = true;
-    }
+        return true;
+    }();
+    (void)configured;
     BwdArgs a;
     a.dqkv = dqkv;
     a.lse = lse;
