@@ -201,6 +201,58 @@ def test_124m_b8_parity(torch_cuda):
     print(f"124M B8: loss {losses[0]:.5f} vs {ref[0][0]:.5f}; worst grad rel L2 {worst:.3e}")
 
 
+def oracle_step_in_shards(cfg, params, tokens, targets, lr, t, shards, dtype):
+    """One oracle step of the whole batch with its gradient formed shard by shard:
+    the gradient of the mean loss over B equal-sized shards is the mean of the
+    shards' mean-loss gradients (the data-parallel identity the two-rank gloo
+    test pins), so the oracle's peak memory is that of one shard. The AdamW
+    update then runs on the averaged gradient, as in R.train_step."""
+    c = rcfg(cfg)
+    B = tokens.shape[0]
+    assert B % shards == 0
+    n = B // shards
+    loss, grads = 0.0, None
+    for i in range(shards):
+        sl = slice(i * n, (i + 1) * n)
+        l_i, cache = R.forward(c, params, tokens[sl], targets[sl], dtype=dtype)
+        g_i = R.backward(c, cache)
+        del cache
+        loss += l_i / shards
+        if grads is None:
+            grads = {k: v.astype(np.float64) / shards for k, v in g_i.items()}
+        else:
+            for k in grads:
+                grads[k] += g_i[k] / shards
+    new_params = {}
+    for name, theta in params.items():
+        theta = np.asarray(theta, dtype=np.float64)
+        z = np.zeros_like(theta)
+        new_params[name], _, _ = R.adamw_update(theta, grads[name], z, z, lr, HP["beta1"], HP["beta2"], HP["eps"],
+                                                HP["weight_decay"], t)
+    return loss, grads, new_params
+
+
+def test_124m_b32_parity(torch_cuda):
+    """The benchmarked workload (GPT-2 124M, bf16, B=32, T=1024, Zipf(1.1) ids with
+    EoS): one full step (loss, every parameter gradient, the updated masters)
+    against the fp32 oracle, at the acceptance tolerances. At B=32 the split-K
+    choice of the weight gradients (K = 32768), the attention schedules and the
+    encoder backward's sort differ from B=8."""
+    torch = torch_cuda
+    w = data.WORKLOADS["124m-b32"]
+    cfg = {k: w[k] for k in ("n_layer", "n_embd", "n_head", "vocab", "vocab_padded", "max_T", "mode")}
+    cfg["max_B"] = 32
+    tok, tgt = data.workload_batches("124m-b32", 1)
+    assert (tok == data.GPT2_EOS).any()
+    model = make_model(cfg)
+    losses, grads, masters = run_steps(torch, model, tok, tgt, 1, warmup=5)
+    model.close()
+    params = R.init_params(rcfg(cfg), 1234)
+    ref = oracle_step_in_shards(cfg, params, tok[0], tgt[0], lr_at(1, 5), 1, 4, np.float32)
+    worst = check_step(cfg, losses[0], grads[0], masters[0], ref, 2e-2, 3e-2, 1e-3)
+    print(f"124M B32: loss {losses[0]:.5f} vs {ref[0]:.5f}; worst grad rel L2 {worst:.3e}")
+
+
 def test_124m_b32_bench_config_sampled(torch_cuda):
     """The benchmarked workload (124M, B=32, T=1024, Zipf + EoS): per-position losses of
     sampled sequences against the oracle's forward on those sequences alone."""
