@@ -236,6 +236,27 @@ def gemm_traffic_from_profile():
         return None
 
 
+# Families bound by HBM bandwidth; the library counts their algorithmic
+# bytes (each tensor read or written once) as their work.
+HBM_FAMILIES = ("encoder_forward", "layernorm_forward", "classifier", "loss_mean", "layernorm_backward",
+                "bias_backward", "encoder_backward", "adamw", "residual_forward", "residual_backward",
+                "gelu_forward", "gelu_backward")
+
+
+def hbm_fractions(fam_ms: dict, stats: dict, steps: int, peaks: dict) -> dict:
+    """Per HBM-bound family: algorithmic GB per step, CUDA-event ms per step,
+    GB/s and the fraction of the measured copy bandwidth."""
+    peak = peaks.get("hbm_gbs") or 6800.0
+    out = {"peak_gbs": peak, "peak_source": "measured (MEASURED_PEAKS.json)" if peaks.get("hbm_gbs") else "fallback"}
+    for f in HBM_FAMILIES:
+        ms, work = fam_ms.get(f, 0.0), stats.get(f, {}).get("work", 0.0)
+        if ms > 0 and work > 0:
+            gbs = work / (ms / 1000.0) / 1e9
+            out[f] = {"gb_per_step": work / steps / 1e9, "ms_per_step": ms / steps, "gbs": gbs,
+                      "frac": gbs / peak}
+    return out
+
+
 def oracle_threads() -> int:
     """Threads the oracle's numpy BLAS runs on: threadpoolctl's report where it
     is installed, else the cores this process may run on."""
@@ -398,11 +419,15 @@ def main():
     barrier()
     t0 = time.perf_counter()
     for k in range(K):
-        s = W + k
+        s, t = W + k, W + K + k
+        if not args.eager:
+            # the library's host-buffer entry point copies the batch in itself
+            model.step_host(pin_tok[s], pin_tgt[s], lr_at(t + 1), t=t + 1, **HP)
+            continue
         with torch.cuda.stream(stream):
             buf_tok.copy_(pin_tok[s], non_blocking=True)
             buf_tgt.copy_(pin_tgt[s], non_blocking=True)
-        step(W + K + k, buf_tok, buf_tgt)  # the loss comes back to the host inside forward
+        step(t, buf_tok, buf_tgt)  # the loss comes back to the host inside forward
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / K
     if world > 1:
@@ -410,7 +435,10 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
     e2e = {"value": tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
-           "d2h_bytes_per_step": 8}
+           "d2h_bytes_per_step": 8,  # the loss and the status word
+           "api": "gpt2_step_host: pinned host token/target buffers, copied to the device inside the call, "
+                  "loss read back" if not args.eager else
+                  "torch copies from pinned host memory, then gpt2_forward / gpt2_backward / gpt2_adamw_step"}
 
     # ---------------------------------------------------------------- instrumented pass: per-kernel times
     model.reset_stats()
@@ -437,6 +465,7 @@ def main():
                 "traffic": traffic, "launches_per_step": mm_launches / K,
                 "flops_per_step": mm_flops / K}
     kernel_ms = {f: v / K for f, v in fam_ms.items() if v > 0}
+    hbm = hbm_fractions(fam_ms, stats, K, peaks)
 
     fpt = model_flops_per_token(cfg["n_layer"], cfg["n_embd"], cfg["vocab"], T)
     tflops = value * fpt / 1e12
@@ -454,7 +483,9 @@ def main():
                        else "gpt2_step (the step replayed as one CUDA graph)",
                        "roofline_pass": "per-kernel times from a separate instrumented pass of the same steps"},
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "roofline": roofline, "mfu": mfu,
-            "kernel_ms_per_step": kernel_ms, "loss_first_last": [losses[0], losses[-1]]}
+            "kernel_ms_per_step": kernel_ms, "hbm": hbm, "loss_first_last": [losses[0], losses[-1]],
+            "workspace_bytes": model.bytes,
+            "peak_device_bytes": torch.cuda.max_memory_allocated()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config)
     if rank == 0:

@@ -180,6 +180,17 @@ int gpt2_adamw_step_ex(gpt2_t* m, const gpt2_adamw_config* cfg);
 int gpt2_step(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T,
               const gpt2_adamw_config* cfg, float* loss_out);
 
+/* gpt2_step with the batch in HOST memory: h_tokens and h_targets (int32
+ * [B,T], row-major, contiguous, owned by the caller) are copied to the
+ * device by the call itself (cudaMemcpyAsync host to device on the model's
+ * stream, before the step's graph), so a caller with data on the host makes
+ * one call per step: 2*B*T*4 bytes go in, the 4-byte loss comes back. Page-
+ * locked (pinned) host buffers make the copies asynchronous; pageable ones
+ * work but are staged by the driver. The buffers may be reused once the call
+ * returns. Same results, errors and state as gpt2_step. */
+int gpt2_step_host(gpt2_t* m, const int32_t* h_tokens, const int32_t* h_targets, int B, int T,
+                   const gpt2_adamw_config* cfg, float* loss_out);
+
 /* ZeRO-1 style sharded update (llm.c "State of the Union", "Multi-GPU
  * training": optimizer state split over data-parallel ranks). AdamW as in
  * gpt2_adamw_step_ex, applied only to the elements [begin, begin + count) of

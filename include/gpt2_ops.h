@@ -112,6 +112,23 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
                    int b_mn_major, const void* bias, int M, int N, int K, void* scratch,
                    size_t scratch_bytes, int* d_status, void* stream);
 
+/* Weight and bias gradient of a linear layer in one tensor-core pass (bf16):
+ * the weight gradient of "matmul_backward" and the bias gradient
+ * "matmul_backward_bias" of llm.c's kernel table ("State of the Union",
+ * "Runtime, DRAM traffic, instructions"), fused:
+ *   dW[m][n] = sum_k dY[k][m] X[k][n]   (fp32 [M,N], overwritten or added to)
+ *   dbias[m] = sum_k dY[k][m]           (fp32 [M], overwritten or added to)
+ * dY [K,M] and X [K,N] bf16 row-major (K = tokens, M = output features, N =
+ * input features), 16-byte aligned; M, N, K multiples of 8. accumulate != 0
+ * adds both results to what dW and dbias hold. The column sums of dY come
+ * from the tensor cores (dY^T times a tile of ones, fp32 accumulation), in the
+ * same pass that reads dY for dW. Scratch: gpt2_op_matmul_bias_grad_scratch()
+ * bytes (partial sums of split K ranges). K = 0 is GPT2_ERR_ARG. */
+size_t gpt2_op_matmul_bias_grad_scratch(int M, int N, int K, int accumulate);
+int gpt2_op_matmul_bias_grad(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
+                             int accumulate, void* scratch, size_t scratch_bytes, int* d_status,
+                             void* stream);
+
 /* FP8 linear layer (the modded-nanogpt project page, "NanoGPT (124M) in 90
  * seconds", "How it works": FP8 for the MLP, the QKV projections and the
  * head), with per-tensor scaling to one of two 8-bit floating-point formats
@@ -212,11 +229,9 @@ size_t gpt2_op_bias_backward_scratch(int N, int C);
 int gpt2_op_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch,
                           size_t scratch_bytes, void* stream);
 
-/* Bias gradient without caller scratch: the reduction of
- * "matmul_backward_bias" in llm.c's kernel table ("State of the Union",
- * "Runtime, DRAM traffic, instructions"), whose code has no entry point of
- * this form. It serves callers that cannot allocate or lend device
- * memory (for example a program whose device memory is wholly owned by
+/* Bias gradient without caller scratch (no counterpart on the pages; in
+ * place of a citation: an addition of this library). It serves callers that
+ * cannot allocate or lend device memory (for example a program whose device memory is wholly owned by
  * another runtime's allocator or a fixed pool, or code that must not call
  * cudaMalloc because it can synchronise the device). It computes exactly
  * what gpt2_op_bias_backward computes, dbias[c] = sum_rows dy[r, c] (fp32,
@@ -259,6 +274,25 @@ int gpt2_op_mean_loss(float* out, const float* losses, int N, void* stream);
 int gpt2_op_adamw(float* master, void* param_bf16, const float* grad, float* m, float* v,
                   int64_t n, float lr, float beta1, float beta2, float eps, float weight_decay,
                   int t, void* stream);
+
+/* Failure-path testing of the bounded device waits (the design's failure
+ * detection: a wait that runs out sets a status bit and the kernel returns;
+ * nothing traps or hangs).
+ * gpt2_debug_set_wait_limit: the bound, in SM clock cycles, of every
+ * mbarrier wait of the tensor-core GEMM, the attention kernels and the
+ * classifier on the current device; cycles <= 0 restores the default
+ * (about 2 s). Takes effect for kernels launched after it returns; must not
+ * be called while such kernels run.
+ * gpt2_debug_stall_matmul: on != 0 makes every tensor-core GEMM launched
+ * afterwards on the current device wait, before its first product, on a
+ * barrier that nothing arrives at. The wait runs out after the bound above;
+ * the kernel then sets the timeout bit (2) of its status word, stops its
+ * other warps, waits (bounded) for its copies in flight, frees its tensor
+ * memory and returns, leaving its output unwritten; the model's calls
+ * report GPT2_ERR_TIMEOUT. on = 0 restores normal operation.
+ * Both return GPT2_OK or GPT2_ERR_CUDA. Test hooks, not for the hot path. */
+int gpt2_debug_set_wait_limit(int64_t cycles);
+int gpt2_debug_stall_matmul(int on);
 
 #ifdef __cplusplus
 }

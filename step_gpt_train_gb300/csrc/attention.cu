@@ -221,10 +221,8 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
     const float scale = 1.0f / sqrtf((float)hd);
     if (dtype == GPT2_MODE_BF16) {
         if (hd != 64) return GPT2_ERR_ARG;
-        launch_dot(D, (const bf16*)dout, (const bf16*)o, B, T, C, H, s);
-        const int r = launch_attention_backward_tc((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, lse, D, B, T, C,
-                                                   H, status, s);
-        return r < 0 ? r : 1 + r;
+        return launch_attention_backward_tc((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv, (const bf16*)o, lse, D,
+                                            B, T, C, H, status, s);
     }
     launch_dot(D, (const float*)dout, (const float*)o, B, T, C, H, s);
     const int64_t n = (int64_t)B * H * T;

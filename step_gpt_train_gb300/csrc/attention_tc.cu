@@ -1,25 +1,32 @@
 // Causal attention forward on the tcgen05 tensor cores (bf16, head size 64).
 //
-// One CTA per (128-query tile, batch, head); two CTAs share an SM. The T x T
-// score matrix exists only as 128 x 128 fp32 tiles in tensor memory (TMEM).
-// Per key block j (causal: j <= query tile):
+// Persistent: two CTAs per SM walk a list of (128-query tile, batch-head)
+// work items ordered longest first (CTA c takes items c, c + G, c + 2G, ...
+// of G CTAs), so the operand rings, the TMEM hand-offs and the next item's
+// loads carry on across items instead of every tile paying a cold start.
+// The T x T score matrix exists only as 128 x 128 fp32 tiles in tensor
+// memory (TMEM). Per key block j (causal: j <= query tile):
 //   S = Q K_j^T           tcgen05.mma M=128 N=128 K=64, into TMEM;
 //   softmax threads       (thread = query row = TMEM lane) load their S row,
 //                         hand the S buffer back, and form
-//                         P = exp2(S log2(e)/sqrt(hd) - m) with a per-row
-//                         reference m, accumulating the row sum l;
-//                         P goes back to TMEM as bf16 pairs (tcgen05.st);
+//                         P = exp2(S log2(e)/sqrt(hd) - m) in fp32 with a
+//                         per-row reference m, accumulating the row sum l;
+//                         P goes back to TMEM as bf16 pairs (tcgen05.st),
+//                         32 keys at a time;
 //   O += P V_j            tcgen05.mma M=128 N=64 K=128 with P read from TMEM
 //                         as the A operand, into a TMEM accumulator.
 // The reference m moves only when a row's maximum grows by more than 8 (log2
 // units), so P <= 256; when it moves, the row's O (in TMEM) and l are scaled
-// by exp2(m_old - m_new) before the next PV MMA. Finally O / l and the
-// log-sum-exp m + log l are written.
+// by exp2(m_old - m_new) before the next PV MMA. At the end of an item the
+// softmax threads read O, hand the accumulator back (the next item's first
+// PV may start) and write O / l and the log-sum-exp m + log l.
 //
-// Warps: 0 TMA producer (Q once; K and V per block, each into a two-stage
+// Warps: 0 TMA producer (Q double-buffered across items, the next item's Q
+// loaded while the current one runs; K and V per block, each into a two-stage
 // ring, so that K(j+1) never waits for PV(j-1)), 1 TMEM allocation and the
-// MMA schedule (run by the whole warp, one elected lane issuing; S for block
-// j+1 is issued before PV for block j), 2..5 softmax. Every wait is bounded.
+// MMA schedule (run by the whole warp, one elected lane issuing; S of the
+// next step is issued before PV of the current one, across item boundaries),
+// 2..5 softmax. Every wait is bounded.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -35,8 +42,8 @@ constexpr int AT_N = 128;                  // keys per block
 constexpr int AT_HD = 64;                  // head size
 constexpr int AT_TILE = AT_M * AT_HD * 2;  // 16 KB: 128 rows of 64 bf16
 constexpr int AT_THREADS = 192;
-// shared memory: Q | K stage 0 | K stage 1 | V stage 0 | V stage 1 | barriers
-constexpr int AT_SMEM = 5 * AT_TILE + 256 + 1024;
+// shared memory: Q stage 0, 1 | K stage 0, 1 | V stage 0, 1 | barriers
+constexpr int AT_SMEM = 6 * AT_TILE + 256 + 1024;
 constexpr uint32_t AT_TMEM_COLS = 256;     // S [0,128), O [128,192), P [192,256) (bf16 pairs)
 constexpr float AT_LN2 = 0.6931471805599453f;
 constexpr float AT_RESCALE = 8.f;          // log2 of the largest P before the reference max moves
@@ -46,8 +53,39 @@ struct FwdArgs {
     float* lse;    // [B, H, T]
     int* status;
     int T, C, H;
+    int nqt;       // 128-query tiles per sequence
+    int items;     // nqt * B * H
     float scale_log2;  // log2(e) / sqrt(hd)
 };
+
+// Work item idx of the longest-first list: query tile and batch-head.
+struct FItem {
+    int qt, bh;
+};
+__device__ __forceinline__ bool fwd_item(const FwdArgs& a, int i, FItem& it) {
+    const int idx = blockIdx.x + i * gridDim.x;
+    if (idx >= a.items) return false;
+    const int BH = a.items / a.nqt;
+    it.qt = a.nqt - 1 - idx / BH;
+    it.bh = idx % BH;
+    return true;
+}
+
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// (lo, hi) rounded to a packed bf16 pair, lo in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// A packed bf16 pair as a packed fp32 pair (low half first).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t p) { return f2_pack(p << 16, p & 0xFFFF0000u); }
+
 
 __global__ void __launch_bounds__(AT_THREADS, 2)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, FwdArgs a) {
@@ -55,32 +93,31 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base;
-    auto sK = [&](int st) { return base + (1 + st) * AT_TILE; };
-    auto sV = [&](int st) { return base + (3 + st) * AT_TILE; };
-    const uint32_t bars = base + 5 * AT_TILE;
-    uint8_t* bar_area = gbase + 5 * AT_TILE;
-    // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free, p_full, p_free,
-    // o_done, drain
-    const uint32_t q_full = bars;
-    auto k_full = [&](int i) { return bars + 8u * (1 + i); };
-    auto k_empty = [&](int i) { return bars + 8u * (3 + i); };
-    auto v_full = [&](int i) { return bars + 8u * (5 + i); };
-    auto v_empty = [&](int i) { return bars + 8u * (7 + i); };
-    const uint32_t s_full = bars + 8u * 9, s_free = bars + 8u * 10;
-    const uint32_t p_full = bars + 8u * 11, p_free = bars + 8u * 12;
-    const uint32_t o_done = bars + 8u * 13, drain = bars + 8u * 14;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * 15);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * 15 + 4);
+    auto sQ = [&](int st) { return base + st * AT_TILE; };
+    auto sK = [&](int st) { return base + (2 + st) * AT_TILE; };
+    auto sV = [&](int st) { return base + (4 + st) * AT_TILE; };
+    const uint32_t bars = base + 6 * AT_TILE;
+    uint8_t* bar_area = gbase + 6 * AT_TILE;
+    // barriers: q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free,
+    // p_full, p_free, o_done, o_free, drain
+    auto q_full = [&](int i) { return bars + 8u * (0 + i); };
+    auto q_empty = [&](int i) { return bars + 8u * (2 + i); };
+    auto k_full = [&](int i) { return bars + 8u * (4 + i); };
+    auto k_empty = [&](int i) { return bars + 8u * (6 + i); };
+    auto v_full = [&](int i) { return bars + 8u * (8 + i); };
+    auto v_empty = [&](int i) { return bars + 8u * (10 + i); };
+    const uint32_t s_full = bars + 8u * 12, s_free = bars + 8u * 13;
+    const uint32_t p_full = bars + 8u * 14, p_free = bars + 8u * 15;
+    const uint32_t o_done = bars + 8u * 16, o_free = bars + 8u * 17, drain = bars + 8u * 18;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * 19);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * 19 + 4);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest rows first
-    const int b = blockIdx.y / a.H, h = blockIdx.y % a.H;
-    const int nkb = qt + 1;                     // causal: key blocks 0..qt
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
         for (int i = 0; i < 2; i++) {
+            mbar_init(q_full(i), 1);
+            mbar_init(q_empty(i), 1);
             mbar_init(k_full(i), 1);
             mbar_init(k_empty(i), 1);
             mbar_init(v_full(i), 1);
@@ -91,6 +128,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
         mbar_init(p_full, 4);
         mbar_init(p_free, 1);
         mbar_init(o_done, 1);
+        mbar_init(o_free, 4);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -105,24 +143,42 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------- TMA producer
-            int k_issued[2] = {-1, -1}, v_issued[2] = {-1, -1};  // parity of each stage's last load
-            mbar_expect_tx(q_full, AT_TILE);
-            tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HD, qt * AT_M, b);
-            for (int j = 0; j < nkb; j++) {
-                const int st = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(k_empty(st), ph ^ 1u, abort_flag, a.status)) break;
-                mbar_expect_tx(k_full(st), AT_TILE);
-                tma_load_3d(sK(st), &tm_qkv, k_full(st), a.C + h * AT_HD, j * AT_N, b);
-                k_issued[st] = (int)ph;
-                // V(j) once PV(j-2) has read the stage
-                if (!mbar_wait(v_empty(st), ph ^ 1u, abort_flag, a.status)) break;
-                mbar_expect_tx(v_full(st), AT_TILE);
-                tma_load_3d(sV(st), &tm_qkv, v_full(st), 2 * a.C + h * AT_HD, j * AT_N, b);
-                v_issued[st] = (int)ph;
+            // Q of item i into stage i & 1 once item i - 2 has finished with
+            // it; K and V of the g-th block (over all items) into stage g & 1.
+            int q_issued[2] = {-1, -1}, k_issued[2] = {-1, -1}, v_issued[2] = {-1, -1};
+            auto load_q = [&](int i, const FItem& it) -> bool {
+                const int st = i & 1;
+                const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(q_empty(st), ph ^ 1u, abort_flag, a.status)) return false;
+                mbar_expect_tx(q_full(st), AT_TILE);
+                tma_load_3d(sQ(st), &tm_qkv, q_full(st), (it.bh % a.H) * AT_HD, it.qt * AT_M, it.bh / a.H);
+                q_issued[st] = (int)ph;
+                return true;
+            };
+            FItem it;
+            bool ok = !fwd_item(a, 0, it) || load_q(0, it);
+            int g = 0;
+            for (int i = 0; ok && fwd_item(a, i, it); i++) {
+                const int b = it.bh / a.H, h = it.bh % a.H;
+                for (int j = 0; j <= it.qt; j++, g++) {
+                    const int st = g & 1;
+                    const uint32_t ph = (uint32_t)(g >> 1) & 1u;
+                    if (!(ok = mbar_wait(k_empty(st), ph ^ 1u, abort_flag, a.status))) break;
+                    mbar_expect_tx(k_full(st), AT_TILE);
+                    tma_load_3d(sK(st), &tm_qkv, k_full(st), a.C + h * AT_HD, j * AT_N, b);
+                    k_issued[st] = (int)ph;
+                    // V(g) once PV(g-2) has read the stage
+                    if (!(ok = mbar_wait(v_empty(st), ph ^ 1u, abort_flag, a.status))) break;
+                    mbar_expect_tx(v_full(st), AT_TILE);
+                    tma_load_3d(sV(st), &tm_qkv, v_full(st), 2 * a.C + h * AT_HD, j * AT_N, b);
+                    v_issued[st] = (int)ph;
+                    // the next item's Q after this item's first K/V block
+                    FItem nit;
+                    if (j == 0 && fwd_item(a, i + 1, nit) && !(ok = load_q(i + 1, nit))) break;
+                }
             }
-            mbar_drain(q_full, 0, a.status);
             for (int st = 0; st < 2; st++) {
+                if (q_issued[st] >= 0) mbar_drain(q_full(st), (uint32_t)q_issued[st], a.status);
                 if (k_issued[st] >= 0) mbar_drain(k_full(st), (uint32_t)k_issued[st], a.status);
                 if (v_issued[st] >= 0) mbar_drain(v_full(st), (uint32_t)v_issued[st], a.status);
             }
@@ -135,40 +191,61 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
             const bool leader = elect_one();
             constexpr uint32_t idesc_s = make_idesc(AT_M, AT_N, false, false);
             constexpr uint32_t idesc_o = make_idesc(AT_M, AT_HD, false, true);
-            bool ok = warp_wait(q_full, 0, abort_flag, a.status);
-            // S(j) = Q K(j)^T; the K stage is free once these MMAs finish
-            auto issue_s = [&](int j) -> bool {
-                const int st = j & 1;
-                if (!warp_wait(k_full(st), (j >> 1) & 1, abort_flag, a.status)) return false;
-                if (!warp_wait(s_free, (j & 1) ^ 1u, abort_flag, a.status)) return false;
+            // S(g) = Q(i) K(g)^T for block j of item i; the K stage is free once
+            // these MMAs finish, the Q stage after the item's last block
+            auto issue_s = [&](int i, int j, int last, int g) -> bool {
+                const int st = g & 1;
+                if (j == 0 && !warp_wait(q_full(i & 1), (i >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(k_full(st), (g >> 1) & 1, abort_flag, a.status)) return false;
+                if (!warp_wait(s_free, (g & 1) ^ 1u, abort_flag, a.status)) return false;
                 tc_fence_after();
+                const uint32_t q = sQ(i & 1);
                 if (leader) {
 #pragma unroll
                     for (int k = 0; k < AT_HD / 16; k++)
-                        tc_mma(tmem, sw128_desc(sQ + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024), idesc_s,
+                        tc_mma(tmem, sw128_desc(q + k * 32, 16, 1024), sw128_desc(sK(st) + k * 32, 16, 1024), idesc_s,
                                k > 0 ? 1u : 0u);
                 }
                 if (leader) tc_commit(s_full);
                 if (leader) tc_commit(k_empty(st));
+                if (leader && j == last) tc_commit(q_empty(i & 1));
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < nkb; j++) {
-                if (j + 1 < nkb && !(ok = issue_s(j + 1))) break;
-                // O += P(j) V(j)
-                if (!(ok = warp_wait(p_full, j & 1, abort_flag, a.status))) break;
-                if (!(ok = warp_wait(v_full(j & 1), (j >> 1) & 1, abort_flag, a.status))) break;
+            FItem it;
+            bool ok = fwd_item(a, 0, it);
+            int i = 0, j = 0, g = 0;
+            if (ok) ok = issue_s(0, 0, it.qt, 0);
+            while (ok) {
+                // the step after (i, j): S for it is issued before PV(i, j)
+                int ni = i, nj = j + 1;
+                FItem nit = it;
+                bool more = true;
+                if (nj > it.qt) {
+                    ni = i + 1;
+                    nj = 0;
+                    more = fwd_item(a, ni, nit);
+                }
+                if (more && !(ok = issue_s(ni, nj, nit.qt, g + 1))) break;
+                // O += P(g) V(g); an item's first PV waits for the previous item's O to be read
+                if (!(ok = warp_wait(p_full, g & 1, abort_flag, a.status))) break;
+                if (!(ok = warp_wait(v_full(g & 1), (g >> 1) & 1, abort_flag, a.status))) break;
+                if (j == 0 && i > 0 && !(ok = warp_wait(o_free, (i - 1) & 1, abort_flag, a.status))) break;
                 tc_fence_after();
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < AT_N / 16; kk++)
-                        tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV(j & 1) + kk * 2048, 8192, 1024), idesc_o,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_ts(tmem + 128u, tmem + 192u + kk * 8, sw128_desc(sV(g & 1) + kk * 2048, 8192, 1024),
+                                  idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (leader) tc_commit(p_free);
-                if (leader) tc_commit(v_empty(j & 1));
+                if (leader) tc_commit(v_empty(g & 1));
+                if (leader && j == it.qt) tc_commit(o_done);
+                if (!more) break;
+                i = ni;
+                j = nj;
+                it = nit;
+                g++;
             }
-            if (leader && ok) tc_commit(o_done);
             if (leader) tc_commit(drain);
             mbar_drain(drain, 0, a.status);
         }
@@ -176,112 +253,110 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
         // ------------------------------------------------------ softmax (warps 2..5)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row in the tile = TMEM lane
-        const int q = qt * AT_M + r;     // query position
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-        float m = -FLT_MAX, l = 0.f;
+        const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
         bool ok = true;
-        for (int j = 0; j < nkb; j++) {
-            uint32_t v[4][32];
-            if (!(ok = warp_wait(s_full, j & 1, abort_flag, a.status))) break;
-            tc_fence_after();
+        FItem it;
+        int g = 0;
+        for (int i = 0; ok && fwd_item(a, i, it); i++) {
+            const int q = it.qt * AT_M + r;  // query position
+            float m = -FLT_MAX, l = 0.f;
+            for (int j = 0; j <= it.qt; j++, g++) {
+                uint32_t v[4][32];
+                if (!(ok = warp_wait(s_full, g & 1, abort_flag, a.status))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; c++) tc_ld32_issue(trow + (uint32_t)(c * 32), v[c]);
+                for (int c = 0; c < 4; c++) tc_ld32_issue(trow + (uint32_t)(c * 32), v[c]);
 #pragma unroll
-            for (int c = 0; c < 4; c++) tc_ld_wait(v[c]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);  // the MMA may now write S(j+1)
-            // The row maximum of the raw scores (the scale is positive), with
-            // the keys after the query masked to -FLT_MAX on the diagonal block;
-            // eight independent maxima keep the dependency chains short.
-            const bool diag = j == qt;
-            if (diag) {
+                for (int c = 0; c < 4; c++) tc_ld_wait(v[c]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);  // the MMA may now write the next S
+                // The row maximum of the raw scores (the scale is positive), with
+                // the keys after the query masked to -FLT_MAX on the diagonal block;
+                // four independent three-input maxima keep the chains short.
+                if (j == it.qt) {
+#pragma unroll
+                    for (int c = 0; c < 4; c++)
+#pragma unroll
+                        for (int e = 0; e < 32; e++)
+                            if (j * AT_N + c * 32 + e > q) v[c][e] = __float_as_uint(-FLT_MAX);
+                }
+                float m4[4] = {-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX};
 #pragma unroll
                 for (int c = 0; c < 4; c++)
 #pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        if (j * AT_N + c * 32 + i > q) v[c][i] = __float_as_uint(-FLT_MAX);
-            }
-            float m8[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) m8[e] = -FLT_MAX;
-#pragma unroll
-            for (int c = 0; c < 4; c++)
-#pragma unroll
-                for (int i = 0; i < 32; i++) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(v[c][i]));
-#pragma unroll
-            for (int e = 0; e < 4; e++) m8[e] = fmaxf(m8[e], m8[e + 4]);
-            const float mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])) * a.scale_log2;
-            // move the reference max only when it grew by more than AT_RESCALE
-            float factor = 1.f;
-            const bool move = mx > m + AT_RESCALE;
-            if (move) {
-                factor = ex2_approx(m - mx);  // 0 on the first block (m = -FLT_MAX)
-                m = mx;
-                l *= factor;
-            }
-            // P = exp2(s scale - m) as packed bf16 pairs (pk[c*16 + i/2] holds keys
-            // c*32+i, c*32+i+1), the row sum in four paired accumulators
-            uint32_t pk[64];
-            const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-m, -m);
-            uint64_t l2[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int c = 0; c < 4; c++)
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(v[c][i], v[c][i + 1]), scale2, nm2), x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    l2[(i >> 1) & 3] = f2_add(l2[(i >> 1) & 3], f2_pack(p0, p1));
-                    __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-                    pk[c * 16 + i / 2] = *reinterpret_cast<uint32_t*>(&hh);
+                    for (int e = 0; e < 32; e += 2)
+                        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[c][e]), __uint_as_float(v[c][e + 1]));
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+                // move the reference max only when it grew by more than AT_RESCALE
+                float factor = 1.f;
+                const bool move = mx > m + AT_RESCALE;
+                if (move) {
+                    factor = ex2_approx(m - mx);  // 0 on the first block (m = -FLT_MAX)
+                    m = mx;
+                    l *= factor;
                 }
-            {
-                float s0, s1, s2, s3, s4, s5, s6, s7;
-                f2_unpack(l2[0], s0, s1);
-                f2_unpack(l2[1], s2, s3);
-                f2_unpack(l2[2], s4, s5);
-                f2_unpack(l2[3], s6, s7);
-                l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-            }
-            // PV(j-1) has finished with the P buffer and with O
-            if (!(ok = warp_wait(p_free, (j & 1) ^ 1u, abort_flag, a.status))) break;
-            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // PV of the previous step has finished with the P buffer and O
+                if (!(ok = warp_wait(p_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
                 tc_fence_after();
+                // P = exp2(s scale - m), 32 keys at a time into TMEM as bf16
+                // pairs (pk[e/2] holds keys c*32+e, c*32+e+1), the row sum in
+                // four paired fp32 accumulators
+                const uint64_t nm2 = f2_pack(-m, -m);
+                uint64_t l2[4] = {0, 0, 0, 0};
 #pragma unroll
-                for (int half = 0; half < 2; half++) {
-                    uint32_t ov[32];
-                    tc_ld32_issue(trow + 128u + half * 32, ov);
-                    tc_ld_wait(ov);
+                for (int c = 0; c < 4; c++) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * factor);
-                    tc_st32(trow + 128u + half * 32, ov);
+                    for (int e = 0; e < 32; e += 2) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(v[c][e], v[c][e + 1]), scale2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        l2[(e >> 1) & 3] = f2_add(l2[(e >> 1) & 3], f2_pack(p0, p1));
+                        pk[e / 2] = cvt_bf16x2(p0, p1);
+                    }
+                    tc_st16(trow + 192u + (uint32_t)(c * 16), pk);
+                }
+                {
+                    float s0, s1, s2, s3, s4, s5, s6, s7;
+                    f2_unpack(l2[0], s0, s1);
+                    f2_unpack(l2[1], s2, s3);
+                    f2_unpack(l2[2], s4, s5);
+                    f2_unpack(l2[3], s6, s7);
+                    l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+                }
+                // O rescaled (once the scores' registers are free) before PV reads it
+                if (j > 0 && __any_sync(0xffffffffu, move)) {
+#pragma unroll
+                    for (int half = 0; half < 2; half++) {
+                        uint32_t ov[32];
+                        tc_ld32_issue(trow + 128u + half * 32, ov);
+                        tc_ld_wait(ov);
+#pragma unroll
+                        for (int e = 0; e < 32; e++) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+                        tc_st32(trow + 128u + half * 32, ov);
+                    }
                 }
                 tc_st_wait();
                 tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
             }
-            // P to TMEM, the A operand of PV
-            {
-                uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-                uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-                tc_fence_after();
-                tc_st32(trow + 192u, p0);
-                tc_st32(trow + 224u, p1);
-                tc_st_wait();
-                tc_fence_before();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-        }
-        // O / l, log-sum-exp
-        if (ok && warp_wait(o_done, 0, abort_flag, a.status)) {
+            if (!ok) break;
+            // O / l, log-sum-exp; O is handed back once it is in registers
+            if (!(ok = warp_wait(o_done, i & 1, abort_flag, a.status))) break;
             tc_fence_after();
             uint32_t ov[2][32];
             tc_ld32_issue(trow + 128u, ov[0]);
             tc_ld32_issue(trow + 160u, ov[1]);
             tc_ld_wait(ov[0]);
             tc_ld_wait(ov[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
             if (q < a.T) {
+                const int b = it.bh / a.H, h = it.bh % a.H;
                 const float inv = 1.f / l;
                 bf16* orow = a.o + ((int64_t)b * a.T + q) * a.C + h * AT_HD;
 #pragma unroll
@@ -291,7 +366,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                     for (int e = 0; e < 8; e++) f[e] = __uint_as_float(ov[u / 4][(u % 4) * 8 + e]) * inv;
                     store8(orow + u * 8, f);
                 }
-                a.lse[((int64_t)b * a.H + h) * a.T + q] = (m + log2f(l)) * AT_LN2;
+                a.lse[(int64_t)it.bh * a.T + q] = (m + log2f(l)) * AT_LN2;
             }
         }
     }
@@ -321,6 +396,8 @@ bool make_qkv_map(CUtensorMap* map, const void* qkv, int B, int T, int C) {
 
 }  // namespace
 
+int attention_tc_set_wait_limit(long long cycles) { return set_wait_limit(cycles); }
+
 // bf16 forward, head size 64 (the attention.cu launcher routes here).
 int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int T, int C, int H, int* status,
                                 cudaStream_t s) {
@@ -339,8 +416,10 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
     a.T = T;
     a.C = C;
     a.H = H;
+    a.nqt = (T + AT_M - 1) / AT_M;
+    a.items = a.nqt * B * H;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)(C / H));
-    dim3 grid((T + AT_M - 1) / AT_M, B * H);
+    const int grid = a.items < 2 * gpt2_num_sms() ? a.items : 2 * gpt2_num_sms();  // persistent: two CTAs per SM
     attn_fwd_tc_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(map, a);
     return 1;
 }
@@ -394,7 +473,8 @@ constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256, Q_DS = 320;
 struct BwdArgs {
     bf16* dqkv;          // [B*T, 3C]
     const float* lse;    // [B, H, T]
-    const float* D;      // [B, H, T]
+    const float* D;      // [B, H, T]: read by the dK/dV kernel
+    float* Dw;           // the same buffer: written by the dQ kernel
     int* status;
     int B, T, C, H;
     int nqt;             // 128-row tiles per sequence
@@ -772,7 +852,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     f2_unpack(f2_fma(f2_pack(sv[cc], sv[cc + 1]), scale2, nl2[cc / 2]), x0, x1);
                     p[cc] = (cc >= lo && cc < hi) ? ex2_approx(x0) : 0.f;
                     p[cc + 1] = (cc + 1 >= lo && cc + 1 < hi) ? ex2_approx(x1) : 0.f;
-                    pk[cc / 2] = pack2(p[cc], p[cc + 1]);
+                    pk[cc / 2] = cvt_bf16x2(p[cc], p[cc + 1]);
                 }
             } else {
 #pragma unroll
@@ -781,7 +861,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     f2_unpack(f2_fma(f2_pack(sv[cc], sv[cc + 1]), scale2, nl2[cc / 2]), x0, x1);
                     p[cc] = ex2_approx(x0);
                     p[cc + 1] = ex2_approx(x1);
-                    pk[cc / 2] = pack2(p[cc], p[cc + 1]);
+                    pk[cc / 2] = cvt_bf16x2(p[cc], p[cc + 1]);
                 }
             }
             // the previous step's P^T and dS^T have been read: its dK product,
@@ -802,13 +882,14 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dp_free);
             const uint64_t* d2 = reinterpret_cast<const uint64_t*>(slot + 32);
+            uint32_t dk[EW_COLS / 2];
 #pragma unroll
             for (int cc = 0; cc < EW_COLS; cc += 2) {
                 float d0, d1;
                 f2_unpack(f2_mul(f2_pack(p[cc], p[cc + 1]), f2_sub(f2_pack(sv[cc], sv[cc + 1]), d2[cc / 2])), d0, d1);
-                pk[cc / 2] = pack2(d0, d1);
+                dk[cc / 2] = cvt_bf16x2(d0, d1);
             }
-            tc_st16(trow + KV_DS + (uint32_t)(part * EW_COLS / 2), pk);
+            tc_st16(trow + KV_DS + (uint32_t)(part * EW_COLS / 2), dk);
             tc_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -830,10 +911,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
 // -------------------------------------------------------------------------- dQ
 // Shared memory: 2 x (Q, dO) (an item's tile and the next one's) | DQ_ST x
-// (K, V) | dQ staging tile for the TMA store | barriers.
+// (K, V) | dQ staging tile for the TMA store | the forward's output O tile of
+// an item | D of two items (128 floats each) | barriers.
+// This kernel runs first and also forms D = rowsum(dO * O) of every query
+// (its store warp, from the dO and O tiles, one item ahead), which it uses
+// itself and writes for the dK/dV kernel.
 __global__ void __launch_bounds__(BW_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                          const __grid_constant__ CUtensorMap tm_dqkv, BwdArgs a) {
+                          const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_dqkv,
+                          BwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -846,8 +932,11 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     auto sV = [&](int st) { return base + (5 + 2 * st) * AT_TILE; };
     uint8_t* stg = gbase + (4 + 2 * NS) * AT_TILE;
     const uint32_t stg_addr = base + (4 + 2 * NS) * AT_TILE;
-    const uint32_t bars = base + (5 + 2 * NS) * AT_TILE;
-    uint8_t* bar_area = gbase + (5 + 2 * NS) * AT_TILE;
+    const uint32_t sX = base + (5 + 2 * NS) * AT_TILE;  // O of the forward
+    const uint8_t* xtile = gbase + (5 + 2 * NS) * AT_TILE;
+    float* dslot = reinterpret_cast<float*>(gbase + (6 + 2 * NS) * AT_TILE);  // [2][128]
+    const uint32_t bars = base + (6 + 2 * NS) * AT_TILE + 1024;
+    uint8_t* bar_area = gbase + (6 + 2 * NS) * AT_TILE + 1024;
     auto q_full = [&](int b) { return bars + 8u * b; };
     auto q_empty = [&](int b) { return bars + 8u * (2 + b); };
     auto o_full = [&](int b) { return bars + 8u * (4 + b); };
@@ -860,8 +949,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t ds_full = bx + 32u, ds_free = bx + 40u;
     const uint32_t acc_full = bx + 48u, acc_empty = bx + 56u, drain = bx + 64u;
     const uint32_t stg_free = bx + 72u, stg_full = bx + 80u;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 88);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 92);
+    const uint32_t x_full = bx + 88u, x_empty = bx + 96u;
+    auto d_full = [&](int sl) { return bx + 104u + 8u * sl; };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (8 + 2 * NS) + 120);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (8 + 2 * NS) + 124);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -887,6 +978,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_init(drain, 1);
         mbar_init(stg_free, 1);
         mbar_init(stg_full, BW_EW);
+        mbar_init(x_full, 1);
+        mbar_init(x_empty, 1);
+        mbar_init(d_full(0), 1);
+        mbar_init(d_full(1), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -901,14 +996,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         if (lane == 0) {
             // -------------------------------------------------- TMA producer
             int kv_issued[NS], qo_issued[2] = {-1, -1};  // parity of each buffer's last load (final drain)
+            int x_issued = -1;
             for (int i = 0; i < NS; i++) kv_issued[i] = -1;
             int g = 0;
-            // Q and dO of item i into buffer i & 1, once the item before last has
-            // finished with it
+            // Q, dO and O of item i: Q and dO into buffer i & 1, once the item
+            // before last has finished with it, O into the one O tile; all three
+            // once D of the previous item is formed (which also means the store
+            // warp is done with the dO tile of the item before last)
             auto load_qo = [&](int i, const Item& it) -> bool {
                 const int b = it.bh / a.H, h = it.bh % a.H;
                 const int qb = i & 1;
                 const uint32_t qph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(x_empty, (uint32_t)(i & 1) ^ 1u, abort_flag, a.status)) return false;
+                mbar_expect_tx(x_full, AT_TILE);
+                tma_load_3d(sX, &tm_o, x_full, h * AT_HD, it.tile * AT_M, b);
+                x_issued = i & 1;
                 if (!mbar_wait(q_empty(qb), qph ^ 1u, abort_flag, a.status)) return false;
                 mbar_expect_tx(q_full(qb), AT_TILE);
                 tma_load_3d(sQ(qb), &tm_qkv, q_full(qb), h * AT_HD, it.tile * AT_M, b);
@@ -947,6 +1049,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                     mbar_drain(q_full(qb), (uint32_t)qo_issued[qb], a.status);
                     mbar_drain(o_full(qb), (uint32_t)qo_issued[qb], a.status);
                 }
+            if (x_issued >= 0) mbar_drain(x_full, (uint32_t)x_issued, a.status);
             for (int st = 0; st < NS; st++)
                 if (kv_issued[st] >= 0) mbar_drain(kv_full(st), (uint32_t)kv_issued[st], a.status);
         }
@@ -1015,10 +1118,50 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             mbar_drain(drain, 0, a.status);
         }
     } else if (warp == BW_STORE_WARP) {
-        // ------------------------------------------------------ accumulator stores
-        // item f's dQ tile, once the elementwise warps have staged it
-        Item it;
-        for (int f = 0; get_item<true>(a, f, it); f++) {
+        // ------------------------------------------------------ D and the accumulator stores
+        // D of item i (rows lane, lane + 32, ...: each lane sums the 64 products
+        // of its row in a fixed order) from the item's dO tile (buffer i & 1) and
+        // O tile, into D slot i & 1 and to global memory for the dK/dV kernel.
+        auto form_d = [&](int i, const Item& it) -> bool {
+            if (!warp_wait(x_full, i & 1, abort_flag, a.status)) return false;
+            if (!warp_wait(o_full(i & 1), (i >> 1) & 1, abort_flag, a.status)) return false;
+            const uint8_t* dot = gbase + (2 * (i & 1) + 1) * AT_TILE;
+            float* dst = dslot + (i & 1) * 128;
+#pragma unroll 1
+            for (int k = 0; k < 4; k++) {
+                const int row = lane + 32 * k;
+                uint64_t acc2 = 0;
+#pragma unroll
+                for (int u = 0; u < 8; u++) {
+                    const int off = row * 128 + ((u ^ (row & 7)) << 4);  // 128-byte swizzle
+                    const uint4 x = *reinterpret_cast<const uint4*>(dot + off);
+                    const uint4 y = *reinterpret_cast<const uint4*>(xtile + off);
+                    acc2 = f2_fma(bf16x2_to_f2(x.x), bf16x2_to_f2(y.x), acc2);
+                    acc2 = f2_fma(bf16x2_to_f2(x.y), bf16x2_to_f2(y.y), acc2);
+                    acc2 = f2_fma(bf16x2_to_f2(x.z), bf16x2_to_f2(y.z), acc2);
+                    acc2 = f2_fma(bf16x2_to_f2(x.w), bf16x2_to_f2(y.w), acc2);
+                }
+                float d0, d1;
+                f2_unpack(acc2, d0, d1);
+                const float d = d0 + d1;
+                dst[row] = d;
+                const int q = it.tile * AT_M + row;
+                if (q < a.T) a.Dw[(int64_t)it.bh * a.T + q] = d;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(x_empty);   // the O tile may be loaded again
+                mbar_arrive(d_full(i & 1));
+            }
+            return true;
+        };
+        // D of the first two items, then per item f: its dQ tile out, once the
+        // elementwise warps have staged it (after they read D(f + 1)), then
+        // D(f + 2) into the slot D(f) used
+        Item it, it2;
+        bool ok = true;
+        for (int i = 0; ok && i < 2 && get_item<true>(a, i, it2); i++) ok = form_d(i, it2);
+        for (int f = 0; ok && get_item<true>(a, f, it); f++) {
             if (!warp_wait(stg_full, f & 1, abort_flag, a.status)) break;
             if (lane == 0) {
                 const int b = it.bh / a.H, h = it.bh % a.H;
@@ -1027,6 +1170,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 mbar_arrive(stg_free);
             }
             __syncwarp();
+            if (get_item<true>(a, f + 2, it2)) ok = form_d(f + 2, it2);
         }
         if (lane == 0) bulk_wait_all();  // the stores are complete before the CTA ends
     } else {
@@ -1034,13 +1178,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         const int quad = warp & 3, part = ew >> 2;
         const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-        // this row's lse and D for an item; the next item's are loaded ahead and
-        // used as they are (converted to log2 units when their item starts)
-        auto load_row = [&](const Item& it, float& l, float& d) {
+        // this row's lse for an item; the next item's is loaded ahead and used as
+        // it is (converted to log2 units when its item starts); D comes from the
+        // store warp's slot
+        auto load_row = [&](const Item& it, float& l) {
             const int q = it.tile * AT_M + r;
-            const int64_t o = (int64_t)it.bh * a.T + (q < a.T ? q : 0);
-            l = a.lse[o];
-            d = a.D[o];
+            l = a.lse[(int64_t)it.bh * a.T + (q < a.T ? q : 0)];
         };
         // An item's dQ leaves TMEM during the next item's first step, once its
         // exponentials are done, so the item's last dQ product runs meanwhile:
@@ -1069,8 +1212,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             return true;
         };
         Cur c = cur_first<true>(a);
-        float l_nx = 0.f, d_nx = 0.f, lse2 = 0.f, Dq = 0.f;
-        if (c.valid) load_row(c.it, l_nx, d_nx);
+        float l_nx = 0.f, lse2 = 0.f, Dq = 0.f;
+        if (c.valid) load_row(c.it, l_nx);
         bool ok = true;
         while (c.valid) {
             const Cur nx = cur_next<true>(a, c);
@@ -1078,9 +1221,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             const int q = c.it.tile * AT_M + r;
             if (c.n == 0) {
                 lse2 = l_nx * 1.4426950408889634f;
-                Dq = d_nx;
                 Item it2;
-                if (get_item<true>(a, c.i + 1, it2)) load_row(it2, l_nx, d_nx);
+                if (get_item<true>(a, c.i + 1, it2)) load_row(it2, l_nx);
+                if (!(ok = warp_wait(d_full(c.i & 1), (c.i >> 1) & 1, abort_flag, a.status))) break;
+                Dq = dslot[(c.i & 1) * 128 + r];
             }
             const int k0 = c.n * AT_N + part * EW_COLS;  // first key of this thread's columns
             const bool diag = c.n == c.it.tile;
@@ -1128,7 +1272,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             for (int cc = 0; cc < EW_COLS; cc += 2) {
                 float d0, d1;
                 f2_unpack(f2_mul(f2_pack(p[cc], p[cc + 1]), f2_sub(f2_pack(sv[cc], sv[cc + 1]), dq2)), d0, d1);
-                pk[cc / 2] = pack2(d0, d1);
+                pk[cc / 2] = cvt_bf16x2(d0, d1);
             }
             if (!(ok = warp_wait(ds_free, (g & 1) ^ 1u, abort_flag, a.status))) break;
             tc_st16(trow + Q_DS + (uint32_t)(part * EW_COLS / 2), pk);
@@ -1165,17 +1309,19 @@ bool make_do_map(CUtensorMap* map, const void* dout, int B, int T, int C) {
 }
 
 constexpr int DKDV_SMEM = (6 + 2 * DKDV_ST) * AT_TILE + BW_EW * 256 + 256 + 1024;
-constexpr int DQ_SMEM = (5 + 2 * DQ_ST) * AT_TILE + 256 + 1024;
+constexpr int DQ_SMEM = (6 + 2 * DQ_ST) * AT_TILE + 1024 + 256 + 1024;
 static_assert(DKDV_SMEM <= 232448 && DQ_SMEM <= 232448, "shared memory per CTA");
 
 }  // namespace
 
-// bf16 backward after D = rowsum(dO * O) is in D (the attention.cu launcher
-// computes it and routes here).
-int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, const float* lse, const float* D,
-                                 int B, int T, int C, int H, int* status, cudaStream_t s) {
-    CUtensorMap mq, mo, md;  // md: the same view of dqkv, for the TMA stores of dQ, dK, dV
-    if (!make_qkv_map(&mq, qkv, B, T, C) || !make_do_map(&mo, dout, B, T, C) || !make_qkv_map(&md, dqkv, B, T, C))
+// bf16 backward (the attention.cu launcher routes here). D = rowsum(dO * O)
+// is formed by the dQ kernel, which runs first, into D ([B, H, T] scratch),
+// and read from there by the dK/dV kernel.
+int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, const bf16* o, const float* lse,
+                                 float* D, int B, int T, int C, int H, int* status, cudaStream_t s) {
+    CUtensorMap mq, mo, mx, md;  // md: the same view of dqkv, for the TMA stores of dQ, dK, dV
+    if (!make_qkv_map(&mq, qkv, B, T, C) || !make_do_map(&mo, dout, B, T, C) || !make_do_map(&mx, o, B, T, C) ||
+        !make_qkv_map(&md, dqkv, B, T, C))
         return GPT2_ERR_CUDA;
     // once per process; a function-local static is initialised thread-safely
     static const bool configured = [] {
@@ -1188,6 +1334,7 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     a.dqkv = dqkv;
     a.lse = lse;
     a.D = D;
+    a.Dw = D;
     a.status = status;
     a.B = B;
     a.T = T;
@@ -1198,7 +1345,7 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     a.scale_log2 = 1.4426950408889634f * a.scale;
     const int items = a.nqt * B * H;
     const int grid = items < gpt2_num_sms() ? items : gpt2_num_sms();  // persistent: one CTA per SM
+    attn_bwd_dq_tc_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, mo, mx, md, a);
     attn_bwd_dkdv_tc_kernel<<<grid, BW_THREADS, DKDV_SMEM, s>>>(mq, mo, md, a);
-    attn_bwd_dq_tc_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, mo, md, a);
     return 2;
 }

@@ -300,6 +300,8 @@ static int classifier_dispatch(void* logits, float* losses, const int32_t* targe
 #undef CLS_CALL
 }
 
+int classifier_set_wait_limit(long long cycles) { return tc::set_wait_limit(cycles); }
+
 int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
                       float dloss, int* status, cudaStream_t s) {
     if (N == 0) return 0;

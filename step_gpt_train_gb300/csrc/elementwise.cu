@@ -4,6 +4,7 @@
 // coalesced 512-byte span.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 #include <algorithm>
 #include <cmath>
@@ -487,13 +488,31 @@ __global__ void __launch_bounds__(EW_THREADS) ew_kernel(T* out, const T* a, T* b
         const int64_t i = base + (int64_t)u * EW_THREADS;
         if (i < n8) {
             float r[8], r2[8];
+            if (sizeof(T) == 2 && (OP == 0 || OP == 1 || OP == 4)) {
+                // bf16: the paired GELU the GEMM epilogues use (same bits)
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if (OP == 0) r[j] = gelu_fwd_f<T>(va[u][j]);
-                else if (OP == 1) r[j] = vb[u][j] * gelu_grad_f<T>(va[u][j]);
-                else if (OP == 2) r[j] = va[u][j] + vb[u][j];
-                else if (OP == 3) r[j] = va[u][j] * vb[u][j];
-                else gelu_both_f<T>(va[u][j], r[j], r2[j]);
+                for (int j = 0; j < 8; j += 2) {
+                    float g0, g1, d0, d1;
+                    tc::gelu_pair(va[u][j], va[u][j + 1], g0, g1, d0, d1);
+                    if (OP == 1) {
+                        r[j] = vb[u][j] * d0;
+                        r[j + 1] = vb[u][j + 1] * d1;
+                    } else {
+                        r[j] = g0;
+                        r[j + 1] = g1;
+                        r2[j] = d0;
+                        r2[j + 1] = d1;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    if (OP == 0) r[j] = gelu_fwd_f<T>(va[u][j]);
+                    else if (OP == 1) r[j] = vb[u][j] * gelu_grad_f<T>(va[u][j]);
+                    else if (OP == 2) r[j] = va[u][j] + vb[u][j];
+                    else if (OP == 3) r[j] = va[u][j] * vb[u][j];
+                    else gelu_both_f<T>(va[u][j], r[j], r2[j]);
+                }
             }
             store8(out + i * 8, r);
             if (OP == 4) store8(b + i * 8, r2);
@@ -538,35 +557,39 @@ int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n
 #define BIAS_ROWS_PER_CHUNK 128
 
 // Stage 1: block (32 column vectors) x (8 row lanes) sums one chunk of rows
-// for 256 columns into partial[chunk][c].
+// for 256 columns into partial[chunk][c]; the blocks of one column slab
+// step over the chunks by gridDim.y (at most 65535 of them per launch).
 template <typename T>
 __global__ void __launch_bounds__(256) bias_partial_kernel(float* __restrict__ partial, const T* __restrict__ dy,
-                                                           int N, int C) {
+                                                           int N, int C, int chunks) {
     __shared__ float sm[8][256 + 8];
     const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
     const int c = (blockIdx.x * 32 + tx) * 8;
-    const int r0 = blockIdx.y * BIAS_ROWS_PER_CHUNK;
-    const int r1 = min(N, r0 + BIAS_ROWS_PER_CHUNK);
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (c < C) {
+    for (int chunk = blockIdx.y; chunk < chunks; chunk += gridDim.y) {
+        const int r0 = chunk * BIAS_ROWS_PER_CHUNK;
+        const int r1 = min(N, r0 + BIAS_ROWS_PER_CHUNK);
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (c < C) {
 #pragma unroll 4
-        for (int r = r0 + ty; r < r1; r += 8) {
-            float v[8];
-            load8_stream(dy + (int64_t)r * C + c, v);
+            for (int r = r0 + ty; r < r1; r += 8) {
+                float v[8];
+                load8_stream(dy + (int64_t)r * C + c, v);
 #pragma unroll
-            for (int j = 0; j < 8; j++) acc[j] += v[j];
+                for (int j = 0; j < 8; j++) acc[j] += v[j];
+            }
         }
-    }
+        __syncthreads();  // the previous chunk's sums have been read
 #pragma unroll
-    for (int j = 0; j < 8; j++) sm[ty][tx * 8 + j] = acc[j];
-    __syncthreads();
-    const int col = threadIdx.x;  // 0..255 within this block's slab
-    const int gc = blockIdx.x * 256 + col;
-    if (gc < C) {
-        float s = 0.f;
+        for (int j = 0; j < 8; j++) sm[ty][tx * 8 + j] = acc[j];
+        __syncthreads();
+        const int col = threadIdx.x;  // 0..255 within this block's slab
+        const int gc = blockIdx.x * 256 + col;
+        if (gc < C) {
+            float s = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; k++) s += sm[k][col];
-        partial[(int64_t)blockIdx.y * C + gc] = s;
+            for (int k = 0; k < 8; k++) s += sm[k][col];
+            partial[(int64_t)chunk * C + gc] = s;
+        }
     }
 }
 
@@ -617,18 +640,18 @@ int launch_colsum(float* out, float* out2, int split, const float* in, int R, in
 }
 
 size_t bias_backward_scratch(int N, int C) {
-    const size_t chunks = (N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
+    const size_t chunks = ((size_t)N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
     return chunks * C * 4;
 }
 
 int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s,
                          int accumulate) {
-    const int chunks = (N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
-    dim3 grid((C + 255) / 256, chunks);
+    const int chunks = (int)(((int64_t)N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK);
+    dim3 grid((C + 255) / 256, chunks < 65535 ? chunks : 65535);
     if (dtype == GPT2_MODE_BF16)
-        bias_partial_kernel<bf16><<<grid, 256, 0, s>>>((float*)scratch, (const bf16*)dy, N, C);
+        bias_partial_kernel<bf16><<<grid, 256, 0, s>>>((float*)scratch, (const bf16*)dy, N, C, chunks);
     else
-        bias_partial_kernel<float><<<grid, 256, 0, s>>>((float*)scratch, (const float*)dy, N, C);
+        bias_partial_kernel<float><<<grid, 256, 0, s>>>((float*)scratch, (const float*)dy, N, C, chunks);
     launch_colsum3(dbias, nullptr, nullptr, C, (const float*)scratch, chunks, C, s, accumulate);
     return 2;
 }

@@ -48,6 +48,8 @@ constexpr int BK = 64;               // 64 bf16 = 128 bytes = one swizzle row
 constexpr int NUM_THREADS = 320;     // 10 warps
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;
+constexpr int BIAS_WARP0 = EPI_WARP0 + EPI_WARPS;  // bias-gradient variant: two more warps
+constexpr int NUM_THREADS_BG = NUM_THREADS + 64;
 
 template <int BN> struct TileCfg {
     static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
@@ -82,6 +84,8 @@ struct GemmArgs {
     const float* a_scale;  // FP8 operands: device scalars by which the codes of A and of B are
     const float* b_scale;  // multiplied back (the product scales the accumulator)
     int a_fmt, b_fmt;      // FP8 operands: their formats (0 e4m3, 1 e5m2)
+    float* dbias;          // bias-gradient variant: row sums of A, [M] fp32 (written when no partials)
+    float* dbias_partial;  // ... with partials: [units][BM], the reduce kernel adds them in split order
 };
 
 // One unit of a CTA's work: k-blocks [kb0, kb1) of a tile; z = partial slot.
@@ -130,31 +134,50 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
                                           const CUtensorMap* mapD2, const uint4 (&aux)[4], int x, int y, int z,
                                           int ncols_valid, int lane, float alpha = 1.f) {
     float f[32];
+    if (!F8 && bias_s) {
 #pragma unroll
-    for (int j = 0; j < 32; j++)
-        f[j] = (F8 ? __uint_as_float(r[j]) * alpha : __uint_as_float(r[j])) + (bias_s ? bias_s[j] : 0.f);
-    if (EPI != EPI_NONE) {
-        // the linear output rounded to bf16, as a separate pass would read it
-#pragma unroll
-        for (int j = 0; j < 32; j++) f[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
-        if (EPI == EPI_MUL) {
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&aux[q]);
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    f[q * 8 + 2 * i] *= __low2float(h[i]);
-                    f[q * 8 + 2 * i + 1] *= __high2float(h[i]);
-                }
-            }
-            stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
-        } else {
-            float gd[32];
-#pragma unroll
-            for (int j = 0; j < 32; j++) gelu_both_f<bf16>(f[j], f[j], gd[j]);
-            stage_store_bf16(gd, stage, stage_addr, mapD, x, y, z, lane);  // gelu'(u), kept for the backward
-            stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane);   // gelu(u)
+        for (int j = 0; j < 32; j += 2) {  // + bias, in pairs
+            const uint64_t v = f2_add(f2_pack(r[j], r[j + 1]), *reinterpret_cast<const uint64_t*>(bias_s + j));
+            f2_unpack(v, f[j], f[j + 1]);
         }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+            f[j] = (F8 ? __uint_as_float(r[j]) * alpha : __uint_as_float(r[j])) + (bias_s ? bias_s[j] : 0.f);
+    }
+    if (EPI == EPI_MUL) {
+        // the linear output rounded to bf16 (as a separate pass would read it)
+        // times gelu'(u): the exact product of two bf16 values rounded once,
+        // which is one bf16 pair multiply
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint32_t* h = reinterpret_cast<const uint32_t*>(&aux[q]);
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                uint32_t xb, pr;
+                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(xb) : "f"(f[q * 8 + 2 * i + 1]), "f"(f[q * 8 + 2 * i]));
+                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(pr) : "r"(xb), "r"(h[i]));
+                o[i] = pr;
+            }
+            stage16(stage, lane, q, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tma_store_3d(mapD, stage_addr, x, y, z);
+    } else if (EPI == EPI_GELU) {
+        // u = the linear output rounded to bf16, then its GELU and GELU'
+        float gd[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            uint32_t ub;
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(ub) : "f"(f[j + 1]), "f"(f[j]));
+            gelu_pair(__uint_as_float(ub << 16), __uint_as_float(ub & 0xFFFF0000u), f[j], f[j + 1], gd[j], gd[j + 1]);
+        }
+        stage_store_bf16(gd, stage, stage_addr, mapD, x, y, z, lane);  // gelu'(u), kept for the backward
+        stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane);   // gelu(u)
     } else if (!fp32_out) {
         stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
     } else {
@@ -177,15 +200,29 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
 
 // ---------------------------------------------------------------- kernel
 
+// Failure-path test switch (off unless gemm_tc_stall_for_test() sets it on
+// the current device): the MMA warp first waits on a barrier that nothing
+// arrives at, so its bounded wait runs out and the kernel takes its abort
+// path (status bit, abort flag, bounded drain of the copies in flight, TMEM
+// freed, return) on otherwise normal inputs.
+static __device__ int stall_for_test = 0;
+
 // F8: FP8 operands, e4m3 or e5m2 each (K-major only): a k-block is 128 values,
 // four K = 32 MMAs of kind::f8f6f4, and the epilogue scales the accumulator by
 // a_scale * b_scale.
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// BG: the weight gradient dW = dY^T X (A = dY read MN-major) also forms the
+// bias gradient db[m] = sum_k A(m, k), the row sums of A, while the A tiles
+// pass through shared memory: two more warps (10 and 11, one per 64-row half
+// of the tile) read each A stage of the units of the first column tile
+// before it is released (the stages' empty barriers count them), summing
+// each k-block in fp32 and adding the block sums in k order (deterministic).
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false, bool BG = false>
+__global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const GemmArgs g) {
     static_assert(!F8 || (!A_MN && !B_MN && EPI == EPI_NONE), "FP8 operands: K-major, plain epilogue");
+    static_assert(!BG || (A_MN && !F8 && EPI == EPI_NONE), "bias gradient: the weight-gradient layout");
     constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
@@ -207,19 +244,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (2 * S + 5));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * S + 5) + 4);
+    const uint32_t stall_bar = bars + 8u * (2 * S + 6);  // never arrived at (failure-path test)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), BG ? 3 : 1);  // the MMAs' commit (+ the two bias warps)
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -296,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            if (*(volatile int*)&stall_for_test) ok = warp_wait(stall_bar, 0, abort_flag, g.status);
             Work w;
             for (int idx = 0; ok && get_work(g, idx, w); idx++) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
@@ -336,7 +376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (leader) tc_commit(drain_bar);
             mbar_drain(drain_bar, 0, g.status);
         }
-    } else {
+    } else if (warp < BIAS_WARP0) {
         // ---------------------------------------------------- epilogue (warps 2..9)
         const int ew = warp - EPI_WARP0;         // 0..7
         const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
@@ -432,6 +472,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (lane == 0) bulk_wait_all();  // this warp's stores are complete
         __syncwarp();
+    } else if (BG) {
+        // ---------------------------------------------------- bias gradient (warps 10, 11)
+        // Warp bw sums rows m = bw * 64 + 2 * lane (+1) of A over k: in the MN-major
+        // stage its 64 rows are the 64-value chunk bw, 64 k-rows of 128 bytes with
+        // the 128-byte swizzle (16-byte unit u of k-row r at u ^ (r & 7)); this lane's
+        // two values are bytes 4 * lane .. +3 of each k-row.
+        const int bw = warp - BIAS_WARP0;
+        const uint32_t unit = (uint32_t)lane >> 2, within = ((uint32_t)lane & 3u) << 2;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        Work w;
+        for (int idx = 0; ok && get_work(g, idx, w); idx++) {
+            const bool bias_unit = (w.tile % g.n_tiles) == 0;
+            uint64_t total = 0;  // the two rows' sums, paired
+            for (int kb = w.kb0; kb < w.kb1; kb++) {
+                if (!warp_wait(full_bar(stage), phase, abort_flag, g.status)) {
+                    ok = false;
+                    break;
+                }
+                if (bias_unit) {
+                    const uint8_t* chunk = gbase + stage * Cfg::A_BYTES + bw * (64 * 128);
+                    uint64_t even = 0, odd = 0;
+#pragma unroll 8
+                    for (int r = 0; r < BK; r += 2) {
+                        const uint32_t v0 =
+                            *reinterpret_cast<const uint32_t*>(chunk + r * 128 + (((unit ^ (r & 7)) << 4) | within));
+                        const uint32_t v1 = *reinterpret_cast<const uint32_t*>(
+                            chunk + (r + 1) * 128 + (((unit ^ ((r + 1) & 7)) << 4) | within));
+                        even = f2_add(even, f2_pack(v0 << 16, v0 & 0xFFFF0000u));
+                        odd = f2_add(odd, f2_pack(v1 << 16, v1 & 0xFFFF0000u));
+                    }
+                    total = f2_add(total, f2_add(even, odd));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));  // this warp is done with the stage
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok || !bias_unit) continue;
+            float t0, t1;
+            f2_unpack(total, t0, t1);
+            const int ml = bw * 64 + 2 * lane, m = (w.tile / g.n_tiles) * BM + ml;
+            if (g.partials) {
+                g.dbias_partial[(int64_t)w.z * BM + ml] = t0;
+                g.dbias_partial[(int64_t)w.z * BM + ml + 1] = t1;
+            } else {
+                if (m < g.M) g.dbias[m] = t0;
+                if (m + 1 < g.M) g.dbias[m + 1] = t1;
+            }
+        }
     }
 
     tc_fence_before();
@@ -447,13 +540,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Split-K reduce: D[m][n] (fp32) = bias[n] (if any) + the partial tiles of
 // the tile of (m, n), added in split order; with accumulate, added to D's
 // current value. 8 consecutive columns per thread (N and BN are multiples of 8).
+// With a bias gradient (dbias != null), the thread of each row's first
+// eight columns also sets dbias[m] (+)= the row's bias partials of the first
+// column tile, in split order.
 __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ D, const float* __restrict__ partial,
                                                            const bf16* __restrict__ bias, int M, int N, int BN,
-                                                           int n_tiles, int splits, int accumulate) {
+                                                           int n_tiles, int splits, int accumulate,
+                                                           float* __restrict__ dbias,
+                                                           const float* __restrict__ dbias_partial) {
     // 32-bit element index (the launcher keeps M * N < 2^31)
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= M * N) return;
     const int m = i / N, n = i - m * N;
+    if (dbias && n == 0) {
+        const float* bp = dbias_partial + (int64_t)(m / BM) * n_tiles * splits * BM + m % BM;
+        float b = accumulate ? dbias[m] : 0.f;
+        for (int sp = 0; sp < splits; sp++) b += bp[sp * BM];
+        dbias[m] = b;
+    }
     const int64_t tile = (int64_t)(m / BM) * n_tiles + n / BN;
     const int64_t tile_elems = (int64_t)BM * BN;
     const float* p = partial + tile * splits * tile_elems + (int64_t)(m % BM) * BN + n % BN;
@@ -573,17 +677,19 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
     return p;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false, bool BG = false>
 void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                const GemmArgs& args, int grid, cudaStream_t s) {
     using Cfg = TileCfg<BN>;
-    static bool configured = false;
-    if (!configured) {
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // once per process; a function-local static is initialised thread-safely
+    static const bool configured = [] {
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8, BG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES);
-        configured = true;
-    }
-    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
+        return true;
+    }();
+    (void)configured;
+    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8, BG>
+        <<<grid, BG ? NUM_THREADS_BG : NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
 }
 
 // The operand layouts, and the fused epilogues only where the step uses them:
@@ -612,17 +718,31 @@ bool launch_tc_layout(int epi, int a_mn, int b_mn, const CUtensorMap& ma, const 
 
 }  // namespace
 
+int gemm_tc_set_wait_limit(long long cycles) { return set_wait_limit(cycles); }
+
+int gemm_tc_stall_for_test(int on) {
+    const int v = on ? 1 : 0;
+    return cudaMemcpyToSymbol(stall_for_test, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
+}
+
 size_t matmul_tc_scratch(int M, int N, int K, int d_fp32, int accumulate) {
     Plan p = make_plan(M, N, K, d_fp32);
     return p.splits > 1 || (d_fp32 && accumulate) ? (size_t)p.units * BM * p.bn * 4 : 0;
 }
 
+size_t matmul_bias_grad_tc_scratch(int M, int N, int K, int accumulate) {
+    Plan p = make_plan(M, N, K, 1);
+    return p.splits > 1 || accumulate ? (size_t)p.units * BM * (p.bn + 1) * 4 : 0;
+}
+
 namespace {
 
-// D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
+// D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc. With
+// dbias (the weight-gradient layout, fp32 out): also dbias = row sums of A.
 int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
               int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s,
-              int accumulate = 0) {
+              int accumulate = 0, float* dbias = nullptr) {
+    if (dbias && (epi != EPI_NONE || !d_fp32 || !a_mn || !b_mn || bias)) return GPT2_ERR_ARG;
     Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
@@ -640,6 +760,9 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     GemmArgs g;
     g.a_scale = g.b_scale = nullptr;
     g.a_fmt = g.b_fmt = 0;
+    g.dbias = dbias;
+    // bias partials after the tile partials: [units][BM]
+    g.dbias_partial = dbias && partials ? (float*)scratch + (size_t)p.units * BM * p.bn : nullptr;
     g.bias = partials ? nullptr : bias;
     g.aux = aux;
     g.status = status;
@@ -653,8 +776,12 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     g.n_tiles = p.n_tiles;
     g.units = p.units;
     g.num_kb = p.num_kb;
-    bool launched;
-    if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
+    bool launched = true;
+    if (dbias) {
+        if (p.bn == 128) launch_tc<128, true, true, EPI_NONE, false, true>(ma, mb, md, md2, g, p.grid, s);
+        else if (p.bn == 192) launch_tc<192, true, true, EPI_NONE, false, true>(ma, mb, md, md2, g, p.grid, s);
+        else launch_tc<256, true, true, EPI_NONE, false, true>(ma, mb, md, md2, g, p.grid, s);
+    } else if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else if (p.bn == 192) launched = launch_tc_layout<192>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else launched = launch_tc_layout<256>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     if (!launched) return GPT2_ERR_ARG;
@@ -662,7 +789,8 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         const int64_t MN = (int64_t)M * N;
         const int blocks = (int)((MN / 8 + 255) / 256);
         split_reduce_kernel<<<blocks, 256, 0, s>>>((float*)D, (const float*)scratch, (const bf16*)bias, M, N, p.bn,
-                                                   p.n_tiles, p.splits, accumulate && d_fp32 ? 1 : 0);
+                                                   p.n_tiles, p.splits, accumulate && d_fp32 ? 1 : 0, dbias,
+                                                   g.dbias_partial);
         return 2;
     }
     return 1;
@@ -703,6 +831,7 @@ int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale
     g.b_scale = b_scale;
     g.a_fmt = a_fmt;
     g.b_fmt = b_fmt;
+    g.dbias = g.dbias_partial = nullptr;
     if (p.bn == 128) launch_tc<128, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
     else if (p.bn == 192) launch_tc<192, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
     else launch_tc<256, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
@@ -713,6 +842,12 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
                      int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate) {
     return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s,
                      accumulate);
+}
+
+int launch_matmul_bias_grad_tc(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
+                               void* scratch, int* status, cudaStream_t s, int accumulate) {
+    return matmul_tc(EPI_NONE, dW, nullptr, nullptr, 1, dY, 1, X, 1, nullptr, M, N, K, scratch, status, s, accumulate,
+                     dbias);
 }
 
 int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,

@@ -69,9 +69,10 @@ int launch_grad_norm(float* norm_out, float* partial, const float* g, int64_t n,
 
 int launch_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
                              int* status, cudaStream_t s);
+// bf16 backward; D ([B, H, T] fp32 scratch) receives rowsum(dO * O).
 int launch_attention_backward_tc(__nv_bfloat16* dqkv, const __nv_bfloat16* dout, const __nv_bfloat16* qkv,
-                                 const float* lse, const float* D, int B, int T, int C, int H, int* status,
-                                 cudaStream_t s);
+                                 const __nv_bfloat16* o, const float* lse, float* D, int B, int T, int C, int H,
+                                 int* status, cudaStream_t s);
 int launch_attention_forward_tc(__nv_bfloat16* o, float* lse, const __nv_bfloat16* qkv, int B, int T, int C, int H,
                                 int* status, cudaStream_t s);
 size_t attention_backward_scratch(int B, int T, int H);
@@ -108,5 +109,21 @@ int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, int
 // accumulate (fp32 D only): D += the product instead of D = it; the scratch
 // size then covers the partial tiles that route through the reduce kernel.
 size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32, int accumulate = 0);
+// bf16 weight gradient with its bias gradient on the tensor cores: dW[M,N]
+// (fp32, (+)=) = dY^T X with dY [K, M] and X [K, N] (both read MN-major), and
+// dbias[M] (fp32, (+)=) = column sums of dY; scratch of
+// matmul_bias_grad_tc_scratch() bytes.
+size_t matmul_bias_grad_tc_scratch(int M, int N, int K, int accumulate);
+int launch_matmul_bias_grad_tc(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
+                               void* scratch, int* status, cudaStream_t s, int accumulate);
 int launch_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias,
                   int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate = 0);
+
+// Failure-path test hooks (current device): each translation unit with
+// bounded tcgen05 / bulk-copy waits sets its own wait bound (cycles <= 0:
+// the default); the GEMM's stall switch makes its MMA warp wait on a barrier
+// nothing arrives at. 0 or -1 on a CUDA error.
+int gemm_tc_set_wait_limit(long long cycles);
+int attention_tc_set_wait_limit(long long cycles);
+int classifier_set_wait_limit(long long cycles);
+int gemm_tc_stall_for_test(int on);

@@ -221,6 +221,7 @@ size_t plan(const gpt2_config* c, gpt2* m) {
         need(matmul_scratch(dt, outs[k], ins[k], iBT, 1, 1));    // dW (also when accumulating)
         need(matmul_scratch(dt, iBT, ins[k], outs[k], 0));       // dX
         need(bias_backward_scratch(iBT, outs[k]));
+        if (dt == GPT2_MODE_BF16) need(matmul_bias_grad_tc_scratch(outs[k], ins[k], iBT, 1));  // dW with db
     }
     need(matmul_scratch(dt, iVp, iC, iBT, 1, 1));
     need(matmul_scratch(dt, iBT, iC, iVp, 0));
@@ -386,6 +387,13 @@ int linear_fwd(gpt2* m, void* y, const void* x, int wi, int bi, int BT, int in, 
 // dx = dy W, dW = dy^T x, db = column sums of dy.
 int linear_bwd(gpt2* m, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in, int out) {
     TRY(op_matmul(m, dx, 0, dy, 0, P(m, wi), 1, nullptr, BT, in, out));
+    if (bi >= 0 && m->dtype == GPT2_MODE_BF16) {
+        // the bias gradient comes out of the weight-gradient GEMM (row sums of dY^T)
+        Op op(m, GPT2_K_MATMUL);
+        return op.done(launch_matmul_bias_grad_tc(G(m, wi), G(m, bi), dy, x, out, in, BT, m->scratch, m->status,
+                                                  m->stream, m->grad_accum),
+                       2.0 * out * in * BT);
+    }
     TRY(op_matmul(m, G(m, wi), 1, dy, 1, x, 1, nullptr, out, in, BT, m->grad_accum));
     if (bi >= 0) {
         Op op(m, GPT2_K_BIAS_BWD);
@@ -725,8 +733,29 @@ int step_body(gpt2* m, int B, int T, const gpt2_adamw_config* c) {
 
 }  // namespace
 
+namespace {
+
+// gpt2_step with the token and target batches read from device memory
+// (cudaMemcpyDeviceToDevice) or host memory (cudaMemcpyHostToDevice).
+int step_impl(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T, const gpt2_adamw_config* c,
+              float* loss_out, cudaMemcpyKind kind);
+
+}  // namespace
+
 int gpt2_step(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T, const gpt2_adamw_config* c,
               float* loss_out) {
+    return step_impl(m, d_tokens, d_targets, B, T, c, loss_out, cudaMemcpyDeviceToDevice);
+}
+
+int gpt2_step_host(gpt2_t* m, const int32_t* h_tokens, const int32_t* h_targets, int B, int T,
+                   const gpt2_adamw_config* c, float* loss_out) {
+    return step_impl(m, h_tokens, h_targets, B, T, c, loss_out, cudaMemcpyHostToDevice);
+}
+
+namespace {
+
+int step_impl(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int B, int T, const gpt2_adamw_config* c,
+              float* loss_out, cudaMemcpyKind kind) {
     if (!m || !d_tokens || !d_targets || !loss_out || !c || B < 1 || T < 1 || B > m->maxB || T > m->maxT)
         return GPT2_ERR_ARG;
     if (c->t < 1 || !(c->beta1 >= 0.f && c->beta1 < 1.f) || !(c->beta2 >= 0.f && c->beta2 < 1.f) || !(c->eps >= 0.f) ||
@@ -743,8 +772,8 @@ int gpt2_step(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int 
     const size_t bt = (size_t)B * T * 4;
     if (cudaMemcpyAsync(m->hp_dev, hp, sizeof(hp), cudaMemcpyHostToDevice, m->stream) != cudaSuccess ||
         cudaMemsetAsync(m->status, 0, sizeof(int), m->stream) != cudaSuccess ||
-        cudaMemcpyAsync(m->tokens, d_tokens, bt, cudaMemcpyDeviceToDevice, m->stream) != cudaSuccess ||
-        cudaMemcpyAsync(m->targets, d_targets, bt, cudaMemcpyDeviceToDevice, m->stream) != cudaSuccess)
+        cudaMemcpyAsync(m->tokens, d_tokens, bt, kind, m->stream) != cudaSuccess ||
+        cudaMemcpyAsync(m->targets, d_targets, bt, kind, m->stream) != cudaSuccess)
         return GPT2_ERR_CUDA;
     const gpt2::StepKey key{B, T, m->grad_accum, c->max_grad_norm > 0.f ? 1 : 0, c->decay_mask, c->max_grad_norm};
     if (!(key == m->step_key)) {
@@ -808,6 +837,8 @@ int gpt2_step(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int 
     m->state = 3;
     return GPT2_OK;
 }
+
+}  // namespace
 
 int gpt2_grad_sumsq_range(gpt2_t* m, int64_t begin, int64_t count, float* out) {
     if (!m || !out || begin < 0 || count < 4 || count % 4 != 0 || begin % 4 != 0 || begin + count > m->np)

@@ -9,6 +9,19 @@
 
 namespace tc {
 
+// The bound of every wait below, in clock cycles: GPT2_WAIT_LIMIT_CYCLES
+// (about 2 s) unless a caller lowers it for the current device with
+// set_wait_limit() (the failure-path test does, for one call). Each
+// translation unit that includes this header has its own copy.
+static __device__ long long wait_limit_cycles = GPT2_WAIT_LIMIT_CYCLES;
+
+// Host side: sets this translation unit's bound on the current device
+// (cycles <= 0: the default). Returns 0 or -1 on a CUDA error.
+[[maybe_unused]] static int set_wait_limit(long long cycles) {
+    const long long v = cycles > 0 ? cycles : GPT2_WAIT_LIMIT_CYCLES;
+    return cudaMemcpyToSymbol(wait_limit_cycles, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
+}
+
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -36,11 +49,12 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
+    const long long limit = *(volatile long long*)&wait_limit_cycles;
     for (uint32_t it = 1;; it++) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
+            if (clock64() - t0 > limit) {
                 set_status(status, GPT2_FLAG_TIMEOUT);
                 *abort_flag = 1;
                 return false;
@@ -65,8 +79,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait used while shutting down (ignores the abort flag).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* status) {
     const long long t0 = clock64();
+    const long long limit = *(volatile long long*)&wait_limit_cycles;
     while (!mbar_try(bar, parity)) {
-        if (clock64() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
+        if (clock64() - t0 > limit) {
             set_status(status, GPT2_FLAG_TIMEOUT);
             return;
         }
@@ -159,6 +174,34 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// GELU (tanh form, through the logistic of 2y as gelu_both_f<bf16>) of a pair
+// of values with paired fp32 arithmetic: g = gelu(u), d = gelu'(u), where
+// s = 1 / (1 + 2^z), z = -2 log2(e) y, y = sqrt(2/pi) (u + 0.044715 u^3),
+// g = u s and d = s + u s (1 - s) 2 sqrt(2/pi) (1 + 3 * 0.044715 u^2).
+// The exponential and the reciprocal are the hardware approximations. Used by
+// every bf16 GELU (the GEMM epilogues and the elementwise kernel), so fused
+// and separate passes give the same bits.
+__device__ __forceinline__ void gelu_pair(float u0, float u1, float& g0, float& g1, float& d0, float& d1) {
+    constexpr float kz = (float)(-2.0 * 1.4426950408889634 * 0.7978845608028654);
+    constexpr float kza = (float)(-2.0 * 1.4426950408889634 * 0.7978845608028654 * 0.044715);
+    constexpr float kw = (float)(2.0 * 0.7978845608028654);
+    constexpr float kwa = (float)(2.0 * 0.7978845608028654 * 3.0 * 0.044715);
+    const uint64_t u = f2_pack(u0, u1);
+    const uint64_t uu = f2_mul(u, u);
+    const uint64_t z = f2_mul(u, f2_fma(uu, f2_pack(kza, kza), f2_pack(kz, kz)));
+    float z0, z1;
+    f2_unpack(z, z0, z1);
+    const uint64_t one = f2_pack(1.f, 1.f);
+    float e0, e1;
+    f2_unpack(f2_add(f2_pack(ex2_approx(z0), ex2_approx(z1)), one), e0, e1);
+    const uint64_t sv = f2_pack(__fdividef(1.f, e0), __fdividef(1.f, e1));
+    const uint64_t g = f2_mul(u, sv);
+    const uint64_t w = f2_fma(uu, f2_pack(kwa, kwa), f2_pack(kw, kw));
+    const uint64_t d = f2_fma(f2_mul(g, w), f2_sub(one, sv), sv);
+    f2_unpack(g, g0, g1);
+    f2_unpack(d, d0, d1);
 }
 
 // Issue a load of 32 consecutive fp32 accumulator columns of this thread's

@@ -69,6 +69,8 @@ _SIGNATURES = {
     "gpt2_grad_sumsq_range": (c_int, [c_void_p, ctypes.c_int64, ctypes.c_int64, POINTER(ctypes.c_float)]),
     "gpt2_flat_params": (c_int64, [c_void_p]),
     "gpt2_step": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, POINTER(gpt2_adamw_config), POINTER(c_float)]),
+    "gpt2_step_host": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, POINTER(gpt2_adamw_config),
+                               POINTER(c_float)]),
     "gpt2_lr_cosine": (c_float, [c_int, c_int, c_int, c_float, c_float]),
     "gpt2_strerror": (c_char_p, [c_int]),
     "gpt2_num_tensors": (c_int, [c_void_p]),
@@ -83,6 +85,11 @@ _SIGNATURES = {
     "gpt2_family_time": (c_int, [c_void_p, c_int, POINTER(c_double)]),
     "gpt2_reset_stats": (c_int, [c_void_p]),
     # gpt2_ops.h
+    "gpt2_op_matmul_bias_grad_scratch": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "gpt2_op_matmul_bias_grad": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                         c_void_p, c_size_t, c_void_p, c_void_p]),
+    "gpt2_debug_set_wait_limit": (c_int, [c_int64]),
+    "gpt2_debug_stall_matmul": (c_int, [c_int]),
     "gpt2_op_encoder_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                         c_void_p, c_void_p]),
     "gpt2_op_encoder_backward_scratch": (c_size_t, [c_int, c_int, c_int]),
@@ -271,6 +278,19 @@ class GPT2:
                                  ctypes.byref(loss)), "gpt2_step")
         return loss.value
 
+    def step_host(self, tokens, targets, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1,
+                  grad_scale=1.0, max_grad_norm=0.0, decay_mask=False) -> float:
+        """gpt2_step_host: gpt2_step with the batch in host memory, copied to the device
+        by the library. tokens/targets: int32 CPU tensors [B, T] (contiguous; pinned
+        for asynchronous copies)."""
+        B, T = tokens.shape
+        c = gpt2_adamw_config(lr, beta1, beta2, eps, weight_decay, t, grad_scale, max_grad_norm,
+                              int(bool(decay_mask)))
+        loss = c_float(0.0)
+        check(self.lib.gpt2_step_host(self.h, tokens.data_ptr(), targets.data_ptr(), B, T, ctypes.byref(c),
+                                      ctypes.byref(loss)), "gpt2_step_host")
+        return loss.value
+
     def adamw_step_shard(self, begin, count, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, t=1,
                          grad_scale=1.0, decay_mask=False):
         """gpt2_adamw_step_shard: AdamW on the flat parameter elements [begin, begin + count)."""
@@ -430,6 +450,18 @@ def gpt2_op_matmul(D, A, a_mn, B, b_mn, M, N, K, bias=None, status=None, stream=
     sc = _scratch(lib.gpt2_op_matmul_scratch(dt, M, N, K, d_fp32))
     check(lib.gpt2_op_matmul(dt, _p(D), d_fp32, _p(A), int(a_mn), _p(B), int(b_mn), _p(bias), M, N, K, _p(sc),
                              sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul")
+    return sc
+
+
+def gpt2_op_matmul_bias_grad(dW, dbias, dY, X, accumulate=False, status=None, stream=None):
+    """dW (fp32 [M,N]) (+)= dY^T X and dbias (fp32 [M]) (+)= column sums of dY, with
+    dY bf16 [K,M] and X bf16 [K,N], in one tensor-core pass."""
+    K, M = dY.shape
+    N = X.shape[1]
+    lib = load_library()
+    sc = _scratch(lib.gpt2_op_matmul_bias_grad_scratch(M, N, K, int(bool(accumulate))))
+    check(lib.gpt2_op_matmul_bias_grad(_p(dW), _p(dbias), _p(dY), _p(X), M, N, K, int(bool(accumulate)), _p(sc),
+                                       sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul_bias_grad")
     return sc
 
 

@@ -9,6 +9,13 @@
       up to the next one: one training step when the marker is its first kernel
   python -m step_gpt_train_gb300.ncu_summary raw <report.ncu-rep> [kernel-regex]
       the headline counters of each captured launch (needs the ncu CLI)
+  python -m step_gpt_train_gb300.ncu_summary step_traffic <launches.csv>
+      DRAM bytes of the matmul family over one training step, from a capture
+      (gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum)
+      of `opbench --ops step_gemms --warmup 0 --iters 1`: every gemm_tc_kernel
+      launch starts the next of the step's matmuls (in opbench.STEP_GEMMS
+      order), a split_reduce_kernel after it belongs to it, and each matmul's
+      bytes count as often as the step runs it
 """
 from __future__ import annotations
 
@@ -113,8 +120,43 @@ def raw(path: str, pattern: str = ".*") -> str:
     return "\n".join(out)
 
 
+def step_traffic(path: str) -> str:
+    from step_gpt_train_gb300.opbench import STEP_GEMMS
+    text = "".join(l for l in open(path) if not l.startswith("=="))
+    per_launch = collections.OrderedDict()
+    for r in csv.DictReader(io.StringIO(text)):
+        d = per_launch.setdefault(r.get("ID"), {"name": short_name(r["Kernel Name"])})
+        m, unit, val = r.get("Metric Name"), r.get("Metric Unit"), r.get("Metric Value")
+        if m == "dram__bytes_read.sum":
+            d["read"] = _bytes(val, unit)
+        elif m == "dram__bytes_write.sum":
+            d["write"] = _bytes(val, unit)
+    ops, cur = [], None
+    for d in per_launch.values():
+        if d["name"].startswith("gemm_tc_kernel"):
+            cur = {"launches": 0, "bytes": 0.0}
+            ops.append(cur)
+        elif not d["name"].startswith("split_reduce_kernel") or cur is None:
+            continue
+        cur["launches"] += 1
+        cur["bytes"] += d["read"] + d["write"]
+    names = list(STEP_GEMMS)
+    if len(ops) != len(names):
+        raise SystemExit(f"{len(ops)} matmuls captured, {len(names)} expected")
+    total_b = sum(STEP_GEMMS[n] * o["bytes"] for n, o in zip(names, ops))
+    total_l = sum(STEP_GEMMS[n] * o["launches"] for n, o in zip(names, ops))
+    out = [f"{'matmul':24s} {'per step':>8s} {'launches':>8s} {'DRAM MB':>10s}"]
+    for n, o in zip(names, ops):
+        out.append(f"{n:24s} {STEP_GEMMS[n]:8d} {o['launches']:8d} {o['bytes'] / 1e6:10.1f}")
+    out += ["", f"launches_per_step: {total_l}", f"traffic_bytes_per_step: {total_b:.0f}",
+            f"traffic_bytes_per_launch_full_step_avg: {total_b / total_l:.1f}"]
+    return "\n".join(out)
+
+
 if __name__ == "__main__":
-    if sys.argv[1] == "launches":
+    if sys.argv[1] == "step_traffic":
+        print(step_traffic(sys.argv[2]))
+    elif sys.argv[1] == "launches":
         print(launches(sys.argv[2], sys.argv[3] if len(sys.argv) > 3 else None,
                        int(sys.argv[4]) if len(sys.argv) > 4 else 1))
     else:

@@ -176,10 +176,12 @@ def test_launch_inventory_matches_page_table(torch_cuda):
     # Fusions: every residual join runs inside the LayerNorm forward that reads
     # its sum (24 of the 25), and the LayerNorm backwards, which add into the
     # residual gradient as in the table, also emit the bias gradients of the
-    # two projections whose outputs join the stream (2 of the 4 per layer).
+    # two projections whose outputs join the stream (2 of the 4 per layer);
+    # the other two (QKV and the MLP's first linear) come out of their
+    # weight-gradient matmuls, so no bias-gradient pass of its own remains.
     L = facts["n_layer"]
     assert st["residual_forward"]["calls"] == facts["residual_forward"] - 2 * L == 0
-    assert st["bias_backward"]["calls"] == facts["bias_backward"] - 2 * L
+    assert st["bias_backward"]["calls"] == facts["bias_backward"] - 4 * L == 0
     assert st["residual_backward"]["calls"] == 0
     assert model.launch_count() == sum(v["launches"] for v in st.values())
     model.close()
@@ -381,3 +383,27 @@ def test_errors_are_reported_not_trapped(torch_cuda):
     with pytest.raises(g.GPT2Error) as e:
         g.gpt2_init(good, 1, base + 256, need, torch.cuda.current_stream().cuda_stream)
     assert e.value.status == -7
+
+
+def test_step_host_equals_step(torch_cuda):
+    """gpt2_step_host (the batch in host memory, copied in by the library) gives
+    the losses and masters of gpt2_step on the same batches bit for bit, with
+    pinned and with pageable host buffers."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import TENSOR_MASTER
+    cfg = SMALL_BF16
+    tok, tgt = data.batches("zipf", 3, 100, 3, 11, vocab=1000)
+    dev_model, host_model = make_model(cfg), make_model(cfg)
+    for s in range(3):
+        lr = lr_at(s + 1, 5)
+        la = dev_model.step(torch.from_numpy(tok[s]).cuda(), torch.from_numpy(tgt[s]).cuda(), lr, t=s + 1, **HP)
+        ht, hg = torch.from_numpy(tok[s].copy()), torch.from_numpy(tgt[s].copy())
+        if s != 1:
+            ht, hg = ht.pin_memory(), hg.pin_memory()
+        lb = host_model.step_host(ht, hg, lr, t=s + 1, **HP)
+        assert la == lb, (s, la, lb)
+    a, b = dev_model.tensors(TENSOR_MASTER), host_model.tensors(TENSOR_MASTER)
+    dev_model.close()
+    host_model.close()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k

@@ -1,8 +1,9 @@
 """Degenerate sizes: every op of gpt2_ops.h called with an empty input, and
 attention over a single position.
 
-Collected last on purpose (like the other test_zz file), so that a run that
-stops at the first failure has already run every other test.
+Collected late on purpose (second to last, before the allocation-free entry
+point's file test_zz_no_alloc.py), so that a run that stops at the first
+failure has already run the per-kernel and whole-step tests.
 """
 import numpy as np
 import pytest
