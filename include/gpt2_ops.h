@@ -112,23 +112,6 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
                    int b_mn_major, const void* bias, int M, int N, int K, void* scratch,
                    size_t scratch_bytes, int* d_status, void* stream);
 
-/* Weight and bias gradient of a linear layer in one tensor-core pass (bf16):
- * the weight gradient of "matmul_backward" and the bias gradient
- * "matmul_backward_bias" of llm.c's kernel table ("State of the Union",
- * "Runtime, DRAM traffic, instructions"), fused:
- *   dW[m][n] = sum_k dY[k][m] X[k][n]   (fp32 [M,N], overwritten or added to)
- *   dbias[m] = sum_k dY[k][m]           (fp32 [M], overwritten or added to)
- * dY [K,M] and X [K,N] bf16 row-major (K = tokens, M = output features, N =
- * input features), 16-byte aligned; M, N, K multiples of 8. accumulate != 0
- * adds both results to what dW and dbias hold. The column sums of dY come
- * from the tensor cores (dY^T times a tile of ones, fp32 accumulation), in the
- * same pass that reads dY for dW. Scratch: gpt2_op_matmul_bias_grad_scratch()
- * bytes (partial sums of split K ranges). K = 0 is GPT2_ERR_ARG. */
-size_t gpt2_op_matmul_bias_grad_scratch(int M, int N, int K, int accumulate);
-int gpt2_op_matmul_bias_grad(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
-                             int accumulate, void* scratch, size_t scratch_bytes, int* d_status,
-                             void* stream);
-
 /* FP8 linear layer (the modded-nanogpt project page, "NanoGPT (124M) in 90
  * seconds", "How it works": FP8 for the MLP, the QKV projections and the
  * head), with per-tensor scaling to one of two 8-bit floating-point formats

@@ -48,26 +48,78 @@ constexpr uint32_t AT_TMEM_COLS = 256;     // S [0,128), O [128,192), P [192,256
 constexpr float AT_LN2 = 0.6931471805599453f;
 constexpr float AT_RESCALE = 8.f;          // log2 of the largest P before the reference max moves
 
+// Work schedule of the persistent attention kernels, over the nqt tiles of
+// each of BH batch-heads, where a tile's work (its key or query blocks)
+// depends on its rank u: rank 0 is the longest tile, rank nqt-1 the shortest,
+// and ranks u and nqt-1-u together make nqt+1 blocks. CTA c of G takes:
+//   first R pair rounds: in round r the pair r*G + c, i.e. batch-head
+//     (r*G + c) / (nqt/2) and ranks p and nqt-1-p with p = (r*G + c) % (nqt/2),
+//     the long one first: every CTA gets the same work, and the CTAs that run
+//     at the same time cover all tiles of G/(nqt/2) batch-heads, so the K/V
+//     (Q/dO) blocks they share are read while they are still in L2;
+//   then the tiles of the remaining batch-heads bh >= bh0, longest first
+//     (rank-major), round robin: t = j*G + c is rank t / NB of batch-head
+//     bh0 + t % NB (NB = BH - bh0).
+// The host chooses R one round short of all the pairs (R = 0 when nqt is odd
+// or there are fewer pairs than CTAs), which leaves the tail enough items to
+// even out.
+struct Sched {
+    int BH, nqt, R, bh0;
+};
+
+__host__ __device__ inline Sched make_sched(int BH, int nqt, int G) {
+    Sched s;
+    s.BH = BH;
+    s.nqt = nqt;
+    s.R = 0;
+    if (nqt % 2 == 0) {
+        const int np = nqt / 2;
+        const int rmax = (int)(((int64_t)BH * np) / G);
+        const int r = rmax >= 1 ? rmax - 1 : 0;
+        if (r > 0 && ((int64_t)r * G) % np == 0) s.R = r;
+    }
+    s.bh0 = s.nqt % 2 == 0 && s.R ? (int)(((int64_t)s.R * G) / (s.nqt / 2)) : 0;
+    return s;
+}
+
+// Item i of this CTA: the tile's rank u (0 = longest) and batch-head, or false.
+__device__ __forceinline__ bool sched_item(const Sched& s, int i, int& u, int& bh) {
+    const int G = gridDim.x, c = blockIdx.x;
+    if (i < 2 * s.R) {
+        const int np = s.nqt / 2;
+        const int pair = (i >> 1) * G + c;
+        bh = pair / np;
+        const int p = pair % np;
+        u = (i & 1) ? s.nqt - 1 - p : p;
+        return true;
+    }
+    const int NB = s.BH - s.bh0;
+    const int t = (i - 2 * s.R) * G + c;
+    if (t >= NB * s.nqt) return false;
+    u = t / NB;
+    bh = s.bh0 + t % NB;
+    return true;
+}
+
 struct FwdArgs {
     bf16* o;       // [B*T, C]
     float* lse;    // [B, H, T]
     int* status;
     int T, C, H;
     int nqt;       // 128-query tiles per sequence
-    int items;     // nqt * B * H
+    Sched sched;
     float scale_log2;  // log2(e) / sqrt(hd)
 };
 
-// Work item idx of the longest-first list: query tile and batch-head.
+// Work item i of this CTA: query tile (rank u is tile nqt-1-u: the last
+// query tile has the most key blocks) and batch-head.
 struct FItem {
     int qt, bh;
 };
 __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int i, FItem& it) {
-    const int idx = blockIdx.x + i * gridDim.x;
-    if (idx >= a.items) return false;
-    const int BH = a.items / a.nqt;
-    it.qt = a.nqt - 1 - idx / BH;
-    it.bh = idx % BH;
+    int u;
+    if (!sched_item(a.sched, i, u, it.bh)) return false;
+    it.qt = a.nqt - 1 - u;
     return true;
 }
 
@@ -417,9 +469,10 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
     a.C = C;
     a.H = H;
     a.nqt = (T + AT_M - 1) / AT_M;
-    a.items = a.nqt * B * H;
+    const int items = a.nqt * B * H;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)(C / H));
-    const int grid = a.items < 2 * gpt2_num_sms() ? a.items : 2 * gpt2_num_sms();  // persistent: two CTAs per SM
+    const int grid = items < 2 * gpt2_num_sms() ? items : 2 * gpt2_num_sms();  // persistent: two CTAs per SM
+    a.sched = make_sched(B * H, a.nqt, grid);
     attn_fwd_tc_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(map, a);
     return 1;
 }
@@ -478,6 +531,7 @@ struct BwdArgs {
     int* status;
     int B, T, C, H;
     int nqt;             // 128-row tiles per sequence
+    Sched sched;
     float scale_log2;    // log2(e) / sqrt(hd)
     float scale;         // 1 / sqrt(hd)
 };
@@ -506,24 +560,23 @@ __device__ __forceinline__ void stage_block_sw128(uint8_t* tile, int row, int ha
 }
 
 // -------------------------------------------------------------------------- schedule
-// Both kernels are persistent: CTA c takes the work items c, c + G, c + 2G, ...
-// (G = grid size) of a list ordered longest first, and its producer, MMA and
-// elementwise roles walk the same sequence of (item, block) steps, so the
-// operand rings run on across item boundaries instead of starting cold.
+// Both kernels are persistent: CTA c takes its work items from the schedule
+// of sched_item (pairs of a long and a short tile of one batch-head, then a
+// longest-first tail), and its producer, MMA and elementwise roles walk the
+// same sequence of (item, block) steps, so the operand rings run on across
+// item boundaries instead of starting cold.
 struct Item {
     int tile, bh, nblk;  // dK/dV: key tile, blocks tile..nqt-1; dQ: query tile, blocks 0..tile
 };
 
 template <bool DQ> __device__ __forceinline__ bool get_item(const BwdArgs& a, int i, Item& it) {
-    const int BH = a.B * a.H;
-    const int idx = blockIdx.x + i * gridDim.x;
-    if (idx >= a.nqt * BH) return false;
-    it.bh = idx % BH;
+    int u;
+    if (!sched_item(a.sched, i, u, it.bh)) return false;
     if (DQ) {
-        it.tile = a.nqt - 1 - idx / BH;
+        it.tile = a.nqt - 1 - u;  // the last query tile has the most key blocks
         it.nblk = it.tile + 1;
     } else {
-        it.tile = idx / BH;
+        it.tile = u;  // the first key tile has the most query blocks
         it.nblk = a.nqt - it.tile;
     }
     return true;
@@ -1345,6 +1398,7 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     a.scale_log2 = 1.4426950408889634f * a.scale;
     const int items = a.nqt * B * H;
     const int grid = items < gpt2_num_sms() ? items : gpt2_num_sms();  // persistent: one CTA per SM
+    a.sched = make_sched(B * H, a.nqt, grid);
     attn_bwd_dq_tc_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, mo, mx, md, a);
     attn_bwd_dkdv_tc_kernel<<<grid, BW_THREADS, DKDV_SMEM, s>>>(mq, mo, md, a);
     return 2;

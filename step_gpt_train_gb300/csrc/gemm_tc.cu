@@ -48,8 +48,6 @@ constexpr int BK = 64;               // 64 bf16 = 128 bytes = one swizzle row
 constexpr int NUM_THREADS = 320;     // 10 warps
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;
-constexpr int BIAS_WARP0 = EPI_WARP0 + EPI_WARPS;  // bias-gradient variant: two more warps
-constexpr int NUM_THREADS_BG = NUM_THREADS + 64;
 
 template <int BN> struct TileCfg {
     static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
@@ -81,24 +79,33 @@ struct GemmArgs {
     int n_tiles;         // ceil(N / BN)
     int units;           // m_tiles * n_tiles * splits
     int num_kb;          // ceil(K / k-block width): 64 bf16 or 128 e4m3 values (128 bytes either way)
+    int m_tiles;         // ceil(M / 128)
+    int group_n;         // tile raster: column tiles per group (n_tiles: plain row-major order)
     const float* a_scale;  // FP8 operands: device scalars by which the codes of A and of B are
     const float* b_scale;  // multiplied back (the product scales the accumulator)
     int a_fmt, b_fmt;      // FP8 operands: their formats (0 e4m3, 1 e5m2)
-    float* dbias;          // bias-gradient variant: row sums of A, [M] fp32 (written when no partials)
-    float* dbias_partial;  // ... with partials: [units][BM], the reduce kernel adds them in split order
 };
 
-// One unit of a CTA's work: k-blocks [kb0, kb1) of a tile; z = partial slot.
+// One unit of a CTA's work: k-blocks [kb0, kb1) of tile (mt, nt); z = partial slot.
 struct Work {
-    int tile, kb0, kb1, z;
+    int tile, mt, nt, kb0, kb1, z;
 };
 
-// The idx-th unit of this CTA, or false when there is none.
+// The idx-th unit of this CTA, or false when there is none. Tile t is the
+// t-th of a grouped raster: groups of group_n column tiles, each walked row
+// by row, so the CTAs at work at one time share a few B tiles through L2
+// instead of streaming all of B for every row of tiles (with group_n =
+// n_tiles this is the plain row-major order; units with partial tiles use it).
 __device__ __forceinline__ bool get_work(const GemmArgs& g, int idx, Work& w) {
     const int u = blockIdx.x + idx * gridDim.x;
     if (u >= g.units) return false;
     const int sp = u % g.splits;
     w.tile = u / g.splits;
+    const int per_group = g.m_tiles * g.group_n;
+    const int gi = w.tile / per_group, r = w.tile - gi * per_group;
+    const int gw = min(g.group_n, g.n_tiles - gi * g.group_n);
+    w.mt = r / gw;
+    w.nt = gi * g.group_n + r % gw;
     w.kb0 = sp * g.kbs;
     w.kb1 = min(g.num_kb, w.kb0 + g.kbs);
     w.z = u;
@@ -146,27 +153,21 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
             f[j] = (F8 ? __uint_as_float(r[j]) * alpha : __uint_as_float(r[j])) + (bias_s ? bias_s[j] : 0.f);
     }
     if (EPI == EPI_MUL) {
-        // the linear output rounded to bf16 (as a separate pass would read it)
-        // times gelu'(u): the exact product of two bf16 values rounded once,
-        // which is one bf16 pair multiply
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+        // the linear output rounded to bf16 (as a separate pass would read it),
+        // times gelu'(u): the product of two bf16 values is exact in fp32 and
+        // rounds once when staged
+#pragma unroll
+        for (int j = 0; j < 32; j++) f[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            const uint32_t* h = reinterpret_cast<const uint32_t*>(&aux[q]);
-            uint32_t o[4];
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&aux[q]);
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                uint32_t xb, pr;
-                asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(xb) : "f"(f[q * 8 + 2 * i + 1]), "f"(f[q * 8 + 2 * i]));
-                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(pr) : "r"(xb), "r"(h[i]));
-                o[i] = pr;
+                f[q * 8 + 2 * i] *= __low2float(h[i]);
+                f[q * 8 + 2 * i + 1] *= __high2float(h[i]);
             }
-            stage16(stage, lane, q, make_uint4(o[0], o[1], o[2], o[3]));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tma_store_3d(mapD, stage_addr, x, y, z);
+        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
     } else if (EPI == EPI_GELU) {
         // u = the linear output rounded to bf16, then its GELU and GELU'
         float gd[32];
@@ -210,19 +211,12 @@ static __device__ int stall_for_test = 0;
 // F8: FP8 operands, e4m3 or e5m2 each (K-major only): a k-block is 128 values,
 // four K = 32 MMAs of kind::f8f6f4, and the epilogue scales the accumulator by
 // a_scale * b_scale.
-// BG: the weight gradient dW = dY^T X (A = dY read MN-major) also forms the
-// bias gradient db[m] = sum_k A(m, k), the row sums of A, while the A tiles
-// pass through shared memory: two more warps (10 and 11, one per 64-row half
-// of the tile) read each A stage of the units of the first column tile
-// before it is released (the stages' empty barriers count them), summing
-// each k-block in fp32 and adding the block sums in k order (deterministic).
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false, bool BG = false>
-__global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const GemmArgs g) {
     static_assert(!F8 || (!A_MN && !B_MN && EPI == EPI_NONE), "FP8 operands: K-major, plain epilogue");
-    static_assert(!BG || (A_MN && !F8 && EPI == EPI_NONE), "bias gradient: the weight-gradient layout");
     constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
@@ -251,7 +245,7 @@ __global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), BG ? 3 : 1);  // the MMAs' commit (+ the two bias warps)
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(tfull_bar(a), 1);
@@ -286,7 +280,7 @@ __global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
             bool ok = true;
             Work w;
             for (int idx = 0; ok && get_work(g, idx, w); idx++) {
-                const int m0 = (w.tile / g.n_tiles) * BM, n0 = (w.tile % g.n_tiles) * BN;
+                const int m0 = w.mt * BM, n0 = w.nt * BN;
                 for (int kb = w.kb0; kb < w.kb1; kb++) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
                         ok = false;
@@ -376,7 +370,7 @@ __global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
             if (leader) tc_commit(drain_bar);
             mbar_drain(drain_bar, 0, g.status);
         }
-    } else if (warp < BIAS_WARP0) {
+    } else {
         // ---------------------------------------------------- epilogue (warps 2..9)
         const int ew = warp - EPI_WARP0;         // 0..7
         const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
@@ -393,7 +387,7 @@ __global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
         uint32_t acc_phase = 0;
         Work w;
         for (int idx = 0; get_work(g, idx, w); idx++) {
-            const int m0 = (w.tile / g.n_tiles) * BM, n0 = (w.tile % g.n_tiles) * BN;
+            const int m0 = w.mt * BM, n0 = w.nt * BN;
             const int cfirst = half * CHUNKS;
             if (use_bias) {
                 // the bias of this warp's half of the tile; the buffer's only
@@ -472,59 +466,6 @@ __global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
         }
         if (lane == 0) bulk_wait_all();  // this warp's stores are complete
         __syncwarp();
-    } else if (BG) {
-        // ---------------------------------------------------- bias gradient (warps 10, 11)
-        // Warp bw sums rows m = bw * 64 + 2 * lane (+1) of A over k: in the MN-major
-        // stage its 64 rows are the 64-value chunk bw, 64 k-rows of 128 bytes with
-        // the 128-byte swizzle (16-byte unit u of k-row r at u ^ (r & 7)); this lane's
-        // two values are bytes 4 * lane .. +3 of each k-row.
-        const int bw = warp - BIAS_WARP0;
-        const uint32_t unit = (uint32_t)lane >> 2, within = ((uint32_t)lane & 3u) << 2;
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        Work w;
-        for (int idx = 0; ok && get_work(g, idx, w); idx++) {
-            const bool bias_unit = (w.tile % g.n_tiles) == 0;
-            uint64_t total = 0;  // the two rows' sums, paired
-            for (int kb = w.kb0; kb < w.kb1; kb++) {
-                if (!warp_wait(full_bar(stage), phase, abort_flag, g.status)) {
-                    ok = false;
-                    break;
-                }
-                if (bias_unit) {
-                    const uint8_t* chunk = gbase + stage * Cfg::A_BYTES + bw * (64 * 128);
-                    uint64_t even = 0, odd = 0;
-#pragma unroll 8
-                    for (int r = 0; r < BK; r += 2) {
-                        const uint32_t v0 =
-                            *reinterpret_cast<const uint32_t*>(chunk + r * 128 + (((unit ^ (r & 7)) << 4) | within));
-                        const uint32_t v1 = *reinterpret_cast<const uint32_t*>(
-                            chunk + (r + 1) * 128 + (((unit ^ ((r + 1) & 7)) << 4) | within));
-                        even = f2_add(even, f2_pack(v0 << 16, v0 & 0xFFFF0000u));
-                        odd = f2_add(odd, f2_pack(v1 << 16, v1 & 0xFFFF0000u));
-                    }
-                    total = f2_add(total, f2_add(even, odd));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(stage));  // this warp is done with the stage
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!ok || !bias_unit) continue;
-            float t0, t1;
-            f2_unpack(total, t0, t1);
-            const int ml = bw * 64 + 2 * lane, m = (w.tile / g.n_tiles) * BM + ml;
-            if (g.partials) {
-                g.dbias_partial[(int64_t)w.z * BM + ml] = t0;
-                g.dbias_partial[(int64_t)w.z * BM + ml + 1] = t1;
-            } else {
-                if (m < g.M) g.dbias[m] = t0;
-                if (m + 1 < g.M) g.dbias[m + 1] = t1;
-            }
-        }
     }
 
     tc_fence_before();
@@ -537,27 +478,419 @@ __global__ void __launch_bounds__(BG ? NUM_THREADS_BG : NUM_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel
+//
+// The same GEMM with the MMAs of two CTAs (a cluster of two on neighbouring
+// SMs) fused into one M = 256 product per instruction (tcgen05.mma
+// .cta_group::2): each CTA holds 128 rows of A and half (128) of the 256
+// columns of B in its shared memory, the pair's 256 x 256 tile is computed by
+// the even CTA's MMA warp, and each CTA's tensor memory receives its own 128
+// rows. Per SM and k-block the operand traffic is 16 KB of A and 16 KB of B
+// for the work that takes 16 KB of A and 32 KB of B in the one-CTA kernel.
+// Cross-CTA hand-offs use only local commits and relayed remote mbarrier
+// arrives (no multicast): the odd CTA's relay warp tells the even CTA when
+// its operand stage has landed; the even CTA's relay warp tells the odd CTA
+// when a stage may be refilled and when an accumulator is complete; the odd
+// CTA's epilogue warps arrive remotely on the even CTA's accumulator-empty
+// barriers. Both CTAs allocate and free tensor memory together
+// (.cta_group::2), and leave only after a cluster barrier, once the even
+// CTA's MMAs, which read the odd CTA's shared memory and write its tensor
+// memory, are complete. Every mbarrier wait is bounded (cluster-scope
+// acquire where the arrival comes from the other CTA).
+constexpr int PBN = 256;                    // pair tile: 256 x 256
+constexpr int PBM = 256;
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;     // this CTA's A rows
+constexpr int P_B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_NACC = 1;                   // accumulators in TMEM
+constexpr int P_TMEM_COLS = 256;
+constexpr int P_THREADS = 352;              // 11 warps: + the relay warp
+constexpr int P_RELAY_WARP = 10;
+constexpr int P_OUT_BYTES = EPI_WARPS * 2048;
+constexpr int P_BAR_BYTES = 512;
+constexpr int P_BIAS_BYTES = EPI_WARPS * (PBN / 2) * 4;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_OUT_BYTES + 1024 + P_BAR_BYTES + P_BIAS_BYTES;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the
+// cluster, with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait, cluster-scope acquire (as mbar_wait otherwise).
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    if (mbar_try_cl(bar, parity)) return true;
+    const long long t0 = clock64();
+    const long long limit = *(volatile long long*)&wait_limit_cycles;
+    for (uint32_t it = 1;; it++) {
+        if (mbar_try_cl(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > limit) {
+                set_status(status, GPT2_FLAG_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool warp_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    const bool ok = mbar_wait_cl(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// The idx-th unit of this CTA pair: pair tile (mt over 256-row tiles, nt) and k-range.
+__device__ __forceinline__ bool get_work_pair(const GemmArgs& g, int idx, Work& w) {
+    const int u = (blockIdx.x >> 1) + idx * (gridDim.x >> 1);
+    if (u >= g.units) return false;
+    const int sp = u % g.splits;
+    w.tile = u / g.splits;
+    const int per_group = g.m_tiles * g.group_n;
+    const int gi = w.tile / per_group, r = w.tile - gi * per_group;
+    const int gw = min(g.group_n, g.n_tiles - gi * g.group_n);
+    w.mt = r / gw;
+    w.nt = gi * g.group_n + r % gw;
+    w.kb0 = sp * g.kbs;
+    w.kb1 = min(g.num_kb, w.kb0 + g.kbs);
+    w.z = u;
+    return true;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(P_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                     const GemmArgs g) {
+    constexpr int S = P_STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t a_stage0 = base;
+    const uint32_t b_stage0 = base + S * P_A_BYTES;
+    uint8_t* out_stage = gbase + S * P_STAGE_BYTES;
+    uint8_t* bar_area = out_stage + P_OUT_BYTES;
+    const uint32_t bars = base + S * P_STAGE_BYTES + P_OUT_BYTES;
+    // barriers: full[S], empty[S], pfull[S], tmem_full[NACC], tmem_empty[NACC], drain
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto pfull_bar = [&](int s) { return bars + 8u * (2 * S + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (3 * S + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (3 * S + P_NACC + a); };
+    const uint32_t drain_bar = bars + 8u * (3 * S + 2 * P_NACC);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar_area + 8 * (3 * S + 2 * P_NACC + 1));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (3 * S + 2 * P_NACC + 1) + 4);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();  // 0: issues the pair's MMAs
+    const uint32_t peer = rank ^ 1u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(pfull_bar(s), 1);
+        }
+        for (int a = 0; a < P_NACC; a++) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * EPI_WARPS);  // both CTAs' epilogue warps
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr((const void*)tmem_slot)),
+                     "r"(P_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers are initialised before either arrives on the other's
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued_phase[S];
+            for (int s = 0; s < S; s++) issued_phase[s] = -1;
+            bool ok = true;
+            Work w;
+            for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
+                const int m0 = w.mt * PBM + (int)rank * 128, n0 = w.nt * PBN + (int)rank * (PBN / 2);
+                for (int kb = w.kb0; kb < w.kb1; kb++) {
+                    if (!mbar_wait_cl(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar(stage), P_STAGE_BYTES);
+                    const uint32_t sa = a_stage0 + stage * P_A_BYTES;
+                    const uint32_t sb = b_stage0 + stage * P_B_BYTES;
+                    if (!A_MN) {
+                        tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m0);
+                    } else {
+                        tma_load_2d(sa, &tmA, full_bar(stage), m0, kb * BK);
+                        tma_load_2d(sa + 64 * 128, &tmA, full_bar(stage), m0 + 64, kb * BK);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, n0);
+                    } else {
+                        tma_load_2d(sb, &tmB, full_bar(stage), n0, kb * BK);
+                        tma_load_2d(sb + 64 * 128, &tmB, full_bar(stage), n0 + 64, kb * BK);
+                    }
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < S; s++)
+                if (issued_phase[s] >= 0) mbar_drain(full_bar(s), (uint32_t)issued_phase[s], g.status);
+        }
+    } else if (warp == 1) {
+        if (rank == 0) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            const bool leader = elect_one();
+            const uint32_t idesc = make_idesc(PBM, PBN, A_MN, B_MN);
+            constexpr uint32_t a_kstep = A_MN ? 16 * 128 : 32;
+            constexpr uint32_t b_kstep = B_MN ? 16 * 128 : 32;
+            constexpr uint32_t a_lbo = A_MN ? 64 * 128 : 16;
+            constexpr uint32_t b_lbo = B_MN ? 64 * 128 : 16;
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            Work w;
+            for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
+                const int kb0 = w.kb0, kb1 = w.kb1;
+                if (!warp_wait_cl(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    // this CTA's operands, then the other CTA's (relayed)
+                    if (!warp_wait(full_bar(stage), phase, abort_flag, g.status) ||
+                        !warp_wait_cl(pfull_bar(stage), phase, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = a_stage0 + stage * P_A_BYTES;
+                    const uint32_t sb = b_stage0 + stage * P_B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; k++) {
+                        const uint64_t ad = sw128_desc(sa + k * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = sw128_desc(sb + k * b_kstep, b_lbo, 1024);
+                        if (leader)
+                            asm volatile(
+                                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                                " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                                ::"r"(d_tmem), "l"(ad), "l"(bd), "r"(idesc), "r"((kb > kb0 || k > 0) ? 1u : 0u)
+                                : "memory");
+                    }
+                    if (leader)
+                        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                         empty_bar(stage))
+                                     : "memory");
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (leader)
+                    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     tfull_bar(acc))
+                                 : "memory");
+                if (++acc == P_NACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (leader)
+                asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 drain_bar)
+                             : "memory");
+            mbar_drain(drain_bar, 0, g.status);
+        }
+    } else if (warp == P_RELAY_WARP) {
+        if (lane == 0) {
+            // ------------------------------------------------ relay
+            // even CTA: each stage's release and each accumulator's completion
+            // to the odd CTA; odd CTA: each of its stages' arrival to the even CTA
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            Work w;
+            for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
+                for (int kb = w.kb0; kb < w.kb1; kb++) {
+                    if (rank == 0) {
+                        if (!(ok = mbar_wait(empty_bar(stage), phase, abort_flag, g.status))) break;
+                        mbar_arrive_cta(empty_bar(stage), peer);
+                    } else {
+                        if (!(ok = mbar_wait(full_bar(stage), phase, abort_flag, g.status))) break;
+                        mbar_arrive_cta(pfull_bar(stage), peer);
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (rank == 0) {
+                    if (!(ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, g.status))) break;
+                    tc_fence_after();
+                    tc_fence_before();
+                    mbar_arrive_cta(tfull_bar(acc), peer);
+                }
+                if (++acc == P_NACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2..9, both CTAs)
+        const int ew = warp - EPI_WARP0;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        constexpr int CHUNKS = PBN / 64;
+        const int row_in_tile = (int)rank * 128 + quad * 32 + lane;  // row in the pair tile
+        float* bias_s = reinterpret_cast<float*>(bar_area + P_BAR_BYTES) + ew * (PBN / 2);
+        uint8_t* stage = out_stage + ew * 2048;
+        const uint32_t stage_addr = smem_addr(stage);
+        const bool use_bias = g.bias != nullptr && !g.partials;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        Work w;
+        for (int idx = 0; get_work_pair(g, idx, w); idx++) {
+            const int m0 = w.mt * PBM, n0 = w.nt * PBN;
+            const int cfirst = half * CHUNKS;
+            if (use_bias) {
+                const bf16* bp = reinterpret_cast<const bf16*>(g.bias);
+                const int nb = n0 + cfirst * 32;
+                __syncwarp();
+                for (int i = lane; i < PBN / 2; i += 32) bias_s[i] = nb + i < g.N ? __bfloat162float(bp[nb + i]) : 0.f;
+                __syncwarp();
+            }
+            uint4 aux[2][4];
+            auto load_aux = [&](int c, uint4 (&dst)[4]) {
+                const int row = m0 + row_in_tile;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int col = n0 + (cfirst + c) * 32 + q * 8;
+                    dst[q] = (row < g.M && col < g.N) ? *reinterpret_cast<const uint4*>(g.aux + (int64_t)row * g.N + col)
+                                                      : make_uint4(0, 0, 0, 0);
+                }
+            };
+            if (EPI == EPI_MUL) {
+                load_aux(0, aux[0]);
+                load_aux(1, aux[1]);
+            }
+            if (!warp_wait_cl(tfull_bar(acc), acc_phase, abort_flag, g.status)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * PBN);
+            const int y = m0 + (int)rank * 128 + quad * 32;
+            int nchunks = 0;
+            if (y < g.M) {
+#pragma unroll
+                for (int c = 0; c < CHUNKS; c++)
+                    if (n0 + (cfirst + c) * 32 < g.N) nchunks = c + 1;
+            }
+            const bool split = g.partials != 0;
+            const bool fp32_out = split || g.d_fp32 != 0;
+            // split partials are stored pair-tile-local: [unit][256 rows][256 columns]
+            const int z = split ? w.z : 0;
+            const int ys = split ? (int)rank * 128 + quad * 32 : y;
+            auto xcol = [&](int c) { return (split ? 0 : n0) + (cfirst + c) * 32; };
+            auto ncols = [&](int c) { return g.N - (n0 + (cfirst + c) * 32); };
+            auto bias_at = [&](int c) -> const float* { return use_bias ? bias_s + c * 32 : nullptr; };
+            uint32_t ra[32], rb[32];
+            if (nchunks > 0) {
+                tc_ld32_issue(tbase + (uint32_t)(cfirst * 32), ra);
+                tc_ld_wait(ra);
+            }
+            for (int c = 0; c < nchunks; c += 2) {
+                const bool more = c + 1 < nchunks;
+                if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
+                epi_chunk<EPI>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
+                               ncols(c), lane);
+                if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
+                __syncwarp();
+                if (!more) break;
+                tc_ld_wait(rb);
+                const bool more2 = c + 2 < nchunks;
+                if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
+                epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1), ys,
+                               z, ncols(c + 1), lane);
+                if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
+                __syncwarp();
+                if (more2) tc_ld_wait(ra);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(tempty_bar(acc));
+                else mbar_arrive_cta(tempty_bar(acc), 0);
+            }
+            if (++acc == P_NACC) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // the pair's MMAs (which read both CTAs' shared memory and write both
+    // tensor memories) are complete before either CTA frees or leaves
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(P_TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // Split-K reduce: D[m][n] (fp32) = bias[n] (if any) + the partial tiles of
 // the tile of (m, n), added in split order; with accumulate, added to D's
 // current value. 8 consecutive columns per thread (N and BN are multiples of 8).
-// With a bias gradient (dbias != null), the thread of each row's first
-// eight columns also sets dbias[m] (+)= the row's bias partials of the first
-// column tile, in split order.
 __global__ void __launch_bounds__(256) split_reduce_kernel(float* __restrict__ D, const float* __restrict__ partial,
                                                            const bf16* __restrict__ bias, int M, int N, int BN,
-                                                           int n_tiles, int splits, int accumulate,
-                                                           float* __restrict__ dbias,
-                                                           const float* __restrict__ dbias_partial) {
+                                                           int n_tiles, int splits, int accumulate) {
     // 32-bit element index (the launcher keeps M * N < 2^31)
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= M * N) return;
     const int m = i / N, n = i - m * N;
-    if (dbias && n == 0) {
-        const float* bp = dbias_partial + (int64_t)(m / BM) * n_tiles * splits * BM + m % BM;
-        float b = accumulate ? dbias[m] : 0.f;
-        for (int sp = 0; sp < splits; sp++) b += bp[sp * BM];
-        dbias[m] = b;
-    }
     const int64_t tile = (int64_t)(m / BM) * n_tiles + n / BN;
     const int64_t tile_elems = (int64_t)BM * BN;
     const float* p = partial + tile * splits * tile_elems + (int64_t)(m % BM) * BN + n % BN;
@@ -628,7 +961,7 @@ bool make_out_map(CUtensorMap* map, const void* ptr, bool fp32, uint64_t N, uint
 }
 
 struct Plan {
-    int bn, n_tiles, m_tiles, tiles, num_kb, splits, kbs, units, grid;
+    int bn, n_tiles, m_tiles, tiles, num_kb, splits, kbs, units, grid, group_n;
 };
 
 // HBM bytes moved in the time one SM takes for one 128 x 256 x 64 k-block of
@@ -674,22 +1007,25 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
     p.splits = (p.num_kb + p.kbs - 1) / p.kbs;  // no empty split
     p.units = p.tiles * p.splits;
     p.grid = p.units < sms ? p.units : sms;
+    // raster: wide outputs (the LM head: 197 column tiles) in groups of 32
+    // column tiles (12.6 MB of B at K = 768), so B is read from DRAM about once
+    // and A once per group instead of B once per row of tiles
+    p.group_n = p.n_tiles > 32 ? 32 : p.n_tiles;
     return p;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false, bool BG = false>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                const GemmArgs& args, int grid, cudaStream_t s) {
     using Cfg = TileCfg<BN>;
     // once per process; a function-local static is initialised thread-safely
     static const bool configured = [] {
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8, BG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES);
         return true;
     }();
     (void)configured;
-    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8, BG>
-        <<<grid, BG ? NUM_THREADS_BG : NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
+    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
 }
 
 // The operand layouts, and the fused epilogues only where the step uses them:
@@ -716,6 +1052,63 @@ bool launch_tc_layout(int epi, int a_mn, int b_mn, const CUtensorMap& ma, const 
     return true;
 }
 
+// CTA-pair kernel: the layouts and epilogues the step uses (as launch_tc_layout),
+// launched in clusters of two.
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
+                        const GemmArgs& args, int pairs, cudaStream_t s) {
+    static const bool configured = [] {
+        cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P_SMEM_BYTES);
+        return true;
+    }();
+    (void)configured;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(P_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<A_MN, B_MN, EPI>, ma, mb, md, md2, args);
+}
+
+// Clusters of two CTA-pair kernel CTAs that can be resident at once on the
+// current device (one CTA per SM; looked up once per process, else #SMs / 2).
+int pair_clusters() {
+    static const int n = [] {
+        int v = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * 256, 1, 1);
+        cfg.blockDim = dim3(P_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaFuncSetAttribute(gemm_pair_kernel<false, false, EPI_NONE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P_SMEM_BYTES);
+        if (cudaOccupancyMaxActiveClusters(&v, gemm_pair_kernel<false, false, EPI_NONE>, &cfg) != cudaSuccess || v < 1)
+            v = gpt2_num_sms() / 2;
+        cudaGetLastError();
+        return v;
+    }();
+    return n;
+}
+
+// The pair kernel takes bf16 products with one k-range per tile (no
+// partials), 256-wide tiles of a wide output (N >= 1024) and at least two
+// 256-row tiles; the rest runs on the one-CTA kernel.
+bool use_pair(int M, int N, bool partials) { return !partials && N >= 1024 && M >= 512; }
+
 }  // namespace
 
 int gemm_tc_set_wait_limit(long long cycles) { return set_wait_limit(cycles); }
@@ -730,23 +1123,65 @@ size_t matmul_tc_scratch(int M, int N, int K, int d_fp32, int accumulate) {
     return p.splits > 1 || (d_fp32 && accumulate) ? (size_t)p.units * BM * p.bn * 4 : 0;
 }
 
-size_t matmul_bias_grad_tc_scratch(int M, int N, int K, int accumulate) {
-    Plan p = make_plan(M, N, K, 1);
-    return p.splits > 1 || accumulate ? (size_t)p.units * BM * (p.bn + 1) * 4 : 0;
-}
 
 namespace {
 
-// D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc. With
-// dbias (the weight-gradient layout, fp32 out): also dbias = row sums of A.
+// D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
 int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
               int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s,
-              int accumulate = 0, float* dbias = nullptr) {
-    if (dbias && (epi != EPI_NONE || !d_fp32 || !a_mn || !b_mn || bias)) return GPT2_ERR_ARG;
+              int accumulate = 0) {
     Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
+    if (use_pair(M, N, partials)) {
+        // 256 x 256 pair tiles, each CTA loading 128 rows of A and 128 columns of B
+        const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + PBN - 1) / PBN;
+        CUtensorMap ma, mb, md, md2;
+        bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, 128);
+        ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
+                         : make_map(&mb, B, (uint64_t)K, (uint64_t)N, PBN / 2));
+        ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
+        if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
+        else md2 = md;
+        if (!ok) return GPT2_ERR_CUDA;
+        GemmArgs g;
+        g.a_scale = g.b_scale = nullptr;
+        g.a_fmt = g.b_fmt = 0;
+        g.bias = bias;
+        g.aux = aux;
+        g.status = status;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.d_fp32 = d_fp32;
+        g.splits = 1;
+        g.partials = 0;
+        g.num_kb = (K + BK - 1) / BK;
+        g.kbs = g.num_kb;
+        g.n_tiles = n_tiles;
+        g.m_tiles = m_tiles;
+        g.units = m_tiles * n_tiles;
+        g.group_n = n_tiles > 32 ? 32 : n_tiles;
+        const int pairs = g.units < pair_clusters() ? g.units : pair_clusters();
+        cudaError_t e;
+        if (epi == EPI_GELU) {
+            if (a_mn || b_mn) return GPT2_ERR_ARG;
+            e = launch_pair<false, false, EPI_GELU>(ma, mb, md, md2, g, pairs, s);
+        } else if (epi == EPI_MUL) {
+            if (a_mn || !b_mn) return GPT2_ERR_ARG;
+            e = launch_pair<false, true, EPI_MUL>(ma, mb, md, md2, g, pairs, s);
+        } else if (!a_mn && !b_mn) {
+            e = launch_pair<false, false, EPI_NONE>(ma, mb, md, md2, g, pairs, s);
+        } else if (!a_mn && b_mn) {
+            e = launch_pair<false, true, EPI_NONE>(ma, mb, md, md2, g, pairs, s);
+        } else if (a_mn && !b_mn) {
+            e = launch_pair<true, false, EPI_NONE>(ma, mb, md, md2, g, pairs, s);
+        } else {
+            e = launch_pair<true, true, EPI_NONE>(ma, mb, md, md2, g, pairs, s);
+        }
+        return e == cudaSuccess ? 1 : GPT2_ERR_CUDA;
+    }
     CUtensorMap ma, mb;
     bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
     ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
@@ -760,9 +1195,6 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     GemmArgs g;
     g.a_scale = g.b_scale = nullptr;
     g.a_fmt = g.b_fmt = 0;
-    g.dbias = dbias;
-    // bias partials after the tile partials: [units][BM]
-    g.dbias_partial = dbias && partials ? (float*)scratch + (size_t)p.units * BM * p.bn : nullptr;
     g.bias = partials ? nullptr : bias;
     g.aux = aux;
     g.status = status;
@@ -776,12 +1208,10 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     g.n_tiles = p.n_tiles;
     g.units = p.units;
     g.num_kb = p.num_kb;
-    bool launched = true;
-    if (dbias) {
-        if (p.bn == 128) launch_tc<128, true, true, EPI_NONE, false, true>(ma, mb, md, md2, g, p.grid, s);
-        else if (p.bn == 192) launch_tc<192, true, true, EPI_NONE, false, true>(ma, mb, md, md2, g, p.grid, s);
-        else launch_tc<256, true, true, EPI_NONE, false, true>(ma, mb, md, md2, g, p.grid, s);
-    } else if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
+    g.m_tiles = p.m_tiles;
+    g.group_n = partials ? p.n_tiles : p.group_n;  // the reduce kernel finds partials in row-major order
+    bool launched;
+    if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else if (p.bn == 192) launched = launch_tc_layout<192>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else launched = launch_tc_layout<256>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     if (!launched) return GPT2_ERR_ARG;
@@ -789,8 +1219,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         const int64_t MN = (int64_t)M * N;
         const int blocks = (int)((MN / 8 + 255) / 256);
         split_reduce_kernel<<<blocks, 256, 0, s>>>((float*)D, (const float*)scratch, (const bf16*)bias, M, N, p.bn,
-                                                   p.n_tiles, p.splits, accumulate && d_fp32 ? 1 : 0, dbias,
-                                                   g.dbias_partial);
+                                                   p.n_tiles, p.splits, accumulate && d_fp32 ? 1 : 0);
         return 2;
     }
     return 1;
@@ -827,11 +1256,12 @@ int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale
     g.n_tiles = p.n_tiles;
     g.units = p.units;
     g.num_kb = p.num_kb;
+    g.m_tiles = p.m_tiles;
+    g.group_n = p.group_n;
     g.a_scale = a_scale;
     g.b_scale = b_scale;
     g.a_fmt = a_fmt;
     g.b_fmt = b_fmt;
-    g.dbias = g.dbias_partial = nullptr;
     if (p.bn == 128) launch_tc<128, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
     else if (p.bn == 192) launch_tc<192, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
     else launch_tc<256, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
@@ -842,12 +1272,6 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
                      int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate) {
     return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, a_mn, B, b_mn, bias, M, N, K, scratch, status, s,
                      accumulate);
-}
-
-int launch_matmul_bias_grad_tc(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
-                               void* scratch, int* status, cudaStream_t s, int accumulate) {
-    return matmul_tc(EPI_NONE, dW, nullptr, nullptr, 1, dY, 1, X, 1, nullptr, M, N, K, scratch, status, s, accumulate,
-                     dbias);
 }
 
 int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,

@@ -109,13 +109,6 @@ int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, int
 // accumulate (fp32 D only): D += the product instead of D = it; the scratch
 // size then covers the partial tiles that route through the reduce kernel.
 size_t matmul_scratch(int dtype, int M, int N, int K, int d_fp32, int accumulate = 0);
-// bf16 weight gradient with its bias gradient on the tensor cores: dW[M,N]
-// (fp32, (+)=) = dY^T X with dY [K, M] and X [K, N] (both read MN-major), and
-// dbias[M] (fp32, (+)=) = column sums of dY; scratch of
-// matmul_bias_grad_tc_scratch() bytes.
-size_t matmul_bias_grad_tc_scratch(int M, int N, int K, int accumulate);
-int launch_matmul_bias_grad_tc(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
-                               void* scratch, int* status, cudaStream_t s, int accumulate);
 int launch_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias,
                   int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate = 0);
 

@@ -221,7 +221,6 @@ size_t plan(const gpt2_config* c, gpt2* m) {
         need(matmul_scratch(dt, outs[k], ins[k], iBT, 1, 1));    // dW (also when accumulating)
         need(matmul_scratch(dt, iBT, ins[k], outs[k], 0));       // dX
         need(bias_backward_scratch(iBT, outs[k]));
-        if (dt == GPT2_MODE_BF16) need(matmul_bias_grad_tc_scratch(outs[k], ins[k], iBT, 1));  // dW with db
     }
     need(matmul_scratch(dt, iVp, iC, iBT, 1, 1));
     need(matmul_scratch(dt, iBT, iC, iVp, 0));
@@ -387,13 +386,6 @@ int linear_fwd(gpt2* m, void* y, const void* x, int wi, int bi, int BT, int in, 
 // dx = dy W, dW = dy^T x, db = column sums of dy.
 int linear_bwd(gpt2* m, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in, int out) {
     TRY(op_matmul(m, dx, 0, dy, 0, P(m, wi), 1, nullptr, BT, in, out));
-    if (bi >= 0 && m->dtype == GPT2_MODE_BF16) {
-        // the bias gradient comes out of the weight-gradient GEMM (row sums of dY^T)
-        Op op(m, GPT2_K_MATMUL);
-        return op.done(launch_matmul_bias_grad_tc(G(m, wi), G(m, bi), dy, x, out, in, BT, m->scratch, m->status,
-                                                  m->stream, m->grad_accum),
-                       2.0 * out * in * BT);
-    }
     TRY(op_matmul(m, G(m, wi), 1, dy, 1, x, 1, nullptr, out, in, BT, m->grad_accum));
     if (bi >= 0) {
         Op op(m, GPT2_K_BIAS_BWD);

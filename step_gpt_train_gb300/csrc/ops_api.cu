@@ -113,22 +113,6 @@ int gpt2_op_matmul(int dtype, void* D, int d_fp32, const void* A, int a_mn_major
                                 st(stream)));
 }
 
-size_t gpt2_op_matmul_bias_grad_scratch(int M, int N, int K, int accumulate) {
-    if (M < 0 || N < 0 || K < 0) return 0;
-    return matmul_bias_grad_tc_scratch(M, N, K, accumulate);
-}
-
-int gpt2_op_matmul_bias_grad(float* dW, float* dbias, const void* dY, const void* X, int M, int N, int K,
-                             int accumulate, void* scratch, size_t scratch_bytes, int* d_status, void* stream) {
-    if (!dW || !dbias || !dY || !X || M < 0 || N < 0 || K < 1 || M % 8 || N % 8 || K % 8) return GPT2_ERR_ARG;
-    if (!al16(dW) || !al16(dY) || !al16(X)) return GPT2_ERR_ARG;
-    if ((int64_t)M * N == 0) return GPT2_OK;
-    const size_t need = matmul_bias_grad_tc_scratch(M, N, K, accumulate);
-    if (need && (!scratch || scratch_bytes < need)) return GPT2_ERR_WORKSPACE;
-    return finish(launch_matmul_bias_grad_tc(dW, dbias, dY, X, M, N, K, scratch, d_status, st(stream),
-                                             accumulate ? 1 : 0));
-}
-
 size_t gpt2_op_quantize_fp8_scratch(void) { return fp8_quantize_scratch(); }
 
 static bool fp8_format_ok(int f) { return f == GPT2_FP8_E4M3 || f == GPT2_FP8_E5M2; }

@@ -85,9 +85,6 @@ _SIGNATURES = {
     "gpt2_family_time": (c_int, [c_void_p, c_int, POINTER(c_double)]),
     "gpt2_reset_stats": (c_int, [c_void_p]),
     # gpt2_ops.h
-    "gpt2_op_matmul_bias_grad_scratch": (c_size_t, [c_int, c_int, c_int, c_int]),
-    "gpt2_op_matmul_bias_grad": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
-                                         c_void_p, c_size_t, c_void_p, c_void_p]),
     "gpt2_debug_set_wait_limit": (c_int, [c_int64]),
     "gpt2_debug_stall_matmul": (c_int, [c_int]),
     "gpt2_op_encoder_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
@@ -450,18 +447,6 @@ def gpt2_op_matmul(D, A, a_mn, B, b_mn, M, N, K, bias=None, status=None, stream=
     sc = _scratch(lib.gpt2_op_matmul_scratch(dt, M, N, K, d_fp32))
     check(lib.gpt2_op_matmul(dt, _p(D), d_fp32, _p(A), int(a_mn), _p(B), int(b_mn), _p(bias), M, N, K, _p(sc),
                              sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul")
-    return sc
-
-
-def gpt2_op_matmul_bias_grad(dW, dbias, dY, X, accumulate=False, status=None, stream=None):
-    """dW (fp32 [M,N]) (+)= dY^T X and dbias (fp32 [M]) (+)= column sums of dY, with
-    dY bf16 [K,M] and X bf16 [K,N], in one tensor-core pass."""
-    K, M = dY.shape
-    N = X.shape[1]
-    lib = load_library()
-    sc = _scratch(lib.gpt2_op_matmul_bias_grad_scratch(M, N, K, int(bool(accumulate))))
-    check(lib.gpt2_op_matmul_bias_grad(_p(dW), _p(dbias), _p(dY), _p(X), M, N, K, int(bool(accumulate)), _p(sc),
-                                       sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul_bias_grad")
     return sc
 
 

@@ -21,12 +21,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # The matmuls of one bf16 training step and how often each runs (per layer
 # the forward QKV, attention projection, MLP up-projection with its GELU and
-# MLP down-projection, their input and weight gradients (the bias gradients of
-# QKV and the up-projection from the weight-gradient pass), and the tied LM
+# MLP down-projection, their input and weight gradients, and the tied LM
 # head's three): `--ops step_gemms` runs each once, in this order.
 def step_gemm_counts(L: int = 12) -> dict:
     per_layer = ["gemm_qkv_fwd", "gemm_proj_fwd", "gemm_fc_fwd_gelu", "gemm_fcproj_fwd", "gemm_fcproj_dw",
-                 "gemm_fcproj_dx_gelu", "gemm_fc_dwb", "gemm_fc_dx", "gemm_proj_dw", "gemm_proj_dx", "gemm_qkv_dwb",
+                 "gemm_fcproj_dx_gelu", "gemm_fc_dw", "gemm_fc_dx", "gemm_proj_dw", "gemm_proj_dx", "gemm_qkv_dw",
                  "gemm_qkv_dx"]
     counts = {n: L for n in per_layer}
     counts.update({"gemm_lmhead_fwd": 1, "gemm_lmhead_dx": 1, "gemm_lmhead_dw": 1})
@@ -97,23 +96,6 @@ def main(argv=None):
         ops[f"gemm_{name}_dx"] = gemm_op(N, inp, out, 0, 1, False, False)
         ops[f"gemm_{name}_dw"] = gemm_op(out, inp, N, 1, 1, True, False)
 
-    def gemm_dwb_op(out, inp):  # weight gradient with the bias gradient from the same pass
-        def setup():
-            dY, X = rnd(N, out), rnd(N, inp)
-            dW, db = torch.empty(out, inp, device=dev), torch.empty(out, device=dev)
-            sc = torch.empty(max(256, g.load_library().gpt2_op_matmul_bias_grad_scratch(out, inp, N, 0)),
-                             dtype=torch.uint8, device=dev)
-            lib = g.load_library()
-
-            def run():
-                g.check(lib.gpt2_op_matmul_bias_grad(dW.data_ptr(), db.data_ptr(), dY.data_ptr(), X.data_ptr(), out,
-                                                     inp, N, 0, sc.data_ptr(), sc.numel(), None,
-                                                     torch.cuda.current_stream().cuda_stream))
-            return run
-        return setup, 2.0 * out * inp * N, "flop"
-
-    ops["gemm_qkv_dwb"] = gemm_dwb_op(3 * C, C)
-    ops["gemm_fc_dwb"] = gemm_dwb_op(4 * C, C)
 
     def gemm_gelu_op():  # the MLP's first linear with its GELU in the epilogue
         def setup():
