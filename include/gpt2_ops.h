@@ -277,6 +277,14 @@ int gpt2_op_adamw(float* master, void* param_bf16, const float* grad, float* m, 
 int gpt2_debug_set_wait_limit(int64_t cycles);
 int gpt2_debug_stall_matmul(int on);
 
+/* gpt2_debug_matmul_pair: on != 0 routes the wide bf16 matmuls (N >= 1024,
+ * M >= 512, one k-range per tile) to the CTA-pair kernel, which issues one
+ * M = 256 tensor-core product for two neighbouring SMs (tcgen05 .cta_group::2)
+ * so that each SM loads half of the B tile; 0 (the default) keeps every
+ * matmul on the one-CTA kernel. Process-wide; takes effect for matmuls
+ * launched after it returns. Returns GPT2_OK. */
+int gpt2_debug_matmul_pair(int on);
+
 #ifdef __cplusplus
 }
 #endif

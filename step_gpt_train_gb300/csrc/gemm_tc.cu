@@ -503,8 +503,8 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = 128 * BK * 2;     // this CTA's A rows
 constexpr int P_B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_NACC = 1;                   // accumulators in TMEM
-constexpr int P_TMEM_COLS = 256;
+constexpr int P_NACC = 2;                   // accumulators in TMEM: a tile's epilogue overlaps the next tile's MMAs
+constexpr int P_TMEM_COLS = 512;
 constexpr int P_THREADS = 352;              // 11 warps: + the relay warp
 constexpr int P_RELAY_WARP = 10;
 constexpr int P_OUT_BYTES = EPI_WARPS * 2048;
@@ -1106,12 +1106,17 @@ int pair_clusters() {
 
 // The pair kernel takes bf16 products with one k-range per tile (no
 // partials), 256-wide tiles of a wide output (N >= 1024) and at least two
-// 256-row tiles; the rest runs on the one-CTA kernel.
-bool use_pair(int M, int N, bool partials) { return !partials && N >= 1024 && M >= 512; }
+// 256-row tiles, when it is switched on (gemm_tc_use_pair; off by default:
+// its relayed hand-offs measured slower than the one-CTA kernel); the rest
+// runs on the one-CTA kernel.
+bool g_use_pair = false;
+bool use_pair(int M, int N, bool partials) { return g_use_pair && !partials && N >= 1024 && M >= 512; }
 
 }  // namespace
 
 int gemm_tc_set_wait_limit(long long cycles) { return set_wait_limit(cycles); }
+
+void gemm_tc_use_pair(int on) { g_use_pair = on != 0; }
 
 int gemm_tc_stall_for_test(int on) {
     const int v = on ? 1 : 0;

@@ -87,6 +87,7 @@ _SIGNATURES = {
     # gpt2_ops.h
     "gpt2_debug_set_wait_limit": (c_int, [c_int64]),
     "gpt2_debug_stall_matmul": (c_int, [c_int]),
+    "gpt2_debug_matmul_pair": (c_int, [c_int]),
     "gpt2_op_encoder_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                         c_void_p, c_void_p]),
     "gpt2_op_encoder_backward_scratch": (c_size_t, [c_int, c_int, c_int]),
