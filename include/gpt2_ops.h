@@ -282,7 +282,9 @@ int gpt2_debug_stall_matmul(int on);
  * M = 256 tensor-core product for two neighbouring SMs (tcgen05 .cta_group::2)
  * so that each SM loads half of the B tile; 0 (the default) keeps every
  * matmul on the one-CTA kernel. Process-wide; takes effect for matmuls
- * launched after it returns. Returns GPT2_OK. */
+ * launched after it returns; on > 1 also sets the number of two-CTA
+ * clusters launched (else the number the device keeps resident). Returns the
+ * number of clusters the pair kernel launches (on != 0) or 0. */
 int gpt2_debug_matmul_pair(int on);
 
 #ifdef __cplusplus

@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
                 const int m0 = w.mt * PBM + (int)rank * 128, n0 = w.nt * PBN + (int)rank * (PBN / 2);
                 for (int kb = w.kb0; kb < w.kb1; kb++) {
-                    if (!mbar_wait_cl(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
+                    if (!mbar_spin<true>(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
@@ -688,13 +688,13 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             Work w;
             for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
-                if (!warp_wait_cl(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
+                if (!warp_spin<true>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
                 for (int kb = kb0; kb < kb1; kb++) {
                     // this CTA's operands, then the other CTA's (relayed)
-                    if (!warp_wait(full_bar(stage), phase, abort_flag, g.status) ||
-                        !warp_wait_cl(pfull_bar(stage), phase, abort_flag, g.status)) {
+                    if (!warp_spin(full_bar(stage), phase, abort_flag, g.status) ||
+                        !warp_spin<true>(pfull_bar(stage), phase, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
@@ -751,10 +751,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
                 for (int kb = w.kb0; kb < w.kb1; kb++) {
                     if (rank == 0) {
-                        if (!(ok = mbar_wait(empty_bar(stage), phase, abort_flag, g.status))) break;
+                        if (!(ok = mbar_spin(empty_bar(stage), phase, abort_flag, g.status))) break;
                         mbar_arrive_cta(empty_bar(stage), peer);
                     } else {
-                        if (!(ok = mbar_wait(full_bar(stage), phase, abort_flag, g.status))) break;
+                        if (!(ok = mbar_spin(full_bar(stage), phase, abort_flag, g.status))) break;
                         mbar_arrive_cta(pfull_bar(stage), peer);
                     }
                     if (++stage == S) {
@@ -764,7 +764,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 }
                 if (!ok) break;
                 if (rank == 0) {
-                    if (!(ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, g.status))) break;
+                    if (!(ok = mbar_spin(tfull_bar(acc), acc_phase, abort_flag, g.status))) break;
                     tc_fence_after();
                     tc_fence_before();
                     mbar_arrive_cta(tfull_bar(acc), peer);
@@ -1110,13 +1110,18 @@ int pair_clusters() {
 // its relayed hand-offs measured slower than the one-CTA kernel); the rest
 // runs on the one-CTA kernel.
 bool g_use_pair = false;
+int g_pair_override = 0;  // > 0: the number of clusters to launch instead of the resident count
 bool use_pair(int M, int N, bool partials) { return g_use_pair && !partials && N >= 1024 && M >= 512; }
 
 }  // namespace
 
 int gemm_tc_set_wait_limit(long long cycles) { return set_wait_limit(cycles); }
 
-void gemm_tc_use_pair(int on) { g_use_pair = on != 0; }
+int gemm_tc_use_pair(int on) {
+    g_use_pair = on != 0;
+    g_pair_override = on > 1 ? on : 0;
+    return on ? (g_pair_override ? g_pair_override : pair_clusters()) : 0;
+}
 
 int gemm_tc_stall_for_test(int on) {
     const int v = on ? 1 : 0;
@@ -1168,7 +1173,8 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         g.m_tiles = m_tiles;
         g.units = m_tiles * n_tiles;
         g.group_n = n_tiles > 32 ? 32 : n_tiles;
-        const int pairs = g.units < pair_clusters() ? g.units : pair_clusters();
+        const int resident = g_pair_override ? g_pair_override : pair_clusters();
+        const int pairs = g.units < resident ? g.units : resident;
         cudaError_t e;
         if (epi == EPI_GELU) {
             if (a_mn || b_mn) return GPT2_ERR_ARG;

@@ -120,5 +120,6 @@ int gemm_tc_set_wait_limit(long long cycles);
 int attention_tc_set_wait_limit(long long cycles);
 int classifier_set_wait_limit(long long cycles);
 int gemm_tc_stall_for_test(int on);
-// The CTA-pair GEMM for the wide matmuls (on != 0) or the one-CTA kernel only (0, the default).
-void gemm_tc_use_pair(int on);
+// The CTA-pair GEMM for the wide matmuls (on != 0) or the one-CTA kernel only
+// (0, the default); returns the pair kernel's resident clusters when on.
+int gemm_tc_use_pair(int on);

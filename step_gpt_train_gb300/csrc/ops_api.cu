@@ -259,9 +259,6 @@ int gpt2_debug_set_wait_limit(int64_t cycles) {
 
 int gpt2_debug_stall_matmul(int on) { return gemm_tc_stall_for_test(on) ? GPT2_ERR_CUDA : GPT2_OK; }
 
-int gpt2_debug_matmul_pair(int on) {
-    gemm_tc_use_pair(on);
-    return GPT2_OK;
-}
+int gpt2_debug_matmul_pair(int on) { return gemm_tc_use_pair(on); }
 
 }  // extern "C"

@@ -62,6 +62,53 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         }
     }
 }
+// Non-blocking probe of the phase with the given parity (test_wait returns at
+// once; try_wait may suspend the thread for a while before it re-checks).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
+        "p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait by spinning on test_wait (as mbar_wait otherwise), for waits on
+// events that come from another role at a steady rate, where a suspended
+// thread would notice the phase change late. CL: cluster-scope acquire.
+template <bool CL = false>
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    if (CL ? mbar_test_cl(bar, parity) : mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    const long long limit = *(volatile long long*)&wait_limit_cycles;
+    for (uint32_t it = 1;; it++) {
+        if (CL ? mbar_test_cl(bar, parity) : mbar_test(bar, parity)) return true;
+        if ((it & 255) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > limit) {
+                set_status(status, GPT2_FLAG_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+template <bool CL = false>
+__device__ __forceinline__ bool warp_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    const bool ok = mbar_spin<CL>(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // One lane of a fully active warp (the lowest), for work that a single
 // thread issues on the warp's behalf.
 __device__ __forceinline__ bool elect_one() {
