@@ -487,9 +487,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // the even CTA's MMA warp, and each CTA's tensor memory receives its own 128
 // rows. Per SM and k-block the operand traffic is 16 KB of A and 16 KB of B
 // for the work that takes 16 KB of A and 32 KB of B in the one-CTA kernel.
-// Cross-CTA hand-offs use only local commits and relayed remote mbarrier
-// arrives (no multicast): the odd CTA's relay warp tells the even CTA when
-// its operand stage has landed; the even CTA's relay warp tells the odd CTA
+// Cross-CTA hand-offs (no multicast): both CTAs' operand copies complete on
+// the even CTA's full barriers (TMA .cta_group::2 with a cluster address);
+// the even CTA's relay warp tells the odd CTA, by remote mbarrier arrives,
 // when a stage may be refilled and when an accumulator is complete; the odd
 // CTA's epilogue warps arrive remotely on the even CTA's accumulator-empty
 // barriers. Both CTAs allocate and free tensor memory together
@@ -553,6 +553,17 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, vola
 __device__ __forceinline__ bool warp_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
     const bool ok = mbar_wait_cl(bar, parity, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on a
+// barrier of the CTA pair's even CTA (cluster address), .cta_group::2.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
 }
 
 // The idx-th unit of this CTA pair: pair tile (mt over 256-row tiles, nt) and k-range.
@@ -646,20 +657,24 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(full_bar(stage), P_STAGE_BYTES);
+                    // both CTAs' loads complete on the even CTA's full barrier,
+                    // which expects the pair's bytes
+                    if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+                    uint32_t fb;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(fb) : "r"(full_bar(stage)));
                     const uint32_t sa = a_stage0 + stage * P_A_BYTES;
                     const uint32_t sb = b_stage0 + stage * P_B_BYTES;
                     if (!A_MN) {
-                        tma_load_2d(sa, &tmA, full_bar(stage), kb * BK, m0);
+                        tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
                     } else {
-                        tma_load_2d(sa, &tmA, full_bar(stage), m0, kb * BK);
-                        tma_load_2d(sa + 64 * 128, &tmA, full_bar(stage), m0 + 64, kb * BK);
+                        tma_load_2d_pair(sa, &tmA, fb, m0, kb * BK);
+                        tma_load_2d_pair(sa + 64 * 128, &tmA, fb, m0 + 64, kb * BK);
                     }
                     if (!B_MN) {
-                        tma_load_2d(sb, &tmB, full_bar(stage), kb * BK, n0);
+                        tma_load_2d_pair(sb, &tmB, fb, kb * BK, n0);
                     } else {
-                        tma_load_2d(sb, &tmB, full_bar(stage), n0, kb * BK);
-                        tma_load_2d(sb + 64 * 128, &tmB, full_bar(stage), n0 + 64, kb * BK);
+                        tma_load_2d_pair(sb, &tmB, fb, n0, kb * BK);
+                        tma_load_2d_pair(sb + 64 * 128, &tmB, fb, n0 + 64, kb * BK);
                     }
                     issued_phase[stage] = (int)phase;
                     if (++stage == S) {
@@ -668,8 +683,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     }
                 }
             }
-            for (int s = 0; s < S; s++)
-                if (issued_phase[s] >= 0) mbar_drain(full_bar(s), (uint32_t)issued_phase[s], g.status);
+            // the even CTA's full barriers count both CTAs' copies: it waits for them
+            // all (the odd CTA stays until the cluster barrier at the end)
+            if (rank == 0)
+                for (int s = 0; s < S; s++)
+                    if (issued_phase[s] >= 0) mbar_drain(full_bar(s), (uint32_t)issued_phase[s], g.status);
         }
     } else if (warp == 1) {
         if (rank == 0) {
@@ -692,9 +710,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
                 for (int kb = kb0; kb < kb1; kb++) {
-                    // this CTA's operands, then the other CTA's (relayed)
-                    if (!warp_spin(full_bar(stage), phase, abort_flag, g.status) ||
-                        !warp_spin<true>(pfull_bar(stage), phase, abort_flag, g.status)) {
+                    // both CTAs' operands (their copies complete on this CTA's barrier)
+                    if (!warp_spin<true>(full_bar(stage), phase, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
@@ -741,7 +758,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         if (lane == 0) {
             // ------------------------------------------------ relay
             // even CTA: each stage's release and each accumulator's completion
-            // to the odd CTA; odd CTA: each of its stages' arrival to the even CTA
+            // to the odd CTA
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -753,9 +770,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     if (rank == 0) {
                         if (!(ok = mbar_spin(empty_bar(stage), phase, abort_flag, g.status))) break;
                         mbar_arrive_cta(empty_bar(stage), peer);
-                    } else {
-                        if (!(ok = mbar_spin(full_bar(stage), phase, abort_flag, g.status))) break;
-                        mbar_arrive_cta(pfull_bar(stage), peer);
                     }
                     if (++stage == S) {
                         stage = 0;
