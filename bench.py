@@ -237,10 +237,12 @@ def gemm_traffic_from_profile():
 
 
 # Families bound by HBM bandwidth; the library counts their algorithmic
-# bytes (each tensor read or written once) as their work.
+# bytes (each tensor read or written once) as their work. grad_colsum's bytes
+# are the partial column sums it reads (scratch of the backward, not tensors
+# of the model).
 HBM_FAMILIES = ("encoder_forward", "layernorm_forward", "classifier", "loss_mean", "layernorm_backward",
                 "bias_backward", "encoder_backward", "adamw", "residual_forward", "residual_backward",
-                "gelu_forward", "gelu_backward")
+                "gelu_forward", "gelu_backward", "grad_colsum")
 
 
 def hbm_fractions(fam_ms: dict, stats: dict, steps: int, peaks: dict) -> dict:

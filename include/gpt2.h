@@ -261,7 +261,9 @@ enum {
     GPT2_K_ENCODER_FWD = 0, GPT2_K_LAYERNORM_FWD, GPT2_K_MATMUL, GPT2_K_ATTENTION_FWD,
     GPT2_K_RESIDUAL_FWD, GPT2_K_GELU_FWD, GPT2_K_CLASSIFIER, GPT2_K_LOSS_MEAN,
     GPT2_K_LAYERNORM_BWD, GPT2_K_GELU_BWD, GPT2_K_BIAS_BWD, GPT2_K_ATTENTION_BWD,
-    GPT2_K_RESIDUAL_BWD, GPT2_K_ENCODER_BWD, GPT2_K_ADAMW, GPT2_K_COUNT
+    GPT2_K_RESIDUAL_BWD, GPT2_K_ENCODER_BWD, GPT2_K_ADAMW,
+    GPT2_K_GRAD_COLSUM, /* the deferred column sums of the LayerNorm and bias gradients */
+    GPT2_K_COUNT
 };
 
 /* Kernels launched by this handle so far (every launch, all families). */

@@ -168,6 +168,19 @@ int gpt2_op_matmul_gelu_backward(int dtype, void* du, const void* dY, const void
                                  const void* dgelu, int M, int N, int K, int* d_status,
                                  void* stream);
 
+/* The same, and the bias gradient of the linear whose output gradient du is
+ * ("matmul_backward"'s bias part): dbias[n] = sum over m of du[m,n], fp32
+ * [N], overwritten, summed from the values as stored in du. bf16: the sums
+ * of each 32-row slice are formed in the matmul's epilogue and reduced by a
+ * second launch; fp32: a separate column-sum pass over du. scratch: at least
+ * gpt2_op_matmul_gelu_backward_bias_scratch(M, N) bytes (else
+ * GPT2_ERR_WORKSPACE). */
+size_t gpt2_op_matmul_gelu_backward_bias_scratch(int M, int N);
+int gpt2_op_matmul_gelu_backward_bias(int dtype, void* du, float* dbias, const void* dY,
+                                      const void* W, const void* dgelu, int M, int N, int K,
+                                      void* scratch, size_t scratch_bytes, int* d_status,
+                                      void* stream);
+
 /* Causal multi-head attention forward ("flash attention", section "Single
  * GPU training"; kernel "cudnn_generated_fort_native_sdpa"): qkv [B*T, 3C]
  * holds q | k | v column blocks, head h at columns h*hd..h*hd+hd-1 of each.

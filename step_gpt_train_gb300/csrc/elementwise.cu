@@ -639,19 +639,81 @@ int launch_colsum(float* out, float* out2, int split, const float* in, int R, in
     return launch_colsum3(out, out2, nullptr, split, in, R, ncols, s);
 }
 
+// Many column sums in one launch: block b serves 32 columns of the job whose
+// block range holds b, with the arithmetic of colsum_kernel (so a job gives
+// the bits colsum_kernel gives for it).
+constexpr int COLSUM_MAX_JOBS = 32;
+struct ColsumBatch {
+    ColsumJob job[COLSUM_MAX_JOBS];
+    int block0[COLSUM_MAX_JOBS + 1];
+    int n;
+};
+
+__global__ void __launch_bounds__(1024) colsum_jobs_kernel(const __grid_constant__ ColsumBatch b) {
+    __shared__ float sm[32][33];
+    int k = 0;
+    while (k + 1 < b.n && (int)blockIdx.x >= b.block0[k + 1]) k++;
+    const ColsumJob& j = b.job[k];
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+    const int c = ((int)blockIdx.x - b.block0[k]) * 32 + tx;
+    float s = 0.f;
+    if (c < j.ncols) {
+#pragma unroll 4
+        for (int r = ty; r < j.R; r += 32) s += j.in[(int64_t)r * j.ncols + c];
+    }
+    sm[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && c < j.ncols) {
+        float t = 0.f;
+        for (int q = 0; q < 32; q++) t += sm[q][tx];
+        const int q = c / j.seg;
+        if (q < 3 && j.out[q]) {
+            float* o = j.out[q] + (c - q * j.seg);
+            *o = j.accumulate ? *o + t : t;
+        }
+    }
+}
+
+int launch_colsum_jobs(const ColsumJob* jobs, int n, cudaStream_t s) {
+    int launches = 0;
+    for (int i0 = 0; i0 < n; i0 += COLSUM_MAX_JOBS) {
+        ColsumBatch b;
+        b.n = n - i0 < COLSUM_MAX_JOBS ? n - i0 : COLSUM_MAX_JOBS;
+        int blocks = 0;
+        for (int k = 0; k < b.n; k++) {
+            b.job[k] = jobs[i0 + k];
+            b.block0[k] = blocks;
+            blocks += b.job[k].R > 0 ? (b.job[k].ncols + 31) / 32 : 0;
+        }
+        b.block0[b.n] = blocks;
+        if (blocks == 0) continue;
+        colsum_jobs_kernel<<<blocks, 1024, 0, s>>>(b);
+        launches++;
+    }
+    return launches;
+}
+
 size_t bias_backward_scratch(int N, int C) {
     const size_t chunks = ((size_t)N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK;
     return chunks * C * 4;
 }
 
-int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s,
-                         int accumulate) {
+int launch_bias_partials(int dtype, float* partial, const void* dy, int N, int C, cudaStream_t s, int* rows) {
     const int chunks = (int)(((int64_t)N + BIAS_ROWS_PER_CHUNK - 1) / BIAS_ROWS_PER_CHUNK);
+    *rows = chunks;
+    if (chunks == 0) return 0;
     dim3 grid((C + 255) / 256, chunks < 65535 ? chunks : 65535);
     if (dtype == GPT2_MODE_BF16)
-        bias_partial_kernel<bf16><<<grid, 256, 0, s>>>((float*)scratch, (const bf16*)dy, N, C, chunks);
+        bias_partial_kernel<bf16><<<grid, 256, 0, s>>>(partial, (const bf16*)dy, N, C, chunks);
     else
-        bias_partial_kernel<float><<<grid, 256, 0, s>>>((float*)scratch, (const float*)dy, N, C, chunks);
+        bias_partial_kernel<float><<<grid, 256, 0, s>>>(partial, (const float*)dy, N, C, chunks);
+    return 1;
+}
+
+int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s,
+                         int accumulate) {
+    int chunks = 0;
+    launch_bias_partials(dtype, (float*)scratch, dy, N, C, s, &chunks);
     launch_colsum3(dbias, nullptr, nullptr, C, (const float*)scratch, chunks, C, s, accumulate);
     return 2;
 }

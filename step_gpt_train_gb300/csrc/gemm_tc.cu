@@ -70,6 +70,7 @@ constexpr int EPI_MUL = 2;   // D = bf16(x) * aux: the input gradient through th
 struct GemmArgs {
     const void* bias;    // bf16 [N] or null
     const bf16* aux;     // EPI_MUL: the factor [M][N]
+    float* colsum;       // EPI_MUL, or null: column sums of the stored D per 32-row slice, [4 * m_tiles][N]
     int* status;
     int M, N, K;
     int d_fp32;
@@ -134,12 +135,15 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
 // One 32-column chunk of this warp's 32 rows: + bias, the epilogue op,
 // convert, stage, TMA store. fp32 output goes out as two 16-column halves.
 // ncols_valid = columns of the chunk inside the matrix (> 0). aux holds this
-// lane's 32 factors (EPI_MUL).
+// lane's 32 factors (EPI_MUL). EPI_MUL with csum_dst: csum_dst[j] (j <
+// ncols_valid) also receives the sum of column j of the stored (bf16) values
+// over the first nrows of the warp's 32 rows, read back from the staging buffer.
 template <int EPI, bool F8 = false>
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
                                           uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD,
                                           const CUtensorMap* mapD2, const uint4 (&aux)[4], int x, int y, int z,
-                                          int ncols_valid, int lane, float alpha = 1.f) {
+                                          int ncols_valid, int lane, float alpha = 1.f, float* csum_dst = nullptr,
+                                          int nrows = 32) {
     float f[32];
     if (!F8 && bias_s) {
 #pragma unroll
@@ -168,6 +172,14 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
             }
         }
         stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
+        if (csum_dst) {
+            // the staged rows (the TMA store only reads them too; the next
+            // chunk overwrites them only after this warp's next sync)
+            int col;
+            const float sum = staged_colsum32(
+                [&](int r, int q) { return stage + r * 64 + ((q ^ ((r >> 1) & 3)) << 4); }, nrows, lane, col);
+            if (col < ncols_valid) csum_dst[col] = sum;
+        }
     } else if (EPI == EPI_GELU) {
         // u = the linear output rounded to bf16, then its GELU and GELU'
         float gd[32];
@@ -383,6 +395,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t stage_addr = smem_addr(stage);
         const bool use_bias = g.bias != nullptr && !g.partials;
         const float alpha = F8 ? *g.a_scale * *g.b_scale : 1.f;
+        // EPI_MUL column sums: each warp writes the sums of its 32 rows of a
+        // tile, row 4 * mt + quad of g.colsum
+        const bool want_csum = EPI == EPI_MUL && g.colsum != nullptr;
         int acc = 0;
         uint32_t acc_phase = 0;
         Work w;
@@ -433,6 +448,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto xcol = [&](int c) { return (split ? 0 : n0) + (cfirst + c) * 32; };
             auto ncols = [&](int c) { return g.N - (n0 + (cfirst + c) * 32); };
             auto bias_at = [&](int c) -> const float* { return use_bias ? bias_s + c * 32 : nullptr; };
+            float* csum_row = want_csum ? g.colsum + (int64_t)(w.mt * 4 + quad) * g.N + n0 + cfirst * 32 : nullptr;
+            auto csum_at = [&](int c) -> float* { return want_csum ? csum_row + c * 32 : nullptr; };
+            const int nrows = max(0, min(32, g.M - y));  // this warp's rows inside the matrix
             uint32_t ra[32], rb[32];
             if (nchunks > 0) {
                 tc_ld32_issue(tbase + (uint32_t)(cfirst * 32), ra);
@@ -443,7 +461,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
                 epi_chunk<EPI, F8>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
-                                   ncols(c), lane, alpha);
+                                   ncols(c), lane, alpha, csum_at(c), nrows);
                 if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();  // reconverge before the warp-collective TMEM ops
                 if (!more) break;
@@ -451,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
                 epi_chunk<EPI, F8>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1),
-                                   ys, z, ncols(c + 1), lane, alpha);
+                                   ys, z, ncols(c + 1), lane, alpha, csum_at(c + 1), nrows);
                 if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
@@ -459,6 +477,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (want_csum) {  // rows outside the matrix: zero sums for the columns inside it
+                for (int c = nchunks; c < CHUNKS; c++)
+                    if (n0 + (cfirst + c) * 32 + lane < g.N) csum_row[c * 32 + lane] = 0.f;
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -1033,13 +1055,15 @@ void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& 
                const GemmArgs& args, int grid, cudaStream_t s) {
     using Cfg = TileCfg<BN>;
     // once per process; a function-local static is initialised thread-safely
+    constexpr int smem = Cfg::SMEM_BYTES;
+    static_assert(smem <= 232448, "shared memory per CTA");
     static const bool configured = [] {
         cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES);
+                             smem);
         return true;
     }();
     (void)configured;
-    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8><<<grid, NUM_THREADS, Cfg::SMEM_BYTES, s>>>(ma, mb, md, md2, args);
+    gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8><<<grid, NUM_THREADS, smem, s>>>(ma, mb, md, md2, args);
 }
 
 // The operand layouts, and the fused epilogues only where the step uses them:
@@ -1153,12 +1177,12 @@ namespace {
 // D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
 int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
               int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s,
-              int accumulate = 0) {
+              int accumulate = 0, float* colsum = nullptr) {
     Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
-    if (use_pair(M, N, partials)) {
+    if (use_pair(M, N, partials) && !colsum) {
         // 256 x 256 pair tiles, each CTA loading 128 rows of A and 128 columns of B
         const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + PBN - 1) / PBN;
         CUtensorMap ma, mb, md, md2;
@@ -1169,7 +1193,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
         else md2 = md;
         if (!ok) return GPT2_ERR_CUDA;
-        GemmArgs g;
+        GemmArgs g = {};
         g.a_scale = g.b_scale = nullptr;
         g.a_fmt = g.b_fmt = 0;
         g.bias = bias;
@@ -1217,11 +1241,12 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
     else md2 = md;
     if (!ok) return GPT2_ERR_CUDA;
-    GemmArgs g;
+    GemmArgs g = {};
     g.a_scale = g.b_scale = nullptr;
     g.a_fmt = g.b_fmt = 0;
     g.bias = partials ? nullptr : bias;
     g.aux = aux;
+    g.colsum = epi == EPI_MUL ? colsum : nullptr;
     g.status = status;
     g.M = M;
     g.N = N;
@@ -1267,7 +1292,7 @@ int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale
     bool ok = make_map_u8(&ma, A, (uint64_t)K, (uint64_t)M, BM) && make_map_u8(&mb, B, (uint64_t)K, (uint64_t)N, p.bn) &&
               make_out_map(&md, D, false, (uint64_t)N, (uint64_t)M, 1);
     if (!ok) return GPT2_ERR_CUDA;
-    GemmArgs g;
+    GemmArgs g = {};
     g.bias = bias;
     g.aux = nullptr;
     g.status = status;
@@ -1306,8 +1331,8 @@ int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, con
 }
 
 int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* dgelu, int M, int N, int K,
-                                int* status, cudaStream_t s) {
+                                int* status, cudaStream_t s, float* du_colsum) {
     if (M == 0 || N == 0) return 0;
     return matmul_tc(EPI_MUL, du, nullptr, (const bf16*)dgelu, 0, dY, 0, W, 1, nullptr, M, N, K, nullptr, status,
-                     s);
+                     s, 0, du_colsum);
 }

@@ -36,6 +36,12 @@ int launch_layernorm_backward_residual(int dtype, void* dres, int accumulate, fl
                                        float* dres_colsum, const void* dy, const void* x, const void* gamma,
                                        const float* mean, const float* rstd, int N, int C, void* scratch,
                                        cudaStream_t s, int grad_accumulate = 0);
+// Its row pass alone: dres (+)= dx and partial [*rows][np * C] (np 2: dgamma,
+// dbeta parts; 3: and the column sums of dres), for a deferred ColsumJob.
+// partial: layernorm_backward_scratch(N, C) bytes.
+int launch_layernorm_backward_residual_rows(int dtype, void* dres, int accumulate, float* partial, int np,
+                                            const void* dy, const void* x, const void* gamma, const float* mean,
+                                            const float* rstd, int N, int C, cudaStream_t s, int* rows);
 
 int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream_t s);
 int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s);
@@ -48,9 +54,24 @@ int launch_colsum(float* out, float* out2, int split, const float* in, int R, in
 int launch_colsum3(float* out0, float* out1, float* out2, int seg, const float* in, int R, int ncols,
                    cudaStream_t s, int accumulate = 0);
 
+// A column sum whose launch is deferred (the parameter-gradient reductions of
+// a backward pass, gathered into one launch at its end): out[q][c] (+)= the
+// sum over r of in[r][q * seg + c], q < 3 (null outputs skipped).
+struct ColsumJob {
+    const float* in;
+    float* out[3];
+    int R, ncols, seg, accumulate;
+};
+// All the jobs, in ceil(n / 32) launches; each job's result has the bits
+// launch_colsum3 gives for it. Returns the launches.
+int launch_colsum_jobs(const ColsumJob* jobs, int n, cudaStream_t s);
+
 size_t bias_backward_scratch(int N, int C);
 int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, void* scratch, cudaStream_t s,
                          int accumulate = 0);
+// The first pass of launch_bias_backward alone: partial [rows][C] of column
+// sums over 128-row chunks of dy; *rows = ceil(N / 128).
+int launch_bias_partials(int dtype, float* partial, const void* dy, int N, int C, cudaStream_t s, int* rows);
 
 int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
                       float dloss, int* status, cudaStream_t s);
@@ -85,9 +106,12 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
 // gelu'(u) (kept for the backward); see gpt2_op_matmul_gelu.
 int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
                        int* status, cudaStream_t s);
-// bf16 input gradient through that GELU: du = bf16(dY W) * dgelu, dY [M,K], W [K,N].
+// bf16 input gradient through that GELU: du = bf16(dY W) * dgelu, dY [M,K], W [K,N];
+// du_colsum (or null): column sums of the stored du per 32-row slice, [4 ceil(M/128)][N]
+// (matmul_gelu_backward_colsum_rows).
+inline int matmul_gelu_backward_colsum_rows(int M) { return 4 * ((M + 127) / 128); }
 int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* dgelu, int M, int N, int K,
-                                int* status, cudaStream_t s);
+                                int* status, cudaStream_t s, float* du_colsum = nullptr);
 // out = gelu(u) and dgelu = gelu'(u) (dgelu may be u itself); n % 8 == 0.
 int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n, cudaStream_t s);
 // out = a * b elementwise; n % 8 == 0.

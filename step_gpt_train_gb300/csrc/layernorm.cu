@@ -732,11 +732,12 @@ static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumula
                                                                      (const bf16*)gamma, mean, rstd, N, C);
 }
 
-static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, float* dbeta, float* dout_colsum,
-                       const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, int N,
-                       int C, void* scratch, cudaStream_t s, int grad_accumulate = 0) {
-    const int np = dout_colsum ? 3 : 2;
-    float* partial_s = (float*)scratch;
+// The row pass of the backward: out (+)= dx and the per-block column sums
+// partial [blocks][np * C] (dy * xhat | dy | the values written, np == 3).
+// Returns the number of blocks (the partial rows).
+static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partial_s, int np, const void* dy,
+                            const void* x, const void* gamma, const float* mean, const float* rstd, int N, int C,
+                            cudaStream_t s) {
     if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
         // 111 KB of ring per block at C = 768 bf16, two blocks per SM
         const int blocks = ln_bwd_staged_blocks(N);
@@ -755,12 +756,11 @@ static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, flo
             default: LN_BWD_STAGED_CALL(4); break;
         }
 #undef LN_BWD_STAGED_CALL
-        launch_colsum3(dgamma, dbeta, dout_colsum, C, partial_s, blocks, np * C, s, grad_accumulate);
-        return 2;
+        return blocks;
     }
     const int blocks = ln_bwd_blocks(N);
     const size_t smem = (size_t)LN_BWD_WARPS * np * C * 4;
-    float* partial = (float*)scratch;
+    float* partial = partial_s;
 #define LN_BWD_CALL(V)                                                                                           \
     if (dtype == GPT2_MODE_BF16)                                                                                 \
         ln_bwd_launch<bf16, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);  \
@@ -768,8 +768,24 @@ static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, flo
         ln_bwd_launch<float, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);
     LN_DISPATCH(ln_vpl(C), LN_BWD_CALL)
 #undef LN_BWD_CALL
-    launch_colsum3(dgamma, dbeta, dout_colsum, C, partial, blocks, np * C, s, grad_accumulate);
+    return blocks;
+}
+
+static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, float* dbeta, float* dout_colsum,
+                       const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, int N,
+                       int C, void* scratch, cudaStream_t s, int grad_accumulate = 0) {
+    const int np = dout_colsum ? 3 : 2;
+    const int blocks =
+        ln_backward_rows(dtype, out, accumulate, (float*)scratch, np, dy, x, gamma, mean, rstd, N, C, s);
+    launch_colsum3(dgamma, dbeta, dout_colsum, C, (const float*)scratch, blocks, np * C, s, grad_accumulate);
     return 2;
+}
+
+int launch_layernorm_backward_residual_rows(int dtype, void* dres, int accumulate, float* partial, int np,
+                                            const void* dy, const void* x, const void* gamma, const float* mean,
+                                            const float* rstd, int N, int C, cudaStream_t s, int* rows) {
+    *rows = ln_backward_rows(dtype, dres, accumulate != 0, partial, np, dy, x, gamma, mean, rstd, N, C, s);
+    return 1;
 }
 
 int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,

@@ -74,6 +74,13 @@ struct gpt2 {
     void *dres, *dtmp, *dbig, *dqkv;
     void* scratch;
     size_t scratch_bytes;
+    // The backward's parameter-gradient column sums (LayerNorm scale and
+    // shift, the four biases of a block): their partial sums go to regions of
+    // this pool as they are formed, and one deferred launch at the end of the
+    // backward reduces them all.
+    float* cs_pool;
+    size_t cs_pool_bytes, cs_used;
+    std::vector<ColsumJob> cs_jobs;
     int B, T;
     int state;  // 0: none, 1: forward with targets done, 2: backward done
     int grad_accum;          // backward adds into the gradients instead of overwriting them
@@ -228,6 +235,16 @@ size_t plan(const gpt2_config* c, gpt2* m) {
     need(attention_backward_scratch(c->max_B, c->max_T, (int)H));
     need(encoder_backward_scratch(c->max_B, c->max_T, iC));
     const size_t o_scratch = take(sc);
+    // the column-sum partials of one backward: per block two LayerNorms, the
+    // MLP's first bias (from the GELU-gradient matmul, or the bias pass) and
+    // the QKV bias (the bias pass); the final LayerNorm (each region rounded
+    // up to WS_ALIGN)
+    const size_t ln_part = align_up(layernorm_backward_scratch(iBT, iC), WS_ALIGN);
+    const size_t fc_mm = (size_t)matmul_gelu_backward_colsum_rows(iBT) * 4 * C * 4;
+    const size_t fc_part = align_up(std::max(bias_backward_scratch(iBT, 4 * iC), fc_mm), WS_ALIGN);
+    const size_t qkv_part = align_up(bias_backward_scratch(iBT, 3 * iC), WS_ALIGN);
+    const size_t cs_bytes = L * (2 * ln_part + fc_part + qkv_part) + ln_part;
+    const size_t o_cs = take(cs_bytes);
     const size_t total = align_up(off, WS_ALIGN);
     if (m) {
         uint8_t* w = m->ws;
@@ -267,6 +284,9 @@ size_t plan(const gpt2_config* c, gpt2* m) {
         m->dqkv = w + o_dqkv;
         m->scratch = w + o_scratch;
         m->scratch_bytes = sc;
+        m->cs_pool = (float*)(w + o_cs);
+        m->cs_pool_bytes = cs_bytes;
+        m->cs_used = 0;
     }
     return total;
 }
@@ -370,6 +390,30 @@ struct Op {
 inline void* P(gpt2* m, int i) { return (uint8_t*)m->params + (size_t)m->tensors[i].offset * m->act; }
 inline float* G(gpt2* m, int i) { return m->grads + m->tensors[i].offset; }
 
+// A region of the column-sum pool for rows x ncols fp32 partials (null when
+// the pool is exhausted, which plan() rules out for the configured sizes).
+float* cs_take(gpt2* m, int rows, int ncols) {
+    const size_t bytes = align_up((size_t)rows * ncols * 4, WS_ALIGN);
+    if (m->cs_used + bytes > m->cs_pool_bytes) return nullptr;
+    float* p = (float*)((uint8_t*)m->cs_pool + m->cs_used);
+    m->cs_used += bytes;
+    return p;
+}
+
+// Defer out_q[c] (+)= column sums of partial [rows][ncols], q < 3.
+void cs_defer(gpt2* m, const float* partial, int rows, int ncols, int seg, float* o0, float* o1, float* o2) {
+    ColsumJob j;
+    j.in = partial;
+    j.out[0] = o0;
+    j.out[1] = o1;
+    j.out[2] = o2;
+    j.R = rows;
+    j.ncols = ncols;
+    j.seg = seg;
+    j.accumulate = m->grad_accum;
+    m->cs_jobs.push_back(j);
+}
+
 int op_matmul(gpt2* m, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
               int N, int K, int accumulate = 0) {
     Op op(m, GPT2_K_MATMUL);
@@ -383,14 +427,18 @@ int linear_fwd(gpt2* m, void* y, const void* x, int wi, int bi, int BT, int in, 
     return op_matmul(m, y, 0, x, 0, P(m, wi), 0, bi >= 0 ? P(m, bi) : nullptr, BT, out, in);
 }
 
-// dx = dy W, dW = dy^T x, db = column sums of dy.
+// dx = dy W, dW = dy^T x, db = column sums of dy (partials now, reduced at
+// the end of the backward).
 int linear_bwd(gpt2* m, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in, int out) {
     TRY(op_matmul(m, dx, 0, dy, 0, P(m, wi), 1, nullptr, BT, in, out));
     TRY(op_matmul(m, G(m, wi), 1, dy, 1, x, 1, nullptr, out, in, BT, m->grad_accum));
     if (bi >= 0) {
+        float* part = cs_take(m, (int)((BT + 127) / 128), out);
+        if (!part) return GPT2_ERR_WORKSPACE;
         Op op(m, GPT2_K_BIAS_BWD);
-        TRY(op.done(launch_bias_backward(m->dtype, G(m, bi), dy, BT, out, m->scratch, m->stream, m->grad_accum),
-                    (double)BT * out * m->act + out * 4.0));
+        int rows = 0;
+        TRY(op.done(launch_bias_partials(m->dtype, part, dy, BT, out, m->stream, &rows), (double)BT * out * m->act));
+        cs_defer(m, part, rows, out, out, G(m, bi), nullptr, nullptr);
     }
     return GPT2_OK;
 }
@@ -414,11 +462,16 @@ int res_ln_fwd(gpt2* m, void* y, float* mean, float* rstd, void* xsum, const voi
 // linear layer whose output joins the residual stream at this point.
 int ln_bwd_res(gpt2* m, int accumulate, const void* dy, const void* x, int gi, const float* mean, const float* rstd,
                int bi, int BT) {
+    const int np = bi >= 0 ? 3 : 2;
+    float* part = (float*)cs_take(m, 1, (int)(layernorm_backward_scratch(BT, m->C) / 4));
+    if (!part) return GPT2_ERR_WORKSPACE;
     Op op(m, GPT2_K_LAYERNORM_BWD);
-    return op.done(launch_layernorm_backward_residual(m->dtype, m->dres, accumulate, G(m, gi), G(m, gi + 1),
-                                                      bi >= 0 ? G(m, bi) : nullptr, dy, x, P(m, gi), mean, rstd, BT,
-                                                      m->C, m->scratch, m->stream, m->grad_accum),
-                   (double)BT * ((3.0 + accumulate) * m->C * m->act + 8));
+    int rows = 0;
+    TRY(op.done(launch_layernorm_backward_residual_rows(m->dtype, m->dres, accumulate, part, np, dy, x, P(m, gi),
+                                                        mean, rstd, BT, m->C, m->stream, &rows),
+                (double)BT * ((3.0 + accumulate) * m->C * m->act + 8)));
+    cs_defer(m, part, rows, np * m->C, m->C, G(m, gi), G(m, gi + 1), bi >= 0 ? G(m, bi) : nullptr);
+    return GPT2_OK;
 }
 
 double attn_fwd_flops(int B, int T, int C) { return 2.0 * 2.0 * B * C * (double)T * (T + 1) / 2.0; }
@@ -480,6 +533,8 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
 
 int backward_impl(gpt2* m) {
     const int B = m->B, T = m->T, BT = B * T, C = m->C, L = m->L;
+    m->cs_used = 0;
+    m->cs_jobs.clear();
     // LM head (tied with wte): dlnf = dlogits wte; dwte = dlogits^T lnf (overwrites dwte)
     TRY(op_matmul(m, m->dtmp, 0, m->logits, 0, P(m, T_WTE), 1, nullptr, BT, C, m->Vp));
     TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT, m->grad_accum));
@@ -492,18 +547,25 @@ int backward_impl(gpt2* m) {
         if (m->dtype == GPT2_MODE_BF16) {
             // dW of the MLP projection, then its input gradient times the
             // GELU's derivative (kept in fch by the forward), in the GEMM epilogue
+            // (and the column sums of that gradient per 32-row slice: the
+            // partials of the first linear's bias gradient)
             TRY(op_matmul(m, G(m, tidx(l, 10)), 1, m->dres, 1, b.fchg, 1, nullptr, C, 4 * C, BT, m->grad_accum));
+            const int rows = matmul_gelu_backward_colsum_rows(BT);
+            float* part = cs_take(m, rows, 4 * C);
+            if (!part) return GPT2_ERR_WORKSPACE;
             Op op(m, GPT2_K_MATMUL);
             TRY(op.done(launch_matmul_gelu_backward(m->dbig, m->dres, P(m, tidx(l, 10)), b.fch, BT, 4 * C, C,
-                                                    m->status, m->stream),
+                                                    m->status, m->stream, part),
                         2.0 * BT * 4 * C * C));
+            cs_defer(m, part, rows, 4 * C, 4 * C, G(m, tidx(l, 9)), nullptr, nullptr);
         } else {
             TRY(linear_bwd(m, m->dbig, m->dres, b.fchg, tidx(l, 10), -1, BT, 4 * C, C));
             Op op(m, GPT2_K_GELU_BWD);
             TRY(op.done(launch_gelu_backward(m->dtype, m->dbig, b.fch, m->dbig, (int64_t)BT * 4 * C, m->stream),
                         3.0 * BT * 4 * C * m->act));
         }
-        TRY(linear_bwd(m, m->dtmp, m->dbig, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
+        TRY(linear_bwd(m, m->dtmp, m->dbig, b.ln2, tidx(l, 8), m->dtype == GPT2_MODE_BF16 ? -1 : tidx(l, 9), BT, C,
+                       4 * C));
         TRY(ln_bwd_res(m, 1, m->dtmp, b.x1, tidx(l, 6), b.mean2, b.rstd2, tidx(l, 5), BT));
         // attention branch
         TRY(linear_bwd(m, m->dtmp, m->dres, b.atty, tidx(l, 4), -1, BT, C, C));
@@ -515,6 +577,13 @@ int backward_impl(gpt2* m) {
         }
         TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
         TRY(ln_bwd_res(m, 1, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, l > 0 ? tidx(l - 1, 11) : -1, BT));
+    }
+    {
+        // every deferred column sum of this backward, in ceil(jobs / 32) launches
+        double bytes = 0;
+        for (const ColsumJob& j : m->cs_jobs) bytes += (double)j.R * j.ncols * 4 + (double)j.ncols * 4;
+        Op op(m, GPT2_K_GRAD_COLSUM);
+        TRY(op.done(launch_colsum_jobs(m->cs_jobs.data(), (int)m->cs_jobs.size(), m->stream), bytes));
     }
     if (T < m->maxT && !m->grad_accum &&
         cudaMemsetAsync(G(m, T_WPE) + (size_t)T * C, 0, (size_t)(m->maxT - T) * C * 4, m->stream) != cudaSuccess)

@@ -170,6 +170,32 @@ int gpt2_op_matmul_gelu_backward(int dtype, void* du, const void* dY, const void
     return finish(launch_mul(dtype, du, du, dgelu, (int64_t)M * N, st(stream)));
 }
 
+size_t gpt2_op_matmul_gelu_backward_bias_scratch(int M, int N) {
+    if (M < 0 || N < 0) return 0;
+    const size_t fused = (size_t)matmul_gelu_backward_colsum_rows(M) * N * 4;  // bf16: per 32-row slice
+    const size_t pass = bias_backward_scratch(M, N);                           // fp32: per 128 rows
+    return fused > pass ? fused : pass;
+}
+
+int gpt2_op_matmul_gelu_backward_bias(int dtype, void* du, float* dbias, const void* dY, const void* W,
+                                      const void* dgelu, int M, int N, int K, void* scratch, size_t scratch_bytes,
+                                      int* d_status, void* stream) {
+    if (!dbias) return GPT2_ERR_ARG;
+    if (!scratch || scratch_bytes < gpt2_op_matmul_gelu_backward_bias_scratch(M, N)) return GPT2_ERR_WORKSPACE;
+    if (dtype != GPT2_MODE_BF16 || (int64_t)M * N == 0) {
+        const int r = gpt2_op_matmul_gelu_backward(dtype, du, dY, W, dgelu, M, N, K, d_status, stream);
+        if (r != GPT2_OK) return r;
+        if (N > 0) return finish(launch_bias_backward(dtype, dbias, du, M, N, scratch, st(stream)));
+        return GPT2_OK;
+    }
+    if (!du || !dY || !W || !dgelu || K < 1 || du == dgelu || K % 8 || N % 8 || M < 0 || N < 0) return GPT2_ERR_ARG;
+    if (!al16(du) || !al16(dY) || !al16(W) || !al16(dgelu)) return GPT2_ERR_ARG;
+    const int r = launch_matmul_gelu_backward(du, dY, W, dgelu, M, N, K, d_status, st(stream), (float*)scratch);
+    if (r < 0) return r;
+    return finish(launch_colsum3(dbias, nullptr, nullptr, N, (const float*)scratch,
+                                 matmul_gelu_backward_colsum_rows(M), N, st(stream)));
+}
+
 int gpt2_op_attention_forward(int dtype, void* o, float* lse, const void* qkv, int B, int T, int C, int H,
                               void* stream) {
     if (!dt_ok(dtype) || !o || !lse || !qkv || B < 0 || T < 0 || C <= 0 || H <= 0 || C % H || C % 8)

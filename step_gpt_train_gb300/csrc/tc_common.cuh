@@ -251,6 +251,48 @@ __device__ __forceinline__ void gelu_pair(float u0, float u1, float& g0, float& 
     f2_unpack(d, d0, d1);
 }
 
+// Column sums of a warp's 32-row x 32-column bf16 block in shared memory held
+// as four 16-byte units per row (unit q: columns 8q .. 8q+7) at
+// unit_addr(r, q). Lane L loads unit L & 3 of rows L/4 + 8i (i < 4; rows >=
+// nrows count as 0) and adds them in fp32 in that order; then the eight lanes
+// that share a unit combine their sums in three halving exchanges (partners
+// across lane bits 4, 3, 2: a lane keeps half of its columns and adds its
+// partner's values of them). Afterwards lane L holds the sum of column
+//   8 (L & 3) + 4 ((L >> 4) & 1) + 2 ((L >> 3) & 1) + ((L >> 2) & 1),
+// which is returned in col. The order of the additions is fixed.
+template <typename UnitAddr>
+__device__ __forceinline__ float staged_colsum32(UnitAddr unit_addr, int nrows, int lane, int& col) {
+    const int q = lane & 3, r0 = lane >> 2;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) v[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int r = r0 + 8 * i;
+        if (r < nrows) {
+            const uint4 w = *reinterpret_cast<const uint4*>(unit_addr(r, q));
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                v[2 * k] += __uint_as_float(u[k] << 16);
+                v[2 * k + 1] += __uint_as_float(u[k] & 0xFFFF0000u);
+            }
+        }
+    }
+#pragma unroll
+    for (int w = 4, m = 16; w >= 1; w /= 2, m /= 2) {
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < w; i++) {
+            const float keep = up ? v[i + w] : v[i];
+            const float send = up ? v[i] : v[i + w];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+    col = 8 * q + 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+    return v[0];
+}
+
 // Issue a load of 32 consecutive fp32 accumulator columns of this thread's
 // TMEM lane; the registers are valid only after tc_ld_wait on them.
 __device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {

@@ -29,7 +29,8 @@ FP8_E4M3, FP8_E5M2 = 0, 1  # the FP8 formats of gpt2_op_quantize_fp8 / gpt2_op_m
 
 FAMILIES = ["encoder_forward", "layernorm_forward", "matmul", "attention_forward", "residual_forward",
             "gelu_forward", "classifier", "loss_mean", "layernorm_backward", "gelu_backward",
-            "bias_backward", "attention_backward", "residual_backward", "encoder_backward", "adamw"]
+            "bias_backward", "attention_backward", "residual_backward", "encoder_backward", "adamw",
+            "grad_colsum"]
 
 WORKSPACE_ALIGN = 1024
 
@@ -114,6 +115,9 @@ _SIGNATURES = {
                                    c_int, c_int, c_void_p, c_void_p]),
     "gpt2_op_matmul_gelu_backward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                              c_void_p, c_void_p]),
+    "gpt2_op_matmul_gelu_backward_bias_scratch": (c_size_t, [c_int, c_int]),
+    "gpt2_op_matmul_gelu_backward_bias": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                                  c_int, c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
     "gpt2_op_attention_forward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                           c_void_p]),
     "gpt2_op_attention_backward_scratch": (c_size_t, [c_int, c_int, c_int]),
@@ -489,6 +493,18 @@ def gpt2_op_matmul_gelu_backward(du, dY, W, dgelu, status=None, stream=None):
     N = W.shape[1]
     check(load_library().gpt2_op_matmul_gelu_backward(_dtype_of(dY), _p(du), _p(dY), _p(W), _p(dgelu), M, N, K,
                                                       _p(status), _s(stream)), "gpt2_op_matmul_gelu_backward")
+
+
+def gpt2_op_matmul_gelu_backward_bias(du, dbias, dY, W, dgelu, status=None, stream=None):
+    """du = (dY W) * dgelu and dbias = column sums of du (fp32 [N])."""
+    M, K = dY.shape
+    N = W.shape[1]
+    lib = load_library()
+    sc = _scratch(lib.gpt2_op_matmul_gelu_backward_bias_scratch(M, N))
+    check(lib.gpt2_op_matmul_gelu_backward_bias(_dtype_of(dY), _p(du), _p(dbias), _p(dY), _p(W), _p(dgelu), M, N,
+                                                K, _p(sc), sc.numel(), _p(status), _s(stream)),
+          "gpt2_op_matmul_gelu_backward_bias")
+    return sc
 
 
 def gpt2_op_attention_forward(o, lse, qkv, B, T, H, stream=None):

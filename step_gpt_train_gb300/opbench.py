@@ -140,8 +140,22 @@ def main(argv=None):
     # input gradient of the MLP down-projection: dY [N, C] (e5m2) times W^T stored [4C, C] (e4m3)
     ops["gemm_fcproj_dx_fp8_e5m2"] = gemm_fp8_op(4 * C, C, a_fmt=g.FP8_E5M2, use_bias=False)
     ops["quantize_fp8"] = quantize_op()
+    def gemm_gelu_bwd_bias_op():  # the same, with the MLP's first bias gradient from its epilogue
+        def setup():
+            dY, W, u = rnd(N, C), rnd(C, 4 * C, std=0.02), rnd(N, 4 * C)
+            du = torch.empty(N, 4 * C, device=dev, dtype=bf)
+            db = torch.empty(4 * C, device=dev)
+            sc = torch.empty(g.load_library().gpt2_op_matmul_gelu_backward_bias_scratch(N, 4 * C), device=dev,
+                             dtype=torch.uint8)
+            lib = g.load_library()
+            return lambda: g.check(lib.gpt2_op_matmul_gelu_backward_bias(
+                1, du.data_ptr(), db.data_ptr(), dY.data_ptr(), W.data_ptr(), u.data_ptr(), N, 4 * C, C,
+                sc.data_ptr(), sc.numel(), None, torch.cuda.current_stream().cuda_stream))
+        return setup, 2.0 * N * 4 * C * C, "flop"
+
     ops["gemm_fc_fwd_gelu"] = gemm_gelu_op()
     ops["gemm_fcproj_dx_gelu"] = gemm_gelu_bwd_op()
+    ops["gemm_fcproj_dx_gelu_bias"] = gemm_gelu_bwd_bias_op()
 
     def attn_fwd():
         qkv = rnd(N, 3 * C)
@@ -238,6 +252,7 @@ def main(argv=None):
         return setup
 
     ops["bias_bwd_fc"] = (bias_bwd(4 * C), N * 4.0 * C * 2, "byte")
+    ops["bias_bwd_qkv"] = (bias_bwd(3 * C), N * 3.0 * C * 2, "byte")
     ops["bias_bwd_proj"] = (bias_bwd(C), N * C * 2.0, "byte")
 
     def classifier():

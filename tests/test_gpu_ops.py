@@ -233,7 +233,7 @@ def test_matmul_gelu(torch_cuda, mode, shape):
     the GELU output bit for bit against the separate matmul and GELU kernels."""
     torch = torch_cuda
     from step_gpt_train_gb300.gpt2 import (gpt2_op_gelu_forward, gpt2_op_matmul, gpt2_op_matmul_gelu,
-                                           gpt2_op_matmul_gelu_backward)
+                                           gpt2_op_matmul_gelu_backward, gpt2_op_matmul_gelu_backward_bias)
     M, N, K = shape  # 300 rows: a ragged 128-row tile; N = 776: a ragged column tile
     A = inputs(60, (M, K), 1.0, mode)
     W = inputs(61, (N, K), K ** -0.5, mode)
@@ -273,6 +273,16 @@ def test_matmul_gelu(torch_cuda, mode, shape):
     floor = 8 * 2.0 ** -23 * float(np.abs(rdg).max())
     assert_close(host(du), R.gelu_backward(hu, rdg), 3 * tol, atol_frac=2e-3 if mode == 1 else 1e-6, atol=floor,
                  what="du vs oracle")
+    # with the bias gradient of the first linear (column sums of du; bf16: from
+    # the matmul's epilogue): du bit for bit as without, dbias = the float64
+    # column sums of du as stored, to fp32 summation error
+    du2 = torch.full_like(dgelu, float("nan"))
+    dbias = torch.full((N,), float("nan"), device="cuda")
+    gpt2_op_matmul_gelu_backward_bias(du2, dbias, dev(dY, mode), dev(W2, mode), dgelu)
+    torch.cuda.synchronize()
+    assert torch.equal(du2, du)
+    hdu = host(du).astype(np.float64)
+    assert_close(host(dbias), hdu.sum(0), 0, atol=1e-5 * float(np.abs(hdu).sum(0).max()), what="dbias = colsum(du)")
 
 
 @pytest.mark.parametrize("mode", [1, 0])

@@ -174,13 +174,18 @@ def test_launch_inventory_matches_page_table(torch_cuda):
     assert st["gelu_forward"]["calls"] == facts["gelu_forward"] - 12 == 0
     assert st["gelu_backward"]["calls"] == facts["gelu_backward"] - 12 == 0
     # Fusions: every residual join runs inside the LayerNorm forward that reads
-    # its sum (24 of the 25), and the LayerNorm backwards, which add into the
-    # residual gradient as in the table, also emit the bias gradients of the
-    # two projections whose outputs join the stream (2 of the 4 per layer).
+    # its sum (24 of the 25). The LayerNorm backwards, which add into the
+    # residual gradient as in the table, also sum the bias gradients of the two
+    # projections whose outputs join the stream, and the GELU-gradient matmul
+    # sums the MLP's first bias gradient in its epilogue: one bias pass per
+    # layer is left (QKV). All their partial sums, and the LayerNorm scale and
+    # shift gradients', are reduced by one deferred op at the end of the backward.
     L = facts["n_layer"]
     assert st["residual_forward"]["calls"] == facts["residual_forward"] - 2 * L == 0
-    assert st["bias_backward"]["calls"] == facts["bias_backward"] - 2 * L
+    assert st["bias_backward"]["calls"] == facts["bias_backward"] - 3 * L == L
     assert st["residual_backward"]["calls"] == 0
+    assert st["grad_colsum"]["calls"] == 1
+    assert st["grad_colsum"]["launches"] == (4 * L + 1 + 31) // 32  # 49 column sums, 32 to a launch
     assert model.launch_count() == sum(v["launches"] for v in st.values())
     model.close()
 
