@@ -242,7 +242,7 @@ def gemm_traffic_from_profile():
 # of the model).
 HBM_FAMILIES = ("encoder_forward", "layernorm_forward", "classifier", "loss_mean", "layernorm_backward",
                 "bias_backward", "encoder_backward", "adamw", "residual_forward", "residual_backward",
-                "gelu_forward", "gelu_backward", "grad_colsum")
+                "gelu_forward", "gelu_backward", "grad_colsum", "fp8_quant")
 
 
 def hbm_fractions(fam_ms: dict, stats: dict, steps: int, peaks: dict) -> dict:
@@ -339,6 +339,9 @@ def main():
     ap.add_argument("--eager", action="store_true",
                     help="separate gpt2_forward / gpt2_backward / gpt2_adamw_step calls instead of gpt2_step")
     ap.add_argument("--ref-T", type=int, default=256)
+    ap.add_argument("--fp8", default="",
+                    help="comma-separated FP8 linear layers (qkv, mlp, head): the FP8 variant of the step, "
+                         "not the bf16 headline")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -364,6 +367,10 @@ def main():
     B, T = cfg["max_B"], w["T"]
     K, W = args.steps, args.warmup
     model = GPT2(cfg, seed=1234)
+    fp8_names = [n for n in args.fp8.split(",") if n]
+    fp8_bits = {"qkv": 1, "mlp": 2, "head": 4}
+    if fp8_names:
+        model.set_fp8(sum(fp8_bits[n] for n in fp8_names))
     stream = model.stream
     tok, tgt = data.workload_batches(args.config, W + K, seed=1234 + rank, B=B, T=T)
     d_tok = torch.from_numpy(tok).cuda()
@@ -460,7 +467,10 @@ def main():
     peak_src = "measured sustained (MEASURED_PEAKS.json)"
     if not peak:
         peak, peak_src = 1700.0, "fallback"
-    traffic = gemm_traffic_from_profile()
+    traffic = gemm_traffic_from_profile() if not fp8_names else None
+    if fp8_names:
+        # the family mixes FP8 and bf16 products: reported against the bf16 peak
+        peak_src += "; the FP8 products' own peak is twice it (the nominal e4m3 : bf16 ratio)"
     roofline = {"kernel": "gemm_tc_kernel (every matmul of the step)", "bound": "tensor",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "peak_source": peak_src,
@@ -476,17 +486,20 @@ def main():
            "vs_measured_burst": (tflops / world / peaks["bf16_tflops"]) if peaks.get("bf16_tflops") else None}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if not fp8_names else "bf16 + fp8 (e4m3 activations/weights, e5m2 gradients) in "
+                                                   + "/".join(fp8_names),
             "data": "synthetic",
             "config": {"workload": workload_label(args.config, w, B, T),
                        "parallelism": f"replicas x{world} (no exchange)" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2: each step touches ~15 GB of weights, activations and state",
                        "api": "gpt2_forward, gpt2_backward, gpt2_adamw_step" if args.eager
                        else "gpt2_step (the step replayed as one CUDA graph)",
-                       "roofline_pass": "per-kernel times from a separate instrumented pass of the same steps"},
+                       "roofline_pass": "per-kernel times from a separate instrumented pass of the same steps",
+                       **({"fp8_linears": fp8_names} if fp8_names else {})},
             "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "roofline": roofline, "mfu": mfu,
             "kernel_ms_per_step": kernel_ms, "hbm": hbm, "loss_first_last": [losses[0], losses[-1]],
-            "workspace_bytes": model.bytes,
+            "workspace_bytes": model.bytes + getattr(model, "fp8_bytes", 0),
             "peak_device_bytes": torch.cuda.max_memory_allocated()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config)

@@ -140,6 +140,34 @@ int gpt2_set_grad_accumulation(gpt2_t* m, int accumulate);
 /* Set every parameter gradient to 0 (enqueued on the model's stream). */
 int gpt2_zero_grad(gpt2_t* m);
 
+/* ---- FP8 linear layers (the modded-nanogpt project page, "NanoGPT (124M)
+ * in 90 seconds", "How it works": FP8 for the MLP forward and backward
+ * passes, the QKV projections and the head) ----
+ *
+ * mask: GPT2_FP8_QKV (the QKV projection), GPT2_FP8_MLP (both MLP linears),
+ * GPT2_FP8_HEAD (the tied LM head), OR-ed; 0 (the default) keeps every
+ * matmul in bf16. In a selected linear all three products (output, input
+ * gradient, weight gradient) take FP8 operands on the tensor cores
+ * (tcgen05 kind::f8f6f4, fp32 accumulation): activations and weights in
+ * e4m3, the output gradient in e5m2, each tensor with its own per-tensor
+ * scale fmax / amax taken just before the product (the forward's scales of
+ * x and W also serve the backward's transposed codes of the same tensors).
+ * Outputs stay bf16 (fp32 for weight gradients), biases, GELU and the bias
+ * gradients as in the bf16 step. bf16 mode only (else GPT2_ERR_ARG); B*T
+ * must then be a multiple of 16 (gpt2_forward returns GPT2_ERR_ARG
+ * otherwise).
+ *
+ * gpt2_fp8_workspace_bytes: the size of the second device workspace the
+ * FP8 codes need (0 for mask 0); gpt2_set_fp8 takes it (1024-byte aligned,
+ * owned by the caller, not needed with mask 0) and the mask. The next
+ * gpt2_forward starts a new step; gpt2_step recaptures its graph. */
+#define GPT2_FP8_QKV 1
+#define GPT2_FP8_MLP 2
+#define GPT2_FP8_HEAD 4
+#define GPT2_FP8_ALL 7
+int gpt2_fp8_workspace_bytes(const gpt2_config* cfg, int mask, size_t* bytes_out);
+int gpt2_set_fp8(gpt2_t* m, int mask, void* d_workspace, size_t workspace_bytes);
+
 /* ||g||_2 over all parameter gradients (fp32, deterministic two-stage sum),
  * kept on the device; if norm_out is not NULL it is also written there after
  * one stream synchronisation. */
@@ -263,6 +291,7 @@ enum {
     GPT2_K_LAYERNORM_BWD, GPT2_K_GELU_BWD, GPT2_K_BIAS_BWD, GPT2_K_ATTENTION_BWD,
     GPT2_K_RESIDUAL_BWD, GPT2_K_ENCODER_BWD, GPT2_K_ADAMW,
     GPT2_K_GRAD_COLSUM, /* the deferred column sums of the LayerNorm and bias gradients */
+    GPT2_K_FP8_QUANT,   /* FP8 quantization of the FP8 linear layers' operands */
     GPT2_K_COUNT
 };
 

@@ -145,6 +145,29 @@ int gpt2_op_quantize_fp8(void* q, float* scales, const void* x, int64_t n, int f
 int gpt2_op_matmul_fp8(void* D, const void* A, int a_format, const float* a_scales, const void* B, int b_format,
                        const float* b_scales, const void* bias, int M, int N, int K, int* d_status, void* stream);
 
+/* The codes of x [R][C] (bf16, row-major, C % 8 == 0, 16-byte aligned) under
+ * the scales of an earlier gpt2_op_quantize_fp8 of the same values (scales[0]
+ * multiplies, as there), written transposed to qt [C][R] and, when q is not
+ * null, also as they are to q [R][C]: the same codes gpt2_op_quantize_fp8
+ * gives, in the K-major layout the weight-gradient and input-gradient
+ * products of an FP8 linear layer read. */
+int gpt2_op_quantize_fp8_transpose(void* qt, void* q, const float* scales, const void* x, int R, int C,
+                                   int format, void* stream);
+
+/* The general FP8 product: epi 0: D[M,N] = (A B^T) a_scales[1] b_scales[1]
+ * (+ bias), in bf16 or (d_fp32) fp32, accumulate (fp32 only): D += instead;
+ * epi 1 (the MLP's first linear and its GELU): u = that product + bias
+ * rounded to bf16, D = gelu'(u), D2 = gelu(u) (bf16); epi 2 (the input
+ * gradient through the GELU): D = bf16(A B^T scales) * aux[m,n] (aux bf16
+ * [M,N]). A [M,K], B [N,K] FP8 codes, K-major, K % 16 == 0, N % 8 == 0;
+ * scratch: gpt2_op_matmul_fp8_scratch(M, N, K, d_fp32, accumulate) bytes
+ * (split-K partial tiles of an fp32 product). */
+size_t gpt2_op_matmul_fp8_scratch(int M, int N, int K, int d_fp32, int accumulate);
+int gpt2_op_matmul_fp8_ex(int epi, void* D, void* D2, const void* aux, int d_fp32, int accumulate, const void* A,
+                          int a_format, const float* a_scales, const void* B, int b_format, const float* b_scales,
+                          const void* bias, int M, int N, int K, void* scratch, size_t scratch_bytes, int* d_status,
+                          void* stream);
+
 /* Linear forward with the GELU after it fused into the GEMM epilogue (the
  * MLP's first linear, "matmul_forward", followed by "gelu_forward" in the
  * kernel table): u = A W^T + bias (A [M,K], W [N,K] row-major, bias [N]

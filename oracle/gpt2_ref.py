@@ -35,6 +35,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
+from oracle import fp8_ref as F8
+
 LN_EPS = 1e-5
 GELU_K = math.sqrt(2.0 / math.pi)
 GELU_A = 0.044715
@@ -178,6 +180,25 @@ def linear_forward(x, w, b=None):
     return y
 
 
+def _fp8(a, fmt):
+    """The values a per-tensor FP8 quantization of a (fp8_ref.quantize: scale
+    fmax / amax, codes rounded to nearest, ties to even) stands for:
+    decode(codes) * amax / fmax, in float64."""
+    codes, scale_inv = F8.quantize(a, fmt)
+    return F8.fp8_decode(codes, fmt) * float(scale_inv)
+
+
+def linear_forward_fp8(x, w, b=None):
+    """The FP8 linear layer (modded-nanogpt project page, "How it works":
+    FP8 for the MLP, the QKV projections and the head): y = x w^T (+ b) with x
+    and w each quantized per tensor to e4m3 first, the product of the
+    quantized values in float64; returned in x's dtype."""
+    y = _fp8(x, "e4m3") @ _fp8(w, "e4m3").T
+    if b is not None:
+        y = y + b
+    return y.astype(np.asarray(x).dtype)
+
+
 def _split_heads(qkv, n_head):
     B, T, C3 = qkv.shape
     C = C3 // 3
@@ -253,6 +274,16 @@ def linear_backward(dy, x, w):
     dy [N, out], x [N, in] (leading axes flattened by the caller).
     """
     return dy @ w, dy.T @ x, dy.sum(axis=0)
+
+
+def linear_backward_fp8(dy, x, w):
+    """The FP8 linear layer's gradients: dy quantized per tensor to e5m2
+    (the wider range of gradients), x and w to e4m3 (as in the forward),
+    dx = dy w and dw = dy^T x of the quantized values in float64; db is the
+    column sums of dy itself. Returned in dy's dtype."""
+    dt = np.asarray(dy).dtype
+    qdy, qx, qw = _fp8(dy, "e5m2"), _fp8(x, "e4m3"), _fp8(w, "e4m3")
+    return (qdy @ qw).astype(dt), (qdy.T @ qx).astype(dt), dy.sum(axis=0)
 
 
 def layernorm_backward(dy, x, gamma, mean, rstd):
@@ -381,34 +412,37 @@ def lr_cosine(t, warmup, total, lr_max, lr_min):
 # The whole step
 # --------------------------------------------------------------------------
 
-def forward(cfg: Config, params: dict, tokens, targets=None, dtype=np.float64):
+def forward(cfg: Config, params: dict, tokens, targets=None, dtype=np.float64, fp8=()):
     """Forward pass. Returns (mean loss or None, cache for backward).
 
     Per layer: h1 = LN1(x); qkv = h1 Wqkv^T + b; o = attn(qkv); x1 = x + o Wproj^T + b;
     h2 = LN2(x1); u = h2 Wfc^T + b; g = gelu(u); x = x1 + g Wfcproj^T + b.
     Then hf = LNf(x); logits = hf wte^T (tied head, no bias).
+    fp8: the linears that run as FP8 linear layers, any of "qkv", "mlp" (both
+    MLP linears) and "head".
     """
     P = {k: np.asarray(v, dtype=dtype) for k, v in params.items()}
     tokens = np.asarray(tokens)
     B, T = tokens.shape
     C = cfg.n_embd
-    cache = {"tokens": tokens, "P": P, "layers": []}
+    lin = {k: (linear_forward_fp8 if k in fp8 else linear_forward) for k in ("qkv", "mlp", "head")}
+    cache = {"tokens": tokens, "P": P, "layers": [], "fp8": tuple(fp8)}
     x = encoder_forward(P["wte"], P["wpe"], tokens)
     for l in range(cfg.n_layer):
         p = f"h{l}."
         lc = {"x": x}
         h1, lc["mean1"], lc["rstd1"] = layernorm_forward(x, P[p + "ln1.g"], P[p + "ln1.b"])
-        qkv = linear_forward(h1, P[p + "qkv.w"], P[p + "qkv.b"])
+        qkv = lin["qkv"](h1, P[p + "qkv.w"], P[p + "qkv.b"])
         o, lse = attention_forward(qkv, cfg.n_head)
         x1 = x + linear_forward(o, P[p + "proj.w"], P[p + "proj.b"])
         h2, lc["mean2"], lc["rstd2"] = layernorm_forward(x1, P[p + "ln2.g"], P[p + "ln2.b"])
-        u = linear_forward(h2, P[p + "fc.w"], P[p + "fc.b"])
+        u = lin["mlp"](h2, P[p + "fc.w"], P[p + "fc.b"])
         g = gelu_forward(u)
-        x = x1 + linear_forward(g, P[p + "fcproj.w"], P[p + "fcproj.b"])
+        x = x1 + lin["mlp"](g, P[p + "fcproj.w"], P[p + "fcproj.b"])
         lc.update(h1=h1, qkv=qkv, o=o, lse=lse, x1=x1, h2=h2, u=u, g=g)
         cache["layers"].append(lc)
     hf, meanf, rstdf = layernorm_forward(x, P["lnf.g"], P["lnf.b"])
-    logits = linear_forward(hf, P["wte"])  # [B, T, Vp]
+    logits = lin["head"](hf, P["wte"])  # [B, T, Vp]
     cache.update(xL=x, hf=hf, meanf=meanf, rstdf=rstdf, logits=logits)
     if targets is None:
         return None, cache
@@ -427,19 +461,21 @@ def backward(cfg: Config, cache: dict) -> dict:
     C = cfg.n_embd
     N = B * T
     grads = {}
+    fp8 = cache.get("fp8", ())
+    lin = {k: (linear_backward_fp8 if k in fp8 else linear_backward) for k in ("qkv", "mlp", "head")}
     dlogits = cache["dlogits"]
     hf = cache["hf"].reshape(N, C)
-    dhf, dwte_head, _ = linear_backward(dlogits, hf, P["wte"])
+    dhf, dwte_head, _ = lin["head"](dlogits, hf, P["wte"])
     dx, grads["lnf.g"], grads["lnf.b"] = layernorm_backward(
         dhf.reshape(B, T, C), cache["xL"], P["lnf.g"], cache["meanf"], cache["rstdf"])
     for l in reversed(range(cfg.n_layer)):
         p = f"h{l}."
         lc = cache["layers"][l]
         # MLP branch: x_out = x1 + fcproj(gelu(fc(LN2(x1))))
-        dg, grads[p + "fcproj.w"], grads[p + "fcproj.b"] = linear_backward(
+        dg, grads[p + "fcproj.w"], grads[p + "fcproj.b"] = lin["mlp"](
             dx.reshape(N, C), lc["g"].reshape(N, 4 * C), P[p + "fcproj.w"])
         du = gelu_backward(lc["u"].reshape(N, 4 * C), dg)
-        dh2, grads[p + "fc.w"], grads[p + "fc.b"] = linear_backward(
+        dh2, grads[p + "fc.w"], grads[p + "fc.b"] = lin["mlp"](
             du, lc["h2"].reshape(N, C), P[p + "fc.w"])
         dx1_ln, grads[p + "ln2.g"], grads[p + "ln2.b"] = layernorm_backward(
             dh2.reshape(B, T, C), lc["x1"], P[p + "ln2.g"], lc["mean2"], lc["rstd2"])
@@ -448,7 +484,7 @@ def backward(cfg: Config, cache: dict) -> dict:
         do, grads[p + "proj.w"], grads[p + "proj.b"] = linear_backward(
             dx1.reshape(N, C), lc["o"].reshape(N, C), P[p + "proj.w"])
         dqkv = attention_backward(do.reshape(B, T, C), lc["qkv"], lc["lse"], cfg.n_head)
-        dh1, grads[p + "qkv.w"], grads[p + "qkv.b"] = linear_backward(
+        dh1, grads[p + "qkv.w"], grads[p + "qkv.b"] = lin["qkv"](
             dqkv.reshape(N, 3 * C), lc["h1"].reshape(N, C), P[p + "qkv.w"])
         dx_ln, grads[p + "ln1.g"], grads[p + "ln1.b"] = layernorm_backward(
             dh1.reshape(B, T, C), lc["x"], P[p + "ln1.g"], lc["mean1"], lc["rstd1"])
@@ -459,12 +495,13 @@ def backward(cfg: Config, cache: dict) -> dict:
 
 
 def train_step(cfg: Config, params: dict, tokens, targets, state: dict | None,
-               lr, beta1, beta2, eps, weight_decay, t, dtype=np.float64):
+               lr, beta1, beta2, eps, weight_decay, t, dtype=np.float64, fp8=()):
     """forward -> backward -> AdamW. Returns (loss, grads, new_params, new_state).
 
     state holds the moments {"m": {name: arr}, "v": {...}}; None means zeros (t = 1).
+    fp8: the FP8 linear layers (see forward).
     """
-    loss, cache = forward(cfg, params, tokens, targets, dtype=dtype)
+    loss, cache = forward(cfg, params, tokens, targets, dtype=dtype, fp8=fp8)
     grads = backward(cfg, cache)
     new_params, m_new, v_new = {}, {}, {}
     for name, theta in params.items():

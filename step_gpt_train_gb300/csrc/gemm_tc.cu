@@ -222,13 +222,13 @@ static __device__ int stall_for_test = 0;
 
 // F8: FP8 operands, e4m3 or e5m2 each (K-major only): a k-block is 128 values,
 // four K = 32 MMAs of kind::f8f6f4, and the epilogue scales the accumulator by
-// a_scale * b_scale.
+// a_scale * b_scale before its bias and operation.
 template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                    const GemmArgs g) {
-    static_assert(!F8 || (!A_MN && !B_MN && EPI == EPI_NONE), "FP8 operands: K-major, plain epilogue");
+    static_assert(!F8 || (!A_MN && !B_MN), "FP8 operands: K-major");
     constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::STAGES;
@@ -1090,6 +1090,16 @@ bool launch_tc_layout(int epi, int a_mn, int b_mn, const CUtensorMap& ma, const 
     return true;
 }
 
+// FP8 operands (K-major): the plain, GELU-forward and GELU-backward epilogues.
+template <int BN>
+bool launch_tc_layout_f8(int epi, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                         const CUtensorMap& md2, const GemmArgs& args, int grid, cudaStream_t s) {
+    if (epi == EPI_GELU) launch_tc<BN, false, false, EPI_GELU, true>(ma, mb, md, md2, args, grid, s);
+    else if (epi == EPI_MUL) launch_tc<BN, false, false, EPI_MUL, true>(ma, mb, md, md2, args, grid, s);
+    else launch_tc<BN, false, false, EPI_NONE, true>(ma, mb, md, md2, args, grid, s);
+    return true;
+}
+
 // CTA-pair kernel: the layouts and epilogues the step uses (as launch_tc_layout),
 // launched in clusters of two.
 template <bool A_MN, bool B_MN, int EPI>
@@ -1171,18 +1181,25 @@ size_t matmul_tc_scratch(int M, int N, int K, int d_fp32, int accumulate) {
     return p.splits > 1 || (d_fp32 && accumulate) ? (size_t)p.units * BM * p.bn * 4 : 0;
 }
 
+// FP8 operands: a k-block holds 128 values (the bytes and MMA time of a 64-value
+// bf16 k-block), so the plan is the one of a bf16 product with K / 2.
+size_t matmul_f8_scratch(int M, int N, int K, int d_fp32, int accumulate) {
+    return matmul_tc_scratch(M, N, (K + 1) / 2, d_fp32, accumulate);
+}
+
 
 namespace {
 
 // D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
 int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
               int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s,
-              int accumulate = 0, float* colsum = nullptr) {
-    Plan p = make_plan(M, N, K, epi == EPI_NONE ? d_fp32 : 0);
+              int accumulate = 0, float* colsum = nullptr, const F8Args* f8 = nullptr) {
+    if (f8 && (a_mn || b_mn || K % 16 || N % 8)) return GPT2_ERR_ARG;
+    Plan p = make_plan(M, N, f8 ? (K + 1) / 2 : K, epi == EPI_NONE ? d_fp32 : 0);
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
-    if (use_pair(M, N, partials) && !colsum) {
+    if (use_pair(M, N, partials) && !colsum && !f8) {
         // 256 x 256 pair tiles, each CTA loading 128 rows of A and 128 columns of B
         const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + PBN - 1) / PBN;
         CUtensorMap ma, mb, md, md2;
@@ -1232,9 +1249,14 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         return e == cudaSuccess ? 1 : GPT2_ERR_CUDA;
     }
     CUtensorMap ma, mb;
-    bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
-    ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
-                     : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
+    bool ok;
+    if (f8) {
+        ok = make_map_u8(&ma, A, (uint64_t)K, (uint64_t)M, BM) && make_map_u8(&mb, B, (uint64_t)K, (uint64_t)N, p.bn);
+    } else {
+        ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, BM);
+        ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
+                         : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)p.bn));
+    }
     CUtensorMap md, md2;
     if (partials) ok = ok && make_out_map(&md, scratch, true, (uint64_t)p.bn, BM, (uint64_t)p.units);
     else ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
@@ -1260,8 +1282,18 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     g.num_kb = p.num_kb;
     g.m_tiles = p.m_tiles;
     g.group_n = partials ? p.n_tiles : p.group_n;  // the reduce kernel finds partials in row-major order
+    if (f8) {
+        g.a_scale = f8->a_scale;
+        g.b_scale = f8->b_scale;
+        g.a_fmt = f8->a_fmt;
+        g.b_fmt = f8->b_fmt;
+    }
     bool launched;
-    if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
+    if (f8) {
+        if (p.bn == 128) launched = launch_tc_layout_f8<128>(epi, ma, mb, md, md2, g, p.grid, s);
+        else if (p.bn == 192) launched = launch_tc_layout_f8<192>(epi, ma, mb, md, md2, g, p.grid, s);
+        else launched = launch_tc_layout_f8<256>(epi, ma, mb, md, md2, g, p.grid, s);
+    } else if (p.bn == 128) launched = launch_tc_layout<128>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else if (p.bn == 192) launched = launch_tc_layout<192>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     else launched = launch_tc_layout<256>(epi, a_mn, b_mn, ma, mb, md, md2, g, p.grid, s);
     if (!launched) return GPT2_ERR_ARG;
@@ -1281,41 +1313,30 @@ int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale
                       const float* b_scale, const bf16* bias, int M, int N, int K, int* status, cudaStream_t s) {
     if (!D || !A || !B || !a_scale || !b_scale || M < 1 || N < 1 || K < 1) return GPT2_ERR_ARG;
     if ((a_fmt != FP8_E4M3 && a_fmt != FP8_E5M2) || (b_fmt != FP8_E4M3 && b_fmt != FP8_E5M2)) return GPT2_ERR_ARG;
-    if (K % 16 != 0 || N % 8 != 0) return GPT2_ERR_ARG;  // 16-byte row strides of A, B and D
-    Plan p = make_plan(M, N, K, 0);  // tile width and grid as for bf16; one k-range per tile
-    p.num_kb = (K + 127) / 128;
-    p.kbs = p.num_kb;
-    p.splits = 1;
-    p.units = p.tiles;
-    p.grid = p.units < gpt2_num_sms() ? p.units : gpt2_num_sms();
-    CUtensorMap ma, mb, md;
-    bool ok = make_map_u8(&ma, A, (uint64_t)K, (uint64_t)M, BM) && make_map_u8(&mb, B, (uint64_t)K, (uint64_t)N, p.bn) &&
-              make_out_map(&md, D, false, (uint64_t)N, (uint64_t)M, 1);
-    if (!ok) return GPT2_ERR_CUDA;
-    GemmArgs g = {};
-    g.bias = bias;
-    g.aux = nullptr;
-    g.status = status;
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.d_fp32 = 0;
-    g.splits = 1;
-    g.partials = 0;
-    g.kbs = p.kbs;
-    g.n_tiles = p.n_tiles;
-    g.units = p.units;
-    g.num_kb = p.num_kb;
-    g.m_tiles = p.m_tiles;
-    g.group_n = p.group_n;
-    g.a_scale = a_scale;
-    g.b_scale = b_scale;
-    g.a_fmt = a_fmt;
-    g.b_fmt = b_fmt;
-    if (p.bn == 128) launch_tc<128, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
-    else if (p.bn == 192) launch_tc<192, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
-    else launch_tc<256, false, false, EPI_NONE, true>(ma, mb, md, md, g, p.grid, s);
-    return 1;
+    const F8Args f8 = {a_fmt, b_fmt, a_scale, b_scale};
+    return matmul_tc(EPI_NONE, D, nullptr, nullptr, 0, A, 0, B, 0, bias, M, N, K, nullptr, status, s, 0, nullptr, &f8);
+}
+
+int launch_matmul_f8(void* D, int d_fp32, const uint8_t* A, const uint8_t* B, const F8Args& f8, const void* bias,
+                     int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate) {
+    if (M == 0 || N == 0) return 0;
+    return matmul_tc(EPI_NONE, D, nullptr, nullptr, d_fp32, A, 0, B, 0, bias, M, N, K, scratch, status, s, accumulate,
+                     nullptr, &f8);
+}
+
+int launch_matmul_gelu_f8(void* dgelu, void* out, const uint8_t* A, const uint8_t* W, const F8Args& f8,
+                          const void* bias, int M, int N, int K, int* status, cudaStream_t s) {
+    if (M == 0 || N == 0) return 0;
+    return matmul_tc(EPI_GELU, dgelu, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s, 0, nullptr,
+                     &f8);
+}
+
+int launch_matmul_gelu_backward_f8(void* du, const uint8_t* dY, const uint8_t* WT, const F8Args& f8,
+                                   const void* dgelu, int M, int N, int K, int* status, cudaStream_t s,
+                                   float* du_colsum) {
+    if (M == 0 || N == 0) return 0;
+    return matmul_tc(EPI_MUL, du, nullptr, (const bf16*)dgelu, 0, dY, 0, WT, 0, nullptr, M, N, K, nullptr, status, s,
+                     0, du_colsum, &f8);
 }
 
 int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,

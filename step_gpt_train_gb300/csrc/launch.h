@@ -128,6 +128,35 @@ int launch_matmul_fp8(bf16* D, const uint8_t* A, int a_fmt, const float* a_scale
 // q = fp8(x * scales[0]), round to nearest even, saturated; partial: fp8_quantize_scratch() bytes.
 size_t fp8_quantize_scratch();
 int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, int fmt, float* partial, cudaStream_t s);
+// Its two passes alone: the scales of n values (2 launches), and the codes of n
+// values under given scales.
+int launch_fp8_amax_scale(float* scales, const bf16* x, int64_t n, int fmt, float* partial, cudaStream_t s);
+int launch_quantize_fp8_rows(uint8_t* q, const float* scales, const bf16* x, int64_t n, int fmt, cudaStream_t s);
+// The codes of x [R][C] (C % 8 == 0) under given scales written transposed,
+// qt [C][R], and (q non-null) also as they are, q [R][C].
+int launch_quantize_fp8_t(uint8_t* qt, uint8_t* q, const float* scales, const bf16* x, int R, int C, int fmt,
+                          cudaStream_t s);
+
+// FP8 operands of the general matmul (K-major codes, scale_inv device scalars).
+struct F8Args {
+    int a_fmt, b_fmt;
+    const float* a_scale;  // amax / fmax of A's codes (the factor that maps them back)
+    const float* b_scale;
+};
+// The matmul, its GELU-forward and GELU-backward epilogue forms with FP8
+// operands: as launch_matmul_tc, launch_matmul_gelu and
+// launch_matmul_gelu_backward, A [M,K] and B [N,K] FP8 codes (both K-major;
+// the input gradient takes the weight's transposed codes), the accumulator
+// scaled by *a_scale * *b_scale. K % 16 == 0, N % 8 == 0.
+int launch_matmul_f8(void* D, int d_fp32, const uint8_t* A, const uint8_t* B, const F8Args& f8, const void* bias,
+                     int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate = 0);
+int launch_matmul_gelu_f8(void* dgelu, void* out, const uint8_t* A, const uint8_t* W, const F8Args& f8,
+                          const void* bias, int M, int N, int K, int* status, cudaStream_t s);
+int launch_matmul_gelu_backward_f8(void* du, const uint8_t* dY, const uint8_t* WT, const F8Args& f8,
+                                   const void* dgelu, int M, int N, int K, int* status, cudaStream_t s,
+                                   float* du_colsum = nullptr);
+// Scratch of launch_matmul_f8 (split-K partial tiles of an fp32 output).
+size_t matmul_f8_scratch(int M, int N, int K, int d_fp32, int accumulate = 0);
 
 // Matmul: D[M,N] = sum_k A(m,k) B(n,k) (+ bias), see gpt2_op_matmul.
 // accumulate (fp32 D only): D += the product instead of D = it; the scratch

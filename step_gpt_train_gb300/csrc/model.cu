@@ -81,6 +81,14 @@ struct gpt2 {
     float* cs_pool;
     size_t cs_pool_bytes, cs_used;
     std::vector<ColsumJob> cs_jobs;
+    // FP8 linear layers (gpt2_set_fp8): which ones, and the codes they read,
+    // in the caller's second workspace
+    int fp8 = 0;
+    uint8_t *f8_x = nullptr, *f8_xT = nullptr, *f8_w = nullptr, *f8_wT = nullptr, *f8_dy = nullptr, *f8_dyT = nullptr;
+    float* f8_scales = nullptr;   // per FP8 linear: (scale, 1/scale) of x, W and dy
+    float* f8_partial = nullptr;  // amax partials
+    void* f8_scratch = nullptr;   // split-K partial tiles of the FP8 weight gradients
+    size_t f8_scratch_bytes = 0;
     int B, T;
     int state;  // 0: none, 1: forward with targets done, 2: backward done
     int grad_accum;          // backward adds into the gradients instead of overwriting them
@@ -96,11 +104,11 @@ struct gpt2 {
     std::vector<cudaEvent_t> pool;
     // gpt2_step: the captured step and what it was captured for
     struct StepKey {
-        int B, T, grad_accum, clip, decay_mask;
+        int B, T, grad_accum, clip, decay_mask, fp8;
         float max_grad_norm;
         bool operator==(const StepKey& o) const {
             return B == o.B && T == o.T && grad_accum == o.grad_accum && clip == o.clip &&
-                   decay_mask == o.decay_mask && max_grad_norm == o.max_grad_norm;
+                   decay_mask == o.decay_mask && fp8 == o.fp8 && max_grad_norm == o.max_grad_norm;
         }
     };
     StepKey step_key{};
@@ -414,6 +422,145 @@ void cs_defer(gpt2* m, const float* partial, int rows, int ncols, int seg, float
     m->cs_jobs.push_back(j);
 }
 
+// ---- FP8 linear layers ----
+// Per-tensor current scaling: each operand's codes use the scale of its own
+// amax, taken just before the product (the scales of x and W taken in the
+// forward serve the backward's transposed codes of the same, unchanged
+// tensors). Activations and weights in e4m3, output gradients in e5m2.
+
+// The FP8 linears as (in, out) sizes: qkv, fc, fcproj, head.
+struct F8Lin {
+    int mask_bit, in, out;
+};
+std::vector<F8Lin> f8_linears(const gpt2_config* c, int mask) {
+    const int C = c->n_embd;
+    std::vector<F8Lin> v;
+    if (mask & GPT2_FP8_QKV) v.push_back({GPT2_FP8_QKV, C, 3 * C});
+    if (mask & GPT2_FP8_MLP) {
+        v.push_back({GPT2_FP8_MLP, C, 4 * C});
+        v.push_back({GPT2_FP8_MLP, 4 * C, C});
+    }
+    if (mask & GPT2_FP8_HEAD) v.push_back({GPT2_FP8_HEAD, C, c->vocab_padded});
+    return v;
+}
+
+// Carve the FP8 workspace (m == nullptr: the size only).
+size_t fp8_plan(const gpt2_config* c, int mask, gpt2* m, uint8_t* w) {
+    const size_t BT = (size_t)c->max_B * c->max_T;
+    size_t max_in = 0, max_out = 0, max_w = 0, scr = 0;
+    for (const F8Lin& f : f8_linears(c, mask)) {
+        max_in = std::max(max_in, (size_t)f.in);
+        max_out = std::max(max_out, (size_t)f.out);
+        max_w = std::max(max_w, (size_t)f.in * f.out);
+        scr = std::max(scr, matmul_f8_scratch(f.out, f.in, (int)BT, 1, 1));
+    }
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        off = align_up(off, WS_ALIGN);
+        const size_t r = off;
+        off += bytes;
+        return r;
+    };
+    const size_t o_x = take(BT * max_in), o_xT = take(BT * max_in), o_w = take(max_w), o_wT = take(max_w);
+    const size_t o_dy = take(BT * max_out), o_dyT = take(BT * max_out);
+    const size_t o_sc = take((size_t)(3 * c->n_layer + 1) * 8 * 4), o_part = take(fp8_quantize_scratch());
+    const size_t o_scr = take(std::max(scr, (size_t)256));
+    if (m) {
+        m->f8_x = w + o_x;
+        m->f8_xT = w + o_xT;
+        m->f8_w = w + o_w;
+        m->f8_wT = w + o_wT;
+        m->f8_dy = w + o_dy;
+        m->f8_dyT = w + o_dyT;
+        m->f8_scales = (float*)(w + o_sc);
+        m->f8_partial = (float*)(w + o_part);
+        m->f8_scratch = w + o_scr;
+        m->f8_scratch_bytes = std::max(scr, (size_t)256);
+    }
+    return align_up(off, WS_ALIGN);
+}
+
+enum { F8_QKV = 0, F8_FC = 1, F8_FCPROJ = 2 };
+inline float* f8_sc(gpt2* m, int slot) { return m->f8_scales + (size_t)slot * 8; }
+
+// y = x W^T + b with FP8 operands (y2: the GELU form, y = gelu'(u), y2 = gelu(u)).
+int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, int bi, int BT, int in, int out) {
+    float* sc = f8_sc(m, slot);
+    const bf16* xb = (const bf16*)x;
+    const bf16* wb = (const bf16*)P(m, wi);
+    {
+        Op op(m, GPT2_K_FP8_QUANT);
+        int n = 0, r;
+        const int64_t nx = (int64_t)BT * in, nw = (int64_t)out * in;
+        if ((r = launch_fp8_amax_scale(sc, xb, nx, FP8_E4M3, m->f8_partial, m->stream)) < 0) return r;
+        n += r;
+        if ((r = launch_quantize_fp8_rows(m->f8_x, sc, xb, nx, FP8_E4M3, m->stream)) < 0) return r;
+        n += r;
+        if ((r = launch_fp8_amax_scale(sc + 2, wb, nw, FP8_E4M3, m->f8_partial, m->stream)) < 0) return r;
+        n += r;
+        if ((r = launch_quantize_fp8_rows(m->f8_w, sc + 2, wb, nw, FP8_E4M3, m->stream)) < 0) return r;
+        TRY(op.done(n + r, 5.0 * (double)(nx + nw)));
+    }
+    const F8Args f8 = {FP8_E4M3, FP8_E4M3, sc + 1, sc + 3};
+    const void* bias = bi >= 0 ? P(m, bi) : nullptr;
+    Op op(m, GPT2_K_MATMUL);
+    const double flops = 2.0 * BT * out * in;
+    if (y2) return op.done(launch_matmul_gelu_f8(y, y2, m->f8_x, m->f8_w, f8, bias, BT, out, in, m->status, m->stream), flops);
+    return op.done(launch_matmul_f8(y, 0, m->f8_x, m->f8_w, f8, bias, BT, out, in, nullptr, m->status, m->stream), flops);
+}
+
+// dx = dy W and dW (+)= dy^T x with FP8 operands (dy in e5m2, its codes in
+// both layouts; W and x transposed under their forward scales); the bias
+// gradient from dy as stored (bf16), deferred. aux: dx is the gradient
+// through the GELU, bf16(dy W) * aux, with its column sums to colsum.
+int f8_linear_bwd(gpt2* m, int slot, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in,
+                  int out, const void* aux, float* colsum) {
+    float* sc = f8_sc(m, slot);
+    const bf16* dyb = (const bf16*)dy;
+    {
+        Op op(m, GPT2_K_FP8_QUANT);
+        int n = 0, r;
+        const int64_t ny = (int64_t)BT * out;
+        if ((r = launch_fp8_amax_scale(sc + 4, dyb, ny, FP8_E5M2, m->f8_partial, m->stream)) < 0) return r;
+        n += r;
+        if ((r = launch_quantize_fp8_t(m->f8_dyT, m->f8_dy, sc + 4, dyb, BT, out, FP8_E5M2, m->stream)) < 0) return r;
+        n += r;
+        if ((r = launch_quantize_fp8_t(m->f8_wT, nullptr, sc + 2, (const bf16*)P(m, wi), out, in, FP8_E4M3,
+                                       m->stream)) < 0)
+            return r;
+        n += r;
+        if ((r = launch_quantize_fp8_t(m->f8_xT, nullptr, sc, (const bf16*)x, BT, in, FP8_E4M3, m->stream)) < 0)
+            return r;
+        TRY(op.done(n + r, 4.0 * ny + 2.0 * ny + 3.0 * (double)out * in + 3.0 * (double)BT * in));
+    }
+    const double flops = 2.0 * BT * in * out;
+    {
+        const F8Args f8 = {FP8_E5M2, FP8_E4M3, sc + 5, sc + 3};
+        Op op(m, GPT2_K_MATMUL);
+        const int r = aux ? launch_matmul_gelu_backward_f8(dx, m->f8_dy, m->f8_wT, f8, aux, BT, in, out, m->status,
+                                                           m->stream, colsum)
+                          : launch_matmul_f8(dx, 0, m->f8_dy, m->f8_wT, f8, nullptr, BT, in, out, nullptr, m->status,
+                                             m->stream);
+        TRY(op.done(r, flops));
+    }
+    {
+        const F8Args f8 = {FP8_E5M2, FP8_E4M3, sc + 5, sc + 1};
+        Op op(m, GPT2_K_MATMUL);
+        TRY(op.done(launch_matmul_f8(G(m, wi), 1, m->f8_dyT, m->f8_xT, f8, nullptr, out, in, BT, m->f8_scratch,
+                                     m->status, m->stream, m->grad_accum),
+                    flops));
+    }
+    if (bi >= 0) {
+        float* part = cs_take(m, (int)((BT + 127) / 128), out);
+        if (!part) return GPT2_ERR_WORKSPACE;
+        Op op(m, GPT2_K_BIAS_BWD);
+        int rows = 0;
+        TRY(op.done(launch_bias_partials(m->dtype, part, dy, BT, out, m->stream, &rows), (double)BT * out * m->act));
+        cs_defer(m, part, rows, out, out, G(m, bi), nullptr, nullptr);
+    }
+    return GPT2_OK;
+}
+
 int op_matmul(gpt2* m, void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
               int N, int K, int accumulate = 0) {
     Op op(m, GPT2_K_MATMUL);
@@ -478,6 +625,8 @@ double attn_fwd_flops(int B, int T, int C) { return 2.0 * 2.0 * B * C * (double)
 
 int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
     const int BT = B * T, C = m->C, L = m->L;
+    if (m->fp8 && BT % 16) return GPT2_ERR_ARG;  // the FP8 weight gradients contract over B*T in 16-byte rows
+    const bool f8_qkv = m->fp8 & GPT2_FP8_QKV, f8_mlp = m->fp8 & GPT2_FP8_MLP, f8_head = m->fp8 & GPT2_FP8_HEAD;
     {
         Op op(m, GPT2_K_ENCODER_FWD);
         TRY(op.done(launch_encoder_forward(m->dtype, m->layers[0].x, m->tokens, P(m, T_WTE), P(m, T_WPE), B, T, C,
@@ -488,7 +637,8 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
     TRY(ln_fwd(m, m->layers[0].ln1, m->layers[0].mean1, m->layers[0].rstd1, m->layers[0].x, tidx(0, 0), BT));
     for (int l = 0; l < L; l++) {
         LayerBufs& b = m->layers[l];
-        TRY(linear_fwd(m, b.qkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
+        if (f8_qkv) TRY(f8_linear_fwd(m, 3 * l + F8_QKV, b.qkv, nullptr, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
+        else TRY(linear_fwd(m, b.qkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
         {
             Op op(m, GPT2_K_ATTENTION_FWD);
             TRY(op.done(launch_attention_forward(m->dtype, b.atty, b.lse, b.qkv, B, T, C, m->H, m->status, m->stream),
@@ -496,7 +646,9 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
         }
         TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
         TRY(res_ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, b.x, m->fwd_tmp, tidx(l, 6), BT));
-        if (m->dtype == GPT2_MODE_BF16) {
+        if (f8_mlp) {
+            TRY(f8_linear_fwd(m, 3 * l + F8_FC, b.fch, b.fchg, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
+        } else if (m->dtype == GPT2_MODE_BF16) {
             // the GELU runs in the epilogue of its linear, which keeps gelu'
             // (in fch) for the backward instead of the GELU input
             Op op(m, GPT2_K_MATMUL);
@@ -509,7 +661,9 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
             TRY(op.done(launch_gelu_forward(m->dtype, b.fchg, b.fch, (int64_t)BT * 4 * C, m->stream),
                         2.0 * BT * 4 * C * m->act));
         }
-        TRY(linear_fwd(m, m->fwd_tmp, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
+        if (f8_mlp)
+            TRY(f8_linear_fwd(m, 3 * l + F8_FCPROJ, m->fwd_tmp, nullptr, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
+        else TRY(linear_fwd(m, m->fwd_tmp, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
         if (l + 1 < L) {
             LayerBufs& n = m->layers[l + 1];
             TRY(res_ln_fwd(m, n.ln1, n.mean1, n.rstd1, n.x, b.x1, m->fwd_tmp, tidx(l + 1, 0), BT));
@@ -517,7 +671,8 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
             TRY(res_ln_fwd(m, m->lnf, m->meanf, m->rstdf, m->xL, b.x1, m->fwd_tmp, tlnf(L, 0), BT));
         }
     }
-    TRY(op_matmul(m, m->logits, 0, m->lnf, 0, P(m, T_WTE), 0, nullptr, BT, m->Vp, C));
+    if (f8_head) TRY(f8_linear_fwd(m, 3 * L, m->logits, nullptr, m->lnf, T_WTE, -1, BT, C, m->Vp));
+    else TRY(op_matmul(m, m->logits, 0, m->lnf, 0, P(m, T_WTE), 0, nullptr, BT, m->Vp, C));
     if (targets) {
         {
             Op op(m, GPT2_K_CLASSIFIER);
@@ -535,16 +690,30 @@ int backward_impl(gpt2* m) {
     const int B = m->B, T = m->T, BT = B * T, C = m->C, L = m->L;
     m->cs_used = 0;
     m->cs_jobs.clear();
+    const bool f8_qkv = m->fp8 & GPT2_FP8_QKV, f8_mlp = m->fp8 & GPT2_FP8_MLP, f8_head = m->fp8 & GPT2_FP8_HEAD;
     // LM head (tied with wte): dlnf = dlogits wte; dwte = dlogits^T lnf (overwrites dwte)
-    TRY(op_matmul(m, m->dtmp, 0, m->logits, 0, P(m, T_WTE), 1, nullptr, BT, C, m->Vp));
-    TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT, m->grad_accum));
+    if (f8_head) {
+        TRY(f8_linear_bwd(m, 3 * L, m->dtmp, m->logits, m->lnf, T_WTE, -1, BT, C, m->Vp, nullptr, nullptr));
+    } else {
+        TRY(op_matmul(m, m->dtmp, 0, m->logits, 0, P(m, T_WTE), 1, nullptr, BT, C, m->Vp));
+        TRY(op_matmul(m, G(m, T_WTE), 1, m->logits, 1, m->lnf, 1, nullptr, m->Vp, C, BT, m->grad_accum));
+    }
     // the LayerNorm backwards write the residual gradient dres and, on the
     // way, the bias gradient of the projection whose output joins there
     TRY(ln_bwd_res(m, 0, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, tidx(L - 1, 11), BT));
     for (int l = L - 1; l >= 0; l--) {
         LayerBufs& b = m->layers[l];
         // MLP branch
-        if (m->dtype == GPT2_MODE_BF16) {
+        if (f8_mlp) {
+            // the projection's input gradient through the GELU, with the first
+            // linear's bias-gradient partials, and its weight gradient
+            const int rows = matmul_gelu_backward_colsum_rows(BT);
+            float* part = cs_take(m, rows, 4 * C);
+            if (!part) return GPT2_ERR_WORKSPACE;
+            TRY(f8_linear_bwd(m, 3 * l + F8_FCPROJ, m->dbig, m->dres, b.fchg, tidx(l, 10), -1, BT, 4 * C, C, b.fch,
+                              part));
+            cs_defer(m, part, rows, 4 * C, 4 * C, G(m, tidx(l, 9)), nullptr, nullptr);
+        } else if (m->dtype == GPT2_MODE_BF16) {
             // dW of the MLP projection, then its input gradient times the
             // GELU's derivative (kept in fch by the forward), in the GEMM epilogue
             // (and the column sums of that gradient per 32-row slice: the
@@ -564,8 +733,9 @@ int backward_impl(gpt2* m) {
             TRY(op.done(launch_gelu_backward(m->dtype, m->dbig, b.fch, m->dbig, (int64_t)BT * 4 * C, m->stream),
                         3.0 * BT * 4 * C * m->act));
         }
-        TRY(linear_bwd(m, m->dtmp, m->dbig, b.ln2, tidx(l, 8), m->dtype == GPT2_MODE_BF16 ? -1 : tidx(l, 9), BT, C,
-                       4 * C));
+        if (f8_mlp) TRY(f8_linear_bwd(m, 3 * l + F8_FC, m->dtmp, m->dbig, b.ln2, tidx(l, 8), -1, BT, C, 4 * C, nullptr, nullptr));
+        else TRY(linear_bwd(m, m->dtmp, m->dbig, b.ln2, tidx(l, 8), m->dtype == GPT2_MODE_BF16 ? -1 : tidx(l, 9), BT, C,
+                            4 * C));
         TRY(ln_bwd_res(m, 1, m->dtmp, b.x1, tidx(l, 6), b.mean2, b.rstd2, tidx(l, 5), BT));
         // attention branch
         TRY(linear_bwd(m, m->dtmp, m->dres, b.atty, tidx(l, 4), -1, BT, C, C));
@@ -575,7 +745,8 @@ int backward_impl(gpt2* m) {
                                                   m->scratch, m->status, m->stream),
                         2.5 * attn_fwd_flops(B, T, C)));
         }
-        TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
+        if (f8_qkv) TRY(f8_linear_bwd(m, 3 * l + F8_QKV, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C, nullptr, nullptr));
+        else TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
         TRY(ln_bwd_res(m, 1, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, l > 0 ? tidx(l - 1, 11) : -1, BT));
     }
     {
@@ -723,6 +894,26 @@ int gpt2_adamw_step(gpt2_t* m, float lr, float beta1, float beta2, float eps, fl
     return GPT2_OK;
 }
 
+int gpt2_fp8_workspace_bytes(const gpt2_config* cfg, int mask, size_t* bytes_out) {
+    if (!config_ok(cfg) || !bytes_out || mask < 0 || mask > GPT2_FP8_ALL) return GPT2_ERR_ARG;
+    if (mask && cfg->mode != GPT2_MODE_BF16) return GPT2_ERR_ARG;
+    *bytes_out = mask ? fp8_plan(cfg, mask, nullptr, nullptr) : 0;
+    return GPT2_OK;
+}
+
+int gpt2_set_fp8(gpt2_t* m, int mask, void* d_workspace, size_t workspace_bytes) {
+    if (!m || mask < 0 || mask > GPT2_FP8_ALL) return GPT2_ERR_ARG;
+    if (mask && m->mode != GPT2_MODE_BF16) return GPT2_ERR_ARG;
+    if (mask) {
+        if (!d_workspace || ((uintptr_t)d_workspace) % WS_ALIGN) return GPT2_ERR_WORKSPACE;
+        if (workspace_bytes < fp8_plan(&m->cfg, mask, nullptr, nullptr)) return GPT2_ERR_WORKSPACE;
+        fp8_plan(&m->cfg, mask, m, (uint8_t*)d_workspace);
+    }
+    m->fp8 = mask;
+    m->state = 0;  // a forward with the new layers comes first
+    return GPT2_OK;
+}
+
 int gpt2_set_grad_accumulation(gpt2_t* m, int accumulate) {
     if (!m || (accumulate != 0 && accumulate != 1)) return GPT2_ERR_ARG;
     m->grad_accum = accumulate;
@@ -836,7 +1027,8 @@ int step_impl(gpt2_t* m, const int32_t* d_tokens, const int32_t* d_targets, int 
         cudaMemcpyAsync(m->tokens, d_tokens, bt, kind, m->stream) != cudaSuccess ||
         cudaMemcpyAsync(m->targets, d_targets, bt, kind, m->stream) != cudaSuccess)
         return GPT2_ERR_CUDA;
-    const gpt2::StepKey key{B, T, m->grad_accum, c->max_grad_norm > 0.f ? 1 : 0, c->decay_mask, c->max_grad_norm};
+    const gpt2::StepKey key{B, T, m->grad_accum, c->max_grad_norm > 0.f ? 1 : 0, c->decay_mask, m->fp8,
+                            c->max_grad_norm};
     if (!(key == m->step_key)) {
         if (m->step_exec) cudaGraphExecDestroy(m->step_exec);
         m->step_exec = nullptr;

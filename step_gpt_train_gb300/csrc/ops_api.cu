@@ -138,6 +138,40 @@ int gpt2_op_matmul_fp8(void* D, const void* A, int a_format, const float* a_scal
                                     b_scales + 1, (const bf16*)bias, M, N, K, d_status, st(stream)));
 }
 
+int gpt2_op_quantize_fp8_transpose(void* qt, void* q, const float* scales, const void* x, int R, int C, int format,
+                                   void* stream) {
+    if (!qt || !scales || !x || R < 0 || C < 0 || C % 8 || !fp8_format_ok(format) || !al16(x)) return GPT2_ERR_ARG;
+    if ((int64_t)R * C == 0) return GPT2_OK;
+    if ((int64_t)R * C >= ((int64_t)1 << 40) || (R + 63) / 64 > 65535) return GPT2_ERR_ARG;
+    return finish(launch_quantize_fp8_t((uint8_t*)qt, (uint8_t*)q, scales, (const bf16*)x, R, C, format, st(stream)));
+}
+
+size_t gpt2_op_matmul_fp8_scratch(int M, int N, int K, int d_fp32, int accumulate) {
+    if (M < 0 || N < 0 || K < 1) return 0;
+    return matmul_f8_scratch(M, N, K, d_fp32, accumulate);
+}
+
+int gpt2_op_matmul_fp8_ex(int epi, void* D, void* D2, const void* aux, int d_fp32, int accumulate, const void* A,
+                          int a_format, const float* a_scales, const void* B, int b_format, const float* b_scales,
+                          const void* bias, int M, int N, int K, void* scratch, size_t scratch_bytes, int* d_status,
+                          void* stream) {
+    if (!D || !A || !B || !a_scales || !b_scales || M < 0 || N < 0 || K < 1 || epi < 0 || epi > 2) return GPT2_ERR_ARG;
+    if (!fp8_format_ok(a_format) || !fp8_format_ok(b_format) || K % 16 || N % 8) return GPT2_ERR_ARG;
+    if (!al16(D) || !al16(A) || !al16(B) || (bias && !al16(bias))) return GPT2_ERR_ARG;
+    if (epi == 1 && (!D2 || !al16(D2) || D2 == D || d_fp32)) return GPT2_ERR_ARG;
+    if (epi == 2 && (!aux || !al16(aux) || aux == D || d_fp32 || bias)) return GPT2_ERR_ARG;
+    if (accumulate && (!d_fp32 || epi)) return GPT2_ERR_ARG;
+    if ((int64_t)M * N == 0) return GPT2_OK;
+    if (scratch_bytes < matmul_f8_scratch(M, N, K, d_fp32, accumulate) || (scratch_bytes && !scratch))
+        return GPT2_ERR_WORKSPACE;
+    const F8Args f8 = {a_format, b_format, a_scales + 1, b_scales + 1};
+    const uint8_t* a8 = (const uint8_t*)A;
+    const uint8_t* b8 = (const uint8_t*)B;
+    if (epi == 1) return finish(launch_matmul_gelu_f8(D, D2, a8, b8, f8, bias, M, N, K, d_status, st(stream)));
+    if (epi == 2) return finish(launch_matmul_gelu_backward_f8(D, a8, b8, f8, aux, M, N, K, d_status, st(stream)));
+    return finish(launch_matmul_f8(D, d_fp32, a8, b8, f8, bias, M, N, K, scratch, d_status, st(stream), accumulate));
+}
+
 int gpt2_op_matmul_gelu(int dtype, void* dgelu, void* out, const void* A, const void* W, const void* bias, int M,
                         int N, int K, int* d_status, void* stream) {
     if (!dt_ok(dtype) || !dgelu || !out || !A || !W || M < 0 || N < 0 || K < 1 || dgelu == out) return GPT2_ERR_ARG;

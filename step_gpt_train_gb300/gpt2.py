@@ -30,7 +30,11 @@ FP8_E4M3, FP8_E5M2 = 0, 1  # the FP8 formats of gpt2_op_quantize_fp8 / gpt2_op_m
 FAMILIES = ["encoder_forward", "layernorm_forward", "matmul", "attention_forward", "residual_forward",
             "gelu_forward", "classifier", "loss_mean", "layernorm_backward", "gelu_backward",
             "bias_backward", "attention_backward", "residual_backward", "encoder_backward", "adamw",
-            "grad_colsum"]
+            "grad_colsum", "fp8_quant"]
+
+# FP8 linear layers (gpt2_set_fp8)
+FP8_QKV, FP8_MLP, FP8_HEAD = 1, 2, 4
+FP8_ALL = FP8_QKV | FP8_MLP | FP8_HEAD
 
 WORKSPACE_ALIGN = 1024
 
@@ -63,6 +67,8 @@ _SIGNATURES = {
     "gpt2_adamw_step": (c_int, [c_void_p, c_float, c_float, c_float, c_float, c_float, c_int]),
     "gpt2_destroy": (c_int, [c_void_p]),
     "gpt2_set_grad_accumulation": (c_int, [c_void_p, c_int]),
+    "gpt2_fp8_workspace_bytes": (c_int, [POINTER(gpt2_config), c_int, POINTER(c_size_t)]),
+    "gpt2_set_fp8": (c_int, [c_void_p, c_int, c_void_p, c_size_t]),
     "gpt2_zero_grad": (c_int, [c_void_p]),
     "gpt2_grad_norm": (c_int, [c_void_p, POINTER(c_float)]),
     "gpt2_adamw_step_ex": (c_int, [c_void_p, POINTER(gpt2_adamw_config)]),
@@ -111,6 +117,12 @@ _SIGNATURES = {
                                     c_void_p, c_void_p]),
     "gpt2_op_quantize_fp8_scratch": (c_size_t, []),
     "gpt2_op_quantize_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_void_p, c_size_t, c_void_p]),
+    "gpt2_op_quantize_fp8_transpose": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                               c_void_p]),
+    "gpt2_op_matmul_fp8_scratch": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "gpt2_op_matmul_fp8_ex": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_void_p,
+                                      c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_size_t,
+                                      c_void_p, c_void_p]),
     "gpt2_op_matmul_fp8": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                    c_int, c_int, c_void_p, c_void_p]),
     "gpt2_op_matmul_gelu_backward": (c_int, [c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
@@ -306,6 +318,24 @@ class GPT2:
               "gpt2_grad_sumsq_range")
         return out.value
 
+    def set_fp8(self, mask: int) -> None:
+        """Run the linears in mask (FP8_QKV | FP8_MLP | FP8_HEAD) with FP8
+        operands; 0 returns every matmul to bf16. Allocates the codes'
+        workspace (torch, on this device) and keeps it with the model."""
+        import torch
+        n = ctypes.c_size_t(0)
+        check(self.lib.gpt2_fp8_workspace_bytes(ctypes.byref(self.cfg), int(mask), ctypes.byref(n)),
+              "gpt2_fp8_workspace_bytes")
+        if mask:
+            self._ws8 = torch.empty(n.value + WORKSPACE_ALIGN, dtype=torch.uint8, device="cuda")
+            ptr = (self._ws8.data_ptr() + WORKSPACE_ALIGN - 1) // WORKSPACE_ALIGN * WORKSPACE_ALIGN
+        else:
+            ptr = None
+        check(self.lib.gpt2_set_fp8(self.h, int(mask), ptr, n.value), "gpt2_set_fp8")
+        if not mask:
+            self._ws8 = None
+        self.fp8_bytes = n.value
+
     def set_grad_accumulation(self, on: bool) -> None:
         check(self.lib.gpt2_set_grad_accumulation(self.h, int(bool(on))), "gpt2_set_grad_accumulation")
 
@@ -477,6 +507,32 @@ def gpt2_op_matmul_fp8(D, A, a_scales, B, b_scales, bias=None, a_fmt=FP8_E4M3, b
     check(load_library().gpt2_op_matmul_fp8(_p(D), _p(A), int(a_fmt), _p(a_scales), _p(B), int(b_fmt),
                                             _p(b_scales), _p(bias), M, N, K, _p(status), _s(stream)),
           "gpt2_op_matmul_fp8")
+
+
+def gpt2_op_quantize_fp8_transpose(qt, scales, x, q=None, fmt=FP8_E4M3, stream=None):
+    """qt (uint8 [C, R]) = the FP8 codes of x (bf16 [R, C]) under scales (from
+    gpt2_op_quantize_fp8 of the same x), transposed; q (uint8 [R, C], optional)
+    the same codes untransposed."""
+    R, C = x.shape
+    check(load_library().gpt2_op_quantize_fp8_transpose(_p(qt), _p(q), _p(scales), _p(x), R, C, int(fmt),
+                                                        _s(stream)), "gpt2_op_quantize_fp8_transpose")
+
+
+def gpt2_op_matmul_fp8_ex(epi, D, A, a_scales, B, b_scales, D2=None, aux=None, bias=None, accumulate=False,
+                          a_fmt=FP8_E4M3, b_fmt=FP8_E4M3, status=None, stream=None):
+    """The general FP8 product (gpt2_op_matmul_fp8_ex): epi 0 plain (D bf16 or
+    fp32, accumulate into fp32 D), 1 the GELU forward (D = gelu'(u), D2 =
+    gelu(u)), 2 the GELU backward (D = bf16(A B^T scales) * aux)."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    d_fp32 = int(D.dtype == torch.float32)
+    lib = load_library()
+    sc = _scratch(lib.gpt2_op_matmul_fp8_scratch(M, N, K, d_fp32, int(accumulate)))
+    check(lib.gpt2_op_matmul_fp8_ex(int(epi), _p(D), _p(D2), _p(aux), d_fp32, int(accumulate), _p(A), int(a_fmt),
+                                    _p(a_scales), _p(B), int(b_fmt), _p(b_scales), _p(bias), M, N, K, _p(sc),
+                                    sc.numel(), _p(status), _s(stream)), "gpt2_op_matmul_fp8_ex")
+    return sc
 
 
 def gpt2_op_matmul_gelu(dgelu, out, A, W, bias=None, status=None, stream=None):

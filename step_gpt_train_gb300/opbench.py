@@ -7,7 +7,10 @@ peak for the matmuls and attention, algorithmic bytes against the measured
 HBM bandwidth for the rest. Also the small, self-contained program for ncu
 captures of one kernel.
 
-  python -m step_gpt_train_gb300.opbench [--ops a,b|all|step_gemms] [--iters N] [--B 32 --T 1024 --C 768 --H 12]
+  python -m step_gpt_train_gb300.opbench [--ops a,b|all|step_gemms|cublas_step_gemms] [--iters N] [--B 32 --T 1024 --C 768 --H 12]
+
+cublas_step_gemms times torch.matmul (cuBLAS) on the plain matmul shapes of the
+step, a reference point for the hand-written kernels (not part of the step).
 """
 from __future__ import annotations
 
@@ -90,11 +93,27 @@ def main(argv=None):
             return run
         return setup, 2.0 * M * Nn * K, "flop"
 
+    def cublas_op(M, Nn, K, a_mn, b_mn):
+        # the same product through torch.matmul (cuBLAS), bf16 output, for
+        # comparison only: D[M, N] = A(m, k) B(n, k), A stored [M][K] or [K][M]
+        # (a_mn), B stored [N][K] or [K][N] (b_mn)
+        def setup():
+            A = rnd(M * K)
+            Bm = rnd(Nn * K, std=0.02)
+            a = A.view(K, M).t() if a_mn else A.view(M, K)
+            b = Bm.view(K, Nn) if b_mn else Bm.view(Nn, K).t()
+            D = torch.empty(M, Nn, device=dev, dtype=bf)
+            return lambda: torch.matmul(a, b, out=D)
+        return setup, 2.0 * M * Nn * K, "flop"
+
     shapes = {"qkv": (3 * C, C), "proj": (C, C), "fc": (4 * C, C), "fcproj": (C, 4 * C), "lmhead": (Vp, C)}
     for name, (out, inp) in shapes.items():
         ops[f"gemm_{name}_fwd"] = gemm_op(N, out, inp, 0, 0, False, name != "lmhead")
         ops[f"gemm_{name}_dx"] = gemm_op(N, inp, out, 0, 1, False, False)
         ops[f"gemm_{name}_dw"] = gemm_op(out, inp, N, 1, 1, True, False)
+        ops[f"cublas_{name}_fwd"] = cublas_op(N, out, inp, 0, 0)
+        ops[f"cublas_{name}_dx"] = cublas_op(N, inp, out, 0, 1)
+        ops[f"cublas_{name}_dw"] = cublas_op(out, inp, N, 1, 1)
 
 
     def gemm_gelu_op():  # the MLP's first linear with its GELU in the epilogue
@@ -298,6 +317,8 @@ def main(argv=None):
 
     if args.ops == "step_gemms":
         names = list(STEP_GEMMS)
+    elif args.ops == "cublas_step_gemms":  # cuBLAS on the step's plain matmul shapes, for comparison
+        names = [n for n in ops if n.startswith("cublas_")]
     else:
         names = list(ops) if args.ops == "all" else args.ops.split(",")
     for name in names:

@@ -147,3 +147,83 @@ def test_matmul_fp8_mixed_formats_closed_form():
     assert np.array_equal(d, np.array([[-2.75, 2.375], [6.0625, -2.78125]]))
     # the same codes read in the other format give other values: the format is not ignored
     assert not np.array_equal(F.matmul_fp8(a, 4.0, b, 0.125, a_fmt="e4m3", b_fmt="e4m3"), d)
+
+
+# ---- the FP8 linear layer of the oracle's step ----
+
+def _grid_values(rng, shape, table, top):
+    """Values drawn from a format's finite values, with the largest finite
+    value present (so amax = fmax, the scale is 1 and quantization is exact)."""
+    v = rng.choice(table, size=shape) * rng.choice([-1.0, 1.0], size=shape)
+    v.reshape(-1)[0] = top
+    return v
+
+
+def test_fp8_linear_exact_on_representable_operands():
+    """Operands that are already format values with amax = fmax quantize
+    exactly (scale 1), so the FP8 linear layer equals the float64 one; with
+    amax = 2 fmax the scale is 1/2, also exact."""
+    from oracle import gpt2_ref as R
+    rng = np.random.default_rng(11)
+    e4 = F.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    e5 = F.e5m2_decode(np.arange(0x7C, dtype=np.uint8))
+    x = _grid_values(rng, (6, 5, 16), e4, 448.0)
+    w = _grid_values(rng, (12, 16), e4, 448.0)
+    b = rng.normal(size=12)
+    assert np.array_equal(R.linear_forward_fp8(x, w, b), R.linear_forward(x, w, b))
+    assert np.array_equal(R.linear_forward_fp8(2 * x, w), R.linear_forward(2 * x, w))
+    dy = _grid_values(rng, (30, 12), e5, 57344.0)
+    dx, dw, db = R.linear_backward_fp8(dy, x.reshape(30, 16), w)
+    rx, rw, rb = R.linear_backward(dy, x.reshape(30, 16), w)
+    assert np.array_equal(dx, rx) and np.array_equal(dw, rw) and np.array_equal(db, rb)
+
+
+def test_fp8_linear_quantizes_each_operand_per_tensor():
+    """A plain operand: the layer equals the product of each operand's
+    quantized values (codes times amax / fmax), dy in e5m2, x and w in e4m3;
+    the error against the exact product stays within the bound the
+    rounding of each operand allows."""
+    from oracle import gpt2_ref as R
+    rng = np.random.default_rng(12)
+    x, w, dy = rng.normal(size=(64, 32)), rng.normal(size=(24, 32)), rng.normal(size=(64, 24))
+    qx, sx = F.quantize_e4m3(x)
+    qw, sw = F.quantize_e4m3(w)
+    ref = (F.e4m3_decode(qx) * float(sx)) @ (F.e4m3_decode(qw) * float(sw)).T
+    assert np.allclose(R.linear_forward_fp8(x, w), ref, rtol=0, atol=1e-12)
+    # per element |q(a) - a| <= 2^-4 |a| + 2^-10 amax / 448 (half the spacing
+    # of normal e4m3 values, and of the subnormals), summed over the products
+    ex = 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * np.abs(x).max() / 448
+    ew = 2.0 ** -4 * np.abs(w) + 2.0 ** -10 * np.abs(w).max() / 448
+    bound = ex @ np.abs(w).T + np.abs(x) @ ew.T + ex @ ew.T
+    assert np.all(np.abs(R.linear_forward_fp8(x, w) - x @ w.T) <= bound * (1 + 1e-9))
+    dx, dw, db = R.linear_backward_fp8(dy, x, w)
+    qd, sd = F.quantize_e5m2(dy)
+    d = F.e5m2_decode(qd) * float(sd)
+    assert np.allclose(dx, d @ (F.e4m3_decode(qw) * float(sw)), rtol=0, atol=1e-12)
+    assert np.allclose(dw, d.T @ (F.e4m3_decode(qx) * float(sx)), rtol=0, atol=1e-12)
+    assert np.array_equal(db, dy.sum(0))
+
+
+def test_fp8_step_runs_the_selected_linears_in_fp8():
+    """The FP8 step changes the loss and the gradients by quantization-sized
+    amounts (not zero, not more than a few percent) and leaves the linears
+    that are not selected alone (with fp8=() the step is the bf16 one)."""
+    from oracle import gpt2_ref as R
+    cfg = R.Config(2, 32, 2, 64, 64, 16)
+    params = R.init_params(cfg, 5)
+    rng = np.random.default_rng(3)
+    tok = rng.integers(0, 64, size=(2, 16))
+    tgt = rng.integers(0, 64, size=(2, 16))
+    l0, c0 = R.forward(cfg, params, tok, tgt)
+    g0 = R.backward(cfg, c0)
+    l1, c1 = R.forward(cfg, params, tok, tgt, fp8=())
+    assert l1 == l0
+    for sel in (("qkv",), ("mlp",), ("head",), ("qkv", "mlp", "head")):
+        l2, c2 = R.forward(cfg, params, tok, tgt, fp8=sel)
+        g2 = R.backward(cfg, c2)
+        assert l2 != l0 and abs(l2 - l0) < 0.05 * l0, (sel, l0, l2)
+        for name in ("h0.qkv.w", "h1.fc.w", "wte"):
+            err = np.linalg.norm(g2[name] - g0[name]) / np.linalg.norm(g0[name])
+            assert err < 0.2, (sel, name, err)
+        changed = {n for n in g0 if not np.array_equal(g0[n], g2[n])}
+        assert changed, sel
