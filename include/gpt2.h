@@ -150,8 +150,10 @@ int gpt2_zero_grad(gpt2_t* m);
  * gradient, weight gradient) take FP8 operands on the tensor cores
  * (tcgen05 kind::f8f6f4, fp32 accumulation): activations and weights in
  * e4m3, the output gradient in e5m2, each tensor with its own per-tensor
- * scale fmax / amax taken just before the product (the forward's scales of
- * x and W also serve the backward's transposed codes of the same tensors).
+ * scale fmax / amax taken just before the product (the forward's codes of x
+ * and scale of W also serve the backward, whose operands are the same
+ * tensors). The workspace keeps each selected linear's transposed input
+ * codes from the forward to the backward (B*T x its input width bytes).
  * Outputs stay bf16 (fp32 for weight gradients), biases, GELU and the bias
  * gradients as in the bf16 step. bf16 mode only (else GPT2_ERR_ARG); B*T
  * must then be a multiple of 16 (gpt2_forward returns GPT2_ERR_ARG

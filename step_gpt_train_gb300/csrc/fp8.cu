@@ -14,7 +14,7 @@
 //   quantize_fp8_t_kernel the same codes for a [R][C] matrix written
 //                        transposed, [C][R] (and optionally also [R][C]): the
 //                        K-major operands of the weight-gradient and
-//                        input-gradient products, 64 x 64 tiles through
+//                        input-gradient products, 128 x 64 tiles through
 //                        shared memory.
 // NaN inputs do not enter amax (fmaxf ignores them) and quantize to NaN.
 #include "common.cuh"
@@ -30,8 +30,20 @@ __global__ void __launch_bounds__(256) amax_partial_kernel(float* __restrict__ p
     const int64_t per = ((n + FP8_BLOCKS - 1) / FP8_BLOCKS + 7) / 8 * 8;  // whole 8-value vectors
     const int64_t lo = (int64_t)blockIdx.x * per;
     const int64_t hi = lo + per < n ? lo + per : n;
+    constexpr int64_t STEP = 8 * 256;
     float m = 0.f;
-    for (int64_t i = lo + 8 * (int64_t)threadIdx.x; i < hi; i += 8 * 256) {
+    int64_t i = lo + 8 * (int64_t)threadIdx.x;
+    // four vectors per thread in flight, then the rest one at a time
+    for (; i + 3 * STEP + 8 <= hi; i += 4 * STEP) {
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; u++) load8(x + i + u * STEP, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+#pragma unroll
+            for (int j = 0; j < 8; j++) m = fmaxf(m, fabsf(v[u][j]));
+    }
+    for (; i < hi; i += STEP) {
         if (i + 8 <= hi) {
             float v[8];
             load8(x + i, v);
@@ -97,64 +109,64 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(uint8_t* __restrict__
     }
 }
 
-// 64 x 64 tile of x [R][C] (bf16) -> codes, written transposed to qt [C][R]
-// and, when q is given, as they are to q [R][C]. 256 threads: each converts
-// two 8-column pieces of the tile (rows r, r + 32), stores the codes to a
-// transposed shared tile, then writes 16 consecutive codes of one output row.
-// Parts of the tile outside the matrix are skipped; R and C need not be
-// multiples of 64, but rows of qt and q are written 16 bytes at a time only
-// where R (resp. C) is a multiple of 16 and the piece is whole.
+// x [R][C] (bf16) -> codes, written transposed to qt [C][R] and, when q is
+// given, as they are to q [R][C]. A block takes 128 rows (r0) and 64 columns
+// (c0): warp w converts rows r0 + 32w .. + 31, lane l the column pair c0 + 2l,
+// c0 + 2l + 1 (the warp reads 128 contiguous bytes of a row at a time, and
+// writes each code pair to q); the codes go to a shared tile [64 columns][128
+// rows], from which the block writes 128-byte pieces of qt's rows (16 bytes
+// a thread; byte by byte at a ragged edge or where R % 16 != 0).
+constexpr int QT_ROWS = 128, QT_PAD = 16;
 template <int FMT>
-__global__ void __launch_bounds__(256) quantize_fp8_t_kernel(uint8_t* __restrict__ qt, uint8_t* __restrict__ q,
+__global__ void __launch_bounds__(128) quantize_fp8_t_kernel(uint8_t* __restrict__ qt, uint8_t* __restrict__ q,
                                                              const bf16* __restrict__ x, int R, int C,
                                                              const float* __restrict__ scales) {
-    __shared__ __align__(16) uint8_t tile[64][64 + 16];  // [column][row]
+    __shared__ __align__(16) uint8_t tile[64][QT_ROWS + QT_PAD];
     const float s = scales[0];
-    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    const int t = threadIdx.x;
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int r0 = blockIdx.y * QT_ROWS, c0 = blockIdx.x * 64;
+    const int rw = r0 + 32 * w;                  // this warp's first row
+    const int cl = 2 * lane, c = c0 + cl;        // this lane's column pair (C is even)
+    const int nr = max(0, min(32, R - rw));
+    if (c < C) {
+        uint32_t lo[8], hi[8];  // codes of column c (lo) and c + 1 (hi), rows rw + 4k .. + 3
 #pragma unroll
-    for (int h = 0; h < 2; h++) {
-        const int rl = t / 8 + 32 * h, cl = (t % 8) * 8;  // row and first column within the tile
-        const int r = r0 + rl, c = c0 + cl;
-        uint8_t code[8];
-        if (r < R && c + 8 <= C) {
-            float v[8];
-            load8(x + (int64_t)r * C + c, v);
+        for (int k = 0; k < 8; k++) {
+            uint32_t a = 0, b = 0;
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const uint16_t w = fp8x2<FMT>(v[j] * s, v[j + 1] * s);
-                code[j] = (uint8_t)(w & 0xFF);
-                code[j + 1] = (uint8_t)(w >> 8);
+            for (int j = 0; j < 4; j++) {
+                const int rr = 4 * k + j;
+                uint32_t v = 0;
+                if (rr < nr) v = *reinterpret_cast<const uint32_t*>(x + (int64_t)(rw + rr) * C + c);
+                const uint16_t cc = fp8x2<FMT>(__uint_as_float(v << 16) * s, __uint_as_float(v & 0xFFFF0000u) * s);
+                a |= (uint32_t)(cc & 0xFF) << (8 * j);
+                b |= (uint32_t)(cc >> 8) << (8 * j);
+                if (q && rr < nr) *reinterpret_cast<uint16_t*>(q + (int64_t)(rw + rr) * C + c) = cc;
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                code[j] = (r < R && c + j < C)
-                              ? (uint8_t)(fp8x2<FMT>(__bfloat162float(x[(int64_t)r * C + c + j]) * s, 0.f) & 0xFF)
-                              : 0;
+            lo[k] = a;
+            hi[k] = b;
         }
-#pragma unroll
-        for (int j = 0; j < 8; j++) tile[cl + j][rl] = code[j];
-        if (q && r < R) {
-            if (c + 8 <= C && C % 8 == 0) {
-                uint2 w;
-                w.x = code[0] | (code[1] << 8) | (code[2] << 16) | ((uint32_t)code[3] << 24);
-                w.y = code[4] | (code[5] << 8) | (code[6] << 16) | ((uint32_t)code[7] << 24);
-                *reinterpret_cast<uint2*>(q + (int64_t)r * C + c) = w;
-            } else {
-                for (int j = 0; j < 8 && c + j < C; j++) q[(int64_t)r * C + c + j] = code[j];
-            }
-        }
+        uint4* t0 = reinterpret_cast<uint4*>(&tile[cl][32 * w]);
+        uint4* t1 = reinterpret_cast<uint4*>(&tile[cl + 1][32 * w]);
+        t0[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        t0[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        t1[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        t1[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
     }
     __syncthreads();
-    const int cl = t / 4, rl = (t % 4) * 16;  // output row (a column of x) and its first code
-    const int c = c0 + cl, r = r0 + rl;
-    if (c < C) {
-        uint8_t* dst = qt + (int64_t)c * R + r;
-        if (r + 16 <= R && R % 16 == 0) {
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[cl][rl]);
+    const int nrows = min(QT_ROWS, R - r0);  // rows of this block inside the matrix
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int idx = threadIdx.x + 128 * i;   // 64 qt rows x 8 pieces of 16 bytes
+        const int row = idx / 8, piece = idx % 8;
+        const int cc = c0 + row;
+        const int rr = 16 * piece;
+        if (cc >= C || rr >= nrows) continue;
+        uint8_t* dst = qt + (int64_t)cc * R + r0 + rr;
+        if (rr + 16 <= nrows && R % 16 == 0) {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[row][rr]);
         } else {
-            for (int j = 0; j < 16 && r + j < R; j++) dst[j] = tile[cl][rl + j];
+            for (int j = 0; j < 16 && rr + j < nrows; j++) dst[j] = tile[row][rr + j];
         }
     }
 }
@@ -185,10 +197,10 @@ int launch_quantize_fp8_t(uint8_t* qt, uint8_t* q, const float* scales, const bf
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return GPT2_ERR_ARG;
     if (R <= 0 || C <= 0) return 0;
     if ((C % 8) != 0) return GPT2_ERR_ARG;  // 16-byte vector reads of x rows
-    const dim3 grid((unsigned)((C + 63) / 64), (unsigned)((R + 63) / 64));
+    const dim3 grid((unsigned)((C + 63) / 64), (unsigned)((R + QT_ROWS - 1) / QT_ROWS));
     if (grid.y > 65535) return GPT2_ERR_ARG;
-    if (fmt == FP8_E4M3) quantize_fp8_t_kernel<FP8_E4M3><<<grid, 256, 0, s>>>(qt, q, x, R, C, scales);
-    else quantize_fp8_t_kernel<FP8_E5M2><<<grid, 256, 0, s>>>(qt, q, x, R, C, scales);
+    if (fmt == FP8_E4M3) quantize_fp8_t_kernel<FP8_E4M3><<<grid, 128, 0, s>>>(qt, q, x, R, C, scales);
+    else quantize_fp8_t_kernel<FP8_E5M2><<<grid, 128, 0, s>>>(qt, q, x, R, C, scales);
     return 1;
 }
 

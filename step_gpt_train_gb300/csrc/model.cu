@@ -84,7 +84,8 @@ struct gpt2 {
     // FP8 linear layers (gpt2_set_fp8): which ones, and the codes they read,
     // in the caller's second workspace
     int fp8 = 0;
-    uint8_t *f8_x = nullptr, *f8_xT = nullptr, *f8_w = nullptr, *f8_wT = nullptr, *f8_dy = nullptr, *f8_dyT = nullptr;
+    uint8_t *f8_x = nullptr, *f8_w = nullptr, *f8_wT = nullptr, *f8_dy = nullptr, *f8_dyT = nullptr;
+    std::vector<uint8_t*> f8_xT;  // per FP8 linear (slot): the forward's transposed codes of its input x
     float* f8_scales = nullptr;   // per FP8 linear: (scale, 1/scale) of x, W and dy
     float* f8_partial = nullptr;  // amax partials
     void* f8_scratch = nullptr;   // split-K partial tiles of the FP8 weight gradients
@@ -424,9 +425,10 @@ void cs_defer(gpt2* m, const float* partial, int rows, int ncols, int seg, float
 
 // ---- FP8 linear layers ----
 // Per-tensor current scaling: each operand's codes use the scale of its own
-// amax, taken just before the product (the scales of x and W taken in the
-// forward serve the backward's transposed codes of the same, unchanged
-// tensors). Activations and weights in e4m3, output gradients in e5m2.
+// amax, taken just before the product (the forward writes x's codes in both
+// layouts and keeps the transposed ones for the weight gradient; W's scale
+// serves the backward's transposed codes of the same, unchanged weight).
+// Activations and weights in e4m3, output gradients in e5m2.
 
 // The FP8 linears as (in, out) sizes: qkv, fc, fcproj, head.
 struct F8Lin {
@@ -442,6 +444,19 @@ std::vector<F8Lin> f8_linears(const gpt2_config* c, int mask) {
     }
     if (mask & GPT2_FP8_HEAD) v.push_back({GPT2_FP8_HEAD, C, c->vocab_padded});
     return v;
+}
+
+// The FP8 linear in slot 3l + k (k: F8_QKV, F8_FC, F8_FCPROJ) or 3L (the head):
+// whether mask selects it, and its input width.
+inline bool f8_slot_on(const gpt2_config* c, int mask, int slot, int* in) {
+    const int C = c->n_embd;
+    if (slot == 3 * c->n_layer) {
+        *in = C;
+        return mask & GPT2_FP8_HEAD;
+    }
+    const int k = slot % 3;
+    *in = k == 2 ? 4 * C : C;
+    return mask & (k == 0 ? GPT2_FP8_QKV : GPT2_FP8_MLP);
 }
 
 // Carve the FP8 workspace (m == nullptr: the size only).
@@ -461,13 +476,23 @@ size_t fp8_plan(const gpt2_config* c, int mask, gpt2* m, uint8_t* w) {
         off += bytes;
         return r;
     };
-    const size_t o_x = take(BT * max_in), o_xT = take(BT * max_in), o_w = take(max_w), o_wT = take(max_w);
+    const size_t o_x = take(BT * max_in), o_w = take(max_w), o_wT = take(max_w);
+    const int slots = 3 * c->n_layer + 1;
+    std::vector<size_t> o_xT(slots, 0);
+    for (int sl = 0; sl < slots; sl++) {
+        int in = 0;
+        if (f8_slot_on(c, mask, sl, &in)) o_xT[sl] = take(BT * in);
+    }
     const size_t o_dy = take(BT * max_out), o_dyT = take(BT * max_out);
     const size_t o_sc = take((size_t)(3 * c->n_layer + 1) * 8 * 4), o_part = take(fp8_quantize_scratch());
     const size_t o_scr = take(std::max(scr, (size_t)256));
     if (m) {
         m->f8_x = w + o_x;
-        m->f8_xT = w + o_xT;
+        m->f8_xT.assign(slots, nullptr);
+        for (int sl = 0; sl < slots; sl++) {
+            int in = 0;
+            if (f8_slot_on(c, mask, sl, &in)) m->f8_xT[sl] = w + o_xT[sl];
+        }
         m->f8_w = w + o_w;
         m->f8_wT = w + o_wT;
         m->f8_dy = w + o_dy;
@@ -492,14 +517,16 @@ int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, i
         Op op(m, GPT2_K_FP8_QUANT);
         int n = 0, r;
         const int64_t nx = (int64_t)BT * in, nw = (int64_t)out * in;
+        // x's codes in both layouts: rows for this product, transposed (kept
+        // until the backward) for the weight gradient
         if ((r = launch_fp8_amax_scale(sc, xb, nx, FP8_E4M3, m->f8_partial, m->stream)) < 0) return r;
         n += r;
-        if ((r = launch_quantize_fp8_rows(m->f8_x, sc, xb, nx, FP8_E4M3, m->stream)) < 0) return r;
+        if ((r = launch_quantize_fp8_t(m->f8_xT[slot], m->f8_x, sc, xb, BT, in, FP8_E4M3, m->stream)) < 0) return r;
         n += r;
         if ((r = launch_fp8_amax_scale(sc + 2, wb, nw, FP8_E4M3, m->f8_partial, m->stream)) < 0) return r;
         n += r;
         if ((r = launch_quantize_fp8_rows(m->f8_w, sc + 2, wb, nw, FP8_E4M3, m->stream)) < 0) return r;
-        TRY(op.done(n + r, 5.0 * (double)(nx + nw)));
+        TRY(op.done(n + r, 6.0 * (double)nx + 5.0 * (double)nw));
     }
     const F8Args f8 = {FP8_E4M3, FP8_E4M3, sc + 1, sc + 3};
     const void* bias = bi >= 0 ? P(m, bi) : nullptr;
@@ -510,7 +537,8 @@ int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, i
 }
 
 // dx = dy W and dW (+)= dy^T x with FP8 operands (dy in e5m2, its codes in
-// both layouts; W and x transposed under their forward scales); the bias
+// both layouts; W transposed under its forward scale; x's transposed codes
+// as the forward wrote them); the bias
 // gradient from dy as stored (bf16), deferred. aux: dx is the gradient
 // through the GELU, bf16(dy W) * aux, with its column sums to colsum.
 int f8_linear_bwd(gpt2* m, int slot, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in,
@@ -528,10 +556,8 @@ int f8_linear_bwd(gpt2* m, int slot, void* dx, const void* dy, const void* x, in
         if ((r = launch_quantize_fp8_t(m->f8_wT, nullptr, sc + 2, (const bf16*)P(m, wi), out, in, FP8_E4M3,
                                        m->stream)) < 0)
             return r;
-        n += r;
-        if ((r = launch_quantize_fp8_t(m->f8_xT, nullptr, sc, (const bf16*)x, BT, in, FP8_E4M3, m->stream)) < 0)
-            return r;
-        TRY(op.done(n + r, 4.0 * ny + 2.0 * ny + 3.0 * (double)out * in + 3.0 * (double)BT * in));
+        TRY(op.done(n + r, 4.0 * ny + 2.0 * ny + 3.0 * (double)out * in));
+        (void)x;  // its transposed codes were written by the forward
     }
     const double flops = 2.0 * BT * in * out;
     {
@@ -546,7 +572,7 @@ int f8_linear_bwd(gpt2* m, int slot, void* dx, const void* dy, const void* x, in
     {
         const F8Args f8 = {FP8_E5M2, FP8_E4M3, sc + 5, sc + 1};
         Op op(m, GPT2_K_MATMUL);
-        TRY(op.done(launch_matmul_f8(G(m, wi), 1, m->f8_dyT, m->f8_xT, f8, nullptr, out, in, BT, m->f8_scratch,
+        TRY(op.done(launch_matmul_f8(G(m, wi), 1, m->f8_dyT, m->f8_xT[slot], f8, nullptr, out, in, BT, m->f8_scratch,
                                      m->status, m->stream, m->grad_accum),
                     flops));
     }

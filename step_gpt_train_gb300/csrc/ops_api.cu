@@ -142,7 +142,7 @@ int gpt2_op_quantize_fp8_transpose(void* qt, void* q, const float* scales, const
                                    void* stream) {
     if (!qt || !scales || !x || R < 0 || C < 0 || C % 8 || !fp8_format_ok(format) || !al16(x)) return GPT2_ERR_ARG;
     if ((int64_t)R * C == 0) return GPT2_OK;
-    if ((int64_t)R * C >= ((int64_t)1 << 40) || (R + 63) / 64 > 65535) return GPT2_ERR_ARG;
+    if ((int64_t)R * C >= ((int64_t)1 << 40) || (R + 127) / 128 > 65535) return GPT2_ERR_ARG;
     return finish(launch_quantize_fp8_t((uint8_t*)qt, (uint8_t*)q, scales, (const bf16*)x, R, C, format, st(stream)));
 }
 

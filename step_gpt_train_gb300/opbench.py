@@ -159,6 +159,18 @@ def main(argv=None):
     # input gradient of the MLP down-projection: dY [N, C] (e5m2) times W^T stored [4C, C] (e4m3)
     ops["gemm_fcproj_dx_fp8_e5m2"] = gemm_fp8_op(4 * C, C, a_fmt=g.FP8_E5M2, use_bias=False)
     ops["quantize_fp8"] = quantize_op()
+
+    def quantize_t_op():  # both layouts of the MLP's hidden activations' codes (the FP8 step's forward)
+        def setup():
+            x = rnd(N, 4 * C)
+            q = torch.empty(N, 4 * C, device=dev, dtype=torch.uint8)
+            qt = torch.empty(4 * C, N, device=dev, dtype=torch.uint8)
+            sc = torch.empty(2, device=dev, dtype=torch.float32)
+            g.gpt2_op_quantize_fp8(q, sc, x)
+            return lambda: g.gpt2_op_quantize_fp8_transpose(qt, sc, x, q=q, stream=torch.cuda.current_stream())
+        return setup, N * 4.0 * C * (2 + 1 + 1), "byte"  # reads x, writes q and qt
+
+    ops["quantize_fp8_transpose"] = quantize_t_op()
     def gemm_gelu_bwd_bias_op():  # the same, with the MLP's first bias gradient from its epilogue
         def setup():
             dY, W, u = rnd(N, C), rnd(C, 4 * C, std=0.02), rnd(N, 4 * C)
