@@ -455,12 +455,7 @@ int launch_attention_forward_tc(bf16* o, float* lse, const bf16* qkv, int B, int
                                 cudaStream_t s) {
     CUtensorMap map;
     if (!make_qkv_map(&map, qkv, B, T, C)) return GPT2_ERR_CUDA;
-    // once per process; a function-local static is initialised thread-safely
-    static const bool configured = [] {
-        cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)attn_fwd_tc_kernel, AT_SMEM);
     FwdArgs a;
     a.o = o;
     a.lse = lse;
@@ -1376,13 +1371,8 @@ int launch_attention_backward_tc(bf16* dqkv, const bf16* dout, const bf16* qkv, 
     if (!make_qkv_map(&mq, qkv, B, T, C) || !make_do_map(&mo, dout, B, T, C) || !make_do_map(&mx, o, B, T, C) ||
         !make_qkv_map(&md, dqkv, B, T, C))
         return GPT2_ERR_CUDA;
-    // once per process; a function-local static is initialised thread-safely
-    static const bool configured = [] {
-        cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DKDV_SMEM);
-        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)attn_bwd_dkdv_tc_kernel, DKDV_SMEM);
+    smem_attr((const void*)attn_bwd_dq_tc_kernel, DQ_SMEM);
     BwdArgs a;
     a.dqkv = dqkv;
     a.lse = lse;

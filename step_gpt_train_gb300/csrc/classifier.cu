@@ -308,15 +308,7 @@ int launch_classifier(int dtype, void* logits, float* losses, const int32_t* tar
     if (dtype == GPT2_MODE_BF16) {
         const size_t smem = (size_t)Vp * 2 * 2;  // two rows per SM either way
         if (Vp > 8 * 256 * 2 && smem <= CLS_STREAM_MAX_SMEM) {
-            // two CTAs of 512 threads per SM, one row buffer each (measured
-            // faster than one CTA with two buffers: the CTAs' phases interleave)
-            // once per process; a function-local static is initialised thread-safely
-            static const bool configured = [] {
-                cudaFuncSetAttribute(classifier_stream_kernel<512, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     CLS_STREAM_MAX_SMEM / 2);
-                return true;
-            }();
-            (void)configured;
+            smem_attr((const void*)classifier_stream_kernel<512, 1>, CLS_STREAM_MAX_SMEM / 2);
             const int grid = N < 2 * gpt2_num_sms() ? N : 2 * gpt2_num_sms();
             classifier_stream_kernel<512, 1><<<grid, 512, smem / 2, s>>>((bf16*)logits, losses, targets, N, V, Vp, dloss,
                                                                          status);

@@ -5,6 +5,10 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "../../include/gpt2.h"
 #include "../../include/gpt2_ops.h"
 
@@ -20,6 +24,23 @@ typedef __nv_bfloat16 bf16;
 
 __device__ __forceinline__ void set_status(int* status, int bit) {
     if (status) atomicOr(status, bit);
+}
+
+// Allow `bytes` of dynamic shared memory for `kernel` on the current device,
+// once per (kernel, device): thread-safe, and a failed attempt is not
+// remembered (the next launch tries again, and a launch that still lacks
+// the attribute fails with an error the caller reports).
+inline cudaError_t smem_attr(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kernel, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({kernel, dev});
+    return e;
 }
 
 // ---- 8-element vector access: one 16-byte access for bf16, two for fp32 ----

@@ -15,7 +15,7 @@
 //                        transposed, [C][R] (and optionally also [R][C]): the
 //                        K-major operands of the weight-gradient and
 //                        input-gradient products, 128 x 64 tiles through
-//                        shared memory.
+//                        shared memory, 16-byte loads.
 // NaN inputs do not enter amax (fmaxf ignores them) and quantize to NaN.
 #include "common.cuh"
 #include "launch.h"
@@ -111,47 +111,54 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(uint8_t* __restrict__
 
 // x [R][C] (bf16) -> codes, written transposed to qt [C][R] and, when q is
 // given, as they are to q [R][C]. A block takes 128 rows (r0) and 64 columns
-// (c0): warp w converts rows r0 + 32w .. + 31, lane l the column pair c0 + 2l,
-// c0 + 2l + 1 (the warp reads 128 contiguous bytes of a row at a time, and
-// writes each code pair to q); the codes go to a shared tile [64 columns][128
-// rows], from which the block writes 128-byte pieces of qt's rows (16 bytes
-// a thread; byte by byte at a ragged edge or where R % 16 != 0).
-constexpr int QT_ROWS = 128, QT_PAD = 16;
+// (c0); warp w rows r0 + 32w .. + 31. Lane l reads 16 bytes (8 columns,
+// 8 (l % 8) ..) of 8 consecutive rows, 8 (l / 8) .., so each load of the warp
+// covers four whole 128-byte row pieces; it writes the row-layout codes 8
+// at a time, and the 8 codes of each of its columns (8 consecutive rows) to a
+// shared tile [64 columns][128 rows] as two 4-byte words (a 132-byte tile
+// row keeps the 8 lanes of a row group on distinct banks but for pairs);
+// the block then writes 16-byte pieces of qt's rows from the tile (byte by
+// byte at a ragged edge or where R % 16 != 0).
+constexpr int QT_ROWS = 128, QT_STRIDE = 132;
 template <int FMT>
 __global__ void __launch_bounds__(128) quantize_fp8_t_kernel(uint8_t* __restrict__ qt, uint8_t* __restrict__ q,
                                                              const bf16* __restrict__ x, int R, int C,
                                                              const float* __restrict__ scales) {
-    __shared__ __align__(16) uint8_t tile[64][QT_ROWS + QT_PAD];
+    __shared__ __align__(16) uint8_t tile[64 * QT_STRIDE];
     const float s = scales[0];
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int r0 = blockIdx.y * QT_ROWS, c0 = blockIdx.x * 64;
-    const int rw = r0 + 32 * w;                  // this warp's first row
-    const int cl = 2 * lane, c = c0 + cl;        // this lane's column pair (C is even)
-    const int nr = max(0, min(32, R - rw));
-    if (c < C) {
-        uint32_t lo[8], hi[8];  // codes of column c (lo) and c + 1 (hi), rows rw + 4k .. + 3
+    const int cl = 8 * (lane % 8);               // first of this lane's 8 columns within the tile
+    const int rl = 32 * w + 8 * (lane / 8);      // first of its 8 rows within the tile
+    const int c = c0 + cl;
+    if (c < C) {  // C % 8 == 0: the 8 columns are all inside
+        uint32_t col[8][2];  // codes of column cl + j, rows rl .. rl + 7, four to a word
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            uint32_t a = 0, b = 0;
+        for (int j = 0; j < 8; j++) col[j][0] = col[j][1] = 0;
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int rr = 4 * k + j;
-                uint32_t v = 0;
-                if (rr < nr) v = *reinterpret_cast<const uint32_t*>(x + (int64_t)(rw + rr) * C + c);
-                const uint16_t cc = fp8x2<FMT>(__uint_as_float(v << 16) * s, __uint_as_float(v & 0xFFFF0000u) * s);
-                a |= (uint32_t)(cc & 0xFF) << (8 * j);
-                b |= (uint32_t)(cc >> 8) << (8 * j);
-                if (q && rr < nr) *reinterpret_cast<uint16_t*>(q + (int64_t)(rw + rr) * C + c) = cc;
+        for (int i = 0; i < 8; i++) {
+            const int r = r0 + rl + i;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < R) v = *reinterpret_cast<const uint4*>(x + (int64_t)r * C + c);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+            uint32_t rowc[2];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const uint16_t cc =
+                    fp8x2<FMT>(__uint_as_float(u[k] << 16) * s, __uint_as_float(u[k] & 0xFFFF0000u) * s);
+                col[2 * k][i / 4] |= (uint32_t)(cc & 0xFF) << (8 * (i % 4));
+                col[2 * k + 1][i / 4] |= (uint32_t)(cc >> 8) << (8 * (i % 4));
+                if (k % 2 == 0) rowc[k / 2] = cc;
+                else rowc[k / 2] |= (uint32_t)cc << 16;
             }
-            lo[k] = a;
-            hi[k] = b;
+            if (q && r < R) *reinterpret_cast<uint2*>(q + (int64_t)r * C + c) = make_uint2(rowc[0], rowc[1]);
         }
-        uint4* t0 = reinterpret_cast<uint4*>(&tile[cl][32 * w]);
-        uint4* t1 = reinterpret_cast<uint4*>(&tile[cl + 1][32 * w]);
-        t0[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        t0[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-        t1[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        t1[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            uint32_t* t = reinterpret_cast<uint32_t*>(tile + (cl + j) * QT_STRIDE + rl);
+            t[0] = col[j][0];
+            t[1] = col[j][1];
+        }
     }
     __syncthreads();
     const int nrows = min(QT_ROWS, R - r0);  // rows of this block inside the matrix
@@ -163,10 +170,12 @@ __global__ void __launch_bounds__(128) quantize_fp8_t_kernel(uint8_t* __restrict
         const int rr = 16 * piece;
         if (cc >= C || rr >= nrows) continue;
         uint8_t* dst = qt + (int64_t)cc * R + r0 + rr;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(tile + row * QT_STRIDE + rr);
         if (rr + 16 <= nrows && R % 16 == 0) {
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[row][rr]);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
         } else {
-            for (int j = 0; j < 16 && rr + j < nrows; j++) dst[j] = tile[row][rr + j];
+            const uint8_t* sb = tile + row * QT_STRIDE + rr;
+            for (int j = 0; j < 16 && rr + j < nrows; j++) dst[j] = sb[j];
         }
     }
 }

@@ -1054,15 +1054,9 @@ template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                const GemmArgs& args, int grid, cudaStream_t s) {
     using Cfg = TileCfg<BN>;
-    // once per process; a function-local static is initialised thread-safely
     constexpr int smem = Cfg::SMEM_BYTES;
     static_assert(smem <= 232448, "shared memory per CTA");
-    static const bool configured = [] {
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, smem);
     gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8><<<grid, NUM_THREADS, smem, s>>>(ma, mb, md, md2, args);
 }
 
@@ -1105,12 +1099,7 @@ bool launch_tc_layout_f8(int epi, const CUtensorMap& ma, const CUtensorMap& mb, 
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                         const GemmArgs& args, int pairs, cudaStream_t s) {
-    static const bool configured = [] {
-        cudaFuncSetAttribute(gemm_pair_kernel<A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             P_SMEM_BYTES);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)gemm_pair_kernel<A_MN, B_MN, EPI>, P_SMEM_BYTES);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(P_THREADS, 1, 1);

@@ -605,13 +605,8 @@ template <typename T, int VPL>
 static void ln_fwd_staged_launch(int blocks, size_t smem, void* y, float* mean, float* rstd, void* xsum,
                                  const void* x, const void* r, const void* gamma, const void* beta, int N, int C,
                                  cudaStream_t s) {
-    // once per process; a function-local static is initialised thread-safely
-    static const bool configured = [] {
-        cudaFuncSetAttribute(ln_fwd_staged_kernel<T, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LN_FWD_STAGED_WARPS * LN_STAGES * 2 * LN_STAGED_MAX_ROW_BYTES);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)ln_fwd_staged_kernel<T, VPL>,
+              LN_FWD_STAGED_WARPS * LN_STAGES * 2 * LN_STAGED_MAX_ROW_BYTES);
     ln_fwd_staged_kernel<T, VPL><<<blocks, LN_FWD_STAGED_WARPS * 32, smem, s>>>(
         (T*)y, mean, rstd, (T*)xsum, (const T*)x, (const T*)r, (const T*)gamma, (const T*)beta, N, C);
 }
@@ -689,14 +684,7 @@ template <typename T, int VPL>
 static void ln_bwd_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np, const void* dy,
                           const void* x, const void* gamma, const float* mean, const float* rstd, int N, int C,
                           cudaStream_t s) {
-    // once per process and instantiation (allow > 48 KB of dynamic shared memory); a
-    // function-local static is initialised thread-safely
-    static const bool configured = [] {
-        cudaFuncSetAttribute(ln_bwd_kernel<T, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LN_BWD_WARPS * 3 * 2048 * 4);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)ln_bwd_kernel<T, VPL>, LN_BWD_WARPS * 3 * 2048 * 4);
     ln_bwd_kernel<T, VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((T*)out, accumulate, partial, np, (const T*)dy,
                                                                   (const T*)x, (const T*)gamma, mean, rstd, N, C);
 }
@@ -705,13 +693,8 @@ template <typename T, int VPL>
 static void ln_bwd_staged_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np,
                                  const void* dy, const void* x, const void* gamma, const float* mean,
                                  const float* rstd, int N, int C, cudaStream_t s) {
-    // once per process; a function-local static is initialised thread-safely
-    static const bool configured = [] {
-        cudaFuncSetAttribute(ln_bwd_staged_kernel<T, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16));
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)ln_bwd_staged_kernel<T, VPL>,
+              LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16));
     ln_bwd_staged_kernel<T, VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>(
         (T*)out, accumulate, partial, np, (const T*)dy, (const T*)x, (const T*)gamma, mean, rstd, N, C);
 }
@@ -720,13 +703,8 @@ template <int VPL>
 static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np,
                                const void* dy, const void* x, const void* gamma, const float* mean,
                                const float* rstd, int N, int C, cudaStream_t s) {
-    // once per process; a function-local static is initialised thread-safely
-    static const bool configured = [] {
-        cudaFuncSetAttribute(ln_bwd_bf16_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16) + 1024 * 4);
-        return true;
-    }();
-    (void)configured;
+    smem_attr((const void*)ln_bwd_bf16_kernel<VPL>,
+              LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16) + 1024 * 4);
     ln_bwd_bf16_kernel<VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((bf16*)out, accumulate, partial, np,
                                                                      (const bf16*)dy, (const bf16*)x,
                                                                      (const bf16*)gamma, mean, rstd, N, C);
