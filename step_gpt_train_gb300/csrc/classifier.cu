@@ -66,10 +66,12 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* sh) {
 }
 
 // NT threads per row, VPT 8-element vectors per thread (Vp <= 8 * NT * VPT).
+// amax (both classifier kernels; or null): the largest |dlogit| as stored is
+// merged into it (float bits), the scale of an FP8 operand.
 template <typename T, int NT, int VPT>
 __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, float* __restrict__ losses,
                                                         const int32_t* __restrict__ targets, int V, int Vp,
-                                                        float dloss, int* status) {
+                                                        float dloss, int* status, unsigned* __restrict__ amax) {
     __shared__ float sh[33];
     const int row = blockIdx.x;
     T* z = logits + (int64_t)row * Vp;
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, 
     s = block_reduce<NT>(s, false, sh);
     const float scale = dloss / s;
     const int tvec = tgt / 8;
+    float am = 0.f;  // this thread's largest |dlogit| (amax)
 #pragma unroll
     for (int i = 0; i < VPT; i++) {
         const int idx = threadIdx.x + i * NT;
@@ -155,8 +158,13 @@ __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, 
                     if (j == jt) f[j] -= dloss;
             }
             store8(z + idx * 8, f);
+            if (amax) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(f[j]));
+            }
         }
     }
+    if (amax) amax_merge(amax, am);
 }
 
 // The bf16 classifier as a persistent kernel: a CTA walks rows row0, row0 + G,
@@ -167,7 +175,9 @@ __global__ void __launch_bounds__(NT) classifier_kernel(T* __restrict__ logits, 
 template <int NT, int NBUF>
 __global__ void __launch_bounds__(NT, 2 / NBUF) classifier_stream_kernel(bf16* __restrict__ logits, float* __restrict__ losses,
                                                                   const int32_t* __restrict__ targets, int N, int V,
-                                                                  int Vp, float dloss, int* status) {
+                                                                  int Vp, float dloss, int* status,
+                                                                  unsigned* __restrict__ amax) {
+    float am = 0.f;  // this thread's largest |dlogit| (amax)
     extern __shared__ __align__(128) uint8_t cls_smem[];  // NBUF rows of Vp bf16
     __shared__ float sh[33];
     __shared__ __align__(8) uint64_t bars[2];
@@ -266,10 +276,15 @@ __global__ void __launch_bounds__(NT, 2 / NBUF) classifier_stream_kernel(bf16* _
                     if (j == jt) f[j] -= dloss;
             }
             store8(zg + idx * 8, f);
+            if (amax) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(f[j]));
+            }
         }
         __syncthreads();  // every thread is done with this buffer before it is refilled
         if (NBUF == 1 && threadIdx.x == 0 && next < N) issue(next, 0, 2 * (k + 1));
     }
+    if (amax) amax_merge(amax, am);
     // copies still in flight after an early exit
     if (threadIdx.x == 0)
         for (int b = 0; b < 2; b++)
@@ -280,11 +295,11 @@ __global__ void __launch_bounds__(NT, 2 / NBUF) classifier_stream_kernel(bf16* _
 
 template <typename T, int NT>
 static int classifier_dispatch(void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
-                               float dloss, int* status, cudaStream_t s) {
+                               float dloss, int* status, cudaStream_t s, unsigned* amax) {
     const int nv = Vp / 8;
     const int vpt = (nv + NT - 1) / NT;
 #define CLS_CALL(K)                                                                                                \
-    classifier_kernel<T, NT, K><<<N, NT, 0, s>>>((T*)logits, losses, targets, V, Vp, dloss, status); \
+    classifier_kernel<T, NT, K><<<N, NT, 0, s>>>((T*)logits, losses, targets, V, Vp, dloss, status, amax); \
     return 1;
     switch (vpt) {
         case 1: CLS_CALL(1)
@@ -303,7 +318,7 @@ static int classifier_dispatch(void* logits, float* losses, const int32_t* targe
 int classifier_set_wait_limit(long long cycles) { return tc::set_wait_limit(cycles); }
 
 int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
-                      float dloss, int* status, cudaStream_t s) {
+                      float dloss, int* status, cudaStream_t s, unsigned* amax) {
     if (N == 0) return 0;
     if (dtype == GPT2_MODE_BF16) {
         const size_t smem = (size_t)Vp * 2 * 2;  // two rows per SM either way
@@ -311,14 +326,16 @@ int launch_classifier(int dtype, void* logits, float* losses, const int32_t* tar
             smem_attr((const void*)classifier_stream_kernel<512, 1>, CLS_STREAM_MAX_SMEM / 2);
             const int grid = N < 2 * gpt2_num_sms() ? N : 2 * gpt2_num_sms();
             classifier_stream_kernel<512, 1><<<grid, 512, smem / 2, s>>>((bf16*)logits, losses, targets, N, V, Vp, dloss,
-                                                                         status);
+                                                                         status, amax);
             return 1;
         }
-        if (Vp <= 8 * 256 * 2) return classifier_dispatch<bf16, 256>(logits, losses, targets, N, V, Vp, dloss, status, s);
-        return classifier_dispatch<bf16, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s);
+        if (Vp <= 8 * 256 * 2)
+            return classifier_dispatch<bf16, 256>(logits, losses, targets, N, V, Vp, dloss, status, s, amax);
+        return classifier_dispatch<bf16, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s, amax);
     }
-    if (Vp <= 8 * 256 * 2) return classifier_dispatch<float, 256>(logits, losses, targets, N, V, Vp, dloss, status, s);
-    return classifier_dispatch<float, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s);
+    if (Vp <= 8 * 256 * 2)
+        return classifier_dispatch<float, 256>(logits, losses, targets, N, V, Vp, dloss, status, s, amax);
+    return classifier_dispatch<float, 1024>(logits, losses, targets, N, V, Vp, dloss, status, s, amax);
 }
 
 // Mean of N losses: each of 1024 threads sums a fixed strided subset in

@@ -26,6 +26,19 @@ __device__ __forceinline__ void set_status(int* status, int bit) {
     if (status) atomicOr(status, bit);
 }
 
+// The largest |value| of what a warp stored as bf16 (m: this lane's largest
+// |value| before the rounding, which is monotone, so rounding the maximum
+// gives the maximum of the rounded values), merged into *amax: the bits of a
+// non-negative float order as unsigned integers, so atomicMax on them is the
+// float maximum, whatever the order of the merges. Every lane of the warp
+// calls it. The amax of an FP8 operand, taken by the kernel that writes it.
+__device__ __forceinline__ void amax_merge(unsigned* amax, float m) {
+    m = __bfloat162float(__float2bfloat16_rn(m));
+#pragma unroll
+    for (int off = 16; off > 0; off /= 2) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(amax, __float_as_uint(m));
+}
+
 // Allow `bytes` of dynamic shared memory for `kernel` on the current device,
 // once per (kernel, device): thread-safe, and a failed attempt is not
 // remembered (the next launch tries again, and a launch that still lacks

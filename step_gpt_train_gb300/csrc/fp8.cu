@@ -120,12 +120,26 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(uint8_t* __restrict__
 // the block then writes 16-byte pieces of qt's rows from the tile (byte by
 // byte at a ragged edge or where R % 16 != 0).
 constexpr int QT_ROWS = 128, QT_STRIDE = 132;
+// With amax (the tensor's largest |value| as float bits, taken by the kernel
+// that wrote x) the scale pair is formed here as amax_scale_kernel forms it,
+// block (0, 0) writing it to scales; else scales holds it already.
 template <int FMT>
 __global__ void __launch_bounds__(128) quantize_fp8_t_kernel(uint8_t* __restrict__ qt, uint8_t* __restrict__ q,
                                                              const bf16* __restrict__ x, int R, int C,
-                                                             const float* __restrict__ scales) {
+                                                             float* __restrict__ scales,
+                                                             const unsigned* __restrict__ amax, float fmax) {
     __shared__ __align__(16) uint8_t tile[64 * QT_STRIDE];
-    const float s = scales[0];
+    float s;
+    if (amax) {
+        const float t = __uint_as_float(*amax);
+        s = t > 0.f ? fmax / t : 1.f;
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+            scales[0] = s;
+            scales[1] = t > 0.f ? t / fmax : 1.f;
+        }
+    } else {
+        s = scales[0];
+    }
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int r0 = blockIdx.y * QT_ROWS, c0 = blockIdx.x * 64;
     const int cl = 8 * (lane % 8);               // first of this lane's 8 columns within the tile
@@ -202,14 +216,16 @@ int launch_quantize_fp8_rows(uint8_t* q, const float* scales, const bf16* x, int
 }
 
 int launch_quantize_fp8_t(uint8_t* qt, uint8_t* q, const float* scales, const bf16* x, int R, int C, int fmt,
-                          cudaStream_t s) {
+                          cudaStream_t s, const unsigned* amax) {
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return GPT2_ERR_ARG;
     if (R <= 0 || C <= 0) return 0;
     if ((C % 8) != 0) return GPT2_ERR_ARG;  // 16-byte vector reads of x rows
     const dim3 grid((unsigned)((C + 63) / 64), (unsigned)((R + QT_ROWS - 1) / QT_ROWS));
     if (grid.y > 65535) return GPT2_ERR_ARG;
-    if (fmt == FP8_E4M3) quantize_fp8_t_kernel<FP8_E4M3><<<grid, 128, 0, s>>>(qt, q, x, R, C, scales);
-    else quantize_fp8_t_kernel<FP8_E5M2><<<grid, 128, 0, s>>>(qt, q, x, R, C, scales);
+    const float fmax = fmt == FP8_E4M3 ? 448.f : 57344.f;
+    float* sc = const_cast<float*>(scales);  // written only when amax is given
+    if (fmt == FP8_E4M3) quantize_fp8_t_kernel<FP8_E4M3><<<grid, 128, 0, s>>>(qt, q, x, R, C, sc, amax, fmax);
+    else quantize_fp8_t_kernel<FP8_E5M2><<<grid, 128, 0, s>>>(qt, q, x, R, C, sc, amax, fmax);
     return 1;
 }
 

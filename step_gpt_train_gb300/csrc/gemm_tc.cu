@@ -71,6 +71,7 @@ struct GemmArgs {
     const void* bias;    // bf16 [N] or null
     const bf16* aux;     // EPI_MUL: the factor [M][N]
     float* colsum;       // EPI_MUL, or null: column sums of the stored D per 32-row slice, [4 * m_tiles][N]
+    unsigned* amax;      // or null: the largest |output| as stored merged in (EPI_GELU: gelu(u); EPI_MUL: D)
     int* status;
     int M, N, K;
     int d_fp32;
@@ -115,8 +116,11 @@ __device__ __forceinline__ bool get_work(const GemmArgs& g, int idx, Work& w) {
 
 // Stage 32 bf16 values of this lane's row (64 bytes) once the buffer's
 // previous TMA store has read it, then store the 32 x 32 box at (x, y, z).
+// am2 (or null): a running maximum of the stored values' magnitudes, as a
+// bf16 pair (NaN-ignoring, as fmaxf).
 __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* stage, uint32_t stage_addr,
-                                                 const CUtensorMap* map, int x, int y, int z, int lane) {
+                                                 const CUtensorMap* map, int x, int y, int z, int lane,
+                                                 __nv_bfloat162* am2 = nullptr) {
     if (lane == 0) bulk_wait_read_all();
     __syncwarp();
 #pragma unroll
@@ -125,6 +129,10 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
         __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
         for (int i = 0; i < 4; i++) h[i] = __floats2bfloat162_rn(f[q * 8 + 2 * i], f[q * 8 + 2 * i + 1]);
+        if (am2) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) *am2 = __hmax2(*am2, __habs2(h[i]));
+        }
         stage16(stage, lane, q, v);
     }
     fence_proxy_async_smem();
@@ -138,12 +146,16 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
 // lane's 32 factors (EPI_MUL). EPI_MUL with csum_dst: csum_dst[j] (j <
 // ncols_valid) also receives the sum of column j of the stored (bf16) values
 // over the first nrows of the warp's 32 rows, read back from the staging buffer.
+// am2 (EPI_GELU, EPI_MUL; or null): this lane's running maximum of |gelu(u)|
+// (resp. |D|) as stored. Only rows inside the matrix may pass it (outside,
+// a GELU row is gelu(bias)); columns outside hold 0 in both forms (B's rows
+// and the bias read as 0 there, and the factor of EPI_MUL is 0).
 template <int EPI, bool F8 = false>
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
                                           uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD,
                                           const CUtensorMap* mapD2, const uint4 (&aux)[4], int x, int y, int z,
                                           int ncols_valid, int lane, float alpha = 1.f, float* csum_dst = nullptr,
-                                          int nrows = 32) {
+                                          int nrows = 32, __nv_bfloat162* am2 = nullptr) {
     float f[32];
     if (!F8 && bias_s) {
 #pragma unroll
@@ -171,7 +183,7 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
                 f[q * 8 + 2 * i + 1] *= __high2float(h[i]);
             }
         }
-        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
+        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane, am2);
         if (csum_dst) {
             // the staged rows (the TMA store only reads them too; the next
             // chunk overwrites them only after this warp's next sync)
@@ -190,7 +202,7 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
             gelu_pair(__uint_as_float(ub << 16), __uint_as_float(ub & 0xFFFF0000u), f[j], f[j + 1], gd[j], gd[j + 1]);
         }
         stage_store_bf16(gd, stage, stage_addr, mapD, x, y, z, lane);  // gelu'(u), kept for the backward
-        stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane);   // gelu(u)
+        stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane, am2);  // gelu(u)
     } else if (!fp32_out) {
         stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
     } else {
@@ -398,6 +410,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // EPI_MUL column sums: each warp writes the sums of its 32 rows of a
         // tile, row 4 * mt + quad of g.colsum
         const bool want_csum = EPI == EPI_MUL && g.colsum != nullptr;
+        // (the FP8 step's operands only: the bf16 kernels carry none of it)
+        const bool want_amax = F8 && (EPI == EPI_GELU || EPI == EPI_MUL) && g.amax != nullptr;
+        __nv_bfloat162 am2 = __floats2bfloat162_rn(0.f, 0.f);  // this lane's largest |output| (amax)
         int acc = 0;
         uint32_t acc_phase = 0;
         Work w;
@@ -461,7 +476,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
                 epi_chunk<EPI, F8>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
-                                   ncols(c), lane, alpha, csum_at(c), nrows);
+                                   ncols(c), lane, alpha, csum_at(c), nrows,
+                                   want_amax && m0 + row_in_tile < g.M ? &am2 : nullptr);
                 if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();  // reconverge before the warp-collective TMEM ops
                 if (!more) break;
@@ -469,7 +485,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
                 epi_chunk<EPI, F8>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1),
-                                   ys, z, ncols(c + 1), lane, alpha, csum_at(c + 1), nrows);
+                                   ys, z, ncols(c + 1), lane, alpha, csum_at(c + 1), nrows,
+                                   want_amax && m0 + row_in_tile < g.M ? &am2 : nullptr);
                 if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
@@ -486,6 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (want_amax) amax_merge(g.amax, fmaxf(__low2float(am2), __high2float(am2)));
         if (lane == 0) bulk_wait_all();  // this warp's stores are complete
         __syncwarp();
     }
@@ -1182,13 +1200,13 @@ namespace {
 // D (and D2) = the epilogue op of A B^T (+ bias); see launch_matmul_tc.
 int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const void* A, int a_mn, const void* B,
               int b_mn, const void* bias, int M, int N, int K, void* scratch, int* status, cudaStream_t s,
-              int accumulate = 0, float* colsum = nullptr, const F8Args* f8 = nullptr) {
+              int accumulate = 0, float* colsum = nullptr, const F8Args* f8 = nullptr, unsigned* amax = nullptr) {
     if (f8 && (a_mn || b_mn || K % 16 || N % 8)) return GPT2_ERR_ARG;
     Plan p = make_plan(M, N, f8 ? (K + 1) / 2 : K, epi == EPI_NONE ? d_fp32 : 0);
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
-    if (use_pair(M, N, partials) && !colsum && !f8) {
+    if (use_pair(M, N, partials) && !colsum && !f8 && !amax) {
         // 256 x 256 pair tiles, each CTA loading 128 rows of A and 128 columns of B
         const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + PBN - 1) / PBN;
         CUtensorMap ma, mb, md, md2;
@@ -1258,6 +1276,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     g.bias = partials ? nullptr : bias;
     g.aux = aux;
     g.colsum = epi == EPI_MUL ? colsum : nullptr;
+    g.amax = epi == EPI_GELU || epi == EPI_MUL ? amax : nullptr;
     g.status = status;
     g.M = M;
     g.N = N;
@@ -1314,18 +1333,18 @@ int launch_matmul_f8(void* D, int d_fp32, const uint8_t* A, const uint8_t* B, co
 }
 
 int launch_matmul_gelu_f8(void* dgelu, void* out, const uint8_t* A, const uint8_t* W, const F8Args& f8,
-                          const void* bias, int M, int N, int K, int* status, cudaStream_t s) {
+                          const void* bias, int M, int N, int K, int* status, cudaStream_t s, unsigned* amax) {
     if (M == 0 || N == 0) return 0;
     return matmul_tc(EPI_GELU, dgelu, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s, 0, nullptr,
-                     &f8);
+                     &f8, amax);
 }
 
 int launch_matmul_gelu_backward_f8(void* du, const uint8_t* dY, const uint8_t* WT, const F8Args& f8,
                                    const void* dgelu, int M, int N, int K, int* status, cudaStream_t s,
-                                   float* du_colsum) {
+                                   float* du_colsum, unsigned* amax) {
     if (M == 0 || N == 0) return 0;
     return matmul_tc(EPI_MUL, du, nullptr, (const bf16*)dgelu, 0, dY, 0, WT, 0, nullptr, M, N, K, nullptr, status, s,
-                     0, du_colsum, &f8);
+                     0, du_colsum, &f8, amax);
 }
 
 int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B, int b_mn, const void* bias, int M,
@@ -1335,14 +1354,15 @@ int launch_matmul_tc(void* D, int d_fp32, const void* A, int a_mn, const void* B
 }
 
 int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
-                       int* status, cudaStream_t s) {
+                       int* status, cudaStream_t s, unsigned* amax) {
     if (M == 0 || N == 0) return 0;
-    return matmul_tc(EPI_GELU, dgelu, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s);
+    return matmul_tc(EPI_GELU, dgelu, out, nullptr, 0, A, 0, W, 0, bias, M, N, K, nullptr, status, s, 0, nullptr,
+                     nullptr, amax);
 }
 
 int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* dgelu, int M, int N, int K,
-                                int* status, cudaStream_t s, float* du_colsum) {
+                                int* status, cudaStream_t s, float* du_colsum, unsigned* amax) {
     if (M == 0 || N == 0) return 0;
     return matmul_tc(EPI_MUL, du, nullptr, (const bf16*)dgelu, 0, dY, 0, W, 1, nullptr, M, N, K, nullptr, status,
-                     s, 0, du_colsum);
+                     s, 0, du_colsum, nullptr, amax);
 }

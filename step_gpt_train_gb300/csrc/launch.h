@@ -17,8 +17,10 @@ size_t encoder_backward_scratch(int B, int T, int C);
 int launch_encoder_backward(int dtype, float* dwte, float* dwpe, const void* dx0, const int32_t* tokens, int B, int T,
                             int C, void* scratch, cudaStream_t s, int accumulate = 0);
 
+// amax (optional, every LayerNorm forward and backward below): the largest |output| as
+// stored is merged into it (float bits; the caller zeroes it), the scale of an FP8 operand.
 int launch_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
-                             const void* beta, int N, int C, cudaStream_t s);
+                             const void* beta, int N, int C, cudaStream_t s, unsigned* amax = nullptr);
 size_t layernorm_backward_scratch(int N, int C);
 int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                               const void* gamma, const float* mean, const float* rstd, int N, int C, void* scratch,
@@ -28,7 +30,7 @@ int launch_layernorm_backward(int dtype, void* dx, float* dgamma, float* dbeta, 
 // y = LayerNorm(xsum).
 int launch_residual_layernorm_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x,
                                       const void* r, const void* gamma, const void* beta, int N, int C,
-                                      cudaStream_t s);
+                                      cudaStream_t s, unsigned* amax = nullptr);
 // LayerNorm backward into the residual gradient: dres = dx (accumulate == 0)
 // or dres += dx; dres_colsum (optional) = column sums of the resulting dres.
 // grad_accumulate: dgamma, dbeta and dres_colsum are added to instead of overwritten.
@@ -41,7 +43,8 @@ int launch_layernorm_backward_residual(int dtype, void* dres, int accumulate, fl
 // partial: layernorm_backward_scratch(N, C) bytes.
 int launch_layernorm_backward_residual_rows(int dtype, void* dres, int accumulate, float* partial, int np,
                                             const void* dy, const void* x, const void* gamma, const float* mean,
-                                            const float* rstd, int N, int C, cudaStream_t s, int* rows);
+                                            const float* rstd, int N, int C, cudaStream_t s, int* rows,
+                                            unsigned* amax = nullptr);
 
 int launch_gelu_forward(int dtype, void* g, const void* u, int64_t n, cudaStream_t s);
 int launch_gelu_backward(int dtype, void* du, const void* u, const void* dg, int64_t n, cudaStream_t s);
@@ -73,8 +76,9 @@ int launch_bias_backward(int dtype, float* dbias, const void* dy, int N, int C, 
 // sums over 128-row chunks of dy; *rows = ceil(N / 128).
 int launch_bias_partials(int dtype, float* partial, const void* dy, int N, int C, cudaStream_t s, int* rows);
 
+// amax (optional): the largest |dlogit| as stored is merged into it (float bits).
 int launch_classifier(int dtype, void* logits, float* losses, const int32_t* targets, int N, int V, int Vp,
-                      float dloss, int* status, cudaStream_t s);
+                      float dloss, int* status, cudaStream_t s, unsigned* amax = nullptr);
 int launch_mean_loss(float* out, const float* losses, int N, cudaStream_t s);
 
 // grad_scale multiplies the gradient; with gnorm (device ||g||) and max_norm > 0
@@ -104,14 +108,16 @@ int launch_attention_backward(int dtype, void* dqkv, const void* dout, const voi
 // bf16 linear forward with the GELU fused into its epilogue: u = A W^T + bias
 // (A [M,K], W [N,K], both K-major) rounded to bf16, out = gelu(u), dgelu =
 // gelu'(u) (kept for the backward); see gpt2_op_matmul_gelu.
+// amax (optional, here and in the GELU backward): the largest |gelu(u)| (resp. |du|) as
+// stored is merged into it (float bits; the caller zeroes it), the scale of an FP8 operand.
 int launch_matmul_gelu(void* dgelu, void* out, const void* A, const void* W, const void* bias, int M, int N, int K,
-                       int* status, cudaStream_t s);
+                       int* status, cudaStream_t s, unsigned* amax = nullptr);
 // bf16 input gradient through that GELU: du = bf16(dY W) * dgelu, dY [M,K], W [K,N];
 // du_colsum (or null): column sums of the stored du per 32-row slice, [4 ceil(M/128)][N]
 // (matmul_gelu_backward_colsum_rows).
 inline int matmul_gelu_backward_colsum_rows(int M) { return 4 * ((M + 127) / 128); }
 int launch_matmul_gelu_backward(void* du, const void* dY, const void* W, const void* dgelu, int M, int N, int K,
-                                int* status, cudaStream_t s, float* du_colsum = nullptr);
+                                int* status, cudaStream_t s, float* du_colsum = nullptr, unsigned* amax = nullptr);
 // out = gelu(u) and dgelu = gelu'(u) (dgelu may be u itself); n % 8 == 0.
 int launch_gelu_both(int dtype, void* out, void* dgelu, const void* u, int64_t n, cudaStream_t s);
 // out = a * b elementwise; n % 8 == 0.
@@ -133,9 +139,11 @@ int launch_quantize_fp8(uint8_t* q, float* scales, const bf16* x, int64_t n, int
 int launch_fp8_amax_scale(float* scales, const bf16* x, int64_t n, int fmt, float* partial, cudaStream_t s);
 int launch_quantize_fp8_rows(uint8_t* q, const float* scales, const bf16* x, int64_t n, int fmt, cudaStream_t s);
 // The codes of x [R][C] (C % 8 == 0) under given scales written transposed,
-// qt [C][R], and (q non-null) also as they are, q [R][C].
+// qt [C][R], and (q non-null) also as they are, q [R][C]. With amax (x's
+// largest |value| as float bits, from the kernel that wrote x) the scales are
+// formed from it first and written to scales.
 int launch_quantize_fp8_t(uint8_t* qt, uint8_t* q, const float* scales, const bf16* x, int R, int C, int fmt,
-                          cudaStream_t s);
+                          cudaStream_t s, const unsigned* amax = nullptr);
 
 // FP8 operands of the general matmul (K-major codes, scale_inv device scalars).
 struct F8Args {
@@ -151,10 +159,11 @@ struct F8Args {
 int launch_matmul_f8(void* D, int d_fp32, const uint8_t* A, const uint8_t* B, const F8Args& f8, const void* bias,
                      int M, int N, int K, void* scratch, int* status, cudaStream_t s, int accumulate = 0);
 int launch_matmul_gelu_f8(void* dgelu, void* out, const uint8_t* A, const uint8_t* W, const F8Args& f8,
-                          const void* bias, int M, int N, int K, int* status, cudaStream_t s);
+                          const void* bias, int M, int N, int K, int* status, cudaStream_t s,
+                          unsigned* amax = nullptr);
 int launch_matmul_gelu_backward_f8(void* du, const uint8_t* dY, const uint8_t* WT, const F8Args& f8,
                                    const void* dgelu, int M, int N, int K, int* status, cudaStream_t s,
-                                   float* du_colsum = nullptr);
+                                   float* du_colsum = nullptr, unsigned* amax = nullptr);
 // Scratch of launch_matmul_f8 (split-K partial tiles of an fp32 output).
 size_t matmul_f8_scratch(int M, int N, int K, int d_fp32, int accumulate = 0);
 

@@ -15,16 +15,18 @@
 // With r != null the row normalised is the residual sum x + r, rounded to T
 // and stored to xsum first (the residual join followed by the next block's
 // LayerNorm, in one pass over the row).
-// VPL = 8-element vectors per lane (C <= 256 * VPL).
+// VPL = 8-element vectors per lane (C <= 256 * VPL). amax (or null): the
+// largest |y| as stored is merged into it (an FP8 operand's scale).
 template <typename T, int VPL>
 __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict__ y, float* __restrict__ mean,
                                                                    float* __restrict__ rstd, T* __restrict__ xsum,
                                                                    const T* __restrict__ x, const T* __restrict__ r,
                                                                    const T* __restrict__ gamma,
-                                                                   const T* __restrict__ beta, int N, int C) {
+                                                                   const T* __restrict__ beta, int N, int C,
+                                                                   unsigned* __restrict__ amax) {
     const int row = blockIdx.x * LN_FWD_WARPS + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (row >= N) return;
+    if (row >= N) return;  // the whole warp
     const int cv = C / 8;
     const T* xr = x + (int64_t)row * C;
     float v[VPL][8];
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict
     }
     const float rs = 1.0f / sqrtf(warp_sum(ss) / (float)C + LN_EPS);
     T* yr = y + (int64_t)row * C;
+    float am = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; i++) {
         const int idx = lane + 32 * i;
@@ -69,12 +72,17 @@ __global__ void __launch_bounds__(LN_FWD_WARPS * 32) ln_fwd_kernel(T* __restrict
 #pragma unroll
             for (int j = 0; j < 8; j++) o[j] = (v[i][j] - mu) * rs * g[j] + b[j];
             store8(yr + idx * 8, o);
+            if (amax) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(o[j]));
+            }
         }
     }
     if (lane == 0) {
         mean[row] = mu;
         rstd[row] = rs;
     }
+    if (amax) amax_merge(amax, am);
 }
 
 // The same forward arranged like the staged backward: a persistent grid,
@@ -87,7 +95,7 @@ template <typename T, int VPL>
 __global__ void __launch_bounds__(LN_FWD_STAGED_WARPS * 32)
     ln_fwd_staged_kernel(T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, T* __restrict__ xsum,
                          const T* __restrict__ x, const T* __restrict__ r, const T* __restrict__ gamma,
-                         const T* __restrict__ beta, int N, int C) {
+                         const T* __restrict__ beta, int N, int C, unsigned* __restrict__ amax) {
     extern __shared__ __align__(16) uint8_t sm_raw[];
     constexpr int PIECES = (int)sizeof(T) / 2;  // 16-byte copies per 8-element vector
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -119,6 +127,7 @@ __global__ void __launch_bounds__(LN_FWD_STAGED_WARPS * 32)
 #pragma unroll
     for (int k = 0; k < LN_STAGES - 1; k++) issue(row0 + k * stride, k);
     int slot = 0;
+    float am = 0.f;  // largest |y| of this lane (amax)
     for (int row = row0; row < N; row += stride) {
         __syncwarp();
         issue(row + (LN_STAGES - 1) * stride, (slot + LN_STAGES - 1) % LN_STAGES);
@@ -167,6 +176,10 @@ __global__ void __launch_bounds__(LN_FWD_STAGED_WARPS * 32)
 #pragma unroll
                 for (int j = 0; j < 8; j++) o[j] = (v[i][j] - mu) * rs * g[j] + b[j];
                 store8(y + (int64_t)row * C + idx * 8, o);
+                if (amax) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(o[j]));
+                }
             }
         }
         if (lane == 0) {
@@ -176,6 +189,7 @@ __global__ void __launch_bounds__(LN_FWD_STAGED_WARPS * 32)
         slot = (slot + 1) % LN_STAGES;
     }
     cp_async_wait<0>();
+    if (amax) amax_merge(amax, am);
 }
 
 // dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat)), dxhat = dy gamma.
@@ -194,7 +208,9 @@ template <typename T, int VPL>
 __global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1)
     ln_bwd_kernel(T* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
                   const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
-                  const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C) {
+                  const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C,
+                  unsigned* __restrict__ amax) {
+    float am = 0.f;  // largest |out| of this lane (amax)
     extern __shared__ float sh[];  // [LN_BWD_WARPS][np][C]
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cv = C / 8;
@@ -272,6 +288,10 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1)
 #pragma unroll
                     for (int j = 0; j < 8; j++) acc_o[j * cv + idx] += to_float(from_float<T>(o[j]));
                 }
+                if (amax) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(o[j]));
+                }
             }
         }
 #pragma unroll
@@ -281,6 +301,7 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, VPL <= 3 ? 2 : 1)
         }
         row = next;
     }
+    if (amax) amax_merge(amax, am);
     __syncthreads();
     for (int a = threadIdx.x; a < np * C; a += blockDim.x) {
         float sum = 0.f;
@@ -446,7 +467,9 @@ template <int VPL>
 __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     ln_bwd_bf16_kernel(bf16* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
                        const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ gamma,
-                       const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C) {
+                       const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C,
+                       unsigned* __restrict__ amax) {
+    float am = 0.f;  // largest |out| of this lane (amax)
     using namespace tc;
     extern __shared__ __align__(16) uint8_t sm_raw[];
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -548,6 +571,7 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
                     if (accumulate) o = f2_add(o, bf2_to_f2(rw[p]));
                     float o0, o1;
                     f2_unpack(o, o0, o1);
+                    if (amax) am = fmaxf(am, fmaxf(fabsf(o0), fabsf(o1)));
                     __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
                     ow[p] = *reinterpret_cast<uint32_t*>(&h);
                     if (np == 3) ao[i][p] = f2_add(ao[i][p], bf2_to_f2(ow[p]));
@@ -557,6 +581,7 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
         }
         slot = (slot + 1) % LN_STAGES;
     }
+    if (amax) amax_merge(amax, am);
     cp_async_wait<0>();
     __syncthreads();
     float* red = reinterpret_cast<float*>(sm_raw + g_bytes);  // [warp][np][C] over the rings
@@ -604,15 +629,15 @@ static int ln_vpl(int C) { return (C / 8 + 31) / 32; }
 template <typename T, int VPL>
 static void ln_fwd_staged_launch(int blocks, size_t smem, void* y, float* mean, float* rstd, void* xsum,
                                  const void* x, const void* r, const void* gamma, const void* beta, int N, int C,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, unsigned* amax) {
     smem_attr((const void*)ln_fwd_staged_kernel<T, VPL>,
               LN_FWD_STAGED_WARPS * LN_STAGES * 2 * LN_STAGED_MAX_ROW_BYTES);
     ln_fwd_staged_kernel<T, VPL><<<blocks, LN_FWD_STAGED_WARPS * 32, smem, s>>>(
-        (T*)y, mean, rstd, (T*)xsum, (const T*)x, (const T*)r, (const T*)gamma, (const T*)beta, N, C);
+        (T*)y, mean, rstd, (T*)xsum, (const T*)x, (const T*)r, (const T*)gamma, (const T*)beta, N, C, amax);
 }
 
 static int ln_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x, const void* r,
-                      const void* gamma, const void* beta, int N, int C, cudaStream_t s) {
+                      const void* gamma, const void* beta, int N, int C, cudaStream_t s, unsigned* amax) {
     const int blocks = (N + LN_FWD_WARPS - 1) / LN_FWD_WARPS;
     if (blocks == 0) return 0;
     const size_t es = dtype == GPT2_MODE_BF16 ? 2 : 4;
@@ -624,9 +649,9 @@ static int ln_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, 
         if (sblocks > need) sblocks = need;
 #define LN_FWD_STAGED_CALL(V)                                                                                     \
     if (dtype == GPT2_MODE_BF16)                                                                                  \
-        ln_fwd_staged_launch<bf16, V>(sblocks, smem, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s);           \
+        ln_fwd_staged_launch<bf16, V>(sblocks, smem, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s, amax);     \
     else                                                                                                          \
-        ln_fwd_staged_launch<float, V>(sblocks, smem, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s);
+        ln_fwd_staged_launch<float, V>(sblocks, smem, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s, amax);
         switch (ln_vpl(C)) {
             case 1: LN_FWD_STAGED_CALL(1); break;
             case 2: LN_FWD_STAGED_CALL(2); break;
@@ -640,26 +665,27 @@ static int ln_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, 
     if (dtype == GPT2_MODE_BF16)                                                                                  \
         ln_fwd_kernel<bf16, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((bf16*)y, mean, rstd, (bf16*)xsum,            \
                                                                     (const bf16*)x, (const bf16*)r,               \
-                                                                    (const bf16*)gamma, (const bf16*)beta, N, C); \
+                                                                    (const bf16*)gamma, (const bf16*)beta, N, C,  \
+                                                                    amax);                                        \
     else                                                                                                          \
         ln_fwd_kernel<float, V><<<blocks, LN_FWD_WARPS * 32, 0, s>>>((float*)y, mean, rstd, (float*)xsum,         \
                                                                      (const float*)x, (const float*)r,            \
                                                                      (const float*)gamma, (const float*)beta, N,  \
-                                                                     C);
+                                                                     C, amax);
     LN_DISPATCH(ln_vpl(C), LN_FWD_CALL)
 #undef LN_FWD_CALL
     return 1;
 }
 
 int launch_layernorm_forward(int dtype, void* y, float* mean, float* rstd, const void* x, const void* gamma,
-                             const void* beta, int N, int C, cudaStream_t s) {
-    return ln_forward(dtype, y, mean, rstd, nullptr, x, nullptr, gamma, beta, N, C, s);
+                             const void* beta, int N, int C, cudaStream_t s, unsigned* amax) {
+    return ln_forward(dtype, y, mean, rstd, nullptr, x, nullptr, gamma, beta, N, C, s, amax);
 }
 
 int launch_residual_layernorm_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, const void* x,
                                       const void* r, const void* gamma, const void* beta, int N, int C,
-                                      cudaStream_t s) {
-    return ln_forward(dtype, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s);
+                                      cudaStream_t s, unsigned* amax) {
+    return ln_forward(dtype, y, mean, rstd, xsum, x, r, gamma, beta, N, C, s, amax);
 }
 
 static int ln_bwd_blocks(int N) {
@@ -683,10 +709,11 @@ size_t layernorm_backward_scratch(int N, int C) {
 template <typename T, int VPL>
 static void ln_bwd_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np, const void* dy,
                           const void* x, const void* gamma, const float* mean, const float* rstd, int N, int C,
-                          cudaStream_t s) {
+                          cudaStream_t s, unsigned* amax) {
     smem_attr((const void*)ln_bwd_kernel<T, VPL>, LN_BWD_WARPS * 3 * 2048 * 4);
     ln_bwd_kernel<T, VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((T*)out, accumulate, partial, np, (const T*)dy,
-                                                                  (const T*)x, (const T*)gamma, mean, rstd, N, C);
+                                                                  (const T*)x, (const T*)gamma, mean, rstd, N, C,
+                                                                  amax);
 }
 
 template <typename T, int VPL>
@@ -702,20 +729,21 @@ static void ln_bwd_staged_launch(int blocks, size_t smem, void* out, bool accumu
 template <int VPL>
 static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np,
                                const void* dy, const void* x, const void* gamma, const float* mean,
-                               const float* rstd, int N, int C, cudaStream_t s) {
+                               const float* rstd, int N, int C, cudaStream_t s, unsigned* amax) {
     smem_attr((const void*)ln_bwd_bf16_kernel<VPL>,
               LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16) + 1024 * 4);
     ln_bwd_bf16_kernel<VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((bf16*)out, accumulate, partial, np,
                                                                      (const bf16*)dy, (const bf16*)x,
-                                                                     (const bf16*)gamma, mean, rstd, N, C);
+                                                                     (const bf16*)gamma, mean, rstd, N, C, amax);
 }
 
 // The row pass of the backward: out (+)= dx and the per-block column sums
 // partial [blocks][np * C] (dy * xhat | dy | the values written, np == 3).
-// Returns the number of blocks (the partial rows).
+// Returns the number of blocks (the partial rows). amax (bf16 only): see
+// launch_layernorm_forward.
 static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partial_s, int np, const void* dy,
                             const void* x, const void* gamma, const float* mean, const float* rstd, int N, int C,
-                            cudaStream_t s) {
+                            cudaStream_t s, unsigned* amax = nullptr) {
     if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
         // 111 KB of ring per block at C = 768 bf16, two blocks per SM
         const int blocks = ln_bwd_staged_blocks(N);
@@ -723,7 +751,7 @@ static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partia
 #define LN_BWD_STAGED_CALL(V)                                                                                   \
     if (dtype == GPT2_MODE_BF16)                                                                                \
         ln_bwd_bf16_launch<V>(blocks, smem + (((size_t)C * 4 + 15) & ~(size_t)15), out, accumulate, partial_s,  \
-                              np, dy, x, gamma, mean, rstd, N, C, s);                                           \
+                              np, dy, x, gamma, mean, rstd, N, C, s, amax);                                     \
     else                                                                                                        \
         ln_bwd_staged_launch<float, V>(blocks, smem, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd,  \
                                        N, C, s);
@@ -741,9 +769,11 @@ static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partia
     float* partial = partial_s;
 #define LN_BWD_CALL(V)                                                                                           \
     if (dtype == GPT2_MODE_BF16)                                                                                 \
-        ln_bwd_launch<bf16, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);  \
+        ln_bwd_launch<bf16, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s,   \
+                               amax);                                                                            \
     else                                                                                                         \
-        ln_bwd_launch<float, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s);
+        ln_bwd_launch<float, V>(blocks, smem, out, accumulate, partial, np, dy, x, gamma, mean, rstd, N, C, s,  \
+                                amax);
     LN_DISPATCH(ln_vpl(C), LN_BWD_CALL)
 #undef LN_BWD_CALL
     return blocks;
@@ -761,8 +791,9 @@ static int ln_backward(int dtype, void* out, bool accumulate, float* dgamma, flo
 
 int launch_layernorm_backward_residual_rows(int dtype, void* dres, int accumulate, float* partial, int np,
                                             const void* dy, const void* x, const void* gamma, const float* mean,
-                                            const float* rstd, int N, int C, cudaStream_t s, int* rows) {
-    *rows = ln_backward_rows(dtype, dres, accumulate != 0, partial, np, dy, x, gamma, mean, rstd, N, C, s);
+                                            const float* rstd, int N, int C, cudaStream_t s, int* rows,
+                                            unsigned* amax) {
+    *rows = ln_backward_rows(dtype, dres, accumulate != 0, partial, np, dy, x, gamma, mean, rstd, N, C, s, amax);
     return 1;
 }
 

@@ -87,6 +87,7 @@ struct gpt2 {
     uint8_t *f8_x = nullptr, *f8_w = nullptr, *f8_wT = nullptr, *f8_dy = nullptr, *f8_dyT = nullptr;
     std::vector<uint8_t*> f8_xT;  // per FP8 linear (slot): the forward's transposed codes of its input x
     float* f8_scales = nullptr;   // per FP8 linear: (scale, 1/scale) of x, W and dy
+    unsigned* f8_amax = nullptr;  // per FP8 linear: amax of x and of dy (float bits) from the kernels that write them
     float* f8_partial = nullptr;  // amax partials
     void* f8_scratch = nullptr;   // split-K partial tiles of the FP8 weight gradients
     size_t f8_scratch_bytes = 0;
@@ -485,6 +486,7 @@ size_t fp8_plan(const gpt2_config* c, int mask, gpt2* m, uint8_t* w) {
     }
     const size_t o_dy = take(BT * max_out), o_dyT = take(BT * max_out);
     const size_t o_sc = take((size_t)(3 * c->n_layer + 1) * 8 * 4), o_part = take(fp8_quantize_scratch());
+    const size_t o_amax = take((size_t)(3 * c->n_layer + 1) * 2 * 4);
     const size_t o_scr = take(std::max(scr, (size_t)256));
     if (m) {
         m->f8_x = w + o_x;
@@ -498,6 +500,7 @@ size_t fp8_plan(const gpt2_config* c, int mask, gpt2* m, uint8_t* w) {
         m->f8_dy = w + o_dy;
         m->f8_dyT = w + o_dyT;
         m->f8_scales = (float*)(w + o_sc);
+        m->f8_amax = (unsigned*)(w + o_amax);
         m->f8_partial = (float*)(w + o_part);
         m->f8_scratch = w + o_scr;
         m->f8_scratch_bytes = std::max(scr, (size_t)256);
@@ -507,9 +510,17 @@ size_t fp8_plan(const gpt2_config* c, int mask, gpt2* m, uint8_t* w) {
 
 enum { F8_QKV = 0, F8_FC = 1, F8_FCPROJ = 2 };
 inline float* f8_sc(gpt2* m, int slot) { return m->f8_scales + (size_t)slot * 8; }
+// The amax word of slot's input x (which = 0) or output gradient dy (which = 1),
+// or null when that linear is not FP8 (what the producing kernel is given).
+inline unsigned* f8_am(gpt2* m, bool on, int slot, int which) {
+    return on ? m->f8_amax + (size_t)slot * 2 + which : nullptr;
+}
 
 // y = x W^T + b with FP8 operands (y2: the GELU form, y = gelu'(u), y2 = gelu(u)).
-int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, int bi, int BT, int in, int out) {
+// x's amax comes from the kernel that wrote x (f8_am(slot, 0)); y2 passes the
+// amax of gelu(u) on to the next FP8 linear (y2_amax).
+int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, int bi, int BT, int in, int out,
+                  unsigned* y2_amax = nullptr) {
     float* sc = f8_sc(m, slot);
     const bf16* xb = (const bf16*)x;
     const bf16* wb = (const bf16*)P(m, wi);
@@ -517,22 +528,26 @@ int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, i
         Op op(m, GPT2_K_FP8_QUANT);
         int n = 0, r;
         const int64_t nx = (int64_t)BT * in, nw = (int64_t)out * in;
-        // x's codes in both layouts: rows for this product, transposed (kept
-        // until the backward) for the weight gradient
-        if ((r = launch_fp8_amax_scale(sc, xb, nx, FP8_E4M3, m->f8_partial, m->stream)) < 0) return r;
-        n += r;
-        if ((r = launch_quantize_fp8_t(m->f8_xT[slot], m->f8_x, sc, xb, BT, in, FP8_E4M3, m->stream)) < 0) return r;
+        // x's codes in both layouts, under the scale of the amax its producer
+        // took: rows for this product, transposed (kept until the backward)
+        // for the weight gradient
+        if ((r = launch_quantize_fp8_t(m->f8_xT[slot], m->f8_x, sc, xb, BT, in, FP8_E4M3, m->stream,
+                                       f8_am(m, true, slot, 0))) < 0)
+            return r;
         n += r;
         if ((r = launch_fp8_amax_scale(sc + 2, wb, nw, FP8_E4M3, m->f8_partial, m->stream)) < 0) return r;
         n += r;
         if ((r = launch_quantize_fp8_rows(m->f8_w, sc + 2, wb, nw, FP8_E4M3, m->stream)) < 0) return r;
-        TRY(op.done(n + r, 6.0 * (double)nx + 5.0 * (double)nw));
+        TRY(op.done(n + r, 4.0 * (double)nx + 5.0 * (double)nw));
     }
     const F8Args f8 = {FP8_E4M3, FP8_E4M3, sc + 1, sc + 3};
     const void* bias = bi >= 0 ? P(m, bi) : nullptr;
     Op op(m, GPT2_K_MATMUL);
     const double flops = 2.0 * BT * out * in;
-    if (y2) return op.done(launch_matmul_gelu_f8(y, y2, m->f8_x, m->f8_w, f8, bias, BT, out, in, m->status, m->stream), flops);
+    if (y2)
+        return op.done(launch_matmul_gelu_f8(y, y2, m->f8_x, m->f8_w, f8, bias, BT, out, in, m->status, m->stream,
+                                             y2_amax),
+                       flops);
     return op.done(launch_matmul_f8(y, 0, m->f8_x, m->f8_w, f8, bias, BT, out, in, nullptr, m->status, m->stream), flops);
 }
 
@@ -541,22 +556,30 @@ int f8_linear_fwd(gpt2* m, int slot, void* y, void* y2, const void* x, int wi, i
 // as the forward wrote them); the bias
 // gradient from dy as stored (bf16), deferred. aux: dx is the gradient
 // through the GELU, bf16(dy W) * aux, with its column sums to colsum.
+// dy's amax comes from the kernel that wrote dy (f8_am(slot, 1)), or, with
+// dy_pass, from a pass of its own over dy (the QKV projection's: taking it in
+// the attention backward's accumulator stores measured no cheaper); with aux,
+// dx_amax takes the amax of the gradient through the GELU for the next FP8
+// linear down.
 int f8_linear_bwd(gpt2* m, int slot, void* dx, const void* dy, const void* x, int wi, int bi, int BT, int in,
-                  int out, const void* aux, float* colsum) {
+                  int out, const void* aux, float* colsum, unsigned* dx_amax = nullptr, bool dy_pass = false) {
     float* sc = f8_sc(m, slot);
     const bf16* dyb = (const bf16*)dy;
     {
         Op op(m, GPT2_K_FP8_QUANT);
         int n = 0, r;
         const int64_t ny = (int64_t)BT * out;
-        if ((r = launch_fp8_amax_scale(sc + 4, dyb, ny, FP8_E5M2, m->f8_partial, m->stream)) < 0) return r;
-        n += r;
-        if ((r = launch_quantize_fp8_t(m->f8_dyT, m->f8_dy, sc + 4, dyb, BT, out, FP8_E5M2, m->stream)) < 0) return r;
+        // dy's codes in both layouts under the scale of its amax
+        if (dy_pass && (r = launch_fp8_amax_scale(sc + 4, dyb, ny, FP8_E5M2, m->f8_partial, m->stream)) < 0) return r;
+        n += dy_pass ? r : 0;
+        if ((r = launch_quantize_fp8_t(m->f8_dyT, m->f8_dy, sc + 4, dyb, BT, out, FP8_E5M2, m->stream,
+                                       dy_pass ? nullptr : f8_am(m, true, slot, 1))) < 0)
+            return r;
         n += r;
         if ((r = launch_quantize_fp8_t(m->f8_wT, nullptr, sc + 2, (const bf16*)P(m, wi), out, in, FP8_E4M3,
                                        m->stream)) < 0)
             return r;
-        TRY(op.done(n + r, 4.0 * ny + 2.0 * ny + 3.0 * (double)out * in));
+        TRY(op.done(n + r, (dy_pass ? 6.0 : 4.0) * ny + 3.0 * (double)out * in));
         (void)x;  // its transposed codes were written by the forward
     }
     const double flops = 2.0 * BT * in * out;
@@ -564,7 +587,7 @@ int f8_linear_bwd(gpt2* m, int slot, void* dx, const void* dy, const void* x, in
         const F8Args f8 = {FP8_E5M2, FP8_E4M3, sc + 5, sc + 3};
         Op op(m, GPT2_K_MATMUL);
         const int r = aux ? launch_matmul_gelu_backward_f8(dx, m->f8_dy, m->f8_wT, f8, aux, BT, in, out, m->status,
-                                                           m->stream, colsum)
+                                                           m->stream, colsum, dx_amax)
                           : launch_matmul_f8(dx, 0, m->f8_dy, m->f8_wT, f8, nullptr, BT, in, out, nullptr, m->status,
                                              m->stream);
         TRY(op.done(r, flops));
@@ -616,17 +639,20 @@ int linear_bwd(gpt2* m, void* dx, const void* dy, const void* x, int wi, int bi,
     return GPT2_OK;
 }
 
-int ln_fwd(gpt2* m, void* y, float* mean, float* rstd, const void* x, int gi, int BT) {
+int ln_fwd(gpt2* m, void* y, float* mean, float* rstd, const void* x, int gi, int BT, unsigned* amax = nullptr) {
     Op op(m, GPT2_K_LAYERNORM_FWD);
-    return op.done(launch_layernorm_forward(m->dtype, y, mean, rstd, x, P(m, gi), P(m, gi + 1), BT, m->C, m->stream),
+    return op.done(launch_layernorm_forward(m->dtype, y, mean, rstd, x, P(m, gi), P(m, gi + 1), BT, m->C, m->stream,
+                                            amax),
                    (double)BT * (2.0 * m->C * m->act + 8));
 }
 
 // Residual join then LayerNorm: xsum = x + r; y = LN(xsum) with the norm at gi.
-int res_ln_fwd(gpt2* m, void* y, float* mean, float* rstd, void* xsum, const void* x, const void* r, int gi, int BT) {
+// amax (or null): the largest |y| is merged into it (an FP8 linear's input).
+int res_ln_fwd(gpt2* m, void* y, float* mean, float* rstd, void* xsum, const void* x, const void* r, int gi, int BT,
+               unsigned* amax = nullptr) {
     Op op(m, GPT2_K_LAYERNORM_FWD);
     return op.done(launch_residual_layernorm_forward(m->dtype, y, mean, rstd, xsum, x, r, P(m, gi), P(m, gi + 1), BT,
-                                                     m->C, m->stream),
+                                                     m->C, m->stream, amax),
                    (double)BT * (4.0 * m->C * m->act + 8));
 }
 
@@ -634,14 +660,14 @@ int res_ln_fwd(gpt2* m, void* y, float* mean, float* rstd, void* xsum, const voi
 // of the new dres go to the bias gradient bi (when bi >= 0): the bias of the
 // linear layer whose output joins the residual stream at this point.
 int ln_bwd_res(gpt2* m, int accumulate, const void* dy, const void* x, int gi, const float* mean, const float* rstd,
-               int bi, int BT) {
+               int bi, int BT, unsigned* amax = nullptr) {
     const int np = bi >= 0 ? 3 : 2;
     float* part = (float*)cs_take(m, 1, (int)(layernorm_backward_scratch(BT, m->C) / 4));
     if (!part) return GPT2_ERR_WORKSPACE;
     Op op(m, GPT2_K_LAYERNORM_BWD);
     int rows = 0;
     TRY(op.done(launch_layernorm_backward_residual_rows(m->dtype, m->dres, accumulate, part, np, dy, x, P(m, gi),
-                                                        mean, rstd, BT, m->C, m->stream, &rows),
+                                                        mean, rstd, BT, m->C, m->stream, &rows, amax),
                 (double)BT * ((3.0 + accumulate) * m->C * m->act + 8)));
     cs_defer(m, part, rows, np * m->C, m->C, G(m, gi), G(m, gi + 1), bi >= 0 ? G(m, bi) : nullptr);
     return GPT2_OK;
@@ -653,6 +679,9 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
     const int BT = B * T, C = m->C, L = m->L;
     if (m->fp8 && BT % 16) return GPT2_ERR_ARG;  // the FP8 weight gradients contract over B*T in 16-byte rows
     const bool f8_qkv = m->fp8 & GPT2_FP8_QKV, f8_mlp = m->fp8 & GPT2_FP8_MLP, f8_head = m->fp8 & GPT2_FP8_HEAD;
+    // the FP8 operands' amax words, filled by the kernels that write the operands
+    if (m->fp8 && cudaMemsetAsync(m->f8_amax, 0, (size_t)(3 * L + 1) * 2 * 4, m->stream) != cudaSuccess)
+        return GPT2_ERR_CUDA;
     {
         Op op(m, GPT2_K_ENCODER_FWD);
         TRY(op.done(launch_encoder_forward(m->dtype, m->layers[0].x, m->tokens, P(m, T_WTE), P(m, T_WPE), B, T, C,
@@ -660,7 +689,8 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
                     (double)BT * (3.0 * C * m->act + 4)));
     }
     // each residual join is fused with the LayerNorm that reads its result
-    TRY(ln_fwd(m, m->layers[0].ln1, m->layers[0].mean1, m->layers[0].rstd1, m->layers[0].x, tidx(0, 0), BT));
+    TRY(ln_fwd(m, m->layers[0].ln1, m->layers[0].mean1, m->layers[0].rstd1, m->layers[0].x, tidx(0, 0), BT,
+               f8_am(m, f8_qkv, F8_QKV, 0)));
     for (int l = 0; l < L; l++) {
         LayerBufs& b = m->layers[l];
         if (f8_qkv) TRY(f8_linear_fwd(m, 3 * l + F8_QKV, b.qkv, nullptr, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
@@ -671,9 +701,11 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
                         attn_fwd_flops(B, T, C)));
         }
         TRY(linear_fwd(m, m->fwd_tmp, b.atty, tidx(l, 4), tidx(l, 5), BT, C, C));
-        TRY(res_ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, b.x, m->fwd_tmp, tidx(l, 6), BT));
+        TRY(res_ln_fwd(m, b.ln2, b.mean2, b.rstd2, b.x1, b.x, m->fwd_tmp, tidx(l, 6), BT,
+                       f8_am(m, f8_mlp, 3 * l + F8_FC, 0)));
         if (f8_mlp) {
-            TRY(f8_linear_fwd(m, 3 * l + F8_FC, b.fch, b.fchg, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C));
+            TRY(f8_linear_fwd(m, 3 * l + F8_FC, b.fch, b.fchg, b.ln2, tidx(l, 8), tidx(l, 9), BT, C, 4 * C,
+                              f8_am(m, true, 3 * l + F8_FCPROJ, 0)));
         } else if (m->dtype == GPT2_MODE_BF16) {
             // the GELU runs in the epilogue of its linear, which keeps gelu'
             // (in fch) for the backward instead of the GELU input
@@ -692,9 +724,11 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
         else TRY(linear_fwd(m, m->fwd_tmp, b.fchg, tidx(l, 10), tidx(l, 11), BT, 4 * C, C));
         if (l + 1 < L) {
             LayerBufs& n = m->layers[l + 1];
-            TRY(res_ln_fwd(m, n.ln1, n.mean1, n.rstd1, n.x, b.x1, m->fwd_tmp, tidx(l + 1, 0), BT));
+            TRY(res_ln_fwd(m, n.ln1, n.mean1, n.rstd1, n.x, b.x1, m->fwd_tmp, tidx(l + 1, 0), BT,
+                           f8_am(m, f8_qkv, 3 * (l + 1) + F8_QKV, 0)));
         } else {
-            TRY(res_ln_fwd(m, m->lnf, m->meanf, m->rstdf, m->xL, b.x1, m->fwd_tmp, tlnf(L, 0), BT));
+            TRY(res_ln_fwd(m, m->lnf, m->meanf, m->rstdf, m->xL, b.x1, m->fwd_tmp, tlnf(L, 0), BT,
+                           f8_am(m, f8_head, 3 * L, 0)));
         }
     }
     if (f8_head) TRY(f8_linear_fwd(m, 3 * L, m->logits, nullptr, m->lnf, T_WTE, -1, BT, C, m->Vp));
@@ -703,7 +737,7 @@ int forward_impl(gpt2* m, const int32_t* targets, int B, int T) {
         {
             Op op(m, GPT2_K_CLASSIFIER);
             TRY(op.done(launch_classifier(m->dtype, m->logits, m->losses, targets, BT, m->V, m->Vp, 1.0f / BT,
-                                          m->status, m->stream),
+                                          m->status, m->stream, f8_am(m, f8_head, 3 * L, 1)),
                         (double)BT * (2.0 * m->Vp * m->act + 8)));
         }
         Op op(m, GPT2_K_LOSS_MEAN);
@@ -726,7 +760,8 @@ int backward_impl(gpt2* m) {
     }
     // the LayerNorm backwards write the residual gradient dres and, on the
     // way, the bias gradient of the projection whose output joins there
-    TRY(ln_bwd_res(m, 0, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, tidx(L - 1, 11), BT));
+    TRY(ln_bwd_res(m, 0, m->dtmp, m->xL, tlnf(L, 0), m->meanf, m->rstdf, tidx(L - 1, 11), BT,
+                   f8_am(m, f8_mlp, 3 * (L - 1) + F8_FCPROJ, 1)));
     for (int l = L - 1; l >= 0; l--) {
         LayerBufs& b = m->layers[l];
         // MLP branch
@@ -737,7 +772,7 @@ int backward_impl(gpt2* m) {
             float* part = cs_take(m, rows, 4 * C);
             if (!part) return GPT2_ERR_WORKSPACE;
             TRY(f8_linear_bwd(m, 3 * l + F8_FCPROJ, m->dbig, m->dres, b.fchg, tidx(l, 10), -1, BT, 4 * C, C, b.fch,
-                              part));
+                              part, f8_am(m, true, 3 * l + F8_FC, 1)));
             cs_defer(m, part, rows, 4 * C, 4 * C, G(m, tidx(l, 9)), nullptr, nullptr);
         } else if (m->dtype == GPT2_MODE_BF16) {
             // dW of the MLP projection, then its input gradient times the
@@ -771,9 +806,12 @@ int backward_impl(gpt2* m) {
                                                   m->scratch, m->status, m->stream),
                         2.5 * attn_fwd_flops(B, T, C)));
         }
-        if (f8_qkv) TRY(f8_linear_bwd(m, 3 * l + F8_QKV, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C, nullptr, nullptr));
+        if (f8_qkv)
+            TRY(f8_linear_bwd(m, 3 * l + F8_QKV, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C, nullptr,
+                              nullptr, nullptr, true));
         else TRY(linear_bwd(m, m->dtmp, m->dqkv, b.ln1, tidx(l, 2), tidx(l, 3), BT, C, 3 * C));
-        TRY(ln_bwd_res(m, 1, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, l > 0 ? tidx(l - 1, 11) : -1, BT));
+        TRY(ln_bwd_res(m, 1, m->dtmp, b.x, tidx(l, 0), b.mean1, b.rstd1, l > 0 ? tidx(l - 1, 11) : -1, BT,
+                       l > 0 ? f8_am(m, f8_mlp, 3 * (l - 1) + F8_FCPROJ, 1) : nullptr));
     }
     {
         // every deferred column sum of this backward, in ceil(jobs / 32) launches
