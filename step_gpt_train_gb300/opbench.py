@@ -28,7 +28,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # head's three): `--ops step_gemms` runs each once, in this order.
 def step_gemm_counts(L: int = 12) -> dict:
     per_layer = ["gemm_qkv_fwd", "gemm_proj_fwd", "gemm_fc_fwd_gelu", "gemm_fcproj_fwd", "gemm_fcproj_dw",
-                 "gemm_fcproj_dx_gelu", "gemm_fc_dw", "gemm_fc_dx", "gemm_proj_dw", "gemm_proj_dx", "gemm_qkv_dw",
+                 "gemm_fcproj_dx_gelu_bias", "gemm_fc_dw", "gemm_fc_dx", "gemm_proj_dw", "gemm_proj_dx", "gemm_qkv_dw",
                  "gemm_qkv_dx"]
     counts = {n: L for n in per_layer}
     counts.update({"gemm_lmhead_fwd": 1, "gemm_lmhead_dx": 1, "gemm_lmhead_dw": 1})
