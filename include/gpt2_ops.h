@@ -313,14 +313,17 @@ int gpt2_op_adamw(float* master, void* param_bf16, const float* grad, float* m, 
 int gpt2_debug_set_wait_limit(int64_t cycles);
 int gpt2_debug_stall_matmul(int on);
 
-/* gpt2_debug_matmul_pair: on != 0 routes the wide bf16 matmuls (N >= 1024,
- * M >= 512, one k-range per tile) to the CTA-pair kernel, which issues one
- * M = 256 tensor-core product for two neighbouring SMs (tcgen05 .cta_group::2)
- * so that each SM loads half of the B tile; 0 (the default) keeps every
- * matmul on the one-CTA kernel. Process-wide; takes effect for matmuls
- * launched after it returns; on > 1 also sets the number of two-CTA
- * clusters launched (else the number the device keeps resident). Returns the
- * number of clusters the pair kernel launches (on != 0) or 0. */
+/* gpt2_debug_matmul_pair: on = 1 (the default) routes the wide plain bf16
+ * matmuls (no GELU epilogue, N >= 1024, M >= 512, one k-range per tile) to
+ * the CTA-pair kernel, which issues one M = 256 tensor-core product for two
+ * neighbouring SMs (tcgen05 .cta_group::2) so that each SM loads half of the
+ * B tile; on = 2 routes the GELU and GELU-gradient matmuls of that size there
+ * too; 0 keeps every matmul on the one-CTA kernel. Process-wide; takes effect
+ * for matmuls launched after it returns (a captured step graph keeps the
+ * kernels it was captured with); on > 2 also sets the number of two-CTA
+ * clusters launched (else the number the device keeps resident). Returns
+ * the number of clusters the pair kernel launches (on != 0) or 0. A switch
+ * for measurements and tests, not needed in normal use. */
 int gpt2_debug_matmul_pair(int on);
 
 #ifdef __cplusplus

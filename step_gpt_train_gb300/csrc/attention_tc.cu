@@ -43,7 +43,8 @@ constexpr int AT_HD = 64;                  // head size
 constexpr int AT_TILE = AT_M * AT_HD * 2;  // 16 KB: 128 rows of 64 bf16
 constexpr int AT_THREADS = 192;
 // shared memory: Q stage 0, 1 | K stage 0, 1 | V stage 0, 1 | barriers
-constexpr int AT_SMEM = 6 * AT_TILE + 256 + 1024;
+constexpr int AT_OSTG = 2048;             // per softmax warp: 16 rows of O (bf16) on their way out
+constexpr int AT_SMEM = 6 * AT_TILE + 4 * AT_OSTG + 256 + 1024;
 constexpr uint32_t AT_TMEM_COLS = 256;     // S [0,128), O [128,192), P [192,256) (bf16 pairs)
 constexpr float AT_LN2 = 0.6931471805599453f;
 constexpr float AT_RESCALE = 8.f;          // log2 of the largest P before the reference max moves
@@ -148,8 +149,9 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     auto sQ = [&](int st) { return base + st * AT_TILE; };
     auto sK = [&](int st) { return base + (2 + st) * AT_TILE; };
     auto sV = [&](int st) { return base + (4 + st) * AT_TILE; };
-    const uint32_t bars = base + 6 * AT_TILE;
-    uint8_t* bar_area = gbase + 6 * AT_TILE;
+    uint8_t* ostg = gbase + 6 * AT_TILE;  // [4 softmax warps][AT_OSTG]
+    const uint32_t bars = base + 6 * AT_TILE + 4 * AT_OSTG;
+    uint8_t* bar_area = gbase + 6 * AT_TILE + 4 * AT_OSTG;
     // barriers: q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free,
     // p_full, p_free, o_done, o_free, drain
     auto q_full = [&](int i) { return bars + 8u * (0 + i); };
@@ -407,18 +409,41 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
-            if (q < a.T) {
+            {
+                // O / l as bf16 pairs (pk[u]: columns 2u, 2u + 1), out through
+                // this warp's staging buffer 16 rows at a time (chunk c of
+                // staged row s at (c ^ (s & 7)) * 16: conflict-free both ways),
+                // so that each global store covers four whole 128-byte rows
                 const int b = it.bh / a.H, h = it.bh % a.H;
                 const float inv = 1.f / l;
-                bf16* orow = a.o + ((int64_t)b * a.T + q) * a.C + h * AT_HD;
+                uint32_t pk[32];
 #pragma unroll
-                for (int u = 0; u < 8; u++) {
-                    float f[8];
+                for (int u = 0; u < 32; u++)
+                    pk[u] = cvt_bf16x2(__uint_as_float(ov[u >> 4][(u & 15) * 2]) * inv,
+                                       __uint_as_float(ov[u >> 4][(u & 15) * 2 + 1]) * inv);
+                uint8_t* st = ostg + (warp - 2) * AT_OSTG;
+                bf16* obase = a.o + (int64_t)b * a.T * a.C + h * AT_HD;
+                const int q0 = it.qt * AT_M + quad * 32;  // the warp's first row
 #pragma unroll
-                    for (int e = 0; e < 8; e++) f[e] = __uint_as_float(ov[u / 4][(u % 4) * 8 + e]) * inv;
-                    store8(orow + u * 8, f);
+                for (int hh = 0; hh < 2; hh++) {
+                    __syncwarp();  // the previous rows have been read out
+                    if ((lane >> 4) == hh) {
+                        const int sr = lane & 15;
+#pragma unroll
+                        for (int c = 0; c < 8; c++)
+                            *reinterpret_cast<uint4*>(st + sr * 128 + ((c ^ (sr & 7)) << 4)) =
+                                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int sr = i * 4 + (lane >> 3), c = lane & 7;
+                        const int qr = q0 + 16 * hh + sr;
+                        const uint4 v = *reinterpret_cast<const uint4*>(st + sr * 128 + ((c ^ (sr & 7)) << 4));
+                        if (qr < a.T) *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.C + c * 8) = v;
+                    }
                 }
-                a.lse[(int64_t)it.bh * a.T + q] = (m + log2f(l)) * AT_LN2;
+                if (q < a.T) a.lse[(int64_t)it.bh * a.T + q] = (m + log2f(l)) * AT_LN2;
             }
         }
     }

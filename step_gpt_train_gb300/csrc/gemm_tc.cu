@@ -529,14 +529,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // for the work that takes 16 KB of A and 32 KB of B in the one-CTA kernel.
 // Cross-CTA hand-offs (no multicast): both CTAs' operand copies complete on
 // the even CTA's full barriers (TMA .cta_group::2 with a cluster address);
-// the even CTA's relay warp tells the odd CTA, by remote mbarrier arrives,
-// when a stage may be refilled and when an accumulator is complete; the odd
-// CTA's epilogue warps arrive remotely on the even CTA's accumulator-empty
-// barriers. Both CTAs allocate and free tensor memory together
-// (.cta_group::2), and leave only after a cluster barrier, once the even
-// CTA's MMAs, which read the odd CTA's shared memory and write its tensor
-// memory, are complete. Every mbarrier wait is bounded (cluster-scope
-// acquire where the arrival comes from the other CTA).
+// the even CTA's MMA warp commits each stage's release and each accumulator's
+// completion twice, to its own barrier and to the odd CTA's (one commit per
+// barrier, by its cluster address), so the odd CTA's producer and epilogue
+// wait on barriers of their own; the odd CTA's epilogue warps arrive remotely
+// on the even CTA's accumulator-empty barriers. (A relay warp that waited on
+// the even CTA's barriers and arrived on the odd CTA's halved the rate: the
+// odd CTA's refills started a relay hop late.) Both CTAs allocate and free
+// tensor memory together (.cta_group::2), and leave only after a cluster
+// barrier, once the even CTA's MMAs, which read the odd CTA's shared memory
+// and write its tensor memory, are complete. Every mbarrier wait is bounded
+// (cluster-scope acquire where the arrival comes from the other CTA) and uses
+// try_wait, so a waiting producer or MMA warp takes no issue slots from the
+// epilogue warps on its scheduler (spinning on test_wait cost the GELU
+// epilogues 8-9%).
+// EPI_MUL's column sums: each warp's 32 rows, as in the one-CTA kernel (row
+// 4 * (128-row tile) + quad of the partials).
 constexpr int PBN = 256;                    // pair tile: 256 x 256
 constexpr int PBM = 256;
 constexpr int P_STAGES = 6;
@@ -545,8 +553,7 @@ constexpr int P_B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_NACC = 2;                   // accumulators in TMEM: a tile's epilogue overlaps the next tile's MMAs
 constexpr int P_TMEM_COLS = 512;
-constexpr int P_THREADS = 352;              // 11 warps: + the relay warp
-constexpr int P_RELAY_WARP = 10;
+constexpr int P_THREADS = 320;              // 10 warps: TMA, MMA, 8 epilogue
 constexpr int P_OUT_BYTES = EPI_WARPS * 2048;
 constexpr int P_BAR_BYTES = 512;
 constexpr int P_BIAS_BYTES = EPI_WARPS * (PBN / 2) * 4;
@@ -593,6 +600,17 @@ __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, vola
 __device__ __forceinline__ bool warp_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
     const bool ok = mbar_wait_cl(bar, parity, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Commit of the pair's MMAs issued so far to the barrier at offset `bar` in
+// both CTAs of the pair: this CTA's, then the odd CTA's (by its cluster
+// address). Each commit arrives once its MMAs are complete.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 1;" : "=r"(remote) : "r"(bar));
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(remote)
+                 : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is signalled on a
@@ -693,7 +711,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
                 const int m0 = w.mt * PBM + (int)rank * 128, n0 = w.nt * PBN + (int)rank * (PBN / 2);
                 for (int kb = w.kb0; kb < w.kb1; kb++) {
-                    if (!mbar_spin<true>(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
+                    if (!mbar_wait_cl(empty_bar(stage), phase ^ 1u, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
@@ -746,12 +764,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             Work w;
             for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
-                if (!warp_spin<true>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
+                if (!warp_wait_cl(tempty_bar(acc), acc_phase ^ 1u, abort_flag, g.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PBN);
                 for (int kb = kb0; kb < kb1; kb++) {
                     // both CTAs' operands (their copies complete on this CTA's barrier)
-                    if (!warp_spin<true>(full_bar(stage), phase, abort_flag, g.status)) {
+                    if (!warp_wait_cl(full_bar(stage), phase, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
@@ -769,20 +787,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                                 ::"r"(d_tmem), "l"(ad), "l"(bd), "r"(idesc), "r"((kb > kb0 || k > 0) ? 1u : 0u)
                                 : "memory");
                     }
-                    if (leader)
-                        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                         empty_bar(stage))
-                                     : "memory");
+                    if (leader) tc_commit_pair(empty_bar(stage));  // the stage may be refilled in both CTAs
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (leader)
-                    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     tfull_bar(acc))
-                                 : "memory");
+                if (leader) tc_commit_pair(tfull_bar(acc));  // both CTAs' accumulator rows are complete
                 if (++acc == P_NACC) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -793,41 +805,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                                  drain_bar)
                              : "memory");
             mbar_drain(drain_bar, 0, g.status);
-        }
-    } else if (warp == P_RELAY_WARP) {
-        if (lane == 0) {
-            // ------------------------------------------------ relay
-            // even CTA: each stage's release and each accumulator's completion
-            // to the odd CTA
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            bool ok = true;
-            Work w;
-            for (int idx = 0; ok && get_work_pair(g, idx, w); idx++) {
-                for (int kb = w.kb0; kb < w.kb1; kb++) {
-                    if (rank == 0) {
-                        if (!(ok = mbar_spin(empty_bar(stage), phase, abort_flag, g.status))) break;
-                        mbar_arrive_cta(empty_bar(stage), peer);
-                    }
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                if (rank == 0) {
-                    if (!(ok = mbar_spin(tfull_bar(acc), acc_phase, abort_flag, g.status))) break;
-                    tc_fence_after();
-                    tc_fence_before();
-                    mbar_arrive_cta(tfull_bar(acc), peer);
-                }
-                if (++acc == P_NACC) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
-            }
         }
     } else {
         // ---------------------------------------------------- epilogue (warps 2..9, both CTAs)
@@ -840,6 +817,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         uint8_t* stage = out_stage + ew * 2048;
         const uint32_t stage_addr = smem_addr(stage);
         const bool use_bias = g.bias != nullptr && !g.partials;
+        const bool want_csum = EPI == EPI_MUL && g.colsum != nullptr;
         int acc = 0;
         uint32_t acc_phase = 0;
         Work w;
@@ -885,6 +863,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             auto xcol = [&](int c) { return (split ? 0 : n0) + (cfirst + c) * 32; };
             auto ncols = [&](int c) { return g.N - (n0 + (cfirst + c) * 32); };
             auto bias_at = [&](int c) -> const float* { return use_bias ? bias_s + c * 32 : nullptr; };
+            // EPI_MUL column sums of this warp's 32 rows: row 4 * (128-row tile) + quad
+            float* csum_row =
+                want_csum ? g.colsum + (int64_t)((2 * w.mt + (int)rank) * 4 + quad) * g.N + n0 + cfirst * 32 : nullptr;
+            auto csum_at = [&](int c) -> float* { return want_csum ? csum_row + c * 32 : nullptr; };
+            const int nrows = max(0, min(32, g.M - y));  // this warp's rows inside the matrix
             uint32_t ra[32], rb[32];
             if (nchunks > 0) {
                 tc_ld32_issue(tbase + (uint32_t)(cfirst * 32), ra);
@@ -894,7 +877,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
                 epi_chunk<EPI>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
-                               ncols(c), lane);
+                               ncols(c), lane, 1.f, csum_at(c), nrows);
                 if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();
                 if (!more) break;
@@ -902,7 +885,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
                 epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1), ys,
-                               z, ncols(c + 1), lane);
+                               z, ncols(c + 1), lane, 1.f, csum_at(c + 1), nrows);
                 if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
                 if (more2) tc_ld_wait(ra);
@@ -912,6 +895,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             if (lane == 0) {
                 if (rank == 0) mbar_arrive(tempty_bar(acc));
                 else mbar_arrive_cta(tempty_bar(acc), 0);
+            }
+            if (want_csum && m0 + (int)rank * 128 < g.M) {
+                // rows outside the matrix in a 128-row tile that has rows inside it (the
+                // partials hold 4 rows per such tile): zero sums for the columns inside it
+                for (int c = nchunks; c < CHUNKS; c++)
+                    if (n0 + (cfirst + c) * 32 + lane < g.N) csum_row[c * 32 + lane] = 0.f;
             }
             if (++acc == P_NACC) {
                 acc = 0;
@@ -1159,14 +1148,20 @@ int pair_clusters() {
     return n;
 }
 
-// The pair kernel takes bf16 products with one k-range per tile (no
-// partials), 256-wide tiles of a wide output (N >= 1024) and at least two
-// 256-row tiles, when it is switched on (gemm_tc_use_pair; off by default:
-// its relayed hand-offs measured slower than the one-CTA kernel); the rest
-// runs on the one-CTA kernel.
-bool g_use_pair = false;
+// The pair kernel takes plain bf16 products (no epilogue op) with one
+// k-range per tile (no partials), 256-wide tiles of a wide output (N >= 1024)
+// and at least two 256-row tiles (gemm_tc_use_pair(0) turns it off); the rest
+// runs on the one-CTA kernel. Measured at 32768 rows: K = 768, N = 2304 78 us
+// against 84 (one CTA), N = 50304 1419 us against 1579; the GELU and
+// GELU-gradient epilogues, which bound their products, ran 7% slower in the
+// pair kernel (152 against 142 us, 172 against 160), so those stay on the
+// one-CTA kernel (gemm_tc_use_pair(2...) routes them too, for measurements).
+bool g_use_pair = true;
+bool g_pair_epi = false;  // also the GELU and GELU-gradient epilogues
 int g_pair_override = 0;  // > 0: the number of clusters to launch instead of the resident count
-bool use_pair(int M, int N, bool partials) { return g_use_pair && !partials && N >= 1024 && M >= 512; }
+bool use_pair(int M, int N, bool partials, int epi) {
+    return g_use_pair && (epi == EPI_NONE || g_pair_epi) && !partials && N >= 1024 && M >= 512;
+}
 
 }  // namespace
 
@@ -1174,7 +1169,8 @@ int gemm_tc_set_wait_limit(long long cycles) { return set_wait_limit(cycles); }
 
 int gemm_tc_use_pair(int on) {
     g_use_pair = on != 0;
-    g_pair_override = on > 1 ? on : 0;
+    g_pair_epi = on > 1;
+    g_pair_override = on > 2 ? on : 0;
     return on ? (g_pair_override ? g_pair_override : pair_clusters()) : 0;
 }
 
@@ -1206,7 +1202,7 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
-    if (use_pair(M, N, partials) && !colsum && !f8 && !amax) {
+    if (use_pair(M, N, partials, epi) && !f8 && !amax) {
         // 256 x 256 pair tiles, each CTA loading 128 rows of A and 128 columns of B
         const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + PBN - 1) / PBN;
         CUtensorMap ma, mb, md, md2;
@@ -1222,6 +1218,8 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         g.a_fmt = g.b_fmt = 0;
         g.bias = bias;
         g.aux = aux;
+        g.colsum = colsum;
+        g.amax = nullptr;
         g.status = status;
         g.M = M;
         g.N = N;

@@ -58,6 +58,8 @@ def main(argv=None):
     ap.add_argument("--H", type=int, default=12)
     ap.add_argument("--V", type=int, default=50257)
     ap.add_argument("--Vp", type=int, default=50304)
+    ap.add_argument("--pair", type=int, default=None,
+                    help="route the wide matmuls to the CTA-pair kernel (1) or to the one-CTA kernel (0)")
     args = ap.parse_args(argv)
 
     import torch
@@ -65,6 +67,8 @@ def main(argv=None):
 
     g.load_library(build=True)
     torch.cuda.set_device(0)
+    if args.pair is not None:
+        g.load_library().gpt2_debug_matmul_pair(args.pair)
     hbm, tc, src = peaks()
     B, T, C, H, V, Vp = args.B, args.T, args.C, args.H, args.V, args.Vp
     N = B * T

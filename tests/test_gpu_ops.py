@@ -85,6 +85,91 @@ def test_matmul(torch_cuda, mode, case):
         assert_close(got, ref, 1e-5, atol_frac=1e-5, what="fp32 matmul")
 
 
+# The CTA-pair kernel's range: at least 512 rows and 1024 columns.
+PAIR_CASES = [
+    # M, N, K, a_mn, b_mn, d_fp32, bias
+    (1000, 1032, 1000, 0, 0, 0, True),   # ragged in every dimension (a half-empty last pair tile)
+    (520, 2304, 768, 0, 1, 0, False),    # B MN-major
+    (768, 1024, 512, 1, 0, 0, False),    # A MN-major
+    (1024, 1280, 256, 1, 1, 1, False),   # both MN-major, fp32 out
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES)
+def test_matmul_pair_kernel(torch_cuda, case):
+    """Plain products in the range of the CTA-pair kernel (tcgen05 .cta_group::2,
+    one M = 256 product for two SMs; the default there) against the oracle, and
+    against the one-CTA kernel on the same inputs (gpt2_debug_matmul_pair(0))."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import gpt2_op_matmul, load_library
+    lib = load_library()
+    M, N, K, a_mn, b_mn, d_fp32, use_bias = case
+    A = inputs(111, (M * K,), 1.0, 1)
+    B = inputs(112, (N * K,), 1.0, 1)
+    bias = inputs(113, (N,), 1.0, 1) if use_bias else None
+    dA, dB = dev(A, 1), dev(B, 1)
+    dbias = dev(bias, 1) if use_bias else None
+    out_dtype = torch.float32 if d_fp32 else torch.bfloat16
+    got = {}
+    try:
+        for pair in (1, 0):
+            assert lib.gpt2_debug_matmul_pair(pair) >= 0
+            D = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
+            gpt2_op_matmul(D, dA, a_mn, dB, b_mn, M, N, K, bias=dbias)
+            torch.cuda.synchronize()
+            got[pair] = host(D)
+    finally:
+        lib.gpt2_debug_matmul_pair(1)
+    ref = _gemm_ref(A, a_mn, B, b_mn, M, N, K, bias)
+    for pair in (1, 0):
+        assert np.all(np.isfinite(got[pair]))
+        if d_fp32:
+            assert_close(got[pair], ref, 1e-5, atol=tc_accum_atol(K, ref), what=f"fp32 matmul, pair={pair}")
+        else:
+            assert_close(got[pair], ref, BF16_REL, atol_frac=1e-3, what=f"bf16 matmul, pair={pair}")
+    # the same products in both kernels: fp32 out to the accumulation bound, bf16
+    # out to one rounding (an ulp is up to 2^-7 of the value)
+    if d_fp32:
+        assert_close(got[1], got[0], 1e-5, atol=tc_accum_atol(K, ref), what="pair vs one-CTA kernel")
+    else:
+        assert_close(got[1], got[0], 2.0 ** -7, atol=1e-30, what="pair vs one-CTA kernel")
+
+
+def test_matmul_gelu_pair_kernel(torch_cuda):
+    """The GELU and GELU-gradient epilogues (with the bias-gradient column sums)
+    in the CTA-pair kernel (gpt2_debug_matmul_pair(2): off by default) against
+    the one-CTA kernel's: the stored values to one bf16 rounding, the column
+    sums to fp32 summation error."""
+    torch = torch_cuda
+    from step_gpt_train_gb300.gpt2 import (gpt2_op_matmul_gelu, gpt2_op_matmul_gelu_backward_bias, load_library)
+    lib = load_library()
+    M, N, K, K2 = 1000, 3072, 768, 512
+    A = dev(inputs(120, (M, K), 1.0, 1))
+    W = dev(inputs(121, (N, K), K ** -0.5, 1))
+    b = dev(inputs(122, (N,), 0.5, 1))
+    dY = dev(inputs(123, (M, K2), 1.0, 1))
+    W2 = dev(inputs(124, (K2, N), K2 ** -0.5, 1))
+    res = {}
+    try:
+        for pair in (2, 0):
+            assert lib.gpt2_debug_matmul_pair(pair) >= 0
+            dgelu = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            out = torch.full_like(dgelu, float("nan"))
+            gpt2_op_matmul_gelu(dgelu, out, A, W, b)
+            du = torch.full_like(dgelu, float("nan"))
+            dbias = torch.full((N,), float("nan"), device="cuda")
+            gpt2_op_matmul_gelu_backward_bias(du, dbias, dY, W2, dgelu)
+            torch.cuda.synchronize()
+            res[pair] = [host(t) for t in (dgelu, out, du, dbias)]
+    finally:
+        lib.gpt2_debug_matmul_pair(1)
+    for name, x2, x0 in zip(("gelu'", "gelu", "du"), res[2][:3], res[0][:3]):
+        assert np.all(np.isfinite(x2)), name
+        assert_close(x2, x0, 2.0 ** -7, atol=1e-30, what=f"{name}: pair vs one-CTA kernel")
+    scale = float(np.abs(res[0][2].astype(np.float64)).sum(0).max())
+    assert_close(res[2][3], res[0][3], 0, atol=1e-5 * scale, what="dbias: pair vs one-CTA kernel")
+
+
 def test_matmul_full_size_sampled(torch_cuda):
     """Bench-size GEMMs (GPT-2 124M at B*T = 32768); outputs sampled and computed one by one."""
     torch = torch_cuda
