@@ -471,7 +471,7 @@ def main():
     if fp8_names:
         # the family mixes FP8 and bf16 products: reported against the bf16 peak
         peak_src += "; the FP8 products' own peak is twice it (the nominal e4m3 : bf16 ratio)"
-    roofline = {"kernel": "gemm_tc_kernel (every matmul of the step)", "bound": "tensor",
+    roofline = {"kernel": "gemm_tc_kernel and gemm_pair_kernel (every matmul of the step)", "bound": "tensor",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "peak_source": peak_src,
                 "traffic": traffic, "launches_per_step": mm_launches / K,

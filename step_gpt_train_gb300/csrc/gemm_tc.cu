@@ -49,14 +49,16 @@ constexpr int NUM_THREADS = 320;     // 10 warps
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;
 
-template <int BN> struct TileCfg {
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 192 ? 5 : 6);
+// NB: output staging buffers per epilogue warp (two for the GELU epilogue's
+// two outputs, paid for with one operand stage).
+template <int BN, int NB = 1> struct TileCfg {
+    static constexpr int STAGES = (BN == 256 ? 4 : (BN == 192 ? 5 : 6)) - (NB == 2 ? 1 : 0);
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // power of two >= two accumulators
     static constexpr int OUT_STAGE_BYTES = 2048;                        // per epilogue warp: 32 rows x 64 B
-    static constexpr int OUT_BYTES = EPI_WARPS * OUT_STAGE_BYTES;
+    static constexpr int OUT_BYTES = EPI_WARPS * NB * OUT_STAGE_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int BIAS_BYTES = EPI_WARPS * (BN / 2) * 4;         // per warp: its half of the tile (fp32)
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 /*align*/ + BAR_BYTES + BIAS_BYTES;
@@ -114,15 +116,39 @@ __device__ __forceinline__ bool get_work(const GemmArgs& g, int idx, Work& w) {
     return true;
 }
 
-// Stage 32 bf16 values of this lane's row (64 bytes) once the buffer's
-// previous TMA store has read it, then store the 32 x 32 box at (x, y, z).
+// A warp's output staging: NB buffers of 2 KB (32 rows x 64 bytes) used in
+// turn, each TMA store from the next one. A buffer is written once the store
+// that last used it has read it: with one buffer that is the store before,
+// with two the one before that (the store before may still be reading the
+// other buffer), so consecutive stores overlap.
+template <int NB>
+struct Stager {
+    uint8_t* base;
+    uint32_t base_addr;
+    int sel;
+    __device__ __forceinline__ uint8_t* buf() const { return base + sel * 2048; }
+    __device__ __forceinline__ uint32_t addr() const { return base_addr + (uint32_t)sel * 2048u; }
+    __device__ __forceinline__ void wait_free(int lane) const {
+        if (lane == 0) {
+            if (NB == 2) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            else bulk_wait_read_all();
+        }
+        __syncwarp();
+    }
+    __device__ __forceinline__ void advance() {
+        if (NB == 2) sel ^= 1;
+    }
+};
+
+// Stage 32 bf16 values of this lane's row (64 bytes) in the stager's next
+// buffer, then store the 32 x 32 box at (x, y, z); returns the buffer written.
 // am2 (or null): a running maximum of the stored values' magnitudes, as a
 // bf16 pair (NaN-ignoring, as fmaxf).
-__device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* stage, uint32_t stage_addr,
-                                                 const CUtensorMap* map, int x, int y, int z, int lane,
-                                                 __nv_bfloat162* am2 = nullptr) {
-    if (lane == 0) bulk_wait_read_all();
-    __syncwarp();
+template <int NB>
+__device__ __forceinline__ uint8_t* stage_store_bf16(const float (&f)[32], Stager<NB>& st, const CUtensorMap* map,
+                                                     int x, int y, int z, int lane, __nv_bfloat162* am2 = nullptr) {
+    st.wait_free(lane);
+    uint8_t* stage = st.buf();
 #pragma unroll
     for (int q = 0; q < 4; q++) {
         uint4 v;
@@ -137,7 +163,9 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) tma_store_3d(map, stage_addr, x, y, z);
+    if (lane == 0) tma_store_3d(map, st.addr(), x, y, z);
+    st.advance();
+    return stage;
 }
 
 // One 32-column chunk of this warp's 32 rows: + bias, the epilogue op,
@@ -150,9 +178,9 @@ __device__ __forceinline__ void stage_store_bf16(const float (&f)[32], uint8_t* 
 // (resp. |D|) as stored. Only rows inside the matrix may pass it (outside,
 // a GELU row is gelu(bias)); columns outside hold 0 in both forms (B's rows
 // and the bias read as 0 there, and the factor of EPI_MUL is 0).
-template <int EPI, bool F8 = false>
+template <int EPI, bool F8 = false, int NB = 1>
 __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* bias_s, bool fp32_out,
-                                          uint8_t* stage, uint32_t stage_addr, const CUtensorMap* mapD,
+                                          Stager<NB>& st, const CUtensorMap* mapD,
                                           const CUtensorMap* mapD2, const uint4 (&aux)[4], int x, int y, int z,
                                           int ncols_valid, int lane, float alpha = 1.f, float* csum_dst = nullptr,
                                           int nrows = 32, __nv_bfloat162* am2 = nullptr) {
@@ -183,10 +211,10 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
                 f[q * 8 + 2 * i + 1] *= __high2float(h[i]);
             }
         }
-        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane, am2);
+        const uint8_t* stage = stage_store_bf16(f, st, mapD, x, y, z, lane, am2);
         if (csum_dst) {
-            // the staged rows (the TMA store only reads them too; the next
-            // chunk overwrites them only after this warp's next sync)
+            // the staged rows (the TMA store only reads them too; they are
+            // written again only after this warp's next sync)
             int col;
             const float sum = staged_colsum32(
                 [&](int r, int q) { return stage + r * 64 + ((q ^ ((r >> 1) & 3)) << 4); }, nrows, lane, col);
@@ -201,16 +229,16 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
             asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(ub) : "f"(f[j + 1]), "f"(f[j]));
             gelu_pair(__uint_as_float(ub << 16), __uint_as_float(ub & 0xFFFF0000u), f[j], f[j + 1], gd[j], gd[j + 1]);
         }
-        stage_store_bf16(gd, stage, stage_addr, mapD, x, y, z, lane);  // gelu'(u), kept for the backward
-        stage_store_bf16(f, stage, stage_addr, mapD2, x, y, z, lane, am2);  // gelu(u)
+        stage_store_bf16(gd, st, mapD, x, y, z, lane);  // gelu'(u), kept for the backward
+        stage_store_bf16(f, st, mapD2, x, y, z, lane, am2);  // gelu(u)
     } else if (!fp32_out) {
-        stage_store_bf16(f, stage, stage_addr, mapD, x, y, z, lane);
+        stage_store_bf16(f, st, mapD, x, y, z, lane);
     } else {
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
             if (hh * 16 >= ncols_valid) break;  // uniform across the warp
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+            st.wait_free(lane);
+            uint8_t* stage = st.buf();
 #pragma unroll
             for (int q = 0; q < 4; q++)
                 stage16(stage, lane, q,
@@ -218,7 +246,8 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&r)[32], const float* 
                                    __float_as_uint(f[hh * 16 + q * 4 + 2]), __float_as_uint(f[hh * 16 + q * 4 + 3])));
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) tma_store_3d(mapD, stage_addr, x + hh * 16, y, z);
+            if (lane == 0) tma_store_3d(mapD, st.addr(), x + hh * 16, y, z);
+            st.advance();
         }
     }
 }
@@ -242,7 +271,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const GemmArgs g) {
     static_assert(!F8 || (!A_MN && !B_MN), "FP8 operands: K-major");
     constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
-    using Cfg = TileCfg<BN>;
+    constexpr int NB = EPI == EPI_GELU ? 2 : 1;  // output staging buffers per epilogue warp
+    using Cfg = TileCfg<BN, NB>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned operand ring (the 128-byte swizzle pattern repeats every 1024 B).
@@ -251,7 +281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t a_stage0 = base;
     const uint32_t b_stage0 = base + S * Cfg::A_BYTES;
-    uint8_t* out_stage = gbase + S * Cfg::STAGE_BYTES;  // [EPI_WARPS][2 KB], 1024-aligned
+    uint8_t* out_stage = gbase + S * Cfg::STAGE_BYTES;  // [EPI_WARPS][NB][2 KB], 1024-aligned
     uint8_t* bar_area = out_stage + Cfg::OUT_BYTES;
     const uint32_t bars = base + S * Cfg::STAGE_BYTES + Cfg::OUT_BYTES;
     // barrier layout: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
@@ -403,8 +433,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row_in_tile = quad * 32 + lane;
         // this warp's bias slice [BN/2 columns] and output staging buffer
         float* bias_s = reinterpret_cast<float*>(bar_area + Cfg::BAR_BYTES) + ew * (BN / 2);
-        uint8_t* stage = out_stage + ew * Cfg::OUT_STAGE_BYTES;
-        const uint32_t stage_addr = smem_addr(stage);
+        uint8_t* stage = out_stage + ew * NB * Cfg::OUT_STAGE_BYTES;
+        Stager<NB> stg{stage, smem_addr(stage), 0};
         const bool use_bias = g.bias != nullptr && !g.partials;
         const float alpha = F8 ? *g.a_scale * *g.b_scale : 1.f;
         // EPI_MUL column sums: each warp writes the sums of its 32 rows of a
@@ -475,7 +505,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // ra holds chunk c; chunk c+1 is loaded into rb while ra is stored
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
-                epi_chunk<EPI, F8>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
+                epi_chunk<EPI, F8>(ra, bias_at(c), fp32_out, stg, &tmD, &tmD2, aux[0], xcol(c), ys, z,
                                    ncols(c), lane, alpha, csum_at(c), nrows,
                                    want_amax && m0 + row_in_tile < g.M ? &am2 : nullptr);
                 if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
@@ -484,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_ld_wait(rb);
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
-                epi_chunk<EPI, F8>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1),
+                epi_chunk<EPI, F8>(rb, bias_at(c + 1), fp32_out, stg, &tmD, &tmD2, aux[1], xcol(c + 1),
                                    ys, z, ncols(c + 1), lane, alpha, csum_at(c + 1), nrows,
                                    want_amax && m0 + row_in_tile < g.M ? &am2 : nullptr);
                 if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
@@ -548,13 +578,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 constexpr int PBN = 256;                    // pair tile: 256 x 256
 constexpr int PBM = 256;
 constexpr int P_STAGES = 6;
+constexpr int P_NBUF = 1;                   // output staging buffers per epilogue warp
 constexpr int P_A_BYTES = 128 * BK * 2;     // this CTA's A rows
 constexpr int P_B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_NACC = 2;                   // accumulators in TMEM: a tile's epilogue overlaps the next tile's MMAs
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_THREADS = 320;              // 10 warps: TMA, MMA, 8 epilogue
-constexpr int P_OUT_BYTES = EPI_WARPS * 2048;
+constexpr int P_OUT_BYTES = EPI_WARPS * P_NBUF * 2048;
 constexpr int P_BAR_BYTES = 512;
 constexpr int P_BIAS_BYTES = EPI_WARPS * (PBN / 2) * 4;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_OUT_BYTES + 1024 + P_BAR_BYTES + P_BIAS_BYTES;
@@ -814,8 +845,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         constexpr int CHUNKS = PBN / 64;
         const int row_in_tile = (int)rank * 128 + quad * 32 + lane;  // row in the pair tile
         float* bias_s = reinterpret_cast<float*>(bar_area + P_BAR_BYTES) + ew * (PBN / 2);
-        uint8_t* stage = out_stage + ew * 2048;
-        const uint32_t stage_addr = smem_addr(stage);
+        uint8_t* stage = out_stage + ew * P_NBUF * 2048;
+        Stager<P_NBUF> stg{stage, smem_addr(stage), 0};
         const bool use_bias = g.bias != nullptr && !g.partials;
         const bool want_csum = EPI == EPI_MUL && g.colsum != nullptr;
         int acc = 0;
@@ -876,7 +907,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             for (int c = 0; c < nchunks; c += 2) {
                 const bool more = c + 1 < nchunks;
                 if (more) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 1) * 32), rb);
-                epi_chunk<EPI>(ra, bias_at(c), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[0], xcol(c), ys, z,
+                epi_chunk<EPI>(ra, bias_at(c), fp32_out, stg, &tmD, &tmD2, aux[0], xcol(c), ys, z,
                                ncols(c), lane, 1.f, csum_at(c), nrows);
                 if (EPI == EPI_MUL && c + 2 < CHUNKS) load_aux(c + 2, aux[0]);
                 __syncwarp();
@@ -884,7 +915,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 tc_ld_wait(rb);
                 const bool more2 = c + 2 < nchunks;
                 if (more2) tc_ld32_issue(tbase + (uint32_t)((cfirst + c + 2) * 32), ra);
-                epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stage, stage_addr, &tmD, &tmD2, aux[1], xcol(c + 1), ys,
+                epi_chunk<EPI>(rb, bias_at(c + 1), fp32_out, stg, &tmD, &tmD2, aux[1], xcol(c + 1), ys,
                                z, ncols(c + 1), lane, 1.f, csum_at(c + 1), nrows);
                 if (EPI == EPI_MUL && c + 3 < CHUNKS) load_aux(c + 3, aux[1]);
                 __syncwarp();
@@ -1060,7 +1091,7 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
 template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                const GemmArgs& args, int grid, cudaStream_t s) {
-    using Cfg = TileCfg<BN>;
+    using Cfg = TileCfg<BN, EPI == EPI_GELU ? 2 : 1>;
     constexpr int smem = Cfg::SMEM_BYTES;
     static_assert(smem <= 232448, "shared memory per CTA");
     smem_attr((const void*)gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, smem);

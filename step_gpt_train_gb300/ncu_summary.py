@@ -13,9 +13,9 @@
       DRAM bytes of the matmul family over one training step, from a capture
       (gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum)
       of `opbench --ops step_gemms --warmup 0 --iters 1`: every gemm_tc_kernel
-      launch starts the next of the step's matmuls (in opbench.STEP_GEMMS
-      order), a split_reduce_kernel after it belongs to it, and each matmul's
-      bytes count as often as the step runs it
+      or gemm_pair_kernel launch starts the next of the step's matmuls (in
+      opbench.STEP_GEMMS order), a split_reduce_kernel after it belongs to it,
+      and each matmul's bytes count as often as the step runs it
 """
 from __future__ import annotations
 
@@ -133,7 +133,7 @@ def step_traffic(path: str) -> str:
             d["write"] = _bytes(val, unit)
     ops, cur = [], None
     for d in per_launch.values():
-        if d["name"].startswith("gemm_tc_kernel"):
+        if d["name"].startswith(("gemm_tc_kernel", "gemm_pair_kernel")):
             cur = {"launches": 0, "bytes": 0.0}
             ops.append(cur)
         elif not d["name"].startswith("split_reduce_kernel") or cur is None:
