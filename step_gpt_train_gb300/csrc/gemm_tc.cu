@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const GemmArgs g) {
     static_assert(!F8 || (!A_MN && !B_MN), "FP8 operands: K-major");
     constexpr int KE = F8 ? 128 : BK;  // values of a k-block (128 bytes of each row either way)
-    constexpr int NB = EPI == EPI_GELU ? 2 : 1;  // output staging buffers per epilogue warp
+    constexpr int NB = EPI != EPI_NONE ? 2 : 1;  // output staging buffers per epilogue warp
     using Cfg = TileCfg<BN, NB>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -1091,7 +1091,7 @@ Plan make_plan(int M, int N, int K, int d_fp32) {
 template <int BN, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 void launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                const GemmArgs& args, int grid, cudaStream_t s) {
-    using Cfg = TileCfg<BN, EPI == EPI_GELU ? 2 : 1>;
+    using Cfg = TileCfg<BN, EPI != EPI_NONE ? 2 : 1>;
     constexpr int smem = Cfg::SMEM_BYTES;
     static_assert(smem <= 232448, "shared memory per CTA");
     smem_attr((const void*)gemm_tc_kernel<BN, A_MN, B_MN, EPI, F8>, smem);
