@@ -607,6 +607,304 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     }
 }
 
+// Wide rows (bf16, C from 1032 to 2048 values, beyond the staged forms: the
+// 1.5B model's 1600), where a warp per row leaves each lane 40 or more columns
+// of accumulators: a block of LN_WIDE_THREADS threads takes a group of rows at a
+// time, and thread t owns the 8 columns of vector t of every row, so its
+// column sums stay in registers and no block merges them across warps. A
+// group's row sums go through one block reduction per quantity: warp
+// shuffles, then the warps' values from shared memory added in warp order
+// (double-buffered by group, so one barrier a reduction suffices). Each
+// thread copies its own 16-byte pieces of the rows LN_WIDE_S - 1 groups ahead
+// into a ring in shared memory (cp.async) and reads only those, so the ring
+// needs no barrier and loads stay in flight through the reductions. Same
+// formulas as the other forms; a row's sums are added in a different order,
+// so results differ from them in the last bits.
+#define LN_WIDE_THREADS 256
+#define LN_WIDE_WARPS (LN_WIDE_THREADS / 32)
+#define LN_WIDE_R 4      // rows a group, forward
+#define LN_WIDE_R_BWD 2  // rows a group, backward
+#define LN_WIDE_S 3      // groups in a block's ring
+// ring bytes of a block: LN_WIDE_S groups x rows x pieces (forward: x, r;
+// backward: x, dy, the residual gradient, mean and rstd) x threads x 16
+#define LN_WIDE_FWD_SMEM (LN_WIDE_S * LN_WIDE_R * 2 * LN_WIDE_THREADS * 16)
+#define LN_WIDE_BWD_SMEM (LN_WIDE_S * LN_WIDE_R_BWD * 4 * LN_WIDE_THREADS * 16)
+
+// The R sums of this thread, summed over the block, into v[] (every thread
+// gets them). red: this call's [LN_WIDE_WARPS][R] buffer, not written again
+// before the block's next barrier.
+template <int R>
+__device__ __forceinline__ void ln_wide_block_sum(float (&v)[R], float* red) {
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+    for (int k = 0; k < R; k++) v[k] = warp_sum(v[k]);
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < R; k++) red[w * R + k] = v[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < R; k++) {
+        float t = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < LN_WIDE_WARPS; ww++) t += red[ww * R + k];
+        v[k] = t;
+    }
+}
+
+__global__ void __launch_bounds__(LN_WIDE_THREADS, 2)
+    ln_fwd_wide_kernel(bf16* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd,
+                       bf16* __restrict__ xsum, const bf16* __restrict__ x, const bf16* __restrict__ r,
+                       const bf16* __restrict__ gamma, const bf16* __restrict__ beta, int N, int C,
+                       unsigned* __restrict__ amax) {
+    constexpr int R = LN_WIDE_R, S = LN_WIDE_S;
+    extern __shared__ __align__(16) uint8_t wring[];  // [S][R][x | r][threads][16 B]
+    __shared__ float red[4][LN_WIDE_WARPS * R];       // two reductions a group, double-buffered by group
+    const int t = threadIdx.x;
+    const bool own = t < C / 8;                       // this thread's vector is inside the row
+    auto piece = [&](int slot, int q, int a) { return wring + ((size_t)((slot * R + q) * 2 + a) * LN_WIDE_THREADS + t) * 16; };
+    const int gstride = gridDim.x * R;
+    auto issue = [&](int r0, int slot) {
+        if (own) {
+#pragma unroll
+            for (int q = 0; q < R; q++) {
+                const int row = r0 + q;
+                if (row < N) {
+                    cp_async16(piece(slot, q, 0), x + (int64_t)row * C + t * 8);
+                    if (r) cp_async16(piece(slot, q, 1), r + (int64_t)row * C + t * 8);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    float g[8], b[8];
+    if (own) {
+        load8(gamma + t * 8, g);
+        load8(beta + t * 8, b);
+    }
+    const int g0 = blockIdx.x * R;
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) issue(g0 + k * gstride, k);
+    float am = 0.f;  // largest |y| of this thread (amax)
+    int slot = 0, it = 0;
+    for (int r0 = g0; r0 < N; r0 += gstride, it ^= 1) {
+        issue(r0 + (S - 1) * gstride, (slot + S - 1) % S);
+        cp_async_wait<S - 1>();  // this thread's pieces of the group have landed
+        float v[R][8];
+#pragma unroll
+        for (int q = 0; q < R; q++) {
+            const int row = r0 + q;
+            if (own && row < N) {
+                load8(reinterpret_cast<const bf16*>(piece(slot, q, 0)), v[q]);
+                if (r) {
+                    float u[8];
+                    load8(reinterpret_cast<const bf16*>(piece(slot, q, 1)), u);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) v[q][j] = to_float(from_float<bf16>(v[q][j] + u[j]));
+                    store8(xsum + (int64_t)row * C + t * 8, v[q]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++) v[q][j] = 0.f;
+            }
+        }
+        float mu[R];
+#pragma unroll
+        for (int q = 0; q < R; q++) {
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; j++) sum += v[q][j];
+            mu[q] = sum;
+        }
+        ln_wide_block_sum<R>(mu, red[2 * it]);
+        float rs[R];
+#pragma unroll
+        for (int q = 0; q < R; q++) {
+            mu[q] /= (float)C;
+            float ss = 0.f;
+            if (own) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float d = v[q][j] - mu[q];
+                    ss += d * d;
+                }
+            }
+            rs[q] = ss;
+        }
+        ln_wide_block_sum<R>(rs, red[2 * it + 1]);
+#pragma unroll
+        for (int q = 0; q < R; q++) {
+            const int row = r0 + q;
+            rs[q] = 1.0f / sqrtf(rs[q] / (float)C + LN_EPS);
+            if (row >= N) continue;
+            if (own) {
+                float o[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) o[j] = (v[q][j] - mu[q]) * rs[q] * g[j] + b[j];
+                store8(y + (int64_t)row * C + t * 8, o);
+                if (amax) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) am = fmaxf(am, fabsf(o[j]));
+                }
+            }
+            if (t == 0) {
+                mean[row] = mu[q];
+                rstd[row] = rs[q];
+            }
+        }
+        slot = (slot + 1) % S;
+    }
+    cp_async_wait<0>();
+    if (amax) amax_merge(amax, am);
+}
+
+__global__ void __launch_bounds__(LN_WIDE_THREADS, 2)
+    ln_bwd_wide_kernel(bf16* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
+                       const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ gamma,
+                       const float* __restrict__ mean, const float* __restrict__ rstd, int N, int C,
+                       unsigned* __restrict__ amax) {
+    using namespace tc;
+    constexpr int R = LN_WIDE_R_BWD, S = LN_WIDE_S;
+    extern __shared__ __align__(16) uint8_t wring[];  // [S][R][x | dy | residual gradient | mean, rstd][threads][16 B]
+    __shared__ float red[2][LN_WIDE_WARPS * 2 * R];   // one reduction a group, double-buffered by group
+    const int t = threadIdx.x;
+    const bool own = t < C / 8;
+    auto piece = [&](int slot, int q, int a) { return wring + ((size_t)((slot * R + q) * 4 + a) * LN_WIDE_THREADS + t) * 16; };
+    const int gstride = gridDim.x * R;
+    auto issue = [&](int r0, int slot) {
+        if (own) {
+#pragma unroll
+            for (int q = 0; q < R; q++) {
+                const int row = r0 + q;
+                if (row < N) {
+                    const int64_t off = (int64_t)row * C + t * 8;
+                    cp_async16(piece(slot, q, 0), x + off);
+                    cp_async16(piece(slot, q, 1), dy + off);
+                    if (accumulate) cp_async16(piece(slot, q, 2), out + off);
+                    cp_async4(piece(slot, q, 3), mean + row);
+                    cp_async4(piece(slot, q, 3) + 4, rstd + row);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    uint64_t g2[4], ag[4], ab[4], ao[4];
+    {
+        uint4 gr = make_uint4(0, 0, 0, 0);
+        if (own) gr = *reinterpret_cast<const uint4*>(gamma + t * 8);
+        const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            g2[p] = bf2_to_f2(gw[p]);
+            ag[p] = ab[p] = ao[p] = 0;
+        }
+    }
+    const int g0 = blockIdx.x * R;
+#pragma unroll
+    for (int k = 0; k < S - 1; k++) issue(g0 + k * gstride, k);
+    float am = 0.f;  // largest |out| of this thread (amax)
+    int slot = 0, it = 0;
+    for (int r0 = g0; r0 < N; r0 += gstride, it ^= 1) {
+        issue(r0 + (S - 1) * gstride, (slot + S - 1) % S);
+        cp_async_wait<S - 1>();
+        // the row sums of dxhat = dy gamma and of dxhat xhat
+        float s[2 * R];
+#pragma unroll
+        for (int q = 0; q < R; q++) {
+            s[2 * q] = s[2 * q + 1] = 0.f;
+            if (own && r0 + q < N) {
+                const float* mr = reinterpret_cast<const float*>(piece(slot, q, 3));
+                const float mu = mr[0], rs = mr[1];
+                const uint64_t rs2 = f2_pack(rs, rs), nmr2 = f2_pack(-mu * rs, -mu * rs);
+                const uint4 xr = *reinterpret_cast<const uint4*>(piece(slot, q, 0));
+                const uint4 dr = *reinterpret_cast<const uint4*>(piece(slot, q, 1));
+                const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w}, dw[4] = {dr.x, dr.y, dr.z, dr.w};
+                uint64_t s1 = 0, s2 = 0;
+#pragma unroll
+                for (int p = 0; p < 4; p++) {
+                    const uint64_t xh = f2_fma(bf2_to_f2(xw[p]), rs2, nmr2);
+                    const uint64_t dh = f2_mul(bf2_to_f2(dw[p]), g2[p]);
+                    s1 = f2_add(s1, dh);
+                    s2 = f2_fma(dh, xh, s2);
+                }
+                float a0, a1, b0, b1;
+                f2_unpack(s1, a0, a1);
+                f2_unpack(s2, b0, b1);
+                s[2 * q] = a0 + a1;
+                s[2 * q + 1] = b0 + b1;
+            }
+        }
+        ln_wide_block_sum<2 * R>(s, red[it]);
+#pragma unroll
+        for (int q = 0; q < R; q++) {
+            const int row = r0 + q;
+            if (!own || row >= N) continue;
+            const float m1 = s[2 * q] / (float)C, m2 = s[2 * q + 1] / (float)C;
+            const float* mr = reinterpret_cast<const float*>(piece(slot, q, 3));
+            const float mu = mr[0], rs = mr[1];
+            const uint64_t rs2 = f2_pack(rs, rs), nmr2 = f2_pack(-mu * rs, -mu * rs);
+            const uint64_t m1_2 = f2_pack(m1, m1), m2_2 = f2_pack(m2, m2);
+            const uint4 xr = *reinterpret_cast<const uint4*>(piece(slot, q, 0));
+            const uint4 dr = *reinterpret_cast<const uint4*>(piece(slot, q, 1));
+            uint4 rr = make_uint4(0, 0, 0, 0);
+            if (accumulate) rr = *reinterpret_cast<const uint4*>(piece(slot, q, 2));
+            const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w}, dw[4] = {dr.x, dr.y, dr.z, dr.w};
+            const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const uint64_t d2 = bf2_to_f2(dw[p]);
+                const uint64_t xh = f2_fma(bf2_to_f2(xw[p]), rs2, nmr2);
+                ag[p] = f2_fma(d2, xh, ag[p]);
+                ab[p] = f2_add(ab[p], d2);
+                const uint64_t dh = f2_mul(d2, g2[p]);
+                // rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat))
+                uint64_t o = f2_mul(rs2, f2_sub(dh, f2_fma(xh, m2_2, m1_2)));
+                if (accumulate) o = f2_add(o, bf2_to_f2(rw[p]));
+                float o0, o1;
+                f2_unpack(o, o0, o1);
+                if (amax) am = fmaxf(am, fmaxf(fabsf(o0), fabsf(o1)));
+                __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+                ow[p] = *reinterpret_cast<uint32_t*>(&h);
+                if (np == 3) ao[p] = f2_add(ao[p], bf2_to_f2(ow[p]));
+            }
+            *reinterpret_cast<uint4*>(out + (int64_t)row * C + t * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        slot = (slot + 1) % S;
+    }
+    cp_async_wait<0>();
+    if (amax) amax_merge(amax, am);
+    // this thread's column sums: partial[block][q * C + column]
+    if (own) {
+        float* pb = partial + (size_t)blockIdx.x * np * C;
+        float vg[8], vb[8], vo[8];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            f2_unpack(ag[p], vg[2 * p], vg[2 * p + 1]);
+            f2_unpack(ab[p], vb[2 * p], vb[2 * p + 1]);
+            f2_unpack(ao[p], vo[2 * p], vo[2 * p + 1]);
+        }
+        store8(pb + t * 8, vg);
+        store8(pb + C + t * 8, vb);
+        if (np == 3) store8(pb + 2 * C + t * 8, vo);
+    }
+}
+
+// The wide-row forms (bf16, rows of LN_WIDE_MIN_C to 8 * LN_WIDE_THREADS
+// values): two resident blocks per SM. At C = 1024 the staged forms measured
+// faster (forward 1.52 against 1.99 ms per step of the 350M model at B = 16,
+// backward equal); at C = 1600 the wide ones (1.5B at B = 8: forward 2.74
+// against 3.25 ms, backward 3.60 against 9.59).
+#define LN_WIDE_MIN_C 1025
+static bool ln_wide(int dtype, int C) {
+    return dtype == GPT2_MODE_BF16 && C >= LN_WIDE_MIN_C && C <= 8 * LN_WIDE_THREADS;
+}
+static int ln_wide_blocks(int N, int rows = LN_WIDE_R) {
+    const int cap = 2 * gpt2_num_sms();
+    const int b = (N + rows - 1) / rows;
+    return b < cap ? (b < 1 ? 1 : b) : cap;
+}
+
 static size_t ln_staged_smem(int dtype, int C) {
     const size_t es = dtype == GPT2_MODE_BF16 ? 2 : 4;
     return (size_t)LN_BWD_WARPS * LN_STAGES * (3 * C * es + 16);
@@ -640,6 +938,13 @@ static int ln_forward(int dtype, void* y, float* mean, float* rstd, void* xsum, 
                       const void* gamma, const void* beta, int N, int C, cudaStream_t s, unsigned* amax) {
     const int blocks = (N + LN_FWD_WARPS - 1) / LN_FWD_WARPS;
     if (blocks == 0) return 0;
+    if (ln_wide(dtype, C)) {
+        smem_attr((const void*)ln_fwd_wide_kernel, LN_WIDE_FWD_SMEM);
+        ln_fwd_wide_kernel<<<ln_wide_blocks(N), LN_WIDE_THREADS, LN_WIDE_FWD_SMEM, s>>>(
+            (bf16*)y, mean, rstd, (bf16*)xsum, (const bf16*)x, (const bf16*)r, (const bf16*)gamma, (const bf16*)beta,
+            N, C, amax);
+        return 1;
+    }
     const size_t es = dtype == GPT2_MODE_BF16 ? 2 : 4;
     if ((size_t)C * es <= LN_STAGED_MAX_ROW_BYTES) {
         // three blocks of 8 warps per SM (74 KB of ring each at C = 768 bf16)
@@ -702,7 +1007,8 @@ static int ln_bwd_staged_blocks(int N) {
 }
 
 size_t layernorm_backward_scratch(int N, int C) {
-    const int b = ln_bwd_blocks(N) > ln_bwd_staged_blocks(N) ? ln_bwd_blocks(N) : ln_bwd_staged_blocks(N);
+    int b = ln_bwd_blocks(N) > ln_bwd_staged_blocks(N) ? ln_bwd_blocks(N) : ln_bwd_staged_blocks(N);
+    if (ln_wide_blocks(N, LN_WIDE_R_BWD) > b) b = ln_wide_blocks(N, LN_WIDE_R_BWD);
     return (size_t)b * 3 * C * 4;
 }
 
@@ -744,6 +1050,14 @@ static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumula
 static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partial_s, int np, const void* dy,
                             const void* x, const void* gamma, const float* mean, const float* rstd, int N, int C,
                             cudaStream_t s, unsigned* amax = nullptr) {
+    if (ln_wide(dtype, C)) {
+        const int blocks = ln_wide_blocks(N, LN_WIDE_R_BWD);
+        smem_attr((const void*)ln_bwd_wide_kernel, LN_WIDE_BWD_SMEM);
+        ln_bwd_wide_kernel<<<blocks, LN_WIDE_THREADS, LN_WIDE_BWD_SMEM, s>>>(
+            (bf16*)out, accumulate, partial_s, np, (const bf16*)dy, (const bf16*)x, (const bf16*)gamma, mean, rstd, N,
+            C, amax);
+        return blocks;
+    }
     if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
         // 111 KB of ring per block at C = 768 bf16, two blocks per SM
         const int blocks = ln_bwd_staged_blocks(N);

@@ -201,7 +201,7 @@ def test_matmul_full_size_sampled(torch_cuda):
 
 
 @pytest.mark.parametrize("mode", [1, 0])
-@pytest.mark.parametrize("C", [64, 768, 1600])
+@pytest.mark.parametrize("C", [64, 768, 1024, 1600, 2048])  # above 1024 (bf16): the wide-row kernels
 def test_layernorm(torch_cuda, mode, C):
     torch = torch_cuda
     from step_gpt_train_gb300.gpt2 import gpt2_op_layernorm_backward, gpt2_op_layernorm_forward
@@ -234,7 +234,7 @@ def test_layernorm(torch_cuda, mode, C):
 
 
 @pytest.mark.parametrize("mode", [1, 0])
-@pytest.mark.parametrize("C", [64, 768])
+@pytest.mark.parametrize("C", [64, 768, 1600])  # 1600 (bf16): the wide-row kernels
 @pytest.mark.parametrize("accumulate", [0, 1])
 def test_residual_layernorm(torch_cuda, mode, C, accumulate):
     """Residual join + LayerNorm forward, and LayerNorm backward into the residual
