@@ -463,7 +463,7 @@ __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return tc::f2_pack(w
 // and the same per-element formulas as ln_bwd_staged_kernel, two columns per
 // instruction; gamma is held in shared memory as fp32 for the block. Column
 // pairs (2p, 2p+1) of a lane's 8-vector sit in one 64-bit accumulator.
-template <int VPL>
+template <int VPL, int STG = LN_STAGES>
 __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     ln_bwd_bf16_kernel(bf16* __restrict__ out, bool accumulate, float* __restrict__ partial, int np,
                        const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ gamma,
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     float* sg = reinterpret_cast<float*>(sm_raw);  // gamma, fp32
     const size_t row_bytes = (size_t)C * 2;
     const size_t slot_bytes = 3 * row_bytes + 16;  // x | dy | residual gradient | mean, rstd
-    uint8_t* ring = sm_raw + g_bytes + (size_t)w * LN_STAGES * slot_bytes;
+    uint8_t* ring = sm_raw + g_bytes + (size_t)w * STG * slot_bytes;
     const int stride = gridDim.x * LN_BWD_WARPS;
     const int row0 = blockIdx.x * LN_BWD_WARPS + w;
     for (int c = threadIdx.x; c < C; c += blockDim.x) sg[c] = __bfloat162float(gamma[c]);
@@ -512,12 +512,12 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
     __syncthreads();  // gamma staged
 
 #pragma unroll
-    for (int k = 0; k < LN_STAGES - 1; k++) issue(row0 + k * stride, k);
+    for (int k = 0; k < STG - 1; k++) issue(row0 + k * stride, k);
     int slot = 0;
     for (int row = row0; row < N; row += stride) {
         __syncwarp();
-        issue(row + (LN_STAGES - 1) * stride, (slot + LN_STAGES - 1) % LN_STAGES);
-        cp_async_wait<LN_STAGES - 1>();
+        issue(row + (STG - 1) * stride, (slot + STG - 1) % STG);
+        cp_async_wait<STG - 1>();
         __syncwarp();
         const uint8_t* sb = ring + (size_t)slot * slot_bytes;
         const float mu = reinterpret_cast<const float*>(sb + 3 * row_bytes)[0];
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(LN_BWD_WARPS * 32, 2)
                 *reinterpret_cast<uint4*>(out + (int64_t)row * C + idx * 8) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
         }
-        slot = (slot + 1) % LN_STAGES;
+        slot = (slot + 1) % STG;
     }
     if (amax) amax_merge(amax, am);
     cp_async_wait<0>();
@@ -1032,15 +1032,28 @@ static void ln_bwd_staged_launch(int blocks, size_t smem, void* out, bool accumu
         (T*)out, accumulate, partial, np, (const T*)dy, (const T*)x, (const T*)gamma, mean, rstd, N, C);
 }
 
-template <int VPL>
+template <int VPL, int STG>
 static void ln_bwd_bf16_launch(int blocks, size_t smem, void* out, bool accumulate, float* partial, int np,
                                const void* dy, const void* x, const void* gamma, const float* mean,
                                const float* rstd, int N, int C, cudaStream_t s, unsigned* amax) {
-    smem_attr((const void*)ln_bwd_bf16_kernel<VPL>,
-              LN_BWD_WARPS * LN_STAGES * (3 * LN_STAGED_MAX_ROW_BYTES + 16) + 1024 * 4);
-    ln_bwd_bf16_kernel<VPL><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((bf16*)out, accumulate, partial, np,
-                                                                     (const bf16*)dy, (const bf16*)x,
-                                                                     (const bf16*)gamma, mean, rstd, N, C, amax);
+    smem_attr((const void*)ln_bwd_bf16_kernel<VPL, STG>,
+              LN_BWD_WARPS * STG * (3 * LN_STAGED_MAX_ROW_BYTES + 16) + 1024 * 4);
+    ln_bwd_bf16_kernel<VPL, STG><<<blocks, LN_BWD_WARPS * 32, smem, s>>>((bf16*)out, accumulate, partial, np,
+                                                                          (const bf16*)dy, (const bf16*)x,
+                                                                          (const bf16*)gamma, mean, rstd, N, C,
+                                                                          amax);
+}
+
+// Shared memory of an SM of the current device, and the part reserved per block.
+static int sm_smem_bytes() {
+    static const int v = [] {
+        int d = 0, x = 0;
+        cudaGetDevice(&d);
+        if (cudaDeviceGetAttribute(&x, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d) != cudaSuccess) x = 0;
+        cudaGetLastError();
+        return x;
+    }();
+    return v;
 }
 
 // The row pass of the backward: out (+)= dx and the per-block column sums
@@ -1059,13 +1072,21 @@ static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partia
         return blocks;
     }
     if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
-        // 111 KB of ring per block at C = 768 bf16, two blocks per SM
+        // bf16: 111 KB of ring per block at C = 768, two blocks per SM; where
+        // two blocks of three slots a warp do not fit (C = 1024: 148 KB each),
+        // two slots a warp (99 KB), so that two blocks do
         const int blocks = ln_bwd_staged_blocks(N);
         const size_t smem = ln_staged_smem(dtype, C);
+        const size_t gbytes = ((size_t)C * 4 + 15) & ~(size_t)15;
+        const size_t smem2 = (size_t)LN_BWD_WARPS * 2 * (3 * (size_t)C * 2 + 16) + gbytes;
+        const bool two = 2 * (smem + gbytes + 1024) > (size_t)sm_smem_bytes();
 #define LN_BWD_STAGED_CALL(V)                                                                                   \
-    if (dtype == GPT2_MODE_BF16)                                                                                \
-        ln_bwd_bf16_launch<V>(blocks, smem + (((size_t)C * 4 + 15) & ~(size_t)15), out, accumulate, partial_s,  \
-                              np, dy, x, gamma, mean, rstd, N, C, s, amax);                                     \
+    if (dtype == GPT2_MODE_BF16 && two)                                                                         \
+        ln_bwd_bf16_launch<V, 2>(blocks, smem2, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd, N, C, \
+                                 s, amax);                                                                      \
+    else if (dtype == GPT2_MODE_BF16)                                                                           \
+        ln_bwd_bf16_launch<V, LN_STAGES>(blocks, smem + gbytes, out, accumulate, partial_s, np, dy, x, gamma,   \
+                                         mean, rstd, N, C, s, amax);                                            \
     else                                                                                                        \
         ln_bwd_staged_launch<float, V>(blocks, smem, out, accumulate, partial_s, np, dy, x, gamma, mean, rstd,  \
                                        N, C, s);
