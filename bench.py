@@ -467,7 +467,9 @@ def main():
     peak_src = "measured sustained (MEASURED_PEAKS.json)"
     if not peak:
         peak, peak_src = 1700.0, "fallback"
-    traffic = gemm_traffic_from_profile() if not fp8_names else None
+    # the committed traffic capture is of the 124M B=32 step's matmuls (bf16): other
+    # workloads have none
+    traffic = gemm_traffic_from_profile() if not fp8_names and args.config == "124m-b32" and B == 32 else None
     if fp8_names:
         # the family mixes FP8 and bf16 products: reported against the bf16 peak
         peak_src += "; the FP8 products' own peak is twice it (the nominal e4m3 : bf16 ratio)"
