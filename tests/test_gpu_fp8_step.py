@@ -159,6 +159,30 @@ def test_fp8_step_small_parity(torch_cuda, sel):
         print(f"fp8 {sel} step {s}: loss {losses[s]:.5f} vs {loss:.5f}, worst grad rel L2 {worst:.3e}")
 
 
+FP8_WIDE = dict(n_layer=1, n_embd=1600, n_head=25, vocab=1000, vocab_padded=1024, max_T=128, max_B=3, mode=1)
+
+
+def test_fp8_step_wide_rows_parity(torch_cuda):
+    """One FP8 step (every linear of the selection) at the 1.5B model's width,
+    C = 1600 (one block, H=25, B=3, T=112), where the LayerNorm forward and
+    backward take their wide-row forms and give the quantizer the amax of what
+    they write: against the oracle's FP8 step at the bounds above."""
+    torch = torch_cuda
+    cfg = FP8_WIDE
+    tok, tgt = data.batches("zipf", 3, 112, 1, 23, vocab=1000)
+    model = make_model(cfg)
+    model.set_fp8(7)
+    losses, grads, masters = run_steps(torch, model, tok, tgt, 1, warmup=5)
+    model.close()
+    c = rcfg(cfg)
+    params = R.init_params(c, 1234)
+    loss, g, params, _ = R.train_step(c, params, tok[0], tgt[0], None, 3e-4 * min(1.0, 1 / 5), HP["beta1"],
+                                      HP["beta2"], HP["eps"], HP["weight_decay"], 1, dtype=np.float64,
+                                      fp8=("qkv", "mlp", "head"))
+    worst = check_step(cfg, losses[0], grads[0], masters[0], (loss, g, params), 2e-2, FP8_GRAD_TOL, 1e-3)
+    print(f"fp8 C=1600: loss {losses[0]:.5f} vs {loss:.5f}, worst grad rel L2 {worst:.3e}")
+
+
 def test_fp8_step_differs_from_bf16_by_quantization(torch_cuda):
     """The FP8 linears are really used: the gradients of the same step with
     and without them differ by a quantization-sized amount."""
