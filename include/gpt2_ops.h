@@ -313,11 +313,12 @@ int gpt2_op_adamw(float* master, void* param_bf16, const float* grad, float* m, 
 int gpt2_debug_set_wait_limit(int64_t cycles);
 int gpt2_debug_stall_matmul(int on);
 
-/* gpt2_debug_matmul_pair: on = 1 (the default) routes the wide plain bf16
- * matmuls (no GELU epilogue, N >= 1024, M >= 512, one k-range per tile) to
- * the CTA-pair kernel, which issues one M = 256 tensor-core product for two
- * neighbouring SMs (tcgen05 .cta_group::2) so that each SM loads half of the
- * B tile; on = 2 routes the GELU and GELU-gradient matmuls of that size there
+/* gpt2_debug_matmul_pair: on = 1 (the default) routes the plain bf16
+ * matmuls with M >= 512 and one k-range per tile (no GELU epilogue) to the
+ * CTA-pair kernel when N >= 1024, or when N is 384 to 960, a multiple of 192,
+ * with B K-major and K >= 2048 (192-wide pair tiles); the pair kernel issues one M = 256
+ * tensor-core product for two neighbouring SMs (tcgen05 .cta_group::2) so
+ * that each SM loads half of the B tile; on = 2 routes the GELU and GELU-gradient matmuls of that size there
  * too; 0 keeps every matmul on the one-CTA kernel. Process-wide; takes effect
  * for matmuls launched after it returns (a captured step graph keeps the
  * kernels it was captured with); on > 2 also sets the number of two-CTA

@@ -575,20 +575,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // epilogues 8-9%).
 // EPI_MUL's column sums: each warp's 32 rows, as in the one-CTA kernel (row
 // 4 * (128-row tile) + quad of the partials).
-constexpr int PBN = 256;                    // pair tile: 256 x 256
-constexpr int PBM = 256;
-constexpr int P_STAGES = 6;
+constexpr int PBM = 256;                    // pair tile: 256 rows x PN (256, or 192 for N = 768 outputs)
 constexpr int P_NBUF = 1;                   // output staging buffers per epilogue warp
 constexpr int P_A_BYTES = 128 * BK * 2;     // this CTA's A rows
-constexpr int P_B_BYTES = (PBN / 2) * BK * 2;  // this CTA's half of B
-constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_NACC = 2;                   // accumulators in TMEM: a tile's epilogue overlaps the next tile's MMAs
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_THREADS = 320;              // 10 warps: TMA, MMA, 8 epilogue
 constexpr int P_OUT_BYTES = EPI_WARPS * P_NBUF * 2048;
 constexpr int P_BAR_BYTES = 512;
-constexpr int P_BIAS_BYTES = EPI_WARPS * (PBN / 2) * 4;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_OUT_BYTES + 1024 + P_BAR_BYTES + P_BIAS_BYTES;
+template <int PN> struct PairCfg {
+    static constexpr int B_BYTES = (PN / 2) * BK * 2;  // this CTA's half of B
+    static constexpr int STAGE_BYTES = P_A_BYTES + B_BYTES;
+    static constexpr int STAGES = PN == 256 ? 6 : 7;
+    static constexpr int BIAS_BYTES = EPI_WARPS * (PN / 2) * 4;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + P_OUT_BYTES + 1024 + P_BAR_BYTES + BIAS_BYTES;
+};
+constexpr int P_SMEM_MAX = PairCfg<256>::SMEM_BYTES > PairCfg<192>::SMEM_BYTES ? PairCfg<256>::SMEM_BYTES
+                                                                                : PairCfg<192>::SMEM_BYTES;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -672,21 +675,24 @@ __device__ __forceinline__ bool get_work_pair(const GemmArgs& g, int idx, Work& 
     return true;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, int PN>
 __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                      const GemmArgs g) {
-    constexpr int S = P_STAGES;
+    static_assert(PN == 256 || (PN == 192 && !B_MN), "192-wide pair tiles: K-major B (96 rows a CTA)");
+    using PC = PairCfg<PN>;
+    constexpr int PBN = PN;
+    constexpr int S = PC::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t a_stage0 = base;
     const uint32_t b_stage0 = base + S * P_A_BYTES;
-    uint8_t* out_stage = gbase + S * P_STAGE_BYTES;
+    uint8_t* out_stage = gbase + S * PC::STAGE_BYTES;
     uint8_t* bar_area = out_stage + P_OUT_BYTES;
-    const uint32_t bars = base + S * P_STAGE_BYTES + P_OUT_BYTES;
+    const uint32_t bars = base + S * PC::STAGE_BYTES + P_OUT_BYTES;
     // barriers: full[S], empty[S], pfull[S], tmem_full[NACC], tmem_empty[NACC], drain
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
@@ -748,11 +754,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     }
                     // both CTAs' loads complete on the even CTA's full barrier,
                     // which expects the pair's bytes
-                    if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * P_STAGE_BYTES);
+                    if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * PC::STAGE_BYTES);
                     uint32_t fb;
                     asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(fb) : "r"(full_bar(stage)));
                     const uint32_t sa = a_stage0 + stage * P_A_BYTES;
-                    const uint32_t sb = b_stage0 + stage * P_B_BYTES;
+                    const uint32_t sb = b_stage0 + stage * PC::B_BYTES;
                     if (!A_MN) {
                         tma_load_2d_pair(sa, &tmA, fb, kb * BK, m0);
                     } else {
@@ -806,7 +812,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = a_stage0 + stage * P_A_BYTES;
-                    const uint32_t sb = b_stage0 + stage * P_B_BYTES;
+                    const uint32_t sb = b_stage0 + stage * PC::B_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; k++) {
                         const uint64_t ad = sw128_desc(sa + k * a_kstep, a_lbo, 1024);
@@ -1134,14 +1140,16 @@ bool launch_tc_layout_f8(int epi, const CUtensorMap& ma, const CUtensorMap& mb, 
 
 // CTA-pair kernel: the layouts and epilogues the step uses (as launch_tc_layout),
 // launched in clusters of two.
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, int PN = 256>
 cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, const CUtensorMap& md2,
                         const GemmArgs& args, int pairs, cudaStream_t s) {
-    smem_attr((const void*)gemm_pair_kernel<A_MN, B_MN, EPI>, P_SMEM_BYTES);
+    constexpr int smem = PairCfg<PN>::SMEM_BYTES;
+    static_assert(smem <= 232448, "shared memory per CTA");
+    smem_attr((const void*)gemm_pair_kernel<A_MN, B_MN, EPI, PN>, smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(P_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1150,7 +1158,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<A_MN, B_MN, EPI>, ma, mb, md, md2, args);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<A_MN, B_MN, EPI, PN>, ma, mb, md, md2, args);
 }
 
 // Clusters of two CTA-pair kernel CTAs that can be resident at once on the
@@ -1161,7 +1169,7 @@ int pair_clusters() {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * 256, 1, 1);
         cfg.blockDim = dim3(P_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        cfg.dynamicSmemBytes = P_SMEM_MAX;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -1169,9 +1177,10 @@ int pair_clusters() {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaFuncSetAttribute(gemm_pair_kernel<false, false, EPI_NONE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             P_SMEM_BYTES);
-        if (cudaOccupancyMaxActiveClusters(&v, gemm_pair_kernel<false, false, EPI_NONE>, &cfg) != cudaSuccess || v < 1)
+        cudaFuncSetAttribute(gemm_pair_kernel<false, false, EPI_NONE, 256>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_MAX);
+        if (cudaOccupancyMaxActiveClusters(&v, gemm_pair_kernel<false, false, EPI_NONE, 256>, &cfg) != cudaSuccess ||
+            v < 1)
             v = gpt2_num_sms() / 2;
         cudaGetLastError();
         return v;
@@ -1180,9 +1189,12 @@ int pair_clusters() {
 }
 
 // The pair kernel takes plain bf16 products (no epilogue op) with one
-// k-range per tile (no partials), 256-wide tiles of a wide output (N >= 1024)
-// and at least two 256-row tiles (gemm_tc_use_pair(0) turns it off); the rest
-// runs on the one-CTA kernel. Measured at 32768 rows: K = 768, N = 2304 78 us
+// k-range per tile (no partials) and at least two 256-row tiles, in 256-wide
+// tiles of a wide output (N >= 1024), or 192-wide tiles of a 384 to 960-wide
+// output with K-major B and K >= 2048 (four column tiles a row of tiles at
+// N = 768; a CTA holds 96 rows of B): at 32768 x 768, K = 3072 92 us against
+// 99.5 (one CTA), but K = 768 36 against 34 (gemm_tc_use_pair(0) turns it
+// off); the rest runs on the one-CTA kernel. Measured at 32768 rows: K = 768, N = 2304 78 us
 // against 84 (one CTA), N = 50304 1419 us against 1579; the GELU and
 // GELU-gradient epilogues, which bound their products, ran 7% slower in the
 // pair kernel (152 against 142 us, 172 against 160), so those stay on the
@@ -1190,8 +1202,11 @@ int pair_clusters() {
 bool g_use_pair = true;
 bool g_pair_epi = false;  // also the GELU and GELU-gradient epilogues
 int g_pair_override = 0;  // > 0: the number of clusters to launch instead of the resident count
-bool use_pair(int M, int N, bool partials, int epi) {
-    return g_use_pair && (epi == EPI_NONE || g_pair_epi) && !partials && N >= 1024 && M >= 512;
+// The pair tile width for this product, or 0 for the one-CTA kernel.
+int use_pair(int M, int N, int K, bool partials, int epi, int b_mn) {
+    if (!g_use_pair || (epi != EPI_NONE && !g_pair_epi) || partials || M < 512) return 0;
+    if (N >= 1024) return 256;
+    return epi == EPI_NONE && !b_mn && N >= 384 && N % 192 == 0 && K >= 2048 ? 192 : 0;
 }
 
 }  // namespace
@@ -1233,13 +1248,14 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
     // partial tiles for the reduce kernel: split-K, or an fp32 result added to D
     const bool partials = p.splits > 1 || (accumulate && d_fp32 && epi == EPI_NONE);
     if (partials && (int64_t)M * N + 2048 >= ((int64_t)1 << 31)) return GPT2_ERR_ARG;  // the reduce uses 32-bit indices
-    if (use_pair(M, N, partials, epi) && !f8 && !amax) {
-        // 256 x 256 pair tiles, each CTA loading 128 rows of A and 128 columns of B
-        const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + PBN - 1) / PBN;
+    const int pn = f8 || amax ? 0 : use_pair(M, N, K, partials, epi, b_mn);
+    if (pn) {
+        // 256 x pn pair tiles, each CTA loading 128 rows of A and pn / 2 columns of B
+        const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + pn - 1) / pn;
         CUtensorMap ma, mb, md, md2;
         bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, 128);
         ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
-                         : make_map(&mb, B, (uint64_t)K, (uint64_t)N, PBN / 2));
+                         : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)(pn / 2)));
         ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
         if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
         else md2 = md;
@@ -1267,7 +1283,11 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         const int resident = g_pair_override ? g_pair_override : pair_clusters();
         const int pairs = g.units < resident ? g.units : resident;
         cudaError_t e;
-        if (epi == EPI_GELU) {
+        if (pn == 192) {
+            if (b_mn || epi != EPI_NONE) return GPT2_ERR_ARG;
+            e = a_mn ? launch_pair<true, false, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s)
+                     : launch_pair<false, false, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s);
+        } else if (epi == EPI_GELU) {
             if (a_mn || b_mn) return GPT2_ERR_ARG;
             e = launch_pair<false, false, EPI_GELU>(ma, mb, md, md2, g, pairs, s);
         } else if (epi == EPI_MUL) {
