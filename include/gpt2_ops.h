@@ -316,7 +316,7 @@ int gpt2_debug_stall_matmul(int on);
 /* gpt2_debug_matmul_pair: on = 1 (the default) routes the plain bf16
  * matmuls with M >= 512 and one k-range per tile (no GELU epilogue) to the
  * CTA-pair kernel when N >= 1024, or when N is 384 to 960, a multiple of 192,
- * with B K-major and K >= 2048 (192-wide pair tiles); the pair kernel issues one M = 256
+ * and K is 2048 to 16384 (192-wide pair tiles); the pair kernel issues one M = 256
  * tensor-core product for two neighbouring SMs (tcgen05 .cta_group::2) so
  * that each SM loads half of the B tile; on = 2 routes the GELU and GELU-gradient matmuls of that size there
  * too; 0 keeps every matmul on the one-CTA kernel. Process-wide; takes effect

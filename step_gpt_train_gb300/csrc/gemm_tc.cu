@@ -680,7 +680,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
                      const GemmArgs g) {
-    static_assert(PN == 256 || (PN == 192 && !B_MN), "192-wide pair tiles: K-major B (96 rows a CTA)");
+    static_assert(PN == 256 || PN == 192, "pair tile width");
+    // 192-wide tiles with MN-major B: a CTA's 96 columns of B as three 32-column
+    // atoms of the 64-byte swizzle (the 128-byte swizzle's atoms are 64 columns)
+    constexpr bool B_SW64 = B_MN && PN == 192;
     using PC = PairCfg<PN>;
     constexpr int PBN = PN;
     constexpr int S = PC::STAGES;
@@ -767,6 +770,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     }
                     if (!B_MN) {
                         tma_load_2d_pair(sb, &tmB, fb, kb * BK, n0);
+                    } else if (B_SW64) {
+#pragma unroll
+                        for (int i = 0; i < 3; i++) tma_load_2d_pair(sb + i * 4096, &tmB, fb, n0 + 32 * i, kb * BK);
                     } else {
                         tma_load_2d_pair(sb, &tmB, fb, n0, kb * BK);
                         tma_load_2d_pair(sb + 64 * 128, &tmB, fb, n0 + 64, kb * BK);
@@ -816,7 +822,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; k++) {
                         const uint64_t ad = sw128_desc(sa + k * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = sw128_desc(sb + k * b_kstep, b_lbo, 1024);
+                        // (64-byte swizzle: a 16-row k step is 1024 bytes, atoms 4096 apart along N)
+                        const uint64_t bd = B_SW64 ? sw64_desc(sb + k * 1024, 4096, 512)
+                                                   : sw128_desc(sb + k * b_kstep, b_lbo, 1024);
                         if (leader)
                             asm volatile(
                                 "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -1009,6 +1017,22 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major [outer, inner] bf16 matrix, box [64, 32] (64 bytes
+// of the inner dimension), 64-byte swizzle: the MN-major B of 192-wide pair
+// tiles, in 32-column atoms.
+bool make_map_sw64(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {32, 64};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 2-D map over a row-major [outer, inner] matrix of bytes (e4m3 codes), box
 // [box_outer, 128] (128 bytes), 128-byte swizzle, out-of-bounds bytes read as zero.
 bool make_map_u8(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
@@ -1191,22 +1215,27 @@ int pair_clusters() {
 // The pair kernel takes plain bf16 products (no epilogue op) with one
 // k-range per tile (no partials) and at least two 256-row tiles, in 256-wide
 // tiles of a wide output (N >= 1024), or 192-wide tiles of a 384 to 960-wide
-// output with K-major B and K >= 2048 (four column tiles a row of tiles at
-// N = 768; a CTA holds 96 rows of B): at 32768 x 768, K = 3072 92 us against
-// 99.5 (one CTA), but K = 768 36 against 34 (gemm_tc_use_pair(0) turns it
-// off); the rest runs on the one-CTA kernel. Measured at 32768 rows: K = 768, N = 2304 78 us
+// output with K from 2048 to 16384 (four column tiles a row of tiles at
+// N = 768; a CTA holds 96 rows or columns of B). At 32768 x 768: K = 3072,
+// B K-major 92 us against 99.5 (one CTA), MN-major 98.6 against 100.0;
+// K = 2304 76.1 against 78.5; but K = 768 36 against 34 and the LM head's
+// K = 50304 1521 against 1460 (gemm_tc_use_pair(0) turns it all off); the
+// rest runs on the one-CTA kernel. Measured at 32768 rows: K = 768, N = 2304 78 us
 // against 84 (one CTA), N = 50304 1419 us against 1579; the GELU and
 // GELU-gradient epilogues, which bound their products, ran 7% slower in the
 // pair kernel (152 against 142 us, 172 against 160), so those stay on the
 // one-CTA kernel (gemm_tc_use_pair(2...) routes them too, for measurements).
 bool g_use_pair = true;
 bool g_pair_epi = false;  // also the GELU and GELU-gradient epilogues
+bool g_pair_mn192 = true;  // 192-wide tiles also with MN-major B
 int g_pair_override = 0;  // > 0: the number of clusters to launch instead of the resident count
 // The pair tile width for this product, or 0 for the one-CTA kernel.
 int use_pair(int M, int N, int K, bool partials, int epi, int b_mn) {
     if (!g_use_pair || (epi != EPI_NONE && !g_pair_epi) || partials || M < 512) return 0;
     if (N >= 1024) return 256;
-    return epi == EPI_NONE && !b_mn && N >= 384 && N % 192 == 0 && K >= 2048 ? 192 : 0;
+    return epi == EPI_NONE && (!b_mn || g_pair_mn192) && N >= 384 && N % 192 == 0 && K >= 2048 && K <= 16384
+               ? 192
+               : 0;
 }
 
 }  // namespace
@@ -1254,7 +1283,8 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         const int m_tiles = (M + PBM - 1) / PBM, n_tiles = (N + pn - 1) / pn;
         CUtensorMap ma, mb, md, md2;
         bool ok = a_mn ? make_map(&ma, A, (uint64_t)M, (uint64_t)K, 64) : make_map(&ma, A, (uint64_t)K, (uint64_t)M, 128);
-        ok = ok && (b_mn ? make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64)
+        ok = ok && (b_mn ? (pn == 192 ? make_map_sw64(&mb, B, (uint64_t)N, (uint64_t)K)
+                                      : make_map(&mb, B, (uint64_t)N, (uint64_t)K, 64))
                          : make_map(&mb, B, (uint64_t)K, (uint64_t)N, (uint32_t)(pn / 2)));
         ok = ok && make_out_map(&md, D, d_fp32 != 0, (uint64_t)N, (uint64_t)M, 1);
         if (epi == EPI_GELU) ok = ok && make_out_map(&md2, D2, false, (uint64_t)N, (uint64_t)M, 1);
@@ -1284,9 +1314,13 @@ int matmul_tc(int epi, void* D, void* D2, const bf16* aux, int d_fp32, const voi
         const int pairs = g.units < resident ? g.units : resident;
         cudaError_t e;
         if (pn == 192) {
-            if (b_mn || epi != EPI_NONE) return GPT2_ERR_ARG;
-            e = a_mn ? launch_pair<true, false, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s)
-                     : launch_pair<false, false, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s);
+            if (epi != EPI_NONE) return GPT2_ERR_ARG;
+            if (!b_mn)
+                e = a_mn ? launch_pair<true, false, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s)
+                         : launch_pair<false, false, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s);
+            else
+                e = a_mn ? launch_pair<true, true, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s)
+                         : launch_pair<false, true, EPI_NONE, 192>(ma, mb, md, md2, g, pairs, s);
         } else if (epi == EPI_GELU) {
             if (a_mn || b_mn) return GPT2_ERR_ARG;
             e = launch_pair<false, false, EPI_GELU>(ma, mb, md, md2, g, pairs, s);

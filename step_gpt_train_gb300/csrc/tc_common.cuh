@@ -397,6 +397,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     d |= (uint64_t)2 << 61;
     return d;
 }
+// The same with the 64-byte swizzle (swizzle field 4): atoms of 8 rows of 64
+// bytes, 512 bytes each.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;
+    return d;
+}
 
 // Instruction descriptor, kind::f8f6f4: fp32 accumulator (bits 4-5 = 1), the
 // formats of A and B in bits 7-9 and 10-12 (0 = e4m3, 1 = e5m2), both K-major,

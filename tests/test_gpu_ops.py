@@ -86,8 +86,8 @@ def test_matmul(torch_cuda, mode, case):
 
 
 # The CTA-pair kernel's range: at least 512 rows and 1024 columns (256-wide
-# pair tiles), or 384 to 960 columns in 192-wide tiles with B K-major and
-# K >= 2048.
+# pair tiles), or 384 to 960 columns in 192-wide tiles with K from 2048 to
+# 16384 (MN-major B there in 64-byte swizzle atoms).
 PAIR_CASES = [
     # M, N, K, a_mn, b_mn, d_fp32, bias
     (1000, 1032, 1000, 0, 0, 0, True),   # ragged in every dimension (a half-empty last pair tile)
@@ -97,6 +97,8 @@ PAIR_CASES = [
     (1000, 768, 2104, 0, 0, 0, True),    # 192-wide tiles, ragged M and K
     (520, 768, 3072, 1, 0, 0, False),    # 192-wide tiles, A MN-major
     (1024, 576, 2048, 0, 0, 1, False),   # 192-wide tiles, fp32 out
+    (1000, 768, 2104, 0, 1, 0, False),   # 192-wide tiles, B MN-major (64-byte swizzle), ragged M and K
+    (520, 576, 2048, 1, 1, 1, False),    # 192-wide tiles, both MN-major, fp32 out
 ]
 
 
