@@ -1074,7 +1074,7 @@ static int ln_backward_rows(int dtype, void* out, bool accumulate, float* partia
     if ((size_t)C * (dtype == GPT2_MODE_BF16 ? 2 : 4) <= LN_STAGED_MAX_ROW_BYTES) {
         // bf16: 111 KB of ring per block at C = 768, two blocks per SM; where
         // two blocks of three slots a warp do not fit (C = 1024: 148 KB each),
-        // two slots a warp (99 KB), so that two blocks do
+        // two slots a warp (100 KB), so that two blocks do
         const int blocks = ln_bwd_staged_blocks(N);
         const size_t smem = ln_staged_smem(dtype, C);
         const size_t gbytes = ((size_t)C * 4 + 15) & ~(size_t)15;
